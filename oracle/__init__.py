@@ -1,0 +1,242 @@
+"""Plain CPU oracle for the decode-time hybrid sparse-attention path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product (the
+CUDA library and its binding) never calls it and has no CPU fallback.
+
+The arithmetic lives in ``hsa_oracle.cpp`` (plain C++, double precision, no
+CUDA headers, no code shared with the GPU path); this module only compiles it,
+marshals numpy arrays into it, and composes the four stages into one decode
+layer step the way the pages order them (append -> compress on block
+completion -> indexer -> top-k -> attention).
+
+Sources (cited by title and section):
+  [KD] kerneldigest.dev, "DeepSeek-V4: optimización de inferencia y RL para
+       modelos con atención híbrida y FP4"
+  [LH] lehuy.net, "DeepSeek-V4: SGLang và Miles mang đến hỗ trợ Day-0 ..."
+  [WK] AI-KOL wiki, "与 SGLang 团队聊 DeepSeek V4:混合注意力的推理与 RL 训练适配"
+
+Arrays of bfloat16 values are passed as ``numpy.uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hsa_oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+C4, C128 = 4, 128
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C++ compiler (no CUDA involved)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
+                               "-o", tmp, _SRC])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            lib.oracle_hardware_threads.restype = ctypes.c_int
+            lib.oracle_compress.argtypes = [P, P, P, I64, I64, I64, I64, P, ctypes.c_int]
+            lib.oracle_indexer_scores.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_int]
+            lib.oracle_topk.argtypes = [P, P, I64, I64, P, P, ctypes.c_int]
+            lib.oracle_decode_attn.argtypes = [P, P, P, I64, P, P, P, I64, I64, I64, I64, I64,
+                                               ctypes.c_double, P, P, ctypes.c_int]
+            lib.oracle_float_to_bf16.argtypes = [P, I64, P]
+            lib.oracle_bf16_to_double.argtypes = [P, I64, P]
+            for f in ("oracle_compress", "oracle_indexer_scores", "oracle_topk",
+                      "oracle_decode_attn"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def hardware_threads() -> int:
+    return _load().oracle_hardware_threads()
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what}: status {rc}")
+
+
+def float_to_bf16(x) -> np.ndarray:
+    """binary32 -> bfloat16 bits, round to nearest even (the oracle's own rounding)."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint16)
+    _load().oracle_float_to_bf16(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def bf16_to_double(x) -> np.ndarray:
+    x = _c(x, np.uint16)
+    out = np.empty(x.shape, np.float64)
+    _load().oracle_bf16_to_double(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def compress(kv, z, b, r: int, threads: int = 1) -> np.ndarray:
+    """Flash Compressor (one block of r tokens -> one row, per-channel softmax gate).
+
+    kv, z: uint16 (bf16) [S, T, C]; b: float32 [r, C].  Returns float64 [S, T//r, C].
+    [KD] §Arquitectura del Sistema (Flash Compressor); [WK] 推理侧优化 (Kernel fusion).
+    """
+    kv, z, b = _c(kv, np.uint16), _c(z, np.uint16), _c(b, np.float32)
+    S, T, C = kv.shape
+    assert z.shape == kv.shape and b.shape == (r, C)
+    out = np.empty((S, T // r, C), np.float64)
+    _check(_load().oracle_compress(_ptr(kv), _ptr(z), _ptr(b), S, T, C, r, _ptr(out), threads),
+           "compress")
+    return out
+
+
+def indexer_scores(iq, w, keys, offsets, threads: int = 1) -> np.ndarray:
+    """s[j] = sum_h w_h * relu(q_h . k_j) over each sequence's compressed entries.
+
+    iq: uint16 [B, Hi, Di]; w: float32 [B, Hi]; keys: uint16 [sum N, Di];
+    offsets: int64 [B+1].  Returns float64 [sum N].  [KD] flow step 6 (indexer).
+    """
+    iq, w, keys, offsets = (_c(iq, np.uint16), _c(w, np.float32), _c(keys, np.uint16),
+                            _c(offsets, np.int64))
+    B, Hi, Di = iq.shape
+    assert keys.ndim == 2 and keys.shape[1] == Di and offsets.shape == (B + 1,)
+    out = np.empty(keys.shape[0], np.float64)
+    _check(_load().oracle_indexer_scores(_ptr(iq), _ptr(w), _ptr(keys), _ptr(offsets), B, Hi, Di,
+                                         _ptr(out), threads), "indexer_scores")
+    return out
+
+
+def topk(scores, offsets, k: int, threads: int = 1):
+    """Top-k by (value desc, index asc) per row; -1 / -inf padding.  Returns (idx, vals).
+
+    scores: float32 [sum N]; offsets: int64 [B+1].  [KD] §Arquitectura (Lightning TopK).
+    """
+    scores, offsets = _c(scores, np.float32), _c(offsets, np.int64)
+    B = offsets.shape[0] - 1
+    idx = np.empty((B, k), np.int32)
+    vals = np.empty((B, k), np.float32)
+    _check(_load().oracle_topk(_ptr(scores), _ptr(offsets), B, k, _ptr(idx), _ptr(vals), threads),
+           "topk")
+    return idx, vals
+
+
+def decode_attn(q, swa, seq_len, W: int, extra, extra_offsets, extra_idx, scale: float,
+                Dv: int, threads: int = 1):
+    """One softmax over the SWA window plus the listed (or all) compressed rows.
+
+    q: uint16 [B, Hq, Dqk]; swa: uint16 [B, W, Dqk] ring (slot = pos mod W);
+    seq_len: int32 [B]; extra: uint16 [sum N, Dqk] or None; extra_offsets: int64
+    [B+1] or None; extra_idx: int32 [B, k] or None (dense).  Returns
+    (out float64 [B, Hq, Dv], lse float64 [B, Hq]).  [KD] flow step 5.
+    """
+    q, swa, seq_len = _c(q, np.uint16), _c(swa, np.uint16), _c(seq_len, np.int32)
+    B, Hq, Dqk = q.shape
+    assert swa.shape == (B, W, Dqk)
+    if extra is not None:
+        extra, extra_offsets = _c(extra, np.uint16), _c(extra_offsets, np.int64)
+    k = 0
+    if extra_idx is not None:
+        extra_idx = _c(extra_idx, np.int32)
+        k = extra_idx.shape[1]
+    out = np.empty((B, Hq, Dv), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    _check(_load().oracle_decode_attn(_ptr(q), _ptr(swa), _ptr(seq_len), W, _ptr(extra),
+                                      _ptr(extra_offsets), _ptr(extra_idx), k, B, Hq, Dqk, Dv,
+                                      float(scale), _ptr(out), _ptr(lse), threads),
+           "decode_attn")
+    return out, lse
+
+
+def compact(pool, pool_offsets, counts):
+    """Rows [off_b, off_b + counts[b]) of a capacity-laid-out pool, concatenated."""
+    parts = [pool[int(pool_offsets[b]):int(pool_offsets[b]) + int(counts[b])]
+             for b in range(len(counts))]
+    offs = np.zeros(len(counts) + 1, np.int64)
+    offs[1:] = np.cumsum([int(c) for c in counts])
+    width = pool.shape[1]
+    rows = np.concatenate(parts, axis=0) if parts else np.zeros((0, width), pool.dtype)
+    return rows.reshape(-1, width), offs
+
+
+def layer_decode(st: dict, threads: int = 1) -> dict:
+    """One decode step of one hybrid layer, composed from the four stages.
+
+    The step order follows the data dependence the pages describe ([WK] 核心观点:
+    compress once a 4- / 128-token block is complete, C4 picks its top-k entries
+    and then attends them; [KD] flow steps 3, 5 and 6):
+
+      a1 append the new token's rows into the SWA ring (slot (L-1) mod W) and the
+         in-flight block rings (slot (L-1) mod r), L = seq_len_in + 1;
+      a2 if L mod r == 0, compress the completed block into pool row L/r - 1
+         (compressor output rounded fp64 -> fp32 -> bf16, as stored);
+      a3 (C4) indexer scores over the sequence's L/4 entries, rounded to fp32;
+      a4 (C4) top-k of those scores;
+      a5 attention over the SWA window and the selected (C4) or all (C128) rows.
+
+    ``st`` holds numpy arrays (see the keys read below); the rings and pools in
+    it are updated in place.  Returns the stage outputs.
+    """
+    kind, r = st["kind"], st["ratio"]
+    B = st["seq_len_in"].shape[0]
+    W = st["swa"].shape[1]
+    L = st["seq_len_in"].astype(np.int64) + 1
+    Dv = st["Dv"]
+    out = {"seq_len_out": L.astype(np.int32)}
+    for b in range(B):
+        st["swa"][b, (L[b] - 1) % W] = st["kv_new"][b]
+        st["kv_ring"][b, (L[b] - 1) % r] = st["kv_new"][b]
+        st["z_ring"][b, (L[b] - 1) % r] = st["z_new"][b]
+        if kind == C4:
+            st["ik_ring"][b, (L[b] - 1) % r] = st["ik_new"][b]
+            st["iz_ring"][b, (L[b] - 1) % r] = st["iz_new"][b]
+    offs = st["pool_offsets"]
+    for b in range(B):
+        if L[b] % r != 0:
+            continue
+        n = L[b] // r - 1
+        assert offs[b] + n < offs[b + 1], "pool capacity exceeded"
+        c = compress(st["kv_ring"][b:b + 1], st["z_ring"][b:b + 1], st["b_kv"], r, threads)
+        st["kv_pool"][offs[b] + n] = float_to_bf16(c.astype(np.float32)).reshape(-1)
+        if kind == C4:
+            ck = compress(st["ik_ring"][b:b + 1], st["iz_ring"][b:b + 1], st["b_ik"], r, threads)
+            st["key_pool"][offs[b] + n] = float_to_bf16(ck.astype(np.float32)).reshape(-1)
+    counts = L // r
+    kv_rows, kv_offs = compact(st["kv_pool"], offs, counts)
+    idx = None
+    if kind == C4:
+        key_rows, key_offs = compact(st["key_pool"], offs, counts)
+        s64 = indexer_scores(st["iq"], st["w"], key_rows, key_offs, threads)
+        s32 = s64.astype(np.float32)
+        idx, vals = topk(s32, key_offs, st["k"], threads)
+        out.update(scores64=s64, scores=s32, score_offsets=key_offs, idx=idx, vals=vals)
+    o, lse = decode_attn(st["q"], st["swa"], L.astype(np.int32), W, kv_rows, kv_offs, idx,
+                         st["scale"], Dv, threads)
+    out.update(out=o, lse=lse)
+    return out

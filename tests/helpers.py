@@ -1,0 +1,36 @@
+"""Shared test helpers: bf16 bit conversions and fixture loading (no method arithmetic)."""
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def closed_form(expr: str) -> float:
+    """Evaluate a closed-form expression from a golden file (exp/log/sqrt only)."""
+    return float(eval(expr, {"__builtins__": {}}, {"exp": math.exp, "log": math.log, "sqrt": math.sqrt}))
+
+
+def as_float(v):
+    return float(v) if not isinstance(v, str) else float(v.replace("inf", "inf"))
+
+
+def bf16_bits(x) -> np.ndarray:
+    """bf16 bit patterns (uint16) of a torch bf16 tensor or of values exactly representable in bf16."""
+    t = x if isinstance(x, torch.Tensor) else torch.tensor(np.asarray(x, dtype=np.float32))
+    t = t.to(torch.bfloat16).contiguous().cpu()
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    """float64 values of bf16 bit patterns (via torch, not the oracle)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
