@@ -1,0 +1,141 @@
+// C ABI: host-side validation, status handling and kernel launches.
+//
+// Nothing here computes: every step of the path runs in the kernels of this
+// library.  Each entry point validates its arguments before any launch and
+// returns an hsa_status_t; no C++ exception crosses the boundary.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace hsa {
+namespace {
+
+thread_local char g_detail[512] = "";
+
+hsa_status_t fail(hsa_status_t s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+hsa_status_t cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return HSA_OK;
+  return fail(HSA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+int device_sms() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace hsa
+
+using namespace hsa;
+
+#define HSA_CHECK(cond, code, ...)      \
+  do {                                  \
+    if (!(cond)) return fail(code, __VA_ARGS__); \
+  } while (0)
+
+extern "C" {
+
+const char* hsa_status_string(hsa_status_t s) {
+  switch (s) {
+    case HSA_OK: return "HSA_OK";
+    case HSA_ERR_INVALID_ARG: return "HSA_ERR_INVALID_ARG";
+    case HSA_ERR_UNSUPPORTED: return "HSA_ERR_UNSUPPORTED";
+    case HSA_ERR_CUDA: return "HSA_ERR_CUDA";
+    case HSA_ERR_DEVICE_BOUNDS: return "HSA_ERR_DEVICE_BOUNDS";
+    case HSA_ERR_TIMEOUT: return "HSA_ERR_TIMEOUT";
+    case HSA_ERR_WORKSPACE: return "HSA_ERR_WORKSPACE";
+    case HSA_ERR_NAN: return "HSA_ERR_NAN";
+  }
+  return "HSA_ERR_UNKNOWN";
+}
+
+const char* hsa_last_error_detail(void) { return g_detail; }
+
+int hsa_version(void) { return 100; }
+
+hsa_status_t hsa_workspace_status(void* ws, void* stream, uint32_t* bits) {
+  HSA_CHECK(ws, HSA_ERR_WORKSPACE, "workspace is null");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  hsa_status_t s = cuda_status(cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, st),
+                               "status read");
+  if (s != HSA_OK) return s;
+  s = cuda_status(cudaStreamSynchronize(st), "status sync");
+  if (s != HSA_OK) return s;
+  s = cuda_status(cudaMemsetAsync(ws, 0, sizeof v, st), "status clear");
+  if (s != HSA_OK) return s;
+  if (bits) *bits = v;
+  if (v & HSA_DEV_BOUNDS) return fail(HSA_ERR_DEVICE_BOUNDS, "device saw an out-of-range index");
+  if (v & HSA_DEV_TIMEOUT) return fail(HSA_ERR_TIMEOUT, "a device wait ran out");
+  if (v & HSA_DEV_NAN) return fail(HSA_ERR_NAN, "NaN score reached the top-k");
+  return HSA_OK;
+}
+
+hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,
+                          int64_t C, int64_t r, void* out, int out_dtype, void* stream) {
+  HSA_CHECK(S >= 0 && T >= 0, HSA_ERR_INVALID_ARG, "S=%lld T=%lld must be >= 0", (long long)S,
+            (long long)T);
+  HSA_CHECK(C > 0 && C % 8 == 0, HSA_ERR_UNSUPPORTED, "C=%lld must be a positive multiple of 8",
+            (long long)C);
+  HSA_CHECK(r >= 1 && r <= 4096, HSA_ERR_UNSUPPORTED, "r=%lld outside [1, 4096]", (long long)r);
+  HSA_CHECK(out_dtype == HSA_F32 || out_dtype == HSA_BF16, HSA_ERR_INVALID_ARG, "bad out_dtype");
+  if (S == 0 || T / r == 0) return HSA_OK;
+  HSA_CHECK(kv && z && b && out, HSA_ERR_INVALID_ARG, "null pointer");
+  HSA_CHECK(aligned(kv, 16) && aligned(z, 16) && aligned(b, 16) && aligned(out, 16),
+            HSA_ERR_INVALID_ARG, "kv, z, b and out must be 16-byte aligned");
+  return cuda_status(launch_compress(kv, z, b, S, T, C, r, out, out_dtype,
+                                     static_cast<cudaStream_t>(stream)),
+                     "compress launch");
+}
+
+size_t hsa_topk_workspace_size(int64_t B, int64_t total_rows, int64_t k) {
+  if (B < 1 || total_rows < 0 || k < 1) return 0;
+  return topk_workspace_bytes(B, total_rows, k);
+}
+
+hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, int64_t total_rows,
+                      int64_t k, int32_t* idx, float* vals, void* ws, size_t ws_bytes,
+                      void* stream) {
+  HSA_CHECK(B >= 1 && B <= (1 << 24), HSA_ERR_INVALID_ARG, "B=%lld out of range", (long long)B);
+  HSA_CHECK(total_rows >= 0 && total_rows < (int64_t(1) << 31), HSA_ERR_INVALID_ARG,
+            "total_rows=%lld out of range", (long long)total_rows);
+  HSA_CHECK(k >= 1, HSA_ERR_INVALID_ARG, "k=%lld must be >= 1", (long long)k);
+  HSA_CHECK(k <= 2048, HSA_ERR_UNSUPPORTED, "k=%lld above 2048", (long long)k);
+  HSA_CHECK(offsets && idx, HSA_ERR_INVALID_ARG, "null pointer");
+  HSA_CHECK(scores || total_rows == 0, HSA_ERR_INVALID_ARG, "null scores");
+  HSA_CHECK(aligned(offsets, 8) && aligned(scores, 4) && aligned(idx, 4) && aligned(vals, 4),
+            HSA_ERR_INVALID_ARG, "misaligned pointer");
+  HSA_CHECK(ws && aligned(ws, 256), HSA_ERR_WORKSPACE, "workspace null or not 256-byte aligned");
+  HSA_CHECK(ws_bytes >= topk_workspace_bytes(B, total_rows, k), HSA_ERR_WORKSPACE,
+            "workspace %zu bytes < %zu needed", ws_bytes, topk_workspace_bytes(B, total_rows, k));
+  Spans sp{offsets, nullptr, 0, 1, total_rows};
+  return cuda_status(launch_topk(scores, sp, static_cast<int>(B), total_rows, static_cast<int>(k),
+                                 idx, vals, ws, static_cast<cudaStream_t>(stream)),
+                     "topk launch");
+}
+
+}  // extern "C"

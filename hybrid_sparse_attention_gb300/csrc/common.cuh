@@ -1,0 +1,136 @@
+// Device helpers shared by the CUDA kernels of the library (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hsa.h"
+#include "internal.h"
+
+#define HSA_DEVINL __device__ __forceinline__
+
+namespace hsa {
+
+constexpr size_t kWsHeader = 256;  // workspace bytes reserved for the status word
+
+HSA_DEVINL void set_status(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// Unpack 8 bf16 (one 16-byte chunk) to fp32.
+HSA_DEVINL void bf16x8_to_f32(const uint4& v, float f[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+HSA_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+HSA_DEVINL uint4 f32x8_to_bf16(const float f[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+HSA_DEVINL uint4 ld_stream_u4(const uint4* p) { return __ldcs(p); }
+
+// Rows of a ragged sequence set.  Sequence b starts at offsets[b]; its row
+// count is offsets[b+1] - offsets[b] when seq_len is null, otherwise
+// (seq_len[b] + add) / ratio (the live prefix of a capacity-laid-out pool).
+// `limit` is the number of rows of the underlying buffer: a sequence whose
+// offsets are not monotone, reach past it, or whose live count exceeds its
+// capacity is invalid, and kernels treat it as empty and flag it.
+struct Spans {
+  const int64_t* offsets;
+  const int32_t* seq_len;
+  int32_t add;
+  int32_t ratio;
+  int64_t limit;
+  HSA_DEVINL int64_t start(int b) const { return offsets[b]; }
+  HSA_DEVINL int64_t raw_count(int b) const {
+    if (!seq_len) return offsets[b + 1] - offsets[b];
+    const int64_t n = (static_cast<int64_t>(seq_len[b]) + add) / ratio;
+    return n < 0 ? 0 : n;
+  }
+  HSA_DEVINL bool valid(int b) const {
+    const int64_t o0 = offsets[b], o1 = offsets[b + 1];
+    return o0 >= 0 && o1 >= o0 && o1 <= limit && raw_count(b) <= o1 - o0;
+  }
+  HSA_DEVINL int64_t count(int b) const { return valid(b) ? raw_count(b) : 0; }
+};
+
+// Block-wide inclusive sum over one value per thread (blockDim.x <= 1024).
+// `scratch` holds 33 elements of shared memory.  Returns the inclusive prefix;
+// *total receives the block total.  All threads must call it.
+template <typename T>
+HSA_DEVINL T block_inclusive_sum(T v, T* scratch, T* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    T s = lane < nwarps ? scratch[lane] : T(0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += n;
+    }
+    if (lane < nwarps) scratch[lane] = s;
+    if (lane == nwarps - 1) scratch[32] = s;
+  }
+  __syncthreads();
+  if (warp > 0) v += scratch[warp - 1];
+  *total = scratch[32];
+  __syncthreads();
+  return v;
+}
+
+// Maps a flat work-item index to (sequence, piece) when sequence b is cut
+// into pieces(b) pieces; pieces() is evaluated per sequence.  Returns false
+// when `item` is past the last piece.  All threads of the block must call it
+// (blockDim.x <= 1024); the result is uniform across the block.
+template <typename PiecesFn>
+HSA_DEVINL bool locate_piece(int B, int64_t item, PiecesFn pieces, int* seq, int64_t* piece,
+                             int64_t* npieces) {
+  __shared__ int64_t s_scratch[33];
+  __shared__ int s_seq;
+  __shared__ int64_t s_piece, s_np;
+  if (threadIdx.x == 0) s_seq = -1;
+  int64_t before = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    const int64_t np = b < B ? pieces(b) : 0;
+    int64_t total;
+    const int64_t incl = block_inclusive_sum<int64_t>(np, s_scratch, &total);
+    const int64_t lo = before + incl - np;
+    if (b < B && item >= lo && item < lo + np) {
+      s_seq = b;
+      s_piece = item - lo;
+      s_np = np;
+    }
+    __syncthreads();
+    if (s_seq >= 0) break;
+    before += total;
+  }
+  const bool found = s_seq >= 0;
+  if (found) {
+    *seq = s_seq;
+    *piece = s_piece;
+    *npieces = s_np;
+  }
+  __syncthreads();
+  return found;
+}
+
+}  // namespace hsa

@@ -1,0 +1,143 @@
+// Flash Compressor: one pass over each complete block of r tokens.
+//
+// [KD] "DeepSeek-V4: optimización de inferencia y RL ...", §Arquitectura del
+// Sistema: the 5-stage compression chain is fused into a single on-chip pass
+// to cut HBM round trips.  [WK] "与 SGLang 团队聊 DeepSeek V4", §推理侧优化,
+// Kernel fusion: read -> add -> softmax -> dot -> write.
+//
+// out[s, n, ch] = sum_i softmax_i(z[s, n*r+i, ch] + b[i, ch]) * kv[s, n*r+i, ch]
+//
+// Layout of the work: one thread owns one 16-byte chunk (8 channels) of one
+// block and streams the block's r rows of kv and z through registers, so each
+// input byte crosses HBM exactly once and the only write is the compressed
+// row.  Consecutive threads own consecutive chunks of the same row (a warp
+// reads 512 contiguous bytes per load).  The softmax is evaluated online in
+// groups of 4 rows: one max per group, one rescale per group.
+#include "common.cuh"
+#include "internal.h"
+
+namespace hsa {
+namespace {
+
+constexpr int kGroup = 4;
+
+// Softmax-gated reduction of `r` rows of one 8-channel chunk.  Row i of the
+// chunk is at kv[i * stride] / z[i * stride] (uint4 units); b_row(i) gives the
+// 8 biases of row i.  Result in out[8] (fp32).
+template <typename BiasFn>
+HSA_DEVINL void compress_chunk(const uint4* kv, const uint4* z, int64_t stride, int r,
+                               BiasFn b_row, float out[8]) {
+  float m[8], l[8], acc[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    m[c] = -INFINITY;
+    l[c] = 0.f;
+    acc[c] = 0.f;
+  }
+  for (int i0 = 0; i0 < r; i0 += kGroup) {
+    const int g = min(kGroup, r - i0);
+    uint4 kraw[kGroup], zraw[kGroup];
+    float4 b0[kGroup], b1[kGroup];
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      if (j < g) {
+        kraw[j] = ld_stream_u4(kv + (i0 + j) * stride);
+        zraw[j] = ld_stream_u4(z + (i0 + j) * stride);
+        b_row(i0 + j, &b0[j], &b1[j]);
+      }
+    }
+    float x[kGroup][8], v[kGroup][8];
+    float gm[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) gm[c] = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      if (j < g) {
+        bf16x8_to_f32(zraw[j], x[j]);
+        bf16x8_to_f32(kraw[j], v[j]);
+        const float bb[8] = {b0[j].x, b0[j].y, b0[j].z, b0[j].w,
+                             b1[j].x, b1[j].y, b1[j].z, b1[j].w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          x[j][c] += bb[c];  // add
+          gm[c] = fmaxf(gm[c], x[j][c]);
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float mn = fmaxf(m[c], gm[c]);
+      const float alpha = __expf(m[c] - mn);  // exp(-inf) = 0 on the first group
+      l[c] *= alpha;
+      acc[c] *= alpha;
+      m[c] = mn;
+    }
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      if (j < g) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float e = __expf(x[j][c] - m[c]);  // softmax numerator
+          l[c] += e;
+          acc[c] = fmaf(e, v[j][c], acc[c]);       // dot
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) out[c] = acc[c] / l[c];
+}
+
+template <bool kBf16Out>
+__global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__ kv,
+                                                       const uint4* __restrict__ z,
+                                                       const float* __restrict__ b, int64_t S,
+                                                       int64_t T, int64_t C, int r,
+                                                       void* __restrict__ out) {
+  const int64_t chunks = C / 8;
+  const int64_t nblk = T / r;
+  const int64_t total = S * nblk * chunks;
+  for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
+       w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t c8 = w % chunks;
+    const int64_t sn = w / chunks;  // s * nblk + n
+    const int64_t s = sn / nblk, n = sn - s * nblk;
+    const int64_t first = (s * T + n * r) * chunks + c8;
+    auto bias = [&](int i, float4* lo, float4* hi) {
+      const float4* p = reinterpret_cast<const float4*>(b + i * C + c8 * 8);
+      *lo = __ldg(p);
+      *hi = __ldg(p + 1);
+    };
+    float o[8];
+    compress_chunk(kv + first, z + first, chunks, r, bias, o);
+    if (kBf16Out) {
+      reinterpret_cast<uint4*>(out)[sn * chunks + c8] = f32x8_to_bf16(o);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(out) + (sn * chunks + c8) * 2;
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,
+                            int64_t C, int64_t r, void* out, int out_dtype, cudaStream_t stream) {
+  const int64_t total = S * (T / r) * (C / 8);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int grid = static_cast<int>(want < device_sms() * 16 ? want : device_sms() * 16);
+  if (out_dtype == HSA_BF16)
+    compress_kernel<true><<<grid, threads, 0, stream>>>(
+        static_cast<const uint4*>(kv), static_cast<const uint4*>(z), b, S, T, C,
+        static_cast<int>(r), out);
+  else
+    compress_kernel<false><<<grid, threads, 0, stream>>>(
+        static_cast<const uint4*>(kv), static_cast<const uint4*>(z), b, S, T, C,
+        static_cast<int>(r), out);
+  return cudaGetLastError();
+}
+
+}  // namespace hsa

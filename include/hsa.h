@@ -1,0 +1,124 @@
+/*
+ * hsa.h — C ABI of the GB300 (sm_103a) decode-time hybrid sparse-attention library.
+ *
+ * One decode layer pairs a sliding-window (SWA) KV pool with one compressed
+ * pool: C4 (every 4 tokens compressed to one entry, attended through a top-k
+ * selection) or C128 (every 128 tokens to one entry, attended densely).
+ * Sources, cited by page title and section:
+ *   [KD] kerneldigest.dev, "DeepSeek-V4: optimización de inferencia y RL para
+ *        modelos con atención híbrida y FP4"
+ *   [LH] lehuy.net, "DeepSeek-V4: SGLang và Miles mang đến hỗ trợ Day-0 cho suy
+ *        luận nhanh và Học tăng cường"
+ *   [WK] AI-KOL wiki, "与 SGLang 团队聊 DeepSeek V4:混合注意力的推理与 RL 训练适配"
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer to caller-owned memory on the
+ *     current CUDA device; the library allocates nothing.  Scratch memory is a
+ *     caller-provided workspace of at least the size returned by the matching
+ *     *_workspace_size() function, 256-byte aligned, ZERO-FILLED before its
+ *     first use (e.g. cudaMemset); every call leaves it zero-filled again
+ *     except for the sticky status word (see hsa_workspace_status).
+ *   - bf16 tensors are IEEE bfloat16 (uint16 storage), row-major, contiguous,
+ *     16-byte aligned.  fp32 and int tensors are contiguous and naturally
+ *     aligned (int64 offsets 8-byte aligned).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Arguments are validated on the host before any launch;
+ *     an invalid call returns an error and launches nothing.  No host
+ *     synchronisation happens inside a call.
+ *   - Ragged sequences: `offsets` is int64 [B+1] (device), sequence b owns rows
+ *     [offsets[b], offsets[b+1]), N_b = offsets[b+1] - offsets[b];
+ *     `total_rows` (host) must equal offsets[B].  Row indices returned by the
+ *     library are row-local (0 .. N_b-1).
+ *   - Errors the device can only see at run time (an index out of range, a
+ *     capacity overflow, a NaN score, a wait that ran out) do not trap: the
+ *     kernel skips the offending access and ORs a bit into the workspace's
+ *     sticky status word, read back with hsa_workspace_status().
+ */
+#ifndef HSA_H_
+#define HSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HSA_OK = 0,
+  HSA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, k <= 0, ... */
+  HSA_ERR_UNSUPPORTED = 2,   /* shape outside the compiled kernels (no fallback) */
+  HSA_ERR_CUDA = 3,          /* a CUDA runtime call failed; see hsa_last_error_detail() */
+  HSA_ERR_DEVICE_BOUNDS = 4, /* device saw an index / length outside its buffer */
+  HSA_ERR_TIMEOUT = 5,       /* a device-side wait gave up after its iteration limit */
+  HSA_ERR_WORKSPACE = 6,     /* workspace null, too small or misaligned */
+  HSA_ERR_NAN = 7            /* a NaN score reached the top-k (result unspecified) */
+} hsa_status_t;
+
+typedef enum { HSA_F32 = 0, HSA_BF16 = 1 } hsa_dtype_t;
+
+/* Sticky device status bits (OR-ed into the workspace status word). */
+#define HSA_DEV_BOUNDS 0x1u
+#define HSA_DEV_TIMEOUT 0x2u
+#define HSA_DEV_NAN 0x4u
+
+/* Human-readable name of a status code (static string). */
+const char* hsa_status_string(hsa_status_t s);
+
+/* Detail of the last failing call on this host thread (static thread-local
+ * buffer; empty string if none). */
+const char* hsa_last_error_detail(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int hsa_version(void);
+
+/* Reads and clears the sticky device status word at the head of a workspace.
+ * Synchronises `stream`.  Returns HSA_OK if no bit was set, else the status
+ * matching the lowest set bit; *bits (may be NULL) receives the raw bits. */
+hsa_status_t hsa_workspace_status(void* ws, void* stream, uint32_t* bits);
+
+/* ------------------------------------------------------------------------
+ * Flash Compressor — [KD] §Arquitectura del Sistema ("Flash Compressor fuses
+ * the 5-stage compression chain into one on-chip pass"); [WK] §推理侧优化,
+ * Kernel fusion (read -> add -> softmax -> dot -> write).
+ *
+ * For every complete block n of r consecutive tokens of sequence s and every
+ * channel ch:
+ *   out[s, n, ch] = sum_{i<r} softmax_i(z[s, n*r+i, ch] + b[i, ch]) * kv[s, n*r+i, ch]
+ * (softmax over the block's r positions, per channel; fp32 arithmetic; the
+ * fp32 result is written as fp32 or rounded to nearest-even bf16).  A trailing
+ * partial block (T mod r tokens) is not compressed.
+ *   kv, z : bf16 [S, T, C]     b : fp32 [r, C]     out : [S, T/r, C] of out_dtype
+ * Requirements: S, T >= 0; C a positive multiple of 8; 1 <= r <= 4096.
+ * Reads each input byte once; one kernel launch; no workspace.
+ * ---------------------------------------------------------------------- */
+hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,
+                          int64_t C, int64_t r, void* out, int out_dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Lightning TopK — [KD] §Arquitectura del Sistema (radix-select reduction in
+ * place of a global sort for the indexer's top-k); [WK] §推理侧优化, Lightning
+ * topk.
+ *
+ * Per sequence b, the first min(k, N_b) row-local indices of the scores
+ * ordered by value descending, lower index first among equal values (-0.0
+ * equals +0.0; +-inf are ordinary values); remaining slots get -1 (idx) and
+ * -inf (vals).  Bit-exact: the result depends only on the fp32 scores.
+ * A NaN score is a precondition violation: the output is unspecified and the
+ * status bit HSA_DEV_NAN is set; nothing faults.
+ *   scores : fp32 [total_rows]   offsets : int64 [B+1]
+ *   idx : int32 [B, k]   vals : fp32 [B, k] or NULL
+ * Requirements: 1 <= k <= 2048; B >= 1.
+ * Method: radix select on order-preserving uint32 keys (histogram of the top
+ * 12 bits per row, threshold digit, compaction, selection among the
+ * threshold bin, sort of the k survivors).  Two kernel launches.
+ * ---------------------------------------------------------------------- */
+size_t hsa_topk_workspace_size(int64_t B, int64_t total_rows, int64_t k);
+hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, int64_t total_rows,
+                      int64_t k, int32_t* idx, float* vals, void* ws, size_t ws_bytes,
+                      void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HSA_H_ */
