@@ -35,6 +35,8 @@ SIGNATURES = {
     "hsa_version": (I32, []),
     "hsa_workspace_status": (I32, [P, P, P]),
     "hsa_compress": (I32, [P, P, P, I64, I64, I64, I64, P, I32, P]),
+    "hsa_indexer_scores_workspace_size": (SZ, []),
+    "hsa_indexer_scores": (I32, [P, P, P, P, I64, I64, I64, I64, P, P, SZ, P]),
     "hsa_topk_workspace_size": (SZ, [I64, I64, I64]),
     "hsa_topk": (I32, [P, P, I64, I64, I64, P, P, P, SZ, P]),
 }
@@ -120,6 +122,26 @@ def hsa_compress(kv, z, b, r: int, out=None, out_dtype=torch.bfloat16, stream=No
           _dev(b, torch.float32, "b"), S, T, C, r, _dev(out, out.dtype, "out"), code,
           _stream(stream))
     return out
+
+
+def hsa_indexer_scores_workspace_size() -> int:
+    return int(load().hsa_indexer_scores_workspace_size())
+
+
+def hsa_indexer_scores(iq, w, keys, offsets, scores=None, ws=None, stream=None):
+    """s[j] = sum_h w[b,h] relu(iq[b,h] . keys[j]): iq bf16 [B,Hi,Di], w fp32 [B,Hi],
+    keys bf16 [total, Di], offsets int64 [B+1] (device) -> scores fp32 [total]."""
+    B, Hi, Di = iq.shape
+    total = keys.shape[0]
+    if scores is None:
+        scores = torch.zeros(total, dtype=torch.float32, device=keys.device)
+    if ws is None:
+        ws = workspace(hsa_indexer_scores_workspace_size(), keys.device)
+    _call("hsa_indexer_scores", _dev(iq, torch.bfloat16, "iq"), _dev(w, torch.float32, "w"),
+          _dev(keys, torch.bfloat16, "keys"), _dev(offsets, torch.int64, "offsets"), B, Hi, Di,
+          total, _dev(scores, torch.float32, "scores"), _dev(ws, torch.uint8, "ws"), ws.numel(),
+          _stream(stream))
+    return scores
 
 
 def hsa_topk_workspace_size(B: int, total_rows: int, k: int) -> int:

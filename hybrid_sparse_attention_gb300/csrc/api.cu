@@ -8,6 +8,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -46,6 +48,32 @@ int device_sms() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                              int box_inner, int box_outer, CUtensorMapSwizzle swizzle) {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                       cudaEnableDefault, &q);
+      if (e != cudaSuccess) return e;
+      if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace hsa
@@ -110,6 +138,32 @@ hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t
   return cuda_status(launch_compress(kv, z, b, S, T, C, r, out, out_dtype,
                                      static_cast<cudaStream_t>(stream)),
                      "compress launch");
+}
+
+size_t hsa_indexer_scores_workspace_size(void) { return kWsHeader; }
+
+hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys,
+                                const int64_t* offsets, int64_t B, int64_t Hi, int64_t Di,
+                                int64_t total_rows, float* scores, void* ws, size_t ws_bytes,
+                                void* stream) {
+  HSA_CHECK(B >= 1 && B <= (1 << 24), HSA_ERR_INVALID_ARG, "B=%lld out of range", (long long)B);
+  HSA_CHECK(Hi >= 1 && Hi <= 16, HSA_ERR_UNSUPPORTED, "Hi=%lld outside [1, 16]", (long long)Hi);
+  HSA_CHECK(Di == 32 || Di == 64 || Di == 128, HSA_ERR_UNSUPPORTED, "Di=%lld not in {32, 64, 128}",
+            (long long)Di);
+  HSA_CHECK(total_rows >= 0 && total_rows < (int64_t(1) << 31), HSA_ERR_INVALID_ARG,
+            "total_rows=%lld out of range", (long long)total_rows);
+  HSA_CHECK(iq && w && offsets && (keys || total_rows == 0) && (scores || total_rows == 0),
+            HSA_ERR_INVALID_ARG, "null pointer");
+  HSA_CHECK(aligned(iq, 16) && aligned(keys, 16) && aligned(w, 4) && aligned(scores, 4) &&
+                aligned(offsets, 8),
+            HSA_ERR_INVALID_ARG, "misaligned pointer (iq, keys: 16 bytes)");
+  HSA_CHECK(ws && aligned(ws, 256) && ws_bytes >= kWsHeader, HSA_ERR_WORKSPACE,
+            "workspace null, misaligned or below %zu bytes", kWsHeader);
+  Spans sp{offsets, nullptr, 0, 1, total_rows};
+  return cuda_status(launch_indexer(iq, w, keys, sp, static_cast<int>(B), static_cast<int>(Hi),
+                                    static_cast<int>(Di), total_rows, scores,
+                                    static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream)),
+                     "indexer launch");
 }
 
 size_t hsa_topk_workspace_size(int64_t B, int64_t total_rows, int64_t k) {

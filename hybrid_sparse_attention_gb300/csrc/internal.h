@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,6 +22,15 @@ int device_sms();
 
 cudaError_t launch_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,
                             int64_t C, int64_t r, void* out, int out_dtype, cudaStream_t stream);
+
+// 2-D bf16 tensor map (inner dimension contiguous) for TMA tiled loads.
+cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                              int box_inner, int box_outer, CUtensorMapSwizzle swizzle);
+
+size_t indexer_smem_bytes(int Di);
+cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
+                           int Di, int64_t total_rows, float* scores, uint32_t* status,
+                           cudaStream_t stream);
 
 size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k);
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,

@@ -96,6 +96,27 @@ hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t
                           int64_t C, int64_t r, void* out, int out_dtype, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Indexer scores — [KD] §Flujo de Inferencia step 6 and §Arquitectura del
+ * Sistema (the DSA indexer whose top-k picks the compressed candidates); [WK]
+ * §RL 训练侧 (the attention indexer works like an MoE router).
+ *
+ * For every compressed entry j of sequence b (rows [offsets[b], offsets[b+1])):
+ *   scores[j] = sum_{h<Hi} w[b, h] * max(0, sum_{d<Di} iq[b, h, d] * keys[j, d])
+ * bf16 products, fp32 accumulation (tcgen05 tensor cores, fp32 TMEM
+ * accumulators), fp32 result at the same row position as the key.
+ *   iq : bf16 [B, Hi, Di]   w : fp32 [B, Hi]   keys : bf16 [total_rows, Di]
+ *   offsets : int64 [B+1]   scores : fp32 [total_rows]
+ * Requirements: 1 <= Hi <= 16; Di in {32, 64, 128}; iq and keys 16-byte
+ * aligned.  Rows outside every sequence are not written.  One launch.
+ * Workspace: hsa_indexer_scores_workspace_size() bytes (status word only).
+ * ---------------------------------------------------------------------- */
+size_t hsa_indexer_scores_workspace_size(void);
+hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys,
+                                const int64_t* offsets, int64_t B, int64_t Hi, int64_t Di,
+                                int64_t total_rows, float* scores, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/* ------------------------------------------------------------------------
  * Lightning TopK — [KD] §Arquitectura del Sistema (radix-select reduction in
  * place of a global sort for the indexer's top-k); [WK] §推理侧优化, Lightning
  * topk.
