@@ -37,6 +37,9 @@ SIGNATURES = {
     "hsa_compress": (I32, [P, P, P, I64, I64, I64, I64, P, I32, P]),
     "hsa_indexer_scores_workspace_size": (SZ, []),
     "hsa_indexer_scores": (I32, [P, P, P, P, I64, I64, I64, I64, P, P, SZ, P]),
+    "hsa_decode_attn_workspace_size": (SZ, [I64, I64, I64, I64, I64, I64]),
+    "hsa_decode_attn": (I32, [P, P, P, I64, P, P, I64, P, I64, I64, I64, I64, I64, I64,
+                              ctypes.c_float, P, I32, P, P, SZ, P]),
     "hsa_topk_workspace_size": (SZ, [I64, I64, I64]),
     "hsa_topk": (I32, [P, P, I64, I64, I64, P, P, P, SZ, P]),
 }
@@ -164,3 +167,39 @@ def hsa_topk(scores, offsets, k: int, idx=None, vals=None, ws=None, with_vals=Tr
           B, total, k, _dev(idx, torch.int32, "idx"), _dev(vals, torch.float32, "vals", True),
           _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
     return idx, vals
+
+
+def hsa_decode_attn_workspace_size(B, Hq, Dqk, Dv, W, extra_slots) -> int:
+    return int(load().hsa_decode_attn_workspace_size(B, Hq, Dqk, Dv, W, extra_slots))
+
+
+def hsa_decode_attn(q, swa, seq_len, extra=None, extra_offsets=None, extra_idx=None,
+                    max_extra_rows=0, scale=None, Dv=None, out=None, out_dtype=torch.bfloat16,
+                    lse=None, ws=None, stream=None):
+    """Fused SWA + compressed attention for one query token per sequence.
+
+    q bf16 [B, Hq, Dqk]; swa bf16 [B, W, Dqk] ring; seq_len int32 [B]; extra bf16
+    [rows, Dqk] with extra_offsets int64 [B+1]; extra_idx int32 [B, k] (sparse) or
+    None (dense, N_b <= max_extra_rows).  Returns (out [B, Hq, Dv], lse fp32 [B, Hq])."""
+    B, Hq, Dqk = q.shape
+    W = swa.shape[1]
+    Dv = Dqk if Dv is None else Dv
+    scale = (1.0 / Dqk ** 0.5) if scale is None else scale
+    k = extra_idx.shape[1] if extra_idx is not None else 0
+    rows = extra.shape[0] if extra is not None else 0
+    if out is None:
+        out = torch.empty(B, Hq, Dv, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    slots = k if extra_idx is not None else max_extra_rows
+    need = hsa_decode_attn_workspace_size(B, Hq, Dqk, Dv, W, slots)
+    if ws is None:
+        ws = workspace(need, q.device)
+    code = {torch.float32: HSA_F32, torch.bfloat16: HSA_BF16}[out.dtype]
+    _call("hsa_decode_attn", _dev(q, torch.bfloat16, "q"), _dev(swa, torch.bfloat16, "swa"),
+          _dev(seq_len, torch.int32, "seq_len"), W, _dev(extra, torch.bfloat16, "extra", True),
+          _dev(extra_offsets, torch.int64, "extra_offsets", True), rows,
+          _dev(extra_idx, torch.int32, "extra_idx", True), k, max_extra_rows, B, Hq, Dqk, Dv,
+          float(scale), _dev(out, out.dtype, "out"), code, _dev(lse, torch.float32, "lse", True),
+          _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    return out, lse

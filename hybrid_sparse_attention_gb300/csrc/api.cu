@@ -5,6 +5,7 @@
 // returns an hsa_status_t; no C++ exception crosses the boundary.
 #include <cstdarg>
 #include <cstdio>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -164,6 +165,80 @@ hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys
                                     static_cast<int>(Di), total_rows, scores,
                                     static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream)),
                      "indexer launch");
+}
+
+size_t hsa_decode_attn_workspace_size(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W,
+                                      int64_t extra_slots) {
+  if (B < 1 || Hq < 1 || Dqk < 1 || Dv < 1 || W < 0 || extra_slots < 0) return 0;
+  return attn_workspace_bytes(attn_plan(B, Hq, Dqk, Dv, W, extra_slots), B, Hq, Dv);
+}
+
+static hsa_status_t check_attn_shape(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W) {
+  HSA_CHECK(B >= 1 && B <= (1 << 20), HSA_ERR_INVALID_ARG, "B=%lld out of range", (long long)B);
+  HSA_CHECK(W >= 0 && W <= (1 << 24), HSA_ERR_INVALID_ARG, "W=%lld out of range", (long long)W);
+  HSA_CHECK(Hq >= 1 && (Hq <= 32 || Hq % 32 == 0) && Hq <= 1024, HSA_ERR_UNSUPPORTED,
+            "Hq=%lld: need Hq <= 32 or a multiple of 32", (long long)Hq);
+  HSA_CHECK(Dqk % 64 == 0 && Dqk >= 128 && Dqk <= 576, HSA_ERR_UNSUPPORTED,
+            "Dqk=%lld: need a multiple of 64 in [128, 576]", (long long)Dqk);
+  HSA_CHECK(Dv % 128 == 0 && Dv >= 128 && Dv <= Dqk, HSA_ERR_UNSUPPORTED,
+            "Dv=%lld: need a multiple of 128 in [128, Dqk]", (long long)Dv);
+  return HSA_OK;
+}
+
+hsa_status_t hsa_decode_attn(const void* q, const void* swa, const int32_t* seq_len, int64_t W,
+                             const void* extra, const int64_t* extra_offsets,
+                             int64_t extra_total_rows, const int32_t* extra_idx, int64_t k,
+                             int64_t max_extra_rows, int64_t B, int64_t Hq, int64_t Dqk,
+                             int64_t Dv, float scale, void* out, int out_dtype, float* lse,
+                             void* ws, size_t ws_bytes, void* stream) {
+  hsa_status_t st = check_attn_shape(B, Hq, Dqk, Dv, W);
+  if (st != HSA_OK) return st;
+  HSA_CHECK(q && seq_len && out && (swa || W == 0), HSA_ERR_INVALID_ARG, "null pointer");
+  HSA_CHECK(out_dtype == HSA_F32 || out_dtype == HSA_BF16, HSA_ERR_INVALID_ARG, "bad out_dtype");
+  HSA_CHECK(isfinite(scale), HSA_ERR_INVALID_ARG, "scale must be finite");
+  HSA_CHECK(aligned(q, 16) && aligned(swa, 16) && aligned(extra, 16) && aligned(out, 16) &&
+                aligned(lse, 4) && aligned(seq_len, 4) && aligned(extra_offsets, 8) &&
+                aligned(extra_idx, 4),
+            HSA_ERR_INVALID_ARG, "misaligned pointer (q, swa, extra, out: 16 bytes)");
+  int64_t slots = 0;
+  if (extra) {
+    HSA_CHECK(extra_offsets, HSA_ERR_INVALID_ARG, "extra given without extra_offsets");
+    HSA_CHECK(extra_total_rows >= 0, HSA_ERR_INVALID_ARG, "extra_total_rows < 0");
+    if (extra_idx) {
+      HSA_CHECK(k >= 1 && k <= (1 << 16), HSA_ERR_INVALID_ARG, "k=%lld out of range", (long long)k);
+      slots = k;
+    } else {
+      HSA_CHECK(max_extra_rows >= 0 && max_extra_rows <= (int64_t(1) << 28), HSA_ERR_INVALID_ARG,
+                "max_extra_rows=%lld out of range", (long long)max_extra_rows);
+      slots = max_extra_rows;
+    }
+  } else {
+    HSA_CHECK(!extra_idx, HSA_ERR_INVALID_ARG, "extra_idx given without extra");
+  }
+  const AttnPlan pl = attn_plan(B, Hq, Dqk, Dv, W, slots);
+  const size_t need = attn_workspace_bytes(pl, B, Hq, Dv);
+  HSA_CHECK(ws && aligned(ws, 256) && ws_bytes >= need, HSA_ERR_WORKSPACE,
+            "workspace null, misaligned or below %zu bytes", need);
+  AttnArgs a;
+  a.q = q;
+  a.swa = swa;
+  a.seq_len = seq_len;
+  a.len_add = 0;
+  a.W = W;
+  a.extra = extra;
+  a.sp = Spans{extra_offsets, nullptr, 0, 1, extra_total_rows};
+  a.idx = extra ? extra_idx : nullptr;
+  a.k = extra_idx ? k : 0;
+  a.max_rows = extra_idx ? 0 : max_extra_rows;
+  a.B = B;
+  a.Hq = Hq;
+  a.Dqk = Dqk;
+  a.Dv = Dv;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  return cuda_status(launch_attn(a, pl, ws, static_cast<cudaStream_t>(stream)), "attention launch");
 }
 
 size_t hsa_topk_workspace_size(int64_t B, int64_t total_rows, int64_t k) {

@@ -65,6 +65,36 @@ struct Spans {
   HSA_DEVINL int64_t count(int b) const { return valid(b) ? raw_count(b) : 0; }
 };
 
+// Arguments of one fused-attention launch (see hsa_decode_attn in hsa.h).
+struct AttnArgs {
+  const void* q;
+  const void* swa;
+  const int32_t* seq_len;
+  int32_t len_add;    // attended window length is seq_len[b] + len_add
+  int64_t W;
+  const void* extra;  // compressed pool (null: window only)
+  Spans sp;           // its sequences
+  const int32_t* idx; // [B, k] row-local indices, or null for dense
+  int64_t k;
+  int64_t max_rows;   // dense: bound on compressed rows per sequence
+  int64_t B, Hq, Dqk, Dv;
+  float scale;
+  void* out;
+  int out_dtype;
+  float* lse;
+};
+
+// Launch geometry of the fused attention: HG heads per CTA (N = MMA width),
+// G head groups, S key splits of tps 128-key tiles, dynamic shared memory.
+struct AttnPlan {
+  int HG, N, G, S, tps;
+  size_t smem;
+};
+
+AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, int64_t extra_slots);
+size_t attn_workspace_bytes(const AttnPlan& pl, int64_t B, int64_t Hq, int64_t Dv);
+cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, cudaStream_t stream);
+
 // Block-wide inclusive sum over one value per thread (blockDim.x <= 1024).
 // `scratch` holds 33 elements of shared memory.  Returns the inclusive prefix;
 // *total receives the block total.  All threads must call it.

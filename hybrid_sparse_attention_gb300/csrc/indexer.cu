@@ -144,7 +144,10 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
     if (mma_issued && !ok) tc::mbar_wait(&bar_mma, 0, p.status);
   }
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 }  // namespace

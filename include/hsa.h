@@ -139,6 +139,48 @@ hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, in
                       int64_t k, int32_t* idx, float* vals, void* ws, size_t ws_bytes,
                       void* stream);
 
+/* ------------------------------------------------------------------------
+ * Fused hybrid attention — [KD] §Flujo de Inferencia step 5 and the
+ * technology table (FlashMLA: SWA + C4/C128 attention fused in one kernel);
+ * [LH] §Tích hợp Kernel (SWA and the extra attention in one kernel call);
+ * [WK] §核心观点 (SWA sees the latest tokens, C4 attends its top-k, C128
+ * attends everything).
+ *
+ * For query token b (one per sequence) and head h, the attended slots are
+ *   - the window rows of positions p in [max(0, L_b - W), L_b), L_b =
+ *     seq_len[b], read from ring slot p mod W of swa[b], and
+ *   - sparse (extra_idx != NULL): the compressed rows extra[offsets[b] + j]
+ *     for every listed j = extra_idx[b, i], i < k, with j >= 0 (one term per
+ *     listed entry; -1 lists nothing; j >= N_b is skipped and sets
+ *     HSA_DEV_BOUNDS), or
+ *   - dense (extra_idx == NULL): every compressed row of the sequence,
+ *     N_b = offsets[b+1] - offsets[b] <= max_extra_rows (excess rows are
+ *     skipped and set HSA_DEV_BOUNDS).
+ * Keys are the full Dqk-wide rows, values their first Dv channels (one shared
+ * latent KV head).  One softmax runs over all slots:
+ *   o[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . K_t) * K_t[0:Dv]
+ *   lse[b,h] = log sum_t exp(scale * q[b,h,:] . K_t)          (natural log)
+ * bf16 MMA inputs (tcgen05), fp32 accumulation and softmax; P is rounded to
+ * bf16 for the second product.  A sequence with no slot gives o = 0, lse = -inf.
+ *   q : bf16 [B, Hq, Dqk]      swa : bf16 [B, W, Dqk] (may be NULL if W == 0)
+ *   seq_len : int32 [B]        extra : bf16 [extra_total_rows, Dqk] or NULL
+ *   extra_offsets : int64 [B+1]   extra_idx : int32 [B, k] or NULL
+ *   out : [B, Hq, Dv] of out_dtype     lse : fp32 [B, Hq] or NULL
+ * Requirements: Hq <= 32 or a multiple of 32; Dqk a multiple of 64 in
+ * [128, 576]; Dv a multiple of 128 in [128, Dqk]; q, swa, extra, out
+ * 16-byte aligned.  Workspace: hsa_decode_attn_workspace_size(B, Hq, Dqk, Dv,
+ * W, extra_slots) with extra_slots = k (sparse) or max_extra_rows (dense);
+ * long slot lists are split across CTAs and merged by a second launch.
+ * ---------------------------------------------------------------------- */
+size_t hsa_decode_attn_workspace_size(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W,
+                                      int64_t extra_slots);
+hsa_status_t hsa_decode_attn(const void* q, const void* swa, const int32_t* seq_len, int64_t W,
+                             const void* extra, const int64_t* extra_offsets,
+                             int64_t extra_total_rows, const int32_t* extra_idx, int64_t k,
+                             int64_t max_extra_rows, int64_t B, int64_t Hq, int64_t Dqk,
+                             int64_t Dv, float scale, void* out, int out_dtype, float* lse,
+                             void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

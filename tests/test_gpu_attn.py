@@ -1,0 +1,162 @@
+"""GPU parity of the fused hybrid attention against the oracle fed the same
+indices: output max abs error <= 1e-2.  The log-sum-exp may differ by at most
+2^-8 (~3.9e-3): the kernel sums the softmax weights after rounding them to
+bf16 (relative error <= 2^-9 each), so the sum, and thus exp(lse), is within a
+factor (1 +- 2^-9) of the exact one."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_bits, closed_form, golden
+from hybrid_sparse_attention_gb300 import _lib, synth
+
+pytestmark = pytest.mark.gpu
+SEED = synth.SEED["c4layer"]
+OUT_TOL, LSE_TOL = 1e-2, 2.0 ** -8
+
+
+def _offsets(counts):
+    offs = torch.zeros(len(counts) + 1, dtype=torch.int64)
+    offs[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int64), 0)
+    return offs
+
+
+def _run(q, swa, L, extra, offs, idx, scale, Dv, max_rows=0, out_dtype=torch.bfloat16):
+    out, lse = _lib.hsa_decode_attn(
+        q.cuda(), swa.cuda(), L.cuda(), None if extra is None else extra.cuda(),
+        None if offs is None else offs.cuda(), None if idx is None else idx.cuda(),
+        max_extra_rows=max_rows, scale=scale, Dv=Dv, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _oracle(oracle_mod, q, swa, L, extra, offs, idx, scale, Dv):
+    return oracle_mod.decode_attn(
+        bf16_bits(q), bf16_bits(swa), L.numpy(), swa.shape[1],
+        None if extra is None else bf16_bits(extra), None if offs is None else offs.numpy(),
+        None if idx is None else idx.numpy(), scale, Dv, threads=16)
+
+
+def _compare(got, want):
+    o, l = got
+    ro, rl = want
+    err = np.abs(o - ro).max() if o.size else 0.0
+    assert err <= OUT_TOL, f"max abs err {err:.3e}"
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isneginf(l), np.isneginf(rl))
+    if fin.any():
+        lerr = np.abs(l[fin] - rl[fin]).max()
+        assert lerr <= LSE_TOL, f"lse err {lerr:.3e}"
+    return err
+
+
+def test_attention_worked_example_embedded(oracle_mod):
+    """The hand-worked 3-channel example, zero-padded to 128 channels (padding
+    adds nothing to any dot product) and checked against its closed form."""
+    g = golden("attn_worked.json")
+    D = 128
+
+    def pad(rows):
+        a = torch.zeros(len(rows), D)
+        a[:, :3] = torch.tensor(rows)
+        return a.to(torch.bfloat16)
+
+    q = pad([g["q"]])[None]                     # [1, 1, 128]
+    swa = pad(g["swa"])[None]
+    extra = pad(g["extra"])
+    offs = torch.tensor([0, 2], dtype=torch.int64)
+    L = torch.tensor([g["seq_len"]], dtype=torch.int32)
+    for idx, key in ((torch.tensor([g["idx"]], dtype=torch.int32), "expected_sparse"),
+                     (None, "expected_dense")):
+        o, l = _run(q, swa, L, extra, offs, idx, 1.0, 128, max_rows=2, out_dtype=torch.float32)
+        want = [closed_form(e) for e in g[key]["out"]]
+        np.testing.assert_allclose(o[0, 0, :2], want, atol=OUT_TOL)
+        assert abs(l[0, 0] - closed_form(g[key]["lse"])) < LSE_TOL
+        assert np.all(o[0, 0, 2:] == 0)
+
+
+def _tiny_case(B=1, Hq=8, D=128, Dv=128, W=64, k=64, counts=(1024,), L=(4096,), tag="tiny"):
+    offs = _offsets(list(counts))
+    q = synth.normal_bf16(SEED, f"at.q.{tag}", (B, Hq, D))
+    swa = synth.normal_bf16(SEED, f"at.swa.{tag}", (B, W, D))
+    extra = synth.normal_bf16(SEED, f"at.ex.{tag}", (int(offs[-1]), D))
+    idx = torch.full((B, k), -1, dtype=torch.int32)
+    for b in range(B):
+        n = counts[b]
+        m = min(k, n)
+        if m:
+            perm = synth.permutation(SEED, f"at.idx.{tag}.{b}", n)[:m]
+            idx[b, :m] = perm.to(torch.int32)
+    return q, swa, torch.tensor(list(L), dtype=torch.int32), extra, offs, idx
+
+
+def test_attention_tiny_config(oracle_mod):
+    q, swa, L, extra, offs, idx = _tiny_case()
+    scale = 1 / math.sqrt(128)
+    for out_dtype in (torch.bfloat16, torch.float32):
+        got = _run(q, swa, L, extra, offs, idx, scale, 128, out_dtype=out_dtype)
+        _compare(got, _oracle(oracle_mod, q, swa, L, extra, offs, idx, scale, 128))
+
+
+def test_attention_full_heads_ragged_sparse(oracle_mod):
+    """64 heads x 576 (512 latent + 64 rope), window 128, top-512 lists with -1
+    padding and repeats; windows shorter than, equal to and longer than W."""
+    counts = [2000, 100, 0, 5000, 513, 1]
+    Ls = [8003, 40, 1, 130000, 128, 3]
+    B = len(counts)
+    q, swa, L, extra, offs, idx = _tiny_case(B, 64, 576, 512, 128, 512, counts, Ls, "full")
+    idx[3, 100:110] = idx[3, 0]          # repeated entries count once each
+    idx[0, 7] = -1                       # a hole in the middle of a list
+    scale = 1 / math.sqrt(576)
+    got = _run(q, swa, L, extra, offs, idx, scale, 512)
+    _compare(got, _oracle(oracle_mod, q, swa, L, extra, offs, idx, scale, 512))
+
+
+def test_attention_dense_c128_with_splits(oracle_mod):
+    """Dense mode over all compressed rows: long lists are split across CTAs and
+    merged by the log-sum-exp combine."""
+    counts = [4000, 37, 1000, 0]
+    Ls = [4000 * 128 + 5, 37 * 128 + 127, 128000, 64]
+    B = len(counts)
+    q, swa, L, extra, offs, _ = _tiny_case(B, 64, 576, 512, 128, 1, counts, Ls, "dense")
+    scale = 1 / math.sqrt(576)
+    got = _run(q, swa, L, extra, offs, None, scale, 512, max_rows=max(counts))
+    _compare(got, _oracle(oracle_mod, q, swa, L, extra, offs, None, scale, 512))
+
+
+def test_attention_rescale_path(oracle_mod):
+    """Later tiles carry much larger logits than the window tile, forcing the
+    running maximum to move and O to be rescaled in TMEM; the first tile of one
+    sequence is entirely masked."""
+    counts = [900, 900]
+    q, swa, L, extra, offs, idx = _tiny_case(2, 64, 576, 512, 128, 512, counts, [5000, 5000], "resc")
+    extra = (extra.float() * torch.linspace(0.5, 6.0, extra.shape[0])[:, None]).to(torch.bfloat16)
+    L[1] = 0                                     # no window: tile 0 = compressed rows only
+    idx[1, :200] = -1                            # ... whose first 128 slots are all masked
+    scale = 1 / math.sqrt(576)
+    got = _run(q, swa, L, extra, offs, idx, scale, 512, out_dtype=torch.float32)
+    _compare(got, _oracle(oracle_mod, q, swa, L, extra, offs, idx, scale, 512))
+
+
+def test_attention_empty_and_window_only(oracle_mod):
+    q, swa, L, extra, offs, idx = _tiny_case(3, 8, 128, 128, 64, 64, [10, 0, 5], [0, 0, 70], "empty")
+    idx[0] = -1
+    scale = 0.1
+    got = _run(q, swa, L, extra, offs, idx, scale, 128)
+    want = _oracle(oracle_mod, q, swa, L, extra, offs, idx, scale, 128)
+    _compare(got, want)
+    assert np.all(got[0][0] == 0) and np.all(np.isneginf(got[1][0]))
+    # window only (no compressed pool at all)
+    got = _run(q, swa, L, None, None, None, scale, 128)
+    _compare(got, _oracle(oracle_mod, q, swa, L, None, None, None, scale, 128))
+
+
+def test_attention_index_out_of_range_flags_bounds():
+    q, swa, L, extra, offs, idx = _tiny_case(1, 8, 128, 128, 64, 64, [10], [100], "oob")
+    idx[0, 3] = 10                                # sequence has 10 rows: 10 is out of range
+    ws = _lib.workspace(_lib.hsa_decode_attn_workspace_size(1, 8, 128, 128, 64, 64))
+    _lib.hsa_decode_attn(q.cuda(), swa.cuda(), L.cuda(), extra.cuda(), offs.cuda(), idx.cuda(),
+                         Dv=128, ws=ws)
+    assert _lib.hsa_workspace_status(ws) & 0x1
