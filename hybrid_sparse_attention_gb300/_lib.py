@@ -203,3 +203,82 @@ def hsa_decode_attn(q, swa, seq_len, extra=None, extra_offsets=None, extra_idx=N
           float(scale), _dev(out, out.dtype, "out"), code, _dev(lse, torch.float32, "lse", True),
           _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
     return out, lse
+
+
+class LayerDesc(ctypes.Structure):
+    """Mirror of hsa_layer_desc (include/hsa.h)."""
+    _fields_ = [
+        ("kind", ctypes.c_int32), ("B", ctypes.c_int32), ("Hq", ctypes.c_int32),
+        ("Dqk", ctypes.c_int32), ("Dv", ctypes.c_int32), ("Hi", ctypes.c_int32),
+        ("Di", ctypes.c_int32), ("W", ctypes.c_int32), ("k", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int32),
+        ("pool_total_rows", ctypes.c_int64), ("max_pool_rows", ctypes.c_int64),
+        ("seq_len_in", P), ("seq_len_out", P), ("pool_offsets", P),
+        ("kv_new", P), ("z_new", P), ("b_kv", P), ("ik_new", P), ("iz_new", P), ("b_ik", P),
+        ("swa", P), ("kv_ring", P), ("z_ring", P), ("ik_ring", P), ("iz_ring", P),
+        ("kv_pool", P), ("key_pool", P), ("q", P), ("iq", P), ("w", P),
+        ("out", P), ("lse", P), ("topk_idx", P), ("scores", P),
+    ]
+
+
+SIGNATURES["hsa_layer_decode_workspace_size"] = (SZ, [ctypes.POINTER(LayerDesc)])
+SIGNATURES["hsa_layer_decode"] = (I32, [ctypes.POINTER(LayerDesc), P, SZ, P])
+
+
+def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
+               max_pool_rows=None) -> LayerDesc:
+    """Descriptor for one decode step over a synth.LayerState-like object whose
+    tensors live on the GPU (argument marshalling only)."""
+    sh = st.shape
+    c4 = st.kind == HSA_LAYER_C4
+    d = LayerDesc()
+    d.kind = st.kind
+    d.B = st.seq_len_in.numel()
+    d.Hq, d.Dqk, d.Dv = sh.Hq, sh.Dqk, sh.Dv
+    d.Hi, d.Di = (sh.Hi, sh.Di) if c4 else (0, 0)
+    d.W, d.k = sh.W, (sh.k if c4 else 0)
+    d.scale = sh.scale
+    d.out_dtype = {torch.float32: HSA_F32, torch.bfloat16: HSA_BF16}[out.dtype]
+    d.pool_total_rows = st.kv_pool.shape[0]
+    if max_pool_rows is None:
+        max_pool_rows = int((st.pool_offsets[1:] - st.pool_offsets[:-1]).max()) if not c4 else 0
+    d.max_pool_rows = max_pool_rows
+    d.seq_len_in = _dev(st.seq_len_in, torch.int32, "seq_len_in")
+    d.seq_len_out = _dev(st.seq_len_in if seq_len_out is None else seq_len_out, torch.int32,
+                         "seq_len_out")
+    d.pool_offsets = _dev(st.pool_offsets, torch.int64, "pool_offsets")
+    d.kv_new = _dev(st.kv_new, torch.bfloat16, "kv_new")
+    d.z_new = _dev(st.z_new, torch.bfloat16, "z_new")
+    d.b_kv = _dev(st.b_kv, torch.float32, "b_kv")
+    d.swa = _dev(st.swa, torch.bfloat16, "swa")
+    d.kv_ring = _dev(st.kv_ring, torch.bfloat16, "kv_ring")
+    d.z_ring = _dev(st.z_ring, torch.bfloat16, "z_ring")
+    d.kv_pool = _dev(st.kv_pool, torch.bfloat16, "kv_pool")
+    d.q = _dev(st.q, torch.bfloat16, "q")
+    if c4:
+        d.ik_new = _dev(st.ik_new, torch.bfloat16, "ik_new")
+        d.iz_new = _dev(st.iz_new, torch.bfloat16, "iz_new")
+        d.b_ik = _dev(st.b_ik, torch.float32, "b_ik")
+        d.ik_ring = _dev(st.ik_ring, torch.bfloat16, "ik_ring")
+        d.iz_ring = _dev(st.iz_ring, torch.bfloat16, "iz_ring")
+        d.key_pool = _dev(st.key_pool, torch.bfloat16, "key_pool")
+        d.iq = _dev(st.iq, torch.bfloat16, "iq")
+        d.w = _dev(st.w, torch.float32, "w")
+        d.topk_idx = _dev(topk_idx, torch.int32, "topk_idx", True)
+        d.scores = _dev(scores, torch.float32, "scores", True)
+    d.out = _dev(out, out.dtype, "out")
+    d.lse = _dev(lse, torch.float32, "lse", True)
+    return d
+
+
+def hsa_layer_decode_workspace_size(desc: LayerDesc) -> int:
+    return int(load().hsa_layer_decode_workspace_size(ctypes.byref(desc)))
+
+
+def hsa_layer_decode(desc: LayerDesc, ws=None, stream=None):
+    """One decode step of one hybrid layer (append, compress, [score, top-k], attend)."""
+    if ws is None:
+        ws = workspace(hsa_layer_decode_workspace_size(desc))
+    _call("hsa_layer_decode", ctypes.byref(desc), _dev(ws, torch.uint8, "ws"), ws.numel(),
+          _stream(stream))
+    return ws

@@ -238,7 +238,63 @@ hsa_status_t hsa_decode_attn(const void* q, const void* swa, const int32_t* seq_
   a.out = out;
   a.out_dtype = out_dtype;
   a.lse = lse;
-  return cuda_status(launch_attn(a, pl, ws, static_cast<cudaStream_t>(stream)), "attention launch");
+  return cuda_status(launch_attn(a, pl, ws, static_cast<uint32_t*>(ws),
+                                 static_cast<cudaStream_t>(stream)),
+                     "attention launch");
+}
+
+static hsa_status_t check_layer(const hsa_layer_desc* d) {
+  HSA_CHECK(d, HSA_ERR_INVALID_ARG, "null descriptor");
+  HSA_CHECK(d->kind == HSA_LAYER_C4 || d->kind == HSA_LAYER_C128, HSA_ERR_INVALID_ARG,
+            "kind=%d not HSA_LAYER_C4 / HSA_LAYER_C128", d->kind);
+  hsa_status_t st = check_attn_shape(d->B, d->Hq, d->Dqk, d->Dv, d->W);
+  if (st != HSA_OK) return st;
+  HSA_CHECK(d->W >= 1, HSA_ERR_INVALID_ARG, "W must be >= 1");
+  HSA_CHECK(d->out_dtype == HSA_F32 || d->out_dtype == HSA_BF16, HSA_ERR_INVALID_ARG,
+            "bad out_dtype");
+  HSA_CHECK(isfinite(d->scale), HSA_ERR_INVALID_ARG, "scale must be finite");
+  HSA_CHECK(d->pool_total_rows >= 0 && d->pool_total_rows < (int64_t(1) << 31),
+            HSA_ERR_INVALID_ARG, "pool_total_rows out of range");
+  HSA_CHECK(d->seq_len_in && d->seq_len_out && d->pool_offsets && d->kv_new && d->z_new &&
+                d->b_kv && d->swa && d->kv_ring && d->z_ring && d->kv_pool && d->q && d->out,
+            HSA_ERR_INVALID_ARG, "null pointer in descriptor");
+  HSA_CHECK(aligned(d->kv_new, 16) && aligned(d->z_new, 16) && aligned(d->b_kv, 16) &&
+                aligned(d->swa, 16) && aligned(d->kv_ring, 16) && aligned(d->z_ring, 16) &&
+                aligned(d->kv_pool, 16) && aligned(d->q, 16) && aligned(d->out, 16) &&
+                aligned(d->pool_offsets, 8) && aligned(d->lse, 4),
+            HSA_ERR_INVALID_ARG, "misaligned pointer in descriptor");
+  if (d->kind == HSA_LAYER_C4) {
+    HSA_CHECK(d->Hi >= 1 && d->Hi <= 16, HSA_ERR_UNSUPPORTED, "Hi=%d outside [1, 16]", d->Hi);
+    HSA_CHECK(d->Di == 32 || d->Di == 64 || d->Di == 128, HSA_ERR_UNSUPPORTED,
+              "Di=%d not in {32, 64, 128}", d->Di);
+    HSA_CHECK(d->k >= 1 && d->k <= 2048, HSA_ERR_UNSUPPORTED, "k=%d outside [1, 2048]", d->k);
+    HSA_CHECK(d->ik_new && d->iz_new && d->b_ik && d->ik_ring && d->iz_ring && d->key_pool &&
+                  d->iq && d->w,
+              HSA_ERR_INVALID_ARG, "C4 layer needs the indexer tensors");
+    HSA_CHECK(aligned(d->ik_new, 16) && aligned(d->iz_new, 16) && aligned(d->b_ik, 16) &&
+                  aligned(d->ik_ring, 16) && aligned(d->iz_ring, 16) &&
+                  aligned(d->key_pool, 16) && aligned(d->iq, 16) && aligned(d->w, 4) &&
+                  aligned(d->topk_idx, 4) && aligned(d->scores, 4),
+              HSA_ERR_INVALID_ARG, "misaligned indexer pointer");
+  } else {
+    HSA_CHECK(d->max_pool_rows >= 0 && d->max_pool_rows <= (int64_t(1) << 28),
+              HSA_ERR_INVALID_ARG, "max_pool_rows out of range");
+  }
+  return HSA_OK;
+}
+
+size_t hsa_layer_decode_workspace_size(const hsa_layer_desc* d) {
+  if (check_layer(d) != HSA_OK) return 0;
+  return layer_workspace_bytes(*d);
+}
+
+hsa_status_t hsa_layer_decode(const hsa_layer_desc* d, void* ws, size_t ws_bytes, void* stream) {
+  hsa_status_t st = check_layer(d);
+  if (st != HSA_OK) return st;
+  const size_t need = layer_workspace_bytes(*d);
+  HSA_CHECK(ws && aligned(ws, 256) && ws_bytes >= need, HSA_ERR_WORKSPACE,
+            "workspace null, misaligned or below %zu bytes", need);
+  return cuda_status(launch_layer(*d, ws, static_cast<cudaStream_t>(stream)), "layer launch");
 }
 
 size_t hsa_topk_workspace_size(int64_t B, int64_t total_rows, int64_t k) {
@@ -263,7 +319,8 @@ hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, in
             "workspace %zu bytes < %zu needed", ws_bytes, topk_workspace_bytes(B, total_rows, k));
   Spans sp{offsets, nullptr, 0, 1, total_rows};
   return cuda_status(launch_topk(scores, sp, static_cast<int>(B), total_rows, static_cast<int>(k),
-                                 idx, vals, ws, static_cast<cudaStream_t>(stream)),
+                                 idx, vals, ws, static_cast<uint32_t*>(ws),
+                                 static_cast<cudaStream_t>(stream)),
                      "topk launch");
 }
 

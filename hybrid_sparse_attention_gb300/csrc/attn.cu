@@ -594,7 +594,8 @@ size_t attn_workspace_bytes(const AttnPlan& pl, int64_t B, int64_t Hq, int64_t D
   return bytes;
 }
 
-cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, cudaStream_t stream) {
+cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_t* status,
+                        cudaStream_t stream) {
   AttnParams p;
   p.q = static_cast<const uint16_t*>(a.q);
   p.swa = static_cast<const uint16_t*>(a.swa);
@@ -618,7 +619,7 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, cudaStr
   p.out = a.out;
   p.out_dtype = a.out_dtype;
   p.lse = a.lse;
-  p.status = static_cast<uint32_t*>(ws);
+  p.status = status;
   char* w = static_cast<char*>(ws) + kWsHeader;
   p.po = reinterpret_cast<float*>(w);
   p.plse = reinterpret_cast<float*>(

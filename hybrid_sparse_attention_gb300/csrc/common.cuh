@@ -93,7 +93,10 @@ struct AttnPlan {
 
 AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, int64_t extra_slots);
 size_t attn_workspace_bytes(const AttnPlan& pl, int64_t B, int64_t Hq, int64_t Dv);
-cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, cudaStream_t stream);
+// ws: attn_workspace_bytes() of scratch (partials after a kWsHeader gap);
+// status: the sticky status word to report into.
+cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_t* status,
+                        cudaStream_t stream);
 
 // Block-wide inclusive sum over one value per thread (blockDim.x <= 1024).
 // `scratch` holds 33 elements of shared memory.  Returns the inclusive prefix;

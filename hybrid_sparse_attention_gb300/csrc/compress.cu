@@ -12,81 +12,14 @@
 // input byte crosses HBM exactly once and the only write is the compressed
 // row.  Consecutive threads own consecutive chunks of the same row (a warp
 // reads 512 contiguous bytes per load).  The softmax is evaluated online in
-// groups of 4 rows: one max per group, one rescale per group.
+// groups of 4 rows: one max per group, one rescale per group (the shared
+// arithmetic lives in compress_core.cuh).
 #include "common.cuh"
+#include "compress_core.cuh"
 #include "internal.h"
 
 namespace hsa {
 namespace {
-
-constexpr int kGroup = 4;
-
-// Softmax-gated reduction of `r` rows of one 8-channel chunk.  Row i of the
-// chunk is at kv[i * stride] / z[i * stride] (uint4 units); b_row(i) gives the
-// 8 biases of row i.  Result in out[8] (fp32).
-template <typename BiasFn>
-HSA_DEVINL void compress_chunk(const uint4* kv, const uint4* z, int64_t stride, int r,
-                               BiasFn b_row, float out[8]) {
-  float m[8], l[8], acc[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    m[c] = -INFINITY;
-    l[c] = 0.f;
-    acc[c] = 0.f;
-  }
-  for (int i0 = 0; i0 < r; i0 += kGroup) {
-    const int g = min(kGroup, r - i0);
-    uint4 kraw[kGroup], zraw[kGroup];
-    float4 b0[kGroup], b1[kGroup];
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) {
-      if (j < g) {
-        kraw[j] = ld_stream_u4(kv + (i0 + j) * stride);
-        zraw[j] = ld_stream_u4(z + (i0 + j) * stride);
-        b_row(i0 + j, &b0[j], &b1[j]);
-      }
-    }
-    float x[kGroup][8], v[kGroup][8];
-    float gm[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) gm[c] = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) {
-      if (j < g) {
-        bf16x8_to_f32(zraw[j], x[j]);
-        bf16x8_to_f32(kraw[j], v[j]);
-        const float bb[8] = {b0[j].x, b0[j].y, b0[j].z, b0[j].w,
-                             b1[j].x, b1[j].y, b1[j].z, b1[j].w};
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          x[j][c] += bb[c];  // add
-          gm[c] = fmaxf(gm[c], x[j][c]);
-        }
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float mn = fmaxf(m[c], gm[c]);
-      const float alpha = __expf(m[c] - mn);  // exp(-inf) = 0 on the first group
-      l[c] *= alpha;
-      acc[c] *= alpha;
-      m[c] = mn;
-    }
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) {
-      if (j < g) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float e = __expf(x[j][c] - m[c]);  // softmax numerator
-          l[c] += e;
-          acc[c] = fmaf(e, v[j][c], acc[c]);       // dot
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int c = 0; c < 8; ++c) out[c] = acc[c] / l[c];
-}
 
 template <bool kBf16Out>
 __global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__ kv,
@@ -108,8 +41,11 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__
       *lo = __ldg(p);
       *hi = __ldg(p + 1);
     };
+    GatePartial part;
+    partial_init(part);
+    partial_rows(kv + first, z + first, chunks, 0, r, bias, part);
     float o[8];
-    compress_chunk(kv + first, z + first, chunks, r, bias, o);
+    partial_result(part, o);
     if (kBf16Out) {
       reinterpret_cast<uint4*>(out)[sn * chunks + c8] = f32x8_to_bf16(o);
     } else {

@@ -34,6 +34,10 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
 
 size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k);
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
-                        int32_t* idx, float* vals, void* ws, cudaStream_t stream);
+                        int32_t* idx, float* vals, void* ws, uint32_t* status,
+                        cudaStream_t stream);
+
+size_t layer_workspace_bytes(const hsa_layer_desc& d);
+cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream);
 
 }  // namespace hsa

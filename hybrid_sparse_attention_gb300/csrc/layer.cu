@@ -1,0 +1,229 @@
+// One decode step of one hybrid layer: append -> compress on block
+// completion -> (C4) indexer scores -> top-k -> fused attention, all on one
+// stream with no host synchronisation.
+//
+// [WK] "与 SGLang 团队聊 DeepSeek V4", §核心观点: a layer keeps five kinds of
+// state — the SWA window, the C4 and C128 pools, and the in-flight C4/C128
+// blocks that are compressed once 4 / 128 tokens have accumulated; C4 picks
+// its top-k entries, C128 attends all.  [KD] "DeepSeek-V4: optimización de
+// inferencia y RL ...", §Arquitectura del Sistema (compression-state ring
+// buffers in their own pool) and §Flujo de Inferencia steps 3, 5 and 6.
+//
+// Step order follows the data dependence (the top-k must pick the C4 entries
+// before the attention reads them):
+//   a1 append   new kv row -> SWA ring slot (L-1) mod W and in-flight slot
+//               (L-1) mod r (kv, gate logits; C4 also the raw indexer key and
+//               its gate), L = seq_len_in + 1; seq_len_out = L
+//   a2 compress if L mod r == 0: the completed block -> pool row L/r - 1
+//   a3 scores   (C4) indexer over the sequence's L/4 entries
+//   a4 top-k    (C4) k largest scores
+//   a5 attend   window + top-k (C4) or all L/128 entries (C128)
+// a1 and a2 run in one small kernel (one CTA per sequence); a3-a5 are the
+// standalone kernels reading the live prefix of the capacity-laid-out pools.
+#include "common.cuh"
+#include "compress_core.cuh"
+#include "internal.h"
+
+namespace hsa {
+namespace {
+
+constexpr int kAppendThreads = 256;
+
+struct AppendParams {
+  int kind, r, B, Dqk, Di, W;
+  const int32_t* seq_len_in;
+  int32_t* seq_len_out;
+  const int64_t* pool_offsets;
+  int64_t pool_total_rows;
+  const uint4* kv_new;
+  const uint4* z_new;
+  const float* b_kv;
+  const uint4* ik_new;
+  const uint4* iz_new;
+  const float* b_ik;
+  uint4* swa;
+  uint4* kv_ring;
+  uint4* z_ring;
+  uint4* ik_ring;
+  uint4* iz_ring;
+  uint4* kv_pool;
+  uint4* key_pool;
+  uint32_t* status;
+};
+
+// Compresses the r-row ring block of width C (C/8 chunks) of sequence b into
+// `dst` (one bf16 row).  Rows are split over `split` adjacent lanes.
+HSA_DEVINL void compress_block(const uint4* kv, const uint4* z, const float* bias, int r, int C,
+                               uint4* dst) {
+  const int chunks = C / 8;
+  const int split = r >= 32 ? 8 : 1;
+  const int items = chunks * split;  // a multiple of 32 whenever split > 1
+  for (int i0 = 0; i0 < items; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    if (split > 1 && i0 + static_cast<int>(threadIdx.x & ~31u) >= items) break;  // whole idle warp
+    const bool live = i < items;
+    const int c = live ? i / split : 0, part = live ? i % split : 0;
+    const int per = (r + split - 1) / split;
+    const int lo = live ? min(r, part * per) : 0, hi = live ? min(r, lo + per) : 0;
+    auto brow = [&](int row, float4* b0, float4* b1) {
+      const float4* bp = reinterpret_cast<const float4*>(bias + static_cast<int64_t>(row) * C + c * 8);
+      *b0 = __ldg(bp);
+      *b1 = __ldg(bp + 1);
+    };
+    GatePartial pt;
+    partial_init(pt);
+    partial_rows(kv + c, z + c, chunks, lo, hi, brow, pt);
+    if (split > 1) partial_merge_lanes(pt, split);
+    if (live && part == 0) {
+      float o[8];
+      partial_result(pt, o);
+      dst[c] = f32x8_to_bf16(o);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendParams p) {
+  const int b = blockIdx.x;
+  const int64_t L = static_cast<int64_t>(p.seq_len_in[b]) + 1;
+  const int cq = p.Dqk / 8, ci = p.Di / 8;
+  const int64_t slot_w = (L - 1) % p.W, slot_r = (L - 1) % p.r;
+  // a1: the new token's rows into the window ring and the in-flight rings
+  for (int c = threadIdx.x; c < cq; c += blockDim.x) {
+    const uint4 kv = p.kv_new[static_cast<int64_t>(b) * cq + c];
+    const uint4 z = p.z_new[static_cast<int64_t>(b) * cq + c];
+    p.swa[(static_cast<int64_t>(b) * p.W + slot_w) * cq + c] = kv;
+    p.kv_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = kv;
+    p.z_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = z;
+  }
+  if (p.kind == HSA_LAYER_C4) {
+    for (int c = threadIdx.x; c < ci; c += blockDim.x) {
+      p.ik_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] =
+          p.ik_new[static_cast<int64_t>(b) * ci + c];
+      p.iz_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] =
+          p.iz_new[static_cast<int64_t>(b) * ci + c];
+    }
+  }
+  __syncthreads();  // ring writes visible to the block; seq_len_in read by all
+  if (threadIdx.x == 0) p.seq_len_out[b] = static_cast<int32_t>(L);
+  if (L % p.r != 0) return;
+  // a2: the block is complete -> compress it into pool row L/r - 1
+  const int64_t n = L / p.r - 1;
+  const int64_t o0 = p.pool_offsets[b], o1 = p.pool_offsets[b + 1];
+  if (o0 < 0 || o1 > p.pool_total_rows || o0 + n >= o1) {
+    if (threadIdx.x == 0) set_status(p.status, HSA_DEV_BOUNDS);
+    return;
+  }
+  compress_block(p.kv_ring + static_cast<int64_t>(b) * p.r * cq,
+                 p.z_ring + static_cast<int64_t>(b) * p.r * cq, p.b_kv, p.r, p.Dqk,
+                 p.kv_pool + (o0 + n) * cq);
+  if (p.kind == HSA_LAYER_C4)
+    compress_block(p.ik_ring + static_cast<int64_t>(b) * p.r * ci,
+                   p.iz_ring + static_cast<int64_t>(b) * p.r * ci, p.b_ik, p.r, p.Di,
+                   p.key_pool + (o0 + n) * ci);
+}
+
+HSA_HOST_DEVICE size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct LayerWs {
+  size_t scores, topk, idx, attn, total;
+  LayerWs(const hsa_layer_desc& d, const AttnPlan& pl) {
+    size_t at = kWsHeader;
+    scores = topk = idx = 0;
+    if (d.kind == HSA_LAYER_C4) {
+      scores = at;
+      if (!d.scores) at += a256(static_cast<size_t>(d.pool_total_rows > 0 ? d.pool_total_rows : 1) * 4);
+      topk = at;
+      at += a256(topk_workspace_bytes(d.B, d.pool_total_rows, d.k));
+      idx = at;
+      if (!d.topk_idx) at += a256(static_cast<size_t>(d.B) * d.k * 4);
+    }
+    attn = at;
+    at += a256(attn_workspace_bytes(pl, d.B, d.Hq, d.Dv));
+    total = at;
+  }
+};
+
+AttnPlan layer_attn_plan(const hsa_layer_desc& d) {
+  const int64_t slots = d.kind == HSA_LAYER_C4 ? d.k : d.max_pool_rows;
+  return attn_plan(d.B, d.Hq, d.Dqk, d.Dv, d.W, slots);
+}
+
+}  // namespace
+
+size_t layer_workspace_bytes(const hsa_layer_desc& d) {
+  return LayerWs(d, layer_attn_plan(d)).total;
+}
+
+cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream) {
+  const int r = d.kind;
+  const AttnPlan pl = layer_attn_plan(d);
+  const LayerWs L(d, pl);
+  char* w = static_cast<char*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(w);
+
+  AppendParams ap;
+  ap.kind = d.kind;
+  ap.r = r;
+  ap.B = d.B;
+  ap.Dqk = d.Dqk;
+  ap.Di = d.kind == HSA_LAYER_C4 ? d.Di : 0;
+  ap.W = d.W;
+  ap.seq_len_in = d.seq_len_in;
+  ap.seq_len_out = d.seq_len_out;
+  ap.pool_offsets = d.pool_offsets;
+  ap.pool_total_rows = d.pool_total_rows;
+  ap.kv_new = static_cast<const uint4*>(d.kv_new);
+  ap.z_new = static_cast<const uint4*>(d.z_new);
+  ap.b_kv = d.b_kv;
+  ap.ik_new = static_cast<const uint4*>(d.ik_new);
+  ap.iz_new = static_cast<const uint4*>(d.iz_new);
+  ap.b_ik = d.b_ik;
+  ap.swa = static_cast<uint4*>(d.swa);
+  ap.kv_ring = static_cast<uint4*>(d.kv_ring);
+  ap.z_ring = static_cast<uint4*>(d.z_ring);
+  ap.ik_ring = static_cast<uint4*>(d.ik_ring);
+  ap.iz_ring = static_cast<uint4*>(d.iz_ring);
+  ap.kv_pool = static_cast<uint4*>(d.kv_pool);
+  ap.key_pool = static_cast<uint4*>(d.key_pool);
+  ap.status = status;
+  layer_append_kernel<<<d.B, kAppendThreads, 0, stream>>>(ap);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  // a3-a5 read the live prefix L/r of each sequence's pool rows
+  const Spans sp{d.pool_offsets, d.seq_len_out, 0, r, d.pool_total_rows};
+  const int32_t* idx = nullptr;
+  if (d.kind == HSA_LAYER_C4) {
+    float* scores = d.scores ? d.scores : reinterpret_cast<float*>(w + L.scores);
+    int32_t* tidx = d.topk_idx ? d.topk_idx : reinterpret_cast<int32_t*>(w + L.idx);
+    e = launch_indexer(d.iq, d.w, d.key_pool, sp, d.B, d.Hi, d.Di, d.pool_total_rows, scores,
+                       status, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_topk(scores, sp, d.B, d.pool_total_rows, d.k, tidx, nullptr, w + L.topk, status,
+                    stream);
+    if (e != cudaSuccess) return e;
+    idx = tidx;
+  }
+  AttnArgs a;
+  a.q = d.q;
+  a.swa = d.swa;
+  a.seq_len = d.seq_len_out;
+  a.len_add = 0;
+  a.W = d.W;
+  a.extra = d.kv_pool;
+  a.sp = sp;
+  a.idx = idx;
+  a.k = d.kind == HSA_LAYER_C4 ? d.k : 0;
+  a.max_rows = d.kind == HSA_LAYER_C4 ? 0 : d.max_pool_rows;
+  a.B = d.B;
+  a.Hq = d.Hq;
+  a.Dqk = d.Dqk;
+  a.Dv = d.Dv;
+  a.scale = d.scale;
+  a.out = d.out;
+  a.out_dtype = d.out_dtype;
+  a.lse = d.lse;
+  return launch_attn(a, pl, w + L.attn, status, stream);
+}
+
+}  // namespace hsa

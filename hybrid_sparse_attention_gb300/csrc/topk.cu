@@ -81,10 +81,10 @@ struct WsLayout {
   }
 };
 
-Ws ws_view(void* base, int64_t B, int64_t total_rows, int64_t k) {
+Ws ws_view(void* base, int64_t B, int64_t total_rows, int64_t k, uint32_t* status) {
   WsLayout L(B, total_rows, k);
   char* p = static_cast<char*>(base);
-  return Ws{reinterpret_cast<uint32_t*>(p), reinterpret_cast<RowState*>(p + L.rows),
+  return Ws{status, reinterpret_cast<RowState*>(p + L.rows),
             reinterpret_cast<uint32_t*>(p + L.hist), reinterpret_cast<uint64_t*>(p + L.win),
             reinterpret_cast<uint64_t*>(p + L.cand)};
 }
@@ -390,10 +390,11 @@ int64_t topk_chunk(int64_t total_rows) {
 }
 
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
-                        int32_t* idx, float* vals, void* ws, cudaStream_t stream) {
+                        int32_t* idx, float* vals, void* ws, uint32_t* status,
+                        cudaStream_t stream) {
   const int64_t chunk = topk_chunk(total_rows);
   const int64_t grid = (total_rows + chunk - 1) / chunk + B;  // upper bound on chunks
-  Ws w = ws_view(ws, B, total_rows, k);
+  Ws w = ws_view(ws, B, total_rows, k, status);
   topk_hist_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(scores, sp, B, k, chunk,
                                                                          w);
   cudaError_t e = cudaGetLastError();

@@ -57,6 +57,9 @@ typedef enum {
 
 typedef enum { HSA_F32 = 0, HSA_BF16 = 1 } hsa_dtype_t;
 
+/* Kind of compressed pool a layer pairs with its window (= compression ratio). */
+typedef enum { HSA_LAYER_C4 = 4, HSA_LAYER_C128 = 128 } hsa_layer_kind_t;
+
 /* Sticky device status bits (OR-ed into the workspace status word). */
 #define HSA_DEV_BOUNDS 0x1u
 #define HSA_DEV_TIMEOUT 0x2u
@@ -180,6 +183,71 @@ hsa_status_t hsa_decode_attn(const void* q, const void* swa, const int32_t* seq_
                              int64_t max_extra_rows, int64_t B, int64_t Hq, int64_t Dqk,
                              int64_t Dv, float scale, void* out, int out_dtype, float* lse,
                              void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * One decode step of one hybrid layer — [WK] §核心观点 (each layer keeps the
+ * SWA window, its compressed pool and the in-flight block that is compressed
+ * once 4 / 128 tokens have accumulated; C4 picks its top-k, C128 attends
+ * all); [KD] §Arquitectura del Sistema (compression-state ring buffers) and
+ * §Flujo de Inferencia steps 3, 5, 6.
+ *
+ * With L_b = seq_len_in[b] + 1 (the context after this step's token), in
+ * stream order and without host synchronisation:
+ *   1. append: kv_new[b] -> swa[b, (L_b-1) mod W]; kv_new, z_new ->
+ *      kv_ring / z_ring[b, (L_b-1) mod r]; (C4) ik_new, iz_new -> ik_ring /
+ *      iz_ring likewise; seq_len_out[b] = L_b (seq_len_out may alias
+ *      seq_len_in: then repeated calls advance the sequence);
+ *   2. if L_b mod r == 0: compress the completed ring block (hsa_compress
+ *      arithmetic, bf16 result) into kv_pool row pool_offsets[b] + L_b/r - 1
+ *      and (C4) the indexer-key ring into key_pool at the same row;
+ *   3. (C4) indexer scores over the N_b = L_b/4 live pool rows;
+ *   4. (C4) top-k of those scores (topk_idx, row-local, -1 padded);
+ *   5. attention over the window and the selected (C4) or all N_b = L_b/128
+ *      (C128) pool rows -> out, lse.
+ * r = kind.  Pools use a capacity layout: sequence b owns rows
+ * [pool_offsets[b], pool_offsets[b+1]) of kv_pool (and key_pool), of which
+ * the first L_b / r are live; a step that would write past the capacity sets
+ * HSA_DEV_BOUNDS and skips that write.  Rings hold r rows per sequence, in
+ * block order.  Five kernel launches for C4, two for C128.
+ * Shapes as for the individual stages; C4 needs Hi, Di, k, iq, w, key_pool,
+ * the ik / iz rings and b_ik; C128 needs max_pool_rows >= every N_b.
+ * ---------------------------------------------------------------------- */
+typedef struct hsa_layer_desc {
+  int32_t kind;             /* HSA_LAYER_C4 or HSA_LAYER_C128 */
+  int32_t B, Hq, Dqk, Dv;   /* sequences, query heads, key / value widths */
+  int32_t Hi, Di;           /* indexer heads and width (C4) */
+  int32_t W, k;             /* window rows; top-k (C4) */
+  float scale;              /* softmax scale */
+  int32_t out_dtype;        /* HSA_BF16 or HSA_F32 */
+  int64_t pool_total_rows;  /* rows of kv_pool / key_pool */
+  int64_t max_pool_rows;    /* C128: bound on live pool rows per sequence */
+  const int32_t* seq_len_in;    /* [B] tokens before this step */
+  int32_t* seq_len_out;         /* [B] tokens after this step (may alias) */
+  const int64_t* pool_offsets;  /* [B+1] capacity layout of the pools */
+  const void* kv_new;       /* bf16 [B, Dqk] new token's latent kv row */
+  const void* z_new;        /* bf16 [B, Dqk] its gate logits */
+  const float* b_kv;        /* fp32 [r, Dqk] positional gate bias */
+  const void* ik_new;       /* bf16 [B, Di] new raw indexer key (C4) */
+  const void* iz_new;       /* bf16 [B, Di] its gate logits (C4) */
+  const float* b_ik;        /* fp32 [r, Di] (C4) */
+  void* swa;                /* bf16 [B, W, Dqk] window ring */
+  void* kv_ring;            /* bf16 [B, r, Dqk] in-flight block */
+  void* z_ring;             /* bf16 [B, r, Dqk] */
+  void* ik_ring;            /* bf16 [B, r, Di] (C4) */
+  void* iz_ring;            /* bf16 [B, r, Di] (C4) */
+  void* kv_pool;            /* bf16 [pool_total_rows, Dqk] */
+  void* key_pool;           /* bf16 [pool_total_rows, Di] (C4) */
+  const void* q;            /* bf16 [B, Hq, Dqk] */
+  const void* iq;           /* bf16 [B, Hi, Di] (C4) */
+  const float* w;           /* fp32 [B, Hi] (C4) */
+  void* out;                /* [B, Hq, Dv] of out_dtype */
+  float* lse;               /* fp32 [B, Hq] or NULL */
+  int32_t* topk_idx;        /* int32 [B, k] or NULL (kept in the workspace) (C4) */
+  float* scores;            /* fp32 [pool_total_rows] or NULL (workspace) (C4) */
+} hsa_layer_desc;
+
+size_t hsa_layer_decode_workspace_size(const hsa_layer_desc* d);
+hsa_status_t hsa_layer_decode(const hsa_layer_desc* d, void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

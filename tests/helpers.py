@@ -34,3 +34,25 @@ def bf16_values(bits: np.ndarray) -> np.ndarray:
     """float64 values of bf16 bit patterns (via torch, not the oracle)."""
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
     return t.to(torch.float64).numpy()
+
+
+def np_state(st):
+    """numpy copy of a synth.LayerState for the oracle (bf16 as uint16 bits)."""
+    out = {k: (bf16_bits(v) if v.dtype == torch.bfloat16 else v.detach().cpu().numpy().copy())
+           for k, v in st.tensors().items()}
+    out.update(kind=st.kind, ratio=st.ratio, Dv=st.shape.Dv, k=st.shape.k, scale=st.shape.scale)
+    return out
+
+
+def set_agreement(idx_a, idx_b, counts, k):
+    """Mean over rows of |A ∩ B| / min(k, N_b) (rows with N_b = 0 count as 1)."""
+    vals = []
+    for b in range(idx_a.shape[0]):
+        m = min(k, int(counts[b]))
+        if m == 0:
+            vals.append(1.0)
+            continue
+        a = set(int(x) for x in idx_a[b] if x >= 0)
+        c = set(int(x) for x in idx_b[b] if x >= 0)
+        vals.append(len(a & c) / m)
+    return float(np.mean(vals))

@@ -1,0 +1,198 @@
+"""End-to-end parity of one hybrid-layer decode step (append, compress on block
+completion, indexer, top-k, attention) against the oracle's composition."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_bits, bf16_values, np_state, set_agreement
+from hybrid_sparse_attention_gb300 import _lib, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def rel_err(gpu, ref):
+    return np.abs(gpu - ref) / np.maximum(np.abs(ref), 1e-2)
+
+
+def score_tol(iq, w, keys, offs, factor):
+    """factor * sum_h |w_h| sum_d |q_hd k_jd| per row (keys in pool rows)."""
+    q = np.abs(bf16_values(iq))
+    k = np.abs(bf16_values(keys))
+    out = np.zeros(k.shape[0])
+    for b in range(len(offs) - 1):
+        lo, hi = int(offs[b]), int(offs[b + 1])
+        out[lo:hi] = (k[lo:hi] @ q[b].T) @ np.abs(w[b].astype(np.float64))
+    return factor * out
+
+
+def run_gpu_step(g, out_dtype=torch.bfloat16, seq_len_out=None):
+    B = g.seq_len_in.numel()
+    sh = g.shape
+    out = torch.empty(B, sh.Hq, sh.Dv, dtype=out_dtype, device="cuda")
+    lse = torch.empty(B, sh.Hq, dtype=torch.float32, device="cuda")
+    so = torch.empty_like(g.seq_len_in) if seq_len_out is None else seq_len_out
+    res = {"out": out, "lse": lse, "seq_len_out": so}
+    kw = {}
+    if g.kind == 4:
+        res["idx"] = torch.empty(B, sh.k, dtype=torch.int32, device="cuda")
+        res["scores"] = torch.zeros(g.kv_pool.shape[0], dtype=torch.float32, device="cuda")
+        kw = dict(topk_idx=res["idx"], scores=res["scores"])
+    desc = _lib.layer_desc(g, out, lse, so, **kw)
+    ws = _lib.hsa_layer_decode(desc)
+    torch.cuda.synchronize()
+    assert _lib.hsa_workspace_status(ws) == 0
+    return res
+
+
+def build_tiny(kind, L=4096):
+    """Tiny layer from raw tokens: the oracle and the GPU each compress the
+    history into their own pools."""
+    st, raw = synth.raw_token_state(synth.SEED["tiny"], kind, synth.TINY, L)
+    return st, raw
+
+
+def gpu_prefix_pools(g, raw, kind):
+    kv = _lib.hsa_compress(raw["kv"].cuda(), raw["z"].cuda(), g.b_kv, kind)
+    g.kv_pool[:kv.shape[1]] = kv[0]
+    if kind == 4:
+        ks = _lib.hsa_compress(raw["ik"].cuda(), raw["iz"].cuda(), g.b_ik, 4)
+        g.key_pool[:ks.shape[1]] = ks[0]
+
+
+def oracle_prefix_pools(oracle_mod, s, raw, kind):
+    pre = oracle_mod.compress(bf16_bits(raw["kv"]), bf16_bits(raw["z"]), s["b_kv"], kind)[0]
+    s["kv_pool"][:pre.shape[0]] = oracle_mod.float_to_bf16(pre.astype(np.float32))
+    if kind == 4:
+        pk = oracle_mod.compress(bf16_bits(raw["ik"]), bf16_bits(raw["iz"]), s["b_ik"], 4)[0]
+        s["key_pool"][:pk.shape[0]] = oracle_mod.float_to_bf16(pk.astype(np.float32))
+
+
+def check_step(oracle_mod, g, s, res, ref, min_agree):
+    kind = g.kind
+    L = ref["seq_len_out"].astype(np.int64)
+    assert np.array_equal(res["seq_len_out"].cpu().numpy(), ref["seq_len_out"])
+    offs = s["pool_offsets"]
+    counts = L // kind
+    # pools: every live row within the compressor tolerance
+    gp = bf16_values(bf16_bits(g.kv_pool.cpu()))
+    rp = bf16_values(s["kv_pool"])
+    for b in range(len(L)):
+        lo = int(offs[b])
+        n = int(counts[b])
+        assert rel_err(gp[lo:lo + n], rp[lo:lo + n]).max() <= 5e-3
+    assert np.array_equal(bf16_bits(g.swa.cpu()), s["swa"])
+    idx_used = None
+    if kind == 4:
+        gs = res["scores"].cpu().numpy().astype(np.float64)
+        key_rows, key_offs = oracle_mod.compact(s["key_pool"], offs, counts)
+        gsc = np.concatenate([gs[int(offs[b]):int(offs[b]) + int(counts[b])] for b in range(len(L))])
+        # keys may differ by one bf16 rounding step: |dk| <= 2^-8 |k|
+        tol = score_tol(s["iq"], s["w"], key_rows, key_offs, 2.0 ** -7) + 1e-30
+        assert np.all(np.abs(gsc - ref["scores64"]) <= tol)
+        gidx = res["idx"].cpu().numpy()
+        # top-k bit-exact on the GPU's own fp32 scores
+        own, _ = oracle_mod.topk(gsc.astype(np.float32), key_offs, s["k"], threads=16)
+        assert np.array_equal(gidx, own)
+        agree = set_agreement(gidx, ref["idx"], counts, s["k"])
+        assert agree >= min_agree, f"top-k set agreement {agree:.5f}"
+        idx_used = gidx
+    # attention: oracle fed the GPU's selected indices (its own pools)
+    kv_rows, kv_offs = oracle_mod.compact(s["kv_pool"], offs, counts)
+    o_ref, l_ref = oracle_mod.decode_attn(s["q"], s["swa"], L.astype(np.int32), s["swa"].shape[1],
+                                          kv_rows, kv_offs, idx_used, s["scale"], s["Dv"],
+                                          threads=16)
+    go = res["out"].float().cpu().numpy()
+    err = np.abs(go - o_ref).max()
+    assert err <= 1e-2, f"attention max abs err {err:.3e}"
+    lerr = np.abs(res["lse"].cpu().numpy() - l_ref).max()
+    assert lerr <= 2.0 ** -8
+    return err
+
+
+@pytest.mark.parametrize("kind", [4, 128])
+def test_layer_tiny_from_raw_tokens(oracle_mod, kind):
+    st, raw = build_tiny(kind)
+    s = np_state(st)
+    oracle_prefix_pools(oracle_mod, s, raw, kind)
+    g = st.to("cuda")
+    gpu_prefix_pools(g, raw, kind)
+    res = run_gpu_step(g)
+    ref = oracle_mod.layer_decode(s)
+    # one sequence with 64 of 1,024 entries: allow one flip at the threshold
+    check_step(oracle_mod, g, s, res, ref, min_agree=62 / 64)
+
+
+def test_layer_tiny_dense_equivalence_k_covers_all():
+    """k >= the number of C4 entries: the sparse C4 layer equals dense attention
+    over every entry (plus the window)."""
+    shape = synth.LayerShape(Hq=8, Dqk=128, Dv=128, Hi=2, Di=32, k=1024, W=64)
+    st, raw = synth.raw_token_state(synth.SEED["tiny"], 4, shape, 4096)
+    g = st.to("cuda")
+    gpu_prefix_pools(g, raw, 4)
+    res = run_gpu_step(g, out_dtype=torch.float32)
+    # dense attention over the same pool rows and window
+    n = 4096 // 4
+    o, l = _lib.hsa_decode_attn(g.q, g.swa, res["seq_len_out"], g.kv_pool[:n].contiguous(),
+                                torch.tensor([0, n], dtype=torch.int64, device="cuda"), None,
+                                max_extra_rows=n, scale=shape.scale, Dv=128,
+                                out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert (res["out"] - o).abs().max().item() <= 1e-3
+    assert (res["lse"] - l).abs().max().item() <= 1e-3
+
+
+def test_layer_multi_step_in_place(oracle_mod):
+    """Six consecutive in-place steps (seq_len_out aliases seq_len_in) crossing
+    two block completions; the state carried by the rings stays in parity."""
+    kind = 4
+    st, raw = build_tiny(kind, L=4091)
+    s = np_state(st)
+    oracle_prefix_pools(oracle_mod, s, raw, kind)
+    g = st.to("cuda")
+    gpu_prefix_pools(g, raw, kind)
+    for step in range(6):
+        name = f"step{step}"
+        for key in ("kv_new", "z_new", "ik_new", "iz_new"):
+            v = synth.normal_bf16(synth.SEED["tiny"], f"{name}.{key}", tuple(getattr(st, key).shape))
+            getattr(g, key).copy_(v.cuda())
+            s[key] = bf16_bits(v)
+        res = run_gpu_step(g, seq_len_out=g.seq_len_in)
+        ref = oracle_mod.layer_decode(s)
+        s["seq_len_in"] = ref["seq_len_out"].copy()
+        assert int(g.seq_len_in.item()) == 4091 + step
+        check_step(oracle_mod, g, s, res, ref, min_agree=62 / 64)
+
+
+def test_layer_step_is_idempotent_with_separate_output_length():
+    L = synth.c4_lengths(synth.SEED["c4layer"], 8, 4000, 9000)
+    g = synth.filled_state(synth.SEED["c4layer"], 4, synth.FULL, L, device="cuda", name="idem")
+    a = run_gpu_step(g)
+    b = run_gpu_step(g)
+    assert torch.equal(a["out"], b["out"]) and torch.equal(a["idx"], b["idx"])
+    assert torch.equal(a["seq_len_out"], L.cuda())
+
+
+def test_layer_c4_full_128k_batch64(oracle_mod):
+    """The headline workload: batch 64, contexts U[16384, 131072], 64 heads x
+    576, indexer 8 x 128, top-512, window 128; every stage against the oracle."""
+    L = synth.c4_lengths(synth.SEED["c4layer"], 64)
+    g = synth.filled_state(synth.SEED["c4layer"], 4, synth.FULL, L, device="cuda")
+    s = np_state(g)           # snapshot before the GPU step mutates rings and pools
+    res = run_gpu_step(g)
+    ref = oracle_mod.layer_decode(s, threads=16)
+    check_step(oracle_mod, g, s, res, ref, min_agree=0.999)
+
+
+@pytest.mark.parametrize("kind", [4, 128])
+def test_layer_long_context_batch4(oracle_mod, kind):
+    """The 1M-token pair: batch 4 at L = 1,048,576 (this step completes a block
+    for both ratios), C4 top-512 over 262,144 entries or C128 dense over 8,192."""
+    L = torch.full((4,), 1048576, dtype=torch.int32)
+    g = synth.filled_state(synth.SEED["longctx"], kind, synth.FULL, L, device="cuda",
+                           name=f"long{kind}")
+    s = np_state(g)
+    res = run_gpu_step(g)
+    ref = oracle_mod.layer_decode(s, threads=16)
+    check_step(oracle_mod, g, s, res, ref, min_agree=0.999)
