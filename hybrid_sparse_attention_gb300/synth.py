@@ -215,13 +215,14 @@ class LayerState:
         return LayerState(**kw)
 
 
-def raw_token_state(seed: int, kind: int, shape: LayerShape, L: int, device="cpu"):
+def raw_token_state(seed: int, kind: int, shape: LayerShape, L: int, device="cpu",
+                    slack: int = 1):
     """A single-sequence layer whose history is L-1 raw tokens (kv, z ~ N(0,1);
     indexer raw keys and their gates ~ N(0,1)), plus the new token, positional
     biases b ~ N(0, 0.5^2), q ~ N(0,1), indexer q ~ N(0,1) and w ~ U(0,1).
     The compressed pools are left empty (zero): the caller builds them from the
-    raw history with its own compressor.  Returns (state, raw) where raw holds
-    the history tensors."""
+    raw history with its own compressor; each pool has room for `slack` rows
+    beyond L // r.  Returns (state, raw) where raw holds the history tensors."""
     r = kind
     name = "c4" if kind == 4 else "c128"
     D, Di = shape.Dqk, shape.Di
@@ -232,7 +233,7 @@ def raw_token_state(seed: int, kind: int, shape: LayerShape, L: int, device="cpu
         raw["ik"] = normal_bf16(seed, f"{name}.ik", (1, hist, Di), device=device)
         raw["iz"] = normal_bf16(seed, f"{name}.iz", (1, hist, Di), device=device)
     n_full = hist // r
-    offs = capacity_offsets([L // r], slack=1)
+    offs = capacity_offsets([L // r], slack=slack)
     W = shape.W
     swa = torch.zeros(1, W, D, dtype=torch.bfloat16, device=device)
     for p in range(max(0, hist - W), hist):

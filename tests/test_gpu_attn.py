@@ -74,7 +74,7 @@ def test_attention_worked_example_embedded(oracle_mod):
         want = [closed_form(e) for e in g[key]["out"]]
         np.testing.assert_allclose(o[0, 0, :2], want, atol=OUT_TOL)
         assert abs(l[0, 0] - closed_form(g[key]["lse"])) < LSE_TOL
-        assert np.all(o[0, 0, 2:] == 0)
+        assert np.all(o[0, 0, 3:] == 0)  # channels past the example are zero padding
 
 
 def _tiny_case(B=1, Hq=8, D=128, Dv=128, W=64, k=64, counts=(1024,), L=(4096,), tag="tiny"):
@@ -129,10 +129,13 @@ def test_attention_dense_c128_with_splits(oracle_mod):
 def test_attention_rescale_path(oracle_mod):
     """Later tiles carry much larger logits than the window tile, forcing the
     running maximum to move and O to be rescaled in TMEM; the first tile of one
-    sequence is entirely masked."""
+    sequence is entirely masked.  Only the rope channels (512..575, keys but not
+    values) are scaled up, so the values keep unit scale."""
     counts = [900, 900]
     q, swa, L, extra, offs, idx = _tiny_case(2, 64, 576, 512, 128, 512, counts, [5000, 5000], "resc")
-    extra = (extra.float() * torch.linspace(0.5, 6.0, extra.shape[0])[:, None]).to(torch.bfloat16)
+    ramp = torch.ones(extra.shape[0], 576)
+    ramp[:, 512:] = torch.linspace(0.5, 40.0, extra.shape[0])[:, None]
+    extra = (extra.float() * ramp).to(torch.bfloat16)
     L[1] = 0                                     # no window: tile 0 = compressed rows only
     idx[1, :200] = -1                            # ... whose first 128 slots are all masked
     scale = 1 / math.sqrt(576)

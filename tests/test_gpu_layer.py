@@ -46,10 +46,10 @@ def run_gpu_step(g, out_dtype=torch.bfloat16, seq_len_out=None):
     return res
 
 
-def build_tiny(kind, L=4096):
+def build_tiny(kind, L=4096, slack=1):
     """Tiny layer from raw tokens: the oracle and the GPU each compress the
     history into their own pools."""
-    st, raw = synth.raw_token_state(synth.SEED["tiny"], kind, synth.TINY, L)
+    st, raw = synth.raw_token_state(synth.SEED["tiny"], kind, synth.TINY, L, slack=slack)
     return st, raw
 
 
@@ -147,7 +147,7 @@ def test_layer_multi_step_in_place(oracle_mod):
     """Six consecutive in-place steps (seq_len_out aliases seq_len_in) crossing
     two block completions; the state carried by the rings stays in parity."""
     kind = 4
-    st, raw = build_tiny(kind, L=4091)
+    st, raw = build_tiny(kind, L=4091, slack=4)   # room for the blocks of 6 more tokens
     s = np_state(st)
     oracle_prefix_pools(oracle_mod, s, raw, kind)
     g = st.to("cuda")
