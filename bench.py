@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of the decode-time hybrid sparse-attention hot path.
+
+One step = one decode step of one C4 hybrid layer through the C ABI
+(hsa_layer_decode): append the new token, compress the completed 4-token
+blocks, score every C4 entry with the indexer, select the top-512, and attend
+the 128-token window plus the selected entries.  Workload: batch 64, context
+lengths uniform in [16,384, 131,072], 64 query heads of 512 latent + 64 rope
+channels sharing one KV head, indexer 8 heads x 128, window 128, top-512,
+bf16 storage, fp32 accumulation, synthetic seeded inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hsa|reference]
+
+Prints one JSON line (rank 0).  Under torchrun with N > 1 every rank runs an
+independent replica of the workload (its own seed): weak scaling, no data-path
+collective; the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from hybrid_sparse_attention_gb300 import _lib, synth  # noqa: E402
+
+METRIC = "us per decode layer (C4+SWA, 128K ctx, batch 64)"
+WORKLOAD = ("C4 hybrid decode layer: B=64, L~U[16384,131072], Hq=64, Dqk=576 (512+64), Dv=512, "
+            "indexer Hi=8 Di=128, top-k 512, SWA window 128, 1 query token")
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def layer_bytes(L, shape):
+    """Algorithmic HBM bytes of one C4 layer step (each byte the method must
+    move, counted once): indexer keys, score write + read, the gathered window
+    and top-k rows, q, o, the index list, plus the new-token append and the
+    4-row block reads/writes of the sequences whose block completes."""
+    L = L.to(torch.int64)
+    n4 = L // 4
+    B = L.numel()
+    D, Di = shape.Dqk, shape.Di
+    keys = int(n4.sum()) * Di * 2
+    iq_w = B * shape.Hi * (Di * 2 + 4)
+    scores = 2 * int(n4.sum()) * 4
+    rows = int((torch.clamp(L, max=shape.W) + torch.clamp(n4, max=shape.k)).sum())
+    gather = rows * D * 2
+    q = B * shape.Hq * D * 2
+    o = B * shape.Hq * shape.Dv * 2 + B * shape.Hq * 4
+    idx = 2 * B * shape.k * 4
+    append = B * (D * 2 * 2 + D * 2 * 3 + Di * 2 * 2 + Di * 2 * 2)   # read new rows, write rings
+    ncomp = int((L % 4 == 0).sum())
+    compress = ncomp * (4 * 2 * (D + Di) * 2 + (D + Di) * 2)
+    indexer = keys + iq_w + int(n4.sum()) * 4
+    total = keys + iq_w + scores + gather + q + o + idx + append + compress
+    return {"total": total, "indexer": indexer, "keys": keys, "gather": gather}
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        return world, rank, local, dist
+    return 1, 0, local, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x, dist):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def sample_state(g, seqs):
+    """numpy copy (oracle input) of sequences `seqs` of a GPU layer state."""
+    offs = g.pool_offsets.cpu()
+    bits = lambda t: t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    kv = torch.cat([g.kv_pool[int(offs[b]):int(offs[b + 1])] for b in seqs])
+    key = torch.cat([g.key_pool[int(offs[b]):int(offs[b + 1])] for b in seqs])
+    caps = torch.tensor([int(offs[b + 1] - offs[b]) for b in seqs], dtype=torch.int64)
+    new_offs = torch.zeros(len(seqs) + 1, dtype=torch.int64)
+    new_offs[1:] = torch.cumsum(caps, 0)
+    sel = torch.tensor(seqs, device=g.q.device)
+    s = {"kind": g.kind, "ratio": g.ratio, "Dv": g.shape.Dv, "k": g.shape.k,
+         "scale": g.shape.scale, "pool_offsets": new_offs.numpy(),
+         "seq_len_in": g.seq_len_in[sel].cpu().numpy(), "kv_pool": bits(kv), "key_pool": bits(key),
+         "b_kv": g.b_kv.cpu().numpy(), "b_ik": g.b_ik.cpu().numpy(),
+         "w": g.w[sel].cpu().numpy()}
+    for name in ("swa", "kv_ring", "z_ring", "ik_ring", "iz_ring", "kv_new", "z_new", "ik_new",
+                 "iz_new", "q", "iq"):
+        s[name] = bits(getattr(g, name)[sel])
+    return s
+
+
+def oracle_layer_time(g, budget_s, per_call=4):
+    """Times the oracle layer step over successive sequence groups until the
+    budget is spent; returns (us per full 64-sequence layer, sequences, threads)."""
+    import oracle
+    oracle.build()
+    threads = oracle.hardware_threads()
+    B = g.seq_len_in.numel()
+    done, spent = 0, 0.0
+    while done < B and (spent < budget_s or done == 0):
+        seqs = list(range(done, min(B, done + per_call)))
+        s = sample_state(g, seqs)
+        t0 = time.perf_counter()
+        oracle.layer_decode(s, threads=threads)
+        spent += time.perf_counter() - t0
+        done += len(seqs)
+    return spent / done * B * 1e6, done, threads
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="hsa", choices=["hsa", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the CPU baseline (0: skip)")
+    ap.add_argument("--no-topk", action="store_true",
+                    help="skip the standalone top-k rows/s measurement")
+    args = ap.parse_args()
+    world, rank, local, dist = dist_setup()
+    torch.cuda.set_device(local)
+    if args.impl == "reference":
+        run_reference(args, world, rank, dist)
+    else:
+        run_hsa(args, world, rank, local, dist)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def build_workload(rank):
+    seed = synth.SEED["c4layer"] + 1000 * rank
+    L = synth.c4_lengths(seed, 64)
+    g = synth.filled_state(seed, 4, synth.FULL, L, device="cuda")
+    return L, g
+
+
+def run_reference(args, world, rank, dist):
+    """The oracle (plain CPU C++), as it stands, on the host cores: each step is
+    one bounded sample of the same workload scaled to a full layer."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    L, g = build_workload(0)
+    threads = oracle.hardware_threads()
+    per_step = 2
+    for i in range(args.warmup):
+        oracle.layer_decode(sample_state(g, [i % 64]), threads=threads)
+    times = []
+    for i in range(args.steps):
+        seqs = [(per_step * i + j) % 64 for j in range(per_step)]
+        s = sample_state(g, seqs)
+        t0 = time.perf_counter()
+        oracle.layer_decode(s, threads=threads)
+        times.append((time.perf_counter() - t0) / per_step * 64 * 1e6)
+    us = statistics.mean(times)
+    sample = f"{per_step} of the 64 sequences per step (rotating), scaled x{64 // per_step}"
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": us, "unit": "us", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_hsa(args, world, rank, local, dist):
+    _lib.load(build_if_missing=True)
+    shape = synth.FULL
+    L, g = build_workload(rank)
+    B = L.numel()
+    stream = torch.cuda.current_stream()
+    out = torch.empty(B, shape.Hq, shape.Dv, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, shape.Hq, dtype=torch.float32, device="cuda")
+    seq_out = torch.empty_like(g.seq_len_in)
+    idx = torch.empty(B, shape.k, dtype=torch.int32, device="cuda")
+    scores = torch.empty(g.kv_pool.shape[0], dtype=torch.float32, device="cuda")
+    stage = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in stage:
+        e.record(stream)          # the events exist from here on
+    desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores,
+                           stage_events=[e.cuda_event for e in stage])
+    ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    nbytes = layer_bytes(L, shape)
+
+    def step():
+        _lib.hsa_layer_decode(desc, ws=ws)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    assert _lib.hsa_workspace_status(ws) == 0
+
+    # ------------------------------------------------ device-timed region
+    t_layer, t_stage = [], [[] for _ in range(4)]
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage_ms = []
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))               # evict the previous step's data from L2
+            ev0[i].record(stream)
+            step()
+            ev1[i].record(stream)
+            ev1[i].synchronize()                # stage events are reused: read them now
+            stage_ms.append([stage[j].elapsed_time(stage[j + 1]) for j in range(4)])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(dist)
+    t_layer = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    ms = statistics.mean(t_layer)
+    ms_max = max_over_ranks(ms, dist)
+    st = np.array(stage_ms)
+    stage_mean = st.mean(axis=0)                # append, indexer, top-k, attention (ms)
+    assert _lib.hsa_workspace_status(ws) == 0
+
+    # ------------------------------------------------ end to end: host buffers
+    host_in = {k: getattr(g, k).cpu().pin_memory() for k in
+               ("kv_new", "z_new", "ik_new", "iz_new", "q", "iq", "w")}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(float(i))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k, t in host_in.items():
+            getattr(g, k).copy_(t, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e = max_over_ranks(statistics.mean(e2e_ms), dist)
+
+    # ------------------------------------------------ standalone top-k (rows / s)
+    topk = topk_rows_per_s(flush) if rank == 0 and not args.no_topk else None
+
+    # ------------------------------------------------ CPU baseline: the oracle
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        us_cpu, nseq, threads = oracle_layer_time(g, args.cpu_budget)
+        cpu = {"value": us_cpu, "unit": "us", "cores": threads, "kind": "oracle",
+               "sample": f"oracle layer step on {nseq} of the 64 sequences "
+                         f"(groups of 4, ~{args.cpu_budget:.0f} s budget), scaled to 64"}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    idx_ms = float(stage_mean[1])
+    achieved = nbytes["indexer"] / (idx_ms * 1e-3) / 1e9
+    layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
+    traffic = indexer_traffic()
+    line = {
+        "metric": METRIC,
+        "value": ms_max * 1000 / world,
+        "unit": "us",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                   "l2": f"{L2_FLUSH_BYTES >> 20} MiB written before every step, outside the timed events",
+                   "sum_c4_entries": int((L // 4).sum()), "seed": synth.SEED["c4layer"]},
+        "roofline": {"bound": "hbm", "kernel": "indexer_kernel (tcgen05 scores)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
+                     "traffic": traffic, "algorithmic_bytes": nbytes["indexer"],
+                     "launch_us": idx_ms * 1000},
+        "layer_roofline": {"algorithmic_bytes": nbytes["total"], "achieved_gbs": layer_gbs,
+                           "frac": layer_gbs / peak},
+        "stage_us": {"append_compress": stage_mean[0] * 1000, "indexer": stage_mean[1] * 1000,
+                     "topk": stage_mean[2] * 1000, "attention": stage_mean[3] * 1000},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e * 1000 / world, "unit": "us", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed": wall,
+        "topk_rows_per_s": topk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def topk_rows_per_s(flush, iters=20):
+    """Standalone Lightning TopK on 64 rows x 262,144 fp32 (5% copied entries),
+    k=512: rows per second, L2 flushed before each launch."""
+    x = synth.topk_scores(synth.SEED["topk"], 64, 262144, 0.05, device="cuda").reshape(-1)
+    offs = torch.arange(65, dtype=torch.int64, device="cuda") * 262144
+    idx = torch.empty(64, 512, dtype=torch.int32, device="cuda")
+    ws = _lib.workspace(_lib.hsa_topk_workspace_size(64, x.numel(), 512))
+    for _ in range(3):
+        _lib.hsa_topk(x, offs, 512, idx=idx, ws=ws, with_vals=False)
+    ts = []
+    for i in range(iters):
+        flush.fill_(float(i))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        _lib.hsa_topk(x, offs, 512, idx=idx, ws=ws, with_vals=False)
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.mean(ts)
+    peak, _ = measured_peaks()
+    gbs = x.numel() * 4 / (ms * 1e-3) / 1e9
+    return {"value": 64 / (ms * 1e-3), "unit": "rows/s", "us_per_call": ms * 1000,
+            "config": "64 x 262,144 fp32, 5% copied entries, k=512",
+            "achieved_gbs": gbs, "frac_of_hbm": gbs / peak}
+
+
+def indexer_traffic():
+    """DRAM bytes per indexer launch from the committed ncu summary, if it was
+    taken on the current indexer source (else null)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "indexer_c4layer_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for name in ("indexer.cu", "tc.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "hybrid_sparse_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+if __name__ == "__main__":
+    main()

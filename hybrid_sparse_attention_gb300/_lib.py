@@ -217,7 +217,7 @@ class LayerDesc(ctypes.Structure):
         ("kv_new", P), ("z_new", P), ("b_kv", P), ("ik_new", P), ("iz_new", P), ("b_ik", P),
         ("swa", P), ("kv_ring", P), ("z_ring", P), ("ik_ring", P), ("iz_ring", P),
         ("kv_pool", P), ("key_pool", P), ("q", P), ("iq", P), ("w", P),
-        ("out", P), ("lse", P), ("topk_idx", P), ("scores", P),
+        ("out", P), ("lse", P), ("topk_idx", P), ("scores", P), ("stage_events", P),
     ]
 
 
@@ -226,7 +226,7 @@ SIGNATURES["hsa_layer_decode"] = (I32, [ctypes.POINTER(LayerDesc), P, SZ, P])
 
 
 def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
-               max_pool_rows=None) -> LayerDesc:
+               max_pool_rows=None, stage_events=None) -> LayerDesc:
     """Descriptor for one decode step over a synth.LayerState-like object whose
     tensors live on the GPU (argument marshalling only)."""
     sh = st.shape
@@ -268,6 +268,10 @@ def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
         d.scores = _dev(scores, torch.float32, "scores", True)
     d.out = _dev(out, out.dtype, "out")
     d.lse = _dev(lse, torch.float32, "lse", True)
+    if stage_events is not None:
+        # keep the handle array alive as long as the descriptor
+        d._events = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(h) for h in stage_events])
+        d.stage_events = ctypes.cast(d._events, ctypes.c_void_p)
     return d
 
 

@@ -186,9 +186,16 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   ap.kv_pool = static_cast<uint4*>(d.kv_pool);
   ap.key_pool = static_cast<uint4*>(d.key_pool);
   ap.status = status;
-  layer_append_kernel<<<d.B, kAppendThreads, 0, stream>>>(ap);
-  cudaError_t e = cudaGetLastError();
+  auto mark = [&](int i) -> cudaError_t {
+    return d.stage_events ? cudaEventRecord(static_cast<cudaEvent_t>(d.stage_events[i]), stream)
+                          : cudaSuccess;
+  };
+  cudaError_t e = mark(0);
   if (e != cudaSuccess) return e;
+  layer_append_kernel<<<d.B, kAppendThreads, 0, stream>>>(ap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = mark(1)) != cudaSuccess) return e;
 
   // a3-a5 read the live prefix L/r of each sequence's pool rows
   const Spans sp{d.pool_offsets, d.seq_len_out, 0, r, d.pool_total_rows};
@@ -199,10 +206,15 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
     e = launch_indexer(d.iq, d.w, d.key_pool, sp, d.B, d.Hi, d.Di, d.pool_total_rows, scores,
                        status, stream);
     if (e != cudaSuccess) return e;
+    if ((e = mark(2)) != cudaSuccess) return e;
     e = launch_topk(scores, sp, d.B, d.pool_total_rows, d.k, tidx, nullptr, w + L.topk, status,
                     stream);
     if (e != cudaSuccess) return e;
+    if ((e = mark(3)) != cudaSuccess) return e;
     idx = tidx;
+  } else {
+    if ((e = mark(2)) != cudaSuccess) return e;
+    if ((e = mark(3)) != cudaSuccess) return e;
   }
   AttnArgs a;
   a.q = d.q;
@@ -223,7 +235,9 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   a.out = d.out;
   a.out_dtype = d.out_dtype;
   a.lse = d.lse;
-  return launch_attn(a, pl, w + L.attn, status, stream);
+  e = launch_attn(a, pl, w + L.attn, status, stream);
+  if (e != cudaSuccess) return e;
+  return mark(4);
 }
 
 }  // namespace hsa

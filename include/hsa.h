@@ -244,6 +244,10 @@ typedef struct hsa_layer_desc {
   float* lse;               /* fp32 [B, Hq] or NULL */
   int32_t* topk_idx;        /* int32 [B, k] or NULL (kept in the workspace) (C4) */
   float* scores;            /* fp32 [pool_total_rows] or NULL (workspace) (C4) */
+  void* const* stage_events;  /* NULL, or 5 caller-created cudaEvent_t recorded on `stream`
+                                 before the append kernel, after it, after the indexer,
+                                 after the top-k and after the attention (C128 records
+                                 events 2 and 3 at the same point as event 1) */
 } hsa_layer_desc;
 
 size_t hsa_layer_decode_workspace_size(const hsa_layer_desc* d);
