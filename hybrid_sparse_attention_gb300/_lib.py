@@ -42,6 +42,7 @@ SIGNATURES = {
                               ctypes.c_float, P, I32, P, P, SZ, P]),
     "hsa_topk_workspace_size": (SZ, [I64, I64, I64]),
     "hsa_topk": (I32, [P, P, I64, I64, I64, P, P, P, SZ, P]),
+    "hsa_topk_noalloc": (I32, [P, P, I64, I64, I64, P, P, P]),
 }
 
 
@@ -203,6 +204,20 @@ def hsa_decode_attn(q, swa, seq_len, extra=None, extra_offsets=None, extra_idx=N
           float(scale), _dev(out, out.dtype, "out"), code, _dev(lse, torch.float32, "lse", True),
           _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
     return out, lse
+
+
+def hsa_topk_noalloc(scores, offsets, k: int, idx=None, vals=None, with_vals=True, stream=None):
+    """Top-k without a workspace (scratch in the library's static device array).
+    Output tensors are allocated here when not given; the C call allocates nothing."""
+    B = offsets.numel() - 1
+    if idx is None:
+        idx = torch.empty(B, k, dtype=torch.int32, device=scores.device)
+    if vals is None and with_vals:
+        vals = torch.empty(B, k, dtype=torch.float32, device=scores.device)
+    _call("hsa_topk_noalloc", _dev(scores, torch.float32, "scores"),
+          _dev(offsets, torch.int64, "offsets"), B, scores.numel(), k,
+          _dev(idx, torch.int32, "idx"), _dev(vals, torch.float32, "vals", True), _stream(stream))
+    return idx, vals
 
 
 class LayerDesc(ctypes.Structure):

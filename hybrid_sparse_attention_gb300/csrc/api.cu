@@ -36,6 +36,11 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 }  // namespace
 
+hsa_status_t set_error_detail(hsa_status_t s, const char* detail) {
+  snprintf(g_detail, sizeof g_detail, "%s", detail);
+  return s;
+}
+
 int device_sms() {
   static std::mutex mu;
   static int cache[64] = {0};

@@ -17,6 +17,9 @@ namespace hsa {
 
 struct Spans;
 
+// Records `detail` as this thread's hsa_last_error_detail() text; returns s.
+hsa_status_t set_error_detail(hsa_status_t s, const char* detail);
+
 // Streaming multiprocessors of the current device (cached per device).
 int device_sms();
 
@@ -33,6 +36,9 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
                            cudaStream_t stream);
 
 size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k);
+// Leading bytes of a top-k workspace (status word, row states, histograms)
+// that must be zero when a call starts.
+size_t topk_zero_prefix_bytes(int64_t B, int64_t total_rows, int64_t k);
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
                         int32_t* idx, float* vals, void* ws, uint32_t* status,
                         cudaStream_t stream);

@@ -382,6 +382,10 @@ size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k) {
   return WsLayout(B, total_rows, k).total;
 }
 
+size_t topk_zero_prefix_bytes(int64_t B, int64_t total_rows, int64_t k) {
+  return WsLayout(B, total_rows, k).win;
+}
+
 int64_t topk_chunk(int64_t total_rows) {
   int64_t want = total_rows / (4 * static_cast<int64_t>(device_sms()));
   int64_t c = 2048;

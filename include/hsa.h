@@ -143,6 +143,32 @@ hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, in
                       void* stream);
 
 /* ------------------------------------------------------------------------
+ * Allocation-free top-k.  The pages have no counterpart to this entry point;
+ * it exists for callers that own only their input and output buffers and
+ * cannot provide a workspace — code running inside a host framework whose
+ * allocator owns all device memory, or a latency-critical path that must not
+ * call cudaMalloc (which can synchronise the device).
+ *
+ * Same arguments, result and requirements as hsa_topk, without the
+ * workspace: the scratch lives in a file-scope device array of 16 MiB that
+ * every GPU which loads the library holds until the process exits.  A call
+ * whose hsa_topk_workspace_size(B, total_rows, k) exceeds 16 MiB is rejected
+ * with HSA_ERR_UNSUPPORTED before any launch (e.g. B = 64 rows fit up to
+ * about 1.9 million scores in total).  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Every call shares the one array and clears the part that
+ * must start at zero (a cudaMemsetAsync on `stream`) before its two kernel
+ * launches; calls that overlap on the same GPU (e.g. issued on different
+ * streams) race on it (each device has its own array).  Device-side status
+ * bits (NaN, bad offsets) are not reported by this entry point.
+ * ---------------------------------------------------------------------- */
+hsa_status_t hsa_topk_noalloc(const float* scores, const int64_t* offsets, int64_t B,
+                              int64_t total_rows, int64_t k, int32_t* idx, float* vals,
+                              void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused hybrid attention — [KD] §Flujo de Inferencia step 5 and the
  * technology table (FlashMLA: SWA + C4/C128 attention fused in one kernel);
  * [LH] §Tích hợp Kernel (SWA and the extra attention in one kernel call);
