@@ -216,11 +216,15 @@ def main():
                     help="seconds of oracle work for the CPU baseline (0: skip)")
     ap.add_argument("--no-topk", action="store_true",
                     help="skip the standalone top-k rows/s measurement")
+    ap.add_argument("--profile", action="store_true",
+                    help="profiling run: build the workload, run two layer steps, exit")
     args = ap.parse_args()
     world, rank, local, dist = dist_setup()
     torch.cuda.set_device(local)
     if args.impl == "reference":
         run_reference(args, world, rank, dist)
+    elif args.profile:
+        run_profile()
     else:
         run_hsa(args, world, rank, local, dist)
     if dist is not None:
@@ -396,6 +400,25 @@ def run_hsa(args, world, rank, local, dist):
         "topk_rows_per_s": topk,
     }
     print(json.dumps(line), flush=True)
+
+
+def run_profile():
+    """Two layer steps of the bench workload (the first warms up), for ncu."""
+    _lib.load(build_if_missing=True)
+    shape = synth.FULL
+    L, g = build_workload(0)
+    B = L.numel()
+    out = torch.empty(B, shape.Hq, shape.Dv, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, shape.Hq, dtype=torch.float32, device="cuda")
+    desc = _lib.layer_desc(g, out, lse, torch.empty_like(g.seq_len_in),
+                           torch.empty(B, shape.k, dtype=torch.int32, device="cuda"),
+                           torch.empty(g.kv_pool.shape[0], dtype=torch.float32, device="cuda"))
+    ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
+    for _ in range(2):
+        _lib.hsa_layer_decode(desc, ws=ws)
+    torch.cuda.synchronize()
+    assert _lib.hsa_workspace_status(ws) == 0
+    print(json.dumps({"profile": "ok", "sum_c4_entries": int((L // 4).sum())}))
 
 
 def topk_rows_per_s(flush, iters=20):
