@@ -153,6 +153,8 @@ hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys
                                 int64_t total_rows, float* scores, void* ws, size_t ws_bytes,
                                 void* stream) {
   HSA_CHECK(B >= 1 && B <= (1 << 24), HSA_ERR_INVALID_ARG, "B=%lld out of range", (long long)B);
+  HSA_CHECK(B <= 4096, HSA_ERR_UNSUPPORTED, "B=%lld above the indexer's 4096 sequences",
+            (long long)B);
   HSA_CHECK(Hi >= 1 && Hi <= 16, HSA_ERR_UNSUPPORTED, "Hi=%lld outside [1, 16]", (long long)Hi);
   HSA_CHECK(Di == 32 || Di == 64 || Di == 128, HSA_ERR_UNSUPPORTED, "Di=%lld not in {32, 64, 128}",
             (long long)Di);
@@ -269,6 +271,7 @@ static hsa_status_t check_layer(const hsa_layer_desc* d) {
                 aligned(d->pool_offsets, 8) && aligned(d->lse, 4),
             HSA_ERR_INVALID_ARG, "misaligned pointer in descriptor");
   if (d->kind == HSA_LAYER_C4) {
+    HSA_CHECK(d->B <= 4096, HSA_ERR_UNSUPPORTED, "B=%d above the indexer's 4096 sequences", d->B);
     HSA_CHECK(d->Hi >= 1 && d->Hi <= 16, HSA_ERR_UNSUPPORTED, "Hi=%d outside [1, 16]", d->Hi);
     HSA_CHECK(d->Di == 32 || d->Di == 64 || d->Di == 128, HSA_ERR_UNSUPPORTED,
               "Di=%d not in {32, 64, 128}", d->Di);

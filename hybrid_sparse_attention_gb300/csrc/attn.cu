@@ -305,19 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         }
       }
     };
-    bool ok = true;
-    for (int t = t0; t < t1; ++t) {
-      const int tt = t - t0;
-      const uint16_t** table = sh.rows[tt & 1];
+    auto build_table = [&](int t) {
+      const uint16_t** table = sh.rows[(t - t0) & 1];
       for (int r = pt_; r < kKeys; r += kProdThreads)
         table[r] = slot_row(p, b, geo, static_cast<int64_t>(t) * kKeys + r, true);
-      // table visible to all producers; also agree on giving up
-      if (tc::named_barrier_or(2, kProdThreads, !ok)) break;
+    };
+    bool ok = true;
+    build_table(t0);
+    tc::named_barrier(2, kProdThreads);
+    for (int t = t0; t < t1; ++t) {
+      const int tt = t - t0;
+      const uint16_t* const* table = sh.rows[tt & 1];
       for (int jj = 0; jj < NSL && ok; ++jj) {
         const int j = slice_order(jj, NSL, NV);
         if (tt > 0) {
           const uint32_t par = (tt - 1) & 1;
-          if (!tc::mbar_try_wait(&sh.empty[j], par)) {
+          if (!tc::mbar_test_wait(&sh.empty[j], par)) {
             retire_to(0);  // never block while holding un-signalled slices
             if (!wait_or_abort(sh, &sh.empty[j], par, p.status)) {
               ok = false;
@@ -335,6 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         ++issued;
         retire_to(kMaxInFlight);
       }
+      // the next tile's rows (index loads) overlap this tile's copies; then every
+      // slice of this tile is signalled before the producer can block again
+      if (t + 1 < t1 && ok) build_table(t + 1);
+      retire_to(0);
+      if (tc::named_barrier_or(2, kProdThreads, !ok)) break;  // table visible; agree on abort
     }
     retire_to(0);
   } else if (warp == kMmaWarp) {

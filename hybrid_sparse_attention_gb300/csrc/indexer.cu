@@ -13,10 +13,14 @@
 // of a tile in TMEM; the ReLU-weighted head sum runs in the epilogue straight
 // out of TMEM, one thread per key.  Keys and queries arrive by TMA into
 // 128-byte (Di >= 64) or 64-byte (Di = 32) swizzled shared memory, exactly
-// the K-major layout the MMA descriptors describe.  Each CTA owns one tile of
-// 128 keys of one sequence; several CTAs per SM keep enough TMA loads in
-// flight to stream the keys at HBM rate (the kernel is bound by the key
-// bytes: 2*Di bytes per entry against 4*Hi*Di flops).
+// the K-major layout the MMA descriptors describe.
+//
+// The kernel is bound by the key bytes (2*Di bytes per entry against 4*Hi*Di
+// flops), so it is built to keep HBM busy: one persistent CTA per SM walks a
+// contiguous range of 128-key tiles (tiles never straddle two sequences)
+// through a 5-stage TMA ring; warp 0 issues the loads, one lane of warp 1
+// issues the MMAs into two alternating TMEM accumulators, and warps 2-5 (one
+// TMEM lane quarter each) drain the accumulators while the next tiles load.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -28,8 +32,10 @@ namespace {
 
 constexpr int kTileRows = 128;  // M
 constexpr int kQRows = 16;      // N (heads, padded)
-constexpr int kThreads = 128;
-constexpr uint32_t kTmemCols = 32;
+constexpr int kStages = 5;
+constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kMaxSeqs = 4096;  // tile prefix table in shared memory
+constexpr uint32_t kTmemCols = 32;  // two 16-column accumulators
 
 struct IndexerParams {
   const float* w;  // [B, Hi]
@@ -39,112 +45,183 @@ struct IndexerParams {
   uint32_t* status;
 };
 
-struct TilePieces {
-  Spans sp;
-  HSA_DEVINL int64_t operator()(int b) const {
-    return (sp.count(b) + kTileRows - 1) / kTileRows;
-  }
+struct Shared {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t fin;
+  uint32_t tmem;
+  int abort;
+  int ntiles;
+  int prefix[kMaxSeqs + 1];  // tiles before sequence b
 };
 
-__global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                          const __grid_constant__ CUtensorMap qmap,
-                                                          IndexerParams p) {
+// Bounded wait that also gives up when another role has aborted.
+HSA_DEVINL bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity, uint32_t* status) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::global_timer();
+  for (uint32_t i = 0;; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u) {
+      if (*reinterpret_cast<volatile int*>(&sh.abort)) return false;
+      if (tc::global_timer() - t0 > tc::kSpinNanos || i > tc::kSpinPolls) {
+        set_status(status, HSA_DEV_TIMEOUT);
+        *reinterpret_cast<volatile int*>(&sh.abort) = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Sequence owning global tile t (largest b with prefix[b] <= t).
+HSA_DEVINL int tile_seq(const Shared& sh, int B, int t) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sh.prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                             const __grid_constant__ CUtensorMap qmap,
+                                                             IndexerParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_tma, bar_mma;
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_ok;
-  __shared__ float s_w[kQRows];
-
-  int seq;
-  int64_t piece, npieces;
-  if (!locate_piece(p.B, blockIdx.x, TilePieces{p.sp}, &seq, &piece, &npieces)) return;
-  const int64_t n = p.sp.count(seq);
-  const int64_t row_lo = p.sp.start(seq) + piece * kTileRows;
-  const int64_t left = n - piece * kTileRows;
-  const int rows = static_cast<int>(left < kTileRows ? left : kTileRows);
-
+  __shared__ Shared sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // tiles per sequence -> prefix table (block-wide scan in chunks of blockDim)
+  __shared__ int s_scan[33];
+  int carry = 0;
+  for (int base = 0; base < p.B; base += kThreads) {
+    const int b = base + threadIdx.x;
+    const int nt = b < p.B ? static_cast<int>((p.sp.count(b) + kTileRows - 1) / kTileRows) : 0;
+    int total;
+    const int incl = block_inclusive_sum<int>(nt, s_scan, &total);
+    if (b < p.B) sh.prefix[b] = carry + incl - nt;
+    carry += total;
+  }
+  if (threadIdx.x == 0) {
+    sh.prefix[p.B] = carry;
+    sh.ntiles = carry;
+  }
+  __syncthreads();
+  const int ntiles = sh.ntiles;
+  const int t_begin = static_cast<int>(static_cast<int64_t>(ntiles) * blockIdx.x / gridDim.x);
+  const int t_end = static_cast<int>(static_cast<int64_t>(ntiles) * (blockIdx.x + 1) / gridDim.x);
+  if (t_begin >= t_end) return;
+
   const int kb_elems = p.Di >= 64 ? 64 : p.Di;  // elements of one swizzle row
   const int nkb = p.Di / kb_elems;
-  const uint32_t a_kb_bytes = kTileRows * kb_elems * 2;
-  const uint32_t b_kb_bytes = kQRows * kb_elems * 2;
+  const uint32_t a_kb = kTileRows * kb_elems * 2, b_kb = kQRows * kb_elems * 2;
+  const uint32_t stage_bytes = nkb * (a_kb + b_kb);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + nkb * a_kb_bytes;
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(&bar_tma, 1);
-    tc::mbar_init(&bar_mma, 1);
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&sh.full[s], 1);
+      tc::mbar_init(&sh.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&sh.acc_full[a], 1);
+      tc::mbar_init(&sh.acc_empty[a], 128);
+    }
+    tc::mbar_init(&sh.fin, 1);
+    sh.abort = 0;
     tc::fence_mbar_init();
-    tc::tma_prefetch_map(&kmap);
-    tc::tma_prefetch_map(&qmap);
-    s_ok = 0;
   }
-  if (warp == 0) {
-    tc::tmem_alloc(&s_tmem, kTmemCols);
+  if (warp == 1) {
+    tc::tmem_alloc(&sh.tmem, kTmemCols);
     tc::tmem_relinquish();
   }
-  if (threadIdx.x < kQRows)
-    s_w[threadIdx.x] = threadIdx.x < p.Hi ? p.w[static_cast<int64_t>(seq) * p.Hi + threadIdx.x] : 0.f;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = s_tmem;
+  const uint32_t tmem = sh.tmem;
 
-  bool tma_done = true, mma_issued = false;
-  if (threadIdx.x == 0) {
-    tc::mbar_arrive_expect_tx(&bar_tma, nkb * (a_kb_bytes + b_kb_bytes));
-    for (int kb = 0; kb < nkb; ++kb) {
-      tc::tma_load_2d(sA + kb * a_kb_bytes, &kmap, kb * kb_elems, static_cast<int32_t>(row_lo),
-                      &bar_tma);
-      tc::tma_load_2d(sB + kb * b_kb_bytes, &qmap, kb * kb_elems, seq * p.Hi, &bar_tma);
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::tma_prefetch_map(&kmap);
+      tc::tma_prefetch_map(&qmap);
+      for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+        const int s = i % kStages;
+        if (i >= kStages &&
+            !wait_or_abort(sh, &sh.empty[s], ((i / kStages) & 1) ^ 1, p.status))
+          break;
+        const int b = tile_seq(sh, p.B, t);
+        const int64_t row0 = p.sp.start(b) + static_cast<int64_t>(t - sh.prefix[b]) * kTileRows;
+        uint8_t* st = smem + s * stage_bytes;
+        tc::mbar_arrive_expect_tx(&sh.full[s], stage_bytes);
+        for (int kb = 0; kb < nkb; ++kb) {
+          tc::tma_load_2d(st + kb * a_kb, &kmap, kb * kb_elems, static_cast<int32_t>(row0),
+                          &sh.full[s]);
+          tc::tma_load_2d(st + nkb * a_kb + kb * b_kb, &qmap, kb * kb_elems, b * p.Hi,
+                          &sh.full[s]);
+        }
+      }
     }
-    tma_done = tc::mbar_wait(&bar_tma, 0, p.status);
-    if (tma_done) {
-      tc::fence_after_sync();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
       const tc::Swizzle sw = kb_elems == 64 ? tc::kSwizzle128B : tc::kSwizzle64B;
       const uint32_t sbo = 8 * kb_elems * 2;  // bytes between 8-row groups
       const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, kQRows);
-      for (int kb = 0; kb < nkb; ++kb) {
-        for (int ks = 0; ks < kb_elems / 16; ++ks) {
-          const uint64_t a = tc::smem_desc(tc::smem_u32(sA + kb * a_kb_bytes + ks * 32), 16, sbo, sw);
-          const uint64_t b = tc::smem_desc(tc::smem_u32(sB + kb * b_kb_bytes + ks * 32), 16, sbo, sw);
-          tc::mma_bf16(tmem, a, b, idesc, (kb | ks) != 0);
+      for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+        const int s = i % kStages, a = i & 1;
+        if (!wait_or_abort(sh, &sh.full[s], (i / kStages) & 1, p.status)) break;
+        if (i >= 2 && !wait_or_abort(sh, &sh.acc_empty[a], ((i >> 1) & 1) ^ 1, p.status)) break;
+        tc::fence_after_sync();
+        const uint32_t sa = tc::smem_u32(smem + s * stage_bytes);
+        const uint32_t sb = sa + nkb * a_kb;
+        for (int kb = 0; kb < nkb; ++kb) {
+          for (int ks = 0; ks < kb_elems / 16; ++ks) {
+            const uint64_t da = tc::smem_desc(sa + kb * a_kb + ks * 32, 16, sbo, sw);
+            const uint64_t db = tc::smem_desc(sb + kb * b_kb + ks * 32, 16, sbo, sw);
+            tc::mma_bf16(tmem + a * kQRows, da, db, idesc, (kb | ks) != 0);
+          }
         }
+        tc::mma_commit(&sh.empty[s]);
+        tc::mma_commit(&sh.acc_full[a]);
       }
-      tc::mma_commit(&bar_mma);
-      mma_issued = true;
-      s_ok = 1;
+      tc::mma_commit(&sh.fin);  // drain before TMEM is freed
+      tc::mbar_wait(&sh.fin, 0, p.status);
     }
-  }
-  __syncthreads();
-  bool ok = s_ok != 0;
-  if (ok) ok = tc::mbar_wait(&bar_mma, 0, p.status);
-  ok = __all_sync(0xffffffffu, ok);
-  if (ok) {
-    tc::fence_after_sync();
-    uint32_t acc[16];
-    tc::tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16), acc);
-    tc::tmem_ld_wait();
-    const int r = warp * 32 + lane;
-    if (r < rows) {
-      float s = 0.f;
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+      const int a = i & 1;
+      const int b = tile_seq(sh, p.B, t);
+      const int64_t piece = t - sh.prefix[b];
+      const int64_t left = p.sp.count(b) - piece * kTileRows;
+      const int64_t row = p.sp.start(b) + piece * kTileRows + r;
+      float wv[kQRows];
 #pragma unroll
       for (int h = 0; h < kQRows; ++h)
-        if (h < p.Hi) s = fmaf(s_w[h], fmaxf(__uint_as_float(acc[h]), 0.f), s);
-      p.scores[row_lo + r] = s;
+        wv[h] = h < p.Hi ? __ldg(p.w + static_cast<int64_t>(b) * p.Hi + h) : 0.f;
+      const bool ok = wait_or_abort(sh, &sh.acc_full[a], (i >> 1) & 1, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc::fence_after_sync();
+      uint32_t acc[16];
+      tc::tmem_ld16(tmem + lane_addr + a * kQRows, acc);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&sh.acc_empty[a]);
+      if (r < left) {
+        float sc = 0.f;
+#pragma unroll
+        for (int h = 0; h < kQRows; ++h)
+          if (h < p.Hi) sc = fmaf(wv[h], fmaxf(__uint_as_float(acc[h]), 0.f), sc);
+        p.scores[row] = sc;
+      }
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // after a timeout, give in-flight copies and MMAs a second bounded chance
-    if (!tma_done) tc::mbar_wait(&bar_tma, 0, p.status);
-    if (mma_issued && !ok) tc::mbar_wait(&bar_mma, 0, p.status);
-  }
-  __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     __syncwarp();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -152,12 +229,15 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
 
 }  // namespace
 
-size_t indexer_smem_bytes(int Di) { return static_cast<size_t>(Di) * 2 * (kTileRows + kQRows) + 1024; }
+size_t indexer_smem_bytes(int Di) {
+  return static_cast<size_t>(kStages) * Di * 2 * (kTileRows + kQRows) + 1024;
+}
 
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
                            cudaStream_t stream) {
   if (total_rows == 0) return cudaSuccess;
+  if (B > kMaxSeqs) return cudaErrorInvalidValue;
   const int kb_elems = Di >= 64 ? 64 : Di;
   const CUtensorMapSwizzle sw = kb_elems == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap kmap, qmap;
@@ -169,9 +249,11 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
   e = cudaFuncSetAttribute(indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(indexer_smem_bytes(128)));
   if (e != cudaSuccess) return e;
-  const int64_t grid = (total_rows + kTileRows - 1) / kTileRows + B;
+  // persistent: one CTA per SM (fewer when there are fewer tiles)
+  const int64_t tiles_bound = (total_rows + kTileRows - 1) / kTileRows + B;
+  const int grid = static_cast<int>(tiles_bound < device_sms() ? tiles_bound : device_sms());
   IndexerParams p{w, sp, B, Hi, Di, scores, status};
-  indexer_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(kmap, qmap, p);
+  indexer_kernel<<<grid, kThreads, smem, stream>>>(kmap, qmap, p);
   return cudaGetLastError();
 }
 

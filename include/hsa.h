@@ -109,8 +109,9 @@ hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t
  * accumulators), fp32 result at the same row position as the key.
  *   iq : bf16 [B, Hi, Di]   w : fp32 [B, Hi]   keys : bf16 [total_rows, Di]
  *   offsets : int64 [B+1]   scores : fp32 [total_rows]
- * Requirements: 1 <= Hi <= 16; Di in {32, 64, 128}; iq and keys 16-byte
- * aligned.  Rows outside every sequence are not written.  One launch.
+ * Requirements: 1 <= B <= 4096; 1 <= Hi <= 16; Di in {32, 64, 128}; iq and
+ * keys 16-byte aligned.  Rows outside every sequence are not written.  One
+ * launch (persistent, one CTA per SM).
  * Workspace: hsa_indexer_scores_workspace_size() bytes (status word only).
  * ---------------------------------------------------------------------- */
 size_t hsa_indexer_scores_workspace_size(void);
