@@ -255,8 +255,8 @@ def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
     d.scale = sh.scale
     d.out_dtype = {torch.float32: HSA_F32, torch.bfloat16: HSA_BF16}[out.dtype]
     d.pool_total_rows = st.kv_pool.shape[0]
-    if max_pool_rows is None:
-        max_pool_rows = int((st.pool_offsets[1:] - st.pool_offsets[:-1]).max()) if not c4 else 0
+    if max_pool_rows is None:   # the largest pool capacity bounds every live count
+        max_pool_rows = int((st.pool_offsets[1:] - st.pool_offsets[:-1]).max())
     d.max_pool_rows = max_pool_rows
     d.seq_len_in = _dev(st.seq_len_in, torch.int32, "seq_len_in")
     d.seq_len_out = _dev(st.seq_len_in if seq_len_out is None else seq_len_out, torch.int32,

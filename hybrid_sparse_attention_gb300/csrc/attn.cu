@@ -55,7 +55,6 @@ constexpr int kThreads = 32 * 8;
 constexpr int kMaxSlices = 9;
 constexpr uint32_t kSliceBytes = kKeys * 128;
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kMaxInFlight = 6;  // cp.async groups (slices) a producer thread keeps in flight
 
 struct AttnParams {
   const uint16_t* q;      // [B, Hq, Dqk]
@@ -249,7 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   uint8_t* kbuf = smem;
   uint8_t* qs = kbuf + NSL * kSliceBytes;
   uint8_t* pt = qs + NSL * qslice;
-  const uint32_t tmem_cols_needed = 2 * kN + NMT * kN;
+  // TMEM columns: S^T of tile parity sb, partial accumulator a at (sb*4 + a)*kN;
+  // O^T M-tile m at (8 + m)*kN.
+  const uint32_t tmem_cols_needed = 8 * kN + NMT * kN;
   uint32_t tmem_cols = 32;
   while (tmem_cols < tmem_cols_needed) tmem_cols <<= 1;
 
@@ -318,15 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       const uint16_t* const* table = sh.rows[tt & 1];
       for (int jj = 0; jj < NSL && ok; ++jj) {
         const int j = slice_order(jj, NSL, NV);
-        if (tt > 0) {
-          const uint32_t par = (tt - 1) & 1;
-          if (!tc::mbar_test_wait(&sh.empty[j], par)) {
-            retire_to(0);  // never block while holding un-signalled slices
-            if (!wait_or_abort(sh, &sh.empty[j], par, p.status)) {
-              ok = false;
-              break;
-            }
-          }
+        // Buffer j is freed by the consumption of tile tt-1, whose slices were
+        // all signalled before this tile began, so blocking here while this
+        // tile's own slices are still in flight cannot stall the MMA.
+        if (tt > 0 && !wait_or_abort(sh, &sh.empty[j], (tt - 1) & 1, p.status)) {
+          ok = false;
+          break;
         }
         uint8_t* base = kbuf + j * kSliceBytes;
         for (int q = pt_; q < kKeys * 8; q += kProdThreads) {
@@ -336,7 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         }
         tc::cp_async_commit();
         ++issued;
-        retire_to(kMaxInFlight);
       }
       // the next tile's rows (index loads) overlap this tile's copies; then every
       // slice of this tile is signalled before the producer can block again
@@ -358,7 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
           break;
         }
         tc::fence_after_sync();
-        const uint32_t d_s = tmem + sb * kN;
+        // Four independent partial accumulators (by K-step within a slice) keep
+        // these small MMAs from waiting on each other's accumulation.
+        const uint32_t d_s = tmem + sb * 4 * kN;
         for (int jj = 0; jj < NSL && ok; ++jj) {
           const int j = slice_order(jj, NSL, NV);
           if (!wait_or_abort(sh, &sh.full[j], tt & 1, p.status)) {
@@ -372,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t a = tc::smem_desc(ka + ks * 32, 16, 1024, tc::kSwizzle128B);
             const uint64_t bq = tc::smem_desc(qa + ks * 32, 16, 1024, tc::kSwizzle128B);
-            tc::mma_bf16(d_s, a, bq, idS, (jj | ks) != 0);
+            tc::mma_bf16(d_s + ks * kN, a, bq, idS, jj != 0);
           }
           if (j >= NV) tc::mma_commit(&sh.empty[j]);
         }
@@ -384,19 +383,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         }
         tc::fence_after_sync();
         const uint32_t pa = tc::smem_u32(pt + sb * pbytes);
-        for (int m = 0; m < NMT; ++m) {
-          const uint32_t d_o = tmem + 2 * kN + m * kN;
-          const uint32_t va = tc::smem_u32(kbuf + 2 * m * kSliceBytes);
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
+        // M-tiles are independent accumulators: interleave them
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t bp =
+              tc::smem_desc(pa + (kk >> 2) * kN * 128 + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
+          for (int m = 0; m < NMT; ++m) {
+            const uint32_t va = tc::smem_u32(kbuf + 2 * m * kSliceBytes);
             const uint64_t a = tc::smem_desc(va + kk * 2048, kSliceBytes, 1024, tc::kSwizzle128B);
-            const uint64_t bp =
-                tc::smem_desc(pa + (kk >> 2) * kN * 128 + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
-            tc::mma_bf16(d_o, a, bp, idO, (tt > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_bf16(tmem + (8 + m) * kN, a, bp, idO, (tt > 0 || kk > 0) ? 1u : 0u);
           }
-          tc::mma_commit(&sh.empty[2 * m]);
-          tc::mma_commit(&sh.empty[2 * m + 1]);
         }
+        for (int j = 0; j < NV; ++j) tc::mma_commit(&sh.empty[j]);
         tc::mma_commit(&sh.o_done[sb]);
       }
       // drain: every MMA this thread issued has completed before TMEM is freed
@@ -420,16 +417,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       }
       tc::fence_after_sync();
       __syncwarp();
-      uint32_t raw[kN];
-      tc::tmem_ld16(tmem + lane_base + sb * kN, raw);
-      if (kN == 32) tc::tmem_ld16(tmem + lane_base + sb * kN + 16, raw + (kN == 32 ? 16 : 0));
-      tc::tmem_ld_wait();
+      float sacc[kN];
+#pragma unroll
+      for (int h = 0; h < kN; ++h) sacc[h] = 0.f;
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+#pragma unroll
+        for (int half = 0; half < kN / 16; ++half) {
+          uint32_t raw[16];
+          tc::tmem_ld16(tmem + lane_base + (sb * 4 + a) * kN + half * 16, raw);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sacc[half * 16 + i] += __uint_as_float(raw[i]);
+        }
+      }
       tc::fence_before_sync();
       tc::mbar_arrive(&sh.s_empty[sb]);
       float x[kN], mx[kN];
 #pragma unroll
       for (int h = 0; h < kN; ++h) {
-        x[h] = valid ? __uint_as_float(raw[h]) * p.scale_log2 : -INFINITY;
+        x[h] = valid ? sacc[h] * p.scale_log2 : -INFINITY;
         mx[h] = x[h];
       }
       const float mcol = warp_transpose_reduce<kN, true>(mx);
@@ -456,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
           tc::fence_after_sync();
           __syncwarp();
           for (int m = 0; m < NMT; ++m) {
-            const uint32_t col = tmem + lane_base + 2 * kN + m * kN;
+            const uint32_t col = tmem + lane_base + (8 + m) * kN;
 #pragma unroll
             for (int half = 0; half < kN / 16; ++half) {
               uint32_t o[16];
@@ -475,17 +482,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         const bool failed = !wait_or_abort(sh, &sh.o_done[sb], ((tt - 2) >> 1) & 1, p.status);
         if (tc::named_barrier_or(1, kKeys, failed)) { ok = false; break; }
       }
+      float mreg[kN];
+#pragma unroll
+      for (int h = 0; h < kN; ++h) mreg[h] = sh.m[h];
+      uint32_t pk[kN / 2];
+#pragma unroll
+      for (int h = 0; h < kN; h += 2) {
+        const float p0 = mreg[h] == -INFINITY ? 0.f : tc::ex2_approx(x[h] - mreg[h]);
+        const float p1 = mreg[h + 1] == -INFINITY ? 0.f : tc::ex2_approx(x[h + 1] - mreg[h + 1]);
+        const __nv_bfloat162 q2 = __floats2bfloat162_rn(p0, p1);
+        l_part[h] += __low2float(q2);
+        l_part[h + 1] += __high2float(q2);
+        pk[h / 2] = *reinterpret_cast<const uint32_t*>(&q2);
+      }
       uint8_t* ptb = pt + sb * pbytes + (tid >> 6) * kN * 128;
       const int kc = (tid & 63) >> 3, ke = (tid & 7) << 1;
 #pragma unroll
-      for (int h = 0; h < kN; ++h) {
-        const float mh = sh.m[h];
-        const float pv = mh == -INFINITY ? 0.f : exp2f(x[h] - mh);
-        const __nv_bfloat16 q = __float2bfloat16_rn(pv);
-        l_part[h] += __bfloat162float(q);
-        *reinterpret_cast<__nv_bfloat16*>(ptb + (h >> 3) * 1024 + (h & 7) * 128 +
-                                          ((kc ^ (h & 7)) << 4) + ke) = q;
-      }
+      for (int h = 0; h < kN; ++h)
+        *reinterpret_cast<uint16_t*>(ptb + (h >> 3) * 1024 + (h & 7) * 128 + ((kc ^ (h & 7)) << 4) +
+                                     ke) = static_cast<uint16_t>(pk[h / 2] >> ((h & 1) * 16));
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       tc::mbar_arrive(&sh.p_full);
@@ -510,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
 #pragma unroll
       for (int h = 0; h < kN; ++h) inv[h] = sh.bc[h] > 0.f ? 1.f / sh.bc[h] : 0.f;
       for (int m = 0; m < NMT; ++m) {
-        const uint32_t col = tmem + lane_base + 2 * kN + m * kN;
+        const uint32_t col = tmem + lane_base + (8 + m) * kN;
         uint32_t acc[kN];
         tc::tmem_ld16(col, acc);
         if (kN == 32) tc::tmem_ld16(col + 16, acc + (kN == 32 ? 16 : 0));
@@ -586,10 +601,12 @@ AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, in
             2 * 2 * pl.N * 128 + 1024;
   // keep co-resident CTAs within the SM's 512 TMEM columns
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(2 * pl.N + (Dv / 128) * pl.N)) cols <<= 1;
+  while (cols < static_cast<uint32_t>(8 * pl.N + (Dv / 128) * pl.N)) cols <<= 1;
+  // (at most n = 512 / cols CTAs fit the TMEM, so shared memory must keep
+  // n + 1 of them from being resident together)
   const size_t per_sm = 227 * 1024;
-  const size_t fit = per_sm / (512 / cols);
-  if (pl.smem < fit + 1) pl.smem = fit + 1;
+  const size_t floor_bytes = per_sm / (512 / cols + 1) + 1;
+  if (pl.smem < floor_bytes) pl.smem = floor_bytes;
   return pl;
 }
 

@@ -208,7 +208,7 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
     e = launch_topk(scores, sp, d.B, d.pool_total_rows, d.k, tidx, nullptr, w + L.topk, status,
-                    stream);
+                    stream, d.max_pool_rows);
     if (e != cudaSuccess) return e;
     if ((e = mark(3)) != cudaSuccess) return e;
     idx = tidx;

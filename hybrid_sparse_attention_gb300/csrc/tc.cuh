@@ -181,6 +181,14 @@ HSA_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" :
 
 // ---------------------------------------------------------------- misc
 
+// 2^x by the PTX ex2.approx instruction (relative error ~2^-22; subnormal
+// results flush to zero, -inf gives +0).
+HSA_DEVINL float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to later
 // async-proxy reads (tcgen05.mma operands, TMA stores).
 HSA_DEVINL void fence_proxy_async_smem() {

@@ -15,8 +15,14 @@
 // orders elements exactly as the result requires, so selection and the final
 // sort work on composites.
 //
-// Passes (two launches; every row is cut into chunks of CH scores, one CTA
-// per chunk, so a long row spreads over many SMs):
+// Rows of at most 32,768 scores (every C4 row up to a 128K context) take a
+// one-CTA-per-row kernel: the row is staged in shared memory, three histogram
+// passes (11, 11, 10 bits) find the exact k-th key, keys above it and the
+// lowest-index keys equal to it are compacted, and the k survivors are
+// placed by counting their ranks.  One launch, no global scratch.
+//
+// Longer rows (two launches; every row is cut into chunks of CH scores, one
+// CTA per chunk, so a long row spreads over many SMs):
 //   1. histogram: each CTA histograms the top 12 key bits of its chunk in
 //      shared memory and adds the non-zero bins into the row's global
 //      histogram.  The row's last CTA to finish (atomic ticket, no waiting)
@@ -115,6 +121,178 @@ HSA_DEVINL uint32_t warp_append(uint32_t* counter, bool take, uint32_t active) {
   return base + __popc(mask & ((1u << lane) - 1u));
 }
 
+// ---------------------------------------------------------------- short rows
+
+constexpr int kRowThreads = 1024;
+constexpr int kRowMax = 32768;   // scores staged in shared memory (128 KB)
+constexpr int kRowBins = 2048;   // 11-bit digits
+
+HSA_DEVINL uint32_t digit_count(int pass) { return pass == 2 ? 1024u : 2048u; }
+HSA_DEVINL int digit_shift(int pass) { return pass == 0 ? 21 : (pass == 1 ? 10 : 0); }
+
+// Finds digit d with (#above d) < need <= (#above d) + hist[d], scanning nb
+// bins from the top (two per thread); returns d and *above.  All threads call.
+HSA_DEVINL uint32_t find_digit(const uint32_t* hist, uint32_t nb, uint32_t need, uint32_t* above,
+                               uint32_t* s_scan, uint32_t* s_out) {
+  const uint32_t b0 = 2 * threadIdx.x, b1 = b0 + 1;  // bins counted from the top
+  const uint32_t c0 = b0 < nb ? hist[nb - 1 - b0] : 0, c1 = b1 < nb ? hist[nb - 1 - b1] : 0;
+  uint32_t total;
+  const uint32_t incl = block_inclusive_sum<uint32_t>(c0 + c1, s_scan, &total);
+  const uint32_t a0 = incl - c0 - c1, a1 = a0 + c0;
+  if (b0 < nb && a0 < need && a0 + c0 >= need) { s_out[0] = nb - 1 - b0; s_out[1] = a0; }
+  if (b1 < nb && a1 < need && a1 + c1 >= need) { s_out[0] = nb - 1 - b1; s_out[1] = a1; }
+  __syncthreads();
+  *above = s_out[1];
+  const uint32_t d = s_out[0];
+  __syncthreads();
+  return d;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 1) topk_row_kernel(const float* __restrict__ scores,
+                                                                 Spans sp, int k, int small_only,
+                                                                 uint32_t* status,
+                                                                 int32_t* __restrict__ idx_out,
+                                                                 float* __restrict__ vals_out) {
+  extern __shared__ uint32_t s_keys[];  // [kRowMax]
+  __shared__ uint32_t s_hist[kRowBins];
+  __shared__ uint64_t s_sel[kMaxK];
+  __shared__ uint32_t s_scan[33], s_out[2], s_count, s_eq_taken;
+  const int row = blockIdx.x;
+  const int64_t raw_n = sp.raw_count(row);
+  const bool valid = sp.valid(row);
+  int64_t n = valid ? raw_n : 0;
+  if (n > kRowMax) {
+    if (!small_only) return;  // a long row: the chunked kernels own it
+    if (threadIdx.x == 0) set_status(status, HSA_DEV_BOUNDS);
+    n = 0;
+  }
+  if (!valid && threadIdx.x == 0) set_status(status, HSA_DEV_BOUNDS);
+  const int64_t off = valid ? sp.start(row) : 0;
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(scores + off);
+  bool nan = false;
+  constexpr int kU = kRowMax / kRowThreads;  // every load of the row in flight at once
+  for (int i0 = threadIdx.x; i0 < n; i0 += kRowThreads * kU) {
+    uint32_t u[kU];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int i = i0 + j * kRowThreads;
+      u[j] = i < n ? __ldcg(src + i) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int i = i0 + j * kRowThreads;
+      if (i < n) {
+        nan |= is_nan_bits(u[j]);
+        s_keys[i] = order_key(u[j]);
+      }
+    }
+  }
+  if (nan) set_status(status, HSA_DEV_NAN);
+  if (threadIdx.x == 0) { s_count = 0; s_eq_taken = 0; }
+  __syncthreads();
+  const uint32_t kk = static_cast<uint32_t>(n < k ? n : k);
+  const int nn = static_cast<int>(n);
+  if (static_cast<uint32_t>(nn) <= kk) {
+    // every entry is selected
+    for (int i = threadIdx.x; i < nn; i += kRowThreads) s_sel[i] = composite(s_keys[i], i);
+  } else {
+    // exact kk-th largest key by three digit passes over the staged row
+    uint32_t prefix = 0, mask = 0, need = kk, in_bin = 0;
+    for (int pass = 0; pass < 3; ++pass) {
+      const uint32_t nb = digit_count(pass);
+      const int shift = digit_shift(pass);
+      for (uint32_t i = threadIdx.x; i < nb; i += kRowThreads) s_hist[i] = 0;
+      __syncthreads();
+      constexpr int kH = 8;
+      for (int i0 = threadIdx.x; i0 < nn; i0 += kRowThreads * kH) {
+        uint32_t key[kH];
+#pragma unroll
+        for (int j = 0; j < kH; ++j) {
+          const int i = i0 + j * kRowThreads;
+          key[j] = i < nn ? s_keys[i] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < kH; ++j)
+          if (i0 + j * kRowThreads < nn && (key[j] & mask) == prefix)
+            atomicAdd(&s_hist[(key[j] >> shift) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      uint32_t above;
+      const uint32_t d = find_digit(s_hist, nb, need, &above, s_scan, s_out);
+      in_bin = s_hist[d];
+      need -= above;
+      prefix |= d << shift;
+      mask |= (nb - 1) << shift;
+      __syncthreads();
+    }
+    const uint32_t thr = prefix;  // the kk-th largest key; take `need` of the in_bin equal keys
+    const bool all_eq = need == in_bin;
+    if (all_eq) {
+      // every key >= thr is selected: no ordering among equal keys is needed
+      constexpr int kC = 8;
+      for (int i0 = threadIdx.x; i0 < nn; i0 += kRowThreads * kC) {
+        uint32_t key[kC];
+#pragma unroll
+        for (int j = 0; j < kC; ++j) {
+          const int i = i0 + j * kRowThreads;
+          key[j] = i < nn ? s_keys[i] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < kC; ++j) {
+          const int i = i0 + j * kRowThreads;
+          if (i < nn && key[j] >= thr) {
+            const uint32_t pos = atomicAdd(&s_count, 1u);
+            if (pos < kMaxK) s_sel[pos] = composite(key[j], static_cast<uint32_t>(i));
+          }
+        }
+      }
+    }
+    for (int i0 = 0; i0 < nn && !all_eq; i0 += kRowThreads) {
+      const int i = i0 + threadIdx.x;
+      const uint32_t key = i < nn ? s_keys[i] : 0u;
+      const bool gt = i < nn && key > thr;
+      const bool eq = i < nn && key == thr;
+      bool take = gt;
+      {
+        // equal keys are taken lowest index first: index-ordered count
+        uint32_t total;
+        const uint32_t before = block_inclusive_sum<uint32_t>(eq ? 1u : 0u, s_scan, &total) -
+                                (eq ? 1u : 0u);
+        take = take || (eq && s_eq_taken + before < need);
+        __syncthreads();
+        if (threadIdx.x == 0) s_eq_taken += total;
+        __syncthreads();
+      }
+      const uint32_t pos = warp_append(&s_count, take, 0xffffffffu);
+      if (take && pos < kMaxK) s_sel[pos] = composite(key, static_cast<uint32_t>(i));
+    }
+  }
+  __syncthreads();
+  // place the kk survivors by rank (composites are unique)
+  int32_t* out_i = idx_out + static_cast<int64_t>(row) * k;
+  float* out_v = vals_out ? vals_out + static_cast<int64_t>(row) * k : nullptr;
+  for (uint32_t e = threadIdx.x; e < kk; e += kRowThreads) {
+    const uint64_t x = s_sel[e];
+    uint32_t r = 0;
+    constexpr uint32_t kR = 16;
+    uint32_t q = 0;
+    for (; q + kR <= kk; q += kR) {
+      uint32_t c = 0;
+#pragma unroll
+      for (uint32_t u = 0; u < kR; ++u) c += s_sel[q + u] > x;
+      r += c;
+    }
+    for (; q < kk; ++q) r += s_sel[q] > x;
+    const int32_t j = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(x));
+    out_i[r] = j;
+    if (out_v) out_v[r] = __uint_as_float(__ldcg(src + j));
+  }
+  for (int e = static_cast<int>(kk) + threadIdx.x; e < k; e += kRowThreads) {
+    out_i[e] = -1;
+    if (out_v) out_v[e] = -INFINITY;
+  }
+}
+
 // ---------------------------------------------------------------- pass 1
 
 __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __restrict__ scores,
@@ -131,7 +309,7 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
     return;
   }
   const int64_t n = row_count(sp, row);
-  if (n <= k) return;  // every entry is selected; no threshold needed
+  if (n <= kRowMax) return;  // short rows belong to topk_row_kernel
   for (int i = threadIdx.x; i < kBins; i += kThreads) s_hist[i] = 0;
   __syncthreads();
   const uint32_t* base = reinterpret_cast<const uint32_t*>(scores + sp.start(row));
@@ -282,6 +460,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __re
   int64_t piece, npieces;
   if (!locate_piece(B, blockIdx.x, ChunkPieces{sp, chunk}, &row, &piece, &npieces)) return;
   const int64_t n = row_count(sp, row);
+  if (n <= kRowMax) return;  // short rows belong to topk_row_kernel
   const bool all = n <= k;
   const uint32_t d = all ? 0u : __ldcg(&ws.rows[row].digit);
   const int64_t off = sp.start(row);
@@ -395,13 +574,24 @@ int64_t topk_chunk(int64_t total_rows) {
 
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
                         int32_t* idx, float* vals, void* ws, uint32_t* status,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int64_t max_row) {
+  // rows known to be short (a bound from the caller, or every row fits in the
+  // whole array) need only the one-CTA-per-row kernel
+  const bool short_only = (max_row > 0 && max_row <= kRowMax) || total_rows <= kRowMax;
+  const size_t row_smem = static_cast<size_t>(kRowMax) * 4;
+  cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(row_smem));
+  if (e != cudaSuccess) return e;
+  topk_row_kernel<<<B, kRowThreads, row_smem, stream>>>(scores, sp, k, short_only ? 1 : 0, status,
+                                                        idx, vals);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || short_only) return e;
   const int64_t chunk = topk_chunk(total_rows);
   const int64_t grid = (total_rows + chunk - 1) / chunk + B;  // upper bound on chunks
   Ws w = ws_view(ws, B, total_rows, k, status);
   topk_hist_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(scores, sp, B, k, chunk,
                                                                          w);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   topk_select_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(scores, sp, B, k, chunk,
                                                                            w, idx, vals);

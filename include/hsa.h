@@ -134,9 +134,12 @@ hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys
  *   scores : fp32 [total_rows]   offsets : int64 [B+1]
  *   idx : int32 [B, k]   vals : fp32 [B, k] or NULL
  * Requirements: 1 <= k <= 2048; B >= 1.
- * Method: radix select on order-preserving uint32 keys (histogram of the top
- * 12 bits per row, threshold digit, compaction, selection among the
- * threshold bin, sort of the k survivors).  Two kernel launches.
+ * Method: radix select on order-preserving uint32 keys.  Rows of up to
+ * 32,768 scores: one CTA per row stages the row in shared memory, finds the
+ * exact k-th key in three digit passes and places the survivors by rank.
+ * Longer rows: histogram of the top 12 bits per row across many CTAs,
+ * threshold digit, compaction, selection in the threshold bin, sort of the k
+ * survivors.  One launch when total_rows <= 32768, else three.
  * ---------------------------------------------------------------------- */
 size_t hsa_topk_workspace_size(int64_t B, int64_t total_rows, int64_t k);
 hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, int64_t total_rows,
@@ -247,7 +250,10 @@ typedef struct hsa_layer_desc {
   float scale;              /* softmax scale */
   int32_t out_dtype;        /* HSA_BF16 or HSA_F32 */
   int64_t pool_total_rows;  /* rows of kv_pool / key_pool */
-  int64_t max_pool_rows;    /* C128: bound on live pool rows per sequence */
+  int64_t max_pool_rows;    /* bound on live pool rows per sequence: required for C128
+                               (dense attention); for C4 an optional hint (0 = unknown)
+                               that lets the top-k run one CTA per row when <= 32768;
+                               a row above the bound is treated as empty and flagged */
   const int32_t* seq_len_in;    /* [B] tokens before this step */
   int32_t* seq_len_out;         /* [B] tokens after this step (may alias) */
   const int64_t* pool_offsets;  /* [B+1] capacity layout of the pools */

@@ -41,10 +41,13 @@ def test_topk_worked_example(oracle_mod):
 
 @pytest.mark.parametrize("k", [1, 64, 512, 2048])
 def test_topk_ragged_rows_with_ties(oracle_mod, k):
-    lens = [0, 1, 5, 63, 64, 65, 511, 512, 513, 2047, 4096, 5000, 20000, 40000]
+    # rows up to 32,768 take the one-CTA-per-row kernel, longer ones the chunked path
+    lens = [0, 1, 5, 63, 64, 65, 511, 512, 513, 2047, 4096, 5000, 20000, 32768, 32769, 40000]
     rows = [synth.topk_scores(SEED, 1, n, 0.05)[0] for n in lens]
-    rows.append(synth.pair_ties_at_top(rows[-1], 600))
-    rows.append(torch.round(rows[-3] * 8) / 8)            # heavy duplicates
+    rows.append(synth.pair_ties_at_top(rows[-1], 600))   # ties at the threshold, long row
+    rows.append(synth.pair_ties_at_top(rows[12], 600))   # ... and in a short row
+    rows.append(torch.round(rows[12] * 8) / 8)            # heavy duplicates, short row
+    rows.append(torch.round(rows[-4] * 8) / 8)            # heavy duplicates, long row
     vals, offs = _ragged(rows)
     _check(oracle_mod, vals, offs, k)
 
