@@ -82,8 +82,98 @@ HSA_DEVINL void compress_block(const uint4* kv, const uint4* z, const float* bia
   }
 }
 
+// Short blocks (r <= 4, the C4 layer): one thread owns one 8-channel chunk of
+// the kv row or of the indexer-key row end to end.  Every load it may need is
+// issued up front (the length, the pool offsets, the new rows, the block's
+// earlier ring rows and the biases), so the step costs one memory round trip;
+// the new row is then written to the rings and, when it completes the block,
+// the block is compressed from registers (the ring row it just wrote is the
+// block's last row).
+constexpr int kShortBlock = 4;
+
+HSA_DEVINL void append_short(const AppendParams& p, int b) {
+  const int cq = p.Dqk / 8, ci = p.kind == HSA_LAYER_C4 ? p.Di / 8 : 0;
+  const int r = p.r;
+  const int32_t lin = p.seq_len_in[b];
+  const int64_t o0 = p.pool_offsets[b], o1 = p.pool_offsets[b + 1];
+  int64_t L = 0;
+  for (int it = threadIdx.x; it < cq + ci; it += blockDim.x) {
+    const bool key = it >= cq;
+    const int c = key ? it - cq : it, n8 = key ? ci : cq, C = n8 * 8;
+    const uint4* nv_src = key ? p.ik_new : p.kv_new;
+    const uint4* nz_src = key ? p.iz_new : p.z_new;
+    uint4* ring_v = (key ? p.ik_ring : p.kv_ring) + static_cast<int64_t>(b) * r * n8 + c;
+    uint4* ring_z = (key ? p.iz_ring : p.z_ring) + static_cast<int64_t>(b) * r * n8 + c;
+    const float* bias = (key ? p.b_ik : p.b_kv) + c * 8;
+    const uint4 nv = nv_src[static_cast<int64_t>(b) * n8 + c];
+    const uint4 nz = nz_src[static_cast<int64_t>(b) * n8 + c];
+    uint4 rv[kShortBlock], rz[kShortBlock];
+    float4 b0[kShortBlock], b1[kShortBlock];
+#pragma unroll
+    for (int i = 0; i < kShortBlock; ++i) {
+      if (i < r) {
+        rv[i] = ring_v[static_cast<int64_t>(i) * n8];
+        rz[i] = ring_z[static_cast<int64_t>(i) * n8];
+        const float4* bp = reinterpret_cast<const float4*>(bias + static_cast<int64_t>(i) * C);
+        b0[i] = __ldg(bp);
+        b1[i] = __ldg(bp + 1);
+      }
+    }
+    L = static_cast<int64_t>(lin) + 1;
+    const int64_t slot = (L - 1) % r;
+    if (!key) p.swa[(static_cast<int64_t>(b) * p.W + (L - 1) % p.W) * cq + c] = nv;
+    ring_v[slot * n8] = nv;
+    ring_z[slot * n8] = nz;
+    if (L % r != 0) continue;
+    const int64_t n = L / r - 1;
+    if (o0 < 0 || o1 > p.pool_total_rows || o0 + n >= o1) {
+      set_status(p.status, HSA_DEV_BOUNDS);
+      continue;
+    }
+    float x[kShortBlock][8], v[kShortBlock][8], mx[8];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) mx[ch] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kShortBlock; ++i) {
+      if (i < r) {
+        const bool last = i == r - 1;  // the completing row is the new one (slot r-1)
+        bf16x8_to_f32(last ? nz : rz[i], x[i]);
+        bf16x8_to_f32(last ? nv : rv[i], v[i]);
+        const float bb[8] = {b0[i].x, b0[i].y, b0[i].z, b0[i].w, b1[i].x, b1[i].y, b1[i].z, b1[i].w};
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          x[i][ch] += bb[ch];  // add
+          mx[ch] = fmaxf(mx[ch], x[i][ch]);
+        }
+      }
+    }
+    float o[8];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      float l = 0.f, acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < kShortBlock; ++i) {
+        if (i < r) {
+          const float e = __expf(x[i][ch] - mx[ch]);  // softmax numerator
+          l += e;
+          acc = fmaf(e, v[i][ch], acc);  // dot
+        }
+      }
+      o[ch] = acc / l;
+    }
+    uint4* dst = key ? p.key_pool : p.kv_pool;
+    dst[(o0 + n) * n8 + c] = f32x8_to_bf16(o);
+  }
+  __syncthreads();  // every thread has read seq_len_in before it may be overwritten
+  if (threadIdx.x == 0) p.seq_len_out[b] = lin + 1;
+}
+
 __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendParams p) {
   const int b = blockIdx.x;
+  if (p.r <= kShortBlock) {
+    append_short(p, b);
+    return;
+  }
   const int64_t L = static_cast<int64_t>(p.seq_len_in[b]) + 1;
   const int cq = p.Dqk / 8, ci = p.Di / 8;
   const int64_t slot_w = (L - 1) % p.W, slot_r = (L - 1) % p.r;

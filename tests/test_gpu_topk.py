@@ -64,7 +64,11 @@ def test_topk_special_values(oracle_mod):
     mixed[1::7] = float("-inf")
     mixed[2::11] = -0.0
     tiny = torch.tensor([1e-45, -1e-45, 0.0, -0.0, 1.17549435e-38, -1.17549435e-38] * 100)
-    vals, offs = _ragged([equal, rev, zeros, infs, mixed, tiny])
+    # short rows whose threshold bin holds more than 4,096 keys (the exact
+    # three-pass fallback of the one-CTA-per-row kernel)
+    equal_big = torch.full((20000,), 1.5)
+    zeros_big = torch.where(torch.arange(32768) % 2 == 0, torch.tensor(-0.0), torch.tensor(0.0))
+    vals, offs = _ragged([equal, rev, zeros, infs, mixed, tiny, equal_big, zeros_big])
     for k in (1, 100, 512):
         _check(oracle_mod, vals, offs, k)
 
