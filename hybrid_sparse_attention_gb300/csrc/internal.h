@@ -39,8 +39,9 @@ size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k);
 // Leading bytes of a top-k workspace (status word, row states, histograms)
 // that must be zero when a call starts.
 size_t topk_zero_prefix_bytes(int64_t B, int64_t total_rows, int64_t k);
-// max_row: a bound on every row's length (0 = unknown); rows are then all
-// handled by the one-CTA-per-row kernel when it is <= 32768.
+// max_row: a bound on every row's length (0 = unknown).  When it (or
+// total_rows) is at most 32768, one clustered launch handles every row and a
+// longer row is flagged as out of bounds and treated as empty.
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
                         int32_t* idx, float* vals, void* ws, uint32_t* status,
                         cudaStream_t stream, int64_t max_row = 0);

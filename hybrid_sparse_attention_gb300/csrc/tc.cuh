@@ -93,6 +93,17 @@ HSA_DEVINL void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Bulk (untiled) copy of `bytes` contiguous bytes from global to shared
+// memory, completing on `bar` as transaction bytes.  Both addresses and the
+// size must be multiples of 16 bytes.
+HSA_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 2-D tiled load of one box into shared memory; completion is signalled on
 // `bar` as transaction bytes.  x is the innermost (contiguous) coordinate.
 HSA_DEVINL void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,

@@ -15,25 +15,24 @@
 // orders elements exactly as the result requires, so selection and the final
 // sort work on composites.
 //
-// Rows of at most 32,768 scores (every C4 row up to a 128K context) take a
-// one-CTA-per-row kernel: the row is staged in shared memory, three histogram
-// passes (11, 11, 10 bits) find the exact k-th key, keys above it and the
-// lowest-index keys equal to it are compacted, and the k survivors are
-// placed by counting their ranks.  One launch, no global scratch.
-//
-// Longer rows (two launches; every row is cut into chunks of CH scores, one
-// CTA per chunk, so a long row spreads over many SMs):
-//   1. histogram: each CTA histograms the top 12 key bits of its chunk in
-//      shared memory and adds the non-zero bins into the row's global
-//      histogram.  The row's last CTA to finish (atomic ticket, no waiting)
-//      scans the histogram from the top and records the threshold digit d*:
-//      fewer than k keys lie above bin d*, at least k at or above it.
-//   2. select: each CTA re-reads its chunk (from L2: the row was just read)
-//      and compacts keys above d* (certain winners, fewer than k) and keys in
-//      bin d* (candidates) into the workspace.  The row's last CTA then picks
-//      the k - #winners largest candidates by a radix select over the
-//      remaining 52 composite bits, bitonic-sorts the k survivors and writes
-//      indices and values.  It leaves the row's workspace zeroed.
+// Every row is cut into chunks of CH scores, one CTA per chunk, so each row
+// spreads over many SMs (two launches):
+//   1. histogram: each CTA histograms the top 11 key bits (digit 1) of its
+//      chunk in shared memory and adds the non-zero bins into the row's
+//      global histogram.  The row's last CTA to finish (atomic ticket, no
+//      waiting) scans it from the top for the threshold digit d1: fewer than
+//      k keys lie above bin d1, at least k at or above it.
+//   2. select: each CTA re-reads its chunk (from L2: it was just read) and,
+//      4,096 scores at a time, counts keys above d1 (certain winners) and in
+//      bin d1 (candidates) per warp by ballots, reserves room in the row's
+//      global lists with one atomic per list and writes its composites there.
+//      Candidates also add their next 11 key bits (digit 2) to a second row
+//      histogram.  The row's last CTA then needs no pass over the row: digit
+//      2's histogram splits the candidates into more winners and a (usually
+//      tiny) set at the boundary, a radix select over the remaining 42 bits
+//      settles those, and the k survivors are sorted (bitonic runs of 32 in
+//      each warp, merged by binary-search ranking) and written.  It leaves
+//      the row's workspace zeroed.
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,10 +40,14 @@ namespace hsa {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kBins = 4096;       // top 12 bits of the key
-constexpr int kDigitShift = 20;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 2048;       // 11-bit digits
+constexpr int kShift1 = 21;       // digit 1: key bits 31..21
+constexpr int kShift2 = 10;       // digit 2: key bits 20..10
 constexpr int kMaxK = 2048;       // final sort buffer
-constexpr int kSmemCand = 2560;   // candidates staged in shared memory when they fit
+constexpr int kSmemCand = 2560;   // boundary candidates staged in shared memory when they fit
+constexpr int kBlockU = 8;        // scores per thread per compaction block
+constexpr int kFastSort = kThreads;  // survivors ranked by warp runs + merge up to this many
 
 HSA_DEVINL uint32_t order_key(uint32_t u) {
   if (u == 0x80000000u) u = 0u;  // -0.0 == +0.0
@@ -59,29 +62,31 @@ HSA_DEVINL uint64_t composite(uint32_t key, uint32_t j) {
 
 struct RowState {
   uint32_t n_win;    // certain winners compacted so far
-  uint32_t n_cand;   // candidates (threshold bin) compacted so far
+  uint32_t n_cand;   // candidates (bin d1) compacted so far
   uint32_t done1;    // CTAs finished with pass 1
   uint32_t done2;    // CTAs finished with pass 2
-  uint32_t digit;    // threshold digit d* (pass 1 result)
+  uint32_t digit;    // threshold digit d1 (pass 1 result)
   uint32_t pad[3];
 };
 
 struct Ws {
   uint32_t* status;
-  RowState* rows;  // [B]
-  uint32_t* hist;  // [B][kBins]
-  uint64_t* win;   // [B][k]
-  uint64_t* cand;  // [total_rows], row b uses [offsets[b], offsets[b] + N_b)
+  RowState* rows;   // [B]
+  uint32_t* hist;   // [B][kBins] digit 1
+  uint32_t* hist2;  // [B][kBins] digit 2 of the candidates
+  uint64_t* win;    // [B][k]
+  uint64_t* cand;   // [total_rows], row b uses [offsets[b], offsets[b] + N_b)
 };
 
 HSA_HOST_DEVICE size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t rows, hist, win, cand, total;
+  size_t rows, hist, hist2, win, cand, total;
   HSA_HOST_DEVICE WsLayout(int64_t B, int64_t total_rows, int64_t k) {
     rows = kWsHeader;
     hist = rows + align256(sizeof(RowState) * B);
-    win = hist + align256(sizeof(uint32_t) * kBins * B);
+    hist2 = hist + align256(sizeof(uint32_t) * kBins * B);
+    win = hist2 + align256(sizeof(uint32_t) * kBins * B);
     cand = win + align256(sizeof(uint64_t) * k * B);
     total = cand + align256(sizeof(uint64_t) * (total_rows > 0 ? total_rows : 1));
   }
@@ -90,8 +95,11 @@ struct WsLayout {
 Ws ws_view(void* base, int64_t B, int64_t total_rows, int64_t k, uint32_t* status) {
   WsLayout L(B, total_rows, k);
   char* p = static_cast<char*>(base);
-  return Ws{status, reinterpret_cast<RowState*>(p + L.rows),
-            reinterpret_cast<uint32_t*>(p + L.hist), reinterpret_cast<uint64_t*>(p + L.win),
+  return Ws{status,
+            reinterpret_cast<RowState*>(p + L.rows),
+            reinterpret_cast<uint32_t*>(p + L.hist),
+            reinterpret_cast<uint32_t*>(p + L.hist2),
+            reinterpret_cast<uint64_t*>(p + L.win),
             reinterpret_cast<uint64_t*>(p + L.cand)};
 }
 
@@ -121,176 +129,36 @@ HSA_DEVINL uint32_t warp_append(uint32_t* counter, bool take, uint32_t active) {
   return base + __popc(mask & ((1u << lane) - 1u));
 }
 
-// ---------------------------------------------------------------- short rows
-
-constexpr int kRowThreads = 1024;
-constexpr int kRowMax = 32768;   // scores staged in shared memory (128 KB)
-constexpr int kRowBins = 2048;   // 11-bit digits
-
-HSA_DEVINL uint32_t digit_count(int pass) { return pass == 2 ? 1024u : 2048u; }
-HSA_DEVINL int digit_shift(int pass) { return pass == 0 ? 21 : (pass == 1 ? 10 : 0); }
-
-// Finds digit d with (#above d) < need <= (#above d) + hist[d], scanning nb
-// bins from the top (two per thread); returns d and *above.  All threads call.
+// Finds digit d with (#above d) < need <= (#above d) + hist[d] among nb <=
+// 4 * blockDim.x bins of a shared histogram, scanned from the top; returns d
+// and *above.  All threads call; returns synchronised.
 HSA_DEVINL uint32_t find_digit(const uint32_t* hist, uint32_t nb, uint32_t need, uint32_t* above,
                                uint32_t* s_scan, uint32_t* s_out) {
-  const uint32_t b0 = 2 * threadIdx.x, b1 = b0 + 1;  // bins counted from the top
-  const uint32_t c0 = b0 < nb ? hist[nb - 1 - b0] : 0, c1 = b1 < nb ? hist[nb - 1 - b1] : 0;
+  const uint32_t per = (nb + blockDim.x - 1) / blockDim.x;
+  const uint32_t first = threadIdx.x * per;  // bins counted from the top
+  uint32_t c[4], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t bb = first + i;
+    c[i] = (static_cast<uint32_t>(i) < per && bb < nb) ? hist[nb - 1 - bb] : 0u;
+    sum += c[i];
+  }
   uint32_t total;
-  const uint32_t incl = block_inclusive_sum<uint32_t>(c0 + c1, s_scan, &total);
-  const uint32_t a0 = incl - c0 - c1, a1 = a0 + c0;
-  if (b0 < nb && a0 < need && a0 + c0 >= need) { s_out[0] = nb - 1 - b0; s_out[1] = a0; }
-  if (b1 < nb && a1 < need && a1 + c1 >= need) { s_out[0] = nb - 1 - b1; s_out[1] = a1; }
+  uint32_t a = block_inclusive_sum<uint32_t>(sum, s_scan, &total) - sum;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t bb = first + i;
+    if (static_cast<uint32_t>(i) < per && bb < nb && a < need && a + c[i] >= need) {
+      s_out[0] = nb - 1 - bb;
+      s_out[1] = a;
+    }
+    a += c[i];
+  }
   __syncthreads();
   *above = s_out[1];
   const uint32_t d = s_out[0];
   __syncthreads();
   return d;
-}
-
-__global__ void __launch_bounds__(kRowThreads, 1) topk_row_kernel(const float* __restrict__ scores,
-                                                                 Spans sp, int k, int small_only,
-                                                                 uint32_t* status,
-                                                                 int32_t* __restrict__ idx_out,
-                                                                 float* __restrict__ vals_out) {
-  extern __shared__ uint32_t s_keys[];  // [kRowMax]
-  __shared__ uint32_t s_hist[kRowBins];
-  __shared__ uint64_t s_sel[kMaxK];
-  __shared__ uint32_t s_scan[33], s_out[2], s_count, s_eq_taken;
-  const int row = blockIdx.x;
-  const int64_t raw_n = sp.raw_count(row);
-  const bool valid = sp.valid(row);
-  int64_t n = valid ? raw_n : 0;
-  if (n > kRowMax) {
-    if (!small_only) return;  // a long row: the chunked kernels own it
-    if (threadIdx.x == 0) set_status(status, HSA_DEV_BOUNDS);
-    n = 0;
-  }
-  if (!valid && threadIdx.x == 0) set_status(status, HSA_DEV_BOUNDS);
-  const int64_t off = valid ? sp.start(row) : 0;
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(scores + off);
-  bool nan = false;
-  constexpr int kU = kRowMax / kRowThreads;  // every load of the row in flight at once
-  for (int i0 = threadIdx.x; i0 < n; i0 += kRowThreads * kU) {
-    uint32_t u[kU];
-#pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int i = i0 + j * kRowThreads;
-      u[j] = i < n ? __ldcg(src + i) : 0u;
-    }
-#pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int i = i0 + j * kRowThreads;
-      if (i < n) {
-        nan |= is_nan_bits(u[j]);
-        s_keys[i] = order_key(u[j]);
-      }
-    }
-  }
-  if (nan) set_status(status, HSA_DEV_NAN);
-  if (threadIdx.x == 0) { s_count = 0; s_eq_taken = 0; }
-  __syncthreads();
-  const uint32_t kk = static_cast<uint32_t>(n < k ? n : k);
-  const int nn = static_cast<int>(n);
-  if (static_cast<uint32_t>(nn) <= kk) {
-    // every entry is selected
-    for (int i = threadIdx.x; i < nn; i += kRowThreads) s_sel[i] = composite(s_keys[i], i);
-  } else {
-    // exact kk-th largest key by three digit passes over the staged row
-    uint32_t prefix = 0, mask = 0, need = kk, in_bin = 0;
-    for (int pass = 0; pass < 3; ++pass) {
-      const uint32_t nb = digit_count(pass);
-      const int shift = digit_shift(pass);
-      for (uint32_t i = threadIdx.x; i < nb; i += kRowThreads) s_hist[i] = 0;
-      __syncthreads();
-      constexpr int kH = 8;
-      for (int i0 = threadIdx.x; i0 < nn; i0 += kRowThreads * kH) {
-        uint32_t key[kH];
-#pragma unroll
-        for (int j = 0; j < kH; ++j) {
-          const int i = i0 + j * kRowThreads;
-          key[j] = i < nn ? s_keys[i] : 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < kH; ++j)
-          if (i0 + j * kRowThreads < nn && (key[j] & mask) == prefix)
-            atomicAdd(&s_hist[(key[j] >> shift) & (nb - 1)], 1u);
-      }
-      __syncthreads();
-      uint32_t above;
-      const uint32_t d = find_digit(s_hist, nb, need, &above, s_scan, s_out);
-      in_bin = s_hist[d];
-      need -= above;
-      prefix |= d << shift;
-      mask |= (nb - 1) << shift;
-      __syncthreads();
-    }
-    const uint32_t thr = prefix;  // the kk-th largest key; take `need` of the in_bin equal keys
-    const bool all_eq = need == in_bin;
-    if (all_eq) {
-      // every key >= thr is selected: no ordering among equal keys is needed
-      constexpr int kC = 8;
-      for (int i0 = threadIdx.x; i0 < nn; i0 += kRowThreads * kC) {
-        uint32_t key[kC];
-#pragma unroll
-        for (int j = 0; j < kC; ++j) {
-          const int i = i0 + j * kRowThreads;
-          key[j] = i < nn ? s_keys[i] : 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < kC; ++j) {
-          const int i = i0 + j * kRowThreads;
-          if (i < nn && key[j] >= thr) {
-            const uint32_t pos = atomicAdd(&s_count, 1u);
-            if (pos < kMaxK) s_sel[pos] = composite(key[j], static_cast<uint32_t>(i));
-          }
-        }
-      }
-    }
-    for (int i0 = 0; i0 < nn && !all_eq; i0 += kRowThreads) {
-      const int i = i0 + threadIdx.x;
-      const uint32_t key = i < nn ? s_keys[i] : 0u;
-      const bool gt = i < nn && key > thr;
-      const bool eq = i < nn && key == thr;
-      bool take = gt;
-      {
-        // equal keys are taken lowest index first: index-ordered count
-        uint32_t total;
-        const uint32_t before = block_inclusive_sum<uint32_t>(eq ? 1u : 0u, s_scan, &total) -
-                                (eq ? 1u : 0u);
-        take = take || (eq && s_eq_taken + before < need);
-        __syncthreads();
-        if (threadIdx.x == 0) s_eq_taken += total;
-        __syncthreads();
-      }
-      const uint32_t pos = warp_append(&s_count, take, 0xffffffffu);
-      if (take && pos < kMaxK) s_sel[pos] = composite(key, static_cast<uint32_t>(i));
-    }
-  }
-  __syncthreads();
-  // place the kk survivors by rank (composites are unique)
-  int32_t* out_i = idx_out + static_cast<int64_t>(row) * k;
-  float* out_v = vals_out ? vals_out + static_cast<int64_t>(row) * k : nullptr;
-  for (uint32_t e = threadIdx.x; e < kk; e += kRowThreads) {
-    const uint64_t x = s_sel[e];
-    uint32_t r = 0;
-    constexpr uint32_t kR = 16;
-    uint32_t q = 0;
-    for (; q + kR <= kk; q += kR) {
-      uint32_t c = 0;
-#pragma unroll
-      for (uint32_t u = 0; u < kR; ++u) c += s_sel[q + u] > x;
-      r += c;
-    }
-    for (; q < kk; ++q) r += s_sel[q] > x;
-    const int32_t j = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(x));
-    out_i[r] = j;
-    if (out_v) out_v[r] = __uint_as_float(__ldcg(src + j));
-  }
-  for (int e = static_cast<int>(kk) + threadIdx.x; e < k; e += kRowThreads) {
-    out_i[e] = -1;
-    if (out_v) out_v[e] = -INFINITY;
-  }
 }
 
 // ---------------------------------------------------------------- pass 1
@@ -299,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
                                                             Spans sp, int B, int k,
                                                             int64_t chunk, Ws ws) {
   __shared__ uint32_t s_hist[kBins];
-  __shared__ uint32_t s_scan[33];
+  __shared__ uint32_t s_scan[33], s_out[2];
   __shared__ int s_last;
   int row;
   int64_t piece, npieces;
@@ -309,13 +177,13 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
     return;
   }
   const int64_t n = row_count(sp, row);
-  if (n <= kRowMax) return;  // short rows belong to topk_row_kernel
+  if (n <= k) return;  // every score is selected: no threshold needed
   for (int i = threadIdx.x; i < kBins; i += kThreads) s_hist[i] = 0;
   __syncthreads();
   const uint32_t* base = reinterpret_cast<const uint32_t*>(scores + sp.start(row));
   const int64_t lo = piece * chunk, hi = min(n, lo + chunk);
   bool nan = false;
-  constexpr int kU = 8;
+  constexpr int kU = 16;  // loads in flight per thread
   for (int64_t i0 = lo + threadIdx.x; i0 < hi; i0 += kThreads * kU) {
     uint32_t u[kU];
 #pragma unroll
@@ -327,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
     for (int j = 0; j < kU; ++j) {
       if (i0 + j * kThreads < hi) {
         nan |= is_nan_bits(u[j]);
-        atomicAdd(&s_hist[order_key(u[j]) >> kDigitShift], 1u);
+        atomicAdd(&s_hist[order_key(u[j]) >> kShift1], 1u);
       }
     }
   }
@@ -336,31 +204,21 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
   uint32_t* gh = ws.hist + static_cast<int64_t>(row) * kBins;
   for (int i = threadIdx.x; i < kBins; i += kThreads)
     if (s_hist[i]) atomicAdd(gh + i, s_hist[i]);
-  // The row's last CTA finds the threshold digit.
+  // the row's last CTA finds the threshold digit
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_last = atomicAdd(&ws.rows[row].done1, 1u) == npieces - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // Thread t owns the 8 bins [kBins - 8(t+1), kBins - 8t) (scan from the top).
-  uint32_t c[8];
-  uint32_t local = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    c[j] = __ldcg(gh + kBins - 1 - (threadIdx.x * 8 + j));
-    local += c[j];
+  for (int i = threadIdx.x; i < kBins; i += kThreads) s_hist[i] = __ldcg(gh + i);
+  __syncthreads();
+  uint32_t above;
+  const uint32_t d = find_digit(s_hist, kBins, static_cast<uint32_t>(k), &above, s_scan, s_out);
+  if (threadIdx.x == 0) {
+    ws.rows[row].digit = d;
+    ws.rows[row].done1 = 0;
   }
-  uint32_t total;
-  const uint32_t incl = block_inclusive_sum<uint32_t>(local, s_scan, &total);
-  uint32_t above = incl - local;  // keys in bins above this thread's bins
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (above < static_cast<uint32_t>(k) && above + c[j] >= static_cast<uint32_t>(k))
-      ws.rows[row].digit = kBins - 1 - (threadIdx.x * 8 + j);
-    above += c[j];
-  }
-  if (threadIdx.x == 0) ws.rows[row].done1 = 0;
 }
 
 // ---------------------------------------------------------------- pass 2 helpers
@@ -385,47 +243,73 @@ HSA_DEVINL void bitonic_sort_desc(uint64_t* a, int n) {
   __syncthreads();
 }
 
-// Appends to out[*count ...] the `need` largest composites of src[0..n), all of
-// which share their top 12 bits.  Radix select over bits 51..0, 8 bits at a
-// time (4 in the last step); composites are unique, so the boundary is exact.
-HSA_DEVINL void select_largest(const uint64_t* src, uint32_t n, uint32_t need, uint64_t* out,
-                               uint32_t* count, uint32_t cap, uint32_t* s_h, uint32_t* s_scan) {
-  __shared__ uint32_t s_digit, s_above, s_in;
+// Rank of this thread's composite among the (at most kThreads) composites
+// a[0..n) when sorted descending; x receives the composite (0, below every
+// real composite, for threads past n).  Each warp sorts its 32 composites by
+// a bitonic network in registers (shuffles only); the sorted runs go to
+// shared memory and each composite's rank is the number of larger
+// composites in every run, found by a branchless binary search per run.
+// Composites are unique, so the ranks of the n real ones are 0..n-1.
+HSA_DEVINL uint32_t rank_desc(const uint64_t* a, int n, uint64_t* s_run, uint64_t* x_out) {
+  const int t = threadIdx.x, lane = t & 31;
+  uint64_t x = t < n ? a[t] : 0ull;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t y = __shfl_xor_sync(0xffffffffu, x, stride);
+      const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
+      const uint64_t hi = x > y ? x : y, lo = x > y ? y : x;
+      x = (lower == desc) ? hi : lo;
+    }
+  }
+  s_run[t] = x;
+  __syncthreads();
+  uint32_t rank = 0;
+#pragma unroll
+  for (int s = 0; s < kWarps; ++s) {
+    const uint64_t* r = s_run + 32 * s;
+    uint32_t c = 0;
+#pragma unroll
+    for (int st = 16; st >= 1; st >>= 1) c += r[c + st - 1] > x ? st : 0;
+    c += r[c] > x ? 1 : 0;
+    rank += c;
+  }
+  *x_out = x;
+  return rank;
+}
+
+// Appends to out[*count ...] the `need` largest of the composites cand[0..n),
+// which all agree above their low `low_bits` bits: radix select with 11-bit
+// digits from the top.  Composites are unique, so the boundary is exact.
+HSA_DEVINL void select_rest(const uint64_t* cand, uint32_t n, uint32_t need, uint64_t* out,
+                            uint32_t* count, uint32_t cap, uint32_t* s_hist, uint32_t* s_scan,
+                            uint32_t* s_out, int low_bits) {
   uint64_t prefix = 0, mask = 0;
-  // bits 51..0 below the 12 shared bits: six 8-bit digits, then one 4-bit digit
-  const int kShift[7] = {44, 36, 28, 20, 12, 4, 0};
-  const int kWidth[7] = {8, 8, 8, 8, 8, 8, 4};
-  for (int step = 0; step < 7 && need > 0; ++step) {
-    const int shift = kShift[step], width = kWidth[step];
+  int rest = low_bits;
+  while (need > 0 && rest > 0) {
+    const int width = rest >= 11 ? 11 : rest;
+    rest -= width;
+    const int shift = rest;
     const uint32_t nb = 1u << width;
-    for (uint32_t i = threadIdx.x; i < nb; i += blockDim.x) s_h[i] = 0;
+    for (uint32_t i = threadIdx.x; i < nb; i += blockDim.x) s_hist[i] = 0;
     __syncthreads();
     for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint64_t x = src[i];
+      const uint64_t x = cand[i];
       if ((x & mask) == prefix)
-        atomicAdd(&s_h[static_cast<uint32_t>(x >> shift) & (nb - 1)], 1u);
+        atomicAdd(&s_hist[static_cast<uint32_t>(x >> shift) & (nb - 1)], 1u);
     }
     __syncthreads();
-    // digit with (#above < need <= #above + #in); one bin per thread from the top
-    const uint32_t tbin = threadIdx.x < nb ? nb - 1 - threadIdx.x : 0;
-    const uint32_t c = threadIdx.x < nb ? s_h[tbin] : 0;
-    uint32_t total;
-    const uint32_t incl = block_inclusive_sum<uint32_t>(c, s_scan, &total);
-    if (threadIdx.x < nb && incl - c < need && incl >= need) {
-      s_digit = tbin;
-      s_above = incl - c;
-      s_in = c;
-    }
-    __syncthreads();
-    const uint32_t d = s_digit, above = s_above, in = s_in;
-    const uint64_t dmask = static_cast<uint64_t>(nb - 1) << shift;
-    const bool take_bin = (in == need - above);  // the whole bin fits
+    uint32_t above;
+    const uint32_t d = find_digit(s_hist, nb, need, &above, s_scan, s_out);
+    const uint32_t in = s_hist[d];
+    const bool take_bin = in == need - above;  // the whole bin fits
     for (uint32_t i0 = 0; i0 < n; i0 += blockDim.x) {
       const uint32_t i = i0 + threadIdx.x;
       bool take = false;
       uint64_t x = 0;
       if (i < n) {
-        x = src[i];
+        x = cand[i];
         if ((x & mask) == prefix) {
           const uint32_t dig = static_cast<uint32_t>(x >> shift) & (nb - 1);
           take = dig > d || (take_bin && dig == d);
@@ -438,9 +322,244 @@ HSA_DEVINL void select_largest(const uint64_t* src, uint32_t n, uint32_t need, u
     if (take_bin) break;
     need -= above;
     prefix |= static_cast<uint64_t>(d) << shift;
-    mask |= dmask;
+    mask |= static_cast<uint64_t>(nb - 1) << shift;
+  }
+}
+
+// ---------------------------------------------------------------- short rows: one cluster per row
+//
+// Rows of at most kClMax scores (every C4 row up to a 128K context) take one
+// launch: a thread-block cluster of kCl CTAs per row, each holding a slice of
+// kClSlice scores in registers.  The CTAs' digit-1 histograms are summed
+// through distributed shared memory (each CTA reduces a quarter of the bins
+// and broadcasts it), so every CTA finds d1 itself; each CTA then compacts
+// its keys at or above bin d1 into shared memory, CTA 0 gathers the lists,
+// finishes the selection and sorts.  No global atomics, no second launch.
+// A threshold bin too full for the shared lists (heavy ties) sends its
+// candidates through the workspace instead.
+
+constexpr int kCl = 4;                     // CTAs per row (one cluster)
+constexpr int kClU = 16;                   // scores per thread, held in registers
+constexpr int kClSlice = kThreads * kClU;  // 8,192 scores per CTA
+constexpr int kClMax = kCl * kClSlice;     // rows up to 32,768
+constexpr int kClList = 2048;              // per-CTA list of composites at or above bin d1
+static_assert(kBins == kCl * kThreads, "each CTA reduces kThreads bins, one per thread");
+
+HSA_DEVINL uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Barrier over every thread of the cluster; orders memory at cluster scope.
+HSA_DEVINL void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Address of the same shared variable in the cluster's CTA `rank`.
+HSA_DEVINL uint32_t map_rank(const void* p, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+HSA_DEVINL uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+HSA_DEVINL uint64_t ld_cluster_u64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+HSA_DEVINL void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+constexpr size_t kClDynSmem = sizeof(uint64_t) * (2 * kClList + kMaxK);
+
+__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
+    topk_cluster_kernel(const float* __restrict__ scores, Spans sp, int k, Ws ws,
+                        int32_t* __restrict__ idx_out, float* __restrict__ vals_out) {
+  __shared__ uint32_t s_hist[kBins];   // this CTA's digit-1 histogram; later select scratch
+  __shared__ uint32_t s_tot[kBins];    // the row's digit-1 histogram
+  extern __shared__ uint64_t s_dyn[];
+  uint64_t* s_loc = s_dyn;                // [kClList] this CTA's composites at or above bin d1
+  uint64_t* s_sel = s_loc + kClList;      // [kMaxK] CTA 0: winners, then every survivor
+  uint64_t* s_cand = s_sel + kMaxK;       // [kClList] CTA 0: candidates (bin d1); sort runs
+  __shared__ uint32_t s_scan[33], s_out[2], s_wt[kWarps], s_nloc, s_count, s_ccount;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  const uint32_t rank = cluster_rank();
+  const int row = static_cast<int>(blockIdx.x) / kCl;
+  const bool valid = sp.valid(row);
+  int64_t n = valid ? sp.raw_count(row) : 0;
+  if (n > kClMax) n = 0;  // longer than the caller's bound: flagged below, treated as empty
+  if (rank == 0 && t == 0 && (!valid || (valid && sp.raw_count(row) > kClMax)))
+    set_status(ws.status, HSA_DEV_BOUNDS);
+  const int64_t off = valid ? sp.start(row) : 0;
+  const uint32_t* base = reinterpret_cast<const uint32_t*>(scores + off);
+  const uint32_t kk = static_cast<uint32_t>(n < k ? n : k);
+  const bool all = n <= k;  // every score is selected
+  const int s0 = static_cast<int>(rank) * kClSlice;
+  for (int i = t; i < kBins; i += kThreads) s_hist[i] = 0;
+  if (t == 0) {
+    s_count = 0;
+    s_ccount = 0;
   }
   __syncthreads();
+  uint32_t key[kClU];
+  bool nan = false;
+#pragma unroll
+  for (int u = 0; u < kClU; ++u) {
+    const int j = s0 + u * kThreads + t;
+    const uint32_t v = j < n ? __ldcg(base + j) : 0u;
+    nan |= is_nan_bits(v);
+    key[u] = order_key(v);
+  }
+  if (nan) set_status(ws.status, HSA_DEV_NAN);
+  if (!all) {
+#pragma unroll
+    for (int u = 0; u < kClU; ++u)
+      if (s0 + u * kThreads + t < n) atomicAdd(&s_hist[key[u] >> kShift1], 1u);
+  }
+  cluster_sync();  // every CTA's histogram is complete (and every CTA is running)
+  {
+    // reduce bin `bin` over the cluster, then broadcast the sum to every CTA
+    const uint32_t bin = rank * kThreads + t;
+    uint32_t sum = 0;
+#pragma unroll
+    for (int q = 0; q < kCl; ++q) sum += ld_cluster_u32(map_rank(&s_hist[bin], q));
+#pragma unroll
+    for (int q = 0; q < kCl; ++q) st_cluster_u32(map_rank(&s_tot[bin], q), sum);
+  }
+  cluster_sync();  // s_tot holds the row's histogram in every CTA
+  uint32_t d1 = 0, above1 = 0, in1 = 0;
+  if (!all) {
+    d1 = find_digit(s_tot, kBins, kk, &above1, s_scan, s_out);
+    in1 = s_tot[d1];
+  }
+  // heavy ties: the candidates go through the workspace (the same decision in every CTA)
+  const bool heavy = !all && above1 + in1 > static_cast<uint32_t>(kClList);
+  RowState* rs = ws.rows + row;
+  {
+    // compact: ballots count per warp, one scan over warps, no atomics
+    auto taken = [&](int u) {
+      const uint32_t dig = key[u] >> kShift1;
+      return s0 + u * kThreads + t < n && (all || dig > d1 || (!heavy && dig == d1));
+    };
+    uint32_t tot = 0;
+#pragma unroll
+    for (int u = 0; u < kClU; ++u) tot += __popc(__ballot_sync(0xffffffffu, taken(u)));
+    if (lane == 0) s_wt[warp] = tot;
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t c = lane < kWarps ? s_wt[lane] : 0u;
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane < kWarps) s_wt[lane] = incl - c;
+      if (lane == 31) s_nloc = incl;
+    }
+    __syncthreads();
+    uint32_t p = s_wt[warp];
+#pragma unroll
+    for (int u = 0; u < kClU; ++u) {
+      const uint32_t m = __ballot_sync(0xffffffffu, taken(u));  // recomputed: saves registers
+      if (m >> lane & 1u) {
+        const uint32_t q = p + __popc(m & lt);
+        if (q < static_cast<uint32_t>(kClList))
+          s_loc[q] = composite(key[u], static_cast<uint32_t>(s0 + u * kThreads + t));
+      }
+      p += __popc(m);
+    }
+    if (heavy) {
+#pragma unroll
+      for (int u = 0; u < kClU; ++u) {
+        const int j = s0 + u * kThreads + t;
+        const bool c = j < n && (key[u] >> kShift1) == d1;
+        const uint32_t q = warp_append(&rs->n_cand, c, 0xffffffffu);
+        if (c) ws.cand[off + q] = composite(key[u], static_cast<uint32_t>(j));
+      }
+      __threadfence();
+    }
+  }
+  cluster_sync();  // every CTA's list is complete
+  if (rank == 0) {
+    // gather the lists: winners to s_sel, candidates to s_cand
+    for (int q = 0; q < kCl; ++q) {
+      const uint32_t nq = ld_cluster_u32(map_rank(&s_nloc, q));
+      const uint32_t nqc = nq < static_cast<uint32_t>(kClList) ? nq : kClList;
+      const uint32_t src = map_rank(&s_loc[0], q);
+      for (uint32_t i0 = 0; i0 < nqc; i0 += kThreads) {
+        const uint32_t i = i0 + t;
+        const uint64_t x = i < nqc ? ld_cluster_u64(src + 8u * i) : 0ull;
+        const uint32_t dig = static_cast<uint32_t>(x >> (32 + kShift1));
+        const bool w = i < nqc && (all || dig > d1), c = i < nqc && !all && dig == d1;
+        const uint32_t pw = warp_append(&s_count, w, 0xffffffffu);
+        if (w && pw < static_cast<uint32_t>(kMaxK)) s_sel[pw] = x;
+        const uint32_t pc = warp_append(&s_ccount, c, 0xffffffffu);
+        if (c && pc < static_cast<uint32_t>(kClList)) s_cand[pc] = x;
+      }
+    }
+  }
+  cluster_sync();  // CTA 0 has read every list: the other CTAs may leave
+  if (rank != 0) return;
+  const uint32_t n_win = s_count < kk ? s_count : kk;
+  const uint32_t need = kk - n_win;
+  if (t == 0) s_count = n_win;
+  __syncthreads();
+  if (need > 0) {
+    if (heavy) {
+      const uint32_t nc = __ldcg(&rs->n_cand);
+      select_rest(ws.cand + off, nc, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 53);
+    } else if (need >= s_ccount) {
+      const uint32_t nc = s_ccount;
+      for (uint32_t i = t; i < nc && n_win + i < kk; i += kThreads) s_sel[n_win + i] = s_cand[i];
+      __syncthreads();
+      if (t == 0) s_count = n_win + (nc < need ? nc : need);
+    } else {
+      select_rest(s_cand, s_ccount, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 53);
+    }
+  }
+  __syncthreads();
+  const uint32_t have = s_count < kk ? s_count : kk;
+  int32_t* out_i = idx_out + static_cast<int64_t>(row) * k;
+  float* out_v = vals_out ? vals_out + static_cast<int64_t>(row) * k : nullptr;
+  if (have <= static_cast<uint32_t>(kFastSort)) {
+    uint64_t x;
+    const uint32_t r = rank_desc(s_sel, static_cast<int>(have), s_cand, &x);
+    if (r < have) {
+      const uint32_t j = 0xffffffffu - static_cast<uint32_t>(x);
+      out_i[r] = static_cast<int32_t>(j);
+      if (out_v) out_v[r] = __uint_as_float(__ldcg(base + j));
+    }
+  } else {
+    int p = 1;
+    while (p < static_cast<int>(have)) p <<= 1;
+    for (int i = have + t; i < p; i += kThreads) s_sel[i] = 0;  // sorts last
+    bitonic_sort_desc(s_sel, p);
+    for (uint32_t i = t; i < have; i += kThreads) {
+      const uint32_t j = 0xffffffffu - static_cast<uint32_t>(s_sel[i]);
+      out_i[i] = static_cast<int32_t>(j);
+      if (out_v) out_v[i] = __uint_as_float(__ldcg(base + j));
+    }
+  }
+  for (int i = static_cast<int>(have) + t; i < k; i += kThreads) {
+    out_i[i] = -1;
+    if (out_v) out_v[i] = -INFINITY;
+  }
+  if (heavy && t == 0) rs->n_cand = 0;  // leave the workspace zeroed
 }
 
 // ---------------------------------------------------------------- pass 2
@@ -452,52 +571,83 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __re
                                                               float* __restrict__ vals_out) {
   __shared__ uint64_t s_sel[kMaxK];
   __shared__ uint64_t s_cand[kSmemCand];
-  __shared__ uint32_t s_h[256];
-  __shared__ uint32_t s_scan[33];
-  __shared__ uint32_t s_count;
+  __shared__ uint32_t s_hist[kBins];
+  __shared__ uint32_t s_scan[33], s_out[2];
+  __shared__ uint32_t s_wt[kWarps], s_ct[kWarps], s_gw, s_gc, s_count, s_ccount;
   __shared__ int s_last;
   int row;
   int64_t piece, npieces;
   if (!locate_piece(B, blockIdx.x, ChunkPieces{sp, chunk}, &row, &piece, &npieces)) return;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
   const int64_t n = row_count(sp, row);
-  if (n <= kRowMax) return;  // short rows belong to topk_row_kernel
   const bool all = n <= k;
-  const uint32_t d = all ? 0u : __ldcg(&ws.rows[row].digit);
+  const uint32_t d1 = all ? 0u : __ldcg(&ws.rows[row].digit);
   const int64_t off = sp.start(row);
   const uint32_t* base = reinterpret_cast<const uint32_t*>(scores + off);
   uint64_t* win = ws.win + static_cast<int64_t>(row) * k;
   uint64_t* cand = ws.cand + off;
+  uint32_t* gh2 = ws.hist2 + static_cast<int64_t>(row) * kBins;
   RowState* rs = ws.rows + row;
   const int64_t lo = piece * chunk, hi = min(n, lo + chunk);
-  constexpr int kU = 8;
-  for (int64_t i0 = lo + threadIdx.x; i0 - threadIdx.x < hi; i0 += kThreads * kU) {
-    uint32_t u[kU];
+  for (int64_t b0 = lo; b0 < hi; b0 += kThreads * kBlockU) {
+    // one block of kThreads * kBlockU scores: classify, count per warp
+    uint32_t key[kBlockU], mw[kBlockU], mc[kBlockU];
 #pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int64_t i = i0 + j * kThreads;
-      u[j] = i < hi ? __ldcg(base + i) : 0u;
+    for (int j = 0; j < kBlockU; ++j) {
+      const int64_t i = b0 + j * kThreads + t;
+      key[j] = i < hi ? order_key(__ldcg(base + i)) : 0u;
     }
+    uint32_t tw = 0, tc = 0;
 #pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int64_t i = i0 + j * kThreads;
-      bool w = false, c = false;
-      uint64_t x = 0;
-      if (i < hi) {
-        const uint32_t key = order_key(u[j]);
-        const uint32_t dig = key >> kDigitShift;
-        w = all || dig > d;
-        c = !all && dig == d;
-        x = composite(key, static_cast<uint32_t>(i));
+    for (int j = 0; j < kBlockU; ++j) {
+      const bool in = b0 + j * kThreads + t < hi;
+      const uint32_t dig = key[j] >> kShift1;
+      mw[j] = __ballot_sync(0xffffffffu, in && (all || dig > d1));
+      mc[j] = __ballot_sync(0xffffffffu, in && !all && dig == d1);
+      tw += __popc(mw[j]);
+      tc += __popc(mc[j]);
+    }
+    if (lane == 0) {
+      s_wt[warp] = tw;
+      s_ct[warp] = tc;
+    }
+    __syncthreads();
+    if (t == 0) {
+      // exclusive prefix over warps, then one reservation per list
+      uint32_t sw = 0, sc = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        const uint32_t a = s_wt[w], c = s_ct[w];
+        s_wt[w] = sw;
+        s_ct[w] = sc;
+        sw += a;
+        sc += c;
       }
-      const uint32_t pw = warp_append(&rs->n_win, w, 0xffffffffu);
-      if (w && pw < static_cast<uint32_t>(k)) win[pw] = x;
-      const uint32_t pc = warp_append(&rs->n_cand, c, 0xffffffffu);
-      if (c) cand[pc] = x;
+      s_gw = sw ? atomicAdd(&rs->n_win, sw) : 0u;
+      s_gc = sc ? atomicAdd(&rs->n_cand, sc) : 0u;
     }
+    __syncthreads();
+    uint32_t pw = s_gw + s_wt[warp], pc = s_gc + s_ct[warp];
+#pragma unroll
+    for (int j = 0; j < kBlockU; ++j) {
+      const uint32_t i = static_cast<uint32_t>(b0 - lo) + j * kThreads + t;  // < chunk
+      const uint64_t x = composite(key[j], static_cast<uint32_t>(lo) + i);
+      if (mw[j] >> lane & 1u) {
+        const uint32_t p = pw + __popc(mw[j] & lt);
+        if (p < static_cast<uint32_t>(k)) win[p] = x;
+      }
+      if (mc[j] >> lane & 1u) {
+        cand[pc + __popc(mc[j] & lt)] = x;
+        atomicAdd(gh2 + ((key[j] >> kShift2) & (kBins - 1)), 1u);
+      }
+      pw += __popc(mw[j]);
+      pc += __popc(mc[j]);
+    }
+    __syncthreads();  // s_wt / s_ct are rewritten by the next block
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&rs->done2, 1u) == npieces - 1;
+  if (t == 0) s_last = atomicAdd(&rs->done2, 1u) == npieces - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -507,47 +657,86 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __re
   const uint32_t n_win = __ldcg(&rs->n_win);
   const uint32_t n_cand = __ldcg(&rs->n_cand);
   const uint32_t n_win_c = n_win < kk ? n_win : kk;  // defensive clamp
-  for (uint32_t i = threadIdx.x; i < n_win_c; i += kThreads) s_sel[i] = __ldcg(win + i);
-  if (threadIdx.x == 0) s_count = n_win_c;
+  for (uint32_t i = t; i < n_win_c; i += kThreads) s_sel[i] = __ldcg(win + i);
+  if (t == 0) {
+    s_count = n_win_c;
+    s_ccount = 0;
+  }
   __syncthreads();
   const uint32_t need = kk - n_win_c;
-  if (need > 0) {
-    if (need >= n_cand) {
-      for (uint32_t i = threadIdx.x; i < n_cand && n_win_c + i < kk; i += kThreads)
-        s_sel[n_win_c + i] = __ldcg(cand + i);
+  if (need > 0 && need >= n_cand) {
+    for (uint32_t i = t; i < n_cand && n_win_c + i < kk; i += kThreads)
+      s_sel[n_win_c + i] = __ldcg(cand + i);
+    __syncthreads();
+    if (t == 0) s_count = n_win_c + (n_cand < need ? n_cand : need);
+  } else if (need > 0) {
+    // digit 2 of the candidates: bins above d2 are winners, bin d2 the boundary
+    for (int i = t; i < kBins; i += kThreads) s_hist[i] = __ldcg(gh2 + i);
+    __syncthreads();
+    uint32_t above2;
+    const uint32_t d2 = find_digit(s_hist, kBins, need, &above2, s_scan, s_out);
+    const uint32_t in2 = s_hist[d2];
+    if (in2 <= kSmemCand) {
+      for (uint32_t i0 = 0; i0 < n_cand; i0 += kThreads) {
+        const uint32_t i = i0 + t;
+        const uint64_t x = i < n_cand ? __ldcg(cand + i) : 0ull;
+        const uint32_t dig = static_cast<uint32_t>(x >> (32 + kShift2)) & (kBins - 1);
+        const bool w = i < n_cand && dig > d2, c = i < n_cand && dig == d2;
+        const uint32_t p = warp_append(&s_count, w, 0xffffffffu);
+        if (w && p < kMaxK) s_sel[p] = x;
+        const uint32_t q = warp_append(&s_ccount, c, 0xffffffffu);
+        if (c && q < kSmemCand) s_cand[q] = x;
+      }
       __syncthreads();
-      if (threadIdx.x == 0) s_count = n_win_c + (n_cand < need ? n_cand : need);
-      __syncthreads();
-    } else if (n_cand <= kSmemCand) {
-      for (uint32_t i = threadIdx.x; i < n_cand; i += kThreads) s_cand[i] = __ldcg(cand + i);
-      __syncthreads();
-      select_largest(s_cand, n_cand, need, s_sel, &s_count, kk, s_h, s_scan);
+      const uint32_t need2 = need - above2;  // >= 1, <= in2
+      if (need2 == in2) {
+        for (uint32_t i = t; i < in2; i += kThreads) s_sel[n_win_c + above2 + i] = s_cand[i];
+        __syncthreads();
+        if (t == 0) s_count = n_win_c + above2 + in2;
+      } else {
+        select_rest(s_cand, in2, need2, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 42);
+      }
     } else {
-      select_largest(cand, n_cand, need, s_sel, &s_count, kk, s_h, s_scan);
+      // heavy ties: select over every candidate's low 53 composite bits
+      select_rest(cand, n_cand, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 53);
     }
   }
   __syncthreads();
   const uint32_t have = s_count < kk ? s_count : kk;
-  int p = 1;
-  while (p < static_cast<int>(have)) p <<= 1;
-  for (int i = have + threadIdx.x; i < p; i += kThreads) s_sel[i] = 0;  // sorts last
-  bitonic_sort_desc(s_sel, p);
-  for (int i = threadIdx.x; i < k; i += kThreads) {
-    int32_t j = -1;
-    float v = -INFINITY;
-    if (static_cast<uint32_t>(i) < have) {
-      j = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(s_sel[i]));
-      v = __uint_as_float(__ldcg(base + j));
+  int32_t* out_i = idx_out + static_cast<int64_t>(row) * k;
+  float* out_v = vals_out ? vals_out + static_cast<int64_t>(row) * k : nullptr;
+  if (have <= static_cast<uint32_t>(kFastSort)) {
+    uint64_t x;
+    const uint32_t r = rank_desc(s_sel, static_cast<int>(have), s_cand, &x);
+    if (r < have) {
+      const uint32_t j = 0xffffffffu - static_cast<uint32_t>(x);
+      out_i[r] = static_cast<int32_t>(j);
+      if (out_v) out_v[r] = __uint_as_float(__ldcg(base + j));
     }
-    idx_out[static_cast<int64_t>(row) * k + i] = j;
-    if (vals_out) vals_out[static_cast<int64_t>(row) * k + i] = v;
+  } else {
+    int p = 1;
+    while (p < static_cast<int>(have)) p <<= 1;
+    for (int i = have + t; i < p; i += kThreads) s_sel[i] = 0;  // sorts last
+    bitonic_sort_desc(s_sel, p);
+    for (uint32_t i = t; i < have; i += kThreads) {
+      const uint32_t j = 0xffffffffu - static_cast<uint32_t>(s_sel[i]);
+      out_i[i] = static_cast<int32_t>(j);
+      if (out_v) out_v[i] = __uint_as_float(__ldcg(base + j));
+    }
+  }
+  for (int i = static_cast<int>(have) + t; i < k; i += kThreads) {
+    out_i[i] = -1;
+    if (out_v) out_v[i] = -INFINITY;
   }
   // leave the row's workspace zeroed for the next call
   if (!all) {
     uint32_t* gh = ws.hist + static_cast<int64_t>(row) * kBins;
-    for (int i = threadIdx.x; i < kBins; i += kThreads) gh[i] = 0;
+    for (int i = t; i < kBins; i += kThreads) {
+      gh[i] = 0;
+      gh2[i] = 0;
+    }
   }
-  if (threadIdx.x == 0) {
+  if (t == 0) {
     rs->n_win = 0;
     rs->n_cand = 0;
     rs->done2 = 0;
@@ -566,8 +755,8 @@ size_t topk_zero_prefix_bytes(int64_t B, int64_t total_rows, int64_t k) {
 }
 
 int64_t topk_chunk(int64_t total_rows) {
-  int64_t want = total_rows / (4 * static_cast<int64_t>(device_sms()));
-  int64_t c = 2048;
+  int64_t want = total_rows / (2 * static_cast<int64_t>(device_sms()));
+  int64_t c = kThreads * kBlockU;
   while (c * 2 <= want && c < 65536) c *= 2;
   return c;
 }
@@ -575,23 +764,22 @@ int64_t topk_chunk(int64_t total_rows) {
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
                         int32_t* idx, float* vals, void* ws, uint32_t* status,
                         cudaStream_t stream, int64_t max_row) {
-  // rows known to be short (a bound from the caller, or every row fits in the
-  // whole array) need only the one-CTA-per-row kernel
-  const bool short_only = (max_row > 0 && max_row <= kRowMax) || total_rows <= kRowMax;
-  const size_t row_smem = static_cast<size_t>(kRowMax) * 4;
-  cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(row_smem));
-  if (e != cudaSuccess) return e;
-  topk_row_kernel<<<B, kRowThreads, row_smem, stream>>>(scores, sp, k, short_only ? 1 : 0, status,
-                                                        idx, vals);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || short_only) return e;
+  Ws w = ws_view(ws, B, total_rows, k, status);
+  if ((max_row > 0 && max_row <= kClMax) || total_rows <= kClMax) {
+    // every row fits one cluster: a single launch
+    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kClDynSmem));
+    if (e != cudaSuccess) return e;
+    topk_cluster_kernel<<<static_cast<unsigned>(B) * kCl, kThreads, kClDynSmem, stream>>>(
+        scores, sp, k, w, idx, vals);
+    return cudaGetLastError();
+  }
   const int64_t chunk = topk_chunk(total_rows);
   const int64_t grid = (total_rows + chunk - 1) / chunk + B;  // upper bound on chunks
-  Ws w = ws_view(ws, B, total_rows, k, status);
   topk_hist_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(scores, sp, B, k, chunk,
                                                                          w);
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   topk_select_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(scores, sp, B, k, chunk,
                                                                            w, idx, vals);

@@ -134,12 +134,16 @@ hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys
  *   scores : fp32 [total_rows]   offsets : int64 [B+1]
  *   idx : int32 [B, k]   vals : fp32 [B, k] or NULL
  * Requirements: 1 <= k <= 2048; B >= 1.
- * Method: radix select on order-preserving uint32 keys.  Rows of up to
- * 32,768 scores: one CTA per row stages the row in shared memory, finds the
- * exact k-th key in three digit passes and places the survivors by rank.
- * Longer rows: histogram of the top 12 bits per row across many CTAs,
- * threshold digit, compaction, selection in the threshold bin, sort of the k
- * survivors.  One launch when total_rows <= 32768, else three.
+ * Method: radix select on order-preserving uint32 keys.  When total_rows <=
+ * 32768, one launch: a cluster of four CTAs per row holds the row in
+ * registers, sums its histogram of the top 11 key bits through distributed
+ * shared memory, compacts the keys at or above the threshold bin, and CTA 0
+ * settles the boundary and sorts.  Otherwise two launches, every row cut into
+ * chunks handled by separate CTAs: launch 1 histograms the top 11 key bits
+ * per row and finds the threshold bin; launch 2 compacts the keys above it
+ * (winners) and in it (candidates, with a histogram of their next 11 bits),
+ * and each row's last CTA settles the boundary by a radix select over the
+ * few remaining candidates, sorts the k survivors and writes them.
  * ---------------------------------------------------------------------- */
 size_t hsa_topk_workspace_size(int64_t B, int64_t total_rows, int64_t k);
 hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, int64_t total_rows,
@@ -252,8 +256,9 @@ typedef struct hsa_layer_desc {
   int64_t pool_total_rows;  /* rows of kv_pool / key_pool */
   int64_t max_pool_rows;    /* bound on live pool rows per sequence: required for C128
                                (dense attention); for C4 an optional hint (0 = unknown)
-                               that lets the top-k run one CTA per row when <= 32768;
-                               a row above the bound is treated as empty and flagged */
+                               that lets the top-k finish in one clustered launch when
+                               <= 32768; a row above the bound is flagged and treated
+                               as empty */
   const int32_t* seq_len_in;    /* [B] tokens before this step */
   int32_t* seq_len_out;         /* [B] tokens after this step (may alias) */
   const int64_t* pool_offsets;  /* [B+1] capacity layout of the pools */

@@ -41,7 +41,7 @@ def test_topk_worked_example(oracle_mod):
 
 @pytest.mark.parametrize("k", [1, 64, 512, 2048])
 def test_topk_ragged_rows_with_ties(oracle_mod, k):
-    # rows up to 32,768 take the one-CTA-per-row kernel, longer ones the chunked path
+    # ragged lengths across one and many 4,096-score compaction blocks and chunks
     lens = [0, 1, 5, 63, 64, 65, 511, 512, 513, 2047, 4096, 5000, 20000, 32768, 32769, 40000]
     rows = [synth.topk_scores(SEED, 1, n, 0.05)[0] for n in lens]
     rows.append(synth.pair_ties_at_top(rows[-1], 600))   # ties at the threshold, long row
@@ -64,13 +64,42 @@ def test_topk_special_values(oracle_mod):
     mixed[1::7] = float("-inf")
     mixed[2::11] = -0.0
     tiny = torch.tensor([1e-45, -1e-45, 0.0, -0.0, 1.17549435e-38, -1.17549435e-38] * 100)
-    # short rows whose threshold bin holds more than 4,096 keys (the exact
-    # three-pass fallback of the one-CTA-per-row kernel)
+    # rows whose boundary bin after two digits holds more candidates than the
+    # final CTA stages in shared memory (selection over the global candidates)
     equal_big = torch.full((20000,), 1.5)
     zeros_big = torch.where(torch.arange(32768) % 2 == 0, torch.tensor(-0.0), torch.tensor(0.0))
     vals, offs = _ragged([equal, rev, zeros, infs, mixed, tiny, equal_big, zeros_big])
     for k in (1, 100, 512):
         _check(oracle_mod, vals, offs, k)
+
+
+@pytest.mark.parametrize("k", [1, 64, 512, 2048])
+def test_topk_single_launch_rows(oracle_mod, k):
+    """At most 32,768 scores in all: one clustered launch (a row spans up to
+    four CTAs of 8,192 scores); ragged rows across the CTA slices, ties."""
+    lens = [0, 1, 5, 511, 512, 513, 2047, 4095, 8191, 8193]
+    rows = [synth.topk_scores(SEED, 1, n, 0.05)[0] for n in lens]
+    rows.append(synth.pair_ties_at_top(rows[6], 600))
+    rows.append(torch.round(rows[6] * 8) / 8)
+    vals, offs = _ragged(rows)
+    assert vals.numel() <= 32768
+    _check(oracle_mod, vals, offs, k)
+
+
+def test_topk_single_launch_full_row_and_heavy_ties(oracle_mod):
+    """One row of exactly 32,768 (all four CTA slices full); then rows whose
+    threshold bin outgrows the shared lists (candidates through the workspace)."""
+    x = synth.pair_ties_at_top(synth.topk_scores(SEED, 1, 32768, 0.05)[0], 600)
+    vals, offs = _ragged([x])
+    for k in (512, 2048):
+        _check(oracle_mod, vals, offs, k)
+    equal = torch.full((20000,), 1.5)
+    zeros = torch.where(torch.arange(12000) % 2 == 0, torch.tensor(-0.0), torch.tensor(0.0))
+    vals, offs = _ragged([equal, zeros])
+    ws = _lib.workspace(_lib.hsa_topk_workspace_size(2, vals.numel(), 512))
+    for k in (1, 100, 512):
+        for _ in range(2):     # the workspace is left reusable
+            _check(oracle_mod, vals, offs, k, ws=ws)
 
 
 def test_topk_same_workspace_reused(oracle_mod):
