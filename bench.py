@@ -283,14 +283,18 @@ def run_hsa(args, world, rank, local, dist):
     stage = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     for e in stage:
         e.record(stream)          # the events exist from here on
-    desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores,
-                           stage_events=[e.cuda_event for e in stage])
+    # the timed steps run without stage events: an event recorded between two
+    # kernels stops the next one from being scheduled while the previous runs
+    desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores)
+    desc_stages = _lib.layer_desc(g, out, lse, seq_out, idx, scores,
+                                  stage_events=[e.cuda_event for e in stage])
     ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
+    launches = _lib.hsa_layer_decode_launches(desc)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     nbytes = layer_bytes(L, shape)
 
-    def step():
-        _lib.hsa_layer_decode(desc, ws=ws)
+    def step(d=desc):
+        _lib.hsa_layer_decode(d, ws=ws)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -299,10 +303,8 @@ def run_hsa(args, world, rank, local, dist):
     assert _lib.hsa_workspace_status(ws) == 0
 
     # ------------------------------------------------ device-timed region
-    t_layer, t_stage = [], [[] for _ in range(4)]
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stage_ms = []
     barrier(dist)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
@@ -312,12 +314,17 @@ def run_hsa(args, world, rank, local, dist):
             ev0[i].record(stream)
             step()
             ev1[i].record(stream)
-            ev1[i].synchronize()                # stage events are reused: read them now
-            stage_ms.append([stage[j].elapsed_time(stage[j + 1]) for j in range(4)])
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     barrier(dist)
     t_layer = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    # per-kernel durations: the same steps again with an event between kernels
+    stage_ms = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        step(desc_stages)
+        stage[4].synchronize()                  # stage events are reused: read them now
+        stage_ms.append([stage[j].elapsed_time(stage[j + 1]) for j in range(4)])
     ms = statistics.mean(t_layer)
     ms_max = max_over_ranks(ms, dist)
     st = np.array(stage_ms)
@@ -394,7 +401,7 @@ def run_hsa(args, world, rank, local, dist):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e * 1000 / world, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed": wall,
         "topk_rows_per_s": topk,

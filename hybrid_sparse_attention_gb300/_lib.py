@@ -237,6 +237,7 @@ class LayerDesc(ctypes.Structure):
 
 
 SIGNATURES["hsa_layer_decode_workspace_size"] = (SZ, [ctypes.POINTER(LayerDesc)])
+SIGNATURES["hsa_layer_decode_launches"] = (I32, [ctypes.POINTER(LayerDesc)])
 SIGNATURES["hsa_layer_decode"] = (I32, [ctypes.POINTER(LayerDesc), P, SZ, P])
 
 
@@ -292,6 +293,11 @@ def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
 
 def hsa_layer_decode_workspace_size(desc: LayerDesc) -> int:
     return int(load().hsa_layer_decode_workspace_size(ctypes.byref(desc)))
+
+
+def hsa_layer_decode_launches(desc: LayerDesc) -> int:
+    """Kernel launches one hsa_layer_decode call with this descriptor makes."""
+    return int(load().hsa_layer_decode_launches(ctypes.byref(desc)))
 
 
 def hsa_layer_decode(desc: LayerDesc, ws=None, stream=None):

@@ -296,6 +296,11 @@ size_t hsa_layer_decode_workspace_size(const hsa_layer_desc* d) {
   return layer_workspace_bytes(*d);
 }
 
+int32_t hsa_layer_decode_launches(const hsa_layer_desc* d) {
+  if (check_layer(d) != HSA_OK) return 0;
+  return layer_launch_count(*d);
+}
+
 hsa_status_t hsa_layer_decode(const hsa_layer_desc* d, void* ws, size_t ws_bytes, void* stream) {
   hsa_status_t st = check_layer(d);
   if (st != HSA_OK) return st;

@@ -217,6 +217,8 @@ template <int kN>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x % p.G;
   const int s = (blockIdx.x / p.G) % p.S;
@@ -555,6 +557,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
                                                           const float* __restrict__ plse, int S,
                                                           int Hq, int Dv, void* out, int out_dtype,
                                                           float* lse) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x / Hq, h = blockIdx.x % Hq;
   const float* ls = plse + static_cast<int64_t>(b) * S * Hq + h;
   float mx = -INFINITY;
@@ -620,7 +624,7 @@ size_t attn_workspace_bytes(const AttnPlan& pl, int64_t B, int64_t Hq, int64_t D
 }
 
 cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_t* status,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool pdl) {
   AttnParams p;
   p.q = static_cast<const uint16_t*>(a.q);
   p.swa = static_cast<const uint16_t*>(a.swa);
@@ -650,23 +654,15 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.plse = reinterpret_cast<float*>(
       w + ((static_cast<size_t>(a.B) * pl.S * a.Hq * a.Dv * 4 + 255) & ~size_t(255)));
   const unsigned grid = static_cast<unsigned>(a.B * pl.G * pl.S);
-  cudaError_t e;
-  if (pl.N == 16) {
-    e = cudaFuncSetAttribute(attn_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(pl.smem));
-    if (e != cudaSuccess) return e;
-    attn_kernel<16><<<grid, kThreads, pl.smem, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(attn_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(pl.smem));
-    if (e != cudaSuccess) return e;
-    attn_kernel<32><<<grid, kThreads, pl.smem, stream>>>(p);
-  }
-  e = cudaGetLastError();
+  auto* kernel = pl.N == 16 ? attn_kernel<16> : attn_kernel<32>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(pl.smem));
+  if (e != cudaSuccess) return e;
+  e = launch_k(kernel, dim3(grid), dim3(kThreads), pl.smem, stream, pdl, p);
   if (e != cudaSuccess || pl.S == 1) return e;
-  attn_combine_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, stream>>>(
-      p.po, p.plse, pl.S, p.Hq, p.Dv, a.out, a.out_dtype, a.lse);
-  return cudaGetLastError();
+  return launch_k(attn_combine_kernel, dim3(static_cast<unsigned>(a.B * a.Hq)), dim3(128), 0, stream,
+                  true, static_cast<const float*>(p.po), static_cast<const float*>(p.plse), pl.S,
+                  p.Hq, p.Dv, a.out, a.out_dtype, a.lse);
 }
 
 }  // namespace hsa

@@ -18,6 +18,15 @@ HSA_DEVINL void set_status(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);
 }
 
+// Programmatic dependent launch.  pdl_trigger lets the next kernel of the
+// stream be scheduled before this one ends; pdl_wait blocks until the previous
+// kernel has completed and its writes are visible (a no-op when this kernel
+// was launched without the programmatic-serialization attribute).  Every
+// kernel calls both first thing, so a chain of launches overlaps only its
+// launch latency and never reads a predecessor's output early.
+HSA_DEVINL void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+HSA_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Unpack 8 bf16 (one 16-byte chunk) to fp32.
 HSA_DEVINL void bf16x8_to_f32(const uint4& v, float f[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -96,7 +105,7 @@ size_t attn_workspace_bytes(const AttnPlan& pl, int64_t B, int64_t Hq, int64_t D
 // ws: attn_workspace_bytes() of scratch (partials after a kWsHeader gap);
 // status: the sticky status word to report into.
 cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_t* status,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool pdl = false);
 
 // Block-wide inclusive sum over one value per thread (blockDim.x <= 1024).
 // `scratch` holds 33 elements of shared memory.  Returns the inclusive prefix;

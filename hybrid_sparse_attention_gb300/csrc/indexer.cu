@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
 
   // tiles per sequence -> prefix table (block-wide scan in chunks of blockDim)
   __shared__ int s_scan[33];
@@ -235,7 +237,7 @@ size_t indexer_smem_bytes(int Di) {
 
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool pdl) {
   if (total_rows == 0) return cudaSuccess;
   if (B > kMaxSeqs) return cudaErrorInvalidValue;
   const int kb_elems = Di >= 64 ? 64 : Di;
@@ -253,8 +255,7 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
   const int64_t tiles_bound = (total_rows + kTileRows - 1) / kTileRows + B;
   const int grid = static_cast<int>(tiles_bound < device_sms() ? tiles_bound : device_sms());
   IndexerParams p{w, sp, B, Hi, Di, scores, status};
-  indexer_kernel<<<grid, kThreads, smem, stream>>>(kmap, qmap, p);
-  return cudaGetLastError();
+  return launch_k(indexer_kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, kmap, qmap, p);
 }
 
 }  // namespace hsa

@@ -23,6 +23,24 @@ hsa_status_t set_error_detail(hsa_status_t s, const char* detail);
 // Streaming multiprocessors of the current device (cached per device).
 int device_sms();
 
+// Kernel launch; with pdl, the kernel may be scheduled while the previous
+// kernel of the stream is still running (it waits for it in pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,
                             int64_t C, int64_t r, void* out, int out_dtype, cudaStream_t stream);
 
@@ -33,7 +51,7 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner,
 size_t indexer_smem_bytes(int Di);
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool pdl = false);
 
 size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k);
 // Leading bytes of a top-k workspace (status word, row states, histograms)
@@ -44,9 +62,12 @@ size_t topk_zero_prefix_bytes(int64_t B, int64_t total_rows, int64_t k);
 // longer row is flagged as out of bounds and treated as empty.
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
                         int32_t* idx, float* vals, void* ws, uint32_t* status,
-                        cudaStream_t stream, int64_t max_row = 0);
+                        cudaStream_t stream, int64_t max_row = 0, bool pdl = false);
 
 size_t layer_workspace_bytes(const hsa_layer_desc& d);
+int layer_launch_count(const hsa_layer_desc& d);
+// Kernel launches launch_topk makes for these arguments.
+int topk_launch_count(int64_t total_rows, int64_t max_row);
 cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream);
 
 }  // namespace hsa

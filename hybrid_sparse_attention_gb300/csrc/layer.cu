@@ -169,6 +169,8 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
 }
 
 __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   if (p.r <= kShortBlock) {
     append_short(p, b);
@@ -244,6 +246,13 @@ size_t layer_workspace_bytes(const hsa_layer_desc& d) {
   return LayerWs(d, layer_attn_plan(d)).total;
 }
 
+int layer_launch_count(const hsa_layer_desc& d) {
+  int n = 1 + 1 + (layer_attn_plan(d).S > 1 ? 1 : 0);  // append, attention (+ combine)
+  if (d.kind == HSA_LAYER_C4)
+    n += (d.pool_total_rows > 0 ? 1 : 0) + topk_launch_count(d.pool_total_rows, d.max_pool_rows);
+  return n;
+}
+
 cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream) {
   const int r = d.kind;
   const AttnPlan pl = layer_attn_plan(d);
@@ -294,11 +303,11 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
     float* scores = d.scores ? d.scores : reinterpret_cast<float*>(w + L.scores);
     int32_t* tidx = d.topk_idx ? d.topk_idx : reinterpret_cast<int32_t*>(w + L.idx);
     e = launch_indexer(d.iq, d.w, d.key_pool, sp, d.B, d.Hi, d.Di, d.pool_total_rows, scores,
-                       status, stream);
+                       status, stream, true);
     if (e != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
     e = launch_topk(scores, sp, d.B, d.pool_total_rows, d.k, tidx, nullptr, w + L.topk, status,
-                    stream, d.max_pool_rows);
+                    stream, d.max_pool_rows, true);
     if (e != cudaSuccess) return e;
     if ((e = mark(3)) != cudaSuccess) return e;
     idx = tidx;
@@ -325,7 +334,7 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   a.out = d.out;
   a.out_dtype = d.out_dtype;
   a.lse = d.lse;
-  e = launch_attn(a, pl, w + L.attn, status, stream);
+  e = launch_attn(a, pl, w + L.attn, status, stream, true);
   if (e != cudaSuccess) return e;
   return mark(4);
 }

@@ -169,6 +169,8 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
   __shared__ uint32_t s_hist[kBins];
   __shared__ uint32_t s_scan[33], s_out[2];
   __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
   int row;
   int64_t piece, npieces;
   if (!locate_piece(B, blockIdx.x, ChunkPieces{sp, chunk}, &row, &piece, &npieces)) return;
@@ -395,6 +397,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   uint64_t* s_sel = s_loc + kClList;      // [kMaxK] CTA 0: winners, then every survivor
   uint64_t* s_cand = s_sel + kMaxK;       // [kClList] CTA 0: candidates (bin d1); sort runs
   __shared__ uint32_t s_scan[33], s_out[2], s_wt[kWarps], s_nloc, s_count, s_ccount;
+  pdl_trigger();
+  pdl_wait();
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t lt = (1u << lane) - 1u;
   const uint32_t rank = cluster_rank();
@@ -575,6 +579,8 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __re
   __shared__ uint32_t s_scan[33], s_out[2];
   __shared__ uint32_t s_wt[kWarps], s_ct[kWarps], s_gw, s_gc, s_count, s_ccount;
   __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
   int row;
   int64_t piece, npieces;
   if (!locate_piece(B, blockIdx.x, ChunkPieces{sp, chunk}, &row, &piece, &npieces)) return;
@@ -761,29 +767,30 @@ int64_t topk_chunk(int64_t total_rows) {
   return c;
 }
 
+int topk_launch_count(int64_t total_rows, int64_t max_row) {
+  return (max_row > 0 && max_row <= kClMax) || total_rows <= kClMax ? 1 : 2;
+}
+
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
                         int32_t* idx, float* vals, void* ws, uint32_t* status,
-                        cudaStream_t stream, int64_t max_row) {
+                        cudaStream_t stream, int64_t max_row, bool pdl) {
   Ws w = ws_view(ws, B, total_rows, k, status);
-  if ((max_row > 0 && max_row <= kClMax) || total_rows <= kClMax) {
+  if (topk_launch_count(total_rows, max_row) == 1) {
     // every row fits one cluster: a single launch
     cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kClDynSmem));
     if (e != cudaSuccess) return e;
-    topk_cluster_kernel<<<static_cast<unsigned>(B) * kCl, kThreads, kClDynSmem, stream>>>(
-        scores, sp, k, w, idx, vals);
-    return cudaGetLastError();
+    return launch_k(topk_cluster_kernel, dim3(static_cast<unsigned>(B) * kCl), dim3(kThreads),
+                    kClDynSmem, stream, pdl, scores, sp, k, w, idx, vals);
   }
   const int64_t chunk = topk_chunk(total_rows);
-  const int64_t grid = (total_rows + chunk - 1) / chunk + B;  // upper bound on chunks
-  topk_hist_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(scores, sp, B, k, chunk,
-                                                                         w);
-  cudaError_t e = cudaGetLastError();
+  const unsigned grid = static_cast<unsigned>((total_rows + chunk - 1) / chunk + B);  // >= chunks
+  cudaError_t e = launch_k(topk_hist_kernel, dim3(grid), dim3(kThreads), 0, stream, pdl, scores, sp,
+                           B, k, chunk, w);
   if (e != cudaSuccess) return e;
-  topk_select_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(scores, sp, B, k, chunk,
-                                                                           w, idx, vals);
-  return cudaGetLastError();
+  return launch_k(topk_select_kernel, dim3(grid), dim3(kThreads), 0, stream, true, scores, sp, B, k,
+                  chunk, w, idx, vals);
 }
 
 }  // namespace hsa

@@ -285,10 +285,14 @@ typedef struct hsa_layer_desc {
   void* const* stage_events;  /* NULL, or 5 caller-created cudaEvent_t recorded on `stream`
                                  before the append kernel, after it, after the indexer,
                                  after the top-k and after the attention (C128 records
-                                 events 2 and 3 at the same point as event 1) */
+                                 events 2 and 3 at the same point as event 1).  Kernels
+                                 separated by an event do not overlap their launches. */
 } hsa_layer_desc;
 
 size_t hsa_layer_decode_workspace_size(const hsa_layer_desc* d);
+/* Kernel launches one hsa_layer_decode call with this descriptor makes (0 if
+ * the descriptor is invalid). */
+int32_t hsa_layer_decode_launches(const hsa_layer_desc* d);
 hsa_status_t hsa_layer_decode(const hsa_layer_desc* d, void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
