@@ -13,28 +13,24 @@
 // latent KV head, values their first Dv channels):
 //   o[b,h] = sum_t softmax_t(scale * q[b,h] . K_t) V_t,   lse[b,h] = log sum_t e^(...)
 //
-// Design (sm_103a):
-//  * The keys are the M = 128 side of both contractions, so one gathered tile
-//    of 128 key rows in shared memory feeds both MMAs without re-layout:
-//      S^T[key, head] = K_tile . Q^T      (A = K tile, K-major over Dqk)
-//      O^T[dv, head] += V_tile^T . P^T    (A = the same tile, MN-major view)
-//    Q (a group of 32 heads) and P^T are the N side.  S^T, O^T live in TMEM.
-//  * The K tile is stored as Dqk/64 slices of [128 keys x 64 channels] in the
-//    128-byte swizzled layout; slice j always lives in buffer j, so slices 2m
-//    and 2m+1 (the value channels of O^T M-tile m) sit 16 KB apart, which is
-//    the MN-major descriptor's leading-byte offset.  A buffer is refilled for
-//    the next tile as soon as its last reader commits (the rope slices after
-//    the S^T MMAs, value slices after their O^T M-tile), so the gather of
-//    tile t+1 overlaps the softmax and O^T of tile t.
-//  * Warp roles: warps 0-3 own TMEM lanes 0-127 (softmax of one key each, then
-//    the epilogue of one value channel each); warp 4 allocates TMEM and one
-//    lane issues every tcgen05.mma; warps 5-7 gather rows with 16-byte
-//    cp.async (8 consecutive threads per 128-byte row segment, zero-fill for
-//    masked slots) from a per-tile table of row addresses in shared memory.
-//  * Softmax: per-head maxima by a warp transpose-reduction plus one shared
-//    exchange; lazy rescaling (the running maximum only moves when a tile
-//    raises it by more than 2^8, so P <= 256 and O^T is corrected in TMEM
-//    only then); row sums accumulate per thread and reduce once at the end.
+// Design (sm_103a).  The kernel is bound by how fast each SM can gather key
+// rows, so it keeps that gather streaming and reads every row once per
+// sequence (all heads of a token in one CTA, up to 64):
+//  * Keys are the M = 128 side of both contractions, so a gathered block of
+//    128 key rows feeds both MMAs without re-layout:
+//      S^T[key, head] = K_tile . Q^T      (A = K, K-major over Dqk)
+//      O^T[dv, head] += V_tile^T . P^T    (A = the same rows, MN-major view)
+//  * Rows arrive through a ring of three 32 KB pair slots (two 64-channel
+//    slices of 128 rows each, 128-byte swizzled, 16 KB apart = the MN-major
+//    leading-byte offset), filled by three gather warps with 16-byte
+//    cp.async and drained by one MMA-issuing thread.
+//  * Two passes per chunk of up to four 128-slot tiles: pass 1 streams all
+//    Dqk channels of the chunk's tiles into S^T accumulators (one per tile,
+//    in TMEM); the softmax warps then take the exact maximum over the chunk,
+//    and pass 2 streams the value channels again (now from L2) into O^T
+//    against P^T, which the softmax warps write tile by tile.  Across chunks
+//    the running maximum moves lazily (only by more than 2^8; O^T is then
+//    rescaled in TMEM).
 //  * Long key lists are split over CTAs; each split writes an fp32 partial
 //    output and log-sum-exp that a combine kernel merges.
 #include <math.h>
@@ -52,8 +48,10 @@ constexpr int kMmaWarp = 4;
 constexpr int kProdWarp0 = 5;
 constexpr int kProdThreads = 96;
 constexpr int kThreads = 32 * 8;
-constexpr int kMaxSlices = 9;
+constexpr int kRing = 3;            // pair slots
+constexpr int kMaxTC = 4;           // tiles per chunk
 constexpr uint32_t kSliceBytes = kKeys * 128;
+constexpr uint32_t kPairBytes = 2 * kSliceBytes;
 constexpr float kRescaleLog2 = 8.f;
 
 struct AttnParams {
@@ -68,7 +66,7 @@ struct AttnParams {
   int k;
   int64_t max_rows;       // dense: cap on compressed rows per sequence
   int B, Hq, Dqk, Dv;
-  int HG, G, S, tps;
+  int HG, G, S, tps, TC;
   float scale_log2;
   void* out;
   int out_dtype;
@@ -126,25 +124,19 @@ HSA_DEVINL const uint16_t* slot_row(const AttnParams& p, int b, const SeqGeom& g
   return p.extra + (g.off + j) * p.Dqk;
 }
 
-// Order in which the slices of a tile are loaded and multiplied: the
-// channels past Dv (rope) first, since their buffers free up first.
-HSA_DEVINL int slice_order(int jj, int NSL, int NV) {
-  return jj < NSL - NV ? NV + jj : jj - (NSL - NV);
-}
-
 // Byte offset of element (row, 16-byte chunk) in a 128-byte-swizzled
 // K-major block whose rows are 128 bytes (8-row atoms of 1024 bytes).
 HSA_DEVINL uint32_t sw128(int row, int chunk) {
   return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-// Column reduction of a 32 x kN register tile held one row per lane: on
-// return lane l holds the reduction of column (l mod kN) over the warp.
-template <int kN, bool kMax>
-HSA_DEVINL float warp_transpose_reduce(float (&v)[kN]) {
+// Column reduction of a 32 x 32 register tile held one row per lane: on
+// return lane l holds the reduction of column l over the warp.
+template <bool kMax>
+HSA_DEVINL float warp_transpose_reduce32(float (&v)[32]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int width = kN / 2; width >= 1; width >>= 1) {
+  for (int width = 16; width >= 1; width >>= 1) {
     const bool upper = (lane & width) != 0;
 #pragma unroll
     for (int i = 0; i < width; ++i) {
@@ -154,25 +146,23 @@ HSA_DEVINL float warp_transpose_reduce(float (&v)[kN]) {
       v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
-  float r = v[0];
-  if (kN == 16) {
-    const float o = __shfl_xor_sync(0xffffffffu, r, 16);
-    r = kMax ? fmaxf(r, o) : r + o;
-  }
-  return r;
+  return v[0];
 }
 
 struct Shared {
-  uint64_t full[kMaxSlices], empty[kMaxSlices];
-  uint64_t s_full[2], s_empty[2], o_done[2];
-  uint64_t p_full, q_full, fin;
+  uint64_t full[kRing], empty[kRing];
+  uint64_t s_full[kMaxTC], s_empty;  // S^T of chunk tile tc written; S^T columns free again
+  uint64_t p_full[2], o_done[2];     // P^T buffer written; O^T of that buffer's tile done
+  uint64_t q_full, fin;
   uint32_t tmem;
   int abort;
-  float red[kSmWarps][32];
-  float bc[32];
-  float m[32];      // running maximum per head (log2 units), identical for every thread
-  float alpha[32];  // rescale factor of the current tile per head
-  const uint16_t* rows[2][kKeys];  // gather table of the producers (per tile parity)
+  float red[kSmWarps][64];
+  float bc[64];
+  float m[64];      // running maximum per head (log2 units), identical for every thread
+  float alpha[64];  // rescale factor of the current chunk per head
+  float inv[64];    // 1 / softmax denominator per head (0 when nothing was attended)
+  int done_ok;      // the softmax warps finished without an abort: O^T may be written out
+  const uint16_t* rows[kMaxTC][kKeys];  // gather tables of the producers (this chunk)
 };
 
 // Bounded wait that also gives up when another role has aborted.
@@ -192,7 +182,6 @@ HSA_DEVINL bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity, uint32
   }
 }
 
-template <int kN>
 HSA_DEVINL void write_result(const AttnParams& p, int b, int g, int s, int h, int dv, float o) {
   const int64_t head = static_cast<int64_t>(b) * p.Hq + g * p.HG + h;
   if (p.S == 1) {
@@ -223,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   const int g = blockIdx.x % p.G;
   const int s = (blockIdx.x / p.G) % p.S;
   const int b = blockIdx.x / (p.G * p.S);
-  const int NSL = p.Dqk / 64, NV = p.Dv / 64, NMT = p.Dv / 128;
+  const int NSL = p.Dqk / 64, NMT = p.Dv / 128, NP1 = (NSL + 1) / 2, TC = p.TC;
   const SeqGeom geo = seq_geom(p, b);
   const int64_t n_slots = geo.n_swa + geo.n_extra;
   const int n_tiles = static_cast<int>((n_slots + kKeys - 1) / kKeys);
@@ -235,38 +224,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     if (tid < kKeys) {
       if (p.S == 1)
         for (int h = 0; h < p.HG; ++h)
-          for (int dv = tid; dv < p.Dv; dv += kKeys) write_result<kN>(p, b, g, s, h, dv, 0.f);
+          for (int dv = tid; dv < p.Dv; dv += kKeys) write_result(p, b, g, s, h, dv, 0.f);
       if (tid < p.HG) write_lse(p, b, g, s, tid, -INFINITY);
     }
     return;
   }
   if (p.extra && !p.idx && geo.nb > p.max_rows && tid == 0 && s == 0 && g == 0)
     set_status(p.status, HSA_DEV_BOUNDS);
+  const int nchunks = (nt + TC - 1) / TC;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const uint32_t qslice = kN * 128;          // bytes of one Q slice (kN heads x 64 ch)
-  const uint32_t pbytes = 2 * kN * 128;      // one P^T buffer (2 K-blocks of 64 keys)
-  uint8_t* kbuf = smem;
-  uint8_t* qs = kbuf + NSL * kSliceBytes;
+  const uint32_t qslice = kN * 128;       // bytes of one Q slice (kN heads x 64 channels)
+  const uint32_t pbytes = 2 * kN * 128;   // one P^T buffer (2 K-blocks of 64 keys)
+  uint8_t* ring = smem;
+  uint8_t* qs = ring + kRing * kPairBytes;
   uint8_t* pt = qs + NSL * qslice;
-  // TMEM columns: S^T of tile parity sb, partial accumulator a at (sb*4 + a)*kN;
-  // O^T M-tile m at (8 + m)*kN.
-  const uint32_t tmem_cols_needed = 8 * kN + NMT * kN;
+  // TMEM columns: S^T of chunk tile tc at tc*kN; O^T M-tile m at (TC + m)*kN
   uint32_t tmem_cols = 32;
-  while (tmem_cols < tmem_cols_needed) tmem_cols <<= 1;
+  while (tmem_cols < static_cast<uint32_t>((TC + NMT) * kN)) tmem_cols <<= 1;
 
   if (tid == 0) {
-    for (int j = 0; j < NSL; ++j) {
-      tc::mbar_init(&sh.full[j], kProdThreads);
-      tc::mbar_init(&sh.empty[j], 1);
+    for (int i = 0; i < kRing; ++i) {
+      tc::mbar_init(&sh.full[i], kProdThreads);
+      tc::mbar_init(&sh.empty[i], 1);
     }
+    for (int i = 0; i < kMaxTC; ++i) tc::mbar_init(&sh.s_full[i], 1);
+    tc::mbar_init(&sh.s_empty, kKeys);
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sh.s_full[i], 1);
-      tc::mbar_init(&sh.s_empty[i], kKeys);
+      tc::mbar_init(&sh.p_full[i], kKeys);
       tc::mbar_init(&sh.o_done[i], 1);
     }
-    tc::mbar_init(&sh.p_full, kKeys);
     tc::mbar_init(&sh.q_full, kProdThreads);
     tc::mbar_init(&sh.fin, 1);
     sh.abort = 0;
@@ -282,66 +270,79 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   const uint32_t tmem = sh.tmem;
 
   if (warp >= kProdWarp0) {
-    // ------------------------------------------------------------ producers
+    // ------------------------------------------------------------ gatherers
     const int pt_ = tid - kProdWarp0 * 32;
-    const int nq = kN * NSL * 8;
-    for (int i = pt_; i < nq; i += kProdThreads) {
-      const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, c = rem & 7;
-      const bool v = h < p.HG;
-      const uint16_t* src =
-          v ? p.q + (static_cast<int64_t>(b) * p.Hq + g * p.HG + h) * p.Dqk + j * 64 + c * 8 : p.q;
-      tc::cp_async16(qs + j * qslice + sw128(h, c), src, v ? 16u : 0u);
-    }
-    tc::cp_async_commit();
-    tc::cp_async_wait<0>();
-    tc::fence_proxy_async_smem();
-    tc::mbar_arrive(&sh.q_full);
-
+    // cp.async groups: group 0 is Q, group i + 1 ring item i
     int64_t issued = 0, retired = 0;
     auto retire_to = [&](int keep) {
       if (issued - retired > keep) {
         tc::cp_async_wait_dyn(keep);
         tc::fence_proxy_async_smem();
         while (issued - retired > keep) {
-          tc::mbar_arrive(&sh.full[slice_order(static_cast<int>(retired % NSL), NSL, NV)]);
+          tc::mbar_arrive(retired == 0 ? &sh.q_full : &sh.full[(retired - 1) % kRing]);
           ++retired;
         }
       }
     };
-    auto build_table = [&](int t) {
-      const uint16_t** table = sh.rows[(t - t0) & 1];
-      for (int r = pt_; r < kKeys; r += kProdThreads)
-        table[r] = slot_row(p, b, geo, static_cast<int64_t>(t) * kKeys + r, true);
+    auto issue_q = [&]() {
+      const int nq = kN * NSL * 8;
+      for (int i = pt_; i < nq; i += kProdThreads) {
+        const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, c = rem & 7;
+        const bool v = h < p.HG;
+        const uint16_t* src =
+            v ? p.q + (static_cast<int64_t>(b) * p.Hq + g * p.HG + h) * p.Dqk + j * 64 + c * 8 : p.q;
+        tc::cp_async16(qs + j * qslice + sw128(h, c), src, v ? 16u : 0u);
+      }
+      tc::cp_async_commit();
+      ++issued;
     };
     bool ok = true;
-    build_table(t0);
-    tc::named_barrier(2, kProdThreads);
-    for (int t = t0; t < t1; ++t) {
-      const int tt = t - t0;
-      const uint16_t* const* table = sh.rows[tt & 1];
-      for (int jj = 0; jj < NSL && ok; ++jj) {
-        const int j = slice_order(jj, NSL, NV);
-        // Buffer j is freed by the consumption of tile tt-1, whose slices were
-        // all signalled before this tile began, so blocking here while this
-        // tile's own slices are still in flight cannot stall the MMA.
-        if (tt > 0 && !wait_or_abort(sh, &sh.empty[j], (tt - 1) & 1, p.status)) {
-          ok = false;
-          break;
+    int64_t item = 0;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
+      // every previous item is issued (its rows were read at issue): refill the tables
+      tc::named_barrier(2, kProdThreads);
+      for (int r = pt_; r < nct * kKeys; r += kProdThreads)
+        sh.rows[r / kKeys][r % kKeys] =
+            slot_row(p, b, geo, static_cast<int64_t>(tb + r / kKeys) * kKeys + r % kKeys, true);
+      tc::named_barrier(2, kProdThreads);
+      if (c == 0) issue_q();  // after the first row tables: the key gathers start sooner
+      // pass 1: every channel pair of every tile; pass 2: the value pairs again
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        const int nit = pass == 0 ? NP1 : NMT;
+        for (int tc_ = 0; tc_ < nct && ok; ++tc_) {
+          const uint16_t* const* table = sh.rows[tc_];
+          for (int it = 0; it < nit; ++it, ++item) {
+            const int slot = static_cast<int>(item % kRing);
+            bool fail = false;  // (ring item `item` is cp.async group item + 1)
+            if (item >= kRing) {
+              const uint32_t par = static_cast<uint32_t>((item / kRing - 1) & 1);
+              if (!tc::mbar_test_wait(&sh.empty[slot], par)) {
+                retire_to(0);  // signal everything issued before blocking
+                fail = !wait_or_abort(sh, &sh.empty[slot], par, p.status);
+              }
+            }
+            if (tc::named_barrier_or(2, kProdThreads, fail)) {
+              ok = false;
+              break;
+            }
+            uint8_t* dst = ring + slot * kPairBytes;
+            for (int half = 0; half < 2; ++half) {
+              const int j = 2 * it + half;
+              if (j >= NSL) break;
+              for (int q = pt_; q < kKeys * 8; q += kProdThreads) {
+                const int r = q >> 3, cc = q & 7;
+                const uint16_t* row = table[r];
+                tc::cp_async16(dst + half * kSliceBytes + sw128(r, cc), row ? row + j * 64 + cc * 8 : p.q,
+                               row ? 16u : 0u);
+              }
+            }
+            tc::cp_async_commit();
+            ++issued;
+            retire_to(kRing - 1);
+          }
         }
-        uint8_t* base = kbuf + j * kSliceBytes;
-        for (int q = pt_; q < kKeys * 8; q += kProdThreads) {
-          const int r = q >> 3, c = q & 7;
-          const uint16_t* row = table[r];
-          tc::cp_async16(base + sw128(r, c), row ? row + j * 64 + c * 8 : p.q, row ? 16u : 0u);
-        }
-        tc::cp_async_commit();
-        ++issued;
       }
-      // the next tile's rows (index loads) overlap this tile's copies; then every
-      // slice of this tile is signalled before the producer can block again
-      if (t + 1 < t1 && ok) build_table(t + 1);
-      retire_to(0);
-      if (tc::named_barrier_or(2, kProdThreads, !ok)) break;  // table visible; agree on abort
     }
     retire_to(0);
   } else if (warp == kMmaWarp) {
@@ -350,53 +351,69 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       const uint32_t idS = tc::idesc_bf16_f32(kKeys, kN);
       const uint32_t idO = tc::idesc_bf16_f32(kKeys, kN, /*a_mn=*/true, /*b_mn=*/false);
       bool ok = wait_or_abort(sh, &sh.q_full, 0, p.status);
-      for (int t = t0; t < t1 && ok; ++t) {
-        const int tt = t - t0, sb = tt & 1;
-        if (tt >= 2 && !wait_or_abort(sh, &sh.s_empty[sb], ((tt - 2) >> 1) & 1, p.status)) {
+      int64_t item = 0;
+      int gt = 0;  // tiles through pass 2 so far (P^T buffer gt & 1)
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
+        if (c > 0 && !wait_or_abort(sh, &sh.s_empty, (c - 1) & 1, p.status)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        // Four independent partial accumulators (by K-step within a slice) keep
-        // these small MMAs from waiting on each other's accumulation.
-        const uint32_t d_s = tmem + sb * 4 * kN;
-        for (int jj = 0; jj < NSL && ok; ++jj) {
-          const int j = slice_order(jj, NSL, NV);
-          if (!wait_or_abort(sh, &sh.full[j], tt & 1, p.status)) {
+        for (int tc_ = 0; tc_ < nct && ok; ++tc_) {
+          const uint32_t d_s = tmem + tc_ * kN;
+          for (int it = 0; it < NP1; ++it, ++item) {
+            const int slot = static_cast<int>(item % kRing);
+            if (!wait_or_abort(sh, &sh.full[slot], static_cast<uint32_t>((item / kRing) & 1),
+                               p.status)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t ka0 = tc::smem_u32(ring + slot * kPairBytes);
+            for (int half = 0; half < 2; ++half) {
+              const int j = 2 * it + half;
+              if (j >= NSL) break;
+              const uint32_t ka = ka0 + half * kSliceBytes;
+              const uint32_t qa = tc::smem_u32(qs + j * qslice);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t a = tc::smem_desc(ka + ks * 32, 16, 1024, tc::kSwizzle128B);
+                const uint64_t bq = tc::smem_desc(qa + ks * 32, 16, 1024, tc::kSwizzle128B);
+                tc::mma_bf16(d_s, a, bq, idS, (j | ks) != 0 ? 1u : 0u);
+              }
+            }
+            tc::mma_commit(&sh.empty[slot]);
+          }
+          if (ok) tc::mma_commit(&sh.s_full[tc_]);
+        }
+        for (int tc_ = 0; tc_ < nct && ok; ++tc_, ++gt) {
+          const int buf = gt & 1;
+          if (!wait_or_abort(sh, &sh.p_full[buf], (gt >> 1) & 1, p.status)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t ka = tc::smem_u32(kbuf + j * kSliceBytes);
-          const uint32_t qa = tc::smem_u32(qs + j * qslice);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t a = tc::smem_desc(ka + ks * 32, 16, 1024, tc::kSwizzle128B);
-            const uint64_t bq = tc::smem_desc(qa + ks * 32, 16, 1024, tc::kSwizzle128B);
-            tc::mma_bf16(d_s + ks * kN, a, bq, idS, jj != 0);
+          const uint32_t pa = tc::smem_u32(pt + buf * pbytes);
+          for (int m = 0; m < NMT; ++m, ++item) {
+            const int slot = static_cast<int>(item % kRing);
+            if (!wait_or_abort(sh, &sh.full[slot], static_cast<uint32_t>((item / kRing) & 1),
+                               p.status)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t va = tc::smem_u32(ring + slot * kPairBytes);
+            for (int kk = 0; kk < kKeys / 16; ++kk) {
+              const uint64_t bp = tc::smem_desc(pa + (kk >> 2) * kN * 128 + (kk & 3) * 32, 16, 1024,
+                                                tc::kSwizzle128B);
+              const uint64_t a = tc::smem_desc(va + kk * 2048, kSliceBytes, 1024, tc::kSwizzle128B);
+              tc::mma_bf16(tmem + (TC + m) * kN, a, bp, idO, (gt > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(&sh.empty[slot]);
           }
-          if (j >= NV) tc::mma_commit(&sh.empty[j]);
+          if (ok) tc::mma_commit(&sh.o_done[buf]);
         }
-        if (!ok) break;
-        tc::mma_commit(&sh.s_full[sb]);
-        if (!wait_or_abort(sh, &sh.p_full, tt & 1, p.status)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        const uint32_t pa = tc::smem_u32(pt + sb * pbytes);
-        // M-tiles are independent accumulators: interleave them
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t bp =
-              tc::smem_desc(pa + (kk >> 2) * kN * 128 + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
-          for (int m = 0; m < NMT; ++m) {
-            const uint32_t va = tc::smem_u32(kbuf + 2 * m * kSliceBytes);
-            const uint64_t a = tc::smem_desc(va + kk * 2048, kSliceBytes, 1024, tc::kSwizzle128B);
-            tc::mma_bf16(tmem + (8 + m) * kN, a, bp, idO, (tt > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        for (int j = 0; j < NV; ++j) tc::mma_commit(&sh.empty[j]);
-        tc::mma_commit(&sh.o_done[sb]);
       }
       // drain: every MMA this thread issued has completed before TMEM is freed
       tc::mma_commit(&sh.fin);
@@ -404,45 +421,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
+    // thread tid owns key lane tid of every S^T tile; heads in groups of 32 columns
+    constexpr int kGroups = (kN + 31) / 32, kGW = kN < 32 ? kN : 32;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float l_part[kN];
 #pragma unroll
     for (int h = 0; h < kN; ++h) l_part[h] = 0.f;
     if (tid < kN) sh.m[tid] = -INFINITY;
     bool ok = true;
-    for (int t = t0; t < t1; ++t) {
-      const int tt = t - t0, sb = tt & 1;
-      const bool valid = slot_row(p, b, geo, static_cast<int64_t>(t) * kKeys + tid, false) != nullptr;
-      {
-        const bool failed = !wait_or_abort(sh, &sh.s_full[sb], (tt >> 1) & 1, p.status);
-        if (tc::named_barrier_or(1, kKeys, failed)) { ok = false; break; }
-      }
-      tc::fence_after_sync();
-      __syncwarp();
-      float sacc[kN];
+    int gt = 0;
+    auto agree = [&](bool failed) { return !tc::named_barrier_or(1, kKeys, failed); };
+    // S^T columns [col, col + kGW) of this lane, scaled to log2 units; -inf when masked
+    auto load_s = [&](uint32_t col, bool valid, float (&x)[32]) {
+      uint32_t raw[32];
+      tc::tmem_ld16(tmem + lane_base + col, raw);
+      if (kGW == 32) tc::tmem_ld16(tmem + lane_base + col + 16, raw + 16);
+      tc::tmem_ld_wait();
 #pragma unroll
-      for (int h = 0; h < kN; ++h) sacc[h] = 0.f;
+      for (int i = 0; i < 32; ++i)
+        x[i] = (i < kGW && valid) ? __uint_as_float(raw[i]) * p.scale_log2 : -INFINITY;
+    };
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
+      // ---- the chunk's maximum per head, each tile folded in as soon as its S^T lands
+      float run[kGroups];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
+      for (int gi = 0; gi < kGroups; ++gi) run[gi] = -INFINITY;
+      for (int tc_ = 0; tc_ < nct && ok; ++tc_) {
+        if (!agree(!wait_or_abort(sh, &sh.s_full[tc_], c & 1, p.status))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        __syncwarp();
+        const bool valid =
+            slot_row(p, b, geo, static_cast<int64_t>(tb + tc_) * kKeys + tid, false) != nullptr;
 #pragma unroll
-        for (int half = 0; half < kN / 16; ++half) {
-          uint32_t raw[16];
-          tc::tmem_ld16(tmem + lane_base + (sb * 4 + a) * kN + half * 16, raw);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) sacc[half * 16 + i] += __uint_as_float(raw[i]);
+        for (int gi = 0; gi < kGroups; ++gi) {
+          float x[32];
+          load_s(tc_ * kN + gi * 32, valid, x);
+          run[gi] = fmaxf(run[gi], warp_transpose_reduce32<true>(x));
         }
       }
-      tc::fence_before_sync();
-      tc::mbar_arrive(&sh.s_empty[sb]);
-      float x[kN], mx[kN];
+      if (!ok) break;
 #pragma unroll
-      for (int h = 0; h < kN; ++h) {
-        x[h] = valid ? sacc[h] * p.scale_log2 : -INFINITY;
-        mx[h] = x[h];
-      }
-      const float mcol = warp_transpose_reduce<kN, true>(mx);
-      if (lane < kN) sh.red[warp][lane] = mcol;
+      for (int gi = 0; gi < kGroups; ++gi)
+        if (gi * 32 + lane < kN) sh.red[warp][gi * 32 + lane] = run[gi];
       tc::named_barrier(1, kKeys);
       bool moved = false;
       if (tid < kN) {
@@ -450,97 +474,139 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
             fmaxf(fmaxf(sh.red[0][tid], sh.red[1][tid]), fmaxf(sh.red[2][tid], sh.red[3][tid]));
         const float mo = sh.m[tid];
         const float mn = fmaxf(mo, mt);
-        moved = mn > mo + kRescaleLog2;
+        moved = mn > mo + kRescaleLog2 || (mo == -INFINITY && mn > -INFINITY);
         sh.alpha[tid] = moved ? exp2f(mo - mn) : 1.f;
         if (moved) sh.m[tid] = mn;
       }
-      const bool any = tc::named_barrier_or(1, kKeys, moved);
-      if (any) {
+      if (tc::named_barrier_or(1, kKeys, moved)) {
 #pragma unroll
         for (int h = 0; h < kN; ++h) l_part[h] *= sh.alpha[h];
-        if (tt > 0) {
-          const bool failed =
-              !wait_or_abort(sh, &sh.o_done[(tt - 1) & 1], ((tt - 1) >> 1) & 1, p.status);
-          if (tc::named_barrier_or(1, kKeys, failed)) { ok = false; break; }
+        if (gt > 0) {
+          // O^T holds earlier chunks: wait for their last MMAs, then rescale in TMEM
+          const int lt = gt - 1;
+          if (!agree(!wait_or_abort(sh, &sh.o_done[lt & 1], (lt >> 1) & 1, p.status))) {
+            ok = false;
+            break;
+          }
           tc::fence_after_sync();
           __syncwarp();
           for (int m = 0; m < NMT; ++m) {
-            const uint32_t col = tmem + lane_base + (8 + m) * kN;
+            const uint32_t col = tmem + lane_base + (TC + m) * kN;
 #pragma unroll
-            for (int half = 0; half < kN / 16; ++half) {
+            for (int q16 = 0; q16 < kN / 16; ++q16) {
               uint32_t o[16];
-              tc::tmem_ld16(col + half * 16, o);
+              tc::tmem_ld16(col + q16 * 16, o);
               tc::tmem_ld_wait();
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                o[i] = __float_as_uint(__uint_as_float(o[i]) * sh.alpha[half * 16 + i]);
-              tc::tmem_st16(col + half * 16, o);
+                o[i] = __float_as_uint(__uint_as_float(o[i]) * sh.alpha[q16 * 16 + i]);
+              tc::tmem_st16(col + q16 * 16, o);
             }
           }
           tc::tmem_st_wait();
         }
       }
-      if (tt >= 2) {  // P^T buffer sb is free once O^T of tile tt-2 has completed
-        const bool failed = !wait_or_abort(sh, &sh.o_done[sb], ((tt - 2) >> 1) & 1, p.status);
-        if (tc::named_barrier_or(1, kKeys, failed)) { ok = false; break; }
+      // ---- P^T tile by tile (each into the buffer its O^T pass reads)
+      for (int tc_ = 0; tc_ < nct; ++tc_, ++gt) {
+        const int buf = gt & 1;
+        if (gt >= 2) {  // the buffer is free once O^T of tile gt-2 has completed
+          const int lt = gt - 2;
+          if (!agree(!wait_or_abort(sh, &sh.o_done[buf], (lt >> 1) & 1, p.status))) {
+            ok = false;
+            break;
+          }
+        }
+        const bool valid =
+            slot_row(p, b, geo, static_cast<int64_t>(tb + tc_) * kKeys + tid, false) != nullptr;
+        uint8_t* ptb = pt + buf * pbytes + (tid >> 6) * kN * 128;
+        const int kc = (tid & 63) >> 3, ke = (tid & 7) << 1;
+#pragma unroll
+        for (int gi = 0; gi < kGroups; ++gi) {
+          float x[32];
+          load_s(tc_ * kN + gi * 32, valid, x);
+#pragma unroll
+          for (int i = 0; i < kGW; i += 2) {
+            const int h = gi * 32 + i;
+            const float m0 = sh.m[h], m1 = sh.m[h + 1];
+            const float p0 = m0 == -INFINITY ? 0.f : tc::ex2_approx(x[i] - m0);
+            const float p1 = m1 == -INFINITY ? 0.f : tc::ex2_approx(x[i + 1] - m1);
+            const __nv_bfloat162 q2 = __floats2bfloat162_rn(p0, p1);
+            l_part[h] += __low2float(q2);
+            l_part[h + 1] += __high2float(q2);
+            const uint32_t pk = *reinterpret_cast<const uint32_t*>(&q2);
+            *reinterpret_cast<uint16_t*>(ptb + (h >> 3) * 1024 + (h & 7) * 128 +
+                                         ((kc ^ (h & 7)) << 4) + ke) = static_cast<uint16_t>(pk);
+            const int h1 = h + 1;
+            *reinterpret_cast<uint16_t*>(ptb + (h1 >> 3) * 1024 + (h1 & 7) * 128 +
+                                         ((kc ^ (h1 & 7)) << 4) + ke) = static_cast<uint16_t>(pk >> 16);
+          }
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&sh.p_full[buf]);
       }
-      float mreg[kN];
-#pragma unroll
-      for (int h = 0; h < kN; ++h) mreg[h] = sh.m[h];
-      uint32_t pk[kN / 2];
-#pragma unroll
-      for (int h = 0; h < kN; h += 2) {
-        const float p0 = mreg[h] == -INFINITY ? 0.f : tc::ex2_approx(x[h] - mreg[h]);
-        const float p1 = mreg[h + 1] == -INFINITY ? 0.f : tc::ex2_approx(x[h + 1] - mreg[h + 1]);
-        const __nv_bfloat162 q2 = __floats2bfloat162_rn(p0, p1);
-        l_part[h] += __low2float(q2);
-        l_part[h + 1] += __high2float(q2);
-        pk[h / 2] = *reinterpret_cast<const uint32_t*>(&q2);
-      }
-      uint8_t* ptb = pt + sb * pbytes + (tid >> 6) * kN * 128;
-      const int kc = (tid & 63) >> 3, ke = (tid & 7) << 1;
-#pragma unroll
-      for (int h = 0; h < kN; ++h)
-        *reinterpret_cast<uint16_t*>(ptb + (h >> 3) * 1024 + (h & 7) * 128 + ((kc ^ (h & 7)) << 4) +
-                                     ke) = static_cast<uint16_t>(pk[h / 2] >> ((h & 1) * 16));
-      tc::fence_proxy_async_smem();
+      if (!ok) break;
+      // this chunk's S^T columns may be overwritten by the next chunk
       tc::fence_before_sync();
-      tc::mbar_arrive(&sh.p_full);
+      tc::mbar_arrive(&sh.s_empty);
     }
     {
       // `ok` is uniform over the softmax warps here (every exit from the loop
       // went through an agreement barrier)
       bool failed = !ok;
-      if (!failed) failed = !wait_or_abort(sh, &sh.o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, p.status);
-      ok = !tc::named_barrier_or(1, kKeys, failed);
+      if (!failed) {
+        const int lt = gt - 1;
+        failed = !wait_or_abort(sh, &sh.o_done[lt & 1], (lt >> 1) & 1, p.status);
+      }
+      ok = agree(failed);
     }
     // every softmax thread reaches these barriers, whether or not it aborted
-    const float lcol = warp_transpose_reduce<kN, false>(l_part);
-    if (lane < kN) sh.red[warp][lane] = lcol;
-    tc::named_barrier(1, kKeys);
-    if (tid < kN) sh.bc[tid] = (sh.red[0][tid] + sh.red[1][tid]) + (sh.red[2][tid] + sh.red[3][tid]);
-    tc::named_barrier(1, kKeys);
-    if (ok) {
-      tc::fence_after_sync();
-      __syncwarp();
-      float inv[kN];
 #pragma unroll
-      for (int h = 0; h < kN; ++h) inv[h] = sh.bc[h] > 0.f ? 1.f / sh.bc[h] : 0.f;
-      for (int m = 0; m < NMT; ++m) {
-        const uint32_t col = tmem + lane_base + (8 + m) * kN;
-        uint32_t acc[kN];
-        tc::tmem_ld16(col, acc);
-        if (kN == 32) tc::tmem_ld16(col + 16, acc + (kN == 32 ? 16 : 0));
+    for (int gi = 0; gi < kGroups; ++gi) {
+      float lv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) lv[i] = (i < kGW) ? l_part[gi * 32 + (i < kGW ? i : 0)] : 0.f;
+      const float lcol = warp_transpose_reduce32<false>(lv);
+      if (gi * 32 + lane < kN) sh.red[warp][gi * 32 + lane] = lcol;
+    }
+    tc::named_barrier(1, kKeys);
+    if (tid < kN) {
+      const float l = (sh.red[0][tid] + sh.red[1][tid]) + (sh.red[2][tid] + sh.red[3][tid]);
+      sh.inv[tid] = l > 0.f ? 1.f / l : 0.f;
+      if (ok && tid < p.HG)
+        write_lse(p, b, g, s, tid, l > 0.f ? (sh.m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY);
+    }
+    if (tid == 0) sh.done_ok = ok ? 1 : 0;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (sh.done_ok) {
+    // ---- O^T / l, written by all eight warps: warp w reads TMEM lane quarter
+    // w & 3 (value channels) and every other 16-head column group from w >> 2
+    tc::fence_after_sync();
+    const int quarter = warp & 3;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool part = p.S > 1, bf = !part && p.out_dtype == HSA_BF16;
+    const int64_t head0 = static_cast<int64_t>(b) * p.Hq + g * p.HG;
+    float* of = part ? p.po + ((static_cast<int64_t>(b) * p.S + s) * p.Hq + g * p.HG) * p.Dv
+                     : reinterpret_cast<float*>(p.out) + head0 * p.Dv;
+    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.out) + head0 * p.Dv;
+    for (int m = 0; m < NMT; ++m) {
+      const int dv = m * kKeys + quarter * 32 + lane;
+      for (int q16 = warp >> 2; q16 < kN / 16; q16 += 2) {
+        uint32_t acc[16];
+        tc::tmem_ld16(lane_addr + (TC + m) * kN + q16 * 16, acc);
         tc::tmem_ld_wait();
-        const int dv = m * kKeys + tid;
 #pragma unroll
-        for (int h = 0; h < kN; ++h)
-          if (h < p.HG) write_result<kN>(p, b, g, s, h, dv, __uint_as_float(acc[h]) * inv[h]);
-      }
-      if (tid < p.HG) {
-        const float mh = sh.m[tid];
-        const float l = sh.bc[tid];
-        write_lse(p, b, g, s, tid, l > 0.f ? (mh + log2f(l)) * 0.69314718055994531f : -INFINITY);
+        for (int i = 0; i < 16; ++i) {
+          const int h = q16 * 16 + i;
+          if (h < p.HG) {
+            const float o = __uint_as_float(acc[i]) * sh.inv[h];
+            const int64_t at = static_cast<int64_t>(h) * p.Dv + dv;
+            if (bf) ob[at] = __float2bfloat16_rn(o);
+            else of[at] = o;
+          }
+        }
       }
     }
   }
@@ -590,8 +656,9 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restri
 
 AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, int64_t extra_slots) {
   AttnPlan pl;
-  pl.HG = static_cast<int>(Hq <= 32 ? Hq : 32);
-  pl.N = pl.HG <= 16 ? 16 : 32;
+  // every head of a token in one CTA when they fit the MMA width (one gather per row)
+  pl.HG = static_cast<int>(Hq <= 32 ? Hq : (Hq % 64 == 0 ? 64 : 32));
+  pl.N = pl.HG <= 16 ? 16 : (pl.HG <= 32 ? 32 : 64);
   pl.G = static_cast<int>(Hq / pl.HG);
   const int64_t slots = W + extra_slots;
   const int64_t tiles = slots > 0 ? (slots + kKeys - 1) / kKeys : 1;
@@ -600,12 +667,14 @@ AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, in
   if (S > tiles) S = tiles;
   pl.tps = static_cast<int>((tiles + S - 1) / S);
   pl.S = static_cast<int>((tiles + pl.tps - 1) / pl.tps);
-  const int NSL = static_cast<int>(Dqk / 64);
-  pl.smem = static_cast<size_t>(NSL) * kSliceBytes + static_cast<size_t>(NSL) * pl.N * 128 +
+  const int NSL = static_cast<int>(Dqk / 64), NMT = static_cast<int>(Dv / 128);
+  const int tc_fit = 512 / pl.N - NMT;  // TMEM columns left for S^T tiles
+  pl.TC = tc_fit < kMaxTC ? tc_fit : kMaxTC;
+  pl.smem = static_cast<size_t>(kRing) * kPairBytes + static_cast<size_t>(NSL) * pl.N * 128 +
             2 * 2 * pl.N * 128 + 1024;
   // keep co-resident CTAs within the SM's 512 TMEM columns
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(8 * pl.N + (Dv / 128) * pl.N)) cols <<= 1;
+  while (cols < static_cast<uint32_t>((pl.TC + NMT) * pl.N)) cols <<= 1;
   // (at most n = 512 / cols CTAs fit the TMEM, so shared memory must keep
   // n + 1 of them from being resident together)
   const size_t per_sm = 227 * 1024;
@@ -644,6 +713,7 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.G = pl.G;
   p.S = pl.S;
   p.tps = pl.tps;
+  p.TC = pl.TC;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.out = a.out;
   p.out_dtype = a.out_dtype;
@@ -654,7 +724,7 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.plse = reinterpret_cast<float*>(
       w + ((static_cast<size_t>(a.B) * pl.S * a.Hq * a.Dv * 4 + 255) & ~size_t(255)));
   const unsigned grid = static_cast<unsigned>(a.B * pl.G * pl.S);
-  auto* kernel = pl.N == 16 ? attn_kernel<16> : attn_kernel<32>;
+  auto* kernel = pl.N == 16 ? attn_kernel<16> : (pl.N == 32 ? attn_kernel<32> : attn_kernel<64>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(pl.smem));
   if (e != cudaSuccess) return e;
