@@ -124,6 +124,32 @@ HSA_DEVINL const uint16_t* slot_row(const AttnParams& p, int b, const SeqGeom& g
   return p.extra + (g.off + j) * p.Dqk;
 }
 
+// slot_row with the list entry for `slot` already loaded (j; ignored for
+// window slots and dense lists).
+HSA_DEVINL const uint16_t* slot_row_j(const AttnParams& p, int b, const SeqGeom& g, int64_t slot,
+                                      int64_t j, bool report) {
+  if (slot < g.n_swa) {
+    const int64_t pos = g.L - g.n_swa + slot;
+    return p.swa + (static_cast<int64_t>(b) * p.W + pos % p.W) * p.Dqk;
+  }
+  const int64_t e = slot - g.n_swa;
+  if (e >= g.n_extra) return nullptr;
+  if (!p.idx) j = e;
+  if (j < 0) return nullptr;
+  if (j >= g.nb) {
+    if (report) set_status(p.status, HSA_DEV_BOUNDS);
+    return nullptr;
+  }
+  return p.extra + (g.off + j) * p.Dqk;
+}
+
+// List entry of slot `slot` (0 when the slot is a window slot or past the list).
+HSA_DEVINL int64_t slot_index(const AttnParams& p, int b, const SeqGeom& g, int64_t slot) {
+  const int64_t e = slot - g.n_swa;
+  return (p.idx && e >= 0 && e < g.n_extra) ? static_cast<int64_t>(p.idx[static_cast<int64_t>(b) * p.k + e])
+                                             : 0;
+}
+
 // Byte offset of element (row, 16-byte chunk) in a 128-byte-swizzled
 // K-major block whose rows are 128 bytes (8-row atoms of 1024 bytes).
 HSA_DEVINL uint32_t sw128(int row, int chunk) {
@@ -246,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
 
   if (tid == 0) {
     for (int i = 0; i < kRing; ++i) {
-      tc::mbar_init(&sh.full[i], kProdThreads);
+      tc::mbar_init(&sh.full[i], 32);
       tc::mbar_init(&sh.empty[i], 1);
     }
     for (int i = 0; i < kMaxTC; ++i) tc::mbar_init(&sh.s_full[i], 1);
@@ -271,66 +297,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
 
   if (warp >= kProdWarp0) {
     // ------------------------------------------------------------ gatherers
-    const int pt_ = tid - kProdWarp0 * 32;
-    // cp.async groups: group 0 is Q, group i + 1 ring item i
-    int64_t issued = 0, retired = 0;
-    auto retire_to = [&](int keep) {
-      if (issued - retired > keep) {
-        tc::cp_async_wait_dyn(keep);
-        tc::fence_proxy_async_smem();
-        while (issued - retired > keep) {
-          tc::mbar_arrive(retired == 0 ? &sh.q_full : &sh.full[(retired - 1) % kRing]);
-          ++retired;
+    // Gather warp w owns ring slot w and every ring item i with i % kRing == w:
+    // it waits for the slot, copies the item, waits for its own copies and
+    // signals the slot, so each slot has one item in flight at all times.
+    static_assert(kProdThreads / 32 == kRing, "one gather warp per ring slot");
+    const int pt_ = tid - kProdWarp0 * 32, pw = warp - kProdWarp0;
+    bool ok = true, q_pending = true;
+    int64_t item = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
+      // every previous item is issued (its rows were read at issue): refill the
+      // tables; a warp that gave up is known to all from here on
+      if (tc::named_barrier_or(2, kProdThreads, !ok)) {
+        ok = false;
+        break;
+      }
+      {
+        constexpr int kPer = (kMaxTC * kKeys + kProdThreads - 1) / kProdThreads;
+        int64_t jv[kPer];
+#pragma unroll
+        for (int k2 = 0; k2 < kPer; ++k2) {  // the list entries first: loads in flight together
+          const int r = pt_ + k2 * kProdThreads;
+          jv[k2] = r < nct * kKeys ? slot_index(p, b, geo, static_cast<int64_t>(tb) * kKeys + r) : 0;
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < kPer; ++k2) {
+          const int r = pt_ + k2 * kProdThreads;
+          if (r < nct * kKeys)
+            sh.rows[r / kKeys][r % kKeys] =
+                slot_row_j(p, b, geo, static_cast<int64_t>(tb) * kKeys + r, jv[k2], true);
         }
       }
-    };
-    auto issue_q = [&]() {
-      const int nq = kN * NSL * 8;
-      for (int i = pt_; i < nq; i += kProdThreads) {
-        const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, c = rem & 7;
-        const bool v = h < p.HG;
-        const uint16_t* src =
-            v ? p.q + (static_cast<int64_t>(b) * p.Hq + g * p.HG + h) * p.Dqk + j * 64 + c * 8 : p.q;
-        tc::cp_async16(qs + j * qslice + sw128(h, c), src, v ? 16u : 0u);
+      tc::named_barrier(2, kProdThreads);
+      if (c == 0) {
+        // Q (every gather thread), landing with each thread's first item
+        const int nq = kN * NSL * 8;
+        for (int i = pt_; i < nq; i += kProdThreads) {
+          const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, cc = rem & 7;
+          const bool v = h < p.HG;
+          const uint16_t* src =
+              v ? p.q + (static_cast<int64_t>(b) * p.Hq + g * p.HG + h) * p.Dqk + j * 64 + cc * 8 : p.q;
+          tc::cp_async16(qs + j * qslice + sw128(h, cc), src, v ? 16u : 0u);
+        }
+        tc::cp_async_commit();
       }
-      tc::cp_async_commit();
-      ++issued;
-    };
-    bool ok = true;
-    int64_t item = 0;
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
-      // every previous item is issued (its rows were read at issue): refill the tables
-      tc::named_barrier(2, kProdThreads);
-      for (int r = pt_; r < nct * kKeys; r += kProdThreads)
-        sh.rows[r / kKeys][r % kKeys] =
-            slot_row(p, b, geo, static_cast<int64_t>(tb + r / kKeys) * kKeys + r % kKeys, true);
-      tc::named_barrier(2, kProdThreads);
-      if (c == 0) issue_q();  // after the first row tables: the key gathers start sooner
       // pass 1: every channel pair of every tile; pass 2: the value pairs again
-      for (int pass = 0; pass < 2 && ok; ++pass) {
+      for (int pass = 0; pass < 2; ++pass) {
         const int nit = pass == 0 ? NP1 : NMT;
-        for (int tc_ = 0; tc_ < nct && ok; ++tc_) {
+        for (int tc_ = 0; tc_ < nct; ++tc_) {
           const uint16_t* const* table = sh.rows[tc_];
           for (int it = 0; it < nit; ++it, ++item) {
-            const int slot = static_cast<int>(item % kRing);
-            bool fail = false;  // (ring item `item` is cp.async group item + 1)
+            if (!ok || item % kRing != pw) continue;
             if (item >= kRing) {
               const uint32_t par = static_cast<uint32_t>((item / kRing - 1) & 1);
-              if (!tc::mbar_test_wait(&sh.empty[slot], par)) {
-                retire_to(0);  // signal everything issued before blocking
-                fail = !wait_or_abort(sh, &sh.empty[slot], par, p.status);
-              }
+              ok = __all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty[pw], par, p.status));
+              if (!ok) continue;
             }
-            if (tc::named_barrier_or(2, kProdThreads, fail)) {
-              ok = false;
-              break;
-            }
-            uint8_t* dst = ring + slot * kPairBytes;
+            uint8_t* dst = ring + pw * kPairBytes;
             for (int half = 0; half < 2; ++half) {
               const int j = 2 * it + half;
               if (j >= NSL) break;
-              for (int q = pt_; q < kKeys * 8; q += kProdThreads) {
+              for (int q = lane; q < kKeys * 8; q += 32) {
                 const int r = q >> 3, cc = q & 7;
                 const uint16_t* row = table[r];
                 tc::cp_async16(dst + half * kSliceBytes + sw128(r, cc), row ? row + j * 64 + cc * 8 : p.q,
@@ -338,13 +365,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
               }
             }
             tc::cp_async_commit();
-            ++issued;
-            retire_to(kRing - 1);
+            tc::cp_async_wait<0>();
+            tc::fence_proxy_async_smem();
+            if (q_pending) {
+              tc::mbar_arrive(&sh.q_full);
+              q_pending = false;
+            }
+            tc::mbar_arrive(&sh.full[pw]);
           }
         }
       }
     }
-    retire_to(0);
+    if (q_pending) {  // a warp without items still owes Q its arrival
+      tc::cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&sh.q_full);
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -443,6 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     };
     for (int c = 0; c < nchunks && ok; ++c) {
       const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
+      // which of this lane's slots are attended, per chunk tile (loads issued before any wait)
+      uint32_t vmask = 0;
+      for (int tc_ = 0; tc_ < nct; ++tc_)
+        vmask |= (slot_row(p, b, geo, static_cast<int64_t>(tb + tc_) * kKeys + tid, false) != nullptr
+                      ? 1u
+                      : 0u)
+                 << tc_;
       // ---- the chunk's maximum per head, each tile folded in as soon as its S^T lands
       float run[kGroups];
 #pragma unroll
@@ -454,8 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         }
         tc::fence_after_sync();
         __syncwarp();
-        const bool valid =
-            slot_row(p, b, geo, static_cast<int64_t>(tb + tc_) * kKeys + tid, false) != nullptr;
+        const bool valid = (vmask >> tc_) & 1u;
 #pragma unroll
         for (int gi = 0; gi < kGroups; ++gi) {
           float x[32];
@@ -516,8 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
             break;
           }
         }
-        const bool valid =
-            slot_row(p, b, geo, static_cast<int64_t>(tb + tc_) * kKeys + tid, false) != nullptr;
+        const bool valid = (vmask >> tc_) & 1u;
         uint8_t* ptb = pt + buf * pbytes + (tid >> 6) * kN * 128;
         const int kc = (tid & 63) >> 3, ke = (tid & 7) << 1;
 #pragma unroll
