@@ -218,22 +218,25 @@ def main():
                     help="skip the standalone top-k rows/s measurement")
     ap.add_argument("--profile", action="store_true",
                     help="profiling run: build the workload, run two layer steps, exit")
+    ap.add_argument("--profile-ctx", type=int, nargs=2, default=None, metavar=("LO", "HI"),
+                    help="with --profile: context lengths ~ U[LO, HI] instead of the bench's "
+                         "(a smaller case of the same layer for multi-pass ncu captures)")
     args = ap.parse_args()
     world, rank, local, dist = dist_setup()
     torch.cuda.set_device(local)
     if args.impl == "reference":
         run_reference(args, world, rank, dist)
     elif args.profile:
-        run_profile()
+        run_profile(args.profile_ctx)
     else:
         run_hsa(args, world, rank, local, dist)
     if dist is not None:
         dist.destroy_process_group()
 
 
-def build_workload(rank):
+def build_workload(rank, ctx=None):
     seed = synth.SEED["c4layer"] + 1000 * rank
-    L = synth.c4_lengths(seed, 64)
+    L = synth.c4_lengths(seed, 64) if ctx is None else synth.c4_lengths(seed, 64, ctx[0], ctx[1])
     g = synth.filled_state(seed, 4, synth.FULL, L, device="cuda")
     return L, g
 
@@ -409,11 +412,11 @@ def run_hsa(args, world, rank, local, dist):
     print(json.dumps(line), flush=True)
 
 
-def run_profile():
+def run_profile(ctx=None):
     """Two layer steps of the bench workload (the first warms up), for ncu."""
     _lib.load(build_if_missing=True)
     shape = synth.FULL
-    L, g = build_workload(0)
+    L, g = build_workload(0, ctx)
     B = L.numel()
     out = torch.empty(B, shape.Hq, shape.Dv, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(B, shape.Hq, dtype=torch.float32, device="cuda")

@@ -20,10 +20,13 @@
 //    128 key rows feeds both MMAs without re-layout:
 //      S^T[key, head] = K_tile . Q^T      (A = K, K-major over Dqk)
 //      O^T[dv, head] += V_tile^T . P^T    (A = the same rows, MN-major view)
-//  * Rows arrive through a ring of three 32 KB pair slots (two 64-channel
+//  * Rows arrive through a ring of four 32 KB pair slots (two 64-channel
 //    slices of 128 rows each, 128-byte swizzled, 16 KB apart = the MN-major
 //    leading-byte offset), filled by three gather warps with 16-byte
-//    cp.async and drained by one MMA-issuing thread.
+//    cp.async (each keeps up to two of its items in flight) and drained by
+//    one MMA-issuing thread.  Q (needed by pass 1 only) and the P^T buffers
+//    (pass 2 only) share one region.
+//  * A token's slots are split over S CTAs in whole 128-slot tiles.
 //  * Two passes per chunk of up to four 128-slot tiles: pass 1 streams all
 //    Dqk channels of the chunk's tiles into S^T accumulators (one per tile,
 //    in TMEM); the softmax warps then take the exact maximum over the chunk,
@@ -47,8 +50,8 @@ constexpr int kSmWarps = 4;
 constexpr int kMmaWarp = 4;
 constexpr int kProdWarp0 = 5;
 constexpr int kProdThreads = 96;
-constexpr int kThreads = 32 * 8;
-constexpr int kRing = 3;            // pair slots
+constexpr int kThreads = 32 * 8;    // (9 warps would cap registers at 168 per thread)
+constexpr int kRing = 4;            // pair slots
 constexpr int kMaxTC = 4;           // tiles per chunk
 constexpr uint32_t kSliceBytes = kKeys * 128;
 constexpr uint32_t kPairBytes = 2 * kSliceBytes;
@@ -66,7 +69,8 @@ struct AttnParams {
   int k;
   int64_t max_rows;       // dense: cap on compressed rows per sequence
   int B, Hq, Dqk, Dv;
-  int HG, G, S, tps, TC;
+  int HG, G, S, TC;
+  int64_t sps;            // attended slots per split
   float scale_log2;
   void* out;
   int out_dtype;
@@ -241,10 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   const int NSL = p.Dqk / 64, NMT = p.Dv / 128, NP1 = (NSL + 1) / 2, TC = p.TC;
   const SeqGeom geo = seq_geom(p, b);
   const int64_t n_slots = geo.n_swa + geo.n_extra;
-  const int n_tiles = static_cast<int>((n_slots + kKeys - 1) / kKeys);
-  const int t0 = s * p.tps;
-  const int t1 = min(t0 + p.tps, n_tiles);
-  const int nt = t1 - t0;
+  // this split's slots [a0, a1), covered by tiles [t0, t1)
+  const int64_t a0 = static_cast<int64_t>(s) * p.sps;
+  const int64_t a1 = min(a0 + p.sps, n_slots);
+  const int t0 = static_cast<int>(a0 / kKeys);
+  const int nt = a1 > a0 ? static_cast<int>((a1 + kKeys - 1) / kKeys) - t0 : 0;
+  const int t1 = t0 + nt;
 
   if (nt <= 0) {  // nothing to attend in this split
     if (tid < kKeys) {
@@ -264,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   const uint32_t qslice = kN * 128;       // bytes of one Q slice (kN heads x 64 channels)
   const uint32_t pbytes = 2 * kN * 128;   // one P^T buffer (2 K-blocks of 64 keys)
   uint8_t* ring = smem;
-  uint8_t* qs = ring + kRing * kPairBytes;
-  uint8_t* pt = qs + NSL * qslice;
+  uint8_t* qs = ring + kRing * kPairBytes;  // Q during pass 1 ...
+  uint8_t* pt = qs;                         // ... and the P^T buffers during pass 2
   // TMEM columns: S^T of chunk tile tc at tc*kN; O^T M-tile m at (TC + m)*kN
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>((TC + NMT) * kN)) tmem_cols <<= 1;
@@ -297,12 +303,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
 
   if (warp >= kProdWarp0) {
     // ------------------------------------------------------------ gatherers
-    // Gather warp w owns ring slot w and every ring item i with i % kRing == w:
-    // it waits for the slot, copies the item, waits for its own copies and
-    // signals the slot, so each slot has one item in flight at all times.
-    static_assert(kProdThreads / 32 == kRing, "one gather warp per ring slot");
+    // Gather warp w issues ring items w, w + 3, w + 6, ... (slot item % kRing)
+    // and keeps up to two of them in flight: its cp.async groups retire in
+    // order, each signalling its slot (or, for a chunk's Q group, q_full).
+    constexpr int kProdWarps = kProdThreads / 32;
     const int pt_ = tid - kProdWarp0 * 32, pw = warp - kProdWarp0;
-    bool ok = true, q_pending = true;
+    bool ok = true;
+    int64_t pend0 = 0, pend1 = 0;  // this warp's unsignalled groups, oldest first (-1: Q)
+    int np = 0;
+    auto signal = [&](int64_t it) { tc::mbar_arrive(it < 0 ? &sh.q_full : &sh.full[it % kRing]); };
+    auto retire_all = [&]() {  // signal each pending group as soon as it has landed
+      if (np == 2) {
+        tc::cp_async_wait<1>();
+        tc::fence_proxy_async_smem();
+        signal(pend0);
+        pend0 = pend1;
+        np = 1;
+      }
+      if (np == 1) {
+        tc::cp_async_wait<0>();
+        tc::fence_proxy_async_smem();
+        signal(pend0);
+        np = 0;
+      }
+    };
+    auto push = [&](int64_t it) {  // right after committing group `it`
+      if (np == 2) {  // three in flight: the oldest must land first
+        tc::cp_async_wait<2>();
+        tc::fence_proxy_async_smem();
+        signal(pend0);
+        pend0 = pend1;
+        np = 1;
+      }
+      if (np == 0) pend0 = it; else pend1 = it;
+      ++np;
+    };
     int64_t item = 0;
     for (int c = 0; c < nchunks; ++c) {
       const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
@@ -323,14 +358,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
 #pragma unroll
         for (int k2 = 0; k2 < kPer; ++k2) {
           const int r = pt_ + k2 * kProdThreads;
+          const int64_t slot = static_cast<int64_t>(tb) * kKeys + r;
           if (r < nct * kKeys)
             sh.rows[r / kKeys][r % kKeys] =
-                slot_row_j(p, b, geo, static_cast<int64_t>(tb) * kKeys + r, jv[k2], true);
+                slot >= a0 && slot < a1 ? slot_row_j(p, b, geo, slot, jv[k2], true) : nullptr;
         }
       }
       tc::named_barrier(2, kProdThreads);
-      if (c == 0) {
-        // Q (every gather thread), landing with each thread's first item
+      {
+        // Q (every gather thread) shares its region with the P^T buffers of the
+        // previous chunk, free once that chunk's last O^T MMAs are done
+        if (c > 0) {
+          const int lt = c * TC - 1;
+          const bool f = !wait_or_abort(sh, &sh.o_done[lt & 1], (lt >> 1) & 1, p.status);
+          if (tc::named_barrier_or(2, kProdThreads, f)) {
+            ok = false;
+            break;
+          }
+        }
         const int nq = kN * NSL * 8;
         for (int i = pt_; i < nq; i += kProdThreads) {
           const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, cc = rem & 7;
@@ -340,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
           tc::cp_async16(qs + j * qslice + sw128(h, cc), src, v ? 16u : 0u);
         }
         tc::cp_async_commit();
+        push(-1);
       }
       // pass 1: every channel pair of every tile; pass 2: the value pairs again
       for (int pass = 0; pass < 2; ++pass) {
@@ -347,51 +393,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         for (int tc_ = 0; tc_ < nct; ++tc_) {
           const uint16_t* const* table = sh.rows[tc_];
           for (int it = 0; it < nit; ++it, ++item) {
-            if (!ok || item % kRing != pw) continue;
+            if (!ok || item % kProdWarps != pw) continue;
+            const int slot = static_cast<int>(item % kRing);
             if (item >= kRing) {
               const uint32_t par = static_cast<uint32_t>((item / kRing - 1) & 1);
-              ok = __all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty[pw], par, p.status));
-              if (!ok) continue;
-            }
-            uint8_t* dst = ring + pw * kPairBytes;
-            for (int half = 0; half < 2; ++half) {
-              const int j = 2 * it + half;
-              if (j >= NSL) break;
-              for (int q = lane; q < kKeys * 8; q += 32) {
-                const int r = q >> 3, cc = q & 7;
-                const uint16_t* row = table[r];
-                tc::cp_async16(dst + half * kSliceBytes + sw128(r, cc), row ? row + j * 64 + cc * 8 : p.q,
-                               row ? 16u : 0u);
+              if (!tc::mbar_test_wait(&sh.empty[slot], par)) {
+                retire_all();  // signal everything issued before blocking
+                ok = __all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty[slot], par, p.status));
+                if (!ok) continue;
               }
             }
-            tc::cp_async_commit();
-            tc::cp_async_wait<0>();
-            tc::fence_proxy_async_smem();
-            if (q_pending) {
-              tc::mbar_arrive(&sh.q_full);
-              q_pending = false;
+            // lane: 16-byte chunk cc of rows r0 + 4k (k < 32) of both slices of the pair
+            const uint32_t dst = tc::smem_u32(ring + slot * kPairBytes);
+            const int cc = lane & 7, r0 = lane >> 3, j0 = 2 * it;
+            const bool two = j0 + 1 < NSL;
+#pragma unroll 4
+            for (int k = 0; k < kKeys / 4; ++k) {
+              const int r = r0 + 4 * k;
+              const uint16_t* row = table[r];
+              const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
+              const uint16_t* src = row ? row + j0 * 64 + cc * 8 : p.q;
+              const uint32_t nb = row ? 16u : 0u;
+              tc::cp_async16_s(dst + off, src, nb);
+              if (two) tc::cp_async16_s(dst + kSliceBytes + off, row ? src + 64 : p.q, nb);
             }
-            tc::mbar_arrive(&sh.full[pw]);
+            tc::cp_async_commit();
+            push(item);
           }
         }
       }
+      retire_all();  // the chunk's Q and items are all signalled
     }
-    if (q_pending) {  // a warp without items still owes Q its arrival
-      tc::cp_async_wait<0>();
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&sh.q_full);
-    }
+    retire_all();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idS = tc::idesc_bf16_f32(kKeys, kN);
       const uint32_t idO = tc::idesc_bf16_f32(kKeys, kN, /*a_mn=*/true, /*b_mn=*/false);
-      bool ok = wait_or_abort(sh, &sh.q_full, 0, p.status);
+      bool ok = true;
       int64_t item = 0;
       int gt = 0;  // tiles through pass 2 so far (P^T buffer gt & 1)
       for (int c = 0; c < nchunks && ok; ++c) {
         const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
         if (c > 0 && !wait_or_abort(sh, &sh.s_empty, (c - 1) & 1, p.status)) {
+          ok = false;
+          break;
+        }
+        if (!wait_or_abort(sh, &sh.q_full, c & 1, p.status)) {
           ok = false;
           break;
         }
@@ -481,11 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
       // which of this lane's slots are attended, per chunk tile (loads issued before any wait)
       uint32_t vmask = 0;
-      for (int tc_ = 0; tc_ < nct; ++tc_)
-        vmask |= (slot_row(p, b, geo, static_cast<int64_t>(tb + tc_) * kKeys + tid, false) != nullptr
-                      ? 1u
-                      : 0u)
+      for (int tc_ = 0; tc_ < nct; ++tc_) {
+        const int64_t slot = static_cast<int64_t>(tb + tc_) * kKeys + tid;
+        vmask |= (slot >= a0 && slot < a1 && slot_row(p, b, geo, slot, false) != nullptr ? 1u : 0u)
                  << tc_;
+      }
       // ---- the chunk's maximum per head, each tile folded in as soon as its S^T lands
       float run[kGroups];
 #pragma unroll
@@ -706,13 +754,15 @@ AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, in
   int64_t S = device_sms() / (B * pl.G);
   if (S < 1) S = 1;
   if (S > tiles) S = tiles;
-  pl.tps = static_cast<int>((tiles + S - 1) / S);
-  pl.S = static_cast<int>((tiles + pl.tps - 1) / pl.tps);
+  // whole tiles per split: a masked slot costs the gather as much as a live one
+  const int64_t tps = (tiles + S - 1) / S;
+  pl.sps = tps * kKeys;
+  pl.S = static_cast<int>((tiles + tps - 1) / tps);
   const int NSL = static_cast<int>(Dqk / 64), NMT = static_cast<int>(Dv / 128);
   const int tc_fit = 512 / pl.N - NMT;  // TMEM columns left for S^T tiles
   pl.TC = tc_fit < kMaxTC ? tc_fit : kMaxTC;
-  pl.smem = static_cast<size_t>(kRing) * kPairBytes + static_cast<size_t>(NSL) * pl.N * 128 +
-            2 * 2 * pl.N * 128 + 1024;
+  const size_t q_bytes = static_cast<size_t>(NSL) * pl.N * 128, p_bytes = 2 * 2 * pl.N * 128;
+  pl.smem = static_cast<size_t>(kRing) * kPairBytes + (q_bytes > p_bytes ? q_bytes : p_bytes) + 1024;
   // keep co-resident CTAs within the SM's 512 TMEM columns
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>((pl.TC + NMT) * pl.N)) cols <<= 1;
@@ -753,7 +803,7 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.HG = pl.HG;
   p.G = pl.G;
   p.S = pl.S;
-  p.tps = pl.tps;
+  p.sps = pl.sps;
   p.TC = pl.TC;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.out = a.out;

@@ -94,10 +94,11 @@ struct AttnArgs {
 };
 
 // Launch geometry of the fused attention: HG heads per CTA (N = MMA width),
-// G head groups, S key splits of tps 128-key tiles, TC tiles per chunk (S^T
-// accumulators held in TMEM at once), dynamic shared memory.
+// G head groups, S key splits of sps attended slots each, TC tiles per chunk
+// (S^T accumulators held in TMEM at once), dynamic shared memory.
 struct AttnPlan {
-  int HG, N, G, S, tps, TC;
+  int HG, N, G, S, TC;
+  int64_t sps;
   size_t smem;
 };
 
