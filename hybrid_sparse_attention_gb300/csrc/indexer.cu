@@ -32,10 +32,12 @@ namespace {
 
 constexpr int kTileRows = 128;  // M
 constexpr int kQRows = 16;      // N (heads, padded)
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kMaxSeqs = 4096;  // tile prefix table in shared memory
-constexpr uint32_t kTmemCols = 32;  // two 16-column accumulators
+constexpr int kMaxSeqs = 4096;  // tile prefix table (built in a stage buffer before the ring starts)
+constexpr int kAcc = 4;         // accumulators in TMEM (tiles the MMA may run ahead of the epilogue)
+constexpr int kParts = 4;           // independent partial accumulators per tile
+constexpr uint32_t kTmemCols = kAcc * kParts * kQRows;
 
 struct IndexerParams {
   const float* w;  // [B, Hi]
@@ -47,12 +49,12 @@ struct IndexerParams {
 
 struct Shared {
   uint64_t full[kStages], empty[kStages];
-  uint64_t acc_full[2], acc_empty[2];
+  uint64_t acc_full[kAcc], acc_empty[kAcc];
   uint64_t fin;
   uint32_t tmem;
   int abort;
   int ntiles;
-  int prefix[kMaxSeqs + 1];  // tiles before sequence b
+  int b0, first0;  // sequence owning this CTA's first tile, and its first tile
 };
 
 // Bounded wait that also gives up when another role has aborted.
@@ -72,15 +74,33 @@ HSA_DEVINL bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity, uint32
   }
 }
 
-// Sequence owning global tile t (largest b with prefix[b] <= t).
-HSA_DEVINL int tile_seq(const Shared& sh, int B, int t) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (sh.prefix[mid] <= t) lo = mid; else hi = mid - 1;
+// Walks a CTA's contiguous range of tiles in order, keeping the owning
+// sequence's first tile, pool start and live count in registers: a new
+// sequence costs a few loads, a tile none, so no tile waits on a global load.
+struct SeqCursor {
+  int b = -1;
+  int first = 0, next = 0;  // tiles [first, next) belong to sequence b
+  int64_t start = 0, count = 0;
+  HSA_DEVINL void load(const IndexerParams& p) {
+    start = p.sp.start(b);
+    count = p.sp.count(b);
+    next = first + static_cast<int>((count + kTileRows - 1) / kTileRows);
   }
-  return lo;
-}
+  HSA_DEVINL bool seek(const Shared& sh, const IndexerParams& p, int t) {
+    if (b >= 0 && t < next) return false;
+    if (b < 0) {
+      b = sh.b0;
+      first = sh.first0;
+      load(p);
+    }
+    while (t >= next) {  // (empty sequences own no tiles and are stepped over)
+      ++b;
+      first = next;
+      load(p);
+    }
+    return true;  // moved to a new sequence
+  }
+};
 
 __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap qmap,
@@ -91,27 +111,6 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
   pdl_trigger();
   pdl_wait();
 
-  // tiles per sequence -> prefix table (block-wide scan in chunks of blockDim)
-  __shared__ int s_scan[33];
-  int carry = 0;
-  for (int base = 0; base < p.B; base += kThreads) {
-    const int b = base + threadIdx.x;
-    const int nt = b < p.B ? static_cast<int>((p.sp.count(b) + kTileRows - 1) / kTileRows) : 0;
-    int total;
-    const int incl = block_inclusive_sum<int>(nt, s_scan, &total);
-    if (b < p.B) sh.prefix[b] = carry + incl - nt;
-    carry += total;
-  }
-  if (threadIdx.x == 0) {
-    sh.prefix[p.B] = carry;
-    sh.ntiles = carry;
-  }
-  __syncthreads();
-  const int ntiles = sh.ntiles;
-  const int t_begin = static_cast<int>(static_cast<int64_t>(ntiles) * blockIdx.x / gridDim.x);
-  const int t_end = static_cast<int>(static_cast<int64_t>(ntiles) * (blockIdx.x + 1) / gridDim.x);
-  if (t_begin >= t_end) return;
-
   const int kb_elems = p.Di >= 64 ? 64 : p.Di;  // elements of one swizzle row
   const int nkb = p.Di / kb_elems;
   const uint32_t a_kb = kTileRows * kb_elems * 2, b_kb = kQRows * kb_elems * 2;
@@ -119,12 +118,47 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
 
+  // tiles per sequence -> prefix table (block-wide scan in chunks of blockDim),
+  // kept in the (not yet used) stage buffers just long enough to find the
+  // sequence owning this CTA's first tile
+  int* prefix = reinterpret_cast<int*>(smem);
+  __shared__ int s_scan[33];
+  int carry = 0;
+  for (int base = 0; base < p.B; base += kThreads) {
+    const int b = base + threadIdx.x;
+    const int nt = b < p.B ? static_cast<int>((p.sp.count(b) + kTileRows - 1) / kTileRows) : 0;
+    int total;
+    const int incl = block_inclusive_sum<int>(nt, s_scan, &total);
+    if (b < p.B) prefix[b] = carry + incl - nt;
+    carry += total;
+    __syncthreads();  // s_scan is reused by the next chunk
+  }
+  if (threadIdx.x == 0) {
+    prefix[p.B] = carry;
+    sh.ntiles = carry;
+  }
+  __syncthreads();
+  const int ntiles = sh.ntiles;
+  const int t_begin = static_cast<int>(static_cast<int64_t>(ntiles) * blockIdx.x / gridDim.x);
+  const int t_end = static_cast<int>(static_cast<int64_t>(ntiles) * (blockIdx.x + 1) / gridDim.x);
+  if (t_begin >= t_end) return;
+  if (threadIdx.x == 0) {
+    int lo = 0, hi = p.B - 1;  // largest b with prefix[b] <= t_begin
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= t_begin) lo = mid; else hi = mid - 1;
+    }
+    sh.b0 = lo;
+    sh.first0 = prefix[lo];
+  }
+  __syncthreads();  // the stage buffers are free again
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&sh.full[s], 1);
       tc::mbar_init(&sh.empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kAcc; ++a) {
       tc::mbar_init(&sh.acc_full[a], 1);
       tc::mbar_init(&sh.acc_empty[a], 128);
     }
@@ -146,13 +180,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
     if (lane == 0) {
       tc::tma_prefetch_map(&kmap);
       tc::tma_prefetch_map(&qmap);
+      SeqCursor cur;
       for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
         const int s = i % kStages;
+        cur.seek(sh, p, t);  // before the wait: a new sequence's loads overlap it
         if (i >= kStages &&
             !wait_or_abort(sh, &sh.empty[s], ((i / kStages) & 1) ^ 1, p.status))
           break;
-        const int b = tile_seq(sh, p.B, t);
-        const int64_t row0 = p.sp.start(b) + static_cast<int64_t>(t - sh.prefix[b]) * kTileRows;
+        const int b = cur.b;
+        const int64_t row0 = cur.start + static_cast<int64_t>(t - cur.first) * kTileRows;
         uint8_t* st = smem + s * stage_bytes;
         tc::mbar_arrive_expect_tx(&sh.full[s], stage_bytes);
         for (int kb = 0; kb < nkb; ++kb) {
@@ -170,17 +206,21 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
       const uint32_t sbo = 8 * kb_elems * 2;  // bytes between 8-row groups
       const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, kQRows);
       for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
-        const int s = i % kStages, a = i & 1;
+        const int s = i % kStages, a = i % kAcc;
         if (!wait_or_abort(sh, &sh.full[s], (i / kStages) & 1, p.status)) break;
-        if (i >= 2 && !wait_or_abort(sh, &sh.acc_empty[a], ((i >> 1) & 1) ^ 1, p.status)) break;
+        if (i >= kAcc && !wait_or_abort(sh, &sh.acc_empty[a], ((i / kAcc) & 1) ^ 1, p.status))
+          break;
         tc::fence_after_sync();
         const uint32_t sa = tc::smem_u32(smem + s * stage_bytes);
         const uint32_t sb = sa + nkb * a_kb;
+        // K-step kk accumulates into partial kk % kParts: chains of small-N
+        // MMAs on one accumulator would serialize
         for (int kb = 0; kb < nkb; ++kb) {
           for (int ks = 0; ks < kb_elems / 16; ++ks) {
+            const int kk = kb * (kb_elems / 16) + ks;
             const uint64_t da = tc::smem_desc(sa + kb * a_kb + ks * 32, 16, sbo, sw);
             const uint64_t db = tc::smem_desc(sb + kb * b_kb + ks * 32, 16, sbo, sw);
-            tc::mma_bf16(tmem + a * kQRows, da, db, idesc, (kb | ks) != 0);
+            tc::mma_bf16(tmem + (a * kParts + kk % kParts) * kQRows, da, db, idesc, kk >= kParts);
           }
         }
         tc::mma_commit(&sh.empty[s]);
@@ -193,30 +233,40 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;
+    const int nparts = p.Di / 16 < kParts ? p.Di / 16 : kParts;  // partials in use
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    SeqCursor cur;
+    float wv[kQRows];
     for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
-      const int a = i & 1;
-      const int b = tile_seq(sh, p.B, t);
-      const int64_t piece = t - sh.prefix[b];
-      const int64_t left = p.sp.count(b) - piece * kTileRows;
-      const int64_t row = p.sp.start(b) + piece * kTileRows + r;
-      float wv[kQRows];
+      const int a = i % kAcc;
+      if (cur.seek(sh, p, t)) {
 #pragma unroll
-      for (int h = 0; h < kQRows; ++h)
-        wv[h] = h < p.Hi ? __ldg(p.w + static_cast<int64_t>(b) * p.Hi + h) : 0.f;
-      const bool ok = wait_or_abort(sh, &sh.acc_full[a], (i >> 1) & 1, p.status);
+        for (int h = 0; h < kQRows; ++h)
+          wv[h] = h < p.Hi ? __ldg(p.w + static_cast<int64_t>(cur.b) * p.Hi + h) : 0.f;
+      }
+      const int64_t piece = t - cur.first;
+      const int64_t left = cur.count - piece * kTileRows;
+      const int64_t row = cur.start + piece * kTileRows + r;
+      const bool ok = wait_or_abort(sh, &sh.acc_full[a], (i / kAcc) & 1, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::fence_after_sync();
-      uint32_t acc[16];
-      tc::tmem_ld16(tmem + lane_addr + a * kQRows, acc);
-      tc::tmem_ld_wait();
+      float dot[kQRows];
+#pragma unroll
+      for (int h = 0; h < kQRows; ++h) dot[h] = 0.f;
+      for (int pa = 0; pa < nparts; ++pa) {
+        uint32_t acc[16];
+        tc::tmem_ld16(tmem + lane_addr + (a * kParts + pa) * kQRows, acc);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < kQRows; ++h) dot[h] += __uint_as_float(acc[h]);
+      }
       tc::fence_before_sync();
       tc::mbar_arrive(&sh.acc_empty[a]);
       if (r < left) {
         float sc = 0.f;
 #pragma unroll
         for (int h = 0; h < kQRows; ++h)
-          if (h < p.Hi) sc = fmaf(wv[h], fmaxf(__uint_as_float(acc[h]), 0.f), sc);
+          if (h < p.Hi) sc = fmaf(wv[h], fmaxf(dot[h], 0.f), sc);
         p.scores[row] = sc;
       }
     }
