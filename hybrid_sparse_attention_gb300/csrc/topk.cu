@@ -15,24 +15,25 @@
 // orders elements exactly as the result requires, so selection and the final
 // sort work on composites.
 //
-// Every row is cut into chunks of CH scores, one CTA per chunk, so each row
-// spreads over many SMs (two launches):
+// Rows of at most 32,768 scores (every C4 row up to a 128K context) take one
+// launch: a thread-block cluster per row (see "short rows" below).
+//
+// Otherwise every row is cut into chunks of CH scores (about one chunk per
+// SM), one CTA per chunk, in two launches:
 //   1. histogram: each CTA histograms the top 11 key bits (digit 1) of its
-//      chunk in shared memory and adds the non-zero bins into the row's
-//      global histogram.  The row's last CTA to finish (atomic ticket, no
-//      waiting) scans it from the top for the threshold digit d1: fewer than
-//      k keys lie above bin d1, at least k at or above it.
-//   2. select: each CTA re-reads its chunk (from L2: it was just read) and,
-//      4,096 scores at a time, counts keys above d1 (certain winners) and in
-//      bin d1 (candidates) per warp by ballots, reserves room in the row's
-//      global lists with one atomic per list and writes its composites there.
-//      Candidates also add their next 11 key bits (digit 2) to a second row
-//      histogram.  The row's last CTA then needs no pass over the row: digit
-//      2's histogram splits the candidates into more winners and a (usually
-//      tiny) set at the boundary, a radix select over the remaining 42 bits
-//      settles those, and the k survivors are sorted (bitonic runs of 32 in
-//      each warp, merged by binary-search ranking) and written.  It leaves
-//      the row's workspace zeroed.
+//      chunk in shared memory (16-byte loads) and adds the non-zero bins into
+//      the row's global histogram.  The row's last CTA to finish (atomic
+//      ticket, no waiting) scans it from the top for the threshold digit d1:
+//      fewer than k keys lie above bin d1, at least k at or above it.
+//   2. select: each warp re-reads its share of the chunk (from L2: it was
+//      just read) and keeps every key at or above bin d1 as a composite,
+//      written over the share's own positions of the workspace, with its
+//      count: no atomics, no reservations.  The row's last CTA gathers the
+//      lists (keys above bin d1 are winners, keys in it candidates), picks
+//      the missing winners by a radix select over the candidates' other 53
+//      composite bits, sorts the k survivors (bitonic runs of 32 in each
+//      warp, merged by binary-search ranking) and writes them.  It leaves the
+//      row's workspace zeroed.
 #include "common.cuh"
 #include "internal.h"
 
@@ -43,10 +44,9 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;       // 11-bit digits
 constexpr int kShift1 = 21;       // digit 1: key bits 31..21
-constexpr int kShift2 = 10;       // digit 2: key bits 20..10
 constexpr int kMaxK = 2048;       // final sort buffer
 constexpr int kSmemCand = 2560;   // boundary candidates staged in shared memory when they fit
-constexpr int kBlockU = 8;        // scores per thread per compaction block
+constexpr int kMinChunk = 4096;   // scores per CTA of the chunked passes, at least
 constexpr int kFastSort = kThreads;  // survivors ranked by warp runs + merge up to this many
 
 HSA_DEVINL uint32_t order_key(uint32_t u) {
@@ -61,33 +61,31 @@ HSA_DEVINL uint64_t composite(uint32_t key, uint32_t j) {
 }
 
 struct RowState {
-  uint32_t n_win;    // certain winners compacted so far
-  uint32_t n_cand;   // candidates (bin d1) compacted so far
+  uint32_t n_cand;   // clustered path, heavy ties: candidates written to the workspace
   uint32_t done1;    // CTAs finished with pass 1
   uint32_t done2;    // CTAs finished with pass 2
   uint32_t digit;    // threshold digit d1 (pass 1 result)
-  uint32_t pad[3];
 };
 
 struct Ws {
   uint32_t* status;
-  RowState* rows;   // [B]
-  uint32_t* hist;   // [B][kBins] digit 1
-  uint32_t* hist2;  // [B][kBins] digit 2 of the candidates
-  uint64_t* win;    // [B][k]
-  uint64_t* cand;   // [total_rows], row b uses [offsets[b], offsets[b] + N_b)
+  RowState* rows;    // [B]
+  uint32_t* hist;    // [B][kBins] digit 1
+  uint32_t* wcount;  // [chunks][kWarps] pass 2: composites each warp kept
+  uint64_t* cand;    // [total_rows], row b uses [offsets[b], offsets[b] + N_b)
 };
 
-HSA_HOST_DEVICE size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t rows, hist, hist2, win, cand, total;
-  HSA_HOST_DEVICE WsLayout(int64_t B, int64_t total_rows, int64_t k) {
+  size_t rows, hist, wcount, cand, total;
+  WsLayout(int64_t B, int64_t total_rows, int64_t /*k*/) {
+    // chunks are at least kMinChunk scores, plus at most one partial chunk per row
+    const int64_t chunks = total_rows / kMinChunk + 1 + B;
     rows = kWsHeader;
     hist = rows + align256(sizeof(RowState) * B);
-    hist2 = hist + align256(sizeof(uint32_t) * kBins * B);
-    win = hist2 + align256(sizeof(uint32_t) * kBins * B);
-    cand = win + align256(sizeof(uint64_t) * k * B);
+    wcount = hist + align256(sizeof(uint32_t) * kBins * B);
+    cand = wcount + align256(sizeof(uint32_t) * kWarps * chunks);
     total = cand + align256(sizeof(uint64_t) * (total_rows > 0 ? total_rows : 1));
   }
 };
@@ -98,8 +96,7 @@ Ws ws_view(void* base, int64_t B, int64_t total_rows, int64_t k, uint32_t* statu
   return Ws{status,
             reinterpret_cast<RowState*>(p + L.rows),
             reinterpret_cast<uint32_t*>(p + L.hist),
-            reinterpret_cast<uint32_t*>(p + L.hist2),
-            reinterpret_cast<uint64_t*>(p + L.win),
+            reinterpret_cast<uint32_t*>(p + L.wcount),
             reinterpret_cast<uint64_t*>(p + L.cand)};
 }
 
@@ -163,7 +160,7 @@ HSA_DEVINL uint32_t find_digit(const uint32_t* hist, uint32_t nb, uint32_t need,
 
 // ---------------------------------------------------------------- pass 1
 
-__global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __restrict__ scores,
+__global__ void __launch_bounds__(kThreads, 2) topk_hist_kernel(const float* __restrict__ scores,
                                                             Spans sp, int B, int k,
                                                             int64_t chunk, Ws ws) {
   __shared__ uint32_t s_hist[kBins];
@@ -185,8 +182,37 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
   const uint32_t* base = reinterpret_cast<const uint32_t*>(scores + sp.start(row));
   const int64_t lo = piece * chunk, hi = min(n, lo + chunk);
   bool nan = false;
-  constexpr int kU = 16;  // loads in flight per thread
-  for (int64_t i0 = lo + threadIdx.x; i0 < hi; i0 += kThreads * kU) {
+  auto count_key = [&](uint32_t u) {
+    nan |= is_nan_bits(u);
+    atomicAdd(&s_hist[order_key(u) >> kShift1], 1u);
+  };
+  // 16-byte loads when the chunk starts 16-byte aligned (eight in flight per thread)
+  int64_t done = lo;
+  if ((reinterpret_cast<uintptr_t>(base + lo) & 15u) == 0) {
+    const int64_t nv = (hi - lo) >> 2;
+    const uint4* b4 = reinterpret_cast<const uint4*>(base + lo);
+    constexpr int kV = 8;
+    for (int64_t v0 = threadIdx.x; v0 < nv; v0 += kThreads * kV) {
+      uint4 w[kV];
+#pragma unroll
+      for (int j = 0; j < kV; ++j) {
+        const int64_t v = v0 + j * kThreads;
+        w[j] = v < nv ? __ldcg(b4 + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < kV; ++j) {
+        if (v0 + j * kThreads < nv) {
+          count_key(w[j].x);
+          count_key(w[j].y);
+          count_key(w[j].z);
+          count_key(w[j].w);
+        }
+      }
+    }
+    done = lo + nv * 4;
+  }
+  constexpr int kU = 16;  // scalar loads in flight per thread
+  for (int64_t i0 = done + threadIdx.x; i0 < hi; i0 += kThreads * kU) {
     uint32_t u[kU];
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
@@ -194,12 +220,8 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
       u[j] = i < hi ? __ldcg(base + i) : 0u;
     }
 #pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      if (i0 + j * kThreads < hi) {
-        nan |= is_nan_bits(u[j]);
-        atomicAdd(&s_hist[order_key(u[j]) >> kShift1], 1u);
-      }
-    }
+    for (int j = 0; j < kU; ++j)
+      if (i0 + j * kThreads < hi) count_key(u[j]);
   }
   if (nan) set_status(ws.status, HSA_DEV_NAN);
   __syncthreads();
@@ -281,13 +303,14 @@ HSA_DEVINL uint32_t rank_desc(const uint64_t* a, int n, uint64_t* s_run, uint64_
   return rank;
 }
 
-// Appends to out[*count ...] the `need` largest of the composites cand[0..n),
-// which all agree above their low `low_bits` bits: radix select with 11-bit
-// digits from the top.  Composites are unique, so the boundary is exact.
+// Appends to out[*count ...] the `need` largest of the composites cand[0..n)
+// that match prefix on mask and all agree above their low `low_bits` bits:
+// radix select with 11-bit digits from the top.  Composites are unique, so
+// the boundary is exact.
 HSA_DEVINL void select_rest(const uint64_t* cand, uint32_t n, uint32_t need, uint64_t* out,
                             uint32_t* count, uint32_t cap, uint32_t* s_hist, uint32_t* s_scan,
-                            uint32_t* s_out, int low_bits) {
-  uint64_t prefix = 0, mask = 0;
+                            uint32_t* s_out, int low_bits, uint64_t prefix = 0, uint64_t mask = 0) {
+  // (composites not matching prefix on mask are not candidates and are skipped)
   int rest = low_bits;
   while (need > 0 && rest > 0) {
     const int width = rest >= 11 ? 11 : rest;
@@ -568,16 +591,21 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
 
 // ---------------------------------------------------------------- pass 2
 
-__global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __restrict__ scores,
+// Warp w of a chunk's CTA keeps, from its contiguous share of the chunk,
+// every score at or above bin d1 (every score when the row has at most k)
+// as a composite, written to the row's workspace over the share's own
+// positions (a share never keeps more than it holds), and records how many.
+// No atomics.  The row's last CTA gathers those lists, settles the boundary
+// and sorts.
+__global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* __restrict__ scores,
                                                               Spans sp, int B, int k,
                                                               int64_t chunk, Ws ws,
                                                               int32_t* __restrict__ idx_out,
                                                               float* __restrict__ vals_out) {
   __shared__ uint64_t s_sel[kMaxK];
   __shared__ uint64_t s_cand[kSmemCand];
-  __shared__ uint32_t s_hist[kBins];
-  __shared__ uint32_t s_scan[33], s_out[2];
-  __shared__ uint32_t s_wt[kWarps], s_ct[kWarps], s_gw, s_gc, s_count, s_ccount;
+  __shared__ uint32_t s_hist[kBins];  // list offsets, then select scratch
+  __shared__ uint32_t s_scan[33], s_out[2], s_count, s_ccount;
   __shared__ int s_last;
   pdl_trigger();
   pdl_wait();
@@ -591,65 +619,60 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __re
   const uint32_t d1 = all ? 0u : __ldcg(&ws.rows[row].digit);
   const int64_t off = sp.start(row);
   const uint32_t* base = reinterpret_cast<const uint32_t*>(scores + off);
-  uint64_t* win = ws.win + static_cast<int64_t>(row) * k;
-  uint64_t* cand = ws.cand + off;
-  uint32_t* gh2 = ws.hist2 + static_cast<int64_t>(row) * kBins;
   RowState* rs = ws.rows + row;
   const int64_t lo = piece * chunk, hi = min(n, lo + chunk);
-  for (int64_t b0 = lo; b0 < hi; b0 += kThreads * kBlockU) {
-    // one block of kThreads * kBlockU scores: classify, count per warp
-    uint32_t key[kBlockU], mw[kBlockU], mc[kBlockU];
+  const int64_t wsub = chunk / kWarps;
+  const int64_t wlo = lo + warp * wsub, whi = min(hi, wlo + wsub);
+  {
+    uint64_t* dst = ws.cand + off + wlo;
+    uint32_t cnt = 0;
+    auto keep = [&](uint32_t u, int64_t i, bool in) {
+      const uint32_t key = order_key(u);
+      const bool take = in && (all || (key >> kShift1) >= d1);
+      const uint32_t m = __ballot_sync(0xffffffffu, take);
+      if (take) dst[cnt + __popc(m & lt)] = composite(key, static_cast<uint32_t>(i));
+      cnt += __popc(m);
+    };
+    int64_t done = wlo;
+    if (wlo < whi && (reinterpret_cast<uintptr_t>(base + wlo) & 15u) == 0) {
+      // 16-byte loads, eight in flight per lane (the trip count is the warp's)
+      const int64_t nv = (whi - wlo) >> 2;
+      const uint4* b4 = reinterpret_cast<const uint4*>(base + wlo);
+      constexpr int kV = 8;
+      for (int64_t v0 = 0; v0 < nv; v0 += 32 * kV) {
+        uint4 w[kV];
 #pragma unroll
-    for (int j = 0; j < kBlockU; ++j) {
-      const int64_t i = b0 + j * kThreads + t;
-      key[j] = i < hi ? order_key(__ldcg(base + i)) : 0u;
-    }
-    uint32_t tw = 0, tc = 0;
+        for (int j = 0; j < kV; ++j) {
+          const int64_t v = v0 + j * 32 + lane;
+          w[j] = v < nv ? __ldcg(b4 + v) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-    for (int j = 0; j < kBlockU; ++j) {
-      const bool in = b0 + j * kThreads + t < hi;
-      const uint32_t dig = key[j] >> kShift1;
-      mw[j] = __ballot_sync(0xffffffffu, in && (all || dig > d1));
-      mc[j] = __ballot_sync(0xffffffffu, in && !all && dig == d1);
-      tw += __popc(mw[j]);
-      tc += __popc(mc[j]);
-    }
-    if (lane == 0) {
-      s_wt[warp] = tw;
-      s_ct[warp] = tc;
-    }
-    __syncthreads();
-    if (t == 0) {
-      // exclusive prefix over warps, then one reservation per list
-      uint32_t sw = 0, sc = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        const uint32_t a = s_wt[w], c = s_ct[w];
-        s_wt[w] = sw;
-        s_ct[w] = sc;
-        sw += a;
-        sc += c;
+        for (int j = 0; j < kV; ++j) {
+          const int64_t v = v0 + j * 32 + lane;
+          const bool in = v < nv;
+          const int64_t i = wlo + 4 * v;
+          keep(w[j].x, i, in);
+          keep(w[j].y, i + 1, in);
+          keep(w[j].z, i + 2, in);
+          keep(w[j].w, i + 3, in);
+        }
       }
-      s_gw = sw ? atomicAdd(&rs->n_win, sw) : 0u;
-      s_gc = sc ? atomicAdd(&rs->n_cand, sc) : 0u;
+      done = wlo + nv * 4;
     }
-    __syncthreads();
-    uint32_t pw = s_gw + s_wt[warp], pc = s_gc + s_ct[warp];
+    for (int64_t i0 = done; i0 < whi; i0 += 32 * 8) {
+      uint32_t u[8];
 #pragma unroll
-    for (int j = 0; j < kBlockU; ++j) {
-      const uint32_t i = static_cast<uint32_t>(b0 - lo) + j * kThreads + t;  // < chunk
-      const uint64_t x = composite(key[j], static_cast<uint32_t>(lo) + i);
-      if (mw[j] >> lane & 1u) {
-        const uint32_t p = pw + __popc(mw[j] & lt);
-        if (p < static_cast<uint32_t>(k)) win[p] = x;
+      for (int j = 0; j < 8; ++j) {
+        const int64_t i = i0 + j * 32 + lane;
+        u[j] = i < whi ? __ldcg(base + i) : 0u;
       }
-      if (mc[j] >> lane & 1u) {
-        cand[pc + __popc(mc[j] & lt)] = x;
-        atomicAdd(gh2 + ((key[j] >> kShift2) & (kBins - 1)), 1u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t i = i0 + j * 32 + lane;
+        keep(u[j], i, i < whi);
       }
-      pw += __popc(mw[j]);
-      pc += __popc(mc[j]);
     }
-    __syncthreads();  // s_wt / s_ct are rewritten by the next block
+    if (lane == 0) ws.wcount[static_cast<int64_t>(blockIdx.x) * kWarps + warp] = cnt;
   }
   __threadfence();
   __syncthreads();
@@ -658,53 +681,80 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __re
   if (!s_last) return;
   __threadfence();
 
-  // ---- the row's last CTA: finish the selection and write the result
+  // ---- the row's last CTA: gather the lists, finish the selection, write the result
   const uint32_t kk = static_cast<uint32_t>(n < k ? n : k);
-  const uint32_t n_win = __ldcg(&rs->n_win);
-  const uint32_t n_cand = __ldcg(&rs->n_cand);
-  const uint32_t n_win_c = n_win < kk ? n_win : kk;  // defensive clamp
-  for (uint32_t i = t; i < n_win_c; i += kThreads) s_sel[i] = __ldcg(win + i);
+  const int64_t first_blk = static_cast<int64_t>(blockIdx.x) - piece;
+  const int64_t nl = npieces * kWarps;
+  // visits every kept composite once, list by list (lists in kThreads-sized
+  // groups: counts scanned into offsets), as fn(x, e) with e its rank in that order
+  auto for_each_kept = [&](auto&& fn) {
+    uint32_t carry = 0;
+    for (int64_t l0 = 0; l0 < nl; l0 += kThreads) {
+      const int64_t l = l0 + t;
+      const uint32_t c = l < nl ? __ldcg(ws.wcount + first_blk * kWarps + l) : 0u;
+      uint32_t tot;
+      const uint32_t incl = block_inclusive_sum<uint32_t>(c, s_scan, &tot);
+      s_hist[t] = incl - c;
+      __syncthreads();
+      const int nlc = static_cast<int>(nl - l0 < kThreads ? nl - l0 : kThreads);
+      for (uint32_t e0 = 0; e0 < tot; e0 += kThreads) {
+        const uint32_t e = e0 + t;
+        uint64_t x = 0;
+        if (e < tot) {
+          int a = 0, z = nlc - 1;  // the last list starting at or before e
+          while (a < z) {
+            const int mid = (a + z + 1) >> 1;
+            if (s_hist[mid] <= e) a = mid; else z = mid - 1;
+          }
+          const int64_t lg = l0 + a;
+          x = __ldcg(ws.cand + off + (lg / kWarps) * chunk + (lg % kWarps) * wsub + (e - s_hist[a]));
+        }
+        fn(x, e < tot, carry + e);
+      }
+      __syncthreads();  // s_hist and s_scan are reused by the next group
+      carry += tot;
+    }
+  };
   if (t == 0) {
-    s_count = n_win_c;
+    s_count = 0;
     s_ccount = 0;
   }
   __syncthreads();
-  const uint32_t need = kk - n_win_c;
-  if (need > 0 && need >= n_cand) {
-    for (uint32_t i = t; i < n_cand && n_win_c + i < kk; i += kThreads)
-      s_sel[n_win_c + i] = __ldcg(cand + i);
-    __syncthreads();
-    if (t == 0) s_count = n_win_c + (n_cand < need ? n_cand : need);
-  } else if (need > 0) {
-    // digit 2 of the candidates: bins above d2 are winners, bin d2 the boundary
-    for (int i = t; i < kBins; i += kThreads) s_hist[i] = __ldcg(gh2 + i);
-    __syncthreads();
-    uint32_t above2;
-    const uint32_t d2 = find_digit(s_hist, kBins, need, &above2, s_scan, s_out);
-    const uint32_t in2 = s_hist[d2];
-    if (in2 <= kSmemCand) {
-      for (uint32_t i0 = 0; i0 < n_cand; i0 += kThreads) {
-        const uint32_t i = i0 + t;
-        const uint64_t x = i < n_cand ? __ldcg(cand + i) : 0ull;
-        const uint32_t dig = static_cast<uint32_t>(x >> (32 + kShift2)) & (kBins - 1);
-        const bool w = i < n_cand && dig > d2, c = i < n_cand && dig == d2;
-        const uint32_t p = warp_append(&s_count, w, 0xffffffffu);
-        if (w && p < kMaxK) s_sel[p] = x;
-        const uint32_t q = warp_append(&s_ccount, c, 0xffffffffu);
-        if (c && q < kSmemCand) s_cand[q] = x;
-      }
-      __syncthreads();
-      const uint32_t need2 = need - above2;  // >= 1, <= in2
-      if (need2 == in2) {
-        for (uint32_t i = t; i < in2; i += kThreads) s_sel[n_win_c + above2 + i] = s_cand[i];
+  for_each_kept([&](uint64_t x, bool in, uint32_t) {
+    const uint32_t dig = static_cast<uint32_t>(x >> (32 + kShift1));
+    const bool w = in && (all || dig > d1), c = in && !all && dig == d1;
+    const uint32_t pw = warp_append(&s_count, w, 0xffffffffu);
+    if (w && pw < static_cast<uint32_t>(kMaxK)) s_sel[pw] = x;
+    const uint32_t pc = warp_append(&s_ccount, c, 0xffffffffu);
+    if (c && pc < static_cast<uint32_t>(kSmemCand)) s_cand[pc] = x;
+  });
+  __syncthreads();
+  const uint32_t n_win = s_count < kk ? s_count : kk;
+  const uint32_t nc = s_ccount;
+  const uint32_t kept = s_count + s_ccount;
+  const uint32_t need = kk - n_win;
+  __syncthreads();
+  if (t == 0) s_count = n_win;
+  __syncthreads();
+  if (need > 0) {
+    if (nc <= static_cast<uint32_t>(kSmemCand)) {
+      if (need >= nc) {
+        for (uint32_t i = t; i < nc && n_win + i < kk; i += kThreads) s_sel[n_win + i] = s_cand[i];
         __syncthreads();
-        if (t == 0) s_count = n_win_c + above2 + in2;
+        if (t == 0) s_count = n_win + (nc < need ? nc : need);
       } else {
-        select_rest(s_cand, in2, need2, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 42);
+        select_rest(s_cand, nc, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 53);
       }
     } else {
-      // heavy ties: select over every candidate's low 53 composite bits
-      select_rest(cand, n_cand, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 53);
+      // heavy ties: pack every kept composite to the front of the row's
+      // workspace (each read lies at or after its write, and every read of a
+      // group precedes its writes), then select among those in bin d1
+      for_each_kept([&](uint64_t x, bool in, uint32_t e) {
+        __syncthreads();
+        if (in) ws.cand[off + e] = x;
+      });
+      select_rest(ws.cand + off, kept, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 53,
+                  static_cast<uint64_t>(d1) << 53, 0x7ffull << 53);
     }
   }
   __syncthreads();
@@ -720,10 +770,10 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __re
       if (out_v) out_v[r] = __uint_as_float(__ldcg(base + j));
     }
   } else {
-    int p = 1;
-    while (p < static_cast<int>(have)) p <<= 1;
-    for (int i = have + t; i < p; i += kThreads) s_sel[i] = 0;  // sorts last
-    bitonic_sort_desc(s_sel, p);
+    int p2 = 1;
+    while (p2 < static_cast<int>(have)) p2 <<= 1;
+    for (int i = have + t; i < p2; i += kThreads) s_sel[i] = 0;  // sorts last
+    bitonic_sort_desc(s_sel, p2);
     for (uint32_t i = t; i < have; i += kThreads) {
       const uint32_t j = 0xffffffffu - static_cast<uint32_t>(s_sel[i]);
       out_i[i] = static_cast<int32_t>(j);
@@ -737,14 +787,9 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const float* __re
   // leave the row's workspace zeroed for the next call
   if (!all) {
     uint32_t* gh = ws.hist + static_cast<int64_t>(row) * kBins;
-    for (int i = t; i < kBins; i += kThreads) {
-      gh[i] = 0;
-      gh2[i] = 0;
-    }
+    for (int i = t; i < kBins; i += kThreads) gh[i] = 0;
   }
   if (t == 0) {
-    rs->n_win = 0;
-    rs->n_cand = 0;
     rs->done2 = 0;
     rs->digit = 0;
   }
@@ -757,12 +802,13 @@ size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k) {
 }
 
 size_t topk_zero_prefix_bytes(int64_t B, int64_t total_rows, int64_t k) {
-  return WsLayout(B, total_rows, k).win;
+  return WsLayout(B, total_rows, k).wcount;
 }
 
 int64_t topk_chunk(int64_t total_rows) {
-  int64_t want = total_rows / (2 * static_cast<int64_t>(device_sms()));
-  int64_t c = kThreads * kBlockU;
+  // about one chunk per SM (a single wave of both passes), 4,096 to 65,536 scores
+  const int64_t want = total_rows / static_cast<int64_t>(device_sms());
+  int64_t c = kMinChunk;
   while (c * 2 <= want && c < 65536) c *= 2;
   return c;
 }

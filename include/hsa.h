@@ -140,10 +140,10 @@ hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys
  * shared memory, compacts the keys at or above the threshold bin, and CTA 0
  * settles the boundary and sorts.  Otherwise two launches, every row cut into
  * chunks handled by separate CTAs: launch 1 histograms the top 11 key bits
- * per row and finds the threshold bin; launch 2 compacts the keys above it
- * (winners) and in it (candidates, with a histogram of their next 11 bits),
- * and each row's last CTA settles the boundary by a radix select over the
- * few remaining candidates, sorts the k survivors and writes them.
+ * per row and finds the threshold bin; in launch 2 each warp keeps the keys
+ * at or above that bin from its share of a chunk (no atomics), and each
+ * row's last CTA gathers them, settles the boundary by a radix select over
+ * the threshold bin, sorts the k survivors and writes them.
  * ---------------------------------------------------------------------- */
 size_t hsa_topk_workspace_size(int64_t B, int64_t total_rows, int64_t k);
 hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, int64_t total_rows,
