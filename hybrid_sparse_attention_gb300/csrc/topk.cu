@@ -697,19 +697,28 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
       s_hist[t] = incl - c;
       __syncthreads();
       const int nlc = static_cast<int>(nl - l0 < kThreads ? nl - l0 : kThreads);
-      for (uint32_t e0 = 0; e0 < tot; e0 += kThreads) {
-        const uint32_t e = e0 + t;
-        uint64_t x = 0;
-        if (e < tot) {
-          int a = 0, z = nlc - 1;  // the last list starting at or before e
-          while (a < z) {
-            const int mid = (a + z + 1) >> 1;
-            if (s_hist[mid] <= e) a = mid; else z = mid - 1;
+      constexpr int kG = 4;  // composites per thread per round: their loads in flight together
+      for (uint32_t e0 = 0; e0 < tot; e0 += kThreads * kG) {
+        uint64_t x[kG];
+#pragma unroll
+        for (int u = 0; u < kG; ++u) {
+          const uint32_t e = e0 + u * kThreads + t;
+          x[u] = 0;
+          if (e < tot) {
+            int a = 0, z = nlc - 1;  // the last list starting at or before e
+            while (a < z) {
+              const int mid = (a + z + 1) >> 1;
+              if (s_hist[mid] <= e) a = mid; else z = mid - 1;
+            }
+            const int64_t lg = l0 + a;
+            x[u] = __ldcg(ws.cand + off + (lg / kWarps) * chunk + (lg % kWarps) * wsub + (e - s_hist[a]));
           }
-          const int64_t lg = l0 + a;
-          x = __ldcg(ws.cand + off + (lg / kWarps) * chunk + (lg % kWarps) * wsub + (e - s_hist[a]));
         }
-        fn(x, e < tot, carry + e);
+#pragma unroll
+        for (int u = 0; u < kG; ++u) {
+          const uint32_t e = e0 + u * kThreads + t;
+          fn(x[u], e < tot, carry + e);
+        }
       }
       __syncthreads();  // s_hist and s_scan are reused by the next group
       carry += tot;
