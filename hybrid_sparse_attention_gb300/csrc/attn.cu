@@ -708,37 +708,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
 }
 
 // Merges the split partials: o = sum_s e^(lse_s - lse) o_s, lse = log sum_s e^lse_s.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const float* __restrict__ po,
+// Two heads per CTA (128 threads each): one thread turns the S partial
+// log-sum-exps into weights, then every thread combines 16-byte groups of
+// value channels with all S partial loads of a group in flight.
+constexpr int kMaxSplits = 1024;
+
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ po,
                                                           const float* __restrict__ plse, int S,
-                                                          int Hq, int Dv, void* out, int out_dtype,
-                                                          float* lse) {
+                                                          int64_t BH, int Hq, int Dv, void* out,
+                                                          int out_dtype, float* lse) {
+  __shared__ float s_w[2][kMaxSplits];
+  __shared__ float s_inv[2];
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x / Hq, h = blockIdx.x % Hq;
-  const float* ls = plse + static_cast<int64_t>(b) * S * Hq + h;
-  float mx = -INFINITY;
-  for (int s = 0; s < S; ++s) mx = fmaxf(mx, ls[static_cast<int64_t>(s) * Hq]);
-  float tot = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float l = ls[static_cast<int64_t>(s) * Hq];
-    if (l > -INFINITY) tot += __expf(l - mx);
-  }
-  const float inv = tot > 0.f ? 1.f / tot : 0.f;
-  const int64_t head = static_cast<int64_t>(b) * Hq + h;
-  for (int dv = threadIdx.x; dv < Dv; dv += blockDim.x) {
-    float acc = 0.f;
+  const int hh = threadIdx.x >> 7, tl = threadIdx.x & 127;
+  const int64_t head = 2 * static_cast<int64_t>(blockIdx.x) + hh;  // b * Hq + h
+  const bool live = head < BH;
+  const int64_t b = head / Hq, h = head % Hq;
+  if (live && tl == 0) {
+    const float* ls = plse + b * S * Hq + h;
+    float mx = -INFINITY;
+    for (int s = 0; s < S; ++s) mx = fmaxf(mx, ls[static_cast<int64_t>(s) * Hq]);
+    float tot = 0.f;
     for (int s = 0; s < S; ++s) {
       const float l = ls[static_cast<int64_t>(s) * Hq];
-      if (l > -INFINITY)
-        acc += __expf(l - mx) * po[((static_cast<int64_t>(b) * S + s) * Hq + h) * Dv + dv];
+      const float w = l > -INFINITY ? __expf(l - mx) : 0.f;
+      s_w[hh][s] = w;
+      tot += w;
     }
-    const float o = acc * inv;
-    if (out_dtype == HSA_BF16)
-      reinterpret_cast<__nv_bfloat16*>(out)[head * Dv + dv] = __float2bfloat16_rn(o);
-    else
-      reinterpret_cast<float*>(out)[head * Dv + dv] = o;
+    s_inv[hh] = tot > 0.f ? 1.f / tot : 0.f;
+    if (lse) lse[head] = tot > 0.f ? mx + logf(tot) : -INFINITY;
   }
-  if (threadIdx.x == 0 && lse) lse[head] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  __syncthreads();
+  if (!live) return;
+  const float inv = s_inv[hh];
+  const float4* p4 = reinterpret_cast<const float4*>(po + (b * S * Hq + h) * Dv);
+  const int64_t split4 = static_cast<int64_t>(Hq) * Dv / 4;  // float4s between splits
+  for (int d4 = tl; d4 < Dv / 4; d4 += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+      const float w = s_w[hh][s];
+      if (w != 0.f) {
+        const float4 v = __ldcs(p4 + s * split4 + d4);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+    }
+    const int64_t at = head * Dv + 4 * d4;
+    if (out_dtype == HSA_BF16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + at) = pk;
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + at) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+  }
 }
 
 }  // namespace
@@ -753,6 +783,7 @@ AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, in
   const int64_t tiles = slots > 0 ? (slots + kKeys - 1) / kKeys : 1;
   int64_t S = device_sms() / (B * pl.G);
   if (S < 1) S = 1;
+  if (S > kMaxSplits) S = kMaxSplits;
   if (S > tiles) S = tiles;
   // whole tiles per split: a masked slot costs the gather as much as a live one
   const int64_t tps = (tiles + S - 1) / S;
@@ -821,9 +852,10 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   if (e != cudaSuccess) return e;
   e = launch_k(kernel, dim3(grid), dim3(kThreads), pl.smem, stream, pdl, p);
   if (e != cudaSuccess || pl.S == 1) return e;
-  return launch_k(attn_combine_kernel, dim3(static_cast<unsigned>(a.B * a.Hq)), dim3(128), 0, stream,
+  const int64_t bh = a.B * a.Hq;
+  return launch_k(attn_combine_kernel, dim3(static_cast<unsigned>((bh + 1) / 2)), dim3(256), 0, stream,
                   true, static_cast<const float*>(p.po), static_cast<const float*>(p.plse), pl.S,
-                  p.Hq, p.Dv, a.out, a.out_dtype, a.lse);
+                  bh, p.Hq, p.Dv, a.out, a.out_dtype, a.lse);
 }
 
 }  // namespace hsa
