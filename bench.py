@@ -76,7 +76,10 @@ def layer_bytes(L, shape):
     compress = ncomp * (4 * 2 * (D + Di) * 2 + (D + Di) * 2)
     indexer = keys + iq_w + int(n4.sum()) * 4
     total = keys + iq_w + scores + gather + q + o + idx + append + compress
-    return {"total": total, "indexer": indexer, "keys": keys, "gather": gather}
+    attention = gather + q + o + idx // 2
+    topk = int(n4.sum()) * 4 + idx // 2
+    return {"total": total, "indexer": indexer, "keys": keys, "gather": gather,
+            "attention": attention, "topk": topk}
 
 
 class ClockSampler:
@@ -400,6 +403,12 @@ def run_hsa(args, world, rank, local, dist):
                      "launch_us": idx_ms * 1000},
         "layer_roofline": {"algorithmic_bytes": nbytes["total"], "achieved_gbs": layer_gbs,
                            "frac": layer_gbs / peak},
+        "stage_rooflines": {
+            name: {"algorithmic_bytes": nbytes[key], "stage_us": stage_mean[j] * 1000,
+                   "achieved_gbs": nbytes[key] / (stage_mean[j] * 1e-3) / 1e9,
+                   "frac": nbytes[key] / (stage_mean[j] * 1e-3) / 1e9 / peak}
+            for name, key, j in (("indexer", "indexer", 1), ("topk", "topk", 2),
+                                 ("attention (+ split combine)", "attention", 3))},
         "stage_us": {"append_compress": stage_mean[0] * 1000, "indexer": stage_mean[1] * 1000,
                      "topk": stage_mean[2] * 1000, "attention": stage_mean[3] * 1000},
         "cpu_baseline": cpu,
