@@ -236,8 +236,10 @@ template <int kN>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
-  pdl_trigger();
-  pdl_wait();
+  // Programmatic dependent launch: the previous kernel (top-k) triggered this
+  // launch only after its own wait, so everything older (the append's window
+  // rows and lengths, q) is complete; only the index lists need the wait,
+  // which the gather and softmax threads take right before reading them.
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x % p.G;
   const int s = (blockIdx.x / p.G) % p.S;
@@ -338,6 +340,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       if (np == 0) pend0 = it; else pend1 = it;
       ++np;
     };
+    auto issue_q = [&]() {  // Q (every gather thread), one cp.async group
+      const int nq = kN * NSL * 8;
+      for (int i = pt_; i < nq; i += kProdThreads) {
+        const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, cc = rem & 7;
+        const bool v = h < p.HG;
+        const uint16_t* src =
+            v ? p.q + (static_cast<int64_t>(b) * p.Hq + g * p.HG + h) * p.Dqk + j * 64 + cc * 8 : p.q;
+        tc::cp_async16(qs + j * qslice + sw128(h, cc), src, v ? 16u : 0u);
+      }
+      tc::cp_async_commit();
+      push(-1);
+    };
     int64_t item = 0;
     for (int c = 0; c < nchunks; ++c) {
       const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
@@ -346,6 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       if (tc::named_barrier_or(2, kProdThreads, !ok)) {
         ok = false;
         break;
+      }
+      if (c == 0) {
+        issue_q();  // q is not written by the previous kernel: load it before waiting
+        pdl_wait();
+        pdl_trigger();
       }
       {
         constexpr int kPer = (kMaxTC * kKeys + kProdThreads - 1) / kProdThreads;
@@ -365,27 +384,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         }
       }
       tc::named_barrier(2, kProdThreads);
-      {
-        // Q (every gather thread) shares its region with the P^T buffers of the
-        // previous chunk, free once that chunk's last O^T MMAs are done
-        if (c > 0) {
-          const int lt = c * TC - 1;
-          const bool f = !wait_or_abort(sh, &sh.o_done[lt & 1], (lt >> 1) & 1, p.status);
-          if (tc::named_barrier_or(2, kProdThreads, f)) {
-            ok = false;
-            break;
-          }
+      if (c > 0) {
+        // Q shares its region with the P^T buffers of the previous chunk, free
+        // once that chunk's last O^T MMAs are done
+        const int lt = c * TC - 1;
+        const bool f = !wait_or_abort(sh, &sh.o_done[lt & 1], (lt >> 1) & 1, p.status);
+        if (tc::named_barrier_or(2, kProdThreads, f)) {
+          ok = false;
+          break;
         }
-        const int nq = kN * NSL * 8;
-        for (int i = pt_; i < nq; i += kProdThreads) {
-          const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, cc = rem & 7;
-          const bool v = h < p.HG;
-          const uint16_t* src =
-              v ? p.q + (static_cast<int64_t>(b) * p.Hq + g * p.HG + h) * p.Dqk + j * 64 + cc * 8 : p.q;
-          tc::cp_async16(qs + j * qslice + sw128(h, cc), src, v ? 16u : 0u);
-        }
-        tc::cp_async_commit();
-        push(-1);
+        issue_q();
       }
       // pass 1: every channel pair of every tile; pass 2: the value pairs again
       for (int pass = 0; pass < 2; ++pass) {
@@ -528,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     for (int c = 0; c < nchunks && ok; ++c) {
       const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
       // which of this lane's slots are attended, per chunk tile (loads issued before any wait)
+      if (c == 0) pdl_wait();  // the index lists come from the previous kernel
       uint32_t vmask = 0;
       for (int tc_ = 0; tc_ < nct; ++tc_) {
         const int64_t slot = static_cast<int64_t>(tb + tc_) * kKeys + tid;
@@ -719,8 +728,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
                                                           int out_dtype, float* lse) {
   __shared__ float s_w[2][kMaxSplits];
   __shared__ float s_inv[2];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int hh = threadIdx.x >> 7, tl = threadIdx.x & 127;
   const int64_t head = 2 * static_cast<int64_t>(blockIdx.x) + hh;  // b * Hq + h
   const bool live = head < BH;

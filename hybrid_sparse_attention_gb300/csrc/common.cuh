@@ -21,9 +21,10 @@ HSA_DEVINL void set_status(uint32_t* status, uint32_t bit) {
 // Programmatic dependent launch.  pdl_trigger lets the next kernel of the
 // stream be scheduled before this one ends; pdl_wait blocks until the previous
 // kernel has completed and its writes are visible (a no-op when this kernel
-// was launched without the programmatic-serialization attribute).  Every
-// kernel calls both first thing, so a chain of launches overlaps only its
-// launch latency and never reads a predecessor's output early.
+// was launched without the programmatic-serialization attribute).  Kernels
+// trigger only after their own wait has returned, so when a kernel starts,
+// every kernel older than its immediate predecessor has completed: it may read
+// their outputs at once and must wait only before reading its predecessor's.
 HSA_DEVINL void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 HSA_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

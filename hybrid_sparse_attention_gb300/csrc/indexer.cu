@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
 
   const int kb_elems = p.Di >= 64 ? 64 : p.Di;  // elements of one swizzle row
   const int nkb = p.Di / kb_elems;

@@ -169,8 +169,8 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
 }
 
 __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendParams p) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   if (p.r <= kShortBlock) {
     append_short(p, b);

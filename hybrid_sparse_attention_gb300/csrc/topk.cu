@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_hist_kernel(const float* __r
   __shared__ uint32_t s_hist[kBins];
   __shared__ uint32_t s_scan[33], s_out[2];
   __shared__ int s_last;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   int row;
   int64_t piece, npieces;
   if (!locate_piece(B, blockIdx.x, ChunkPieces{sp, chunk}, &row, &piece, &npieces)) return;
@@ -420,8 +420,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   uint64_t* s_sel = s_loc + kClList;      // [kMaxK] CTA 0: winners, then every survivor
   uint64_t* s_cand = s_sel + kMaxK;       // [kClList] CTA 0: candidates (bin d1); sort runs
   __shared__ uint32_t s_scan[33], s_out[2], s_wt[kWarps], s_nloc, s_count, s_ccount;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t lt = (1u << lane) - 1u;
   const uint32_t rank = cluster_rank();
@@ -607,8 +607,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
   __shared__ uint32_t s_hist[kBins];  // list offsets, then select scratch
   __shared__ uint32_t s_scan[33], s_out[2], s_count, s_ccount;
   __shared__ int s_last;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   int row;
   int64_t piece, npieces;
   if (!locate_piece(B, blockIdx.x, ChunkPieces{sp, chunk}, &row, &piece, &npieces)) return;
