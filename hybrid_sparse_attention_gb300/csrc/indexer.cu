@@ -108,8 +108,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait();
-  pdl_trigger();
+  // Programmatic dependent launch: the prologue (tile table, barriers, TMEM)
+  // needs nothing the previous kernel writes; the TMA producer waits before
+  // its first key load (the append may have written a new compressed key).
 
   const int kb_elems = p.Di >= 64 ? 64 : p.Di;  // elements of one swizzle row
   const int nkb = p.Di / kb_elems;
@@ -180,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
     if (lane == 0) {
       tc::tma_prefetch_map(&kmap);
       tc::tma_prefetch_map(&qmap);
+      pdl_wait();
+      pdl_trigger();
       SeqCursor cur;
       for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
         const int s = i % kStages;

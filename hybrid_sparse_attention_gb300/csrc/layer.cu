@@ -302,7 +302,10 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   if (d.kind == HSA_LAYER_C4) {
     float* scores = d.scores ? d.scores : reinterpret_cast<float*>(w + L.scores);
     int32_t* tidx = d.topk_idx ? d.topk_idx : reinterpret_cast<int32_t*>(w + L.idx);
-    e = launch_indexer(d.iq, d.w, d.key_pool, sp, d.B, d.Hi, d.Di, d.pool_total_rows, scores,
+    // the lengths after the append are the ones before it plus one: the
+    // indexer's tile table can be built before the append has finished
+    const Spans sp_in{d.pool_offsets, d.seq_len_in, 1, r, d.pool_total_rows};
+    e = launch_indexer(d.iq, d.w, d.key_pool, sp_in, d.B, d.Hi, d.Di, d.pool_total_rows, scores,
                        status, stream, true);
     if (e != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;

@@ -420,8 +420,6 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   uint64_t* s_sel = s_loc + kClList;      // [kMaxK] CTA 0: winners, then every survivor
   uint64_t* s_cand = s_sel + kMaxK;       // [kClList] CTA 0: candidates (bin d1); sort runs
   __shared__ uint32_t s_scan[33], s_out[2], s_wt[kWarps], s_nloc, s_count, s_ccount;
-  pdl_wait();
-  pdl_trigger();
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t lt = (1u << lane) - 1u;
   const uint32_t rank = cluster_rank();
@@ -442,6 +440,10 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
     s_ccount = 0;
   }
   __syncthreads();
+  // the row's geometry needs only the append's lengths (older than the
+  // previous kernel); the scores need the wait
+  pdl_wait();
+  pdl_trigger();
   uint32_t key[kClU];
   bool nan = false;
 #pragma unroll
