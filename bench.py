@@ -338,28 +338,51 @@ def run_hsa(args, world, rank, local, dist):
     assert _lib.hsa_workspace_status(ws) == 0
 
     # ------------------------------------------------ end to end: host buffers
-    host_in = {k: getattr(g, k).cpu().pin_memory() for k in
-               ("kv_new", "z_new", "ik_new", "iz_new", "q", "iq", "w")}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+    # The step's inputs travel in one host-to-device copy (one pinned staging
+    # buffer, each input at a 256-byte-aligned offset) and its outputs in one
+    # device-to-host copy; the library reads and writes views of the device
+    # staging buffers.
+    import copy as _copy
+
+    def packed(tensors):
+        offs, at = [], 0
+        for t in tensors:
+            offs.append(at)
+            at += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, at
+
+    names_in = ("kv_new", "z_new", "ik_new", "iz_new", "q", "iq", "w")
+    t_in = [getattr(g, k) for k in names_in]
+    offs_in, n_in = packed(t_in)
+    dev_in = torch.empty(n_in, dtype=torch.uint8, device="cuda")
+    host_in = torch.empty(n_in, dtype=torch.uint8).pin_memory()
+    g2 = _copy.copy(g)
+    for k, t, o in zip(names_in, t_in, offs_in):
+        nb = t.numel() * t.element_size()
+        host_in[o:o + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
+        setattr(g2, k, dev_in[o:o + nb].view(t.dtype).view(t.shape))
+    offs_out, n_out = packed([out, lse])
+    dev_out = torch.empty(n_out, dtype=torch.uint8, device="cuda")
+    out2 = dev_out[:out.numel() * 2].view(out.dtype).view(out.shape)
+    lse2 = dev_out[offs_out[1]:offs_out[1] + lse.numel() * 4].view(lse.dtype).view(lse.shape)
+    host_out = torch.empty(n_out, dtype=torch.uint8).pin_memory()
+    desc_e2e = _lib.layer_desc(g2, out2, lse2, seq_out, idx, scores)
+    h2d, d2h = n_in, n_out
     e2e_ms = []
     for i in range(args.warmup + args.steps):
         flush(i)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for k, t in host_in.items():
-            getattr(g, k).copy_(t, non_blocking=True)
-        step()
-        host_out.copy_(out, non_blocking=True)
-        host_lse.copy_(lse, non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
+        step(desc_e2e)
+        host_out.copy_(dev_out, non_blocking=True)
         b.record(stream)
         b.synchronize()
         if i >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
     e2e = max_over_ranks(statistics.mean(e2e_ms), dist)
+    assert torch.equal(host_out[:out.numel() * 2].view(out.dtype).view(out.shape), out.cpu())
 
     # ------------------------------------------------ standalone top-k (rows / s)
     topk = topk_rows_per_s(flush) if rank == 0 and not args.no_topk else None
