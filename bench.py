@@ -217,6 +217,8 @@ def main():
     ap.add_argument("--impl", default="hsa", choices=["hsa", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline (0: skip)")
+    ap.add_argument("--layers", type=int, default=60,
+                    help="layers in the CUDA-graph multi-layer step measurement (0: skip)")
     ap.add_argument("--no-topk", action="store_true",
                     help="skip the standalone top-k rows/s measurement")
     ap.add_argument("--profile", action="store_true",
@@ -384,6 +386,9 @@ def run_hsa(args, world, rank, local, dist):
     e2e = max_over_ranks(statistics.mean(e2e_ms), dist)
     assert torch.equal(host_out[:out.numel() * 2].view(out.dtype).view(out.shape), out.cpu())
 
+    # ------------------------------------------------ a 60-layer step in one CUDA graph
+    multi = multi_layer_graph(args, flush) if rank == 0 and args.layers > 0 else None
+
     # ------------------------------------------------ standalone top-k (rows / s)
     topk = topk_rows_per_s(flush) if rank == 0 and not args.no_topk else None
 
@@ -441,6 +446,7 @@ def run_hsa(args, world, rank, local, dist):
         "clocks": clocks.summary(),
         "wall_s_timed": wall,
         "topk_rows_per_s": topk,
+        "multi_layer_graph": multi,
     }
     print(json.dumps(line), flush=True)
 
@@ -462,6 +468,64 @@ def run_profile(ctx=None):
     torch.cuda.synchronize()
     assert _lib.hsa_workspace_status(ws) == 0
     print(json.dumps({"profile": "ok", "sum_c4_entries": int((L // 4).sum())}))
+
+
+def multi_layer_graph(args, flush, nstates=4, iters=10):
+    """A decode step over `args.layers` C4 layers (the bench's shapes; layer i
+    works on state i mod nstates, each larger than L2) captured once in a CUDA
+    graph: us per layer of the replayed step, next to the same layers launched
+    one call at a time."""
+    shape = synth.FULL
+    states = []
+    for j in range(nstates):
+        L, g = build_workload(0) if j == 0 else (None, None)
+        if j:
+            seed = synth.SEED["c4layer"] + 7919 * j
+            L = synth.c4_lengths(seed, 64)
+            g = synth.filled_state(seed, 4, shape, L, device="cuda", name=f"layer{j}")
+        B = L.numel()
+        out = torch.empty(B, shape.Hq, shape.Dv, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(B, shape.Hq, dtype=torch.float32, device="cuda")
+        idx = torch.empty(B, shape.k, dtype=torch.int32, device="cuda")
+        scores = torch.empty(g.kv_pool.shape[0], dtype=torch.float32, device="cuda")
+        desc = _lib.layer_desc(g, out, lse, torch.empty_like(g.seq_len_in), idx, scores)
+        ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
+        states.append((g, desc, ws, out, lse, idx, scores))
+    descs = [states[i % nstates] for i in range(args.layers)]
+
+    def eager():
+        for _, desc, ws, *_ in descs:
+            _lib.hsa_layer_decode(desc, ws=ws)
+
+    for _ in range(3):
+        eager()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        eager()
+    times = {"graph": [], "eager": []}
+    for i in range(3 + iters):
+        for mode in ("graph", "eager"):
+            flush(i)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            if mode == "graph":
+                graph.replay()
+            else:
+                eager()
+            b.record()
+            b.synchronize()
+            if i >= 3:
+                times[mode].append(a.elapsed_time(b))
+    for _, _, ws, *_ in states:
+        assert _lib.hsa_workspace_status(ws) == 0
+    per = {m: statistics.mean(v) * 1000 / args.layers for m, v in times.items()}
+    return {"layers": args.layers, "states": nstates, "us_per_layer_graph": per["graph"],
+            "us_per_layer_eager": per["eager"],
+            "note": "C4 layers of the bench workload, layer i on state i mod 4; L2 flushed "
+                    "before each step, not between layers"}
 
 
 class L2Flush:

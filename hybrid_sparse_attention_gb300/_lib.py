@@ -288,6 +288,10 @@ def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
         # keep the handle array alive as long as the descriptor
         d._events = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(h) for h in stage_events])
         d.stage_events = ctypes.cast(d._events, ctypes.c_void_p)
+    # the descriptor holds raw device pointers: keep every tensor behind them
+    # alive as long as it is (a temporary passed here would otherwise be freed
+    # and its memory handed to another tensor while the library still writes it)
+    d._keep = (st, out, lse, seq_len_out, topk_idx, scores)
     return d
 
 

@@ -78,6 +78,7 @@ struct AttnParams {
   float* po;              // partial outputs [B, S, Hq, Dv] (S > 1)
   float* plse;            // partial lse [B, S, Hq] (S > 1)
   uint32_t* status;
+  int early;              // the previous kernel writes only idx (see AttnArgs)
 };
 
 struct SeqGeom {
@@ -236,10 +237,15 @@ template <int kN>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
-  // Programmatic dependent launch: the previous kernel (top-k) triggered this
-  // launch only after its own wait, so everything older (the append's window
-  // rows and lengths, q) is complete; only the index lists need the wait,
-  // which the gather and softmax threads take right before reading them.
+  // Programmatic dependent launch.  When the previous kernel is the top-k
+  // (p.early), it triggered this launch only after its own wait, so everything
+  // older (the append's window rows and lengths, q) is complete and only the
+  // index lists need the wait, which the gather and softmax threads take right
+  // before reading them.  Otherwise every thread waits first.
+  if (!p.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x % p.G;
   const int s = (blockIdx.x / p.G) % p.S;
@@ -850,6 +856,7 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.out_dtype = a.out_dtype;
   p.lse = a.lse;
   p.status = status;
+  p.early = a.only_idx_pending ? 1 : 0;
   char* w = static_cast<char*>(ws) + kWsHeader;
   p.po = reinterpret_cast<float*>(w);
   p.plse = reinterpret_cast<float*>(

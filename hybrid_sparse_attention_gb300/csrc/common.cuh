@@ -92,6 +92,10 @@ struct AttnArgs {
   void* out;
   int out_dtype;
   float* lse;
+  // The previous kernel of the stream (under programmatic dependent launch)
+  // writes only the index lists: the window rows, lengths and q may be read
+  // before waiting for it.  False when it may write anything else.
+  bool only_idx_pending = false;
 };
 
 // Launch geometry of the fused attention: HG heads per CTA (N = MMA width),

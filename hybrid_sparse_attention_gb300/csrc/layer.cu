@@ -337,6 +337,7 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   a.out = d.out;
   a.out_dtype = d.out_dtype;
   a.lse = d.lse;
+  a.only_idx_pending = d.kind == HSA_LAYER_C4;  // C128: the append comes right before
   e = launch_attn(a, pl, w + L.attn, status, stream, true);
   if (e != cudaSuccess) return e;
   return mark(4);
