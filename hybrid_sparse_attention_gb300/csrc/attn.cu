@@ -723,67 +723,70 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
 }
 
 // Merges the split partials: o = sum_s e^(lse_s - lse) o_s, lse = log sum_s e^lse_s.
-// Two heads per CTA (128 threads each): one thread turns the S partial
-// log-sum-exps into weights, then every thread combines 16-byte groups of
-// value channels with all S partial loads of a group in flight.
+// One thread per two 16-byte groups of value channels of one head: it loads
+// the head's S partial log-sum-exps itself (the same few words for every
+// thread of a head: cached), forms the weights in registers and combines with
+// every split's partial loads in flight; no shared memory, no barriers.
 constexpr int kMaxSplits = 1024;
+constexpr int kCombineRegs = 16;  // splits whose weights stay in registers
 
-__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ po,
+__global__ void __launch_bounds__(512) attn_combine_kernel(const float* __restrict__ po,
                                                           const float* __restrict__ plse, int S,
                                                           int64_t BH, int Hq, int Dv, void* out,
                                                           int out_dtype, float* lse) {
-  __shared__ float s_w[2][kMaxSplits];
-  __shared__ float s_inv[2];
   pdl_wait();
   pdl_trigger();
-  const int hh = threadIdx.x >> 7, tl = threadIdx.x & 127;
-  const int64_t head = 2 * static_cast<int64_t>(blockIdx.x) + hh;  // b * Hq + h
-  const bool live = head < BH;
+  const int d4n = Dv / 4;
+  const int64_t gi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 2;
+  if (gi >= BH * d4n) return;
+  const int64_t head = gi / d4n;  // b * Hq + h; both groups of this thread share it (d4n even)
+  const int d4 = static_cast<int>(gi % d4n);
   const int64_t b = head / Hq, h = head % Hq;
-  if (live && tl == 0) {
-    const float* ls = plse + b * S * Hq + h;
-    float mx = -INFINITY;
-    for (int s = 0; s < S; ++s) mx = fmaxf(mx, ls[static_cast<int64_t>(s) * Hq]);
-    float tot = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float l = ls[static_cast<int64_t>(s) * Hq];
-      const float w = l > -INFINITY ? __expf(l - mx) : 0.f;
-      s_w[hh][s] = w;
-      tot += w;
-    }
-    s_inv[hh] = tot > 0.f ? 1.f / tot : 0.f;
-    if (lse) lse[head] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+  const float* ls = plse + b * S * Hq + h;
+  float lv[kCombineRegs];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < kCombineRegs; ++s) {
+    lv[s] = s < S ? __ldg(ls + static_cast<int64_t>(s) * Hq) : -INFINITY;
+    mx = fmaxf(mx, lv[s]);
   }
-  __syncthreads();
-  if (!live) return;
-  const float inv = s_inv[hh];
-  const float4* p4 = reinterpret_cast<const float4*>(po + (b * S * Hq + h) * Dv);
+  for (int s = kCombineRegs; s < S; ++s) mx = fmaxf(mx, __ldg(ls + static_cast<int64_t>(s) * Hq));
+  const float4* p4 = reinterpret_cast<const float4*>(po + (b * S * Hq + h) * Dv) + d4;
   const int64_t split4 = static_cast<int64_t>(Hq) * Dv / 4;  // float4s between splits
-  for (int d4 = tl; d4 < Dv / 4; d4 += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
-      const float w = s_w[hh][s];
-      if (w != 0.f) {
-        const float4 v = __ldcs(p4 + s * split4 + d4);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-      }
-    }
-    const int64_t at = head * Dv + 4 * d4;
-    if (out_dtype == HSA_BF16) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + at) = pk;
-    } else {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + at) =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    }
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+  float tot = 0.f;
+  auto add = [&](float l, int s) {
+    if (l == -INFINITY) return;
+    const float w = __expf(l - mx);
+    tot += w;
+    const float4 v0 = __ldcs(p4 + s * split4), v1 = __ldcs(p4 + s * split4 + 1);
+    a0.x = fmaf(w, v0.x, a0.x); a0.y = fmaf(w, v0.y, a0.y);
+    a0.z = fmaf(w, v0.z, a0.z); a0.w = fmaf(w, v0.w, a0.w);
+    a1.x = fmaf(w, v1.x, a1.x); a1.y = fmaf(w, v1.y, a1.y);
+    a1.z = fmaf(w, v1.z, a1.z); a1.w = fmaf(w, v1.w, a1.w);
+  };
+#pragma unroll
+  for (int s = 0; s < kCombineRegs; ++s) add(lv[s], s);
+  for (int s = kCombineRegs; s < S; ++s) add(__ldg(ls + static_cast<int64_t>(s) * Hq), s);
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  const int64_t at = head * Dv + 4 * d4;
+  if (out_dtype == HSA_BF16) {
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(a0.x * inv, a0.y * inv);
+    const __nv_bfloat162 p1 = __floats2bfloat162_rn(a0.z * inv, a0.w * inv);
+    const __nv_bfloat162 p2 = __floats2bfloat162_rn(a1.x * inv, a1.y * inv);
+    const __nv_bfloat162 p3 = __floats2bfloat162_rn(a1.z * inv, a1.w * inv);
+    uint4 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&p0);
+    pk.y = *reinterpret_cast<const uint32_t*>(&p1);
+    pk.z = *reinterpret_cast<const uint32_t*>(&p2);
+    pk.w = *reinterpret_cast<const uint32_t*>(&p3);
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + at) = pk;
+  } else {
+    float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + at);
+    o4[0] = make_float4(a0.x * inv, a0.y * inv, a0.z * inv, a0.w * inv);
+    o4[1] = make_float4(a1.x * inv, a1.y * inv, a1.z * inv, a1.w * inv);
   }
+  if (d4 == 0 && lse) lse[head] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
 
 }  // namespace
@@ -869,9 +872,11 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   e = launch_k(kernel, dim3(grid), dim3(kThreads), pl.smem, stream, pdl, p);
   if (e != cudaSuccess || pl.S == 1) return e;
   const int64_t bh = a.B * a.Hq;
-  return launch_k(attn_combine_kernel, dim3(static_cast<unsigned>((bh + 1) / 2)), dim3(256), 0, stream,
-                  true, static_cast<const float*>(p.po), static_cast<const float*>(p.plse), pl.S,
-                  bh, p.Hq, p.Dv, a.out, a.out_dtype, a.lse);
+  const int64_t threads = bh * (a.Dv / 8);  // two 16-byte groups each
+  return launch_k(attn_combine_kernel, dim3(static_cast<unsigned>((threads + 511) / 512)), dim3(512),
+                  0, stream, true, static_cast<const float*>(p.po),
+                  static_cast<const float*>(p.plse), pl.S, bh, p.Hq, p.Dv, a.out, a.out_dtype,
+                  a.lse);
 }
 
 }  // namespace hsa
