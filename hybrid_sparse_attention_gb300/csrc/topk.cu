@@ -354,8 +354,8 @@ HSA_DEVINL void select_rest(const uint64_t* cand, uint32_t n, uint32_t need, uin
 // ---------------------------------------------------------------- short rows: one cluster per row
 //
 // Rows of at most kClMax scores (every C4 row up to a 128K context) take one
-// launch: a thread-block cluster of kCl CTAs per row, each holding a slice of
-// kClSlice scores in registers.  The CTAs' digit-1 histograms are summed
+// launch: a thread-block cluster of kCl CTAs per row, each holding an equal
+// slice of the row (at most kClSlice scores) in registers.  The CTAs' digit-1 histograms are summed
 // through distributed shared memory (each CTA reduces a quarter of the bins
 // and broadcasts it), so every CTA finds d1 itself; each CTA then compacts
 // its keys at or above bin d1 into shared memory, CTA 0 gathers the lists,
@@ -425,15 +425,19 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   const uint32_t rank = cluster_rank();
   const int row = static_cast<int>(blockIdx.x) / kCl;
   const bool valid = sp.valid(row);
-  int64_t n = valid ? sp.raw_count(row) : 0;
-  if (n > kClMax) n = 0;  // longer than the caller's bound: flagged below, treated as empty
-  if (rank == 0 && t == 0 && (!valid || (valid && sp.raw_count(row) > kClMax)))
+  const int64_t n_raw = valid ? sp.raw_count(row) : 0;
+  // longer than the caller's bound: flagged below, treated as empty
+  const int n = n_raw > kClMax ? 0 : static_cast<int>(n_raw);
+  if (rank == 0 && t == 0 && (!valid || n_raw > kClMax))
     set_status(ws.status, HSA_DEV_BOUNDS);
   const int64_t off = valid ? sp.start(row) : 0;
   const uint32_t* base = reinterpret_cast<const uint32_t*>(scores + off);
   const uint32_t kk = static_cast<uint32_t>(n < k ? n : k);
   const bool all = n <= k;  // every score is selected
-  const int s0 = static_cast<int>(rank) * kClSlice;
+  // equal slices of the row per CTA (each at most kClSlice since n <= kClMax)
+  const int slice = (n + kCl - 1) / kCl;
+  const int s0 = static_cast<int>(rank) * slice;
+  const int s1 = s0 + slice < n ? s0 + slice : n;
   for (int i = t; i < kBins; i += kThreads) s_hist[i] = 0;
   if (t == 0) {
     s_count = 0;
@@ -449,7 +453,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
 #pragma unroll
   for (int u = 0; u < kClU; ++u) {
     const int j = s0 + u * kThreads + t;
-    const uint32_t v = j < n ? __ldcg(base + j) : 0u;
+    const uint32_t v = j < s1 ? __ldcg(base + j) : 0u;
     nan |= is_nan_bits(v);
     key[u] = order_key(v);
   }
@@ -457,7 +461,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   if (!all) {
 #pragma unroll
     for (int u = 0; u < kClU; ++u)
-      if (s0 + u * kThreads + t < n) atomicAdd(&s_hist[key[u] >> kShift1], 1u);
+      if (s0 + u * kThreads + t < s1) atomicAdd(&s_hist[key[u] >> kShift1], 1u);
   }
   cluster_sync();  // every CTA's histogram is complete (and every CTA is running)
   {
@@ -482,7 +486,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
     // compact: ballots count per warp, one scan over warps, no atomics
     auto taken = [&](int u) {
       const uint32_t dig = key[u] >> kShift1;
-      return s0 + u * kThreads + t < n && (all || dig > d1 || (!heavy && dig == d1));
+      return s0 + u * kThreads + t < s1 && (all || dig > d1 || (!heavy && dig == d1));
     };
     uint32_t tot = 0;
 #pragma unroll
@@ -516,7 +520,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int u = 0; u < kClU; ++u) {
         const int j = s0 + u * kThreads + t;
-        const bool c = j < n && (key[u] >> kShift1) == d1;
+        const bool c = j < s1 && (key[u] >> kShift1) == d1;
         const uint32_t q = warp_append(&rs->n_cand, c, 0xffffffffu);
         if (c) ws.cand[off + q] = composite(key[u], static_cast<uint32_t>(j));
       }
