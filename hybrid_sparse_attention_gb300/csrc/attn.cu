@@ -56,6 +56,10 @@ constexpr int kMaxTC = 4;           // tiles per chunk
 constexpr uint32_t kSliceBytes = kKeys * 128;
 constexpr uint32_t kPairBytes = 2 * kSliceBytes;
 constexpr float kRescaleLog2 = 8.f;
+constexpr int kMaxCl = 4;           // splits merged inside one cluster
+constexpr uint32_t kUnitBytes = kKeys * 16 * 4;  // one merge unit: 128 lanes x 16 fp32 columns
+static_assert(16 * kUnitBytes <= kRing * kPairBytes, "a split's O^T units fit its ring");
+constexpr size_t kMergeScratch = 8 * 16 * 32 * 4;  // eight warps' 16 x 32 fp32 transpose tiles
 
 struct AttnParams {
   const uint16_t* q;      // [B, Hq, Dqk]
@@ -79,6 +83,7 @@ struct AttnParams {
   float* plse;            // partial lse [B, S, Hq] (S > 1)
   uint32_t* status;
   int early;              // the previous kernel writes only idx (see AttnArgs)
+  int cl;                 // the S splits form a cluster and merge in shared memory
 };
 
 struct SeqGeom {
@@ -192,6 +197,10 @@ struct Shared {
   float m[64];      // running maximum per head (log2 units), identical for every thread
   float alpha[64];  // rescale factor of the current chunk per head
   float inv[64];    // 1 / softmax denominator per head (0 when nothing was attended)
+  float l[64];      // softmax denominator per head (relative to m)
+  float xm[kMaxCl][64], xl[kMaxCl][64];  // cluster merge: every split's m and l
+  float xw[kMaxCl][64];                   // cluster merge: every split's weight per head
+  int xok[kMaxCl];  // cluster merge: the split has a partial output
   int done_ok;      // the softmax warps finished without an abort: O^T may be written out
   const uint16_t* rows[kMaxTC][kKeys];  // gather tables of the producers (this chunk)
 };
@@ -233,6 +242,120 @@ HSA_DEVINL void write_lse(const AttnParams& p, int b, int g, int s, int h, float
   }
 }
 
+// Merge of the S splits of one (token, head group) inside their cluster (all
+// threads of every CTA call it).  Each split copies its raw O^T from TMEM into
+// its own ring (free by now) in units of 128 value channels x 16 heads and
+// publishes its m and l; unit u is then finished by split u % S, which reads
+// the unit from every split through distributed shared memory and writes
+//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
+// The loops are kept rolled: this code runs once per launch, so its size (the
+// instruction fetches) costs more than its loop overhead.
+template <int kN>
+HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, uint8_t* scratch,
+                              uint32_t tmem, int b, int g, bool own, int TC, int NMT) {
+  constexpr int kQ = kN / 16;  // 16-head column groups
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.S;
+  const int rank = static_cast<int>(cluster_rank());
+  const int U = NMT * kQ;
+  // warp w reads TMEM lane quarter w & 3 (value channels); the two warps of a
+  // quarter (halves hw) take alternate units
+  const int quarter = warp & 3, hw = warp >> 2, row = quarter * 32 + lane;
+  if (own) {
+    tc::fence_after_sync();
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+    for (int u = hw; u < U; u += 2) {
+      uint32_t a[16];
+      tc::tmem_ld16(lane_addr + (TC + u / kQ) * kN + (u % kQ) * 16, a);
+      tc::tmem_ld_wait();
+      uint4* d = reinterpret_cast<uint4*>(ring + u * kUnitBytes + row * 16);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4)
+        d[c4 * kKeys] = make_uint4(a[4 * c4], a[4 * c4 + 1], a[4 * c4 + 2], a[4 * c4 + 3]);
+    }
+  }
+  if (tid < kN) {
+    const float mv = own ? sh.m[tid] : -INFINITY, lv = own ? sh.l[tid] : 0.f;
+    for (int q = 0; q < S; ++q) {
+      st_cluster_u32(map_rank(&sh.xm[rank][tid], q), __float_as_uint(mv));
+      st_cluster_u32(map_rank(&sh.xl[rank][tid], q), __float_as_uint(lv));
+    }
+  }
+  if (tid < S) st_cluster_u32(map_rank(&sh.xok[rank], tid), own ? 1u : 0u);
+  cluster_sync();  // every split's O^T units and statistics are published
+  if (tid < kN) {
+    float M = -INFINITY;
+    for (int r = 0; r < S; ++r)
+      if (sh.xl[r][tid] > 0.f) M = fmaxf(M, sh.xm[r][tid]);
+    float L = 0.f;
+    for (int r = 0; r < S; ++r) {
+      const float w = sh.xl[r][tid] > 0.f ? tc::ex2_approx(sh.xm[r][tid] - M) : 0.f;
+      sh.xw[r][tid] = w;
+      L += w * sh.xl[r][tid];
+    }
+    sh.inv[tid] = L > 0.f ? __frcp_rn(L) : 0.f;
+    if (rank == 0 && tid < p.HG && p.lse)
+      p.lse[static_cast<int64_t>(b) * p.Hq + g * p.HG + tid] =
+          L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncthreads();
+  const bool bf = p.out_dtype == HSA_BF16;
+  const int64_t head0 = static_cast<int64_t>(b) * p.Hq + g * p.HG;
+  uint8_t* tr = scratch + warp * (16 * 32 * 4);  // per-warp transpose buffer (kMergeScratch)
+#pragma unroll 1
+  for (int u = rank + S * hw; u < U; u += 2 * S) {
+    const int q16 = u % kQ;
+    float o[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) o[e] = 0.f;
+#pragma unroll 1
+    for (int r = 0; r < S; ++r) {
+      if (!sh.xok[r]) continue;
+      const uint32_t src = map_rank(ring + u * kUnitBytes + row * 16, r);
+      const float* w = &sh.xw[r][q16 * 16];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const float4 v = ld_cluster_f32x4(src + c4 * (kKeys * 16u));
+        o[4 * c4] = fmaf(v.x, w[4 * c4], o[4 * c4]);
+        o[4 * c4 + 1] = fmaf(v.y, w[4 * c4 + 1], o[4 * c4 + 1]);
+        o[4 * c4 + 2] = fmaf(v.z, w[4 * c4 + 2], o[4 * c4 + 2]);
+        o[4 * c4 + 3] = fmaf(v.w, w[4 * c4 + 3], o[4 * c4 + 3]);
+      }
+    }
+    // transpose through shared memory: lane l holds channel l of 16 heads; the
+    // stores then write 16 contiguous bytes of one head per lane
+    const int64_t base = (head0 + q16 * 16) * p.Dv + (u / kQ) * kKeys + quarter * 32;
+    __syncwarp();
+    if (bf) {
+      __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(tr);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) t[e * 32 + lane] = __float2bfloat16_rn(o[e] * sh.inv[q16 * 16 + e]);
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = lane + 32 * j, h = c >> 2, part = c & 3;  // 4 chunks of 8 channels per head
+        if (q16 * 16 + h < p.HG)
+          *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + base + h * p.Dv + part * 8) =
+              *reinterpret_cast<const uint4*>(t + h * 32 + part * 8);
+      }
+    } else {
+      float* t = reinterpret_cast<float*>(tr);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) t[e * 32 + lane] = o[e] * sh.inv[q16 * 16 + e];
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = lane + 32 * j, h = c >> 3, part = c & 7;  // 8 chunks of 4 channels per head
+        if (q16 * 16 + h < p.HG)
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + base + h * p.Dv + part * 4) =
+              *reinterpret_cast<const float4*>(t + h * 32 + part * 4);
+      }
+    }
+  }
+  cluster_sync();  // no split leaves while another may still read its ring
+}
+
 template <int kN>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -247,8 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     pdl_trigger();
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.x % p.G;
-  const int s = (blockIdx.x / p.G) % p.S;
+  // the S splits of a (token, head group) are consecutive CTAs (one cluster with cl)
+  const int s = blockIdx.x % p.S;
+  const int g = (blockIdx.x / p.S) % p.G;
   const int b = blockIdx.x / (p.G * p.S);
   const int NSL = p.Dqk / 64, NMT = p.Dv / 128, NP1 = (NSL + 1) / 2, TC = p.TC;
   const SeqGeom geo = seq_geom(p, b);
@@ -260,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   const int nt = a1 > a0 ? static_cast<int>((a1 + kKeys - 1) / kKeys) - t0 : 0;
   const int t1 = t0 + nt;
 
-  if (nt <= 0) {  // nothing to attend in this split
+  if (nt <= 0 && !p.cl) {  // nothing to attend in this split (a cluster member still merges)
     if (tid < kKeys) {
       if (p.S == 1)
         for (int h = 0; h < p.HG; ++h)
@@ -304,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     tc::tmem_alloc(&sh.tmem, tmem_cols);
     tc::tmem_relinquish();
   }
+  // the ring starts zeroed: rows that are never gathered hold finite values
+  for (int i = tid; i < static_cast<int>(kRing * kPairBytes / 16); i += kThreads)
+    reinterpret_cast<uint4*>(ring)[i] = make_uint4(0u, 0u, 0u, 0u);
+  tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -417,19 +545,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
                 if (!ok) continue;
               }
             }
-            // lane: 16-byte chunk cc of rows r0 + 4k (k < 32) of both slices of the pair
+            // Masked rows are not copied (no memory request): the slot keeps finite
+            // data (zeroed at start, or rows of this token gathered earlier) that
+            // the softmax weighs with 0.
             const uint32_t dst = tc::smem_u32(ring + slot * kPairBytes);
+            // lane: 16-byte chunk cc of rows r0 + 4k (k < 32) of both slices of the pair
             const int cc = lane & 7, r0 = lane >> 3, j0 = 2 * it;
             const bool two = j0 + 1 < NSL;
 #pragma unroll 4
             for (int k = 0; k < kKeys / 4; ++k) {
               const int r = r0 + 4 * k;
               const uint16_t* row = table[r];
-              const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
-              const uint16_t* src = row ? row + j0 * 64 + cc * 8 : p.q;
-              const uint32_t nb = row ? 16u : 0u;
-              tc::cp_async16_s(dst + off, src, nb);
-              if (two) tc::cp_async16_s(dst + kSliceBytes + off, row ? src + 64 : p.q, nb);
+              if (row) {
+                const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
+                const uint16_t* src = row + j0 * 64 + cc * 8;
+                tc::cp_async16_s(dst + off, src, 16u);
+                if (two) tc::cp_async16_s(dst + kSliceBytes + off, src + 64, 16u);
+              }
             }
             tc::cp_async_commit();
             push(item);
@@ -514,8 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         }
       }
       // drain: every MMA this thread issued has completed before TMEM is freed
-      tc::mma_commit(&sh.fin);
-      tc::mbar_wait(&sh.fin, 0, p.status);
+      if (nchunks > 0) {
+        tc::mma_commit(&sh.fin);
+        tc::mbar_wait(&sh.fin, 0, p.status);
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
@@ -658,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       // `ok` is uniform over the softmax warps here (every exit from the loop
       // went through an agreement barrier)
       bool failed = !ok;
-      if (!failed) {
+      if (!failed && gt > 0) {
         const int lt = gt - 1;
         failed = !wait_or_abort(sh, &sh.o_done[lt & 1], (lt >> 1) & 1, p.status);
       }
@@ -677,14 +811,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     if (tid < kN) {
       const float l = (sh.red[0][tid] + sh.red[1][tid]) + (sh.red[2][tid] + sh.red[3][tid]);
       sh.inv[tid] = l > 0.f ? 1.f / l : 0.f;
-      if (ok && tid < p.HG)
+      sh.l[tid] = l;
+      if (ok && tid < p.HG && !p.cl)
         write_lse(p, b, g, s, tid, l > 0.f ? (sh.m[tid] + log2f(l)) * 0.69314718055994531f : -INFINITY);
     }
     if (tid == 0) sh.done_ok = ok ? 1 : 0;
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (sh.done_ok) {
+  if (p.cl) {
+    cluster_merge<kN>(p, sh, ring, qs, tmem, b, g, nt > 0 && sh.done_ok, p.TC, NMT);
+  } else if (sh.done_ok) {
     // ---- O^T / l, written by all eight warps: warp w reads TMEM lane quarter
     // w & 3 (value channels) and every other 16-head column group from w >> 2
     tc::fence_after_sync();
@@ -803,15 +940,20 @@ AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, in
   if (S < 1) S = 1;
   if (S > kMaxSplits) S = kMaxSplits;
   if (S > tiles) S = tiles;
-  // whole tiles per split: a masked slot costs the gather as much as a live one
+  // whole tiles per split: a ring item's time is set by the gather latency,
+  // not by its live rows, so a partly masked tile costs about a full one
   const int64_t tps = (tiles + S - 1) / S;
   pl.sps = tps * kKeys;
   pl.S = static_cast<int>((tiles + tps - 1) / tps);
+  pl.cl = pl.S >= 2 && pl.S <= kMaxCl ? 1 : 0;
   const int NSL = static_cast<int>(Dqk / 64), NMT = static_cast<int>(Dv / 128);
   const int tc_fit = 512 / pl.N - NMT;  // TMEM columns left for S^T tiles
   pl.TC = tc_fit < kMaxTC ? tc_fit : kMaxTC;
+  // the Q / P^T region also holds the merge's per-warp transpose buffers
   const size_t q_bytes = static_cast<size_t>(NSL) * pl.N * 128, p_bytes = 2 * 2 * pl.N * 128;
-  pl.smem = static_cast<size_t>(kRing) * kPairBytes + (q_bytes > p_bytes ? q_bytes : p_bytes) + 1024;
+  size_t region = q_bytes > p_bytes ? q_bytes : p_bytes;
+  if (region < kMergeScratch) region = kMergeScratch;
+  pl.smem = static_cast<size_t>(kRing) * kPairBytes + region + 1024;
   // keep co-resident CTAs within the SM's 512 TMEM columns
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>((pl.TC + NMT) * pl.N)) cols <<= 1;
@@ -825,7 +967,7 @@ AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, in
 
 size_t attn_workspace_bytes(const AttnPlan& pl, int64_t B, int64_t Hq, int64_t Dv) {
   size_t bytes = kWsHeader;
-  if (pl.S > 1) {
+  if (pl.S > 1 && !pl.cl) {
     bytes += (static_cast<size_t>(B) * pl.S * Hq * Dv * 4 + 255) & ~size_t(255);
     bytes += (static_cast<size_t>(B) * pl.S * Hq * 4 + 255) & ~size_t(255);
   }
@@ -860,6 +1002,7 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.lse = a.lse;
   p.status = status;
   p.early = a.only_idx_pending ? 1 : 0;
+  p.cl = pl.cl;
   char* w = static_cast<char*>(ws) + kWsHeader;
   p.po = reinterpret_cast<float*>(w);
   p.plse = reinterpret_cast<float*>(
@@ -869,8 +1012,9 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(pl.smem));
   if (e != cudaSuccess) return e;
-  e = launch_k(kernel, dim3(grid), dim3(kThreads), pl.smem, stream, pdl, p);
-  if (e != cudaSuccess || pl.S == 1) return e;
+  e = launch_kc(kernel, dim3(grid), dim3(kThreads), pl.smem, stream, pdl,
+                static_cast<unsigned>(pl.cl ? pl.S : 0), p);
+  if (e != cudaSuccess || pl.S == 1 || pl.cl) return e;
   const int64_t bh = a.B * a.Hq;
   const int64_t threads = bh * (a.Dv / 8);  // two 16-byte groups each
   return launch_k(attn_combine_kernel, dim3(static_cast<unsigned>((threads + 511) / 512)), dim3(512),

@@ -28,6 +28,61 @@ HSA_DEVINL void set_status(uint32_t* status, uint32_t bit) {
 HSA_DEVINL void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 HSA_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---- thread-block clusters (distributed shared memory)
+
+HSA_DEVINL uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Barrier over every thread of the cluster; orders memory at cluster scope.
+HSA_DEVINL void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Address of the same shared variable in the cluster's CTA `rank`.
+HSA_DEVINL uint32_t map_rank(const void* p, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+HSA_DEVINL uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+HSA_DEVINL uint64_t ld_cluster_u64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+HSA_DEVINL void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+HSA_DEVINL float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+HSA_DEVINL void st_cluster_f32x4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
 // Unpack 8 bf16 (one 16-byte chunk) to fp32.
 HSA_DEVINL void bf16x8_to_f32(const uint4& v, float f[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -100,11 +155,15 @@ struct AttnArgs {
 
 // Launch geometry of the fused attention: HG heads per CTA (N = MMA width),
 // G head groups, S key splits of sps attended slots each, TC tiles per chunk
-// (S^T accumulators held in TMEM at once), dynamic shared memory.
+// (S^T accumulators held in TMEM at once), dynamic shared memory.  With cl,
+// the S splits of a (token, head group) form one thread-block cluster and
+// merge their partial outputs through distributed shared memory (no combine
+// kernel, no partials in global memory).
 struct AttnPlan {
   int HG, N, G, S, TC;
   int64_t sps;
   size_t smem;
+  int cl;
 };
 
 AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, int64_t extra_slots);

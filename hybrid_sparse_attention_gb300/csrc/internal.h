@@ -24,21 +24,40 @@ hsa_status_t set_error_detail(hsa_status_t s, const char* detail);
 int device_sms();
 
 // Kernel launch; with pdl, the kernel may be scheduled while the previous
-// kernel of the stream is still running (it waits for it in pdl_wait).
+// kernel of the stream is still running (it waits for it in pdl_wait).  With
+// cluster > 0, consecutive groups of `cluster` CTAs (along x) form thread-block
+// clusters (for kernels without a compile-time cluster shape).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                     cudaStream_t stream, bool pdl, Args... args) {
+cudaError_t launch_kc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, bool pdl, unsigned cluster, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, bool pdl, Args... args) {
+  return launch_kc(kernel, grid, block, smem, stream, pdl, 0u, args...);
 }
 
 cudaError_t launch_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,

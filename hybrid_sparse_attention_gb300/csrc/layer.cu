@@ -247,7 +247,8 @@ size_t layer_workspace_bytes(const hsa_layer_desc& d) {
 }
 
 int layer_launch_count(const hsa_layer_desc& d) {
-  int n = 1 + 1 + (layer_attn_plan(d).S > 1 ? 1 : 0);  // append, attention (+ combine)
+  const AttnPlan pl = layer_attn_plan(d);
+  int n = 1 + 1 + (pl.S > 1 && !pl.cl ? 1 : 0);  // append, attention (+ combine)
   if (d.kind == HSA_LAYER_C4)
     n += (d.pool_total_rows > 0 ? 1 : 0) + topk_launch_count(d.pool_total_rows, d.max_pool_rows);
   return n;

@@ -226,8 +226,8 @@ HSA_DEVINL bool named_barrier_or(uint32_t id, uint32_t count, bool pred) {
   return r != 0;
 }
 
-// 16-byte asynchronous global -> shared copy; src_bytes = 0 zero-fills.
-// 16-byte copy to a shared::cta address (bytes past src_bytes are zero-filled).
+// 16-byte asynchronous global -> shared copy to a shared::cta address
+// (bytes past src_bytes are zero-filled).
 HSA_DEVINL void cp_async16_s(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");

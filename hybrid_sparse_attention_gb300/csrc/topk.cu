@@ -370,44 +370,6 @@ constexpr int kClMax = kCl * kClSlice;     // rows up to 32,768
 constexpr int kClList = 2048;              // per-CTA list of composites at or above bin d1
 static_assert(kBins == kCl * kThreads, "each CTA reduces kThreads bins, one per thread");
 
-HSA_DEVINL uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Barrier over every thread of the cluster; orders memory at cluster scope.
-HSA_DEVINL void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
-
-// Address of the same shared variable in the cluster's CTA `rank`.
-HSA_DEVINL uint32_t map_rank(const void* p, uint32_t rank) {
-  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  return r;
-}
-
-HSA_DEVINL uint32_t ld_cluster_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-HSA_DEVINL uint64_t ld_cluster_u64(uint32_t addr) {
-  uint64_t v;
-  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-HSA_DEVINL void st_cluster_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 constexpr size_t kClDynSmem = sizeof(uint64_t) * (2 * kClList + kMaxK);
 
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)

@@ -207,7 +207,10 @@ hsa_status_t hsa_topk_noalloc(const float* scores, const int64_t* offsets, int64
  * [128, 576]; Dv a multiple of 128 in [128, Dqk]; q, swa, extra, out
  * 16-byte aligned.  Workspace: hsa_decode_attn_workspace_size(B, Hq, Dqk, Dv,
  * W, extra_slots) with extra_slots = k (sparse) or max_extra_rows (dense);
- * long slot lists are split across CTAs and merged by a second launch.
+ * long slot lists are split across S CTAs; with 2 <= S <= 4 the splits of a
+ * token form one thread-block cluster and merge in distributed shared memory
+ * (the workspace is then the 256-byte header alone), otherwise their fp32
+ * partials go through the workspace and a second launch merges them.
  * ---------------------------------------------------------------------- */
 size_t hsa_decode_attn_workspace_size(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W,
                                       int64_t extra_slots);

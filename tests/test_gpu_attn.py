@@ -43,7 +43,9 @@ def _compare(got, want):
     o, l = got
     ro, rl = want
     err = np.abs(o - ro).max() if o.size else 0.0
-    assert err <= OUT_TOL, f"max abs err {err:.3e}"
+    if err > OUT_TOL:
+        at = np.unravel_index(np.argmax(np.abs(o - ro)), o.shape)
+        raise AssertionError(f"max abs err {err:.3e} at {at}: got {o[at]:.6f} want {ro[at]:.6f}")
     fin = np.isfinite(rl)
     assert np.array_equal(np.isneginf(l), np.isneginf(rl))
     if fin.any():
@@ -138,6 +140,51 @@ def test_attention_rescale_path(oracle_mod):
     extra = (extra.float() * ramp).to(torch.bfloat16)
     L[1] = 0                                     # no window: tile 0 = compressed rows only
     idx[1, :200] = -1                            # ... whose first 128 slots are all masked
+    scale = 1 / math.sqrt(576)
+    got = _run(q, swa, L, extra, offs, idx, scale, 512, out_dtype=torch.float32)
+    _compare(got, _oracle(oracle_mod, q, swa, L, extra, offs, idx, scale, 512))
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("splits", [2, 3, 4])
+def test_attention_cluster_merge_dense(oracle_mod, splits):
+    """Dense lists of at most 896 rows (8 tiles with the 128-row window): with
+    B = SMs // splits, the splits of a token form one thread-block cluster and
+    merge in shared memory (no partials in global memory: the workspace is the
+    header alone); short sequences leave their later splits empty."""
+    B = _sms() // splits
+    base_c = [896, 0, 5, 300, 700, 129, 896, 64]
+    base_l = [896 * 128 + 5, 3, 64, 300 * 128, 128000, 130, 896 * 128 + 127, 0]
+    counts = [base_c[i % 8] for i in range(B)]
+    Ls = [base_l[i % 8] for i in range(B)]
+    assert _lib.hsa_decode_attn_workspace_size(B, 64, 576, 512, 128, 896) == 256
+    q, swa, L, extra, offs, _ = _tiny_case(B, 64, 576, 512, 128, 1, counts, Ls, f"cl{splits}")
+    scale = 1 / math.sqrt(576)
+    want = _oracle(oracle_mod, q, swa, L, extra, offs, None, scale, 512)
+    _compare(_run(q, swa, L, extra, offs, None, scale, 512, max_rows=896, out_dtype=torch.float32), want)
+
+
+def test_attention_cluster_merge_sparse_rescale(oracle_mod):
+    """Top-512 lists (5 tiles with the window) at B = SMs // 2: two splits per
+    token merged in their cluster; ragged and padded lists, a hole, repeated
+    entries, a token whose first tile is entirely masked, and rope logits that
+    grow along the pool (the running maximum moves and O^T is rescaled)."""
+    B = _sms() // 2
+    base_c = [2000, 100, 0, 5000, 513, 1, 900, 900]
+    base_l = [8003, 40, 1, 130000, 128, 3, 5000, 0]
+    counts = [base_c[i % 8] for i in range(B)]
+    Ls = [base_l[i % 8] for i in range(B)]
+    assert _lib.hsa_decode_attn_workspace_size(B, 64, 576, 512, 128, 512) == 256
+    q, swa, L, extra, offs, idx = _tiny_case(B, 64, 576, 512, 128, 512, counts, Ls, "clsp")
+    ramp = torch.ones(extra.shape[0], 576)
+    ramp[:, 512:] = torch.linspace(0.5, 40.0, extra.shape[0])[:, None]
+    extra = (extra.float() * ramp).to(torch.bfloat16)
+    idx[0, 7] = -1
+    idx[3, 100:110] = idx[3, 0]
+    idx[7, :200] = -1          # no window (L = 0): the first 128 slots are all masked
     scale = 1 / math.sqrt(576)
     got = _run(q, swa, L, extra, offs, idx, scale, 512, out_dtype=torch.float32)
     _compare(got, _oracle(oracle_mod, q, swa, L, extra, offs, idx, scale, 512))
