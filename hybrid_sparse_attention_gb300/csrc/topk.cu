@@ -291,7 +291,7 @@ HSA_DEVINL uint32_t rank_desc(const uint64_t* a, int n, uint64_t* s_run, uint64_
   __syncthreads();
   uint32_t rank = 0;
 #pragma unroll
-  for (int s = 0; s < kWarps; ++s) {
+  for (int s = 0; s < kWarps; ++s) {  // unrolled: the 16 searches overlap their load latencies
     const uint64_t* r = s_run + 32 * s;
     uint32_t c = 0;
 #pragma unroll
@@ -355,7 +355,7 @@ HSA_DEVINL void select_rest(const uint64_t* cand, uint32_t n, uint32_t need, uin
 //
 // Rows of at most kClMax scores (every C4 row up to a 128K context) take one
 // launch: a thread-block cluster of kCl CTAs per row, each holding an equal
-// slice of the row (at most kClSlice scores) in registers.  The CTAs' digit-1 histograms are summed
+// slice of the row (at most kClSlice scores) in shared memory.  The CTAs' digit-1 histograms are summed
 // through distributed shared memory (each CTA reduces a quarter of the bins
 // and broadcasts it), so every CTA finds d1 itself; each CTA then compacts
 // its keys at or above bin d1 into shared memory, CTA 0 gathers the lists,
@@ -364,13 +364,22 @@ HSA_DEVINL void select_rest(const uint64_t* cand, uint32_t n, uint32_t need, uin
 // candidates through the workspace instead.
 
 constexpr int kCl = 4;                     // CTAs per row (one cluster)
-constexpr int kClU = 16;                   // scores per thread, held in registers
+constexpr int kClU = 16;                   // scores per thread (rounds over the slice)
 constexpr int kClSlice = kThreads * kClU;  // 8,192 scores per CTA
 constexpr int kClMax = kCl * kClSlice;     // rows up to 32,768
 constexpr int kClList = 2048;              // per-CTA list of composites at or above bin d1
 static_assert(kBins == kCl * kThreads, "each CTA reduces kThreads bins, one per thread");
+static_assert(kCl == 4, "the list gather selects among four prefix counts");
 
-constexpr size_t kClDynSmem = sizeof(uint64_t) * (2 * kClList + kMaxK);
+constexpr size_t kClDynSmem = sizeof(uint64_t) * (2 * kClList + kMaxK) + sizeof(uint32_t) * kClSlice;
+
+// 4-byte asynchronous copy global -> shared (any 4-byte-aligned score).
+HSA_DEVINL void cp_async4(uint32_t* dst, const uint32_t* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
 
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
     topk_cluster_kernel(const float* __restrict__ scores, Spans sp, int k, Ws ws,
@@ -381,9 +390,10 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   uint64_t* s_loc = s_dyn;                // [kClList] this CTA's composites at or above bin d1
   uint64_t* s_sel = s_loc + kClList;      // [kMaxK] CTA 0: winners, then every survivor
   uint64_t* s_cand = s_sel + kMaxK;       // [kClList] CTA 0: candidates (bin d1); sort runs
-  __shared__ uint32_t s_scan[33], s_out[2], s_wt[kWarps], s_nloc, s_count, s_ccount;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const uint32_t lt = (1u << lane) - 1u;
+  // [kClSlice] this CTA's slice: score bits, then order keys
+  uint32_t* s_key = reinterpret_cast<uint32_t*>(s_cand + kClList);
+  __shared__ uint32_t s_scan[33], s_out[2], s_nloc, s_count, s_ccount;
+  const int t = threadIdx.x;
   const uint32_t rank = cluster_rank();
   const int row = static_cast<int>(blockIdx.x) / kCl;
   const bool valid = sp.valid(row);
@@ -410,21 +420,25 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   // previous kernel); the scores need the wait
   pdl_wait();
   pdl_trigger();
-  uint32_t key[kClU];
+  // The slice goes to shared memory with every copy in flight at once; the
+  // passes over it below are rolled loops (this code runs once per launch,
+  // so its instruction fetches cost more than loop overhead).
+  const int m = s1 > s0 ? s1 - s0 : 0;
+  const uint32_t* src = base + s0;
+#pragma unroll 1
+  for (int i = t; i < m; i += kThreads) cp_async4(s_key + i, src + i);
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
   bool nan = false;
-#pragma unroll
-  for (int u = 0; u < kClU; ++u) {
-    const int j = s0 + u * kThreads + t;
-    const uint32_t v = j < s1 ? __ldcg(base + j) : 0u;
+#pragma unroll 1
+  for (int i = t; i < m; i += kThreads) {
+    const uint32_t v = s_key[i];
     nan |= is_nan_bits(v);
-    key[u] = order_key(v);
+    const uint32_t key = order_key(v);
+    s_key[i] = key;
+    if (!all) atomicAdd(&s_hist[key >> kShift1], 1u);
   }
   if (nan) set_status(ws.status, HSA_DEV_NAN);
-  if (!all) {
-#pragma unroll
-    for (int u = 0; u < kClU; ++u)
-      if (s0 + u * kThreads + t < s1) atomicAdd(&s_hist[key[u] >> kShift1], 1u);
-  }
   cluster_sync();  // every CTA's histogram is complete (and every CTA is running)
   {
     // reduce bin `bin` over the cluster, then broadcast the sum to every CTA
@@ -445,67 +459,60 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   const bool heavy = !all && above1 + in1 > static_cast<uint32_t>(kClList);
   RowState* rs = ws.rows + row;
   {
-    // compact: ballots count per warp, one scan over warps, no atomics
-    auto taken = [&](int u) {
-      const uint32_t dig = key[u] >> kShift1;
-      return s0 + u * kThreads + t < s1 && (all || dig > d1 || (!heavy && dig == d1));
+    // compact: each thread counts its kept keys, one block scan gives every
+    // thread its place, no atomics
+    auto taken = [&](uint32_t key) {
+      const uint32_t dig = key >> kShift1;
+      return all || dig > d1 || (!heavy && dig == d1);
     };
-    uint32_t tot = 0;
-#pragma unroll
-    for (int u = 0; u < kClU; ++u) tot += __popc(__ballot_sync(0xffffffffu, taken(u)));
-    if (lane == 0) s_wt[warp] = tot;
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t c = lane < kWarps ? s_wt[lane] : 0u;
-      uint32_t incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+    uint32_t cnt = 0;
+#pragma unroll 4
+    for (int i = t; i < m; i += kThreads) cnt += taken(s_key[i]) ? 1u : 0u;
+    uint32_t nloc;
+    uint32_t pos = block_inclusive_sum<uint32_t>(cnt, s_scan, &nloc) - cnt;
+    if (t == 0) s_nloc = nloc;
+#pragma unroll 4
+    for (int i = t; i < m; i += kThreads) {
+      const uint32_t key = s_key[i];
+      if (taken(key)) {
+        if (pos < static_cast<uint32_t>(kClList)) s_loc[pos] = composite(key, static_cast<uint32_t>(s0 + i));
+        ++pos;
       }
-      if (lane < kWarps) s_wt[lane] = incl - c;
-      if (lane == 31) s_nloc = incl;
-    }
-    __syncthreads();
-    uint32_t p = s_wt[warp];
-#pragma unroll
-    for (int u = 0; u < kClU; ++u) {
-      const uint32_t m = __ballot_sync(0xffffffffu, taken(u));  // recomputed: saves registers
-      if (m >> lane & 1u) {
-        const uint32_t q = p + __popc(m & lt);
-        if (q < static_cast<uint32_t>(kClList))
-          s_loc[q] = composite(key[u], static_cast<uint32_t>(s0 + u * kThreads + t));
-      }
-      p += __popc(m);
     }
     if (heavy) {
-#pragma unroll
-      for (int u = 0; u < kClU; ++u) {
-        const int j = s0 + u * kThreads + t;
-        const bool c = j < s1 && (key[u] >> kShift1) == d1;
+#pragma unroll 1
+      for (int i = t; i < kClSlice; i += kThreads) {
+        const bool c = i < m && (s_key[i] >> kShift1) == d1;
         const uint32_t q = warp_append(&rs->n_cand, c, 0xffffffffu);
-        if (c) ws.cand[off + q] = composite(key[u], static_cast<uint32_t>(j));
+        if (c) ws.cand[off + q] = composite(s_key[i], static_cast<uint32_t>(s0 + i));
       }
       __threadfence();
     }
   }
   cluster_sync();  // every CTA's list is complete
   if (rank == 0) {
-    // gather the lists: winners to s_sel, candidates to s_cand
+    // gather the lists (all of them at once): winners to s_sel, candidates to s_cand
+    uint32_t pre[kCl + 1];
+    pre[0] = 0;
+#pragma unroll
     for (int q = 0; q < kCl; ++q) {
       const uint32_t nq = ld_cluster_u32(map_rank(&s_nloc, q));
-      const uint32_t nqc = nq < static_cast<uint32_t>(kClList) ? nq : kClList;
-      const uint32_t src = map_rank(&s_loc[0], q);
-      for (uint32_t i0 = 0; i0 < nqc; i0 += kThreads) {
-        const uint32_t i = i0 + t;
-        const uint64_t x = i < nqc ? ld_cluster_u64(src + 8u * i) : 0ull;
-        const uint32_t dig = static_cast<uint32_t>(x >> (32 + kShift1));
-        const bool w = i < nqc && (all || dig > d1), c = i < nqc && !all && dig == d1;
-        const uint32_t pw = warp_append(&s_count, w, 0xffffffffu);
-        if (w && pw < static_cast<uint32_t>(kMaxK)) s_sel[pw] = x;
-        const uint32_t pc = warp_append(&s_ccount, c, 0xffffffffu);
-        if (c && pc < static_cast<uint32_t>(kClList)) s_cand[pc] = x;
-      }
+      pre[q + 1] = pre[q] + (nq < static_cast<uint32_t>(kClList) ? nq : kClList);
+    }
+    for (uint32_t i0 = 0; i0 < pre[kCl]; i0 += kThreads) {
+      const uint32_t i = i0 + t;
+      const bool v = i < pre[kCl];
+      uint32_t q = 0;
+#pragma unroll
+      for (int r = 1; r < kCl; ++r) q += i >= pre[r] ? 1u : 0u;
+      const uint32_t first = q == 0 ? 0u : (q == 1 ? pre[1] : (q == 2 ? pre[2] : pre[3]));
+      const uint64_t x = v ? ld_cluster_u64(map_rank(&s_loc[i - first], q)) : 0ull;
+      const uint32_t dig = static_cast<uint32_t>(x >> (32 + kShift1));
+      const bool w = v && (all || dig > d1), c = v && !all && dig == d1;
+      const uint32_t pw = warp_append(&s_count, w, 0xffffffffu);
+      if (w && pw < static_cast<uint32_t>(kMaxK)) s_sel[pw] = x;
+      const uint32_t pc = warp_append(&s_ccount, c, 0xffffffffu);
+      if (c && pc < static_cast<uint32_t>(kClList)) s_cand[pc] = x;
     }
   }
   cluster_sync();  // CTA 0 has read every list: the other CTAs may leave
