@@ -436,7 +436,7 @@ def run_hsa(args, world, rank, local, dist):
                    "achieved_gbs": nbytes[key] / (stage_mean[j] * 1e-3) / 1e9,
                    "frac": nbytes[key] / (stage_mean[j] * 1e-3) / 1e9 / peak}
             for name, key, j in (("indexer", "indexer", 1), ("topk", "topk", 2),
-                                 ("attention (+ split combine)", "attention", 3))},
+                                 ("attention (+ split merge)", "attention", 3))},
         "stage_us": {"append_compress": stage_mean[0] * 1000, "indexer": stage_mean[1] * 1000,
                      "topk": stage_mean[2] * 1000, "attention": stage_mean[3] * 1000},
         "cpu_baseline": cpu,

@@ -34,8 +34,10 @@
 //    against P^T, which the softmax warps write tile by tile.  Across chunks
 //    the running maximum moves lazily (only by more than 2^8; O^T is then
 //    rescaled in TMEM).
-//  * Long key lists are split over CTAs; each split writes an fp32 partial
-//    output and log-sum-exp that a combine kernel merges.
+//  * Long key lists are split over CTAs.  Two to four splits of a token form
+//    one thread-block cluster and merge through distributed shared memory;
+//    with more, each split writes an fp32 partial output and log-sum-exp that
+//    a combine kernel merges.
 #include <math.h>
 
 #include "common.cuh"
