@@ -29,11 +29,11 @@
 //  * A token's slots are split over S CTAs in whole 128-slot tiles.
 //  * Two passes per chunk of up to four 128-slot tiles: pass 1 streams all
 //    Dqk channels of the chunk's tiles into S^T accumulators (one per tile,
-//    in TMEM); the softmax warps then take the exact maximum over the chunk,
-//    and pass 2 streams the value channels again (now from L2) into O^T
-//    against P^T, which the softmax warps write tile by tile.  Across chunks
-//    the running maximum moves lazily (only by more than 2^8; O^T is then
-//    rescaled in TMEM).
+//    in TMEM); as each tile's S^T lands the softmax warps fold its maximum
+//    into the running maximum and write its P^T (online softmax; the running
+//    maximum moves lazily, only by more than 2^8, and O^T and l are then
+//    rescaled), and pass 2 streams the value channels again (now from L2)
+//    into O^T against P^T.
 //  * Long key lists are split over CTAs.  Two to four splits of a token form
 //    one thread-block cluster and merge through distributed shared memory;
 //    with more, each split writes an fp32 partial output and log-sum-exp that
@@ -62,6 +62,16 @@ constexpr int kMaxCl = 4;           // splits merged inside one cluster
 constexpr uint32_t kUnitBytes = kKeys * 16 * 4;  // one merge unit: 128 lanes x 16 fp32 columns
 static_assert(16 * kUnitBytes <= kRing * kPairBytes, "a split's O^T units fit its ring");
 constexpr size_t kMergeScratch = 8 * 16 * 32 * 4;  // eight warps' 16 x 32 fp32 transpose tiles
+
+// Dynamic shared memory after the ring: the Q region (Q during pass 1; then
+// the odd tiles' P^T buffer; at the end the merge's transpose tiles), then the
+// even tiles' P^T buffer, which is never part of Q (it is written while the
+// chunk's pass 1 may still read Q).
+__host__ __device__ inline uint32_t attn_q_region(int NSL, int N) {
+  const uint32_t q = static_cast<uint32_t>(NSL) * N * 128, pb = 2u * N * 128;
+  uint32_t r = q > pb ? q : pb;
+  return r > kMergeScratch ? r : static_cast<uint32_t>(kMergeScratch);
+}
 
 struct AttnParams {
   const uint16_t* q;      // [B, Hq, Dqk]
@@ -402,10 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t qslice = kN * 128;       // bytes of one Q slice (kN heads x 64 channels)
-  const uint32_t pbytes = 2 * kN * 128;   // one P^T buffer (2 K-blocks of 64 keys)
   uint8_t* ring = smem;
   uint8_t* qs = ring + kRing * kPairBytes;  // Q during pass 1 ...
-  uint8_t* pt = qs;                         // ... and the P^T buffers during pass 2
+  // P^T buffers (2 K-blocks of 64 keys x kN heads each): tile gt uses buffer
+  // gt & 1; buffer 1 is the start of the Q region, written only once the
+  // chunk's pass 1 is complete
+  uint8_t* const pbuf0 = qs + attn_q_region(NSL, kN);
+  uint8_t* const pbuf1 = qs;
   // TMEM columns: S^T of chunk tile tc at tc*kN; O^T M-tile m at (TC + m)*kN
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>((TC + NMT) * kN)) tmem_cols <<= 1;
@@ -626,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
             break;
           }
           tc::fence_after_sync();
-          const uint32_t pa = tc::smem_u32(pt + buf * pbytes);
+          const uint32_t pa = tc::smem_u32(buf ? pbuf1 : pbuf0);
           for (int m = 0; m < NMT; ++m, ++item) {
             const int slot = static_cast<int>(item % kRing);
             if (!wait_or_abort(sh, &sh.full[slot], static_cast<uint32_t>((item / kRing) & 1),
@@ -685,11 +698,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         vmask |= (slot >= a0 && slot < a1 && slot_row(p, b, geo, slot, false) != nullptr ? 1u : 0u)
                  << tc_;
       }
-      // ---- the chunk's maximum per head, each tile folded in as soon as its S^T lands
-      float run[kGroups];
-#pragma unroll
-      for (int gi = 0; gi < kGroups; ++gi) run[gi] = -INFINITY;
-      for (int tc_ = 0; tc_ < nct && ok; ++tc_) {
+      // ---- tile by tile, as soon as its S^T lands (online softmax): the tile's
+      // maximum per head moves the running maximum m only when it rises by more
+      // than 2^8 (O^T and l are then rescaled); P^T = 2^(S^T - m) goes to the
+      // buffer its O^T pass reads, so the first tiles' P^T is ready before the
+      // chunk's last S^T
+      for (int tc_ = 0; tc_ < nct; ++tc_, ++gt) {
         if (!agree(!wait_or_abort(sh, &sh.s_full[tc_], c & 1, p.status))) {
           ok = false;
           break;
@@ -701,54 +715,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         for (int gi = 0; gi < kGroups; ++gi) {
           float x[32];
           load_s(tc_ * kN + gi * 32, valid, x);
-          run[gi] = fmaxf(run[gi], warp_transpose_reduce32<true>(x));
+          const float mcol = warp_transpose_reduce32<true>(x);
+          if (gi * 32 + lane < kN) sh.red[warp][gi * 32 + lane] = mcol;
         }
-      }
-      if (!ok) break;
+        tc::named_barrier(1, kKeys);
+        bool rescale = false;  // O^T holds earlier tiles weighted by a finite old maximum
+        if (tid < kN) {
+          const float mt =
+              fmaxf(fmaxf(sh.red[0][tid], sh.red[1][tid]), fmaxf(sh.red[2][tid], sh.red[3][tid]));
+          const float mo = sh.m[tid];
+          const float mn = fmaxf(mo, mt);
+          const bool moved = mn > mo + kRescaleLog2 || (mo == -INFINITY && mn > -INFINITY);
+          sh.alpha[tid] = moved ? exp2f(mo - mn) : 1.f;
+          if (moved) sh.m[tid] = mn;
+          rescale = moved && mo > -INFINITY;
+        }
+        if (tc::named_barrier_or(1, kKeys, rescale)) {
 #pragma unroll
-      for (int gi = 0; gi < kGroups; ++gi)
-        if (gi * 32 + lane < kN) sh.red[warp][gi * 32 + lane] = run[gi];
-      tc::named_barrier(1, kKeys);
-      bool moved = false;
-      if (tid < kN) {
-        const float mt =
-            fmaxf(fmaxf(sh.red[0][tid], sh.red[1][tid]), fmaxf(sh.red[2][tid], sh.red[3][tid]));
-        const float mo = sh.m[tid];
-        const float mn = fmaxf(mo, mt);
-        moved = mn > mo + kRescaleLog2 || (mo == -INFINITY && mn > -INFINITY);
-        sh.alpha[tid] = moved ? exp2f(mo - mn) : 1.f;
-        if (moved) sh.m[tid] = mn;
-      }
-      if (tc::named_barrier_or(1, kKeys, moved)) {
-#pragma unroll
-        for (int h = 0; h < kN; ++h) l_part[h] *= sh.alpha[h];
-        if (gt > 0) {
-          // O^T holds earlier chunks: wait for their last MMAs, then rescale in TMEM
-          const int lt = gt - 1;
-          if (!agree(!wait_or_abort(sh, &sh.o_done[lt & 1], (lt >> 1) & 1, p.status))) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          __syncwarp();
-          for (int m = 0; m < NMT; ++m) {
-            const uint32_t col = tmem + lane_base + (TC + m) * kN;
-#pragma unroll
-            for (int q16 = 0; q16 < kN / 16; ++q16) {
-              uint32_t o[16];
-              tc::tmem_ld16(col + q16 * 16, o);
-              tc::tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                o[i] = __float_as_uint(__uint_as_float(o[i]) * sh.alpha[q16 * 16 + i]);
-              tc::tmem_st16(col + q16 * 16, o);
+          for (int h = 0; h < kN; ++h) l_part[h] *= sh.alpha[h];
+          if (gt > 0) {
+            // wait for the earlier tiles' O^T MMAs, then rescale O^T in TMEM
+            const int lt = gt - 1;
+            if (!agree(!wait_or_abort(sh, &sh.o_done[lt & 1], (lt >> 1) & 1, p.status))) {
+              ok = false;
+              break;
             }
+            tc::fence_after_sync();
+            __syncwarp();
+            for (int m = 0; m < NMT; ++m) {
+              const uint32_t col = tmem + lane_base + (TC + m) * kN;
+#pragma unroll
+              for (int q16 = 0; q16 < kN / 16; ++q16) {
+                uint32_t o[16];
+                tc::tmem_ld16(col + q16 * 16, o);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  o[i] = __float_as_uint(__uint_as_float(o[i]) * sh.alpha[q16 * 16 + i]);
+                tc::tmem_st16(col + q16 * 16, o);
+              }
+            }
+            tc::tmem_st_wait();
           }
-          tc::tmem_st_wait();
         }
-      }
-      // ---- P^T tile by tile (each into the buffer its O^T pass reads)
-      for (int tc_ = 0; tc_ < nct; ++tc_, ++gt) {
+        // (a head whose old maximum was -inf has weighed everything with 0 so far:
+        // its O^T columns and l are 0 and need no rescale)
         const int buf = gt & 1;
         if (gt >= 2) {  // the buffer is free once O^T of tile gt-2 has completed
           const int lt = gt - 2;
@@ -757,8 +768,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
             break;
           }
         }
-        const bool valid = (vmask >> tc_) & 1u;
-        uint8_t* ptb = pt + buf * pbytes + (tid >> 6) * kN * 128;
+        if (buf == 1 && tc_ < nct - 1) {
+          // buffer 1 overlays Q: wait until the chunk's pass 1 has read it for the last time
+          if (!agree(!wait_or_abort(sh, &sh.s_full[nct - 1], c & 1, p.status))) {
+            ok = false;
+            break;
+          }
+        }
+        uint8_t* ptb = (buf ? pbuf1 : pbuf0) + (tid >> 6) * kN * 128;
         const int kc = (tid & 63) >> 3, ke = (tid & 7) << 1;
 #pragma unroll
         for (int gi = 0; gi < kGroups; ++gi) {
@@ -951,11 +968,7 @@ AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, in
   const int NSL = static_cast<int>(Dqk / 64), NMT = static_cast<int>(Dv / 128);
   const int tc_fit = 512 / pl.N - NMT;  // TMEM columns left for S^T tiles
   pl.TC = tc_fit < kMaxTC ? tc_fit : kMaxTC;
-  // the Q / P^T region also holds the merge's per-warp transpose buffers
-  const size_t q_bytes = static_cast<size_t>(NSL) * pl.N * 128, p_bytes = 2 * 2 * pl.N * 128;
-  size_t region = q_bytes > p_bytes ? q_bytes : p_bytes;
-  if (region < kMergeScratch) region = kMergeScratch;
-  pl.smem = static_cast<size_t>(kRing) * kPairBytes + region + 1024;
+  pl.smem = static_cast<size_t>(kRing) * kPairBytes + attn_q_region(NSL, pl.N) + 2 * pl.N * 128 + 1024;
   // keep co-resident CTAs within the SM's 512 TMEM columns
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>((pl.TC + NMT) * pl.N)) cols <<= 1;
