@@ -233,6 +233,7 @@ class LayerDesc(ctypes.Structure):
         ("swa", P), ("kv_ring", P), ("z_ring", P), ("ik_ring", P), ("iz_ring", P),
         ("kv_pool", P), ("key_pool", P), ("q", P), ("iq", P), ("w", P),
         ("out", P), ("lse", P), ("topk_idx", P), ("scores", P), ("stage_events", P),
+        ("q_ready_event", P),
     ]
 
 
@@ -242,7 +243,7 @@ SIGNATURES["hsa_layer_decode"] = (I32, [ctypes.POINTER(LayerDesc), P, SZ, P])
 
 
 def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
-               max_pool_rows=None, stage_events=None) -> LayerDesc:
+               max_pool_rows=None, stage_events=None, q_ready_event=None) -> LayerDesc:
     """Descriptor for one decode step over a synth.LayerState-like object whose
     tensors live on the GPU (argument marshalling only)."""
     sh = st.shape
@@ -288,6 +289,8 @@ def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
         # keep the handle array alive as long as the descriptor
         d._events = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(h) for h in stage_events])
         d.stage_events = ctypes.cast(d._events, ctypes.c_void_p)
+    if q_ready_event is not None:   # a cudaEvent_t handle (torch.cuda.Event.cuda_event)
+        d.q_ready_event = q_ready_event
     # the descriptor holds raw device pointers: keep every tensor behind them
     # alive as long as it is (a temporary passed here would otherwise be freed
     # and its memory handed to another tensor while the library still writes it)

@@ -339,7 +339,14 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   a.out_dtype = d.out_dtype;
   a.lse = d.lse;
   a.only_idx_pending = d.kind == HSA_LAYER_C4;  // C128: the append comes right before
-  e = launch_attn(a, pl, w + L.attn, status, stream, true);
+  bool pdl = true;
+  if (d.q_ready_event) {
+    // q may still be arriving on another stream: the attention waits for it
+    e = cudaStreamWaitEvent(stream, static_cast<cudaEvent_t>(d.q_ready_event), 0);
+    if (e != cudaSuccess) return e;
+    pdl = false;
+  }
+  e = launch_attn(a, pl, w + L.attn, status, stream, pdl);
   if (e != cudaSuccess) return e;
   return mark(4);
 }

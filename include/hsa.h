@@ -290,6 +290,13 @@ typedef struct hsa_layer_desc {
                                  after the top-k and after the attention (C128 records
                                  events 2 and 3 at the same point as event 1).  Kernels
                                  separated by an event do not overlap their launches. */
+  void* q_ready_event;      /* NULL, or a caller-created cudaEvent_t that `stream` waits
+                               for right before the attention kernel, the only reader of
+                               q: q may then still be arriving (e.g. copied from the host
+                               on another stream) while the append, indexer and top-k
+                               run — [KD] §Arquitectura del Sistema (multi-stream overlap).
+                               The attention is then launched without programmatic
+                               dependent launch. */
 } hsa_layer_desc;
 
 size_t hsa_layer_decode_workspace_size(const hsa_layer_desc* d);

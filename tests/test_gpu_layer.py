@@ -174,6 +174,39 @@ def test_layer_step_is_idempotent_with_separate_output_length():
     assert torch.equal(a["seq_len_out"], L.cuda())
 
 
+def test_layer_attention_waits_for_q_ready_event():
+    """q arrives on a side stream after a delay; the layer waits for the event
+    right before the attention (the only reader of q), so the upload overlaps
+    the append, indexer and top-k, and the result equals the step with q
+    resident beforehand."""
+    L = synth.c4_lengths(synth.SEED["c4layer"], 8, 4000, 9000)
+    g = synth.filled_state(synth.SEED["c4layer"], 4, synth.FULL, L, device="cuda", name="qev")
+    ref = run_gpu_step(g)
+    q_host = g.q.cpu().pin_memory()
+    g.q.zero_()
+    B, sh = L.numel(), g.shape
+    out = torch.empty(B, sh.Hq, sh.Dv, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, sh.Hq, dtype=torch.float32, device="cuda")
+    so = torch.empty_like(g.seq_len_in)
+    idx = torch.empty(B, sh.k, dtype=torch.int32, device="cuda")
+    scores = torch.zeros(g.kv_pool.shape[0], dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    ready = torch.cuda.Event()
+    ready.record(side)                    # the event exists before its handle is taken
+    desc = _lib.layer_desc(g, out, lse, so, topk_idx=idx, scores=scores,
+                           q_ready_event=ready.cuda_event)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(2_000_000)      # about a millisecond: q lands after the top-k
+        g.q.copy_(q_host, non_blocking=True)
+        ready.record(side)
+    ws = _lib.hsa_layer_decode(desc)
+    torch.cuda.synchronize()
+    assert _lib.hsa_workspace_status(ws) == 0
+    assert torch.equal(out, ref["out"]) and torch.equal(lse, ref["lse"])
+    assert torch.equal(idx, ref["idx"])
+
+
 def test_layer_c4_full_128k_batch64(oracle_mod):
     """The headline workload: batch 64, contexts U[16384, 131072], 64 heads x
     576, indexer 8 x 128, top-512, window 128; every stage against the oracle."""
