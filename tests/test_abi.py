@@ -75,3 +75,19 @@ def test_host_validation_rejects_before_launch(lib):
     assert b"16-byte" in lib.hsa_last_error_detail()
     # empty work is a successful no-op that touches nothing
     assert _rc("hsa_compress", None, None, None, 0, 8, 16, 4, None, 1, None) == 0
+
+
+def test_layer_desc_binding_matches_header():
+    """The ctypes descriptor lists hsa_layer_desc's fields in the header's order."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct hsa_layer_desc \{(.*?)\} hsa_layer_desc;", text, re.S).group(1)
+    names = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        # "int32_t B, Hq, Dqk, Dv" or "const void* const* stage_events" -> field names
+        head, *rest = [d.strip() for d in decl.split(",")]
+        names.append(re.findall(r"[A-Za-z_][A-Za-z0-9_]*", head)[-1])
+        names.extend(rest)
+    assert [f[0] for f in _lib.LayerDesc._fields_] == names
