@@ -45,6 +45,7 @@ struct IndexerParams {
   int B, Hi, Di;
   float* scores;
   uint32_t* status;
+  int wait_mode;   // programmatic dependent launch: see launch_indexer in internal.h
 };
 
 struct Shared {
@@ -86,6 +87,15 @@ struct SeqCursor {
     count = p.sp.count(b);
     next = first + static_cast<int>((count + kTileRows - 1) / kTileRows);
   }
+  // Tile of the current sequence holding a row the previous kernel may have
+  // just written, or -1: the last live row, when the new length completes a
+  // block (the lengths here are the ones after the previous kernel).
+  HSA_DEVINL int appended_tile(const IndexerParams& p) const {
+    if (!p.sp.seq_len || count <= 0) return -1;
+    const int64_t L = static_cast<int64_t>(p.sp.seq_len[b]) + p.sp.add;
+    if (L % p.sp.ratio != 0) return -1;
+    return first + static_cast<int>((count - 1) / kTileRows);
+  }
   HSA_DEVINL bool seek(const Shared& sh, const IndexerParams& p, int t) {
     if (b >= 0 && t < next) return false;
     if (b < 0) {
@@ -108,9 +118,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Programmatic dependent launch: the prologue (tile table, barriers, TMEM)
-  // needs nothing the previous kernel writes; the TMA producer waits before
-  // its first key load (the append may have written a new compressed key).
+  // Programmatic dependent launch (wait_mode): 0 every thread waits first;
+  // otherwise the prologue (tile table, barriers, TMEM) needs nothing the
+  // previous kernel writes and only the TMA producer waits — before its first
+  // key load (1), or right before the first tile holding a key the previous
+  // kernel may have written, after triggering the next kernel (2).
+  if (p.wait_mode == 0) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   const int kb_elems = p.Di >= 64 ? 64 : p.Di;  // elements of one swizzle row
   const int nkb = p.Di / kb_elems;
@@ -142,7 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
   const int ntiles = sh.ntiles;
   const int t_begin = static_cast<int>(static_cast<int64_t>(ntiles) * blockIdx.x / gridDim.x);
   const int t_end = static_cast<int>(static_cast<int64_t>(ntiles) * (blockIdx.x + 1) / gridDim.x);
-  if (t_begin >= t_end) return;
+  if (t_begin >= t_end) {
+    if (p.wait_mode != 0 && threadIdx.x == 0) pdl_wait();  // complete only after the previous kernel
+    return;
+  }
   if (threadIdx.x == 0) {
     int lo = 0, hi = p.B - 1;  // largest b with prefix[b] <= t_begin
     while (lo < hi) {
@@ -181,12 +200,22 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
     if (lane == 0) {
       tc::tma_prefetch_map(&kmap);
       tc::tma_prefetch_map(&qmap);
-      pdl_wait();
+      bool waited = p.wait_mode == 0;
+      if (p.wait_mode == 1) {
+        pdl_wait();
+        waited = true;
+      }
       pdl_trigger();
       SeqCursor cur;
+      int dep = -1;  // (wait_mode 2) tile that must wait for the previous kernel
       for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
         const int s = i % kStages;
-        cur.seek(sh, p, t);  // before the wait: a new sequence's loads overlap it
+        // before the wait: a new sequence's loads overlap it
+        if (cur.seek(sh, p, t) && !waited) dep = cur.appended_tile(p);
+        if (!waited && t == dep) {
+          pdl_wait();
+          waited = true;
+        }
         if (i >= kStages &&
             !wait_or_abort(sh, &sh.empty[s], ((i / kStages) & 1) ^ 1, p.status))
           break;
@@ -201,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
                           &sh.full[s]);
         }
       }
+      if (!waited) pdl_wait();  // the grid completes only after the previous kernel
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -290,7 +320,7 @@ size_t indexer_smem_bytes(int Di) {
 
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
-                           cudaStream_t stream, bool pdl) {
+                           cudaStream_t stream, bool pdl, int wait_mode) {
   if (total_rows == 0) return cudaSuccess;
   if (B > kMaxSeqs) return cudaErrorInvalidValue;
   const int kb_elems = Di >= 64 ? 64 : Di;
@@ -307,7 +337,7 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
   // persistent: one CTA per SM (fewer when there are fewer tiles)
   const int64_t tiles_bound = (total_rows + kTileRows - 1) / kTileRows + B;
   const int grid = static_cast<int>(tiles_bound < device_sms() ? tiles_bound : device_sms());
-  IndexerParams p{w, sp, B, Hi, Di, scores, status};
+  IndexerParams p{w, sp, B, Hi, Di, scores, status, pdl ? wait_mode : 0};
   return launch_k(indexer_kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, kmap, qmap, p);
 }
 

@@ -68,9 +68,16 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner,
                               int box_inner, int box_outer, CUtensorMapSwizzle swizzle);
 
 size_t indexer_smem_bytes(int Di);
+// With pdl, wait_mode says where the kernel waits for the previous one: 0
+// every thread at the start; 1 the loads (the tile table is built before,
+// from sp, which the previous kernel must not write); 2 only the loads of a
+// tile holding a row the previous kernel may have written (the last live row
+// of a sequence whose length, per sp, completes a block), the next kernel
+// being triggered first (it must read nothing the previous kernel writes
+// before its own wait).
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
-                           cudaStream_t stream, bool pdl = false);
+                           cudaStream_t stream, bool pdl = false, int wait_mode = 0);
 
 size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k);
 // Leading bytes of a top-k workspace (status word, row states, histograms)

@@ -303,15 +303,20 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   if (d.kind == HSA_LAYER_C4) {
     float* scores = d.scores ? d.scores : reinterpret_cast<float*>(w + L.scores);
     int32_t* tidx = d.topk_idx ? d.topk_idx : reinterpret_cast<int32_t*>(w + L.idx);
-    // the lengths after the append are the ones before it plus one: the
-    // indexer's tile table can be built before the append has finished
+    // The lengths after the append are the ones before it plus one, so the
+    // indexer and the top-k can read their row geometry before the append has
+    // finished, and the indexer streams every key the append cannot have
+    // written (all but a completed block's new row) while it runs.  When the
+    // output lengths overwrite the input ones, the geometry is read from the
+    // output lengths after the append instead.
+    const bool alias = d.seq_len_out == d.seq_len_in;
     const Spans sp_in{d.pool_offsets, d.seq_len_in, 1, r, d.pool_total_rows};
-    e = launch_indexer(d.iq, d.w, d.key_pool, sp_in, d.B, d.Hi, d.Di, d.pool_total_rows, scores,
-                       status, stream, true);
+    e = launch_indexer(d.iq, d.w, d.key_pool, alias ? sp : sp_in, d.B, d.Hi, d.Di,
+                       d.pool_total_rows, scores, status, stream, true, alias ? 0 : 2);
     if (e != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
-    e = launch_topk(scores, sp, d.B, d.pool_total_rows, d.k, tidx, nullptr, w + L.topk, status,
-                    stream, d.max_pool_rows, true);
+    e = launch_topk(scores, alias ? sp : sp_in, d.B, d.pool_total_rows, d.k, tidx, nullptr,
+                    w + L.topk, status, stream, d.max_pool_rows, true);
     if (e != cudaSuccess) return e;
     if ((e = mark(3)) != cudaSuccess) return e;
     idx = tidx;
