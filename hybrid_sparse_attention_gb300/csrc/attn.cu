@@ -24,8 +24,9 @@
 //    slices of 128 rows each, 128-byte swizzled, 16 KB apart = the MN-major
 //    leading-byte offset), filled by three gather warps with 16-byte
 //    cp.async (each keeps up to two of its items in flight) and drained by
-//    one MMA-issuing thread.  Q (needed by pass 1 only) and the P^T buffers
-//    (pass 2 only) share one region.
+//    one MMA-issuing thread.  Q (needed by pass 1 only) shares its region
+//    with the odd tiles' P^T buffer; the even tiles' P^T buffer has its own
+//    (it is written while the chunk's pass 1 may still read Q).
 //  * A token's slots are split over S CTAs in whole 128-slot tiles.
 //  * Two passes per chunk of up to four 128-slot tiles: pass 1 streams all
 //    Dqk channels of the chunk's tiles into S^T accumulators (one per tile,
