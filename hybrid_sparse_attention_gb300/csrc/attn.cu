@@ -550,6 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         const int nit = pass == 0 ? NP1 : NMT;
         for (int tc_ = 0; tc_ < nct; ++tc_) {
           const uint16_t* const* table = sh.rows[tc_];
+          // this lane's rows r0 + 4k of the tile, held in registers for the
+          // tile's items: the copy loop below then issues back to back (its
+          // shared-memory table loads were on the ring's critical path)
+          const uint16_t* rp[kKeys / 4];
+#pragma unroll
+          for (int k = 0; k < kKeys / 4; ++k) rp[k] = table[(lane >> 3) + 4 * k];
           for (int it = 0; it < nit; ++it, ++item) {
             if (!ok || item % kProdWarps != pw) continue;
             const int slot = static_cast<int>(item % kRing);
@@ -568,10 +574,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
             // lane: 16-byte chunk cc of rows r0 + 4k (k < 32) of both slices of the pair
             const int cc = lane & 7, r0 = lane >> 3, j0 = 2 * it;
             const bool two = j0 + 1 < NSL;
-#pragma unroll 4
+#pragma unroll
             for (int k = 0; k < kKeys / 4; ++k) {
               const int r = r0 + 4 * k;
-              const uint16_t* row = table[r];
+              const uint16_t* row = rp[k];
               if (row) {
                 const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
                 const uint16_t* src = row + j0 * 64 + cc * 8;
