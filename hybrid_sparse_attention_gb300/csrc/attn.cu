@@ -179,6 +179,15 @@ HSA_DEVINL uint32_t sw128(int row, int chunk) {
   return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
+// 16-byte asynchronous copy issued only when `pred` (predicated, no branch).
+HSA_DEVINL void cp_async16_if(uint32_t dst, const void* src, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+      "@p cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(dst),
+      "l"(src), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+
 // Column reduction of a 32 x 32 register tile held one row per lane: on
 // return lane l holds the reduction of column l over the warp.
 template <bool kMax>
@@ -577,13 +586,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
 #pragma unroll
             for (int k = 0; k < kKeys / 4; ++k) {
               const int r = r0 + 4 * k;
-              const uint16_t* row = rp[k];
-              if (row) {
-                const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
-                const uint16_t* src = row + j0 * 64 + cc * 8;
-                tc::cp_async16_s(dst + off, src, 16u);
-                if (two) tc::cp_async16_s(dst + kSliceBytes + off, src + 64, 16u);
-              }
+              const uintptr_t row = reinterpret_cast<uintptr_t>(rp[k]);
+              const bool live = row != 0;
+              const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
+              const uintptr_t src = row + (j0 * 64 + cc * 8) * sizeof(uint16_t);
+              cp_async16_if(dst + off, reinterpret_cast<const void*>(src), live);
+              cp_async16_if(dst + kSliceBytes + off, reinterpret_cast<const void*>(src + 128), live && two);
             }
             tc::cp_async_commit();
             push(item);
