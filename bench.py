@@ -10,10 +10,18 @@ channels sharing one KV head, indexer 8 heads x 128, window 128, top-512,
 bf16 storage, fp32 accumulation, synthetic seeded inputs.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hsa|reference]
+                    [--config c4layer|topk|compress|longctx]
 
-Prints one JSON line (rank 0).  Under torchrun with N > 1 every rank runs an
-independent replica of the workload (its own seed): weak scaling, no data-path
-collective; the time is the maximum over ranks.
+Prints one JSON line (rank 0).  With --gpus N > 1 (and no torchrun
+environment) the script re-launches itself under torch.distributed.run with N
+ranks; every rank runs an independent replica of the workload (its own seed):
+weak scaling, no data-path collective.  The reported latency is the maximum
+over ranks; the aggregate throughput of all replicas is a separate key.
+
+--config picks the headline line: the C4 layer (default; its line also carries
+the other configurations' timings as extra keys), the standalone top-k
+(64 x 262,144), the standalone compressor (32 x 65,536 x 512 at r = 4 and 128)
+or the 1M-token pair (C4 and C128 layers, batch 4).
 """
 from __future__ import annotations
 
@@ -54,32 +62,43 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def layer_bytes(L, shape):
-    """Algorithmic HBM bytes of one C4 layer step (each byte the method must
-    move, counted once): indexer keys, score write + read, the gathered window
-    and top-k rows, q, o, the index list, plus the new-token append and the
-    4-row block reads/writes of the sequences whose block completes."""
+def layer_bytes(L, shape, kind=4):
+    """Algorithmic HBM bytes of one layer step (each byte the method must move,
+    counted once).  C4: indexer keys, score write + read, the gathered window
+    and top-k rows, q, o, the index list, the new-token append and the 4-row
+    block reads / writes of the sequences whose block completes.  C128: the
+    gathered window and every C128 row, q, o, the append and the 128-row
+    block compression of the sequences whose block completes."""
     L = L.to(torch.int64)
-    n4 = L // 4
     B = L.numel()
     D, Di = shape.Dqk, shape.Di
-    keys = int(n4.sum()) * Di * 2
-    iq_w = B * shape.Hi * (Di * 2 + 4)
-    scores = 2 * int(n4.sum()) * 4
-    rows = int((torch.clamp(L, max=shape.W) + torch.clamp(n4, max=shape.k)).sum())
-    gather = rows * D * 2
+    win = int(torch.clamp(L, max=shape.W).sum())
     q = B * shape.Hq * D * 2
     o = B * shape.Hq * shape.Dv * 2 + B * shape.Hq * 4
+    if kind == 128:
+        n = L // 128
+        gather = (win + int(n.sum())) * D * 2
+        append = B * (D * 2 * 2 + D * 2 * 3)              # read kv, z rows; write window + rings
+        ncomp = int((L % 128 == 0).sum())
+        compress = ncomp * (128 * 2 * D * 2 + D * 2)
+        total = gather + q + o + append + compress
+        return {"total": total, "gather": gather, "attention": gather + q + o,
+                "append_compress": append + compress}
+    n4 = L // 4
+    N = int(n4.sum())
+    keys = N * Di * 2
+    iq_w = B * shape.Hi * (Di * 2 + 4)
+    scores = 2 * N * 4
+    gather = (win + int(torch.clamp(n4, max=shape.k).sum())) * D * 2
     idx = 2 * B * shape.k * 4
     append = B * (D * 2 * 2 + D * 2 * 3 + Di * 2 * 2 + Di * 2 * 2)   # read new rows, write rings
     ncomp = int((L % 4 == 0).sum())
     compress = ncomp * (4 * 2 * (D + Di) * 2 + (D + Di) * 2)
-    indexer = keys + iq_w + int(n4.sum()) * 4
+    indexer = keys + iq_w + N * 4
     total = keys + iq_w + scores + gather + q + o + idx + append + compress
-    attention = gather + q + o + idx // 2
-    topk = int(n4.sum()) * 4 + idx // 2
     return {"total": total, "indexer": indexer, "keys": keys, "gather": gather,
-            "attention": attention, "topk": topk}
+            "attention": gather + q + o + idx // 2, "topk": N * 4 + idx // 2,
+            "append_compress": append + compress}
 
 
 class ClockSampler:
@@ -141,14 +160,35 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def dist_setup():
+def free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def relaunch(n, argv):
+    """Runs this script again under torch.distributed.run with n local ranks
+    (rendezvous on 127.0.0.1); returns its exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()),
+           os.path.abspath(sys.argv[0])] + list(argv)
+    return subprocess.call(cmd)
+
+
+def dist_setup(gpu=True):
+    """(world, rank, local rank, torch.distributed or None) from the torchrun
+    environment; NCCL between GPU ranks, gloo when the measurement is a CPU stub."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if gpu:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
         return world, rank, local, dist
     return 1, 0, local, None
 
@@ -169,185 +209,282 @@ def max_over_ranks(x, dist):
 
 # ----------------------------------------------------------------------------- oracle arm
 
+def _bits(t):
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16).copy()
+
+
 def sample_state(g, seqs):
-    """numpy copy (oracle input) of sequences `seqs` of a GPU layer state."""
+    """numpy copy (oracle input) of sequences `seqs` of a layer state."""
     offs = g.pool_offsets.cpu()
-    bits = lambda t: t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    c4 = g.kind == 4
     kv = torch.cat([g.kv_pool[int(offs[b]):int(offs[b + 1])] for b in seqs])
-    key = torch.cat([g.key_pool[int(offs[b]):int(offs[b + 1])] for b in seqs])
     caps = torch.tensor([int(offs[b + 1] - offs[b]) for b in seqs], dtype=torch.int64)
     new_offs = torch.zeros(len(seqs) + 1, dtype=torch.int64)
     new_offs[1:] = torch.cumsum(caps, 0)
     sel = torch.tensor(seqs, device=g.q.device)
-    s = {"kind": g.kind, "ratio": g.ratio, "Dv": g.shape.Dv, "k": g.shape.k,
+    s = {"kind": g.kind, "ratio": g.ratio, "Dv": g.shape.Dv, "k": g.shape.k if c4 else 0,
          "scale": g.shape.scale, "pool_offsets": new_offs.numpy(),
-         "seq_len_in": g.seq_len_in[sel].cpu().numpy(), "kv_pool": bits(kv), "key_pool": bits(key),
-         "b_kv": g.b_kv.cpu().numpy(), "b_ik": g.b_ik.cpu().numpy(),
-         "w": g.w[sel].cpu().numpy()}
-    for name in ("swa", "kv_ring", "z_ring", "ik_ring", "iz_ring", "kv_new", "z_new", "ik_new",
-                 "iz_new", "q", "iq"):
-        s[name] = bits(getattr(g, name)[sel])
+         "seq_len_in": g.seq_len_in[sel].cpu().numpy(), "kv_pool": _bits(kv),
+         "b_kv": g.b_kv.cpu().numpy()}
+    names = ["swa", "kv_ring", "z_ring", "kv_new", "z_new", "q"]
+    if c4:
+        key = torch.cat([g.key_pool[int(offs[b]):int(offs[b + 1])] for b in seqs])
+        s.update(key_pool=_bits(key), b_ik=g.b_ik.cpu().numpy(), w=g.w[sel].cpu().numpy())
+        names += ["ik_ring", "iz_ring", "ik_new", "iz_new", "iq"]
+    for name in names:
+        s[name] = _bits(getattr(g, name)[sel])
     return s
 
 
-def oracle_layer_time(g, budget_s, per_call=4):
-    """Times the oracle layer step over successive sequence groups until the
-    budget is spent; returns (us per full 64-sequence layer, sequences, threads)."""
+def oracle_threads():
     import oracle
     oracle.build()
-    threads = oracle.hardware_threads()
+    return oracle.hardware_threads()
+
+
+def oracle_layer_runner(g):
+    """One oracle decode step over the whole batch of layer state g.  The step
+    rewrites the same ring slots and pool rows with the same values each time
+    (its input lengths are not advanced), so repeated calls time the same
+    step.  Returns (run, description of the threads that do the work)."""
+    import oracle
+    threads = oracle_threads()
     B = g.seq_len_in.numel()
-    done, spent = 0, 0.0
-    while done < B and (spent < budget_s or done == 0):
-        seqs = list(range(done, min(B, done + per_call)))
-        s = sample_state(g, seqs)
-        t0 = time.perf_counter()
+    s = sample_state(g, list(range(B)))
+
+    def run():
         oracle.layer_decode(s, threads=threads)
+
+    busy = {"attention": min(threads, B * g.shape.Hq), "topk": min(threads, B),
+            "indexer": threads if g.kind == 4 else 0, "compress": 1}
+    return run, threads, busy
+
+
+def time_oracle(run, budget_s, min_calls=1):
+    """Calls run() until budget_s of wall time is spent (at least min_calls);
+    returns (mean seconds per call, calls)."""
+    spent, n = 0.0, 0
+    while n < min_calls or spent < budget_s:
+        t0 = time.perf_counter()
+        run()
         spent += time.perf_counter() - t0
-        done += len(seqs)
-    return spent / done * B * 1e6, done, threads
+        n += 1
+    return spent / n, n
 
 
 # ----------------------------------------------------------------------------- main
 
-def main():
+def parse_args(argv):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="hsa", choices=["hsa", "reference"])
+    ap.add_argument("--config", default="c4layer", choices=["c4layer", "topk", "compress", "longctx"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline (0: skip)")
     ap.add_argument("--layers", type=int, default=60,
                     help="layers in the CUDA-graph multi-layer step measurement (0: skip)")
-    ap.add_argument("--no-topk", action="store_true",
-                    help="skip the standalone top-k rows/s measurement")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="c4layer: skip the other configurations' timings")
     ap.add_argument("--profile", action="store_true",
                     help="profiling run: build the workload, run two layer steps, exit")
     ap.add_argument("--profile-ctx", type=int, nargs=2, default=None, metavar=("LO", "HI"),
                     help="with --profile: context lengths ~ U[LO, HI] instead of the bench's "
                          "(a smaller case of the same layer for multi-pass ncu captures)")
-    args = ap.parse_args()
-    world, rank, local, dist = dist_setup()
-    torch.cuda.set_device(local)
-    if args.impl == "reference":
-        run_reference(args, world, rank, dist)
-    elif args.profile:
-        run_profile(args.profile_ctx)
-    else:
-        run_hsa(args, world, rank, local, dist)
-    if dist is not None:
-        dist.destroy_process_group()
+    return ap.parse_args(argv)
 
 
-def build_workload(rank, ctx=None):
+def main(argv=None, measure=None):
+    """measure: the per-rank measurement (default: the GPU measurement of
+    --config); the replica logic around it is the same for any measurement."""
+    argv = sys.argv[1:] if argv is None else list(argv)
+    args = parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch(args.gpus, argv))
+    world, rank, local, dist = dist_setup(gpu=measure is None)
+    try:
+        if world != args.gpus:
+            raise SystemExit(f"bench.py: --gpus {args.gpus} but the launch has {world} ranks")
+        if measure is None:
+            torch.cuda.set_device(local)
+        if args.impl == "reference":
+            run_reference(args, world, rank, dist)
+        elif args.profile:
+            run_profile(args.profile_ctx)
+        else:
+            run_hsa(args, world, rank, local, dist, measure)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+def build_workload(rank, ctx=None, device="cuda"):
     seed = synth.SEED["c4layer"] + 1000 * rank
     L = synth.c4_lengths(seed, 64) if ctx is None else synth.c4_lengths(seed, 64, ctx[0], ctx[1])
-    g = synth.filled_state(seed, 4, synth.FULL, L, device="cuda")
+    g = synth.filled_state(seed, 4, synth.FULL, L, device=device)
     return L, g
 
 
+def longctx_workload(kind, rank=0, device="cuda"):
+    """The 1M-token pair: batch 4 at L = 1,048,576 tokens after this step (the
+    step completes both a 4- and a 128-token block), the bench's head shapes."""
+    seed = synth.SEED["longctx"] + 1000 * rank
+    L = torch.full((4,), 1 << 20, dtype=torch.int32)
+    g = synth.filled_state(seed, kind, synth.FULL, L, device=device, name=f"long{kind}")
+    return L, g
+
+
+def base_line(args, world, metric, unit, higher, workload, value):
+    return {"metric": metric, "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+            "higher_is_better": higher, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload, "parallelism": f"replicas x{world}"}}
+
+
 def run_reference(args, world, rank, dist):
-    """The oracle (plain CPU C++), as it stands, on the host cores: each step is
-    one bounded sample of the same workload scaled to a full layer."""
+    """The oracle (plain CPU C++), as it stands, on the host cores, timed on
+    the configuration's own workload: each step is one whole oracle step (the
+    full 64-sequence layer for the default configuration).  Under torchrun
+    only rank 0 runs it; the other ranks return without work."""
     if rank != 0:
-        return
-    import oracle
-    oracle.build()
-    L, g = build_workload(0)
-    threads = oracle.hardware_threads()
-    per_step = 2
-    for i in range(args.warmup):
-        oracle.layer_decode(sample_state(g, [i % 64]), threads=threads)
+        return None
+    cfg = args.config
+    if cfg == "c4layer":
+        L, g = build_workload(0)
+        run, threads, busy = oracle_layer_runner(g)
+        metric, unit, workload, per = METRIC, "us", WORKLOAD, 1.0
+        sample = "the whole 64-sequence layer step per timed step"
+        to_value = lambda sec: sec * 1e6
+        higher = False
+    elif cfg == "longctx":
+        L, g = longctx_workload(4)
+        run, threads, busy = oracle_layer_runner(g)
+        metric, unit, workload = LONG_METRIC, "us", LONG_WORKLOAD
+        sample = "the whole batch-4 C4 layer step per timed step"
+        to_value = lambda sec: sec * 1e6
+        higher = False
+    elif cfg == "topk":
+        run, threads, busy, sample = oracle_topk_runner()
+        metric, unit, workload = TOPK_METRIC, "rows/s", TOPK_WORKLOAD
+        to_value = lambda sec: 64 / sec
+        higher = True
+    else:
+        run, threads, busy, sample, scale = oracle_compress_runner(4)
+        metric, unit, workload = COMPRESS_METRIC, "us", COMPRESS_WORKLOAD
+        to_value = lambda sec: sec * scale * 1e6
+        higher = False
+    for _ in range(args.warmup):
+        run()
     times = []
-    for i in range(args.steps):
-        seqs = [(per_step * i + j) % 64 for j in range(per_step)]
-        s = sample_state(g, seqs)
+    for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.layer_decode(s, threads=threads)
-        times.append((time.perf_counter() - t0) / per_step * 64 * 1e6)
-    us = statistics.mean(times)
-    sample = f"{per_step} of the 64 sequences per step (rotating), scaled x{64 // per_step}"
-    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000,
-            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD},
-            "cpu_baseline": {"value": us, "unit": "us", "cores": threads, "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        run()
+        times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    v = to_value(sec)
+    line = base_line(args, 1, metric, unit, higher, workload, v)
+    line.update({"impl": "reference", "dtype": "f64", "ms_per_step": sec * 1000,
+                 "cpu_baseline": {"value": v, "unit": unit, "cores": threads, "kind": "oracle",
+                                  "sample": sample, "threads_busy_by_stage": busy},
+                 "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,
+                         "d2h_bytes_per_step": 0}})
     print(json.dumps(line), flush=True)
+    return line
 
 
-def run_hsa(args, world, rank, local, dist):
-    _lib.load(build_if_missing=True)
-    shape = synth.FULL
-    L, g = build_workload(rank)
-    B = L.numel()
-    stream = torch.cuda.current_stream()
+class L2Flush:
+    """Evicts L2 between steps, outside the timed events: writes a buffer larger
+    than L2, then reads another one, so that the lines left behind are clean and
+    the next step does not pay for writing back the flush's own dirty data."""
+
+    def __init__(self):
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device="cuda")
+        self.sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def __call__(self, i):
+        self.w.fill_(float(i))
+        torch.sum(self.r, dim=0, out=self.sink)
+
+
+L2_NOTE = (f"{L2_FLUSH_BYTES >> 20} MiB written, then {L2_FLUSH_BYTES >> 21} MiB read, before "
+           "every step, outside the timed events (L2 cold and clean)")
+
+
+def timed(fn, flush, warmup, steps, stream=None):
+    """CUDA-event milliseconds of `steps` calls of fn() after `warmup` calls,
+    L2 flushed before each, events on the launching stream."""
+    stream = stream or torch.cuda.current_stream()
+    for i in range(warmup):
+        flush(i)
+        fn()
+    ts = []
+    for i in range(steps):
+        flush(i)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return ts
+
+
+def run_hsa(args, world, rank, local, dist, measure=None):
+    measure = measure or {"c4layer": measure_c4layer, "topk": measure_topk_line,
+                          "compress": measure_compress_line,
+                          "longctx": measure_longctx_line}[args.config]
+    res = measure(args, rank, local, dist)
+    # latency: the slowest replica; every replica runs the full workload
+    ms_max = max_over_ranks(res["ms"], dist)
+    e2e_max = max_over_ranks(res["e2e_ms"], dist) if res.get("e2e_ms") is not None else None
+    if rank != 0:
+        return None
+    line = res["line"]
+    higher = line["higher_is_better"]
+    per_unit = res.get("units_per_step", 1)
+    if higher:      # a rate: value is per replica-step units / time, summed over replicas
+        line["value"] = world * per_unit / (ms_max * 1e-3)
+    else:
+        line["value"] = ms_max * 1000
+    line["n_gpus"] = world
+    line["ms_per_step"] = ms_max
+    line["config"]["parallelism"] = f"replicas x{world}"
+    line["throughput_all_replicas"] = {
+        "value": world * res.get("tokens_per_step", per_unit) / (ms_max * 1e-3),
+        "unit": res.get("throughput_unit", "units/s"),
+        "note": "aggregate of every replica: each runs the full workload"}
+    if e2e_max is not None:
+        e = line["e2e"]
+        e["value"] = world * per_unit / (e2e_max * 1e-3) if higher else e2e_max * 1000
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def layer_outputs(g):
+    B, shape = g.seq_len_in.numel(), g.shape
     out = torch.empty(B, shape.Hq, shape.Dv, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(B, shape.Hq, dtype=torch.float32, device="cuda")
     seq_out = torch.empty_like(g.seq_len_in)
-    idx = torch.empty(B, shape.k, dtype=torch.int32, device="cuda")
-    scores = torch.empty(g.kv_pool.shape[0], dtype=torch.float32, device="cuda")
-    stage = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-    for e in stage:
-        e.record(stream)          # the events exist from here on
-    # the timed steps run without stage events: an event recorded between two
-    # kernels stops the next one from being scheduled while the previous runs
-    desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores)
-    desc_stages = _lib.layer_desc(g, out, lse, seq_out, idx, scores,
-                                  stage_events=[e.cuda_event for e in stage])
-    ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
-    launches = _lib.hsa_layer_decode_launches(desc)
-    flush = L2Flush()
-    nbytes = layer_bytes(L, shape)
+    idx = scores = None
+    if g.kind == 4:
+        idx = torch.empty(B, shape.k, dtype=torch.int32, device="cuda")
+        scores = torch.empty(g.kv_pool.shape[0], dtype=torch.float32, device="cuda")
+    return out, lse, seq_out, idx, scores
 
-    def step(d=desc):
-        _lib.hsa_layer_decode(d, ws=ws)
 
-    for _ in range(args.warmup):
-        flush(0)
-        step()
-    torch.cuda.synchronize()
-    assert _lib.hsa_workspace_status(ws) == 0
-
-    # ------------------------------------------------ device-timed region
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(dist)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush(i)                            # evict the previous step's data from L2
-            ev0[i].record(stream)
-            step()
-            ev1[i].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
-    barrier(dist)
-    t_layer = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
-    # per-kernel durations: the same steps again with an event between kernels
-    stage_ms = []
-    for i in range(args.steps):
-        flush(i)
-        step(desc_stages)
-        stage[4].synchronize()                  # stage events are reused: read them now
-        stage_ms.append([stage[j].elapsed_time(stage[j + 1]) for j in range(4)])
-    ms = statistics.mean(t_layer)
-    ms_max = max_over_ranks(ms, dist)
-    st = np.array(stage_ms)
-    stage_mean = st.mean(axis=0)                # append, indexer, top-k, attention (ms)
-    assert _lib.hsa_workspace_status(ws) == 0
-
-    # ------------------------------------------------ end to end: host buffers
-    # The step's small inputs travel in one host-to-device copy (one pinned
-    # staging buffer, each input at a 256-byte-aligned offset) and its outputs
-    # in one device-to-host copy; the library reads and writes views of the
-    # device staging buffers.  q (4.7 MB, read only by the attention) is copied
-    # on a second stream inside the timed region and the layer waits for it
-    # right before the attention (the descriptor's q-ready event), so its
-    # upload overlaps the append, indexer and top-k.
+def e2e_layer(g, out, lse, seq_out, idx, scores, flush, warmup, steps):
+    """The layer step through host buffers: the step's small inputs travel in
+    one host-to-device copy (one pinned staging buffer, each input at a
+    256-byte-aligned offset) and its outputs in one device-to-host copy; the
+    library reads and writes views of the device staging buffers.  q, read
+    only by the attention, is copied on a second stream inside the timed
+    region and the layer waits for it right before the attention (the
+    descriptor's q-ready event), so its upload overlaps the earlier kernels.
+    Returns (mean ms, h2d bytes, d2h bytes)."""
     import copy as _copy
 
     def packed(tensors):
@@ -357,7 +494,8 @@ def run_hsa(args, world, rank, local, dist):
             at += (t.numel() * t.element_size() + 255) // 256 * 256
         return offs, at
 
-    names_in = ("kv_new", "z_new", "ik_new", "iz_new", "iq", "w")
+    stream = torch.cuda.current_stream()
+    names_in = ("kv_new", "z_new") + (("ik_new", "iz_new", "iq", "w") if g.kind == 4 else ())
     t_in = [getattr(g, k) for k in names_in]
     offs_in, n_in = packed(t_in)
     dev_in = torch.empty(n_in, dtype=torch.uint8, device="cuda")
@@ -377,11 +515,11 @@ def run_hsa(args, world, rank, local, dist):
     side = torch.cuda.Stream()
     q_ready = torch.cuda.Event()
     q_ready.record(side)                        # the event exists before its handle is taken
-    desc_e2e = _lib.layer_desc(g2, out2, lse2, seq_out, idx, scores,
-                               q_ready_event=q_ready.cuda_event)
+    desc = _lib.layer_desc(g2, out2, lse2, seq_out, idx, scores, q_ready_event=q_ready.cuda_event)
+    ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
     h2d, d2h = n_in + q_host.numel() * q_host.element_size(), n_out
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
+    ts = []
+    for i in range(warmup + steps):
         flush(i)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
@@ -391,57 +529,107 @@ def run_hsa(args, world, rank, local, dist):
             g2.q.copy_(q_host, non_blocking=True)
             q_ready.record(side)
         dev_in.copy_(host_in, non_blocking=True)
-        step(desc_e2e)
+        _lib.hsa_layer_decode(desc, ws=ws)
         host_out.copy_(dev_out, non_blocking=True)
         b.record(stream)
         b.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append(a.elapsed_time(b))
-    e2e = max_over_ranks(statistics.mean(e2e_ms), dist)
-    assert torch.equal(host_out[:out.numel() * 2].view(out.dtype).view(out.shape), out.cpu())
+        if i >= warmup:
+            ts.append(a.elapsed_time(b))
+    assert _lib.hsa_workspace_status(ws) == 0
+    return statistics.mean(ts), h2d, d2h, host_out[:out.numel() * 2].view(out.dtype).view(out.shape)
 
-    # ------------------------------------------------ a 60-layer step in one CUDA graph
-    multi = multi_layer_graph(args, flush) if rank == 0 and args.layers > 0 else None
 
-    # ------------------------------------------------ standalone top-k (rows / s)
-    topk = topk_rows_per_s(flush) if rank == 0 and not args.no_topk else None
+def measure_c4layer(args, rank, local, dist):
+    """The headline: one C4 layer step of the bench workload (see the module
+    docstring), device-timed and end to end; on rank 0 also the other
+    configurations, the 60-layer CUDA graph and the oracle baseline."""
+    _lib.load(build_if_missing=True)
+    shape = synth.FULL
+    L, g = build_workload(rank)
+    stream = torch.cuda.current_stream()
+    out, lse, seq_out, idx, scores = layer_outputs(g)
+    stage = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in stage:
+        e.record(stream)          # the events exist from here on
+    # the timed steps run without stage events: an event recorded between two
+    # kernels stops the next one from being scheduled while the previous runs
+    desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores)
+    desc_stages = _lib.layer_desc(g, out, lse, seq_out, idx, scores,
+                                  stage_events=[e.cuda_event for e in stage])
+    ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
+    launches = _lib.hsa_layer_decode_launches(desc)
+    flush = L2Flush()
+    nbytes = layer_bytes(L, shape)
 
-    # ------------------------------------------------ CPU baseline: the oracle
+    def step(d=desc):
+        _lib.hsa_layer_decode(d, ws=ws)
+
+    for i in range(args.warmup):
+        flush(i)
+        step()
+    torch.cuda.synchronize()
+    assert _lib.hsa_workspace_status(ws) == 0
+
+    # ------------------------------------------------ device-timed region
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush(i)                            # evict the previous step's data from L2
+            ev0[i].record(stream)
+            step()
+            ev1[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(dist)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev0, ev1))
+    # per-kernel durations: the same steps again with an event between kernels
+    stage_ms = []
+    for i in range(args.steps):
+        flush(i)
+        step(desc_stages)
+        stage[4].synchronize()                  # stage events are reused: read them now
+        stage_ms.append([stage[j].elapsed_time(stage[j + 1]) for j in range(4)])
+    stage_mean = np.array(stage_ms).mean(axis=0)  # append, indexer, top-k, attention (ms)
+    assert _lib.hsa_workspace_status(ws) == 0
+
+    e2e_ms, h2d, d2h, host_o = e2e_layer(g, out, lse, seq_out, idx, scores, flush, args.warmup,
+                                         args.steps)
+    step()
+    torch.cuda.synchronize()
+    assert torch.equal(host_o, out.cpu())
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        if args.layers > 0:
+            extra["multi_layer_graph"] = multi_layer_graph(args, flush)
+        extra["topk_rows_per_s"] = bench_topk(flush, args)
+        extra["compress"] = bench_compress(flush, args)
+        extra["longctx"] = bench_longctx(flush, args)
     cpu = None
-    if rank == 0 and world == 1 and args.cpu_budget > 0:
-        us_cpu, nseq, threads = oracle_layer_time(g, args.cpu_budget)
-        cpu = {"value": us_cpu, "unit": "us", "cores": threads, "kind": "oracle",
-               "sample": f"oracle layer step on {nseq} of the 64 sequences "
-                         f"(groups of 4, ~{args.cpu_budget:.0f} s budget), scaled to 64"}
+    if rank == 0 and args.cpu_budget > 0:
+        run, threads, busy = oracle_layer_runner(g)
+        sec, calls = time_oracle(run, args.cpu_budget)
+        cpu = {"value": sec * 1e6, "unit": "us", "cores": threads, "kind": "oracle",
+               "sample": f"the whole 64-sequence layer step, {calls} calls "
+                         f"(~{args.cpu_budget:.0f} s budget), mean",
+               "threads_busy_by_stage": busy}
 
-    if rank != 0:
-        return
     peak, peak_kind = measured_peaks()
     idx_ms = float(stage_mean[1])
     achieved = nbytes["indexer"] / (idx_ms * 1e-3) / 1e9
     layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
-    traffic = indexer_traffic()
-    line = {
-        "metric": METRIC,
-        "value": ms_max * 1000 / world,
-        "unit": "us",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": ms_max,
-        "higher_is_better": False,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
-                   "l2": f"{L2_FLUSH_BYTES >> 20} MiB written, then {L2_FLUSH_BYTES >> 21} MiB read, "
-                         "before every step, outside the timed events (L2 cold and clean)",
-                   "sum_c4_entries": int((L // 4).sum()), "seed": synth.SEED["c4layer"]},
+    line = base_line(args, 1, METRIC, "us", False, WORKLOAD, ms * 1000)
+    line["config"].update({"l2": L2_NOTE, "sum_c4_entries": int((L // 4).sum()),
+                           "seed": synth.SEED["c4layer"]})
+    line.update({
         "roofline": {"bound": "hbm", "kernel": "indexer_kernel (tcgen05 scores)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
-                     "traffic": traffic, "algorithmic_bytes": nbytes["indexer"],
+                     "traffic": indexer_traffic(), "algorithmic_bytes": nbytes["indexer"],
                      "launch_us": idx_ms * 1000},
         "layer_roofline": {"algorithmic_bytes": nbytes["total"], "achieved_gbs": layer_gbs,
                            "frac": layer_gbs / peak},
@@ -454,28 +642,24 @@ def run_hsa(args, world, rank, local, dist):
         "stage_us": {"append_compress": stage_mean[0] * 1000, "indexer": stage_mean[1] * 1000,
                      "topk": stage_mean[2] * 1000, "attention": stage_mean[3] * 1000},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e * 1000 / world, "unit": "us", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": e2e_ms * 1000, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed": wall,
-        "topk_rows_per_s": topk,
-        "multi_layer_graph": multi,
-    }
-    print(json.dumps(line), flush=True)
+    })
+    line.update(extra)
+    B = L.numel()
+    return {"ms": ms, "e2e_ms": e2e_ms, "line": line, "units_per_step": 1,
+            "tokens_per_step": B, "throughput_unit": "decode tokens/s through one layer"}
 
 
 def run_profile(ctx=None):
     """Two layer steps of the bench workload (the first warms up), for ncu."""
     _lib.load(build_if_missing=True)
-    shape = synth.FULL
     L, g = build_workload(0, ctx)
-    B = L.numel()
-    out = torch.empty(B, shape.Hq, shape.Dv, dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty(B, shape.Hq, dtype=torch.float32, device="cuda")
-    desc = _lib.layer_desc(g, out, lse, torch.empty_like(g.seq_len_in),
-                           torch.empty(B, shape.k, dtype=torch.int32, device="cuda"),
-                           torch.empty(g.kv_pool.shape[0], dtype=torch.float32, device="cuda"))
+    out, lse, seq_out, idx, scores = layer_outputs(g)
+    desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores)
     ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
     for _ in range(2):
         _lib.hsa_layer_decode(desc, ws=ws)
@@ -489,20 +673,16 @@ def multi_layer_graph(args, flush, nstates=4, iters=10):
     works on state i mod nstates, each larger than L2) captured once in a CUDA
     graph: us per layer of the replayed step, next to the same layers launched
     one call at a time."""
-    shape = synth.FULL
     states = []
     for j in range(nstates):
-        L, g = build_workload(0) if j == 0 else (None, None)
-        if j:
+        if j == 0:
+            L, g = build_workload(0)
+        else:
             seed = synth.SEED["c4layer"] + 7919 * j
             L = synth.c4_lengths(seed, 64)
-            g = synth.filled_state(seed, 4, shape, L, device="cuda", name=f"layer{j}")
-        B = L.numel()
-        out = torch.empty(B, shape.Hq, shape.Dv, dtype=torch.bfloat16, device="cuda")
-        lse = torch.empty(B, shape.Hq, dtype=torch.float32, device="cuda")
-        idx = torch.empty(B, shape.k, dtype=torch.int32, device="cuda")
-        scores = torch.empty(g.kv_pool.shape[0], dtype=torch.float32, device="cuda")
-        desc = _lib.layer_desc(g, out, lse, torch.empty_like(g.seq_len_in), idx, scores)
+            g = synth.filled_state(seed, 4, synth.FULL, L, device="cuda", name=f"layer{j}")
+        out, lse, seq_out, idx, scores = layer_outputs(g)
+        desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores)
         ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
         states.append((g, desc, ws, out, lse, idx, scores))
     descs = [states[i % nstates] for i in range(args.layers)]
@@ -536,52 +716,300 @@ def multi_layer_graph(args, flush, nstates=4, iters=10):
     for _, _, ws, *_ in states:
         assert _lib.hsa_workspace_status(ws) == 0
     per = {m: statistics.mean(v) * 1000 / args.layers for m, v in times.items()}
+    del graph, states, descs
+    torch.cuda.empty_cache()
     return {"layers": args.layers, "states": nstates, "us_per_layer_graph": per["graph"],
             "us_per_layer_eager": per["eager"],
             "note": "C4 layers of the bench workload, layer i on state i mod 4; L2 flushed "
                     "before each step, not between layers"}
 
 
-class L2Flush:
-    """Evicts L2 between steps, outside the timed events: writes a buffer larger
-    than L2, then reads another one, so that the lines left behind are clean and
-    the next step does not pay for writing back the flush's own dirty data."""
+# ----------------------------------------------------------------------------- other configurations
 
-    def __init__(self):
-        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device="cuda")
-        self.sink = torch.empty((), dtype=torch.float32, device="cuda")
-
-    def __call__(self, i):
-        self.w.fill_(float(i))
-        torch.sum(self.r, dim=0, out=self.sink)
+TOPK_METRIC = "top-512 rows/s (Lightning TopK, 64 rows x 262,144 fp32)"
+TOPK_WORKLOAD = "64 x 262,144 fp32 N(0,1), 5% of entries copies of others (ties), k=512"
+COMPRESS_METRIC = "us per Flash Compressor call (32 x 65,536 tokens x 512 channels, r=4)"
+COMPRESS_WORKLOAD = ("Flash Compressor: 32 sequences x 65,536 tokens x 512 channels, kv and z bf16 "
+                     "N(0,1), b fp32 N(0,0.5^2), bf16 output; r=4 (headline) and r=128")
+LONG_METRIC = "us per decode layer (C4+SWA, 1M ctx, batch 4)"
+LONG_WORKLOAD = ("1M-token pair: B=4, L=1,048,576 (the step completes a 4- and a 128-token "
+                 "block), Hq=64, Dqk=576, Dv=512, window 128; (a) C4: indexer 8x128, top-512 "
+                 "over 262,144 entries; (b) C128: dense over 8,192 entries")
 
 
-def topk_rows_per_s(flush, iters=20):
+def topk_inputs(device="cuda"):
+    x = synth.topk_scores(synth.SEED["topk"], 64, 262144, 0.05, device=device).reshape(-1)
+    offs = torch.arange(65, dtype=torch.int64, device=device) * 262144
+    return x, offs
+
+
+def oracle_topk_runner():
+    import oracle
+    threads = oracle_threads()
+    x, offs = topk_inputs("cuda" if torch.cuda.is_available() else "cpu")
+    xs, os_ = x.cpu().numpy(), offs.cpu().numpy()
+
+    def run():
+        oracle.topk(xs, os_, 512, threads=threads)
+
+    return run, threads, {"topk": min(threads, 64)}, "all 64 rows per timed step"
+
+
+def bench_topk(flush, args, iters=20):
     """Standalone Lightning TopK on 64 rows x 262,144 fp32 (5% copied entries),
     k=512: rows per second, L2 flushed before each launch."""
-    x = synth.topk_scores(synth.SEED["topk"], 64, 262144, 0.05, device="cuda").reshape(-1)
-    offs = torch.arange(65, dtype=torch.int64, device="cuda") * 262144
+    x, offs = topk_inputs()
     idx = torch.empty(64, 512, dtype=torch.int32, device="cuda")
     ws = _lib.workspace(_lib.hsa_topk_workspace_size(64, x.numel(), 512))
-    for _ in range(3):
-        _lib.hsa_topk(x, offs, 512, idx=idx, ws=ws, with_vals=False)
-    ts = []
-    for i in range(iters):
-        flush(i)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        _lib.hsa_topk(x, offs, 512, idx=idx, ws=ws, with_vals=False)
-        b.record()
-        b.synchronize()
-        ts.append(a.elapsed_time(b))
+    ts = timed(lambda: _lib.hsa_topk(x, offs, 512, idx=idx, ws=ws, with_vals=False), flush, 3, iters)
+    assert _lib.hsa_workspace_status(ws) == 0
     ms = statistics.mean(ts)
     peak, _ = measured_peaks()
     gbs = x.numel() * 4 / (ms * 1e-3) / 1e9
-    return {"value": 64 / (ms * 1e-3), "unit": "rows/s", "us_per_call": ms * 1000,
-            "config": "64 x 262,144 fp32, 5% copied entries, k=512",
-            "achieved_gbs": gbs, "frac_of_hbm": gbs / peak}
+    res = {"value": 64 / (ms * 1e-3), "unit": "rows/s", "us_per_call": ms * 1000,
+           "config": "64 x 262,144 fp32, 5% copied entries, k=512",
+           "algorithmic_bytes": x.numel() * 4 + 64 * 512 * 4,
+           "achieved_gbs": gbs, "frac_of_hbm": gbs / peak}
+    if args.cpu_budget > 0:
+        run, threads, busy, sample = oracle_topk_runner()
+        sec, calls = time_oracle(run, 0.0)
+        res["cpu_baseline"] = {"value": 64 / sec, "unit": "rows/s", "cores": threads,
+                               "kind": "oracle", "sample": sample, "threads_busy_by_stage": busy}
+    return res
+
+
+def measure_topk_line(args, rank, local, dist):
+    _lib.load(build_if_missing=True)
+    flush = L2Flush()
+    x, offs = topk_inputs()
+    idx = torch.empty(64, 512, dtype=torch.int32, device="cuda")
+    ws = _lib.workspace(_lib.hsa_topk_workspace_size(64, x.numel(), 512))
+    fn = lambda: _lib.hsa_topk(x, offs, 512, idx=idx, ws=ws, with_vals=False)
+    barrier(dist)
+    with ClockSampler(local) as clocks:
+        ts = timed(fn, flush, args.warmup, args.steps)
+    barrier(dist)
+    ms = statistics.mean(ts)
+    # end to end: scores from pinned host memory, indices back
+    xh = x.cpu().pin_memory()
+    ih = torch.empty(64, 512, dtype=torch.int32).pin_memory()
+    xd = torch.empty_like(x)
+
+    def e2e():
+        xd.copy_(xh, non_blocking=True)
+        _lib.hsa_topk(xd, offs, 512, idx=idx, ws=ws, with_vals=False)
+        ih.copy_(idx, non_blocking=True)
+
+    e2e_ms = statistics.mean(timed(e2e, flush, args.warmup, args.steps))
+    assert torch.equal(ih, idx.cpu())
+    peak, peak_kind = measured_peaks()
+    nb = x.numel() * 4 + 64 * 512 * 4
+    gbs = nb / (ms * 1e-3) / 1e9
+    line = base_line(args, 1, TOPK_METRIC, "rows/s", True, TOPK_WORKLOAD, 64 / (ms * 1e-3))
+    line["dtype"] = "u32"
+    line["config"]["l2"] = L2_NOTE
+    cpu = None
+    if rank == 0 and args.cpu_budget > 0:
+        run, threads, busy, sample = oracle_topk_runner()
+        sec, calls = time_oracle(run, min(args.cpu_budget, 5.0))
+        cpu = {"value": 64 / sec, "unit": "rows/s", "cores": threads, "kind": "oracle",
+               "sample": sample, "threads_busy_by_stage": busy}
+    launches = 1 if x.numel() <= 32768 else 2
+    line.update({"roofline": {"bound": "hbm", "kernel": "topk_hist_kernel + topk_select_kernel",
+                              "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                              "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "traffic": None,
+                              "algorithmic_bytes": nb, "launch_us": ms * 1000},
+                 "cpu_baseline": cpu,
+                 "e2e": {"value": None, "unit": "rows/s", "h2d_bytes_per_step": x.numel() * 4,
+                         "d2h_bytes_per_step": 64 * 512 * 4},
+                 "gpu_launches": launches * args.steps, "clocks": clocks.summary()})
+    return {"ms": ms, "e2e_ms": e2e_ms, "line": line, "units_per_step": 64,
+            "throughput_unit": "rows/s"}
+
+
+def compress_inputs(r, device="cuda"):
+    seed = synth.SEED["compress"]
+    S, T, C = 32, 65536, 512
+    kv = synth.normal_bf16(seed, "compress.kv", (S, T, C), device=device)
+    z = synth.normal_bf16(seed, "compress.z", (S, T, C), device=device)
+    b = synth.normal(seed, f"compress.b{r}", (r, C), std=0.5, device=device)
+    return kv, z, b
+
+
+def compress_bytes(S, T, C, r):
+    return 2 * S * T * C * 2 + S * (T // r) * C * 2 + r * C * 4
+
+
+def oracle_compress_runner(r, kv=None, z=None, b=None, seqs=2):
+    """The oracle compressor on `seqs` of the 32 sequences; returns (run,
+    threads, busy, sample, scale to the full 32)."""
+    import oracle
+    threads = oracle_threads()
+    if kv is None:
+        kv, z, b = compress_inputs(r, "cuda" if torch.cuda.is_available() else "cpu")
+    kvs, zs, bs = _bits(kv[:seqs]), _bits(z[:seqs]), b.cpu().numpy()
+
+    def run():
+        oracle.compress(kvs, zs, bs, r, threads=threads)
+
+    nblk = seqs * (kv.shape[1] // r)
+    return (run, threads, {"compress": min(threads, nblk)},
+            f"{seqs} of the 32 sequences per timed step, scaled x{32 // seqs}", 32 / seqs)
+
+
+def bench_compress(flush, args, iters=5):
+    """Flash Compressor standalone, 32 x 65,536 x 512, r = 4 and r = 128, bf16 output."""
+    peak, _ = measured_peaks()
+    res = {}
+    kv = z = None
+    for r in (4, 128):
+        if kv is None:
+            kv, z, b = compress_inputs(r)
+        else:
+            b = synth.normal(synth.SEED["compress"], f"compress.b{r}", (r, 512), std=0.5,
+                             device="cuda")
+        out = torch.empty(32, 65536 // r, 512, dtype=torch.bfloat16, device="cuda")
+        ms = statistics.mean(timed(lambda: _lib.hsa_compress(kv, z, b, r, out=out), flush, 2, iters))
+        nb = compress_bytes(32, 65536, 512, r)
+        gbs = nb / (ms * 1e-3) / 1e9
+        ent = {"us": ms * 1000, "algorithmic_bytes": nb, "achieved_gbs": gbs, "frac": gbs / peak,
+               "roofline_us_at_peak": nb / (peak * 1e9) * 1e6}
+        if args.cpu_budget > 0:
+            run, threads, busy, sample, scale = oracle_compress_runner(r, kv, z, b)
+            sec, calls = time_oracle(run, 0.0)
+            ent["cpu_baseline"] = {"value": sec * scale * 1e6, "unit": "us", "cores": threads,
+                                   "kind": "oracle", "sample": sample,
+                                   "threads_busy_by_stage": busy}
+        res[f"r{r}"] = ent
+        del out
+    del kv, z
+    torch.cuda.empty_cache()
+    res["config"] = COMPRESS_WORKLOAD
+    return res
+
+
+def measure_compress_line(args, rank, local, dist):
+    _lib.load(build_if_missing=True)
+    flush = L2Flush()
+    kv, z, b = compress_inputs(4)
+    out = torch.empty(32, 16384, 512, dtype=torch.bfloat16, device="cuda")
+    fn = lambda: _lib.hsa_compress(kv, z, b, 4, out=out)
+    barrier(dist)
+    with ClockSampler(local) as clocks:
+        ts = timed(fn, flush, args.warmup, args.steps)
+    barrier(dist)
+    ms = statistics.mean(ts)
+    # end to end: kv and z from pinned host memory, the compressed rows back
+    kvh, zh = kv.cpu().pin_memory(), z.cpu().pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e():
+        kv.copy_(kvh, non_blocking=True)
+        z.copy_(zh, non_blocking=True)
+        _lib.hsa_compress(kv, z, b, 4, out=out)
+        oh.copy_(out, non_blocking=True)
+
+    e2e_ms = statistics.mean(timed(e2e, flush, 1, max(2, args.steps // 5)))
+    peak, peak_kind = measured_peaks()
+    nb = compress_bytes(32, 65536, 512, 4)
+    gbs = nb / (ms * 1e-3) / 1e9
+    line = base_line(args, 1, COMPRESS_METRIC, "us", False, COMPRESS_WORKLOAD, ms * 1000)
+    line["config"]["l2"] = L2_NOTE
+    cpu = None
+    if rank == 0 and args.cpu_budget > 0:
+        run, threads, busy, sample, scale = oracle_compress_runner(4, kv, z, b)
+        sec, calls = time_oracle(run, min(args.cpu_budget, 5.0))
+        cpu = {"value": sec * scale * 1e6, "unit": "us", "cores": threads, "kind": "oracle",
+               "sample": sample, "threads_busy_by_stage": busy}
+    line.update({"roofline": {"bound": "hbm", "kernel": "compress_kernel", "achieved": gbs,
+                              "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                              "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "traffic": None,
+                              "algorithmic_bytes": nb, "launch_us": ms * 1000},
+                 "cpu_baseline": cpu,
+                 "e2e": {"value": None, "unit": "us", "h2d_bytes_per_step": 2 * kv.numel() * 2,
+                         "d2h_bytes_per_step": out.numel() * 2},
+                 "gpu_launches": args.steps, "clocks": clocks.summary()})
+    if rank == 0:
+        line["r128"] = bench_compress(flush, args)["r128"]
+    return {"ms": ms, "e2e_ms": e2e_ms, "line": line, "units_per_step": 1,
+            "tokens_per_step": 32 * 65536, "throughput_unit": "tokens compressed/s"}
+
+
+def bench_layer_state(L, g, flush, warmup, steps, cpu_budget, clocks=None, dist=None):
+    """Device time, algorithmic bytes, end-to-end time and oracle baseline of
+    one layer step of state g (clocks, if given, is sampled around the
+    device-timed steps only, which barriers bracket)."""
+    out, lse, seq_out, idx, scores = layer_outputs(g)
+    desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores)
+    ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
+    fn = lambda: _lib.hsa_layer_decode(desc, ws=ws)
+    for i in range(warmup):
+        flush(i)
+        fn()
+    torch.cuda.synchronize()
+    barrier(dist)
+    if clocks is not None:
+        with clocks:
+            ts = timed(fn, flush, 0, steps)
+    else:
+        ts = timed(fn, flush, 0, steps)
+    barrier(dist)
+    ms = statistics.mean(ts)
+    assert _lib.hsa_workspace_status(ws) == 0
+    peak, _ = measured_peaks()
+    nb = layer_bytes(L, g.shape, g.kind)
+    gbs = nb["total"] / (ms * 1e-3) / 1e9
+    ent = {"us": ms * 1000, "algorithmic_bytes": nb["total"], "achieved_gbs": gbs,
+           "frac": gbs / peak, "launches": _lib.hsa_layer_decode_launches(desc),
+           "e2e": None}
+    e2e_ms, h2d, d2h, _ = e2e_layer(g, out, lse, seq_out, idx, scores, flush, warmup, steps)
+    ent["e2e"] = {"value": e2e_ms * 1000, "unit": "us", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": d2h}
+    if cpu_budget > 0:
+        run, threads, busy = oracle_layer_runner(g)
+        sec, calls = time_oracle(run, 0.0)
+        ent["cpu_baseline"] = {"value": sec * 1e6, "unit": "us", "cores": threads,
+                               "kind": "oracle", "sample": "the whole batch-4 layer step",
+                               "threads_busy_by_stage": busy}
+    return ent, ms, e2e_ms
+
+
+def bench_longctx(flush, args, steps=10):
+    res = {"config": LONG_WORKLOAD}
+    for kind in (4, 128):
+        L, g = longctx_workload(kind)
+        ent, _, _ = bench_layer_state(L, g, flush, 3, steps, args.cpu_budget)
+        res["c4" if kind == 4 else "c128"] = ent
+        del g
+        torch.cuda.empty_cache()
+    return res
+
+
+def measure_longctx_line(args, rank, local, dist):
+    _lib.load(build_if_missing=True)
+    flush = L2Flush()
+    L, g = longctx_workload(4, rank)
+    clocks = ClockSampler(local)
+    ent, ms, e2e_ms = bench_layer_state(L, g, flush, args.warmup, args.steps,
+                                        args.cpu_budget if rank == 0 else 0, clocks, dist)
+    del g
+    torch.cuda.empty_cache()
+    peak, peak_kind = measured_peaks()
+    line = base_line(args, 1, LONG_METRIC, "us", False, LONG_WORKLOAD, ms * 1000)
+    line["config"]["l2"] = L2_NOTE
+    line.update({"layer_roofline": {"algorithmic_bytes": ent["algorithmic_bytes"],
+                                    "achieved_gbs": ent["achieved_gbs"], "frac": ent["frac"]},
+                 "roofline": {"bound": "hbm", "kernel": "whole C4 layer step", "achieved":
+                              ent["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                              "frac": ent["frac"], "peak_kind": f"{peak_kind} hbm_gbs",
+                              "traffic": None, "algorithmic_bytes": ent["algorithmic_bytes"]},
+                 "cpu_baseline": ent.get("cpu_baseline"), "e2e": ent["e2e"],
+                 "gpu_launches": ent["launches"] * args.steps, "clocks": clocks.summary()})
+    if rank == 0:
+        L2_, g2 = longctx_workload(128)
+        line["c128"], _, _ = bench_layer_state(L2_, g2, flush, 3, args.steps, args.cpu_budget)
+    return {"ms": ms, "e2e_ms": e2e_ms, "line": line, "units_per_step": 1,
+            "tokens_per_step": 4, "throughput_unit": "decode tokens/s through one layer"}
 
 
 def indexer_traffic():

@@ -22,18 +22,61 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch[64] = {};
+
+// The address is cached per device together with the unique id of the CUDA
+// context it was taken in: after a cudaDeviceReset (or any other end of the
+// primary context) the next call finds a different context id and looks the
+// address up again instead of reusing a stale one.
+struct Cached {
+  unsigned long long ctx_id;
+  void* addr;
+};
+Cached g_scratch[64] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the current thread's CUDA context (driver entry points looked
+// up through the runtime, so the library needs no link against libcuda).
+hsa_status_t current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  if (!get_current || !get_id) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      return set_error_detail(HSA_ERR_CUDA, "driver entry points cuCtxGetCurrent / cuCtxGetId");
+    get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, id) != CUDA_SUCCESS)
+    return set_error_detail(HSA_ERR_CUDA, "no current CUDA context");
+  return HSA_OK;
+}
 
 // Device address of the scratch array on the current device, looked up once
-// per device (host code cannot use the symbol itself: it is a host-side
-// stand-in, not a device address).
+// per device and context (host code cannot use the symbol itself: it is a
+// host-side stand-in, not a device address).
 hsa_status_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_error_detail(HSA_ERR_CUDA, cudaGetErrorString(e));
   if (dev < 0 || dev >= 64) return set_error_detail(HSA_ERR_UNSUPPORTED, "device index >= 64");
+  // makes the device's primary context current (and creates it on first use)
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return set_error_detail(HSA_ERR_CUDA, cudaGetErrorString(e));
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch[dev]) {
+  unsigned long long ctx = 0;
+  hsa_status_t st = current_context_id(&ctx);
+  if (st != HSA_OK) return st;
+  if (!g_scratch[dev].addr || g_scratch[dev].ctx_id != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_topk_scratch);
     if (e != cudaSuccess || !p) {
@@ -41,9 +84,9 @@ hsa_status_t scratch_address(void** out) {
       snprintf(msg, sizeof msg, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
       return set_error_detail(HSA_ERR_CUDA, msg);
     }
-    g_scratch[dev] = p;
+    g_scratch[dev] = Cached{ctx, p};
   }
-  *out = g_scratch[dev];
+  *out = g_scratch[dev].addr;
   return HSA_OK;
 }
 

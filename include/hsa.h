@@ -166,7 +166,9 @@ hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, in
  * cudaMalloc, no cudaFree, no allocating library routine.
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Every call shares the one array and clears the part that
+ * stream capture.  The address is cached per device with the id of the CUDA
+ * context it was taken in, and looked up again (the same way) when that
+ * context has changed, e.g. after cudaDeviceReset.  Every call shares the one array and clears the part that
  * must start at zero (a cudaMemsetAsync on `stream`) before its two kernel
  * launches; calls that overlap on the same GPU (e.g. issued on different
  * streams) race on it (each device has its own array).  Device-side status

@@ -146,17 +146,21 @@ int oracle_indexer_scores(const uint16_t* iq, const float* w, const uint16_t* ke
   if (B < 0 || Hi <= 0 || Di <= 0) return 1;
   for (int64_t b = 0; b < B; ++b)
     if (offsets[b + 1] < offsets[b]) return 1;
-  parallel_for(B, threads, [&](int64_t b) {
-    for (int64_t j = offsets[b]; j < offsets[b + 1]; ++j) {
-      double s = 0.0;
-      for (int64_t h = 0; h < Hi; ++h) {
-        double dot = 0.0;
-        for (int64_t d = 0; d < Di; ++d)
-          dot += bf16_to_double(iq[(b * Hi + h) * Di + d]) * bf16_to_double(keys[j * Di + d]);
-        s += static_cast<double>(w[b * Hi + h]) * std::max(0.0, dot);
-      }
-      scores[j] = s;
+  // every entry is independent: the entries of all sequences are shared out
+  // among the threads in contiguous ranges; entry j belongs to the sequence b
+  // whose range [offsets[b], offsets[b+1]) holds it
+  const int64_t first = offsets[0], total = offsets[B] - offsets[0];
+  parallel_for(total, threads, [&](int64_t e) {
+    const int64_t j = first + e;
+    const int64_t b = (std::upper_bound(offsets, offsets + B + 1, j) - offsets) - 1;
+    double s = 0.0;
+    for (int64_t h = 0; h < Hi; ++h) {
+      double dot = 0.0;
+      for (int64_t d = 0; d < Di; ++d)
+        dot += bf16_to_double(iq[(b * Hi + h) * Di + d]) * bf16_to_double(keys[j * Di + d]);
+      s += static_cast<double>(w[b * Hi + h]) * std::max(0.0, dot);
     }
+    scores[j] = s;
   });
   return 0;
 }
@@ -237,50 +241,53 @@ int oracle_decode_attn(const uint16_t* q, const uint16_t* swa, const int32_t* se
         if (extra_idx[b * k + i] >= n) return 3;
     }
   }
-  parallel_for(B, threads, [&](int64_t b) {
-    // gather the attended rows (pointers into the pools)
-    std::vector<const uint16_t*> rows;
+  // the attended rows of each sequence (pointers into the pools)
+  std::vector<std::vector<const uint16_t*>> rows(B);
+  for (int64_t b = 0; b < B; ++b) {
     const int64_t L = seq_len[b];
     for (int64_t p = std::max<int64_t>(0, L - W); p < L; ++p)
-      rows.push_back(swa + (b * W + p % W) * Dqk);
+      rows[b].push_back(swa + (b * W + p % W) * Dqk);
     if (extra_offsets) {
       const int64_t off = extra_offsets[b], n = extra_offsets[b + 1] - off;
       if (extra_idx) {
         for (int64_t i = 0; i < k; ++i) {
           const int32_t j = extra_idx[b * k + i];
-          if (j >= 0) rows.push_back(extra + (off + j) * Dqk);
+          if (j >= 0) rows[b].push_back(extra + (off + j) * Dqk);
         }
       } else {
-        for (int64_t j = 0; j < n; ++j) rows.push_back(extra + (off + j) * Dqk);
+        for (int64_t j = 0; j < n; ++j) rows[b].push_back(extra + (off + j) * Dqk);
       }
     }
-    const int64_t nt = static_cast<int64_t>(rows.size());
-    for (int64_t h = 0; h < Hq; ++h) {
-      double* o = out + (b * Hq + h) * Dv;
-      if (nt == 0) {
-        for (int64_t d = 0; d < Dv; ++d) o[d] = 0.0;
-        if (lse) lse[b * Hq + h] = -std::numeric_limits<double>::infinity();
-        continue;
-      }
-      const uint16_t* qh = q + (b * Hq + h) * Dqk;
-      std::vector<double> logit(nt);
-      for (int64_t t = 0; t < nt; ++t) {
-        double dot = 0.0;
-        for (int64_t d = 0; d < Dqk; ++d) dot += bf16_to_double(qh[d]) * bf16_to_double(rows[t][d]);
-        logit[t] = scale * dot;
-      }
-      double m = logit[0];
-      for (int64_t t = 1; t < nt; ++t) m = std::max(m, logit[t]);
-      double den = 0.0;
-      std::vector<double> num(Dv, 0.0);
-      for (int64_t t = 0; t < nt; ++t) {
-        const double e = std::exp(logit[t] - m);
-        den += e;
-        for (int64_t d = 0; d < Dv; ++d) num[d] += e * bf16_to_double(rows[t][d]);
-      }
-      for (int64_t d = 0; d < Dv; ++d) o[d] = num[d] / den;
-      if (lse) lse[b * Hq + h] = m + std::log(den);
+  }
+  // every (sequence, head) pair is independent
+  parallel_for(B * Hq, threads, [&](int64_t bh) {
+    const int64_t b = bh / Hq, h = bh % Hq;
+    const std::vector<const uint16_t*>& rb = rows[b];
+    const int64_t nt = static_cast<int64_t>(rb.size());
+    double* o = out + (b * Hq + h) * Dv;
+    if (nt == 0) {
+      for (int64_t d = 0; d < Dv; ++d) o[d] = 0.0;
+      if (lse) lse[b * Hq + h] = -std::numeric_limits<double>::infinity();
+      return;
     }
+    const uint16_t* qh = q + (b * Hq + h) * Dqk;
+    std::vector<double> logit(nt);
+    for (int64_t t = 0; t < nt; ++t) {
+      double dot = 0.0;
+      for (int64_t d = 0; d < Dqk; ++d) dot += bf16_to_double(qh[d]) * bf16_to_double(rb[t][d]);
+      logit[t] = scale * dot;
+    }
+    double m = logit[0];
+    for (int64_t t = 1; t < nt; ++t) m = std::max(m, logit[t]);
+    double den = 0.0;
+    std::vector<double> num(Dv, 0.0);
+    for (int64_t t = 0; t < nt; ++t) {
+      const double e = std::exp(logit[t] - m);
+      den += e;
+      for (int64_t d = 0; d < Dv; ++d) num[d] += e * bf16_to_double(rb[t][d]);
+    }
+    for (int64_t d = 0; d < Dv; ++d) o[d] = num[d] / den;
+    if (lse) lse[b * Hq + h] = m + std::log(den);
   });
   return 0;
 }

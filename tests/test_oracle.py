@@ -386,3 +386,30 @@ def test_layer_step_pools_match_bulk_compression_of_history(oracle_mod, kind):
         assert res["idx"].shape == (1, shape.k)
         assert sorted(res["idx"][0][res["idx"][0] >= 0].tolist()) == \
             sorted(set(res["idx"][0][res["idx"][0] >= 0].tolist()))
+
+
+# ---------------------------------------------------------------- threading
+
+def test_threaded_stages_equal_single_thread(oracle_mod):
+    """The oracle shares out independent outputs (indexer entries, attention
+    (sequence, head) pairs, top-k rows) among threads; every output is still
+    computed by one thread in the same order, so any thread count gives the
+    same bits as one thread."""
+    B, Hi, Di = 3, 4, 32
+    counts = [17, 0, 40]
+    offs = np.zeros(B + 1, np.int64)
+    offs[1:] = np.cumsum(counts)
+    keys = _normal_bits("t.k", (int(offs[-1]), Di))
+    q = _normal_bits("t.q", (B, Hi, Di))
+    w = synth.uniform(RNG_SEED, "t.w", (B, Hi)).numpy()
+    one = oracle_mod.indexer_scores(q, w, keys, offs, threads=1)
+    for t in (2, 5, 64):
+        assert np.array_equal(oracle_mod.indexer_scores(q, w, keys, offs, threads=t), one)
+    ti, tv = oracle_mod.topk(one.astype(np.float32), offs, 8, threads=1)
+    ti5, tv5 = oracle_mod.topk(one.astype(np.float32), offs, 8, threads=5)
+    assert np.array_equal(ti, ti5) and np.array_equal(tv, tv5)
+    qa, swa, L, W, extra, aoffs, idx, Dv = _rand_attn()
+    o1, l1 = oracle_mod.decode_attn(qa, swa, L, W, extra, aoffs, idx, 0.3, Dv, threads=1)
+    for t in (3, 16):
+        o, l = oracle_mod.decode_attn(qa, swa, L, W, extra, aoffs, idx, 0.3, Dv, threads=t)
+        assert np.array_equal(o, o1) and np.array_equal(l, l1)

@@ -51,3 +51,36 @@ def test_replicas_draw_distinct_workloads():
     b = synth.c4_lengths(base + 1000, 64)   # rank 1's seed in bench.build_workload
     assert not torch.equal(a, b)
     assert torch.equal(a, synth.c4_lengths(base, 64))
+
+
+def test_bench_gpus_2_self_launches_two_replicas():
+    """`bench.py --gpus 2` without a torchrun environment re-launches itself
+    with two ranks; rank 0 prints one line whose latency is the slower rank's
+    (not divided by the rank count) and whose aggregate throughput counts both
+    replicas."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env["OMP_NUM_THREADS"] = "1"
+    script = os.path.join(ROOT, "tests", "replica_stub_bench.py")
+    r = subprocess.run([sys.executable, script, "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=240)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2
+    assert abs(line["value"] - 110.0) < 1e-6            # max over ranks, in us
+    assert abs(line["e2e"]["value"] - 220.0) < 1e-6
+    assert abs(line["throughput_all_replicas"]["value"] - 2 * 64 / 110e-6) < 1e-3
+    assert line["config"]["parallelism"] == "replicas x2"
+
+
+def test_bench_rejects_mismatched_world_size():
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    script = os.path.join(ROOT, "tests", "replica_stub_bench.py")
+    r = subprocess.run([sys.executable, script, "--gpus", "2"], capture_output=True, text=True,
+                       env=env, timeout=120)
+    assert r.returncode != 0 and "--gpus 2" in (r.stderr + r.stdout)
