@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "select_core.cuh"
 #include "tc.cuh"
 
 namespace hsa {
@@ -97,6 +98,13 @@ struct AttnParams {
   uint32_t* status;
   int early;              // the previous kernel writes only idx (see AttnArgs)
   int cl;                 // the S splits form a cluster and merge in shared memory
+  // Fused selection (the layer's C4 path; sel_scores != null): idx is null and
+  // the last split of every token selects the token's top-k itself from the
+  // indexer's scores and per-row key histogram (see select_token).
+  const float* sel_scores;  // scores at the pool's row positions
+  uint32_t* row_hist;       // [B, kRowHistBins], zeroed again by the selection
+  uint64_t* cand_ws;        // heavy-tie candidates, at the pool's row positions
+  int32_t* topk_out;        // [B, k] the selection in order (may be null)
 };
 
 struct SeqGeom {
@@ -116,7 +124,7 @@ HSA_DEVINL SeqGeom seq_geom(const AttnParams& p, int b) {
   if (p.extra) {
     g.off = p.sp.start(b);
     g.nb = p.sp.count(b);
-    if (p.idx) {
+    if (p.idx || p.sel_scores) {
       g.n_extra = p.k;
     } else {
       g.n_extra = g.nb < p.max_rows ? g.nb : p.max_rows;
@@ -157,7 +165,7 @@ HSA_DEVINL const uint16_t* slot_row_j(const AttnParams& p, int b, const SeqGeom&
   }
   const int64_t e = slot - g.n_swa;
   if (e >= g.n_extra) return nullptr;
-  if (!p.idx) j = e;
+  if (!p.idx && !p.sel_scores) j = e;
   if (j < 0) return nullptr;
   if (j >= g.nb) {
     if (report) set_status(p.status, HSA_DEV_BOUNDS);
@@ -214,18 +222,23 @@ struct Shared {
   uint64_t q_full, fin;
   uint32_t tmem;
   int abort;
-  float red[kSmWarps][64];
-  float bc[64];
+  float red[kSmWarps][64];  // softmax: per-warp column reductions; merge: every split's weight
   float m[64];      // running maximum per head (log2 units), identical for every thread
   float alpha[64];  // rescale factor of the current chunk per head
   float inv[64];    // 1 / softmax denominator per head (0 when nothing was attended)
   float l[64];      // softmax denominator per head (relative to m)
   float xm[kMaxCl][64], xl[kMaxCl][64];  // cluster merge: every split's m and l
-  float xw[kMaxCl][64];                   // cluster merge: every split's weight per head
   int xok[kMaxCl];  // cluster merge: the split has a partial output
   int done_ok;      // the softmax warps finished without an abort: O^T may be written out
   const uint16_t* rows[kMaxTC][kKeys];  // gather tables of the producers (this chunk)
+  // fused selection: this split's share of the token's selected entries
+  // (row-local indices, 0xffff past the selection), their total, and the
+  // barrier the selecting split arrives on once both are written
+  uint16_t sel[kMaxTC * kKeys];
+  uint32_t sel_n;
+  uint64_t sel_full;
 };
+static_assert(kKeys * kMaxTC >= 512, "a split's share of a fused selection (k <= 512) fits");
 
 // Bounded wait that also gives up when another role has aborted.
 HSA_DEVINL bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity, uint32_t* status) {
@@ -242,6 +255,304 @@ HSA_DEVINL bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity, uint32
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- fused selection
+//
+// In the layer's C4 path the token's last split selects the token's top-k
+// itself, after the indexer, from its scores and from the per-row histogram
+// of the top kRowHistBits order-key bits that the indexer built while writing
+// them (Lightning TopK: [KD] §Arquitectura del Sistema; [WK] §推理侧优化).  It
+// finds the threshold bin d (fewer than k scores above it, at least k at or
+// above it), keeps the scores above bin d and in it in one pass over the row,
+// sorts those survivors by composite (value descending, lower index first) and
+// takes the first k: the same list, in the same order, as the standalone
+// top-k.  The other splits of the token attend the rows that need no
+// selection (the window) meanwhile, and wait for the selecting split to write
+// their share of the list into their shared memory.
+
+constexpr int kSelRowMax = 32768;  // scores per row the fused selection handles
+static_assert(kRing * kPairBytes >= 4 * kSelRowMax, "a selected row's scores fit the ring");
+static_assert(kRowHistBins % (4 * kThreads) == 0, "whole 16-byte histogram loads per thread");
+constexpr int kSelMax = 2048;      // composites of the selection's shared-memory buffer
+constexpr int kSelSort = 1024;     // winners + candidates held in shared memory, at most
+constexpr int kSelRank = 512;      // candidates ranked by counting, at most
+constexpr int kSelMaxK = 512;      // k the fused selection handles
+
+// Remote arrive (release, cluster scope) on the barrier at cluster address `bar`.
+HSA_DEVINL void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait (acquire, cluster scope) for the barrier's phase `parity`;
+// also gives up when another role has aborted.
+HSA_DEVINL bool wait_cluster_or_abort(int* abort, uint64_t* bar, uint32_t parity, uint32_t* status) {
+  const uint32_t a = tc::smem_u32(bar);
+  const uint64_t t0 = tc::global_timer();
+  for (uint32_t i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((i & 63u) == 63u) {
+      if (*reinterpret_cast<volatile int*>(abort)) return false;
+      if (tc::global_timer() - t0 > tc::kSpinNanos || i > tc::kSpinPolls) {
+        set_status(status, HSA_DEV_TIMEOUT);
+        *reinterpret_cast<volatile int*>(abort) = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// First C4 entry of split q's share of a token's selection.
+HSA_DEVINL int64_t share_first(const AttnParams& p, int n_swa, int q) {
+  const int64_t e = static_cast<int64_t>(q) * p.sps - n_swa;
+  return e < 0 ? 0 : (e > p.k ? p.k : e);
+}
+
+HSA_DEVINL void st_cluster_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// 4-byte asynchronous global -> shared copy (any 4-byte-aligned source).
+HSA_DEVINL void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+// Selects token b's top-k and hands every split of the token its share (every
+// thread of the CTA calls it; the ring and `sbuf` (kSelMax composites) are
+// free scratch).  n: the row's live scores (at most kSelRowMax); rank: this
+// CTA's rank in the token's cluster.  No step appends through a shared
+// counter: survivors get their places from one block-wide scan of per-thread
+// counts, and candidates are chosen by counting ranks, so every step is a few
+// block-wide phases whatever the row holds.  The list the splits attend is in
+// a fixed order (not sorted by value); its sorted copy, when asked for, is
+// written at the end of the kernel (write_topk_sorted).
+HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uint64_t* sbuf, int b,
+                             const SeqGeom& g, int n, uint32_t rank) {
+  __shared__ uint32_t s_scan[33], s_out[3], s_cnt;
+  __shared__ __align__(16) uint32_t s_hbins[kRowHistBins / kThreads];
+  const int t = threadIdx.x;
+  uint32_t* s_row = reinterpret_cast<uint32_t*>(ring);  // [kSelRowMax] score bits
+  const uint32_t kk = static_cast<uint32_t>(n < p.k ? n : p.k);
+  const bool all = n <= p.k;
+  const uint32_t* row = reinterpret_cast<const uint32_t*>(p.sel_scores + g.off);
+  // Loops stay rolled throughout: this code runs once per launch, and its
+  // instruction fetches cost more than loop overhead.
+  // (1) the row's scores to shared memory, every copy in flight at once: the
+  // 16-byte-aligned body to s_row[0, 4 nv), then the at most 3 + 3 scores
+  // before and after it; and the sum of this thread's kPer bins of the row's
+  // histogram (bins counted from the top bin down)
+  constexpr int kPer = kRowHistBins / kThreads;
+  const int lo = kRowHistBins - kPer * (t + 1);  // this thread's bins: [lo, lo + kPer)
+  uint4* gh = reinterpret_cast<uint4*>(p.row_hist + static_cast<int64_t>(b) * kRowHistBins + lo);
+  const int head = static_cast<int>(
+      min(static_cast<uintptr_t>(n), ((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) >> 2));
+  const int nv = (n - head) >> 2, body = 4 * nv;
+#pragma unroll 1
+  for (int v = t; v < nv; v += kThreads) tc::cp_async16(s_row + 4 * v, row + head + 4 * v, 16u);
+#pragma unroll 1
+  for (int j = t; j < n - body; j += kThreads) cp_async4(s_row + body + j, row + (j < head ? j : body + j));
+  tc::cp_async_commit();
+  uint4 hv[kPer / 4];  // this thread's bins, kept for the threshold search
+#pragma unroll
+  for (int i = 0; i < kPer / 4; ++i) hv[i] = __ldcg(gh + i);
+  uint32_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer / 4; ++i) sum += (hv[i].x + hv[i].y) + (hv[i].z + hv[i].w);
+  // (2) the threshold bin d: fewer than kk scores above it, at least kk at or
+  // above it.  One scan of the per-thread sums finds the thread whose bins
+  // hold it; that thread hands its bins to warp 0 (shared memory), which
+  // scans them.
+  uint32_t d = 0;
+  if (!all) {
+    uint32_t total;
+    const uint32_t a = block_inclusive_sum<uint32_t>(sum, s_scan, &total) - sum;
+    if (a < kk && a + sum >= kk) {
+      uint4* hb = reinterpret_cast<uint4*>(s_hbins);
+#pragma unroll
+      for (int i = 0; i < kPer / 4; ++i) hb[i] = hv[i];
+      s_out[0] = static_cast<uint32_t>(lo);
+      s_out[1] = a;
+    }
+    __syncthreads();
+    if (t < 32) {
+      const uint32_t blo = s_out[0], above = s_out[1];
+      const uint32_t cnt = s_hbins[kPer - 1 - t];  // lane 0: the range's top bin
+      uint32_t incl = cnt;
+#pragma unroll 1
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (t >= o) incl += y;
+      }
+      const uint32_t hit = __ballot_sync(0xffffffffu, above + incl >= kk);
+      if (t == 0) s_out[2] = blo + kPer - 1 - (hit ? __ffs(hit) - 1 : 0);
+    }
+    __syncthreads();
+    d = s_out[2];
+  }
+  // the histogram is zeroed again for the next step
+#pragma unroll
+  for (int i = 0; i < kPer / 4; ++i) gh[i] = make_uint4(0u, 0u, 0u, 0u);
+  tc::cp_async_wait<0>();
+  __syncthreads();
+  // (3) winners (above bin d; every score when all) and candidates (in bin d).
+  // One pass classifies every score and keeps, per thread, masks of its
+  // winners and candidates (kGrp slots per group, at most kGroups groups) and
+  // their counts; one scan gives every thread its places; the second pass
+  // visits only the masked slots.  Slot s of s_row holds row entry idx(s).
+  // Group gi covers slots [gi * kThreads * kGrp, (gi + 1) * kThreads * kGrp);
+  // thread t reads its 16-byte chunks gi * (kGrp / 4) * kThreads + q * kThreads
+  // + t (consecutive lanes, consecutive chunks).
+  constexpr int kGrp = 16;                              // slots per thread per group
+  constexpr int kGroups = kSelRowMax / (kThreads * kGrp);
+  auto slot_of = [&](int gi, int bit) { return ((gi * (kGrp / 4) + (bit >> 2)) * kThreads + t) * 4 + (bit & 3); };
+  const int dd = all ? -1 : static_cast<int>(d);       // winners: digit > dd
+  uint32_t wmask[kGroups], cmask[kGroups];
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int gi = 0; gi < kGroups; ++gi) {
+    wmask[gi] = cmask[gi] = 0u;
+    if (gi * kThreads * kGrp >= n) continue;      // (uniform)
+#pragma unroll
+    for (int q4 = 0; q4 < kGrp / 4; ++q4) {
+      const uint4 w = reinterpret_cast<const uint4*>(s_row)[(gi * (kGrp / 4) + q4) * kThreads + t];
+      const uint32_t u4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int bit = 4 * q4 + e;
+        const int dig = static_cast<int>(order_key(u4[e]) >> kRowHistShift);
+        const bool in = slot_of(gi, bit) < n;
+        wmask[gi] |= (in && dig > dd ? 1u : 0u) << bit;
+        cmask[gi] |= (in && !all && dig == dd ? 1u : 0u) << bit;
+      }
+    }
+    cnt += __popc(wmask[gi]) + (__popc(cmask[gi]) << 16);
+  }
+  uint32_t total;
+  const uint32_t off = block_inclusive_sum<uint32_t>(cnt, s_scan, &total) - cnt;
+  const uint32_t nw = total & 0xffffu, ncd = total >> 16;
+  // winners then candidates, contiguous in sbuf, when both fit the merge sort;
+  // otherwise ("heavy") the candidates go to the row's workspace
+  const bool heavy = nw + ncd > static_cast<uint32_t>(kSelSort);  // (uniform)
+  uint64_t* cand = heavy ? p.cand_ws + g.off : sbuf + nw;
+  uint32_t wo = off & 0xffffu, co = off >> 16;
+  bool nan = false;
+#pragma unroll
+  for (int gi = 0; gi < kGroups; ++gi) {  // (unrolled: the masks stay in registers)
+    uint32_t m = wmask[gi] | cmask[gi];
+#pragma unroll 1
+    while (m) {
+      const int bit = __ffs(m) - 1;
+      m &= m - 1;
+      const int slot = slot_of(gi, bit);
+      const uint32_t u = s_row[slot];
+      nan |= is_nan_bits(u);
+      const int ix = slot < body ? slot + head : (slot - body < head ? slot - body : slot);
+      const uint64_t x = composite(order_key(u), static_cast<uint32_t>(ix));
+      if ((wmask[gi] >> bit) & 1u) {
+        if (wo < static_cast<uint32_t>(kSelMaxK)) sbuf[wo] = x;
+        ++wo;
+      } else {
+        if (co < static_cast<uint32_t>(n)) cand[co] = x;
+        ++co;
+      }
+    }
+  }
+  if (nan) set_status(p.status, HSA_DEV_NAN);
+  __syncthreads();
+  // (4) the attended list: the winners in the order of the pass (fixed by the
+  // scan, so every run lists them alike), then the `need` largest candidates
+  // by their rank among the candidates (few: ranked by counting; many: radix
+  // select).  The list, as composites, is kept in the row's workspace for the
+  // ordered copy (topk_out) written at the end of the kernel.
+  uint32_t nsel = nw < kk ? nw : kk;
+  if (!all && kk > nsel && ncd > 0) {
+    const uint32_t need = kk - nsel;
+    if (need >= ncd) {
+      for (uint32_t i = t; i < ncd; i += kThreads) sbuf[nsel + i] = cand[i];
+      nsel += ncd;
+    } else if (!heavy && ncd <= static_cast<uint32_t>(kSelRank)) {
+      // candidate c's rank = the number of candidates greater than it (unique composites)
+      uint64_t x[kSelRank / kThreads];
+      uint32_t r[kSelRank / kThreads];
+#pragma unroll
+      for (int q = 0; q < kSelRank / kThreads; ++q) {
+        const uint32_t ci = t + q * kThreads;
+        x[q] = ci < ncd ? cand[ci] : ~0ull;
+        r[q] = 0;
+      }
+#pragma unroll 4
+      for (uint32_t i = 0; i < ncd; ++i) {
+        const uint64_t y = cand[i];
+#pragma unroll
+        for (int q = 0; q < kSelRank / kThreads; ++q) r[q] += y > x[q] ? 1u : 0u;
+      }
+      __syncthreads();  // every candidate read before the list grows over them
+#pragma unroll
+      for (int q = 0; q < kSelRank / kThreads; ++q)
+        if (t + q * kThreads < static_cast<int>(ncd) && r[q] < need) sbuf[nsel + r[q]] = x[q];
+      nsel += need;
+    } else {
+      if (t == 0) s_cnt = nsel;
+      __syncthreads();
+      select_rest<2048 / kThreads>(cand, ncd < static_cast<uint32_t>(n) ? ncd : static_cast<uint32_t>(n),
+                                   need, sbuf, &s_cnt, kSelMaxK, s_row, s_scan, s_out,
+                                   64 - kRowHistBits);  // 11-bit digits
+      __syncthreads();
+      nsel = s_cnt < kk ? s_cnt : kk;
+    }
+  }
+  __syncthreads();
+  // (5) every split's share of the list, every listed row prefetched into L2
+  // for the splits' gathers, and the list kept for the ordered copy
+  for (int e = t; e < p.k; e += kThreads) {
+    const bool live = e < static_cast<int>(nsel);
+    const uint64_t x = live ? sbuf[e] : 0ull;
+    const uint32_t j = live ? 0xffffffffu - static_cast<uint32_t>(x) : 0u;
+    if (live) {
+      const uint16_t* rowp = p.extra + (g.off + j) * p.Dqk;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rowp),
+                   "r"(static_cast<uint32_t>(p.Dqk * 2))
+                   : "memory");
+      if (p.topk_out) p.cand_ws[g.off + e] = x;
+    }
+    const int q = static_cast<int>((g.n_swa + e) / p.sps);  // the split attending entry e
+    uint16_t* dst = &sh.sel[e - share_first(p, g.n_swa, q)];
+    const uint16_t v = live ? static_cast<uint16_t>(j) : uint16_t(0xffff);
+    if (static_cast<uint32_t>(q) == rank) *dst = v;
+    else st_cluster_u16(map_rank(dst, static_cast<uint32_t>(q)), v);
+  }
+  if (t < p.S) st_cluster_u32(map_rank(&sh.sel_n, static_cast<uint32_t>(t)), nsel);
+  __syncthreads();
+  if (t == 0) {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    for (int q = 0; q < p.S; ++q) mbar_arrive_cluster(map_rank(&sh.sel_full, static_cast<uint32_t>(q)));
+  }
+}
+
+// The selection of token b in order (value descending, lower index first),
+// to topk_out: the listed composites, kept in the row's workspace by the
+// selection, sorted in shared memory (every thread of the selecting CTA,
+// after its attention; the ring is free).
+HSA_DEVINL void write_topk_sorted(const AttnParams& p, uint8_t* ring, int b, const SeqGeom& g,
+                                  int nsel) {
+  const int t = threadIdx.x;
+  uint64_t* a = reinterpret_cast<uint64_t*>(ring);
+  for (int i = t; i < nsel; i += kThreads) a[i] = p.cand_ws[g.off + i];
+  int P = 32;
+  while (P < nsel) P <<= 1;
+  merge_sort_desc<kSelMaxK / kThreads>(a, a + kSelMaxK, nsel, P);
+  int32_t* o = p.topk_out + static_cast<int64_t>(b) * p.k;
+  for (int e = t; e < p.k; e += kThreads)
+    o[e] = e < nsel ? static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(a[e])) : -1;
 }
 
 HSA_DEVINL void write_result(const AttnParams& p, int b, int g, int s, int h, int dv, float o) {
@@ -313,7 +624,7 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
     float L = 0.f;
     for (int r = 0; r < S; ++r) {
       const float w = sh.xl[r][tid] > 0.f ? tc::ex2_approx(sh.xm[r][tid] - M) : 0.f;
-      sh.xw[r][tid] = w;
+      sh.red[r][tid] = w;  // (the softmax's reduction scratch is free by now)
       L += w * sh.xl[r][tid];
     }
     sh.inv[tid] = L > 0.f ? __frcp_rn(L) : 0.f;
@@ -335,7 +646,7 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
     for (int r = 0; r < S; ++r) {
       if (!sh.xok[r]) continue;
       const uint32_t src = map_rank(ring + u * kUnitBytes + row * 16, r);
-      const float* w = &sh.xw[r][q16 * 16];
+      const float* w = &sh.red[r][q16 * 16];
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         const float4 v = ld_cluster_f32x4(src + c4 * (kKeys * 16u));
@@ -378,7 +689,8 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
   cluster_sync();  // no split leaves while another may still read its ring
 }
 
-template <int kN>
+// kSel: the fused selection of the layer's C4 path (see select_token).
+template <int kN, bool kSel>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
@@ -415,9 +727,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     }
     return;
   }
-  if (p.extra && !p.idx && geo.nb > p.max_rows && tid == 0 && s == 0 && g == 0)
+  if (!kSel && p.extra && !p.idx && geo.nb > p.max_rows && tid == 0 && s == 0 && g == 0)
     set_status(p.status, HSA_DEV_BOUNDS);
-  const int nchunks = (nt + TC - 1) / TC;
+  // Chunks of up to TC tiles.  With the fused selection the leading tiles that
+  // hold window rows only form a chunk of their own, attended while the
+  // token's last split selects the rest; chunks holding compressed rows wait
+  // for that selection.
+  const int win_tiles = kSel ? max(0, min(geo.n_swa / kKeys - t0, min(nt, TC))) : 0;
+  auto chunk_tb = [&](int c) { return c == 0 ? t0 : t0 + win_tiles + (win_tiles > 0 ? c - 1 : c) * TC; };
+  auto chunk_nct = [&](int c) { return min(c == 0 && win_tiles > 0 ? win_tiles : TC, t1 - chunk_tb(c)); };
+  auto chunk_sel = [&](int c) {
+    return kSel && static_cast<int64_t>(chunk_tb(c) + chunk_nct(c)) * kKeys > geo.n_swa;
+  };
+  const int nchunks = win_tiles > 0 ? 1 + (nt - win_tiles + TC - 1) / TC : (nt + TC - 1) / TC;
+  const uint32_t crank = p.cl ? cluster_rank() : 0u;
+  const bool selector = kSel && s == p.S - 1;
+  const int64_t sel_e0 = kSel ? share_first(p, geo.n_swa, s) : 0;  // first entry of this split's share
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -446,6 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     }
     tc::mbar_init(&sh.q_full, kProdThreads);
     tc::mbar_init(&sh.fin, 1);
+    if (kSel) tc::mbar_init(&sh.sel_full, 1);
     sh.abort = 0;
     tc::fence_mbar_init();
   }
@@ -461,6 +787,53 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sh.tmem;
+  if (kSel) {
+    // every split's barriers exist before the selecting split arrives on them
+    if (p.cl) cluster_sync();
+    // the window rows this split attends first, into L2 while the previous
+    // kernels finish (the append's new row included: a prefetch brings no
+    // stale copy, the append's store updates L2)
+#pragma unroll 1
+    for (int r = tid; r < win_tiles * kKeys; r += kThreads) {
+      const int64_t pos = geo.L - geo.n_swa + static_cast<int64_t>(t0) * kKeys + r;
+      const uint16_t* rowp = p.swa + (static_cast<int64_t>(b) * p.W + pos % p.W) * p.Dqk;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rowp),
+                   "r"(static_cast<uint32_t>(p.Dqk * 2))
+                   : "memory");
+    }
+    if (selector) {
+      // Q first (the previous kernel does not write it), then the selection,
+      // which needs the indexer's scores and histogram
+      if (warp >= kProdWarp0) {
+        const int pt_ = tid - kProdWarp0 * 32, nq = kN * NSL * 8;
+        for (int i = pt_; i < nq; i += kProdThreads) {
+          const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, cc = rem & 7;
+          const bool v = h < p.HG;
+          const uint16_t* src =
+              v ? p.q + (static_cast<int64_t>(b) * p.Hq + g * p.HG + h) * p.Dqk + j * 64 + cc * 8 : p.q;
+          tc::cp_async16(qs + j * (kN * 128) + sw128(h, cc), src, v ? 16u : 0u);
+        }
+        tc::cp_async_commit();
+      }
+      pdl_wait();
+      int n = static_cast<int>(geo.nb);
+      // an invalid span (bad offsets or a live count above the capacity), or a
+      // row longer than the host-checked bound: flagged, treated as empty
+      if (!p.sp.valid(b) || geo.nb > kSelRowMax) {
+        if (tid == 0) set_status(p.status, HSA_DEV_BOUNDS);
+        n = 0;
+      }
+      // survivors: the even tiles' P^T buffer when it holds kSelMax composites,
+      // else the region the plan adds after it
+      uint8_t* sel_buf = 2 * kN * 128 >= kSelMax * 8 ? pbuf0 : pbuf0 + 2 * kN * 128;
+      select_token(p, sh, ring, reinterpret_cast<uint64_t*>(sel_buf), b, geo, n, crank);
+      // the ring held scores: zeroed again (rows never gathered must be finite)
+      for (int i = tid; i < static_cast<int>(kRing * kPairBytes / 16); i += kThreads)
+        reinterpret_cast<uint4*>(ring)[i] = make_uint4(0u, 0u, 0u, 0u);
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+    }
+  }
 
   if (warp >= kProdWarp0) {
     // ------------------------------------------------------------ gatherers
@@ -499,7 +872,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       if (np == 0) pend0 = it; else pend1 = it;
       ++np;
     };
+    bool q_pre = selector;  // the selecting split issued chunk 0's Q before selecting
     auto issue_q = [&]() {  // Q (every gather thread), one cp.async group
+      if (q_pre) {
+        q_pre = false;
+        push(-1);
+        return;
+      }
       const int nq = kN * NSL * 8;
       for (int i = pt_; i < nq; i += kProdThreads) {
         const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, cc = rem & 7;
@@ -513,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     };
     int64_t item = 0;
     for (int c = 0; c < nchunks; ++c) {
-      const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
+      const int tb = chunk_tb(c), nct = chunk_nct(c);
       // every previous item is issued (its rows were read at issue): refill the
       // tables; a warp that gave up is known to all from here on
       if (tc::named_barrier_or(2, kProdThreads, !ok)) {
@@ -525,13 +904,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         pdl_wait();
         pdl_trigger();
       }
+      if (chunk_sel(c)) {  // this chunk's compressed rows come from the selection
+        const bool f = !wait_cluster_or_abort(&sh.abort, &sh.sel_full, 0, p.status);
+        if (tc::named_barrier_or(2, kProdThreads, f)) {
+          ok = false;
+          break;
+        }
+      }
       {
         constexpr int kPer = (kMaxTC * kKeys + kProdThreads - 1) / kProdThreads;
         int64_t jv[kPer];
 #pragma unroll
         for (int k2 = 0; k2 < kPer; ++k2) {  // the list entries first: loads in flight together
           const int r = pt_ + k2 * kProdThreads;
-          jv[k2] = r < nct * kKeys ? slot_index(p, b, geo, static_cast<int64_t>(tb) * kKeys + r) : 0;
+          const int64_t slot = static_cast<int64_t>(tb) * kKeys + r;
+          if (kSel) {
+            const int64_t e = slot - geo.n_swa;
+            const uint16_t v = r < nct * kKeys && e >= 0 && e < p.k ? sh.sel[e - sel_e0] : uint16_t(0);
+            jv[k2] = v == 0xffff ? -1 : static_cast<int64_t>(v);
+          } else {
+            jv[k2] = r < nct * kKeys ? slot_index(p, b, geo, slot) : 0;
+          }
         }
 #pragma unroll
         for (int k2 = 0; k2 < kPer; ++k2) {
@@ -546,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       if (c > 0) {
         // Q shares its region with the P^T buffers of the previous chunk, free
         // once that chunk's last O^T MMAs are done
-        const int lt = c * TC - 1;
+        const int lt = tb - t0 - 1;
         const bool f = !wait_or_abort(sh, &sh.o_done[lt & 1], (lt >> 1) & 1, p.status);
         if (tc::named_barrier_or(2, kProdThreads, f)) {
           ok = false;
@@ -610,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       int64_t item = 0;
       int gt = 0;  // tiles through pass 2 so far (P^T buffer gt & 1)
       for (int c = 0; c < nchunks && ok; ++c) {
-        const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
+        const int nct = chunk_nct(c);
         if (c > 0 && !wait_or_abort(sh, &sh.s_empty, (c - 1) & 1, p.status)) {
           ok = false;
           break;
@@ -692,6 +1085,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     if (tid < kN) sh.m[tid] = -INFINITY;
     bool ok = true;
     int gt = 0;
+    // bit i: phase parity of s_full[i] in the current chunk (chunks may use
+    // different numbers of tiles, so each barrier keeps its own count)
+    uint32_t sf_par = 0;
     auto agree = [&](bool failed) { return !tc::named_barrier_or(1, kKeys, failed); };
     // S^T columns [col, col + kGW) of this lane, scaled to log2 units; -inf when masked
     auto load_s = [&](uint32_t col, bool valid, float (&x)[32]) {
@@ -704,14 +1100,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         x[i] = (i < kGW && valid) ? __uint_as_float(raw[i]) * p.scale_log2 : -INFINITY;
     };
     for (int c = 0; c < nchunks && ok; ++c) {
-      const int tb = t0 + c * TC, nct = min(TC, t1 - tb);
+      const int tb = chunk_tb(c), nct = chunk_nct(c);
       // which of this lane's slots are attended, per chunk tile (loads issued before any wait)
       if (c == 0) pdl_wait();  // the index lists come from the previous kernel
+      if (chunk_sel(c) && !agree(!wait_cluster_or_abort(&sh.abort, &sh.sel_full, 0, p.status))) {
+        ok = false;
+        break;
+      }
       uint32_t vmask = 0;
       for (int tc_ = 0; tc_ < nct; ++tc_) {
         const int64_t slot = static_cast<int64_t>(tb + tc_) * kKeys + tid;
-        vmask |= (slot >= a0 && slot < a1 && slot_row(p, b, geo, slot, false) != nullptr ? 1u : 0u)
-                 << tc_;
+        bool v;
+        if (kSel)  // window rows, and the selected entries (sel_n of them)
+          v = slot < geo.n_swa || (slot - geo.n_swa < static_cast<int64_t>(sh.sel_n) &&
+                                   slot - geo.n_swa < p.k);
+        else
+          v = slot_row(p, b, geo, slot, false) != nullptr;
+        vmask |= (slot >= a0 && slot < a1 && v ? 1u : 0u) << tc_;
       }
       // ---- tile by tile, as soon as its S^T lands (online softmax): the tile's
       // maximum per head moves the running maximum m only when it rises by more
@@ -719,7 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       // buffer its O^T pass reads, so the first tiles' P^T is ready before the
       // chunk's last S^T
       for (int tc_ = 0; tc_ < nct; ++tc_, ++gt) {
-        if (!agree(!wait_or_abort(sh, &sh.s_full[tc_], c & 1, p.status))) {
+        if (!agree(!wait_or_abort(sh, &sh.s_full[tc_], (sf_par >> tc_) & 1u, p.status))) {
           ok = false;
           break;
         }
@@ -785,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         }
         if (buf == 1 && tc_ < nct - 1) {
           // buffer 1 overlays Q: wait until the chunk's pass 1 has read it for the last time
-          if (!agree(!wait_or_abort(sh, &sh.s_full[nct - 1], c & 1, p.status))) {
+          if (!agree(!wait_or_abort(sh, &sh.s_full[nct - 1], (sf_par >> (nct - 1)) & 1u, p.status))) {
             ok = false;
             break;
           }
@@ -818,6 +1223,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
         tc::mbar_arrive(&sh.p_full[buf]);
       }
       if (!ok) break;
+      sf_par ^= (1u << nct) - 1u;  // s_full[0 .. nct) each completed one phase
       // this chunk's S^T columns may be overwritten by the next chunk
       tc::fence_before_sync();
       tc::mbar_arrive(&sh.s_empty);
@@ -891,6 +1297,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     __syncwarp();
     tc::tmem_dealloc(tmem, tmem_cols);
   }
+  if (selector && p.topk_out) write_topk_sorted(p, ring, b, geo, static_cast<int>(sh.sel_n));
 }
 
 // Merges the split partials: o = sum_s e^(lse_s - lse) o_s, lse = log sum_s e^lse_s.
@@ -984,6 +1391,9 @@ AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, in
   const int tc_fit = 512 / pl.N - NMT;  // TMEM columns left for S^T tiles
   pl.TC = tc_fit < kMaxTC ? tc_fit : kMaxTC;
   pl.smem = static_cast<size_t>(kRing) * kPairBytes + attn_q_region(NSL, pl.N) + 2 * pl.N * 128 + 1024;
+  // a fused selection's survivors live in the even tiles' P^T buffer, or
+  // after it when it is smaller than kSelMax composites
+  if (2 * pl.N * 128 < kSelMax * 8) pl.smem += kSelMax * 8;
   // keep co-resident CTAs within the SM's 512 TMEM columns
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>((pl.TC + NMT) * pl.N)) cols <<= 1;
@@ -993,6 +1403,11 @@ AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, in
   const size_t floor_bytes = per_sm / (512 / cols + 1) + 1;
   if (pl.smem < floor_bytes) pl.smem = floor_bytes;
   return pl;
+}
+
+bool attn_fused_ok(const AttnPlan& pl, int64_t k, int64_t max_row) {
+  return k >= 1 && k <= kSelMaxK && max_row > 0 && max_row <= kSelRowMax && pl.G == 1 &&
+         (pl.S == 1 || pl.cl);
 }
 
 size_t attn_workspace_bytes(const AttnPlan& pl, int64_t B, int64_t Hq, int64_t Dv) {
@@ -1033,12 +1448,20 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.status = status;
   p.early = a.only_idx_pending ? 1 : 0;
   p.cl = pl.cl;
+  p.sel_scores = a.sel_scores;
+  p.row_hist = a.row_hist;
+  p.cand_ws = a.cand_ws;
+  p.topk_out = a.topk_out;
+  const bool fused = a.sel_scores != nullptr;
   char* w = static_cast<char*>(ws) + kWsHeader;
   p.po = reinterpret_cast<float*>(w);
   p.plse = reinterpret_cast<float*>(
       w + ((static_cast<size_t>(a.B) * pl.S * a.Hq * a.Dv * 4 + 255) & ~size_t(255)));
   const unsigned grid = static_cast<unsigned>(a.B * pl.G * pl.S);
-  auto* kernel = pl.N == 16 ? attn_kernel<16> : (pl.N == 32 ? attn_kernel<32> : attn_kernel<64>);
+  auto* kernel = fused ? (pl.N == 16 ? attn_kernel<16, true>
+                                     : (pl.N == 32 ? attn_kernel<32, true> : attn_kernel<64, true>))
+                       : (pl.N == 16 ? attn_kernel<16, false>
+                                     : (pl.N == 32 ? attn_kernel<32, false> : attn_kernel<64, false>));
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(pl.smem));
   if (e != cudaSuccess) return e;

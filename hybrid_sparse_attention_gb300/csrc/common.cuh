@@ -105,6 +105,21 @@ HSA_DEVINL uint4 f32x8_to_bf16(const float f[8]) {
 
 HSA_DEVINL uint4 ld_stream_u4(const uint4* p) { return __ldcs(p); }
 
+// Order-preserving key of an fp32 score (its bits): larger key <=> larger
+// value; -0.0 is first folded onto +0.0 so the two compare equal.  Shared by
+// the top-k and by the indexer, which histograms the keys of the scores it
+// writes for the top-k.
+HSA_DEVINL uint32_t order_key(uint32_t u) {
+  if (u == 0x80000000u) u = 0u;  // -0.0 == +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The layer's indexer -> top-k histogram: per sequence, counts of the top
+// kRowHistBits bits of every score's order key.
+constexpr int kRowHistBits = 13;
+constexpr int kRowHistBins = 1 << kRowHistBits;
+constexpr int kRowHistShift = 32 - kRowHistBits;
+
 // Rows of a ragged sequence set.  Sequence b starts at offsets[b]; its row
 // count is offsets[b+1] - offsets[b] when seq_len is null, otherwise
 // (seq_len[b] + add) / ratio (the live prefix of a capacity-laid-out pool).
@@ -151,6 +166,17 @@ struct AttnArgs {
   // writes only the index lists: the window rows, lengths and q may be read
   // before waiting for it.  False when it may write anything else.
   bool only_idx_pending = false;
+  // Fused selection (idx null): the kernel selects every token's top-k itself
+  // from these scores (at the pool's row positions) and the per-row key
+  // histograms the indexer built (zeroed again), writing the selection in
+  // order to topk_out when it is not null; cand_ws holds heavy-tie
+  // candidates (one slot per pool row).  Only the kernels' own reads of their
+  // predecessor's outputs wait for it: every read of the append's outputs
+  // (window rows) and of the indexer's comes after the wait.
+  const float* sel_scores = nullptr;
+  uint32_t* row_hist = nullptr;
+  uint64_t* cand_ws = nullptr;
+  int32_t* topk_out = nullptr;
 };
 
 // Launch geometry of the fused attention: HG heads per CTA (N = MMA width),
@@ -167,6 +193,9 @@ struct AttnPlan {
 };
 
 AttnPlan attn_plan(int64_t B, int64_t Hq, int64_t Dqk, int64_t Dv, int64_t W, int64_t extra_slots);
+// Whether a plan can run the fused selection for a top-k of k over rows of at
+// most max_row scores.
+bool attn_fused_ok(const AttnPlan& pl, int64_t k, int64_t max_row);
 size_t attn_workspace_bytes(const AttnPlan& pl, int64_t B, int64_t Hq, int64_t Dv);
 // ws: attn_workspace_bytes() of scratch (partials after a kWsHeader gap);
 // status: the sticky status word to report into.

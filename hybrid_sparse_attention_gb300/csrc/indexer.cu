@@ -46,6 +46,7 @@ struct IndexerParams {
   float* scores;
   uint32_t* status;
   int wait_mode;   // programmatic dependent launch: see launch_indexer in internal.h
+  uint32_t* row_hist;  // per-sequence order-key histograms for the top-k (may be null)
 };
 
 struct Shared {
@@ -207,6 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
       }
       pdl_trigger();
       SeqCursor cur;
+      // the keys are read once: they leave L2 first, so the scores and
+      // histograms written here stay for the top-k that reads them next
+      const uint64_t keys_policy = tc::l2_policy_evict_first();
       int dep = -1;  // (wait_mode 2) tile that must wait for the previous kernel
       for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
         const int s = i % kStages;
@@ -224,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
         uint8_t* st = smem + s * stage_bytes;
         tc::mbar_arrive_expect_tx(&sh.full[s], stage_bytes);
         for (int kb = 0; kb < nkb; ++kb) {
-          tc::tma_load_2d(st + kb * a_kb, &kmap, kb * kb_elems, static_cast<int32_t>(row0),
-                          &sh.full[s]);
+          tc::tma_load_2d_hint(st + kb * a_kb, &kmap, kb * kb_elems, static_cast<int32_t>(row0),
+                               &sh.full[s], keys_policy);
           tc::tma_load_2d(st + nkb * a_kb + kb * b_kb, &qmap, kb * kb_elems, b * p.Hi,
                           &sh.full[s]);
         }
@@ -301,6 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
         for (int h = 0; h < kQRows; ++h)
           if (h < p.Hi) sc = fmaf(wv[h], fmaxf(dot[h], 0.f), sc);
         p.scores[row] = sc;
+        // the top-k's histogram: one count in the bin of the score's top key
+        // bits (a reduction: nothing waits for it)
+        if (p.row_hist)
+          atomicAdd(p.row_hist + static_cast<int64_t>(cur.b) * kRowHistBins +
+                        (order_key(__float_as_uint(sc)) >> kRowHistShift),
+                    1u);
       }
     }
   }
@@ -320,7 +330,7 @@ size_t indexer_smem_bytes(int Di) {
 
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
-                           cudaStream_t stream, bool pdl, int wait_mode) {
+                           cudaStream_t stream, bool pdl, int wait_mode, uint32_t* row_hist) {
   if (total_rows == 0) return cudaSuccess;
   if (B > kMaxSeqs) return cudaErrorInvalidValue;
   const int kb_elems = Di >= 64 ? 64 : Di;
@@ -337,7 +347,7 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
   // persistent: one CTA per SM (fewer when there are fewer tiles)
   const int64_t tiles_bound = (total_rows + kTileRows - 1) / kTileRows + B;
   const int grid = static_cast<int>(tiles_bound < device_sms() ? tiles_bound : device_sms());
-  IndexerParams p{w, sp, B, Hi, Di, scores, status, pdl ? wait_mode : 0};
+  IndexerParams p{w, sp, B, Hi, Di, scores, status, pdl ? wait_mode : 0, row_hist};
   return launch_k(indexer_kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, kmap, qmap, p);
 }
 

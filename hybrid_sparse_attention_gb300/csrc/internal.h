@@ -75,9 +75,12 @@ size_t indexer_smem_bytes(int Di);
 // of a sequence whose length, per sp, completes a block), the next kernel
 // being triggered first (it must read nothing the previous kernel writes
 // before its own wait).
+// row_hist (may be null): B x kRowHistBins counters to which every score
+// written adds one in the bin of its top kRowHistBits order-key bits.
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
-                           cudaStream_t stream, bool pdl = false, int wait_mode = 0);
+                           cudaStream_t stream, bool pdl = false, int wait_mode = 0,
+                           uint32_t* row_hist = nullptr);
 
 size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k);
 // Leading bytes of a top-k workspace (status word, row states, histograms)
@@ -89,6 +92,9 @@ size_t topk_zero_prefix_bytes(int64_t B, int64_t total_rows, int64_t k);
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
                         int32_t* idx, float* vals, void* ws, uint32_t* status,
                         cudaStream_t stream, int64_t max_row = 0, bool pdl = false);
+
+// The top-k workspace's candidate area (one 8-byte slot per score).
+uint64_t* topk_cand_area(void* ws, int64_t B, int64_t total_rows, int64_t k);
 
 size_t layer_workspace_bytes(const hsa_layer_desc& d);
 int layer_launch_count(const hsa_layer_desc& d);

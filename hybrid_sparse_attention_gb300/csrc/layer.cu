@@ -216,11 +216,26 @@ __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendPara
 
 HSA_HOST_DEVICE size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
+AttnPlan layer_attn_plan(const hsa_layer_desc& d) {
+  const int64_t slots = d.kind == HSA_LAYER_C4 ? d.k : d.max_pool_rows;
+  return attn_plan(d.B, d.Hq, d.Dqk, d.Dv, d.W, slots);
+}
+
+// A C4 layer whose rows and plan allow it selects its top-k inside the
+// attention kernel, from the indexer's scores and the per-row key histograms
+// the indexer builds while writing them (no top-k launch, no index list in
+// global memory); otherwise the top-k runs as its own kernels.
+bool layer_fused(const hsa_layer_desc& d) {
+  if (d.kind != HSA_LAYER_C4) return false;
+  const int64_t max_row = d.max_pool_rows > 0 ? d.max_pool_rows : d.pool_total_rows;
+  return attn_fused_ok(layer_attn_plan(d), d.k, max_row);
+}
+
 struct LayerWs {
-  size_t scores, topk, idx, attn, total;
+  size_t scores, topk, idx, hist, attn, total;
   LayerWs(const hsa_layer_desc& d, const AttnPlan& pl) {
     size_t at = kWsHeader;
-    scores = topk = idx = 0;
+    scores = topk = idx = hist = 0;
     if (d.kind == HSA_LAYER_C4) {
       scores = at;
       if (!d.scores) at += a256(static_cast<size_t>(d.pool_total_rows > 0 ? d.pool_total_rows : 1) * 4);
@@ -228,17 +243,16 @@ struct LayerWs {
       at += a256(topk_workspace_bytes(d.B, d.pool_total_rows, d.k));
       idx = at;
       if (!d.topk_idx) at += a256(static_cast<size_t>(d.B) * d.k * 4);
+      if (layer_fused(d)) {
+        hist = at;
+        at += a256(static_cast<size_t>(d.B) * kRowHistBins * sizeof(uint32_t));
+      }
     }
     attn = at;
     at += a256(attn_workspace_bytes(pl, d.B, d.Hq, d.Dv));
     total = at;
   }
 };
-
-AttnPlan layer_attn_plan(const hsa_layer_desc& d) {
-  const int64_t slots = d.kind == HSA_LAYER_C4 ? d.k : d.max_pool_rows;
-  return attn_plan(d.B, d.Hq, d.Dqk, d.Dv, d.W, slots);
-}
 
 }  // namespace
 
@@ -250,7 +264,8 @@ int layer_launch_count(const hsa_layer_desc& d) {
   const AttnPlan pl = layer_attn_plan(d);
   int n = 1 + 1 + (pl.S > 1 && !pl.cl ? 1 : 0);  // append, attention (+ combine)
   if (d.kind == HSA_LAYER_C4)
-    n += (d.pool_total_rows > 0 ? 1 : 0) + topk_launch_count(d.pool_total_rows, d.max_pool_rows);
+    n += (d.pool_total_rows > 0 ? 1 : 0) +
+         (layer_fused(d) ? 0 : topk_launch_count(d.pool_total_rows, d.max_pool_rows));
   return n;
 }
 
@@ -311,10 +326,50 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
     // output lengths after the append instead.
     const bool alias = d.seq_len_out == d.seq_len_in;
     const Spans sp_in{d.pool_offsets, d.seq_len_in, 1, r, d.pool_total_rows};
+    const bool fused = layer_fused(d);
+    uint32_t* hist = fused ? reinterpret_cast<uint32_t*>(w + L.hist) : nullptr;
     e = launch_indexer(d.iq, d.w, d.key_pool, alias ? sp : sp_in, d.B, d.Hi, d.Di,
-                       d.pool_total_rows, scores, status, stream, true, alias ? 0 : 2);
+                       d.pool_total_rows, scores, status, stream, true, alias ? 0 : 2, hist);
     if (e != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
+    if (fused) {
+      // the attention selects the top-k itself (its geometry from the input
+      // lengths + 1, as the top-k's would be)
+      if ((e = mark(3)) != cudaSuccess) return e;
+      AttnArgs a;
+      a.q = d.q;
+      a.swa = d.swa;
+      a.seq_len = alias ? d.seq_len_out : d.seq_len_in;
+      a.len_add = alias ? 0 : 1;
+      a.W = d.W;
+      a.extra = d.kv_pool;
+      a.sp = alias ? sp : sp_in;
+      a.idx = nullptr;
+      a.k = d.k;
+      a.max_rows = 0;
+      a.B = d.B;
+      a.Hq = d.Hq;
+      a.Dqk = d.Dqk;
+      a.Dv = d.Dv;
+      a.scale = d.scale;
+      a.out = d.out;
+      a.out_dtype = d.out_dtype;
+      a.lse = d.lse;
+      a.only_idx_pending = true;
+      a.sel_scores = scores;
+      a.row_hist = hist;
+      a.cand_ws = topk_cand_area(w + L.topk, d.B, d.pool_total_rows, d.k);
+      a.topk_out = d.topk_idx;
+      bool pdl = true;
+      if (d.q_ready_event) {
+        e = cudaStreamWaitEvent(stream, static_cast<cudaEvent_t>(d.q_ready_event), 0);
+        if (e != cudaSuccess) return e;
+        pdl = false;
+      }
+      e = launch_attn(a, pl, w + L.attn, status, stream, pdl);
+      if (e != cudaSuccess) return e;
+      return mark(4);
+    }
     e = launch_topk(scores, alias ? sp : sp_in, d.B, d.pool_total_rows, d.k, tidx, nullptr,
                     w + L.topk, status, stream, d.max_pool_rows, true);
     if (e != cudaSuccess) return e;

@@ -115,6 +115,25 @@ HSA_DEVINL void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_
       : "memory");
 }
 
+// An L2 cache policy that evicts the lines a load brings in first: for data
+// streamed once (a pool read end to end), so that it does not push out the
+// lines that are reused (outputs the next kernel reads, other small state).
+HSA_DEVINL uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// tma_load_2d with an L2 cache policy (e.g. l2_policy_evict_first()).
+HSA_DEVINL void tma_load_2d_hint(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 // Allocate `ncols` (power of two >= 32) TMEM columns; the address lands in

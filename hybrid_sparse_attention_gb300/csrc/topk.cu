@@ -36,6 +36,7 @@
 //      row's workspace zeroed.
 #include "common.cuh"
 #include "internal.h"
+#include "select_core.cuh"
 
 namespace hsa {
 namespace {
@@ -48,17 +49,6 @@ constexpr int kMaxK = 2048;       // final sort buffer
 constexpr int kSmemCand = 2560;   // boundary candidates staged in shared memory when they fit
 constexpr int kMinChunk = 4096;   // scores per CTA of the chunked passes, at least
 constexpr int kFastSort = kThreads;  // survivors ranked by warp runs + merge up to this many
-
-HSA_DEVINL uint32_t order_key(uint32_t u) {
-  if (u == 0x80000000u) u = 0u;  // -0.0 == +0.0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-HSA_DEVINL bool is_nan_bits(uint32_t u) { return (u & 0x7fffffffu) > 0x7f800000u; }
-
-HSA_DEVINL uint64_t composite(uint32_t key, uint32_t j) {
-  return (static_cast<uint64_t>(key) << 32) | static_cast<uint64_t>(0xffffffffu - j);
-}
 
 struct RowState {
   uint32_t n_cand;   // clustered path, heavy ties: candidates written to the workspace
@@ -113,50 +103,6 @@ struct ChunkPieces {
     return c > 0 ? c : 1;  // every row gets a CTA, even an empty one
   }
 };
-
-// Warp-aggregated append: lanes with `take` get consecutive slots of *counter.
-HSA_DEVINL uint32_t warp_append(uint32_t* counter, bool take, uint32_t active) {
-  const uint32_t mask = __ballot_sync(active, take);
-  if (!mask) return 0;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(mask) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(counter, __popc(mask));
-  base = __shfl_sync(active, base, leader);
-  return base + __popc(mask & ((1u << lane) - 1u));
-}
-
-// Finds digit d with (#above d) < need <= (#above d) + hist[d] among nb <=
-// 4 * blockDim.x bins of a shared histogram, scanned from the top; returns d
-// and *above.  All threads call; returns synchronised.
-HSA_DEVINL uint32_t find_digit(const uint32_t* hist, uint32_t nb, uint32_t need, uint32_t* above,
-                               uint32_t* s_scan, uint32_t* s_out) {
-  const uint32_t per = (nb + blockDim.x - 1) / blockDim.x;
-  const uint32_t first = threadIdx.x * per;  // bins counted from the top
-  uint32_t c[4], sum = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t bb = first + i;
-    c[i] = (static_cast<uint32_t>(i) < per && bb < nb) ? hist[nb - 1 - bb] : 0u;
-    sum += c[i];
-  }
-  uint32_t total;
-  uint32_t a = block_inclusive_sum<uint32_t>(sum, s_scan, &total) - sum;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t bb = first + i;
-    if (static_cast<uint32_t>(i) < per && bb < nb && a < need && a + c[i] >= need) {
-      s_out[0] = nb - 1 - bb;
-      s_out[1] = a;
-    }
-    a += c[i];
-  }
-  __syncthreads();
-  *above = s_out[1];
-  const uint32_t d = s_out[0];
-  __syncthreads();
-  return d;
-}
 
 // ---------------------------------------------------------------- pass 1
 
@@ -242,112 +188,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_hist_kernel(const float* __r
   if (threadIdx.x == 0) {
     ws.rows[row].digit = d;
     ws.rows[row].done1 = 0;
-  }
-}
-
-// ---------------------------------------------------------------- pass 2 helpers
-
-// Bitonic sort (descending) of n = power of two <= kMaxK composites in shared memory.
-HSA_DEVINL void bitonic_sort_desc(uint64_t* a, int n) {
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int t = threadIdx.x; t < n / 2; t += blockDim.x) {
-        const int lo = 2 * t - (t & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const uint64_t x = a[lo], y = a[hi];
-        if ((x < y) == desc) {
-          a[lo] = y;
-          a[hi] = x;
-        }
-      }
-    }
-  }
-  __syncthreads();
-}
-
-// Rank of this thread's composite among the (at most kThreads) composites
-// a[0..n) when sorted descending; x receives the composite (0, below every
-// real composite, for threads past n).  Each warp sorts its 32 composites by
-// a bitonic network in registers (shuffles only); the sorted runs go to
-// shared memory and each composite's rank is the number of larger
-// composites in every run, found by a branchless binary search per run.
-// Composites are unique, so the ranks of the n real ones are 0..n-1.
-HSA_DEVINL uint32_t rank_desc(const uint64_t* a, int n, uint64_t* s_run, uint64_t* x_out) {
-  const int t = threadIdx.x, lane = t & 31;
-  uint64_t x = t < n ? a[t] : 0ull;
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const uint64_t y = __shfl_xor_sync(0xffffffffu, x, stride);
-      const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
-      const uint64_t hi = x > y ? x : y, lo = x > y ? y : x;
-      x = (lower == desc) ? hi : lo;
-    }
-  }
-  s_run[t] = x;
-  __syncthreads();
-  uint32_t rank = 0;
-#pragma unroll
-  for (int s = 0; s < kWarps; ++s) {  // unrolled: the 16 searches overlap their load latencies
-    const uint64_t* r = s_run + 32 * s;
-    uint32_t c = 0;
-#pragma unroll
-    for (int st = 16; st >= 1; st >>= 1) c += r[c + st - 1] > x ? st : 0;
-    c += r[c] > x ? 1 : 0;
-    rank += c;
-  }
-  *x_out = x;
-  return rank;
-}
-
-// Appends to out[*count ...] the `need` largest of the composites cand[0..n)
-// that match prefix on mask and all agree above their low `low_bits` bits:
-// radix select with 11-bit digits from the top.  Composites are unique, so
-// the boundary is exact.
-HSA_DEVINL void select_rest(const uint64_t* cand, uint32_t n, uint32_t need, uint64_t* out,
-                            uint32_t* count, uint32_t cap, uint32_t* s_hist, uint32_t* s_scan,
-                            uint32_t* s_out, int low_bits, uint64_t prefix = 0, uint64_t mask = 0) {
-  // (composites not matching prefix on mask are not candidates and are skipped)
-  int rest = low_bits;
-  while (need > 0 && rest > 0) {
-    const int width = rest >= 11 ? 11 : rest;
-    rest -= width;
-    const int shift = rest;
-    const uint32_t nb = 1u << width;
-    for (uint32_t i = threadIdx.x; i < nb; i += blockDim.x) s_hist[i] = 0;
-    __syncthreads();
-    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint64_t x = cand[i];
-      if ((x & mask) == prefix)
-        atomicAdd(&s_hist[static_cast<uint32_t>(x >> shift) & (nb - 1)], 1u);
-    }
-    __syncthreads();
-    uint32_t above;
-    const uint32_t d = find_digit(s_hist, nb, need, &above, s_scan, s_out);
-    const uint32_t in = s_hist[d];
-    const bool take_bin = in == need - above;  // the whole bin fits
-    for (uint32_t i0 = 0; i0 < n; i0 += blockDim.x) {
-      const uint32_t i = i0 + threadIdx.x;
-      bool take = false;
-      uint64_t x = 0;
-      if (i < n) {
-        x = cand[i];
-        if ((x & mask) == prefix) {
-          const uint32_t dig = static_cast<uint32_t>(x >> shift) & (nb - 1);
-          take = dig > d || (take_bin && dig == d);
-        }
-      }
-      const uint32_t pos = warp_append(count, take, 0xffffffffu);
-      if (take && pos < cap) out[pos] = x;
-    }
-    __syncthreads();
-    if (take_bin) break;
-    need -= above;
-    prefix |= static_cast<uint64_t>(d) << shift;
-    mask |= static_cast<uint64_t>(nb - 1) << shift;
   }
 }
 
@@ -540,7 +380,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   float* out_v = vals_out ? vals_out + static_cast<int64_t>(row) * k : nullptr;
   if (have <= static_cast<uint32_t>(kFastSort)) {
     uint64_t x;
-    const uint32_t r = rank_desc(s_sel, static_cast<int>(have), s_cand, &x);
+    const uint32_t r = rank_desc<kWarps>(s_sel, static_cast<int>(have), s_cand, &x);
     if (r < have) {
       const uint32_t j = 0xffffffffu - static_cast<uint32_t>(x);
       out_i[r] = static_cast<int32_t>(j);
@@ -747,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
   float* out_v = vals_out ? vals_out + static_cast<int64_t>(row) * k : nullptr;
   if (have <= static_cast<uint32_t>(kFastSort)) {
     uint64_t x;
-    const uint32_t r = rank_desc(s_sel, static_cast<int>(have), s_cand, &x);
+    const uint32_t r = rank_desc<kWarps>(s_sel, static_cast<int>(have), s_cand, &x);
     if (r < have) {
       const uint32_t j = 0xffffffffu - static_cast<uint32_t>(x);
       out_i[r] = static_cast<int32_t>(j);
@@ -787,6 +627,10 @@ size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k) {
 
 size_t topk_zero_prefix_bytes(int64_t B, int64_t total_rows, int64_t k) {
   return WsLayout(B, total_rows, k).wcount;
+}
+
+uint64_t* topk_cand_area(void* ws, int64_t B, int64_t total_rows, int64_t k) {
+  return reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + WsLayout(B, total_rows, k).cand);
 }
 
 int64_t topk_chunk(int64_t total_rows) {
