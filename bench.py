@@ -476,15 +476,18 @@ def layer_outputs(g):
     return out, lse, seq_out, idx, scores
 
 
-def e2e_layer(g, out, lse, seq_out, idx, scores, flush, warmup, steps):
-    """The layer step through host buffers: the step's small inputs travel in
-    one host-to-device copy (one pinned staging buffer, each input at a
-    256-byte-aligned offset) and its outputs in one device-to-host copy; the
-    library reads and writes views of the device staging buffers.  q, read
-    only by the attention, is copied on a second stream inside the timed
+def e2e_layer(runs, flush, warmup, steps):
+    """The layer step through host buffers, over the given layer runs (step i
+    on run i mod len(runs); with several runs, inputs larger than L2 and no
+    flush, else the L2 flushed before each step): the step's small inputs
+    travel in one host-to-device copy (one pinned staging buffer, each input
+    at a 256-byte-aligned offset) and its outputs in one device-to-host copy;
+    the library reads and writes views of the device staging buffers.  q,
+    read only by the attention, is copied on a second stream inside the timed
     region and the layer waits for it right before the attention (the
     descriptor's q-ready event), so its upload overlaps the earlier kernels.
-    Returns (mean ms, h2d bytes, d2h bytes)."""
+    Returns (mean ms, h2d bytes, d2h bytes, host output of the last step of
+    run 0, that run's device output)."""
     import copy as _copy
 
     def packed(tensors):
@@ -495,32 +498,40 @@ def e2e_layer(g, out, lse, seq_out, idx, scores, flush, warmup, steps):
         return offs, at
 
     stream = torch.cuda.current_stream()
-    names_in = ("kv_new", "z_new") + (("ik_new", "iz_new", "iq", "w") if g.kind == 4 else ())
-    t_in = [getattr(g, k) for k in names_in]
-    offs_in, n_in = packed(t_in)
-    dev_in = torch.empty(n_in, dtype=torch.uint8, device="cuda")
-    host_in = torch.empty(n_in, dtype=torch.uint8).pin_memory()
-    g2 = _copy.copy(g)
-    for k, t, o in zip(names_in, t_in, offs_in):
-        nb = t.numel() * t.element_size()
-        host_in[o:o + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
-        setattr(g2, k, dev_in[o:o + nb].view(t.dtype).view(t.shape))
-    offs_out, n_out = packed([out, lse])
-    dev_out = torch.empty(n_out, dtype=torch.uint8, device="cuda")
-    out2 = dev_out[:out.numel() * 2].view(out.dtype).view(out.shape)
-    lse2 = dev_out[offs_out[1]:offs_out[1] + lse.numel() * 4].view(lse.dtype).view(lse.shape)
-    host_out = torch.empty(n_out, dtype=torch.uint8).pin_memory()
-    q_host = g.q.cpu().pin_memory()
-    g2.q = torch.empty_like(g.q)
     side = torch.cuda.Stream()
-    q_ready = torch.cuda.Event()
-    q_ready.record(side)                        # the event exists before its handle is taken
-    desc = _lib.layer_desc(g2, out2, lse2, seq_out, idx, scores, q_ready_event=q_ready.cuda_event)
-    ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
-    h2d, d2h = n_in + q_host.numel() * q_host.element_size(), n_out
+    staged = []
+    for r in runs:
+        g = r.g
+        names_in = ("kv_new", "z_new") + (("ik_new", "iz_new", "iq", "w") if g.kind == 4 else ())
+        t_in = [getattr(g, k) for k in names_in]
+        offs_in, n_in = packed(t_in)
+        dev_in = torch.empty(n_in, dtype=torch.uint8, device="cuda")
+        host_in = torch.empty(n_in, dtype=torch.uint8).pin_memory()
+        g2 = _copy.copy(g)
+        for k, t, o in zip(names_in, t_in, offs_in):
+            nb = t.numel() * t.element_size()
+            host_in[o:o + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
+            setattr(g2, k, dev_in[o:o + nb].view(t.dtype).view(t.shape))
+        offs_out, n_out = packed([r.out, r.lse])
+        dev_out = torch.empty(n_out, dtype=torch.uint8, device="cuda")
+        out2 = dev_out[:r.out.numel() * 2].view(r.out.dtype).view(r.out.shape)
+        lse2 = dev_out[offs_out[1]:offs_out[1] + r.lse.numel() * 4].view(r.lse.dtype).view(r.lse.shape)
+        host_out = torch.empty(n_out, dtype=torch.uint8).pin_memory()
+        q_host = g.q.cpu().pin_memory()
+        g2.q = torch.empty_like(g.q)
+        q_ready = torch.cuda.Event()
+        q_ready.record(side)                    # the event exists before its handle is taken
+        desc = _lib.layer_desc(g2, out2, lse2, r.seq_out, None, r.scores,
+                               q_ready_event=q_ready.cuda_event)
+        ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
+        staged.append((dev_in, host_in, dev_out, host_out, q_host, g2, q_ready, desc, ws,
+                       n_in + q_host.numel() * q_host.element_size(), n_out, out2))
     ts = []
     for i in range(warmup + steps):
-        flush(i)
+        dev_in, host_in, dev_out, host_out, q_host, g2, q_ready, desc, ws, h2d, d2h, _ = \
+            staged[i % len(staged)]
+        if len(staged) == 1:
+            flush(i)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -535,41 +546,78 @@ def e2e_layer(g, out, lse, seq_out, idx, scores, flush, warmup, steps):
         b.synchronize()
         if i >= warmup:
             ts.append(a.elapsed_time(b))
-    assert _lib.hsa_workspace_status(ws) == 0
-    return statistics.mean(ts), h2d, d2h, host_out[:out.numel() * 2].view(out.dtype).view(out.shape)
+    for st in staged:
+        assert _lib.hsa_workspace_status(st[8]) == 0
+    h2d, d2h = staged[0][9], staged[0][10]
+    host_o = staged[0][3][:runs[0].out.numel() * 2].view(runs[0].out.dtype).view(runs[0].out.shape)
+    return statistics.mean(ts), h2d, d2h, host_o, staged[0][11]
+
+
+NSTATES = 4
+
+
+class LayerRun:
+    """One layer state of the bench workload with its outputs, descriptors
+    (plain and with stage events) and workspace."""
+
+    def __init__(self, L, g, stage_events=None):
+        self.L, self.g = L, g
+        self.out, self.lse, self.seq_out, _, self.scores = layer_outputs(g)
+        # a decode loop needs the attention output, not the index list
+        self.desc = _lib.layer_desc(g, self.out, self.lse, self.seq_out, None, self.scores)
+        self.desc_stages = None
+        if stage_events is not None:
+            self.desc_stages = _lib.layer_desc(g, self.out, self.lse, self.seq_out, None,
+                                               self.scores, stage_events=stage_events)
+        self.ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(self.desc))
+        self.nbytes = layer_bytes(L, g.shape, g.kind)
+
+    def step(self, stages=False):
+        _lib.hsa_layer_decode(self.desc_stages if stages else self.desc, ws=self.ws)
+
+
+def layer_runs(rank, n=NSTATES, stage_events=None):
+    """n layer states of the bench workload (the rank's own first), each ~1.7
+    GB of pools and rings: together far larger than L2."""
+    runs = []
+    for j in range(n):
+        if j == 0:
+            L, g = build_workload(rank)
+        else:
+            seed = synth.SEED["c4layer"] + 1000 * rank + 7919 * j
+            L = synth.c4_lengths(seed, 64)
+            g = synth.filled_state(seed, 4, synth.FULL, L, device="cuda", name=f"layer{j}")
+        runs.append(LayerRun(L, g, stage_events))
+    return runs
 
 
 def measure_c4layer(args, rank, local, dist):
     """The headline: one C4 layer step of the bench workload (see the module
-    docstring), device-timed and end to end; on rank 0 also the other
-    configurations, the 60-layer CUDA graph and the oracle baseline."""
+    docstring), device-timed and end to end.  Step i works on layer state i
+    mod 4 (each larger than L2, 368 MB of algorithmic traffic per step), with
+    no L2 flush: like consecutive layers of a decode step, each step's data is
+    cold while the kernels' code and small state stay in L2.  The same step
+    with the L2 flushed before it (state 0 every time) is reported beside it.
+    On rank 0 also the other configurations, the 60-layer CUDA graph and the
+    oracle baseline."""
     _lib.load(build_if_missing=True)
-    shape = synth.FULL
-    L, g = build_workload(rank)
     stream = torch.cuda.current_stream()
-    out, lse, seq_out, idx, scores = layer_outputs(g)
-    idx = None   # a decode loop needs the attention output, not the index list
     stage = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     for e in stage:
         e.record(stream)          # the events exist from here on
     # the timed steps run without stage events: an event recorded between two
     # kernels stops the next one from being scheduled while the previous runs
-    desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores)
-    desc_stages = _lib.layer_desc(g, out, lse, seq_out, idx, scores,
-                                  stage_events=[e.cuda_event for e in stage])
-    ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
-    launches = _lib.hsa_layer_decode_launches(desc)
+    runs = layer_runs(rank, stage_events=[e.cuda_event for e in stage])
+    launches = _lib.hsa_layer_decode_launches(runs[0].desc)
     flush = L2Flush()
-    nbytes = layer_bytes(L, shape)
+    total_bytes = statistics.mean(r.nbytes["total"] for r in runs)
+    nbytes = {k: statistics.mean(r.nbytes[k] for r in runs) for k in runs[0].nbytes}
 
-    def step(d=desc):
-        _lib.hsa_layer_decode(d, ws=ws)
-
-    for i in range(args.warmup):
-        flush(i)
-        step()
+    for i in range(max(args.warmup, NSTATES)):
+        runs[i % NSTATES].step()
     torch.cuda.synchronize()
-    assert _lib.hsa_workspace_status(ws) == 0
+    for r in runs:
+        assert _lib.hsa_workspace_status(r.ws) == 0
 
     # ------------------------------------------------ device-timed region
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -579,71 +627,78 @@ def measure_c4layer(args, rank, local, dist):
     with ClockSampler(local) as clocks:
         wall0 = time.perf_counter()
         for i in range(args.steps):
-            flush(i)                            # evict the previous step's data from L2
             ev0[i].record(stream)
-            step()
+            runs[i % NSTATES].step()
             ev1[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     barrier(dist)
     ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev0, ev1))
-    # per-kernel durations: the same steps again with an event between kernels
+    # the same step with the L2 flushed before it (state 0)
+    ms_flushed = statistics.mean(timed(lambda: runs[0].step(), flush, 2, args.steps, stream))
+    # per-kernel durations: the same rotation with an event between kernels
     stage_ms = []
     for i in range(args.steps):
-        flush(i)
-        step(desc_stages)
+        runs[i % NSTATES].step(stages=True)
         stage[4].synchronize()                  # stage events are reused: read them now
         stage_ms.append([stage[j].elapsed_time(stage[j + 1]) for j in range(4)])
     stage_mean = np.array(stage_ms).mean(axis=0)  # append, indexer, top-k, attention (ms)
-    assert _lib.hsa_workspace_status(ws) == 0
+    for r in runs:
+        assert _lib.hsa_workspace_status(r.ws) == 0
 
-    e2e_ms, h2d, d2h, host_o = e2e_layer(g, out, lse, seq_out, idx, scores, flush, args.warmup,
-                                         args.steps)
-    step()
+    e2e_ms, h2d, d2h, host_o, dev_o = e2e_layer(runs, flush, args.warmup, args.steps)
     torch.cuda.synchronize()
-    assert torch.equal(host_o, out.cpu())
+    runs[0].step()
+    torch.cuda.synchronize()
+    assert torch.equal(host_o, runs[0].out.cpu())
 
     extra = {}
     if rank == 0 and not args.no_extra:
         if args.layers > 0:
-            extra["multi_layer_graph"] = multi_layer_graph(args, flush)
+            extra["multi_layer_graph"] = multi_layer_graph(args, flush, runs)
         extra["topk_rows_per_s"] = bench_topk(flush, args)
         extra["compress"] = bench_compress(flush, args)
         extra["longctx"] = bench_longctx(flush, args)
     cpu = None
     if rank == 0 and args.cpu_budget > 0:
-        run, threads, busy = oracle_layer_runner(g)
+        run, threads, busy = oracle_layer_runner(runs[0].g)
         sec, calls = time_oracle(run, args.cpu_budget)
         cpu = {"value": sec * 1e6, "unit": "us", "cores": threads, "kind": "oracle",
-               "sample": f"the whole 64-sequence layer step, {calls} calls "
+               "sample": f"the whole 64-sequence layer step (state 0), {calls} calls "
                          f"(~{args.cpu_budget:.0f} s budget), mean",
                "threads_busy_by_stage": busy}
 
     peak, peak_kind = measured_peaks()
     idx_ms = float(stage_mean[1])
     achieved = nbytes["indexer"] / (idx_ms * 1e-3) / 1e9
-    layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
+    layer_gbs = total_bytes / (ms * 1e-3) / 1e9
     line = base_line(args, 1, METRIC, "us", False, WORKLOAD, ms * 1000)
-    line["config"].update({"l2": L2_NOTE, "sum_c4_entries": int((L // 4).sum()),
-                           "seed": synth.SEED["c4layer"],
-                           "outputs": "attention output and log-sum-exp (the top-k index list "
-                                      "is not requested)"})
+    line["config"].update({
+        "l2": f"inputs larger than L2: step i on layer state i mod {NSTATES} (each ~1.7 GB, "
+              f"{total_bytes / 1e6:.0f} MB of algorithmic traffic per step), no flush; "
+              f"l2_flushed_us: the same step on state 0 after {L2_NOTE}",
+        "sum_c4_entries": int((runs[0].L // 4).sum()), "seed": synth.SEED["c4layer"],
+        "states": NSTATES,
+        "outputs": "attention output and log-sum-exp (the top-k index list is not requested)"})
     line.update({
+        "l2_flushed_us": ms_flushed * 1000,
         "roofline": {"bound": "hbm", "kernel": "indexer_kernel (tcgen05 scores)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
                      "traffic": indexer_traffic(), "algorithmic_bytes": nbytes["indexer"],
                      "launch_us": idx_ms * 1000},
-        "layer_roofline": {"algorithmic_bytes": nbytes["total"], "achieved_gbs": layer_gbs,
+        "layer_roofline": {"algorithmic_bytes": total_bytes, "achieved_gbs": layer_gbs,
                            "frac": layer_gbs / peak},
         "stage_rooflines": {
             name: {"algorithmic_bytes": nbytes[key], "stage_us": stage_mean[j] * 1000,
                    "achieved_gbs": nbytes[key] / (stage_mean[j] * 1e-3) / 1e9,
                    "frac": nbytes[key] / (stage_mean[j] * 1e-3) / 1e9 / peak}
-            for name, key, j in (("indexer", "indexer", 1), ("topk", "topk", 2),
-                                 ("attention (+ split merge)", "attention", 3))},
+            for name, key, j in (("indexer", "indexer", 1),
+                                 ("selection + attention (+ split merge)", "attention", 3))},
         "stage_us": {"append_compress": stage_mean[0] * 1000, "indexer": stage_mean[1] * 1000,
-                     "topk": stage_mean[2] * 1000, "attention": stage_mean[3] * 1000},
+                     "topk (own kernels only; fused into the attention otherwise)":
+                         stage_mean[2] * 1000,
+                     "attention": stage_mean[3] * 1000},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_ms * 1000, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -652,7 +707,7 @@ def measure_c4layer(args, rank, local, dist):
         "wall_s_timed": wall,
     })
     line.update(extra)
-    B = L.numel()
+    B = runs[0].L.numel()
     return {"ms": ms, "e2e_ms": e2e_ms, "line": line, "units_per_step": 1,
             "tokens_per_step": B, "throughput_unit": "decode tokens/s through one layer"}
 
@@ -671,28 +726,16 @@ def run_profile(ctx=None):
     print(json.dumps({"profile": "ok", "sum_c4_entries": int((L // 4).sum())}))
 
 
-def multi_layer_graph(args, flush, nstates=4, iters=10):
+def multi_layer_graph(args, flush, runs, iters=10):
     """A decode step over `args.layers` C4 layers (the bench's shapes; layer i
-    works on state i mod nstates, each larger than L2) captured once in a CUDA
-    graph: us per layer of the replayed step, next to the same layers launched
-    one call at a time."""
-    states = []
-    for j in range(nstates):
-        if j == 0:
-            L, g = build_workload(0)
-        else:
-            seed = synth.SEED["c4layer"] + 7919 * j
-            L = synth.c4_lengths(seed, 64)
-            g = synth.filled_state(seed, 4, synth.FULL, L, device="cuda", name=f"layer{j}")
-        out, lse, seq_out, idx, scores = layer_outputs(g)
-        desc = _lib.layer_desc(g, out, lse, seq_out, None, scores)
-        ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
-        states.append((g, desc, ws, out, lse, idx, scores))
-    descs = [states[i % nstates] for i in range(args.layers)]
+    works on state i mod len(runs), each larger than L2) captured once in a
+    CUDA graph: us per layer of the replayed step, next to the same layers
+    launched one call at a time; the L2 is flushed before each step."""
+    descs = [runs[i % len(runs)] for i in range(args.layers)]
 
     def eager():
-        for _, desc, ws, *_ in descs:
-            _lib.hsa_layer_decode(desc, ws=ws)
+        for r in descs:
+            r.step()
 
     for _ in range(3):
         eager()
@@ -716,15 +759,15 @@ def multi_layer_graph(args, flush, nstates=4, iters=10):
             b.synchronize()
             if i >= 3:
                 times[mode].append(a.elapsed_time(b))
-    for _, _, ws, *_ in states:
-        assert _lib.hsa_workspace_status(ws) == 0
+    for r in runs:
+        assert _lib.hsa_workspace_status(r.ws) == 0
     per = {m: statistics.mean(v) * 1000 / args.layers for m, v in times.items()}
-    del graph, states, descs
+    del graph
     torch.cuda.empty_cache()
-    return {"layers": args.layers, "states": nstates, "us_per_layer_graph": per["graph"],
+    return {"layers": args.layers, "states": len(runs), "us_per_layer_graph": per["graph"],
             "us_per_layer_eager": per["eager"],
-            "note": "C4 layers of the bench workload, layer i on state i mod 4; L2 flushed "
-                    "before each step, not between layers"}
+            "note": f"C4 layers of the bench workload, layer i on state i mod {len(runs)}; L2 "
+                    "flushed before each step, not between layers"}
 
 
 # ----------------------------------------------------------------------------- other configurations
@@ -965,7 +1008,8 @@ def bench_layer_state(L, g, flush, warmup, steps, cpu_budget, clocks=None, dist=
     ent = {"us": ms * 1000, "algorithmic_bytes": nb["total"], "achieved_gbs": gbs,
            "frac": gbs / peak, "launches": _lib.hsa_layer_decode_launches(desc),
            "e2e": None}
-    e2e_ms, h2d, d2h, _ = e2e_layer(g, out, lse, seq_out, idx, scores, flush, warmup, steps)
+    run = LayerRun(L, g)
+    e2e_ms, h2d, d2h, _, _ = e2e_layer([run], flush, warmup, steps)
     ent["e2e"] = {"value": e2e_ms * 1000, "unit": "us", "h2d_bytes_per_step": h2d,
                   "d2h_bytes_per_step": d2h}
     if cpu_budget > 0:

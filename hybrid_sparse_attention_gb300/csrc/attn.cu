@@ -237,6 +237,7 @@ struct Shared {
   uint16_t sel[kMaxTC * kKeys];
   uint32_t sel_n;
   uint64_t sel_full;
+  uint64_t sel_cp;  // the selecting split's copy of its row's scores landed
 };
 static_assert(kKeys * kMaxTC >= 512, "a split's share of a fused selection (k <= 512) fits");
 
@@ -356,8 +357,14 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
   const int head = static_cast<int>(
       min(static_cast<uintptr_t>(n), ((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) >> 2));
   const int nv = (n - head) >> 2, body = 4 * nv;
+  if (t == 0 && nv > 0) {  // the body: bulk copies (32 KB each) completing on sel_cp
+    const uint32_t bytes = 16u * static_cast<uint32_t>(nv);
+    tc::mbar_arrive_expect_tx(&sh.sel_cp, bytes);
 #pragma unroll 1
-  for (int v = t; v < nv; v += kThreads) tc::cp_async16(s_row + 4 * v, row + head + 4 * v, 16u);
+    for (uint32_t o = 0; o < bytes; o += 32768u)
+      tc::bulk_load(reinterpret_cast<uint8_t*>(s_row) + o, reinterpret_cast<const uint8_t*>(row + head) + o,
+                    bytes - o < 32768u ? bytes - o : 32768u, &sh.sel_cp);
+  }
 #pragma unroll 1
   for (int j = t; j < n - body; j += kThreads) cp_async4(s_row + body + j, row + (j < head ? j : body + j));
   tc::cp_async_commit();
@@ -402,6 +409,7 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
 #pragma unroll
   for (int i = 0; i < kPer / 4; ++i) gh[i] = make_uint4(0u, 0u, 0u, 0u);
   tc::cp_async_wait<0>();
+  if (nv > 0) tc::mbar_wait(&sh.sel_cp, 0, p.status);
   __syncthreads();
   // (3) winners (above bin d; every score when all) and candidates (in bin d).
   // One pass classifies every score and keeps, per thread, masks of its
@@ -597,15 +605,22 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
   if (own) {
     tc::fence_after_sync();
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    // two units per round: both TMEM loads in flight before one wait
 #pragma unroll 1
-    for (int u = hw; u < U; u += 2) {
-      uint32_t a[16];
+    for (int u = hw; u < U; u += 4) {
+      uint32_t a[16], c[16];
+      const bool two = u + 2 < U;
       tc::tmem_ld16(lane_addr + (TC + u / kQ) * kN + (u % kQ) * 16, a);
+      const int u2 = two ? u + 2 : u;
+      tc::tmem_ld16(lane_addr + (TC + u2 / kQ) * kN + (u2 % kQ) * 16, c);
       tc::tmem_ld_wait();
       uint4* d = reinterpret_cast<uint4*>(ring + u * kUnitBytes + row * 16);
+      uint4* d2 = reinterpret_cast<uint4*>(ring + u2 * kUnitBytes + row * 16);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
+      for (int c4 = 0; c4 < 4; ++c4) {
         d[c4 * kKeys] = make_uint4(a[4 * c4], a[4 * c4 + 1], a[4 * c4 + 2], a[4 * c4 + 3]);
+        d2[c4 * kKeys] = make_uint4(c[4 * c4], c[4 * c4 + 1], c[4 * c4 + 2], c[4 * c4 + 3]);
+      }
     }
   }
   if (tid < kN) {
@@ -642,18 +657,27 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
     float o[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) o[e] = 0.f;
-#pragma unroll 1
-    for (int r = 0; r < S; ++r) {
-      if (!sh.xok[r]) continue;
-      const uint32_t src = map_rank(ring + u * kUnitBytes + row * 16, r);
+    // every split's part of the unit: all loads in flight at once (a split
+    // without a partial, or past S, contributes weight 0 and is not read)
+    float4 v[kMaxCl][4];
+#pragma unroll
+    for (int r = 0; r < kMaxCl; ++r) {
+      const bool use = r < S && sh.xok[r];
+      const uint32_t src = map_rank(ring + u * kUnitBytes + row * 16, use ? r : rank);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4)
+        v[r][c4] = use ? ld_cluster_f32x4(src + c4 * (kKeys * 16u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < kMaxCl; ++r) {
+      if (!(r < S && sh.xok[r])) continue;
       const float* w = &sh.red[r][q16 * 16];
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        const float4 v = ld_cluster_f32x4(src + c4 * (kKeys * 16u));
-        o[4 * c4] = fmaf(v.x, w[4 * c4], o[4 * c4]);
-        o[4 * c4 + 1] = fmaf(v.y, w[4 * c4 + 1], o[4 * c4 + 1]);
-        o[4 * c4 + 2] = fmaf(v.z, w[4 * c4 + 2], o[4 * c4 + 2]);
-        o[4 * c4 + 3] = fmaf(v.w, w[4 * c4 + 3], o[4 * c4 + 3]);
+        o[4 * c4] = fmaf(v[r][c4].x, w[4 * c4], o[4 * c4]);
+        o[4 * c4 + 1] = fmaf(v[r][c4].y, w[4 * c4 + 1], o[4 * c4 + 1]);
+        o[4 * c4 + 2] = fmaf(v[r][c4].z, w[4 * c4 + 2], o[4 * c4 + 2]);
+        o[4 * c4 + 3] = fmaf(v[r][c4].w, w[4 * c4 + 3], o[4 * c4 + 3]);
       }
     }
     // transpose through shared memory: lane l holds channel l of 16 heads; the
@@ -689,9 +713,22 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
   cluster_sync();  // no split leaves while another may still read its ring
 }
 
+// Q of token b, head group g into the Q region by TMA: NSL boxes of 64
+// channels x kN heads (128-byte swizzled, the layout the S^T MMA reads), one
+// issuing thread, completing on q_full.  Heads past the group's (kN > HG)
+// load the next rows of q, which no output reads (zeros past the tensor).
+template <int kN>
+HSA_DEVINL void issue_q_tma(const CUtensorMap* qmap, Shared& sh, uint8_t* qs, int NSL, int row0) {
+  tc::mbar_arrive_expect_tx(&sh.q_full, static_cast<uint32_t>(NSL) * kN * 128);
+#pragma unroll 1
+  for (int j = 0; j < NSL; ++j) tc::tma_load_2d(qs + j * (kN * 128), qmap, j * 64, row0, &sh.q_full);
+}
+
 // kSel: the fused selection of the layer's C4 path (see select_token).
 template <int kN, bool kSel>
-__global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
+__global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ CUtensorMap qmap,
+                                                          const __grid_constant__ CUtensorMap swamap,
+                                                          int swa_tma, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   // Programmatic dependent launch.  When the previous kernel is the top-k
@@ -769,9 +806,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       tc::mbar_init(&sh.p_full[i], kKeys);
       tc::mbar_init(&sh.o_done[i], 1);
     }
-    tc::mbar_init(&sh.q_full, kProdThreads);
+    tc::mbar_init(&sh.q_full, 1);
     tc::mbar_init(&sh.fin, 1);
-    if (kSel) tc::mbar_init(&sh.sel_full, 1);
+    if (kSel) {
+      tc::mbar_init(&sh.sel_full, 1);
+      tc::mbar_init(&sh.sel_cp, 1);
+    }
     sh.abort = 0;
     tc::fence_mbar_init();
   }
@@ -804,17 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     if (selector) {
       // Q first (the previous kernel does not write it), then the selection,
       // which needs the indexer's scores and histogram
-      if (warp >= kProdWarp0) {
-        const int pt_ = tid - kProdWarp0 * 32, nq = kN * NSL * 8;
-        for (int i = pt_; i < nq; i += kProdThreads) {
-          const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, cc = rem & 7;
-          const bool v = h < p.HG;
-          const uint16_t* src =
-              v ? p.q + (static_cast<int64_t>(b) * p.Hq + g * p.HG + h) * p.Dqk + j * 64 + cc * 8 : p.q;
-          tc::cp_async16(qs + j * (kN * 128) + sw128(h, cc), src, v ? 16u : 0u);
-        }
-        tc::cp_async_commit();
-      }
+      if (tid == kProdWarp0 * 32) issue_q_tma<kN>(&qmap, sh, qs, NSL, b * p.Hq + g * p.HG);
       pdl_wait();
       int n = static_cast<int>(geo.nb);
       // an invalid span (bad offsets or a live count above the capacity), or a
@@ -839,13 +869,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
     // ------------------------------------------------------------ gatherers
     // Gather warp w issues ring items w, w + 3, w + 6, ... (slot item % kRing)
     // and keeps up to two of them in flight: its cp.async groups retire in
-    // order, each signalling its slot (or, for a chunk's Q group, q_full).
+    // order, each signalling its slot.  Q arrives by TMA on q_full.
     constexpr int kProdWarps = kProdThreads / 32;
     const int pt_ = tid - kProdWarp0 * 32, pw = warp - kProdWarp0;
     bool ok = true;
-    int64_t pend0 = 0, pend1 = 0;  // this warp's unsignalled groups, oldest first (-1: Q)
+    int64_t pend0 = 0, pend1 = 0;  // this warp's unsignalled groups, oldest first
     int np = 0;
-    auto signal = [&](int64_t it) { tc::mbar_arrive(it < 0 ? &sh.q_full : &sh.full[it % kRing]); };
+    auto signal = [&](int64_t it) { tc::mbar_arrive(&sh.full[it % kRing]); };
     auto retire_all = [&]() {  // signal each pending group as soon as it has landed
       if (np == 2) {
         tc::cp_async_wait<1>();
@@ -873,22 +903,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
       ++np;
     };
     bool q_pre = selector;  // the selecting split issued chunk 0's Q before selecting
-    auto issue_q = [&]() {  // Q (every gather thread), one cp.async group
+    auto issue_q = [&]() {  // Q by TMA, one thread
       if (q_pre) {
         q_pre = false;
-        push(-1);
         return;
       }
-      const int nq = kN * NSL * 8;
-      for (int i = pt_; i < nq; i += kProdThreads) {
-        const int h = i / (NSL * 8), rem = i - h * NSL * 8, j = rem >> 3, cc = rem & 7;
-        const bool v = h < p.HG;
-        const uint16_t* src =
-            v ? p.q + (static_cast<int64_t>(b) * p.Hq + g * p.HG + h) * p.Dqk + j * 64 + cc * 8 : p.q;
-        tc::cp_async16(qs + j * qslice + sw128(h, cc), src, v ? 16u : 0u);
-      }
-      tc::cp_async_commit();
-      push(-1);
+      if (pt_ == 0) issue_q_tma<kN>(&qmap, sh, qs, NSL, b * p.Hq + g * p.HG);
     };
     int64_t item = 0;
     for (int c = 0; c < nchunks; ++c) {
@@ -958,6 +978,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
           const uint16_t* rp[kKeys / 4];
 #pragma unroll
           for (int k = 0; k < kKeys / 4; ++k) rp[k] = table[(lane >> 3) + 4 * k];
+          // A full window tile (the token's 128 ring rows, every one a window
+          // row) arrives by TMA: the ring's rows in slot order, 64-channel
+          // boxes, 128-byte swizzled as the MMA reads them.
+          const bool win_tma = swa_tma && tb + tc_ == 0 && geo.n_swa == kKeys && a0 == 0;
           for (int it = 0; it < nit; ++it, ++item) {
             if (!ok || item % kProdWarps != pw) continue;
             const int slot = static_cast<int>(item % kRing);
@@ -968,6 +992,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(AttnParams p) {
                 ok = __all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty[slot], par, p.status));
                 if (!ok) continue;
               }
+            }
+            if (win_tma) {
+              // lane 0 arms the slot with the bytes and issues both slices; the
+              // other lanes arrive (the slot's barrier counts 32 arrivals)
+              const int j0 = 2 * it;
+              const bool two = j0 + 1 < NSL;
+              if (lane == 0) {
+                tc::mbar_arrive_expect_tx(&sh.full[slot], (two ? 2u : 1u) * kSliceBytes);
+                tc::tma_load_2d(ring + slot * kPairBytes, &swamap, j0 * 64, b * p.W, &sh.full[slot]);
+                if (two)
+                  tc::tma_load_2d(ring + slot * kPairBytes + kSliceBytes, &swamap, (j0 + 1) * 64,
+                                  b * p.W, &sh.full[slot]);
+              } else {
+                tc::mbar_arrive(&sh.full[slot]);
+              }
+              continue;
             }
             // Masked rows are not copied (no memory request): the slot keeps finite
             // data (zeroed at start, or rows of this token gathered earlier) that
@@ -1458,15 +1498,25 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.plse = reinterpret_cast<float*>(
       w + ((static_cast<size_t>(a.B) * pl.S * a.Hq * a.Dv * 4 + 255) & ~size_t(255)));
   const unsigned grid = static_cast<unsigned>(a.B * pl.G * pl.S);
+  CUtensorMap qmap, swamap;
+  cudaError_t e = make_tmap_2d_bf16(&qmap, a.q, a.Dqk, a.B * a.Hq, 64, pl.N, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  // full 128-row windows are loaded by TMA (a map over the ring's rows)
+  const int swa_tma = a.swa && a.W == kKeys ? 1 : 0;
+  swamap = qmap;  // (unused unless swa_tma)
+  if (swa_tma) {
+    e = make_tmap_2d_bf16(&swamap, a.swa, a.Dqk, a.B * a.W, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+  }
   auto* kernel = fused ? (pl.N == 16 ? attn_kernel<16, true>
                                      : (pl.N == 32 ? attn_kernel<32, true> : attn_kernel<64, true>))
                        : (pl.N == 16 ? attn_kernel<16, false>
                                      : (pl.N == 32 ? attn_kernel<32, false> : attn_kernel<64, false>));
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(pl.smem));
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(pl.smem));
   if (e != cudaSuccess) return e;
   e = launch_kc(kernel, dim3(grid), dim3(kThreads), pl.smem, stream, pdl,
-                static_cast<unsigned>(pl.cl ? pl.S : 0), p);
+                static_cast<unsigned>(pl.cl ? pl.S : 0), qmap, swamap, swa_tma, p);
   if (e != cudaSuccess || pl.S == 1 || pl.cl) return e;
   const int64_t bh = a.B * a.Hq;
   const int64_t threads = bh * (a.Dv / 8);  // two 16-byte groups each
