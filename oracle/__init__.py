@@ -62,9 +62,15 @@ def _load():
             lib.oracle_decode_attn.argtypes = [P, P, P, I64, P, P, P, I64, I64, I64, I64, I64,
                                                ctypes.c_double, P, P, ctypes.c_int]
             lib.oracle_float_to_bf16.argtypes = [P, I64, P]
+            lib.oracle_e4m3_to_double.argtypes = [P, I64, P]
+            lib.oracle_float_to_e4m3.argtypes = [P, I64, P]
+            lib.oracle_quantize_e4m3.argtypes = [P, I64, I64, P, P, ctypes.c_int]
+            lib.oracle_indexer_scores_e4m3.argtypes = [P, P, P, P, P, I64, I64, I64, P,
+                                                       ctypes.c_int]
             lib.oracle_bf16_to_double.argtypes = [P, I64, P]
             for f in ("oracle_compress", "oracle_indexer_scores", "oracle_topk",
-                      "oracle_decode_attn"):
+                      "oracle_decode_attn", "oracle_quantize_e4m3",
+                      "oracle_indexer_scores_e4m3"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -99,6 +105,60 @@ def bf16_to_double(x) -> np.ndarray:
     x = _c(x, np.uint16)
     out = np.empty(x.shape, np.float64)
     _load().oracle_bf16_to_double(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def e4m3_to_double(codes) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) -> their values (the format definition; NaN for s.1111.111)."""
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    _load().oracle_e4m3_to_double(_ptr(codes), codes.size, _ptr(out))
+    return out
+
+
+def float_to_e4m3(x) -> np.ndarray:
+    """binary32 -> E4M3 codes: nearest, ties to the even code, saturating at +-448."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _load().oracle_float_to_e4m3(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def quantize_e4m3(x, threads: int = 1):
+    """Per-row E4M3 quantization: (codes uint8 [rows, C], scales float32 [rows]).
+
+    scale = amax / 448 and code = e4m3(x * (448 / amax)), each step in binary32;
+    a zero row gets scale 0.  The library's FP8 storage of the indexer-key pool.
+    """
+    x = _c(x, np.float32)
+    rows, C = x.shape
+    codes = np.empty((rows, C), np.uint8)
+    scales = np.empty(rows, np.float32)
+    _check(_load().oracle_quantize_e4m3(_ptr(x), rows, C, _ptr(codes), _ptr(scales), threads),
+           "quantize_e4m3")
+    return codes, scales
+
+
+def dequantize_e4m3(codes, scales) -> np.ndarray:
+    """scale[j] * value(code[j, d]) in float64."""
+    return e4m3_to_double(codes) * np.asarray(scales, np.float64)[:, None]
+
+
+def indexer_scores_e4m3(iq, w, keys, kscale, offsets, threads: int = 1) -> np.ndarray:
+    """Indexer scores over an E4M3 key pool: the score formula on the dequantized
+    keys and on the query rows quantized the same way (per (b, h) row).
+
+    iq: uint16 [B, Hi, Di]; w: float32 [B, Hi]; keys: uint8 [sum N, Di];
+    kscale: float32 [sum N]; offsets: int64 [B+1].  Returns float64 [sum N].
+    """
+    iq, w, keys, kscale, offsets = (_c(iq, np.uint16), _c(w, np.float32), _c(keys, np.uint8),
+                                    _c(kscale, np.float32), _c(offsets, np.int64))
+    B, Hi, Di = iq.shape
+    assert keys.ndim == 2 and keys.shape[1] == Di and kscale.shape == (keys.shape[0],)
+    out = np.empty(keys.shape[0], np.float64)
+    _check(_load().oracle_indexer_scores_e4m3(_ptr(iq), _ptr(w), _ptr(keys), _ptr(kscale),
+                                              _ptr(offsets), B, Hi, Di, _ptr(out), threads),
+           "indexer_scores_e4m3")
     return out
 
 
@@ -195,7 +255,9 @@ def layer_decode(st: dict, threads: int = 1) -> dict:
       a1 append the new token's rows into the SWA ring (slot (L-1) mod W) and the
          in-flight block rings (slot (L-1) mod r), L = seq_len_in + 1;
       a2 if L mod r == 0, compress the completed block into pool row L/r - 1
-         (compressor output rounded fp64 -> fp32 -> bf16, as stored);
+         (compressor output rounded fp64 -> fp32 -> bf16, as stored; with an
+         E4M3 key pool (``st["key_fp8"]``) the indexer key is rounded to fp32
+         and quantized per row into ``key_pool`` codes and ``key_scale``);
       a3 (C4) indexer scores over the sequence's L/4 entries, rounded to fp32;
       a4 (C4) top-k of those scores;
       a5 attention over the SWA window and the selected (C4) or all (C128) rows.
@@ -226,13 +288,23 @@ def layer_decode(st: dict, threads: int = 1) -> dict:
         st["kv_pool"][offs[b] + n] = float_to_bf16(c.astype(np.float32)).reshape(-1)
         if kind == C4:
             ck = compress(st["ik_ring"][b:b + 1], st["iz_ring"][b:b + 1], st["b_ik"], r, threads)
-            st["key_pool"][offs[b] + n] = float_to_bf16(ck.astype(np.float32)).reshape(-1)
+            if st.get("key_fp8"):
+                codes, sc = quantize_e4m3(ck.astype(np.float32).reshape(1, -1))
+                st["key_pool"][offs[b] + n] = codes[0]
+                st["key_scale"][offs[b] + n] = sc[0]
+            else:
+                st["key_pool"][offs[b] + n] = float_to_bf16(ck.astype(np.float32)).reshape(-1)
     counts = L // r
     kv_rows, kv_offs = compact(st["kv_pool"], offs, counts)
     idx = None
     if kind == C4:
         key_rows, key_offs = compact(st["key_pool"], offs, counts)
-        s64 = indexer_scores(st["iq"], st["w"], key_rows, key_offs, threads)
+        if st.get("key_fp8"):
+            ksc, _ = compact(st["key_scale"].reshape(-1, 1), offs, counts)
+            s64 = indexer_scores_e4m3(st["iq"], st["w"], key_rows, ksc.reshape(-1), key_offs,
+                                      threads)
+        else:
+            s64 = indexer_scores(st["iq"], st["w"], key_rows, key_offs, threads)
         s32 = s64.astype(np.float32)
         idx, vals = topk(s32, key_offs, st["k"], threads)
         out.update(scores64=s64, scores=s32, score_offsets=key_offs, idx=idx, vals=vals)

@@ -28,6 +28,12 @@
 //                          nth_element cross-check, all-equal / reversed rows
 //   oracle_decode_attn     hand-worked example, single row, equal logits,
 //                          split + log-sum-exp recombination, dense equivalence
+//   oracle_e4m3_to_double  every code against torch's float8_e4m3fn decoding,
+//                          the format's named values
+//   oracle_quantize_e4m3   encodings against torch's float8_e4m3fn rounding,
+//                          saturation, amax -> 448, zero rows, error bound
+//   oracle_indexer_scores_e4m3  hand-worked example, numpy float64 brute force
+//                          on the dequantized operands, one-hot keys
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -58,6 +64,68 @@ uint16_t float_to_bf16_rne(float f) {
   uint32_t kept = u >> 16;
   if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u))) kept += 1;
   return static_cast<uint16_t>(kept);
+}
+
+// FP8 E4M3 (the 8-bit "e4m3fn" interchange format): a sign bit, 4 exponent
+// bits with bias 7 and 3 mantissa bits; exponent field 0 holds the subnormals
+// m * 2^-9; the pattern s.1111.111 is NaN and there is no infinity, so the
+// largest finite magnitude is 1.75 * 2^8 = 448.  The library's reading of the
+// pages' FP8 KV storage ([LH] §Hỗ trợ Học tăng cường: FP8 rollout; [WK]
+// 新架构: a 1M-token KV cache under 10 GB) for the indexer-key pool.
+double e4m3_to_double(uint8_t c) {
+  const int e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+  const double v = e == 0 ? std::ldexp(static_cast<double>(m), -9)
+                          : std::ldexp(1.0 + m / 8.0, e - 7);
+  return (c & 0x80) ? -v : v;
+}
+
+// binary32 -> E4M3: the nearest finite code (the even code on a tie), finite
+// magnitudes beyond 448 saturating to 448 and infinities too; NaN -> 0x7f.
+// The non-negative finite codes 0x00..0x7e are increasing in value, so the
+// nearest is one of the two neighbours a binary search finds.
+uint8_t float_to_e4m3_sat(float f) {
+  if (std::isnan(f)) return 0x7f;
+  static const std::vector<double> values = [] {
+    std::vector<double> v(0x7f);
+    for (int c = 0; c < 0x7f; ++c) v[c] = e4m3_to_double(static_cast<uint8_t>(c));
+    return v;
+  }();
+  const double a = std::fabs(static_cast<double>(f));
+  const uint8_t sign = std::signbit(f) ? 0x80 : 0x00;
+  const size_t i = std::lower_bound(values.begin(), values.end(), a) - values.begin();
+  int c;
+  if (i == 0) {
+    c = 0;
+  } else if (i == values.size()) {
+    c = 0x7e;
+  } else {
+    const double dlo = a - values[i - 1], dhi = values[i] - a;
+    if (dlo < dhi) c = static_cast<int>(i - 1);
+    else if (dhi < dlo) c = static_cast<int>(i);
+    else c = ((i - 1) & 1) == 0 ? static_cast<int>(i - 1) : static_cast<int>(i);
+  }
+  return static_cast<uint8_t>(c) | sign;
+}
+
+// One row of C binary32 values -> E4M3 codes and a binary32 scale, every step
+// rounded to binary32 as the stored result is: amax = max |x|, scale = amax /
+// 448, code[d] = e4m3(x[d] * (448 / amax)); a row of zeros gets scale 0 and
+// zero codes.  Dequantized value: scale * e4m3_to_double(code).
+void quantize_row_e4m3(const float* x, int64_t C, uint8_t* codes, float* scale) {
+  float amax = 0.0f;
+  for (int64_t d = 0; d < C; ++d) amax = std::max(amax, std::fabs(x[d]));
+  if (amax == 0.0f) {
+    for (int64_t d = 0; d < C; ++d) codes[d] = 0;
+    *scale = 0.0f;
+    return;
+  }
+  const float inv = 448.0f / amax;
+  *scale = amax / 448.0f;
+  for (int64_t d = 0; d < C; ++d) {
+    const float y = x[d] * inv;
+    codes[d] = float_to_e4m3_sat(y);
+  }
 }
 
 // Runs fn(i) for i in [0, n) on up to `threads` std::threads (contiguous
@@ -288,6 +356,70 @@ int oracle_decode_attn(const uint16_t* q, const uint16_t* swa, const int32_t* se
     }
     for (int64_t d = 0; d < Dv; ++d) o[d] = num[d] / den;
     if (lse) lse[b * Hq + h] = m + std::log(den);
+  });
+  return 0;
+}
+
+void oracle_e4m3_to_double(const uint8_t* x, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(x[i]);
+}
+
+void oracle_float_to_e4m3(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = float_to_e4m3_sat(x[i]);
+}
+
+// Per-row E4M3 quantization (quantize_row_e4m3 on each of `rows` rows of C).
+//   x : fp32 [rows, C]   codes : u8 [rows, C]   scales : fp32 [rows]
+int oracle_quantize_e4m3(const float* x, int64_t rows, int64_t C, uint8_t* codes, float* scales,
+                         int threads) {
+  if (rows < 0 || C <= 0) return 1;
+  parallel_for(rows, threads, [&](int64_t i) {
+    quantize_row_e4m3(x + i * C, C, codes + i * C, scales + i);
+  });
+  return 0;
+}
+
+// Indexer scores over an E4M3 key pool: the score of oracle_indexer_scores on
+// the dequantized operands,
+//     s[b, j] = sum_h w[b, h] * max(0, sum_d qhat[b, h, d] * khat[j, d]),
+//     khat[j, d] = kscale[j] * e4m3(keys[j, d]),
+//     qhat[b, h, d] = qscale[b, h] * e4m3(qcode[b, h, d]),
+// where each query row iq[b, h, :] (bf16, widened exactly) is quantized as
+// oracle_quantize_e4m3 quantizes a row.
+//   iq : bf16 [B, Hi, Di]   w : fp32 [B, Hi]   keys : u8 [sum N_b, Di]
+//   kscale : fp32 [sum N_b]   offsets : int64 [B+1]   scores : fp64 [sum N_b]
+int oracle_indexer_scores_e4m3(const uint16_t* iq, const float* w, const uint8_t* keys,
+                               const float* kscale, const int64_t* offsets, int64_t B,
+                               int64_t Hi, int64_t Di, double* scores, int threads) {
+  if (B < 0 || Hi <= 0 || Di <= 0) return 1;
+  for (int64_t b = 0; b < B; ++b)
+    if (offsets[b + 1] < offsets[b]) return 1;
+  // the quantized, then dequantized, query rows
+  std::vector<double> qhat(static_cast<size_t>(B * Hi * Di));
+  {
+    std::vector<float> row(Di);
+    std::vector<uint8_t> code(Di);
+    for (int64_t bh = 0; bh < B * Hi; ++bh) {
+      for (int64_t d = 0; d < Di; ++d) row[d] = static_cast<float>(bf16_to_double(iq[bh * Di + d]));
+      float sq;
+      quantize_row_e4m3(row.data(), Di, code.data(), &sq);
+      for (int64_t d = 0; d < Di; ++d)
+        qhat[bh * Di + d] = static_cast<double>(sq) * e4m3_to_double(code[d]);
+    }
+  }
+  const int64_t first = offsets[0], total = offsets[B] - offsets[0];
+  parallel_for(total, threads, [&](int64_t e) {
+    const int64_t j = first + e;
+    const int64_t b = (std::upper_bound(offsets, offsets + B + 1, j) - offsets) - 1;
+    double s = 0.0;
+    for (int64_t h = 0; h < Hi; ++h) {
+      double dot = 0.0;
+      for (int64_t d = 0; d < Di; ++d)
+        dot += qhat[(b * Hi + h) * Di + d] *
+               (static_cast<double>(kscale[j]) * e4m3_to_double(keys[j * Di + d]));
+      s += static_cast<double>(w[b * Hi + h]) * std::max(0.0, dot);
+    }
+    scores[j] = s;
   });
   return 0;
 }

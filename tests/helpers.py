@@ -15,8 +15,9 @@ def golden(name):
 
 
 def closed_form(expr: str) -> float:
-    """Evaluate a closed-form expression from a golden file (exp/log/sqrt only)."""
-    return float(eval(expr, {"__builtins__": {}}, {"exp": math.exp, "log": math.log, "sqrt": math.sqrt}))
+    """Evaluate a closed-form expression from a golden file (exp/log/sqrt/float only)."""
+    return float(eval(expr, {"__builtins__": {}}, {"exp": math.exp, "log": math.log, "sqrt": math.sqrt,
+                                                   "float": float}))
 
 
 def as_float(v):

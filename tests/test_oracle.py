@@ -413,3 +413,135 @@ def test_threaded_stages_equal_single_thread(oracle_mod):
     for t in (3, 16):
         o, l = oracle_mod.decode_attn(qa, swa, L, W, extra, aoffs, idx, 0.3, Dv, threads=t)
         assert np.array_equal(o, o1) and np.array_equal(l, l1)
+
+
+# ---------------------------------------------------------------- FP8 E4M3 (indexer-key pool)
+
+def test_e4m3_decode_every_code_matches_torch(oracle_mod):
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle_mod.e4m3_to_double(codes)
+    lib = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(lib))
+    assert np.isnan(got).sum() == 2                          # 0x7f and 0xff
+    live = ~np.isnan(got)
+    assert np.array_equal(got[live], lib[live])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+    assert got[0x38] == 1.0 and got[0xB8] == -1.0
+
+
+def test_e4m3_encode_named_values(oracle_mod):
+    g = golden("e4m3_worked.json")
+    x = np.array([closed_form(e) for e, _, _ in g["encode"]], np.float32)
+    want = [c for _, c, _ in g["encode"]]
+    assert [int(v) for v in oracle_mod.float_to_e4m3(x)] == want
+    assert int(oracle_mod.float_to_e4m3(np.array([np.nan], np.float32))[0]) & 0x7F == 0x7F
+
+
+def test_e4m3_encode_matches_torch_rounding(oracle_mod):
+    rng = np.random.default_rng(RNG_SEED)
+    vals = oracle_mod.e4m3_to_double(np.arange(0x7F, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2                         # every tie, exactly
+    x = np.concatenate([
+        rng.uniform(-448, 448, 200_000),
+        rng.standard_normal(100_000) * 0.02,                  # the subnormal range
+        mids, -mids,
+        np.nextafter(mids.astype(np.float32), np.float32(np.inf)),
+        np.nextafter(mids.astype(np.float32), np.float32(-np.inf)),
+    ]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle_mod.float_to_e4m3(x), lib)
+
+
+def test_e4m3_quantize_rows(oracle_mod):
+    rng = np.random.default_rng(RNG_SEED + 1)
+    x = (rng.standard_normal((300, 128)) * rng.uniform(1e-3, 50, (300, 1))).astype(np.float32)
+    x[7] = 0.0
+    x[11, :] = 0.0
+    x[11, 5] = -3.0                                           # a row whose amax is one negative value
+    codes, scales = oracle_mod.quantize_e4m3(x)
+    assert scales[7] == 0 and not codes[7].any()
+    amax = np.abs(x).max(axis=1)
+    live = amax > 0
+    assert np.array_equal(scales[live], (amax[live] / np.float32(448)).astype(np.float32))
+    # each row's largest magnitude lands on the format's largest finite value
+    arg = np.abs(x).argmax(axis=1)
+    top = codes[np.arange(300), arg][live]
+    assert np.all((top & 0x7F) == 0x7E)
+    assert codes[11, 5] == 0xFE
+    # every code is the nearest to x * (448 / amax): at most half a code step
+    y = x[live] * (np.float32(448) / amax[live])[:, None]
+    yv = oracle_mod.e4m3_to_double(codes[live])
+    e = np.floor(np.log2(np.maximum(np.abs(y).astype(np.float64), 2.0 ** -6)))
+    half_step = 2.0 ** (e - 3) / 2
+    assert np.all(np.abs(y - yv) <= half_step * (1 + 1e-12))
+
+
+def test_indexer_e4m3_worked_example(oracle_mod):
+    g = golden("e4m3_worked.json")["scores"]
+    q = bf16_bits(torch.tensor(g["q"], dtype=torch.float32)).reshape(1, 1, 4)
+    w = np.array([g["w"]], np.float32)
+    codes, sc = oracle_mod.quantize_e4m3(np.array(g["keys"], np.float32))
+    got = oracle_mod.indexer_scores_e4m3(q, w, codes, sc, np.array([0, 4], np.int64))
+    want = np.array([closed_form(e) for e in g["expected"]])
+    assert np.allclose(got, want, rtol=g["rel_tol"], atol=0)
+    assert got[1] == 0.0 and got[3] == 0.0
+
+
+def test_indexer_e4m3_library_matmul_and_one_hot(oracle_mod):
+    rng = np.random.default_rng(RNG_SEED + 2)
+    B, Hi, Di = 3, 5, 64
+    counts = [17, 0, 40]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    q_bits = _normal_bits("e4m3_q", (B, Hi, Di))
+    w = rng.uniform(0, 1, (B, Hi)).astype(np.float32)
+    kx = (rng.standard_normal((int(offs[-1]), Di)) * 3).astype(np.float32)
+    kx[5] = 0.0
+    kx[6] = 0.0
+    kx[6, 9] = -2.5                                           # a one-hot key
+    codes, sc = oracle_mod.quantize_e4m3(kx)
+    got = oracle_mod.indexer_scores_e4m3(q_bits, w, codes, sc, offs)
+    # numpy float64 on the dequantized operands (queries quantized per row)
+    qc, qs = oracle_mod.quantize_e4m3(bf16_values(q_bits).reshape(-1, Di).astype(np.float32))
+    qhat = oracle_mod.dequantize_e4m3(qc, qs).reshape(B, Hi, Di)
+    khat = oracle_mod.dequantize_e4m3(codes, sc)
+    for b in range(B):
+        rows = slice(int(offs[b]), int(offs[b + 1]))
+        want = np.maximum(khat[rows] @ qhat[b].T, 0.0) @ w[b].astype(np.float64)
+        assert np.allclose(got[rows], want, rtol=1e-12, atol=1e-300)
+    assert got[5] == 0.0
+    # the one-hot key: sum_h w_h max(0, qhat[h, 9] * khat[6, 9])
+    assert khat[6, 9] == pytest.approx(-2.5, rel=1e-6)
+    want6 = sum(float(w[0, h]) * max(0.0, qhat[0, h, 9] * khat[6, 9]) for h in range(Hi))
+    assert got[6] == pytest.approx(want6, rel=1e-12)
+
+
+def test_layer_step_e4m3_key_pool_matches_bulk_compression_of_history(oracle_mod):
+    """With an E4M3 key pool the step writes the completed block's indexer key
+    as the per-row quantization of the fp32-rounded compressor output: after
+    the step the pool equals the quantized bulk compression of the history,
+    and the scores are the E4M3 scores over that pool."""
+    shape = synth.TINY
+    L = 64
+    st, raw = synth.raw_token_state(RNG_SEED, 4, shape, L)
+    s = _np_state(st)
+    kvh = bf16_bits(raw["kv"])
+    prefix = oracle_mod.compress(kvh, bf16_bits(raw["z"]), s["b_kv"], 4)[0]
+    s["kv_pool"][:prefix.shape[0]] = oracle_mod.float_to_bf16(prefix.astype(np.float32))
+    pk = oracle_mod.compress(bf16_bits(raw["ik"]), bf16_bits(raw["iz"]), s["b_ik"], 4)[0]
+    cap = s["key_pool"].shape[0]
+    s["key_fp8"] = True
+    s["key_pool"] = np.zeros((cap, shape.Di), np.uint8)
+    s["key_scale"] = np.zeros(cap, np.float32)
+    c0, s0 = oracle_mod.quantize_e4m3(pk.astype(np.float32))
+    s["key_pool"][:pk.shape[0]] = c0
+    s["key_scale"][:pk.shape[0]] = s0
+    res = oracle_mod.layer_decode(s)
+    full_ik = np.concatenate([bf16_bits(raw["ik"])[0], s["ik_new"]], axis=0)[None]
+    full_iz = np.concatenate([bf16_bits(raw["iz"])[0], s["iz_new"]], axis=0)[None]
+    bulk = oracle_mod.compress(full_ik, full_iz, s["b_ik"], 4)[0].astype(np.float32)
+    bc, bs = oracle_mod.quantize_e4m3(bulk)
+    n = L // 4
+    assert np.array_equal(s["key_pool"][:n], bc) and np.array_equal(s["key_scale"][:n], bs)
+    want = oracle_mod.indexer_scores_e4m3(s["iq"], s["w"], bc, bs, np.array([0, n], np.int64))
+    assert np.array_equal(res["scores64"], want)
