@@ -62,13 +62,15 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def layer_bytes(L, shape, kind=4):
+def layer_bytes(L, shape, kind=4, key_entry_bytes=None):
     """Algorithmic HBM bytes of one layer step (each byte the method must move,
     counted once).  C4: indexer keys, score write + read, the gathered window
     and top-k rows, q, o, the index list, the new-token append and the 4-row
     block reads / writes of the sequences whose block completes.  C128: the
     gathered window and every C128 row, q, o, the append and the 128-row
-    block compression of the sequences whose block completes."""
+    block compression of the sequences whose block completes.
+    key_entry_bytes: bytes of one stored indexer key (bf16: 2 Di; E4M3 codes
+    and their fp32 scale: Di + 4)."""
     L = L.to(torch.int64)
     B = L.numel()
     D, Di = shape.Dqk, shape.Di
@@ -86,14 +88,15 @@ def layer_bytes(L, shape, kind=4):
                 "append_compress": append + compress}
     n4 = L // 4
     N = int(n4.sum())
-    keys = N * Di * 2
+    kb = Di * 2 if key_entry_bytes is None else key_entry_bytes
+    keys = N * kb
     iq_w = B * shape.Hi * (Di * 2 + 4)
     scores = 2 * N * 4
     gather = (win + int(torch.clamp(n4, max=shape.k).sum())) * D * 2
     idx = 2 * B * shape.k * 4
     append = B * (D * 2 * 2 + D * 2 * 3 + Di * 2 * 2 + Di * 2 * 2)   # read new rows, write rings
     ncomp = int((L % 4 == 0).sum())
-    compress = ncomp * (4 * 2 * (D + Di) * 2 + (D + Di) * 2)
+    compress = ncomp * (4 * 2 * (D + Di) * 2 + D * 2 + kb)
     indexer = keys + iq_w + N * 4
     total = keys + iq_w + scores + gather + q + o + idx + append + compress
     return {"total": total, "indexer": indexer, "keys": keys, "gather": gather,
@@ -476,6 +479,79 @@ def layer_outputs(g):
     return out, lse, seq_out, idx, scores
 
 
+def rotating_us(steps_fns, warmup, steps, stream):
+    """Mean CUDA-event microseconds of one step, step i running steps_fns[i mod
+    n] (each on its own layer state: inputs larger than L2, no flush)."""
+    n = len(steps_fns)
+    for i in range(max(warmup, n)):
+        steps_fns[i % n]()
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        ev0[i].record(stream)
+        steps_fns[i % n]()
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in zip(ev0, ev1)) * 1000
+
+
+def layer_variants(args, runs, peak):
+    """The headline step in two variants, each over the same rotating layer
+    states: (1) the top-k as its own kernels after the indexer instead of
+    fused into the attention kernel (no overlap of the window's attention
+    with the selection); (2) an E4M3 indexer-key pool (the states' bf16 key
+    pools quantized per row by the library: codes plus one fp32 scale per
+    entry; every other tensor as in the headline)."""
+    import copy as _copy
+    stream = torch.cuda.current_stream()
+    out = {}
+    # (1) separate top-k: a bound on the rows above the fused selection's limit
+    descs = [_lib.layer_desc(r.g, r.out, r.lse, r.seq_out, None, r.scores, max_pool_rows=40000)
+             for r in runs]
+    wss = [_lib.workspace(_lib.hsa_layer_decode_workspace_size(d)) for d in descs]
+    us = rotating_us([lambda d=d, w=w: _lib.hsa_layer_decode(d, ws=w) for d, w in zip(descs, wss)],
+                     args.warmup, args.steps, stream)
+    out["topk_separate_kernels"] = {"us": us, "launches": _lib.hsa_layer_decode_launches(descs[0])}
+    del descs, wss
+    # (2) E4M3 key pools
+    stage = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in stage:
+        e.record(stream)
+    fns, stage_fns, keep = [], [], []
+    for r in runs:
+        g8 = _copy.copy(r.g)
+        g8.key_pool, g8.key_scale = _lib.hsa_quantize_e4m3(r.g.key_pool.float())
+        d = _lib.layer_desc(g8, r.out, r.lse, r.seq_out, None, r.scores)
+        ds = _lib.layer_desc(g8, r.out, r.lse, r.seq_out, None, r.scores,
+                             stage_events=[e.cuda_event for e in stage])
+        w = _lib.workspace(_lib.hsa_layer_decode_workspace_size(d))
+        fns.append(lambda d=d, w=w: _lib.hsa_layer_decode(d, ws=w))
+        stage_fns.append(lambda d=ds, w=w: _lib.hsa_layer_decode(d, ws=w))
+        keep.append((g8, d, ds, w))
+    torch.cuda.synchronize()
+    us = rotating_us(fns, args.warmup, args.steps, stream)
+    idx_ms = []
+    for i in range(args.steps):
+        stage_fns[i % len(stage_fns)]()
+        stage[4].synchronize()
+        idx_ms.append(stage[1].elapsed_time(stage[2]))
+    for g8, d, ds, w in keep:
+        assert _lib.hsa_workspace_status(w) == 0
+    Di = runs[0].g.shape.Di
+    nb = statistics.mean(layer_bytes(r.L, r.g.shape, 4, key_entry_bytes=Di + 4)["total"] for r in runs)
+    ib = statistics.mean(layer_bytes(r.L, r.g.shape, 4, key_entry_bytes=Di + 4)["indexer"] for r in runs)
+    it = statistics.mean(idx_ms)
+    out["e4m3_keys"] = {
+        "us": us, "algorithmic_bytes": nb, "achieved_gbs": nb / (us * 1e-6) / 1e9,
+        "frac": nb / (us * 1e-6) / 1e9 / peak,
+        "indexer_stage_us": it * 1000, "indexer_algorithmic_bytes": ib,
+        "indexer_frac": ib / (it * 1e-3) / 1e9 / peak,
+        "format": "E4M3 codes [rows, 128] + fp32 scale per row (amax / 448); queries "
+                  "quantized per (sequence, head) in the kernel; tcgen05 kind::f8f6f4"}
+    return out
+
+
 def e2e_layer(runs, flush, warmup, steps):
     """The layer step through host buffers, over the given layer runs (step i
     on run i mod len(runs); with several runs, inputs larger than L2 and no
@@ -642,7 +718,9 @@ def measure_c4layer(args, rank, local, dist):
     assert torch.equal(host_o, runs[0].out.cpu())
 
     extra = {}
+    peak, peak_kind = measured_peaks()
     if rank == 0 and not args.no_extra:
+        extra["layer_variants"] = layer_variants(args, runs, peak)
         if args.layers > 0:
             extra["multi_layer_graph"] = multi_layer_graph(args, flush, runs)
         extra["topk_rows_per_s"] = bench_topk(flush, args)
@@ -657,7 +735,6 @@ def measure_c4layer(args, rank, local, dist):
                          f"(~{args.cpu_budget:.0f} s budget), mean",
                "threads_busy_by_stage": busy}
 
-    peak, peak_kind = measured_peaks()
     idx_ms = float(stage_mean[1])
     achieved = nbytes["indexer"] / (idx_ms * 1e-3) / 1e9
     layer_gbs = total_bytes / (ms * 1e-3) / 1e9

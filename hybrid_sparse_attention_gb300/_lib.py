@@ -43,6 +43,8 @@ SIGNATURES = {
     "hsa_topk_workspace_size": (SZ, [I64, I64, I64]),
     "hsa_topk": (I32, [P, P, I64, I64, I64, P, P, P, SZ, P]),
     "hsa_topk_noalloc": (I32, [P, P, I64, I64, I64, P, P, P]),
+    "hsa_quantize_e4m3": (I32, [P, I64, I64, P, P, P]),
+    "hsa_indexer_scores_e4m3": (I32, [P, P, P, P, P, I64, I64, I64, I64, P, P, SZ, P]),
 }
 
 
@@ -148,6 +150,38 @@ def hsa_indexer_scores(iq, w, keys, offsets, scores=None, ws=None, stream=None):
     return scores
 
 
+def hsa_quantize_e4m3(x, codes=None, scales=None, stream=None):
+    """Per-row E4M3 quantization: x fp32 [rows, C] -> (codes uint8 [rows, C],
+    scales fp32 [rows]), scale = amax / 448, code = e4m3(x * 448 / amax)."""
+    rows, C = x.shape
+    if codes is None:
+        codes = torch.empty(rows, C, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _call("hsa_quantize_e4m3", _dev(x, torch.float32, "x"), rows, C,
+          _dev(codes, torch.uint8, "codes"), _dev(scales, torch.float32, "scales"),
+          _stream(stream))
+    return codes, scales
+
+
+def hsa_indexer_scores_e4m3(iq, w, keys, key_scales, offsets, scores=None, ws=None, stream=None):
+    """Indexer scores over an E4M3 key pool: iq bf16 [B,Hi,128] (quantized per row
+    in the kernel), w fp32 [B,Hi], keys uint8 [total,128], key_scales fp32
+    [total], offsets int64 [B+1] (device) -> scores fp32 [total]."""
+    B, Hi, Di = iq.shape
+    total = keys.shape[0]
+    if scores is None:
+        scores = torch.zeros(total, dtype=torch.float32, device=keys.device)
+    if ws is None:
+        ws = workspace(hsa_indexer_scores_workspace_size(), keys.device)
+    _call("hsa_indexer_scores_e4m3", _dev(iq, torch.bfloat16, "iq"), _dev(w, torch.float32, "w"),
+          _dev(keys, torch.uint8, "keys"), _dev(key_scales, torch.float32, "key_scales"),
+          _dev(offsets, torch.int64, "offsets"), B, Hi, Di, total,
+          _dev(scores, torch.float32, "scores"), _dev(ws, torch.uint8, "ws"), ws.numel(),
+          _stream(stream))
+    return scores
+
+
 def hsa_topk_workspace_size(B: int, total_rows: int, k: int) -> int:
     return int(load().hsa_topk_workspace_size(B, total_rows, k))
 
@@ -233,7 +267,7 @@ class LayerDesc(ctypes.Structure):
         ("swa", P), ("kv_ring", P), ("z_ring", P), ("ik_ring", P), ("iz_ring", P),
         ("kv_pool", P), ("key_pool", P), ("q", P), ("iq", P), ("w", P),
         ("out", P), ("lse", P), ("topk_idx", P), ("scores", P), ("stage_events", P),
-        ("q_ready_event", P),
+        ("q_ready_event", P), ("key_fp8", ctypes.c_int32), ("key_scale", P),
     ]
 
 
@@ -278,7 +312,13 @@ def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
         d.b_ik = _dev(st.b_ik, torch.float32, "b_ik")
         d.ik_ring = _dev(st.ik_ring, torch.bfloat16, "ik_ring")
         d.iz_ring = _dev(st.iz_ring, torch.bfloat16, "iz_ring")
-        d.key_pool = _dev(st.key_pool, torch.bfloat16, "key_pool")
+        # an E4M3 key pool: uint8 codes with one fp32 scale per row
+        key_scale = getattr(st, "key_scale", None)
+        d.key_pool = _dev(st.key_pool, torch.bfloat16 if key_scale is None else torch.uint8,
+                          "key_pool")
+        if key_scale is not None:
+            d.key_fp8 = 1
+            d.key_scale = _dev(key_scale, torch.float32, "key_scale")
         d.iq = _dev(st.iq, torch.bfloat16, "iq")
         d.w = _dev(st.w, torch.float32, "w")
         d.topk_idx = _dev(topk_idx, torch.int32, "topk_idx", True)

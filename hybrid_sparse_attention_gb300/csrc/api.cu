@@ -56,8 +56,11 @@ int device_sms() {
   return cache[dev];
 }
 
-cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
-                              int box_inner, int box_outer, CUtensorMapSwizzle swizzle) {
+namespace {
+
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType type, int esize,
+                         int64_t inner, int64_t outer, int box_inner, int box_outer,
+                         CUtensorMapSwizzle swizzle) {
   static std::mutex mu;
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   {
@@ -73,13 +76,27 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner,
     }
   }
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * esize};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                              int box_inner, int box_outer, CUtensorMapSwizzle swizzle) {
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, box_inner,
+                      box_outer, swizzle);
+}
+
+cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                            int box_inner, int box_outer, CUtensorMapSwizzle swizzle) {
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, inner, outer, box_inner,
+                      box_outer, swizzle);
 }
 
 }  // namespace hsa
@@ -171,6 +188,48 @@ hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys
   return cuda_status(launch_indexer(iq, w, keys, sp, static_cast<int>(B), static_cast<int>(Hi),
                                     static_cast<int>(Di), total_rows, scores,
                                     static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream)),
+                     "indexer launch");
+}
+
+hsa_status_t hsa_quantize_e4m3(const float* x, int64_t rows, int64_t C, uint8_t* codes,
+                               float* scales, void* stream) {
+  HSA_CHECK(rows >= 0 && rows < (int64_t(1) << 34), HSA_ERR_INVALID_ARG, "rows=%lld out of range",
+            (long long)rows);
+  HSA_CHECK(C > 0 && C % 4 == 0 && C < (int64_t(1) << 30), HSA_ERR_UNSUPPORTED,
+            "C=%lld must be a positive multiple of 4", (long long)C);
+  if (rows == 0) return HSA_OK;
+  HSA_CHECK(x && codes && scales, HSA_ERR_INVALID_ARG, "null pointer");
+  HSA_CHECK(aligned(x, 16) && aligned(codes, 4) && aligned(scales, 4), HSA_ERR_INVALID_ARG,
+            "misaligned pointer (x: 16 bytes, codes: 4)");
+  return cuda_status(launch_quantize_e4m3(x, rows, C, codes, scales,
+                                          static_cast<cudaStream_t>(stream)),
+                     "quantize launch");
+}
+
+hsa_status_t hsa_indexer_scores_e4m3(const void* iq, const float* w, const uint8_t* keys,
+                                     const float* key_scales, const int64_t* offsets, int64_t B,
+                                     int64_t Hi, int64_t Di, int64_t total_rows, float* scores,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  HSA_CHECK(B >= 1 && B <= (1 << 24), HSA_ERR_INVALID_ARG, "B=%lld out of range", (long long)B);
+  HSA_CHECK(B <= 4096, HSA_ERR_UNSUPPORTED, "B=%lld above the indexer's 4096 sequences",
+            (long long)B);
+  HSA_CHECK(Hi >= 1 && Hi <= 16, HSA_ERR_UNSUPPORTED, "Hi=%lld outside [1, 16]", (long long)Hi);
+  HSA_CHECK(Di == 128, HSA_ERR_UNSUPPORTED, "Di=%lld: E4M3 keys need Di = 128", (long long)Di);
+  HSA_CHECK(total_rows >= 0 && total_rows < (int64_t(1) << 31), HSA_ERR_INVALID_ARG,
+            "total_rows=%lld out of range", (long long)total_rows);
+  HSA_CHECK(iq && w && offsets && (keys || total_rows == 0) && (key_scales || total_rows == 0) &&
+                (scores || total_rows == 0),
+            HSA_ERR_INVALID_ARG, "null pointer");
+  HSA_CHECK(aligned(iq, 16) && aligned(keys, 16) && aligned(w, 4) && aligned(scores, 4) &&
+                aligned(key_scales, 4) && aligned(offsets, 8),
+            HSA_ERR_INVALID_ARG, "misaligned pointer (iq, keys: 16 bytes)");
+  HSA_CHECK(ws && aligned(ws, 256) && ws_bytes >= kWsHeader, HSA_ERR_WORKSPACE,
+            "workspace null, misaligned or below %zu bytes", kWsHeader);
+  Spans sp{offsets, nullptr, 0, 1, total_rows};
+  return cuda_status(launch_indexer(iq, w, keys, sp, static_cast<int>(B), static_cast<int>(Hi),
+                                    static_cast<int>(Di), total_rows, scores,
+                                    static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream),
+                                    false, 0, nullptr, key_scales),
                      "indexer launch");
 }
 
@@ -284,6 +343,12 @@ static hsa_status_t check_layer(const hsa_layer_desc* d) {
                   aligned(d->key_pool, 16) && aligned(d->iq, 16) && aligned(d->w, 4) &&
                   aligned(d->topk_idx, 4) && aligned(d->scores, 4),
               HSA_ERR_INVALID_ARG, "misaligned indexer pointer");
+    HSA_CHECK(d->key_fp8 == 0 || d->key_fp8 == 1, HSA_ERR_INVALID_ARG, "key_fp8 must be 0 or 1");
+    if (d->key_fp8) {
+      HSA_CHECK(d->Di == 128, HSA_ERR_UNSUPPORTED, "Di=%d: E4M3 keys need Di = 128", d->Di);
+      HSA_CHECK(d->key_scale && aligned(d->key_scale, 4), HSA_ERR_INVALID_ARG,
+                "E4M3 keys need an aligned key_scale");
+    }
   } else {
     HSA_CHECK(d->max_pool_rows >= 0 && d->max_pool_rows <= (int64_t(1) << 28),
               HSA_ERR_INVALID_ARG, "max_pool_rows out of range");

@@ -18,10 +18,22 @@
 // The kernel is bound by the key bytes (2*Di bytes per entry against 4*Hi*Di
 // flops), so it is built to keep HBM busy: one persistent CTA per SM walks a
 // contiguous range of 128-key tiles (tiles never straddle two sequences)
-// through a 5-stage TMA ring; warp 0 issues the loads, one lane of warp 1
-// issues the MMAs into two alternating TMEM accumulators, and warps 2-5 (one
-// TMEM lane quarter each) drain the accumulators while the next tiles load.
+// through a TMA ring; warp 0 issues the loads, one lane of warp 1 issues the
+// MMAs into alternating TMEM accumulators, and warps 2-5 (one TMEM lane
+// quarter each) drain the accumulators while the next tiles load.
+//
+// E4M3 key pool (kFp8): the keys are 8-bit codes with one fp32 scale per entry
+// (half the bytes), the MMAs are kind::f8f6f4 E4M3 x E4M3, and the queries
+// are quantized the same way per (sequence, head) row inside the kernel: the
+// epilogue warps write the E4M3 query rows of the CTA's next sequences into
+// two shared-memory buffers ahead of the MMA (a buffer is refilled once the
+// last tile of its previous sequence has been drained), so the kernel reads
+// nothing the previous kernel writes before its first key tile.  With
+// qhat = sq * code(q) and khat = sk * code(k), sq, sk > 0:
+//     s[j] = sum_h w_h max(0, qhat_h . khat_j)
+//          = sk_j * sum_h (w_h sq_h) max(0, code(q_h) . code(k_j)).
 #include <cuda.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -32,7 +44,11 @@ namespace {
 
 constexpr int kTileRows = 128;  // M
 constexpr int kQRows = 16;      // N (heads, padded)
-constexpr int kStages = 6;
+constexpr int kStagesBf16 = 6;  // 36 KB stages (keys + queries)
+constexpr int kStagesFp8 = 12;  // 16 KB stages (keys): as many key bytes in flight
+constexpr int kMaxStages = 12;
+constexpr int kFp8Di = 128;     // E4M3 keys: one 128-byte swizzle row per entry
+constexpr uint32_t kQ8Bytes = kQRows * kFp8Di;  // one sequence's E4M3 query rows
 constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kMaxSeqs = 4096;  // tile prefix table (built in a stage buffer before the ring starts)
 constexpr int kAcc = 4;         // accumulators in TMEM (tiles the MMA may run ahead of the epilogue)
@@ -47,11 +63,15 @@ struct IndexerParams {
   uint32_t* status;
   int wait_mode;   // programmatic dependent launch: see launch_indexer in internal.h
   uint32_t* row_hist;  // per-sequence order-key histograms for the top-k (may be null)
+  const float* key_scale;  // E4M3 keys: fp32 [total_rows]
+  const uint16_t* iq;      // E4M3 keys: the bf16 queries [B, Hi, Di], quantized in the kernel
 };
 
 struct Shared {
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t acc_full[kAcc], acc_empty[kAcc];
+  uint64_t q8_full[2];      // E4M3 query buffer written (128 epilogue arrivals)
+  float q8w[2][kQRows];     // the buffer's w[b, h] * query scale (0 past Hi)
   uint64_t fin;
   uint32_t tmem;
   int abort;
@@ -97,6 +117,24 @@ struct SeqCursor {
     if (L % p.sp.ratio != 0) return -1;
     return first + static_cast<int>((count - 1) / kTileRows);
   }
+  // Moves to the first sequence of the CTA's range (start) or to the next
+  // sequence owning tiles; false when that sequence's tiles start at or past
+  // t_end (or there is none).
+  HSA_DEVINL bool step(const Shared& sh, const IndexerParams& p, bool start, int t_end) {
+    if (start) {
+      b = sh.b0;
+      first = sh.first0;
+      load(p);
+      return first < t_end;
+    }
+    do {
+      if (b + 1 >= p.B) return false;
+      ++b;
+      first = next;
+      load(p);
+    } while (next == first);
+    return first < t_end;
+  }
   HSA_DEVINL bool seek(const Shared& sh, const IndexerParams& p, int t) {
     if (b >= 0 && t < next) return false;
     if (b < 0) {
@@ -113,6 +151,49 @@ struct SeqCursor {
   }
 };
 
+// E4M3 query rows of sequence b into buffer `buf` (the 128 epilogue threads,
+// e = 0..127: head e / 8, channels 16 (e % 8) .. +16): per row amax over the
+// 8 lanes of the head, code = e4m3(q * (448 / amax)) (round to nearest even,
+// saturating), stored 128-byte swizzled as the MMA's K-major B operand; the
+// head's weight w[b, h] * amax / 448 goes to q8w.  Then the buffer's barrier.
+HSA_DEVINL void quantize_queries(const IndexerParams& p, Shared& sh, uint8_t* q8, int b, int buf,
+                                 int e) {
+  const int h = e >> 3, part = e & 7;
+  float x[16];
+  if (h < p.Hi) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.iq + (static_cast<int64_t>(b) * p.Hi + h) * kFp8Di +
+                                                      part * 16);
+    bf16x8_to_f32(__ldg(src), x);
+    bf16x8_to_f32(__ldg(src + 1), x + 8);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = 0.f;
+  }
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(x[i]));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  const float inv = am > 0.f ? __fdiv_rn(448.f, am) : 0.f;
+  uint32_t w4[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fmul_rn(x[4 * i], inv), __fmul_rn(x[4 * i + 1], inv)), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fmul_rn(x[4 * i + 2], inv), __fmul_rn(x[4 * i + 3], inv)), __NV_SATFINITE, __NV_E4M3);
+    w4[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  uint8_t* buf_base = q8 + buf * kQ8Bytes;
+  *reinterpret_cast<uint4*>(buf_base + (h >> 3) * 1024 + (h & 7) * 128 + ((part ^ (h & 7)) << 4)) =
+      make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  if (part == 0)
+    sh.q8w[buf][h] = h < p.Hi ? p.w[static_cast<int64_t>(b) * p.Hi + h] * __fdiv_rn(am, 448.f) : 0.f;
+  tc::fence_proxy_async_smem();
+  tc::mbar_arrive(&sh.q8_full[buf]);
+}
+
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap qmap,
                                                              IndexerParams p) {
@@ -129,12 +210,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
     pdl_trigger();
   }
 
-  const int kb_elems = p.Di >= 64 ? 64 : p.Di;  // elements of one swizzle row
-  const int nkb = p.Di / kb_elems;
-  const uint32_t a_kb = kTileRows * kb_elems * 2, b_kb = kQRows * kb_elems * 2;
+  constexpr int kStages = kFp8 ? kStagesFp8 : kStagesBf16;
+  const int kb_elems = kFp8 ? kFp8Di : (p.Di >= 64 ? 64 : p.Di);  // elements of one swizzle row
+  const int nkb = kFp8 ? 1 : p.Di / kb_elems;
+  const uint32_t a_kb = kFp8 ? kTileRows * kFp8Di : kTileRows * kb_elems * 2;
+  const uint32_t b_kb = kFp8 ? 0u : kQRows * kb_elems * 2;
   const uint32_t stage_bytes = nkb * (a_kb + b_kb);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
+  uint8_t* q8 = smem + kStages * stage_bytes;  // (kFp8) two E4M3 query buffers
 
   // tiles per sequence -> prefix table (block-wide scan in chunks of blockDim),
   // kept in the (not yet used) stage buffers just long enough to find the
@@ -183,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
       tc::mbar_init(&sh.acc_full[a], 1);
       tc::mbar_init(&sh.acc_empty[a], 128);
     }
+    for (int q = 0; q < 2; ++q) tc::mbar_init(&sh.q8_full[q], 128);
     tc::mbar_init(&sh.fin, 1);
     sh.abort = 0;
     tc::fence_mbar_init();
@@ -207,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
         waited = true;
       }
       pdl_trigger();
+      (void)b_kb;
       SeqCursor cur;
       // the keys are read once: they leave L2 first, so the scores and
       // histograms written here stay for the top-k that reads them next
@@ -230,8 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
         for (int kb = 0; kb < nkb; ++kb) {
           tc::tma_load_2d_hint(st + kb * a_kb, &kmap, kb * kb_elems, static_cast<int32_t>(row0),
                                &sh.full[s], keys_policy);
-          tc::tma_load_2d(st + nkb * a_kb + kb * b_kb, &qmap, kb * kb_elems, b * p.Hi,
-                          &sh.full[s]);
+          if (!kFp8)
+            tc::tma_load_2d(st + nkb * a_kb + kb * b_kb, &qmap, kb * kb_elems, b * p.Hi,
+                            &sh.full[s]);
         }
       }
       if (!waited) pdl_wait();  // the grid completes only after the previous kernel
@@ -239,16 +326,36 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const tc::Swizzle sw = kb_elems == 64 ? tc::kSwizzle128B : tc::kSwizzle64B;
-      const uint32_t sbo = 8 * kb_elems * 2;  // bytes between 8-row groups
-      const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, kQRows);
+      const tc::Swizzle sw = kFp8 || kb_elems == 64 ? tc::kSwizzle128B : tc::kSwizzle64B;
+      const uint32_t sbo = kFp8 ? 8u * kFp8Di : 8u * kb_elems * 2;  // bytes between 8-row groups
+      const uint32_t idesc =
+          kFp8 ? tc::idesc_e4m3_f32(kTileRows, kQRows) : tc::idesc_bf16_f32(kTileRows, kQRows);
+      SeqCursor mc;
+      int ord = -1;  // (kFp8) ordinal of the tile's sequence in this CTA's range
       for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
         const int s = i % kStages, a = i % kAcc;
+        if (kFp8 && mc.seek(sh, p, t)) {
+          ++ord;
+          if (!wait_or_abort(sh, &sh.q8_full[ord & 1], (ord >> 1) & 1, p.status)) break;
+        }
         if (!wait_or_abort(sh, &sh.full[s], (i / kStages) & 1, p.status)) break;
         if (i >= kAcc && !wait_or_abort(sh, &sh.acc_empty[a], ((i / kAcc) & 1) ^ 1, p.status))
           break;
         tc::fence_after_sync();
         const uint32_t sa = tc::smem_u32(smem + s * stage_bytes);
+        if (kFp8) {
+          // K = 32 codes (32 bytes) per MMA; each K-step into its own partial
+          const uint32_t sb = tc::smem_u32(q8 + (ord & 1) * kQ8Bytes);
+#pragma unroll
+          for (int ks = 0; ks < kFp8Di / 32; ++ks) {
+            const uint64_t da = tc::smem_desc(sa + ks * 32, 16, sbo, sw);
+            const uint64_t db = tc::smem_desc(sb + ks * 32, 16, sbo, sw);
+            tc::mma_f8(tmem + (a * kParts + ks % kParts) * kQRows, da, db, idesc, ks >= kParts);
+          }
+          tc::mma_commit(&sh.empty[s]);
+          tc::mma_commit(&sh.acc_full[a]);
+          continue;
+        }
         const uint32_t sb = sa + nkb * a_kb;
         // K-step kk accumulates into partial kk % kParts: chains of small-N
         // MMAs on one accumulator would serialize
@@ -270,22 +377,63 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;
-    const int nparts = p.Di / 16 < kParts ? p.Di / 16 : kParts;  // partials in use
+    const int e = threadIdx.x - 64;  // 0..127 over the epilogue warps
+    const int nparts = kFp8 ? kFp8Di / 32 : (p.Di / 16 < kParts ? p.Di / 16 : kParts);  // partials in use
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     SeqCursor cur;
     float wv[kQRows];
+    // (kFp8) the E4M3 queries of the range's first two sequences; `ahead` is the
+    // sequence of the last buffer written, `made` how many were written
+    SeqCursor ahead;
+    int made = 0, ord = -1;
+    if (kFp8) {
+      if (ahead.step(sh, p, true, t_end)) {
+        quantize_queries(p, sh, q8, ahead.b, 0, e);
+        made = 1;
+        if (ahead.step(sh, p, false, t_end)) {
+          quantize_queries(p, sh, q8, ahead.b, 1, e);
+          made = 2;
+        }
+      }
+      tc::named_barrier(1, 128);  // every buffer's weights visible to every epilogue thread
+    }
+    // A warp whose wait gave up (an abort) stops working; with kFp8 it keeps
+    // walking the tiles so that every epilogue thread reaches the same named
+    // barriers, where the warps agree on the abort.
+    bool dead = false;
+    // (kFp8, wait_mode 2) the key scale of a row the previous kernel may have
+    // just written is read only after the wait for that kernel, as the
+    // producer loads that row's codes
+    bool ewaited = !kFp8 || p.wait_mode != 2;
+    int edep = -1;
     for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
       const int a = i % kAcc;
       if (cur.seek(sh, p, t)) {
+        ++ord;
+        if (!ewaited) edep = cur.appended_tile(p);
+        if (!kFp8) {
 #pragma unroll
-        for (int h = 0; h < kQRows; ++h)
-          wv[h] = h < p.Hi ? __ldg(p.w + static_cast<int64_t>(cur.b) * p.Hi + h) : 0.f;
+          for (int h = 0; h < kQRows; ++h)
+            wv[h] = h < p.Hi ? __ldg(p.w + static_cast<int64_t>(cur.b) * p.Hi + h) : 0.f;
+        }
       }
       const int64_t piece = t - cur.first;
       const int64_t left = cur.count - piece * kTileRows;
       const int64_t row = cur.start + piece * kTileRows + r;
-      const bool ok = wait_or_abort(sh, &sh.acc_full[a], (i / kAcc) & 1, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (!ewaited && t == edep) {
+        pdl_wait();
+        ewaited = true;
+      }
+      const float ks = kFp8 && !dead && r < left ? p.key_scale[row] : 1.f;
+      if (!dead) dead = !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.acc_full[a], (i / kAcc) & 1, p.status));
+      if (dead && !kFp8) break;
+      if (!dead) {
+      if (kFp8) {
+        // written by the epilogue threads before the named barrier that
+        // followed (at the start, or at the end of the previous sequence)
+#pragma unroll
+        for (int h = 0; h < kQRows; ++h) wv[h] = sh.q8w[ord & 1][h];
+      }
       tc::fence_after_sync();
       float dot[kQRows];
 #pragma unroll
@@ -304,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
 #pragma unroll
         for (int h = 0; h < kQRows; ++h)
           if (h < p.Hi) sc = fmaf(wv[h], fmaxf(dot[h], 0.f), sc);
+        if (kFp8) sc *= ks;
         p.scores[row] = sc;
         // the top-k's histogram: one count in the bin of the score's top key
         // bits (a reduction: nothing waits for it)
@@ -311,6 +460,19 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
           atomicAdd(p.row_hist + static_cast<int64_t>(cur.b) * kRowHistBins +
                         (order_key(__float_as_uint(sc)) >> kRowHistShift),
                     1u);
+      }
+      }  // !dead
+      if (kFp8 && (t + 1 == cur.next || t + 1 == t_end) && made == ord + 2) {
+        // the sequence's last tile here is drained: its MMAs (and every
+        // earlier one) are complete, so its buffer takes sequence ord + 2,
+        // once every epilogue thread has read the buffer's weights (and
+        // agreed whether any warp gave up)
+        dead = tc::named_barrier_or(1, 128, dead);
+        if (!dead && ahead.step(sh, p, false, t_end)) {
+          quantize_queries(p, sh, q8, ahead.b, ord & 1, e);
+          ++made;
+        }
+        tc::named_barrier(1, 128);
       }
     }
   }
@@ -324,31 +486,43 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
 
 }  // namespace
 
-size_t indexer_smem_bytes(int Di) {
-  return static_cast<size_t>(kStages) * Di * 2 * (kTileRows + kQRows) + 1024;
+size_t indexer_smem_bytes(int Di, bool fp8) {
+  if (fp8) return static_cast<size_t>(kStagesFp8) * kTileRows * kFp8Di + 2 * kQ8Bytes + 1024;
+  return static_cast<size_t>(kStagesBf16) * Di * 2 * (kTileRows + kQRows) + 1024;
 }
 
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
-                           cudaStream_t stream, bool pdl, int wait_mode, uint32_t* row_hist) {
+                           cudaStream_t stream, bool pdl, int wait_mode, uint32_t* row_hist,
+                           const float* key_scale) {
   if (total_rows == 0) return cudaSuccess;
   if (B > kMaxSeqs) return cudaErrorInvalidValue;
+  const bool fp8 = key_scale != nullptr;
+  if (fp8 && (Di != kFp8Di || Hi > kQRows)) return cudaErrorInvalidValue;
   const int kb_elems = Di >= 64 ? 64 : Di;
   const CUtensorMapSwizzle sw = kb_elems == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap kmap, qmap;
-  cudaError_t e = make_tmap_2d_bf16(&kmap, keys, Di, total_rows, kb_elems, kTileRows, sw);
+  cudaError_t e;
+  if (fp8) {
+    e = make_tmap_2d_u8(&kmap, keys, Di, total_rows, kFp8Di, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B);
+    qmap = kmap;  // (unused: the queries are quantized in the kernel)
+  } else {
+    e = make_tmap_2d_bf16(&kmap, keys, Di, total_rows, kb_elems, kTileRows, sw);
+    if (e == cudaSuccess)
+      e = make_tmap_2d_bf16(&qmap, iq, Di, static_cast<int64_t>(B) * Hi, kb_elems, kQRows, sw);
+  }
   if (e != cudaSuccess) return e;
-  e = make_tmap_2d_bf16(&qmap, iq, Di, static_cast<int64_t>(B) * Hi, kb_elems, kQRows, sw);
-  if (e != cudaSuccess) return e;
-  const size_t smem = indexer_smem_bytes(Di);
-  e = cudaFuncSetAttribute(indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(indexer_smem_bytes(128)));
+  const size_t smem = indexer_smem_bytes(Di, fp8);
+  auto kernel = fp8 ? indexer_kernel<true> : indexer_kernel<false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(fp8 ? smem : indexer_smem_bytes(128)));
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (fewer when there are fewer tiles)
   const int64_t tiles_bound = (total_rows + kTileRows - 1) / kTileRows + B;
   const int grid = static_cast<int>(tiles_bound < device_sms() ? tiles_bound : device_sms());
-  IndexerParams p{w, sp, B, Hi, Di, scores, status, pdl ? wait_mode : 0, row_hist};
-  return launch_k(indexer_kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, kmap, qmap, p);
+  IndexerParams p{w, sp, B, Hi, Di, scores, status, pdl ? wait_mode : 0, row_hist, key_scale,
+                  static_cast<const uint16_t*>(iq)};
+  return launch_k(kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, kmap, qmap, p);
 }
 
 }  // namespace hsa

@@ -66,8 +66,17 @@ cudaError_t launch_compress(const void* kv, const void* z, const float* b, int64
 // 2-D bf16 tensor map (inner dimension contiguous) for TMA tiled loads.
 cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
                               int box_inner, int box_outer, CUtensorMapSwizzle swizzle);
+// The same over bytes (8-bit elements, e.g. E4M3 codes).
+cudaError_t make_tmap_2d_u8(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                            int box_inner, int box_outer, CUtensorMapSwizzle swizzle);
 
-size_t indexer_smem_bytes(int Di);
+// Per-row E4M3 quantization of an fp32 [rows, C] matrix (C a multiple of 4):
+// scale = amax / 448, code = e4m3(x * (448 / amax)), rounded to nearest even
+// and saturated; a zero row gets scale 0 and zero codes.
+cudaError_t launch_quantize_e4m3(const float* x, int64_t rows, int64_t C, uint8_t* codes,
+                                 float* scales, cudaStream_t stream);
+
+size_t indexer_smem_bytes(int Di, bool fp8 = false);
 // With pdl, wait_mode says where the kernel waits for the previous one: 0
 // every thread at the start; 1 the loads (the tile table is built before,
 // from sp, which the previous kernel must not write); 2 only the loads of a
@@ -77,10 +86,13 @@ size_t indexer_smem_bytes(int Di);
 // before its own wait).
 // row_hist (may be null): B x kRowHistBins counters to which every score
 // written adds one in the bin of its top kRowHistBits order-key bits.
+// key_scale non-null: keys are E4M3 codes [total_rows, Di] (Di = 128) with one
+// fp32 scale per row, and the kernel quantizes each (sequence, head) query
+// row of iq the same way (E4M3 tensor-core products, fp32 accumulation).
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
                            cudaStream_t stream, bool pdl = false, int wait_mode = 0,
-                           uint32_t* row_hist = nullptr);
+                           uint32_t* row_hist = nullptr, const float* key_scale = nullptr);
 
 size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k);
 // Leading bytes of a top-k workspace (status word, row states, histograms)

@@ -20,6 +20,8 @@
 //   a5 attend   window + top-k (C4) or all L/128 entries (C128)
 // a1 and a2 run in one small kernel (one CTA per sequence); a3-a5 are the
 // standalone kernels reading the live prefix of the capacity-laid-out pools.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "compress_core.cuh"
 #include "internal.h"
@@ -48,8 +50,11 @@ struct AppendParams {
   uint4* iz_ring;
   uint4* kv_pool;
   uint4* key_pool;
+  float* key_scale;  // non-null: key_pool holds E4M3 codes [rows, Di] with these fp32 scales
   uint32_t* status;
 };
+
+constexpr int kMaxKeyDi = 128;  // E4M3 key rows (one warp quantizes a row, 4 channels a lane)
 
 // Compresses the r-row ring block of width C (C/8 chunks) of sequence b into
 // `dst` (one bf16 row).  Rows are split over `split` adjacent lanes.
@@ -92,6 +97,7 @@ HSA_DEVINL void compress_block(const uint4* kv, const uint4* z, const float* bia
 constexpr int kShortBlock = 4;
 
 HSA_DEVINL void append_short(const AppendParams& p, int b) {
+  __shared__ float s_key[kMaxKeyDi];  // E4M3 pool: the completed block's fp32 key row
   const int cq = p.Dqk / 8, ci = p.kind == HSA_LAYER_C4 ? p.Di / 8 : 0;
   const int r = p.r;
   const int32_t lin = p.seq_len_in[b];
@@ -161,10 +167,40 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
       }
       o[ch] = acc / l;
     }
+    if (key && p.key_scale) {  // E4M3 pool: quantized below, once the whole row is here
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) s_key[c * 8 + ch] = o[ch];
+      continue;
+    }
     uint4* dst = key ? p.key_pool : p.kv_pool;
     dst[(o0 + n) * n8 + c] = f32x8_to_bf16(o);
   }
   __syncthreads();  // every thread has read seq_len_in before it may be overwritten
+  const int64_t Lw = static_cast<int64_t>(lin) + 1;
+  if (p.key_scale && threadIdx.x < 32 && Lw % r == 0) {
+    // warp 0 quantizes the completed block's key row: amax over the row, then
+    // 4 channels a lane
+    const int64_t n = Lw / r - 1;
+    if (!(o0 < 0 || o1 > p.pool_total_rows || o0 + n >= o1)) {
+      const int lane = threadIdx.x;
+      const bool live = 4 * lane < p.Di;
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = live ? s_key[4 * lane + i] : 0.f;
+      float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const float inv = am > 0.f ? __fdiv_rn(448.f, am) : 0.f;
+      const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+          make_float2(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv)), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+          make_float2(__fmul_rn(v[2], inv), __fmul_rn(v[3], inv)), __NV_SATFINITE, __NV_E4M3);
+      if (live)
+        reinterpret_cast<uint32_t*>(p.key_pool)[((o0 + n) * p.Di) / 4 + lane] =
+            static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      if (lane == 0) p.key_scale[o0 + n] = __fdiv_rn(am, 448.f);
+    }
+  }
   if (threadIdx.x == 0) p.seq_len_out[b] = lin + 1;
 }
 
@@ -300,6 +336,7 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   ap.iz_ring = static_cast<uint4*>(d.iz_ring);
   ap.kv_pool = static_cast<uint4*>(d.kv_pool);
   ap.key_pool = static_cast<uint4*>(d.key_pool);
+  ap.key_scale = d.kind == HSA_LAYER_C4 && d.key_fp8 ? d.key_scale : nullptr;
   ap.status = status;
   auto mark = [&](int i) -> cudaError_t {
     return d.stage_events ? cudaEventRecord(static_cast<cudaEvent_t>(d.stage_events[i]), stream)
@@ -329,7 +366,8 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
     const bool fused = layer_fused(d);
     uint32_t* hist = fused ? reinterpret_cast<uint32_t*>(w + L.hist) : nullptr;
     e = launch_indexer(d.iq, d.w, d.key_pool, alias ? sp : sp_in, d.B, d.Hi, d.Di,
-                       d.pool_total_rows, scores, status, stream, true, alias ? 0 : 2, hist);
+                       d.pool_total_rows, scores, status, stream, true, alias ? 0 : 2, hist,
+                       d.key_fp8 ? d.key_scale : nullptr);
     if (e != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
     if (fused) {

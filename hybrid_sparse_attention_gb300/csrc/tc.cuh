@@ -173,6 +173,18 @@ HSA_DEVINL void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint
       : "memory");
 }
 
+// D (+)= A . B^T for 8-bit floating-point operands (kind::f8f6f4; the types
+// are named in the instruction descriptor), fp32 accumulation in TMEM.
+HSA_DEVINL void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
 HSA_DEVINL void mma_commit(uint64_t* bar) {
@@ -304,6 +316,16 @@ HSA_HOST_DEVICE uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = fals
          | (1u << 10)                     // B format: bf16
          | (a_mn ? 1u << 15 : 0u)         // A major-ness
          | (b_mn ? 1u << 16 : 0u)         // B major-ness
+         | ((N >> 3) << 17)               // N / 8
+         | ((M >> 4) << 24);              // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0),
+// fp32 D, both operands K-major.
+HSA_HOST_DEVICE uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)                        // D format: f32
+         | (0u << 7)                      // A format: E4M3
+         | (0u << 10)                     // B format: E4M3
          | ((N >> 3) << 17)               // N / 8
          | ((M >> 4) << 24);              // M / 16
 }

@@ -203,6 +203,7 @@ class LayerState:
     iz_new: torch.Tensor = None     # [B, Di]      (C4)
     iq: torch.Tensor = None         # [B, Hi, Di]  (C4)
     w: torch.Tensor = None          # fp32 [B, Hi] (C4)
+    key_scale: torch.Tensor = None  # fp32 [cap] when key_pool holds E4M3 codes (uint8 [cap, Di])
     extra: dict = field(default_factory=dict)
 
     def tensors(self):

@@ -121,6 +121,39 @@ hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys
                                 void* stream);
 
 /* ------------------------------------------------------------------------
+ * E4M3 storage of the indexer-key pool — the pages speak of FP8 rollout
+ * ([LH] §Hỗ trợ Học tăng cường) and of a 1M-token KV cache under 10 GB ([WK]
+ * §DeepSeek V4 的新架构) without fixing a format; the library's format is
+ * one row of E4M3 codes ("e4m3fn": bias 7, 3 mantissa bits, largest finite
+ * 448, no infinities) with one fp32 scale per row, value = scale * code.
+ *
+ * hsa_quantize_e4m3: per row of x, amax = max |x|, scales[i] = amax / 448 and
+ * codes[i, d] = e4m3(x[i, d] * (448 / amax)), rounded to nearest even and
+ * saturated at +-448, every step in binary32; a zero row gets scale 0 and
+ * zero codes (a NaN entry gives the NaN code; rows are otherwise finite).
+ *   x : fp32 [rows, C]   codes : u8 [rows, C]   scales : fp32 [rows]
+ * Requirements: rows >= 0; C a positive multiple of 4; x 16-byte aligned,
+ * codes 4-byte aligned.  One launch, no workspace.
+ *
+ * hsa_indexer_scores_e4m3: the indexer scores over an E4M3 key pool, on the
+ * dequantized operands: each query row iq[b, h, :] is quantized as above
+ * inside the kernel (qhat = sq * code), khat[j] = key_scales[j] * keys[j], and
+ *   scores[j] = sum_{h<Hi} w[b, h] * max(0, qhat[b, h, :] . khat[j, :])
+ * computed as key_scales[j] * sum_h (w[b, h] sq[b, h]) max(0, codes . codes):
+ * E4M3 tensor-core products (tcgen05 kind::f8f6f4), fp32 accumulation.
+ *   iq : bf16 [B, Hi, Di]   w : fp32 [B, Hi]   keys : u8 [total_rows, Di]
+ *   key_scales : fp32 [total_rows]   offsets : int64 [B+1]   scores : fp32 [total_rows]
+ * Requirements as hsa_indexer_scores, with Di = 128; keys 16-byte aligned.
+ * Workspace: hsa_indexer_scores_workspace_size() bytes.
+ * ---------------------------------------------------------------------- */
+hsa_status_t hsa_quantize_e4m3(const float* x, int64_t rows, int64_t C, uint8_t* codes,
+                               float* scales, void* stream);
+hsa_status_t hsa_indexer_scores_e4m3(const void* iq, const float* w, const uint8_t* keys,
+                                     const float* key_scales, const int64_t* offsets, int64_t B,
+                                     int64_t Hi, int64_t Di, int64_t total_rows, float* scores,
+                                     void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Lightning TopK — [KD] §Arquitectura del Sistema (radix-select reduction in
  * place of a global sort for the indexer's top-k); [WK] §推理侧优化, Lightning
  * topk.
@@ -299,6 +332,12 @@ typedef struct hsa_layer_desc {
                                run — [KD] §Arquitectura del Sistema (multi-stream overlap).
                                The attention is then launched without programmatic
                                dependent launch. */
+  int32_t key_fp8;          /* (C4) 0: key_pool holds bf16 rows; 1: key_pool holds E4M3
+                               codes u8 [pool_total_rows, Di] with key_scale (Di = 128):
+                               step 2 quantizes the completed block's fp32 key as
+                               hsa_quantize_e4m3 does and step 3 is
+                               hsa_indexer_scores_e4m3 */
+  float* key_scale;         /* fp32 [pool_total_rows] when key_fp8, else ignored */
 } hsa_layer_desc;
 
 size_t hsa_layer_decode_workspace_size(const hsa_layer_desc* d);

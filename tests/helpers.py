@@ -42,6 +42,7 @@ def np_state(st):
     out = {k: (bf16_bits(v) if v.dtype == torch.bfloat16 else v.detach().cpu().numpy().copy())
            for k, v in st.tensors().items()}
     out.update(kind=st.kind, ratio=st.ratio, Dv=st.shape.Dv, k=st.shape.k, scale=st.shape.scale)
+    out["key_fp8"] = getattr(st, "key_scale", None) is not None
     return out
 
 
