@@ -44,6 +44,7 @@ SIGNATURES = {
     "hsa_topk": (I32, [P, P, I64, I64, I64, P, P, P, SZ, P]),
     "hsa_topk_noalloc": (I32, [P, P, I64, I64, I64, P, P, P]),
     "hsa_quantize_e4m3": (I32, [P, I64, I64, P, P, P]),
+    "hsa_set_wait_limit": (I32, [ctypes.c_uint64, ctypes.c_uint32]),
     "hsa_indexer_scores_e4m3": (I32, [P, P, P, P, P, I64, I64, I64, I64, P, P, SZ, P]),
 }
 
@@ -180,6 +181,11 @@ def hsa_indexer_scores_e4m3(iq, w, keys, key_scales, offsets, scores=None, ws=No
           _dev(scores, torch.float32, "scores"), _dev(ws, torch.uint8, "ws"), ws.numel(),
           _stream(stream))
     return scores
+
+
+def hsa_set_wait_limit(nanos: int = 0, polls: int = 0) -> None:
+    """Bound of the indexer kernels' pipeline waits for later launches (0: default)."""
+    _call("hsa_set_wait_limit", int(nanos), int(polls))
 
 
 def hsa_topk_workspace_size(B: int, total_rows: int, k: int) -> int:

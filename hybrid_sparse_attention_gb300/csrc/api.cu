@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -86,6 +87,16 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
 }
 
 }  // namespace
+
+namespace {
+constexpr uint64_t kDefaultWaitNs = 200ull * 1000 * 1000;  // 200 ms
+constexpr uint32_t kDefaultWaitPolls = 1u << 24;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<uint32_t> g_wait_polls{kDefaultWaitPolls};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+uint32_t wait_limit_polls() { return g_wait_polls.load(std::memory_order_relaxed); }
 
 cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
                               int box_inner, int box_outer, CUtensorMapSwizzle swizzle) {
@@ -189,6 +200,12 @@ hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys
                                     static_cast<int>(Di), total_rows, scores,
                                     static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream)),
                      "indexer launch");
+}
+
+hsa_status_t hsa_set_wait_limit(uint64_t nanos, uint32_t polls) {
+  g_wait_ns.store(nanos == 0 ? kDefaultWaitNs : nanos, std::memory_order_relaxed);
+  g_wait_polls.store(polls == 0 ? kDefaultWaitPolls : polls, std::memory_order_relaxed);
+  return HSA_OK;
 }
 
 hsa_status_t hsa_quantize_e4m3(const float* x, int64_t rows, int64_t C, uint8_t* codes,

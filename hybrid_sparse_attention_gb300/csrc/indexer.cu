@@ -44,9 +44,12 @@ namespace {
 
 constexpr int kTileRows = 128;  // M
 constexpr int kQRows = 16;      // N (heads, padded)
-constexpr int kStagesBf16 = 6;  // 36 KB stages (keys + queries)
-constexpr int kStagesFp8 = 12;  // 16 KB stages (keys): as many key bytes in flight
-constexpr int kMaxStages = 12;
+constexpr int kStagesBf16 = 6;  // 36 KB stages (keys + queries), one CTA per SM
+// 16 KB stages (keys), two CTAs per SM: the E4M3 stream is bound by a per-CTA
+// tile rate (more stages, larger boxes or fewer MMAs per tile measured no
+// faster; a second CTA per SM did: 54 -> 42 us over 1.18 M keys)
+constexpr int kStagesFp8 = 6;
+constexpr int kMaxStages = 6;
 constexpr int kFp8Di = 128;     // E4M3 keys: one 128-byte swizzle row per entry
 constexpr uint32_t kQ8Bytes = kQRows * kFp8Di;  // one sequence's E4M3 query rows
 constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
@@ -65,6 +68,8 @@ struct IndexerParams {
   uint32_t* row_hist;  // per-sequence order-key histograms for the top-k (may be null)
   const float* key_scale;  // E4M3 keys: fp32 [total_rows]
   const uint16_t* iq;      // E4M3 keys: the bf16 queries [B, Hi, Di], quantized in the kernel
+  uint64_t spin_ns;        // a pipeline wait gives up after this long ...
+  uint32_t spin_polls;     // ... or this many polls (then HSA_DEV_TIMEOUT and the abort)
 };
 
 struct Shared {
@@ -79,20 +84,20 @@ struct Shared {
   int b0, first0;  // sequence owning this CTA's first tile, and its first tile
 };
 
-// Bounded wait that also gives up when another role has aborted.
-HSA_DEVINL bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity, uint32_t* status) {
-  if (tc::mbar_try_wait(bar, parity)) return true;
+// Bounded wait of a pipeline role that also gives up when another role has
+// aborted: after p.spin_polls failed checks (the first a non-blocking test) or
+// p.spin_ns nanoseconds it sets HSA_DEV_TIMEOUT and the shared abort flag.
+HSA_DEVINL bool wait_or_abort(Shared& sh, uint64_t* bar, uint32_t parity, const IndexerParams& p) {
+  if (tc::mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = tc::global_timer();
-  for (uint32_t i = 0;; ++i) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 63u) {
-      if (*reinterpret_cast<volatile int*>(&sh.abort)) return false;
-      if (tc::global_timer() - t0 > tc::kSpinNanos || i > tc::kSpinPolls) {
-        set_status(status, HSA_DEV_TIMEOUT);
-        *reinterpret_cast<volatile int*>(&sh.abort) = 1;
-        return false;
-      }
+  for (uint32_t i = 1;; ++i) {
+    if (*reinterpret_cast<volatile int*>(&sh.abort)) return false;
+    if (i >= p.spin_polls || tc::global_timer() - t0 > p.spin_ns) {
+      set_status(p.status, HSA_DEV_TIMEOUT);
+      *reinterpret_cast<volatile int*>(&sh.abort) = 1;
+      return false;
     }
+    if (tc::mbar_try_wait(bar, parity)) return true;
   }
 }
 
@@ -194,7 +199,7 @@ HSA_DEVINL void quantize_queries(const IndexerParams& p, Shared& sh, uint8_t* q8
 }
 
 template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap qmap,
                                                              IndexerParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
       // histograms written here stay for the top-k that reads them next
       const uint64_t keys_policy = tc::l2_policy_evict_first();
       int dep = -1;  // (wait_mode 2) tile that must wait for the previous kernel
+      int issued = 0;
       for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
         const int s = i % kStages;
         // before the wait: a new sequence's loads overlap it
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
           waited = true;
         }
         if (i >= kStages &&
-            !wait_or_abort(sh, &sh.empty[s], ((i / kStages) & 1) ^ 1, p.status))
+            !wait_or_abort(sh, &sh.empty[s], ((i / kStages) & 1) ^ 1, p))
           break;
         const int b = cur.b;
         const int64_t row0 = cur.start + static_cast<int64_t>(t - cur.first) * kTileRows;
@@ -320,7 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
             tc::tma_load_2d(st + nkb * a_kb + kb * b_kb, &qmap, kb * kb_elems, b * p.Hi,
                             &sh.full[s]);
         }
+        issued = i + 1;
       }
+      // Every load issued lands in this CTA's shared memory before the CTA may
+      // exit: after an abort the MMA may not have waited for the last stages.
+      // (Only the last kStages can be outstanding; each stage's barrier is then
+      // at most one phase behind.  The default bound: these loads do complete.)
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+        tc::mbar_wait(&sh.full[j % kStages], (j / kStages) & 1, p.status);
       if (!waited) pdl_wait();  // the grid completes only after the previous kernel
     }
   } else if (warp == 1) {
@@ -336,10 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
         const int s = i % kStages, a = i % kAcc;
         if (kFp8 && mc.seek(sh, p, t)) {
           ++ord;
-          if (!wait_or_abort(sh, &sh.q8_full[ord & 1], (ord >> 1) & 1, p.status)) break;
+          if (!wait_or_abort(sh, &sh.q8_full[ord & 1], (ord >> 1) & 1, p)) break;
         }
-        if (!wait_or_abort(sh, &sh.full[s], (i / kStages) & 1, p.status)) break;
-        if (i >= kAcc && !wait_or_abort(sh, &sh.acc_empty[a], ((i / kAcc) & 1) ^ 1, p.status))
+        if (!wait_or_abort(sh, &sh.full[s], (i / kStages) & 1, p)) break;
+        if (i >= kAcc && !wait_or_abort(sh, &sh.acc_empty[a], ((i / kAcc) & 1) ^ 1, p))
           break;
         tc::fence_after_sync();
         const uint32_t sa = tc::smem_u32(smem + s * stage_bytes);
@@ -401,16 +414,34 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
     // walking the tiles so that every epilogue thread reaches the same named
     // barriers, where the warps agree on the abort.
     bool dead = false;
-    // (kFp8, wait_mode 2) the key scale of a row the previous kernel may have
-    // just written is read only after the wait for that kernel, as the
-    // producer loads that row's codes
+    // (kFp8) this thread's key scales of the next kPf tiles, loaded kPf tiles
+    // ahead (a DRAM round trip per tile would otherwise bound the loop).  With
+    // wait_mode 2 the scale of a row the previous kernel may have just written
+    // is read only after the wait for that kernel, as the producer loads that
+    // row's codes.
+    constexpr int kPf = 4;
+    float ksr[kPf];
+    SeqCursor pc;
     bool ewaited = !kFp8 || p.wait_mode != 2;
-    int edep = -1;
+    int pdep = -1;
+    auto fetch_scale = [&](int tt) -> float {
+      if (tt >= t_end) return 0.f;
+      if (pc.seek(sh, p, tt) && !ewaited) pdep = pc.appended_tile(p);
+      if (!ewaited && tt == pdep) {
+        pdl_wait();
+        ewaited = true;
+      }
+      const int64_t pp = tt - pc.first;
+      return r < pc.count - pp * kTileRows ? p.key_scale[pc.start + pp * kTileRows + r] : 0.f;
+    };
+    if (kFp8) {
+#pragma unroll
+      for (int j = 0; j < kPf; ++j) ksr[j] = fetch_scale(t_begin + j);
+    }
     for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
       const int a = i % kAcc;
       if (cur.seek(sh, p, t)) {
         ++ord;
-        if (!ewaited) edep = cur.appended_tile(p);
         if (!kFp8) {
 #pragma unroll
           for (int h = 0; h < kQRows; ++h)
@@ -420,12 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_kernel(const __grid_const
       const int64_t piece = t - cur.first;
       const int64_t left = cur.count - piece * kTileRows;
       const int64_t row = cur.start + piece * kTileRows + r;
-      if (!ewaited && t == edep) {
-        pdl_wait();
-        ewaited = true;
+      float ks = 1.f;
+      if (kFp8) {
+        ks = ksr[0];
+#pragma unroll
+        for (int j = 0; j + 1 < kPf; ++j) ksr[j] = ksr[j + 1];
+        ksr[kPf - 1] = dead ? 0.f : fetch_scale(t + kPf);
       }
-      const float ks = kFp8 && !dead && r < left ? p.key_scale[row] : 1.f;
-      if (!dead) dead = !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.acc_full[a], (i / kAcc) & 1, p.status));
+      if (!dead) dead = !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.acc_full[a], (i / kAcc) & 1, p));
       if (dead && !kFp8) break;
       if (!dead) {
       if (kFp8) {
@@ -517,11 +550,12 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(fp8 ? smem : indexer_smem_bytes(128)));
   if (e != cudaSuccess) return e;
-  // persistent: one CTA per SM (fewer when there are fewer tiles)
+  // persistent: one CTA per SM (E4M3: two), fewer when there are fewer tiles
   const int64_t tiles_bound = (total_rows + kTileRows - 1) / kTileRows + B;
-  const int grid = static_cast<int>(tiles_bound < device_sms() ? tiles_bound : device_sms());
+  const int nres = (fp8 ? 2 : 1) * device_sms();
+  const int grid = static_cast<int>(tiles_bound < nres ? tiles_bound : nres);
   IndexerParams p{w, sp, B, Hi, Di, scores, status, pdl ? wait_mode : 0, row_hist, key_scale,
-                  static_cast<const uint16_t*>(iq)};
+                  static_cast<const uint16_t*>(iq), wait_limit_ns(), wait_limit_polls()};
   return launch_k(kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, kmap, qmap, p);
 }
 

@@ -23,6 +23,11 @@ hsa_status_t set_error_detail(hsa_status_t s, const char* detail);
 // Streaming multiprocessors of the current device (cached per device).
 int device_sms();
 
+// The bound on a kernel's pipeline waits (hsa_set_wait_limit; process-wide):
+// nanoseconds and polls after which a wait gives up with HSA_DEV_TIMEOUT.
+uint64_t wait_limit_ns();
+uint32_t wait_limit_polls();
+
 // Kernel launch; with pdl, the kernel may be scheduled while the previous
 // kernel of the stream is still running (it waits for it in pdl_wait).  With
 // cluster > 0, consecutive groups of `cluster` CTAs (along x) form thread-block

@@ -148,6 +148,20 @@ hsa_status_t hsa_indexer_scores(const void* iq, const float* w, const void* keys
  * ---------------------------------------------------------------------- */
 hsa_status_t hsa_quantize_e4m3(const float* x, int64_t rows, int64_t C, uint8_t* codes,
                                float* scales, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Bounded waits.  Every spin of a kernel on a barrier gives up after a bound
+ * (default 2^24 polls or 200 ms), sets HSA_DEV_TIMEOUT in the workspace's
+ * status word and stops the kernel: each role leaves its loop, the copies and
+ * tensor-core operations already issued are waited for (with the default
+ * bound), TMEM is freed and the kernel returns, so the stream and the context
+ * stay usable.  hsa_set_wait_limit sets the bound of the indexer kernels'
+ * pipeline waits for every later launch in the process (nanos and polls, the
+ * first check being a non-blocking test; 0 restores the default of either) so
+ * that the abort path can be exercised: with polls = 1 a wait whose phase is
+ * not complete at its first check runs out.  Always returns HSA_OK.
+ * ---------------------------------------------------------------------- */
+hsa_status_t hsa_set_wait_limit(uint64_t nanos, uint32_t polls);
 hsa_status_t hsa_indexer_scores_e4m3(const void* iq, const float* w, const uint8_t* keys,
                                      const float* key_scales, const int64_t* offsets, int64_t B,
                                      int64_t Hi, int64_t Di, int64_t total_rows, float* scores,
