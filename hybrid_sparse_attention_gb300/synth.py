@@ -204,6 +204,10 @@ class LayerState:
     iq: torch.Tensor = None         # [B, Hi, Di]  (C4)
     w: torch.Tensor = None          # fp32 [B, Hi] (C4)
     key_scale: torch.Tensor = None  # fp32 [cap] when key_pool holds E4M3 codes (uint8 [cap, Di])
+    T: int = 1                      # query tokens per sequence and step; with T > 1 the
+                                    # per-token tensors (q, kv_new, z_new, ik_new, iz_new,
+                                    # iq, w) have a token axis after the batch axis and the
+                                    # window ring holds W + T - 1 rows
     extra: dict = field(default_factory=dict)
 
     def tensors(self):
@@ -270,36 +274,40 @@ def _ring_from_history(t: torch.Tensor, start: int, end: int, r: int) -> torch.T
 
 
 def filled_state(seed: int, kind: int, shape: LayerShape, L: torch.Tensor, device="cpu",
-                 name: str = "c4layer") -> LayerState:
-    """A batch of sequences at context lengths L (tokens after this step) whose
-    pools, rings and SWA windows are filled directly with N(0,1) bf16 values
-    (the large workloads: no history is compressed)."""
+                 name: str = "c4layer", T: int = 1) -> LayerState:
+    """A batch of sequences at context lengths L (tokens after this step, which
+    appends T tokens) whose pools, rings and SWA windows are filled directly
+    with N(0,1) bf16 values (the large workloads: no history is compressed).
+    With T > 1 the per-token inputs get a token axis and the window ring
+    W + T - 1 rows; T = 1 draws exactly what it always drew."""
     r = kind
     D, Di, W = shape.Dqk, shape.Di, shape.W
     B = L.numel()
-    Lin = (L.to(torch.int64) - 1)
+    Lin = (L.to(torch.int64) - T)
     counts = (L.to(torch.int64) // r)
     offs = capacity_offsets(counts.tolist(), slack=1)
     cap = int(offs[-1])
+    tk = (B,) if T == 1 else (B, T)          # leading axes of the per-token inputs
+    sfx = "" if T == 1 else f".t{T}"
     st = LayerState(
         kind=kind, ratio=r, shape=shape,
         seq_len_in=Lin.to(torch.int32).to(device),
         pool_offsets=offs.to(device),
-        swa=normal_bf16(seed, f"{name}.swa", (B, W, D), device=device),
+        swa=normal_bf16(seed, f"{name}.swa", (B, W + T - 1, D), device=device),
         kv_ring=normal_bf16(seed, f"{name}.kv_ring", (B, r, D), device=device),
         z_ring=normal_bf16(seed, f"{name}.z_ring", (B, r, D), device=device),
         kv_pool=normal_bf16(seed, f"{name}.kv_pool", (cap, D), device=device),
         b_kv=normal(seed, f"{name}.b_kv", (r, D), std=0.5, device=device),
-        kv_new=normal_bf16(seed, f"{name}.kv_new", (B, D), device=device),
-        z_new=normal_bf16(seed, f"{name}.z_new", (B, D), device=device),
-        q=normal_bf16(seed, f"{name}.q", (B, shape.Hq, D), device=device))
+        kv_new=normal_bf16(seed, f"{name}.kv_new{sfx}", tk + (D,), device=device),
+        z_new=normal_bf16(seed, f"{name}.z_new{sfx}", tk + (D,), device=device),
+        q=normal_bf16(seed, f"{name}.q{sfx}", tk + (shape.Hq, D), device=device), T=T)
     if kind == 4:
         st.ik_ring = normal_bf16(seed, f"{name}.ik_ring", (B, r, Di), device=device)
         st.iz_ring = normal_bf16(seed, f"{name}.iz_ring", (B, r, Di), device=device)
         st.key_pool = normal_bf16(seed, f"{name}.key_pool", (cap, Di), device=device)
         st.b_ik = normal(seed, f"{name}.b_ik", (r, Di), std=0.5, device=device)
-        st.ik_new = normal_bf16(seed, f"{name}.ik_new", (B, Di), device=device)
-        st.iz_new = normal_bf16(seed, f"{name}.iz_new", (B, Di), device=device)
-        st.iq = normal_bf16(seed, f"{name}.iq", (B, shape.Hi, Di), device=device)
-        st.w = uniform(seed, f"{name}.w", (B, shape.Hi), device=device)
+        st.ik_new = normal_bf16(seed, f"{name}.ik_new{sfx}", tk + (Di,), device=device)
+        st.iz_new = normal_bf16(seed, f"{name}.iz_new{sfx}", tk + (Di,), device=device)
+        st.iq = normal_bf16(seed, f"{name}.iq{sfx}", tk + (shape.Hi, Di), device=device)
+        st.w = uniform(seed, f"{name}.w{sfx}", tk + (shape.Hi,), device=device)
     return st

@@ -245,6 +245,18 @@ def compact(pool, pool_offsets, counts):
     return rows.reshape(-1, width), offs
 
 
+def _window_ring(swa, L, W):
+    """The last W positions of each sequence (positions [max(0, L-W), L)) from a
+    ring of any size Wr >= W (slot = position mod Wr), re-laid as a ring of W
+    slots (slot = position mod W): data movement only."""
+    B, Wr, D = swa.shape
+    out = np.zeros((B, W, D), swa.dtype)
+    for b in range(B):
+        for p in range(max(0, int(L[b]) - W), int(L[b])):
+            out[b, p % W] = swa[b, p % Wr]
+    return out
+
+
 def layer_decode(st: dict, threads: int = 1) -> dict:
     """One decode step of one hybrid layer, composed from the four stages.
 
@@ -252,63 +264,100 @@ def layer_decode(st: dict, threads: int = 1) -> dict:
     compress once a 4- / 128-token block is complete, C4 picks its top-k entries
     and then attends them; [KD] flow steps 3, 5 and 6):
 
-      a1 append the new token's rows into the SWA ring (slot (L-1) mod W) and the
-         in-flight block rings (slot (L-1) mod r), L = seq_len_in + 1;
-      a2 if L mod r == 0, compress the completed block into pool row L/r - 1
-         (compressor output rounded fp64 -> fp32 -> bf16, as stored; with an
-         E4M3 key pool (``st["key_fp8"]``) the indexer key is rounded to fp32
-         and quantized per row into ``key_pool`` codes and ``key_scale``);
-      a3 (C4) indexer scores over the sequence's L/4 entries, rounded to fp32;
+      a1 append the new tokens' rows, in order, into the SWA ring (slot p mod
+         Wr) and the in-flight block rings (slot p mod r), p = L_in + t;
+      a2 when a token completes a block ((p + 1) mod r == 0), compress the block
+         into pool row (p + 1)/r - 1 (compressor output rounded fp64 -> fp32
+         -> bf16, as stored; with an E4M3 key pool (``st["key_fp8"]``) the
+         indexer key is rounded to fp32 and quantized per row into
+         ``key_pool`` codes and ``key_scale``);
+      a3 (C4) for each query token t (length L_t = L_in + t + 1), indexer
+         scores over its L_t/4 entries, rounded to fp32;
       a4 (C4) top-k of those scores;
-      a5 attention over the SWA window and the selected (C4) or all (C128) rows.
+      a5 attention of token t over its window (positions [L_t - W, L_t)) and
+         its selected (C4) or all (C128) rows.
+
+    ``st["T"]`` (default 1) query tokens per sequence — T = 2 is one step of
+    speculative decoding with a one-layer multi-token-prediction head ([LH]
+    §Tích hợp Kernel và Giải mã suy đoán): the current token and a draft
+    token, verified together.  Token t sees exactly what it would see had the
+    tokens been decoded one per step (its own and earlier positions only); the
+    window ring holds Wr = W + T - 1 rows so that the first token's oldest
+    window row survives the later appends.  With T > 1 the per-token inputs
+    carry a token axis after the batch axis (q [B, T, Hq, Dqk], kv_new
+    [B, T, Dqk], iq [B, T, Hi, Di], w [B, T, Hi], ...) and so do the outputs.
 
     ``st`` holds numpy arrays (see the keys read below); the rings and pools in
     it are updated in place.  Returns the stage outputs.
     """
     kind, r = st["kind"], st["ratio"]
+    T = int(st.get("T", 1))
     B = st["seq_len_in"].shape[0]
-    W = st["swa"].shape[1]
-    L = st["seq_len_in"].astype(np.int64) + 1
+    Wr = st["swa"].shape[1]
+    W = int(st.get("W", Wr - (T - 1)))
+    assert Wr >= W + T - 1, "the window ring needs W + T - 1 rows"
+    Lin = st["seq_len_in"].astype(np.int64)
+    L = Lin + T
     Dv = st["Dv"]
+
+    def tok(name, t):
+        a = st[name]
+        return a if T == 1 else a[:, t]
+
     out = {"seq_len_out": L.astype(np.int32)}
-    for b in range(B):
-        st["swa"][b, (L[b] - 1) % W] = st["kv_new"][b]
-        st["kv_ring"][b, (L[b] - 1) % r] = st["kv_new"][b]
-        st["z_ring"][b, (L[b] - 1) % r] = st["z_new"][b]
-        if kind == C4:
-            st["ik_ring"][b, (L[b] - 1) % r] = st["ik_new"][b]
-            st["iz_ring"][b, (L[b] - 1) % r] = st["iz_new"][b]
     offs = st["pool_offsets"]
-    for b in range(B):
-        if L[b] % r != 0:
-            continue
-        n = L[b] // r - 1
-        assert offs[b] + n < offs[b + 1], "pool capacity exceeded"
-        c = compress(st["kv_ring"][b:b + 1], st["z_ring"][b:b + 1], st["b_kv"], r, threads)
-        st["kv_pool"][offs[b] + n] = float_to_bf16(c.astype(np.float32)).reshape(-1)
+    for t in range(T):
+        for b in range(B):
+            p = int(Lin[b]) + t
+            st["swa"][b, p % Wr] = tok("kv_new", t)[b]
+            st["kv_ring"][b, p % r] = tok("kv_new", t)[b]
+            st["z_ring"][b, p % r] = tok("z_new", t)[b]
+            if kind == C4:
+                st["ik_ring"][b, p % r] = tok("ik_new", t)[b]
+                st["iz_ring"][b, p % r] = tok("iz_new", t)[b]
+            if (p + 1) % r != 0:
+                continue
+            n = (p + 1) // r - 1
+            assert offs[b] + n < offs[b + 1], "pool capacity exceeded"
+            c = compress(st["kv_ring"][b:b + 1], st["z_ring"][b:b + 1], st["b_kv"], r, threads)
+            st["kv_pool"][offs[b] + n] = float_to_bf16(c.astype(np.float32)).reshape(-1)
+            if kind == C4:
+                ck = compress(st["ik_ring"][b:b + 1], st["iz_ring"][b:b + 1], st["b_ik"], r,
+                              threads)
+                if st.get("key_fp8"):
+                    codes, sc = quantize_e4m3(ck.astype(np.float32).reshape(1, -1))
+                    st["key_pool"][offs[b] + n] = codes[0]
+                    st["key_scale"][offs[b] + n] = sc[0]
+                else:
+                    st["key_pool"][offs[b] + n] = float_to_bf16(ck.astype(np.float32)).reshape(-1)
+    res = []
+    for t in range(T):
+        Lt = Lin + t + 1
+        counts = Lt // r
+        kv_rows, kv_offs = compact(st["kv_pool"], offs, counts)
+        rt = {}
+        idx = None
         if kind == C4:
-            ck = compress(st["ik_ring"][b:b + 1], st["iz_ring"][b:b + 1], st["b_ik"], r, threads)
+            key_rows, key_offs = compact(st["key_pool"], offs, counts)
             if st.get("key_fp8"):
-                codes, sc = quantize_e4m3(ck.astype(np.float32).reshape(1, -1))
-                st["key_pool"][offs[b] + n] = codes[0]
-                st["key_scale"][offs[b] + n] = sc[0]
+                ksc, _ = compact(st["key_scale"].reshape(-1, 1), offs, counts)
+                s64 = indexer_scores_e4m3(tok("iq", t), tok("w", t), key_rows, ksc.reshape(-1),
+                                          key_offs, threads)
             else:
-                st["key_pool"][offs[b] + n] = float_to_bf16(ck.astype(np.float32)).reshape(-1)
-    counts = L // r
-    kv_rows, kv_offs = compact(st["kv_pool"], offs, counts)
-    idx = None
-    if kind == C4:
-        key_rows, key_offs = compact(st["key_pool"], offs, counts)
-        if st.get("key_fp8"):
-            ksc, _ = compact(st["key_scale"].reshape(-1, 1), offs, counts)
-            s64 = indexer_scores_e4m3(st["iq"], st["w"], key_rows, ksc.reshape(-1), key_offs,
-                                      threads)
-        else:
-            s64 = indexer_scores(st["iq"], st["w"], key_rows, key_offs, threads)
-        s32 = s64.astype(np.float32)
-        idx, vals = topk(s32, key_offs, st["k"], threads)
-        out.update(scores64=s64, scores=s32, score_offsets=key_offs, idx=idx, vals=vals)
-    o, lse = decode_attn(st["q"], st["swa"], L.astype(np.int32), W, kv_rows, kv_offs, idx,
-                         st["scale"], Dv, threads)
-    out.update(out=o, lse=lse)
+                s64 = indexer_scores(tok("iq", t), tok("w", t), key_rows, key_offs, threads)
+            s32 = s64.astype(np.float32)
+            idx, vals = topk(s32, key_offs, st["k"], threads)
+            rt.update(scores64=s64, scores=s32, score_offsets=key_offs, idx=idx, vals=vals)
+        ring = st["swa"] if Wr == W else _window_ring(st["swa"], Lt, W)
+        o, lse = decode_attn(tok("q", t), ring, Lt.astype(np.int32), W, kv_rows, kv_offs, idx,
+                             st["scale"], Dv, threads)
+        rt.update(out=o, lse=lse)
+        res.append(rt)
+    if T == 1:
+        out.update(res[0])
+    else:
+        out["tokens"] = res
+        for key in ("out", "lse", "idx"):
+            if key in res[0]:
+                out[key] = np.stack([rt[key] for rt in res], axis=1)
     return out

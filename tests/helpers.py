@@ -43,6 +43,8 @@ def np_state(st):
            for k, v in st.tensors().items()}
     out.update(kind=st.kind, ratio=st.ratio, Dv=st.shape.Dv, k=st.shape.k, scale=st.shape.scale)
     out["key_fp8"] = getattr(st, "key_scale", None) is not None
+    out["T"] = getattr(st, "T", 1)
+    out["W"] = st.shape.W
     return out
 
 

@@ -545,3 +545,51 @@ def test_layer_step_e4m3_key_pool_matches_bulk_compression_of_history(oracle_mod
     assert np.array_equal(s["key_pool"][:n], bc) and np.array_equal(s["key_scale"][:n], bs)
     want = oracle_mod.indexer_scores_e4m3(s["iq"], s["w"], bc, bs, np.array([0, n], np.int64))
     assert np.array_equal(res["scores64"], want)
+
+
+# ---------------------------------------------------------------- multi-token queries
+
+@pytest.mark.parametrize("kind,phase", [(4, 0), (4, 1), (4, 2), (4, 3),
+                                        (128, 0), (128, 1), (128, 2), (128, 64)])
+def test_layer_two_token_step_equals_two_single_token_steps(oracle_mod, kind, phase):
+    """A step with T = 2 query tokens (the current token and a draft token of
+    speculative decoding, verified together) gives each token exactly what
+    decoding the two tokens one per step gives it: outputs, log-sum-exps,
+    scores and selections, and the same pools and rings afterwards.  The
+    phases put a block completion on the first token, on the second, or on
+    neither."""
+    shape = synth.TINY
+    r = kind
+    base = [4096, 384, 256] if kind == 4 else [8192, 1024, 256]
+    L = torch.tensor([b + phase for b in base], dtype=torch.int32)   # tokens after the step
+    st2 = synth.filled_state(RNG_SEED, kind, shape, L, name=f"mtp{kind}", T=2)
+    s2 = _np_state(st2)
+    s2["T"], s2["W"] = 2, shape.W
+    s1 = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in s2.items()}
+    Lin = s2["seq_len_in"].astype(np.int64)
+    s1["swa"] = oracle_mod._window_ring(s2["swa"], Lin, shape.W)
+    s1["T"] = 1
+    per_token = ["q", "kv_new", "z_new"] + (["ik_new", "iz_new", "iq", "w"] if kind == 4 else [])
+    r2 = oracle_mod.layer_decode(s2)
+    singles = []
+    for t in range(2):
+        for name in per_token:
+            s1[name] = np.ascontiguousarray(s2[name][:, t])
+        s1["seq_len_in"] = (Lin + t).astype(np.int32)
+        singles.append(oracle_mod.layer_decode(s1))
+    assert np.array_equal(r2["seq_len_out"], singles[1]["seq_len_out"])
+    for t in range(2):
+        a, b = r2["tokens"][t], singles[t]
+        assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
+        assert np.array_equal(r2["out"][:, t], b["out"])
+        if kind == 4:
+            assert np.array_equal(a["scores64"], b["scores64"])
+            assert np.array_equal(a["idx"], b["idx"]) and np.array_equal(r2["idx"][:, t], b["idx"])
+    for name in ["kv_pool", "kv_ring", "z_ring"] + (["key_pool", "ik_ring", "iz_ring"] if kind == 4 else []):
+        assert np.array_equal(s2[name], s1[name]), name
+    Lout = Lin + 2
+    assert np.array_equal(oracle_mod._window_ring(s2["swa"], Lout, shape.W),
+                          oracle_mod._window_ring(s1["swa"], Lout, shape.W))
+    # a block completed in the step: the pool's last live row was written in it
+    done = [(int(Lin[b]) + t + 1) % r == 0 for b in range(3) for t in range(2)]
+    assert any(done) == (phase in ((0, 1) if kind == 4 else (0, 1)))
