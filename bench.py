@@ -62,7 +62,7 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def layer_bytes(L, shape, kind=4, key_entry_bytes=None):
+def layer_bytes(L, shape, kind=4, key_entry_bytes=None, T=1):
     """Algorithmic HBM bytes of one layer step (each byte the method must move,
     counted once).  C4: indexer keys, score write + read, the gathered window
     and top-k rows, q, o, the index list, the new-token append and the 4-row
@@ -70,13 +70,16 @@ def layer_bytes(L, shape, kind=4, key_entry_bytes=None):
     gathered window and every C128 row, q, o, the append and the 128-row
     block compression of the sequences whose block completes.
     key_entry_bytes: bytes of one stored indexer key (bf16: 2 Di; E4M3 codes
-    and their fp32 scale: Di + 4)."""
+    and their fp32 scale: Di + 4).  T query tokens per step (L: tokens after
+    it): the keys are read once for all tokens; scores, gathers, q, o, the
+    index lists and the appended rows count once per token."""
     L = L.to(torch.int64)
     B = L.numel()
     D, Di = shape.Dqk, shape.Di
-    win = int(torch.clamp(L, max=shape.W).sum())
-    q = B * shape.Hq * D * 2
-    o = B * shape.Hq * shape.Dv * 2 + B * shape.Hq * 4
+    Lt = [L - (T - 1 - t) for t in range(T)]   # each token's length
+    win = sum(int(torch.clamp(x, max=shape.W).sum()) for x in Lt)
+    q = T * B * shape.Hq * D * 2
+    o = T * (B * shape.Hq * shape.Dv * 2 + B * shape.Hq * 4)
     if kind == 128:
         n = L // 128
         gather = (win + int(n.sum())) * D * 2
@@ -88,19 +91,20 @@ def layer_bytes(L, shape, kind=4, key_entry_bytes=None):
                 "append_compress": append + compress}
     n4 = L // 4
     N = int(n4.sum())
+    Nt = sum(int((x // 4).sum()) for x in Lt)            # scores over all tokens
     kb = Di * 2 if key_entry_bytes is None else key_entry_bytes
     keys = N * kb
-    iq_w = B * shape.Hi * (Di * 2 + 4)
-    scores = 2 * N * 4
-    gather = (win + int(torch.clamp(n4, max=shape.k).sum())) * D * 2
-    idx = 2 * B * shape.k * 4
-    append = B * (D * 2 * 2 + D * 2 * 3 + Di * 2 * 2 + Di * 2 * 2)   # read new rows, write rings
-    ncomp = int((L % 4 == 0).sum())
+    iq_w = T * B * shape.Hi * (Di * 2 + 4)
+    scores = 2 * Nt * 4
+    gather = (win + sum(int(torch.clamp(x // 4, max=shape.k).sum()) for x in Lt)) * D * 2
+    idx = 2 * T * B * shape.k * 4
+    append = T * B * (D * 2 * 2 + D * 2 * 3 + Di * 2 * 2 + Di * 2 * 2)   # read new rows, write rings
+    ncomp = int(((L // 4) != ((L - T) // 4)).sum())
     compress = ncomp * (4 * 2 * (D + Di) * 2 + D * 2 + kb)
-    indexer = keys + iq_w + N * 4
+    indexer = keys + iq_w + Nt * 4
     total = keys + iq_w + scores + gather + q + o + idx + append + compress
     return {"total": total, "indexer": indexer, "keys": keys, "gather": gather,
-            "attention": gather + q + o + idx // 2, "topk": N * 4 + idx // 2,
+            "attention": gather + q + o + idx // 2, "topk": Nt * 4 + idx // 2,
             "append_compress": append + compress}
 
 
@@ -542,6 +546,7 @@ def layer_variants(args, runs, peak):
     nb = statistics.mean(layer_bytes(r.L, r.g.shape, 4, key_entry_bytes=Di + 4)["total"] for r in runs)
     ib = statistics.mean(layer_bytes(r.L, r.g.shape, 4, key_entry_bytes=Di + 4)["indexer"] for r in runs)
     it = statistics.mean(idx_ms)
+    out["two_query_tokens"] = two_token_layer(args, peak)
     out["e4m3_keys"] = {
         "us": us, "algorithmic_bytes": nb, "achieved_gbs": nb / (us * 1e-6) / 1e9,
         "frac": nb / (us * 1e-6) / 1e9 / peak,
@@ -550,6 +555,35 @@ def layer_variants(args, runs, peak):
         "format": "E4M3 codes [rows, 128] + fp32 scale per row (amax / 448); queries "
                   "quantized per (sequence, head) in the kernel; tcgen05 kind::f8f6f4"}
     return out
+
+
+def two_token_layer(args, peak, n=4):
+    """The headline workload with two query tokens per sequence and step
+    (speculative decoding with a one-layer MTP head: the current and a draft
+    token verified together; the keys are streamed once for both), over n
+    rotating layer states."""
+    stream = torch.cuda.current_stream()
+    fns, keep, nbytes = [], [], []
+    for j in range(n):
+        seed = synth.SEED["c4layer"] + 7919 * j
+        L = synth.c4_lengths(seed, 64) + 1
+        g = synth.filled_state(seed, 4, synth.FULL, L, device="cuda", name=f"mtp{j}", T=2)
+        B, sh = L.numel(), g.shape
+        out = torch.empty(B, 2, sh.Hq, sh.Dv, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(B, 2, sh.Hq, dtype=torch.float32, device="cuda")
+        so = torch.empty_like(g.seq_len_in)
+        d = _lib.layer_desc(g, out, lse, so)
+        w = _lib.workspace(_lib.hsa_layer_decode_workspace_size(d))
+        fns.append(lambda d=d, w=w: _lib.hsa_layer_decode(d, ws=w))
+        keep.append((g, out, lse, so, d, w))
+        nbytes.append(layer_bytes(L, sh, 4, T=2)["total"])
+    us = rotating_us(fns, args.warmup, args.steps, stream)
+    for *_, w in keep:
+        assert _lib.hsa_workspace_status(w) == 0
+    nb = statistics.mean(nbytes)
+    return {"us_per_step": us, "us_per_token": us / 2, "tokens_per_step": 128,
+            "algorithmic_bytes": nb, "achieved_gbs": nb / (us * 1e-6) / 1e9,
+            "frac": nb / (us * 1e-6) / 1e9 / peak, "launches": _lib.hsa_layer_decode_launches(keep[0][4])}
 
 
 def e2e_layer(runs, flush, warmup, steps):

@@ -274,6 +274,7 @@ class LayerDesc(ctypes.Structure):
         ("kv_pool", P), ("key_pool", P), ("q", P), ("iq", P), ("w", P),
         ("out", P), ("lse", P), ("topk_idx", P), ("scores", P), ("stage_events", P),
         ("q_ready_event", P), ("key_fp8", ctypes.c_int32), ("key_scale", P),
+        ("T", ctypes.c_int32),
     ]
 
 
@@ -295,6 +296,7 @@ def layer_desc(st, out, lse=None, seq_len_out=None, topk_idx=None, scores=None,
     d.Hi, d.Di = (sh.Hi, sh.Di) if c4 else (0, 0)
     d.W, d.k = sh.W, (sh.k if c4 else 0)
     d.scale = sh.scale
+    d.T = getattr(st, "T", 1)
     d.out_dtype = {torch.float32: HSA_F32, torch.bfloat16: HSA_BF16}[out.dtype]
     d.pool_total_rows = st.kv_pool.shape[0]
     if max_pool_rows is None:   # the largest pool capacity bounds every live count

@@ -346,8 +346,11 @@ static hsa_status_t check_layer(const hsa_layer_desc* d) {
                 aligned(d->kv_pool, 16) && aligned(d->q, 16) && aligned(d->out, 16) &&
                 aligned(d->pool_offsets, 8) && aligned(d->lse, 4),
             HSA_ERR_INVALID_ARG, "misaligned pointer in descriptor");
+  HSA_CHECK(d->T >= 0 && d->T <= 4, HSA_ERR_UNSUPPORTED, "T=%d outside [0, 4]", d->T);
   if (d->kind == HSA_LAYER_C4) {
     HSA_CHECK(d->B <= 4096, HSA_ERR_UNSUPPORTED, "B=%d above the indexer's 4096 sequences", d->B);
+    HSA_CHECK(d->Hi * (d->T > 1 ? d->T : 1) <= 16, HSA_ERR_UNSUPPORTED,
+              "T * Hi = %d above the indexer's 16 query rows", d->Hi * (d->T > 1 ? d->T : 1));
     HSA_CHECK(d->Hi >= 1 && d->Hi <= 16, HSA_ERR_UNSUPPORTED, "Hi=%d outside [1, 16]", d->Hi);
     HSA_CHECK(d->Di == 32 || d->Di == 64 || d->Di == 128, HSA_ERR_UNSUPPORTED,
               "Di=%d not in {32, 64, 128}", d->Di);

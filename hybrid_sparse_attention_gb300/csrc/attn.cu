@@ -76,11 +76,13 @@ __host__ __device__ inline uint32_t attn_q_region(int NSL, int N) {
 }
 
 struct AttnParams {
-  const uint16_t* q;      // [B, Hq, Dqk]
-  const uint16_t* swa;    // [B, W, Dqk]
-  const int32_t* seq_len;
+  const uint16_t* q;      // [B, Hq, Dqk] (B tokens)
+  const uint16_t* swa;    // [B / T, Wr, Dqk] window rings
+  const int32_t* seq_len; // [B / T]
   int32_t len_add;
-  int W;
+  int W;                  // window rows attended
+  int T;                  // query tokens per sequence: token b is token b % T of sequence b / T
+  int Wr;                 // ring rows (slot = position mod Wr)
   const uint16_t* extra;  // compressed pool rows (may be null)
   Spans sp;
   const int32_t* idx;     // [B, k] or null (dense)
@@ -107,22 +109,29 @@ struct AttnParams {
   int32_t* topk_out;        // [B, k] the selection in order (may be null)
 };
 
+// Token b's geometry: its sequence bs, window length L (the token's own
+// position + 1), pool start off, live compressed rows nb and the start soff of
+// its score / candidate rows (off + t * the per-token stride).
 struct SeqGeom {
-  int64_t L, off, nb;
+  int64_t L, off, nb, soff;
+  int bs;
   int n_swa;
   int64_t n_extra;
 };
 
 HSA_DEVINL SeqGeom seq_geom(const AttnParams& p, int b) {
   SeqGeom g;
-  int64_t L = static_cast<int64_t>(p.seq_len[b]) + p.len_add;
+  g.bs = p.T == 1 ? b : b / p.T;
+  int64_t L = static_cast<int64_t>(p.seq_len[g.bs]) + p.len_add + (p.T == 1 ? 0 : b % p.T);
   g.L = L < 0 ? 0 : L;
   g.n_swa = static_cast<int>(g.L < p.W ? g.L : p.W);
   g.off = 0;
+  g.soff = 0;
   g.nb = 0;
   g.n_extra = 0;
   if (p.extra) {
-    g.off = p.sp.start(b);
+    g.off = p.sp.pool_start(b);
+    g.soff = p.sp.start(b);
     g.nb = p.sp.count(b);
     if (p.idx || p.sel_scores) {
       g.n_extra = p.k;
@@ -139,7 +148,7 @@ HSA_DEVINL const uint16_t* slot_row(const AttnParams& p, int b, const SeqGeom& g
                                     bool report) {
   if (slot < g.n_swa) {
     const int64_t pos = g.L - g.n_swa + slot;
-    return p.swa + (static_cast<int64_t>(b) * p.W + pos % p.W) * p.Dqk;
+    return p.swa + (static_cast<int64_t>(g.bs) * p.Wr + pos % p.Wr) * p.Dqk;
   }
   const int64_t e = slot - g.n_swa;
   if (e >= g.n_extra) return nullptr;
@@ -161,7 +170,7 @@ HSA_DEVINL const uint16_t* slot_row_j(const AttnParams& p, int b, const SeqGeom&
                                       int64_t j, bool report) {
   if (slot < g.n_swa) {
     const int64_t pos = g.L - g.n_swa + slot;
-    return p.swa + (static_cast<int64_t>(b) * p.W + pos % p.W) * p.Dqk;
+    return p.swa + (static_cast<int64_t>(g.bs) * p.Wr + pos % p.Wr) * p.Dqk;
   }
   const int64_t e = slot - g.n_swa;
   if (e >= g.n_extra) return nullptr;
@@ -344,7 +353,7 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
   uint32_t* s_row = reinterpret_cast<uint32_t*>(ring);  // [kSelRowMax] score bits
   const uint32_t kk = static_cast<uint32_t>(n < p.k ? n : p.k);
   const bool all = n <= p.k;
-  const uint32_t* row = reinterpret_cast<const uint32_t*>(p.sel_scores + g.off);
+  const uint32_t* row = reinterpret_cast<const uint32_t*>(p.sel_scores + g.soff);
   // Loops stay rolled throughout: this code runs once per launch, and its
   // instruction fetches cost more than loop overhead.
   // (1) the row's scores to shared memory, every copy in flight at once: the
@@ -450,7 +459,7 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
   // winners then candidates, contiguous in sbuf, when both fit the merge sort;
   // otherwise ("heavy") the candidates go to the row's workspace
   const bool heavy = nw + ncd > static_cast<uint32_t>(kSelSort);  // (uniform)
-  uint64_t* cand = heavy ? p.cand_ws + g.off : sbuf + nw;
+  uint64_t* cand = heavy ? p.cand_ws + g.soff : sbuf + nw;
   uint32_t wo = off & 0xffffu, co = off >> 16;
   bool nan = false;
 #pragma unroll
@@ -530,7 +539,7 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rowp),
                    "r"(static_cast<uint32_t>(p.Dqk * 2))
                    : "memory");
-      if (p.topk_out) p.cand_ws[g.off + e] = x;
+      if (p.topk_out) p.cand_ws[g.soff + e] = x;
     }
     const int q = static_cast<int>((g.n_swa + e) / p.sps);  // the split attending entry e
     uint16_t* dst = &sh.sel[e - share_first(p, g.n_swa, q)];
@@ -554,7 +563,7 @@ HSA_DEVINL void write_topk_sorted(const AttnParams& p, uint8_t* ring, int b, con
                                   int nsel) {
   const int t = threadIdx.x;
   uint64_t* a = reinterpret_cast<uint64_t*>(ring);
-  for (int i = t; i < nsel; i += kThreads) a[i] = p.cand_ws[g.off + i];
+  for (int i = t; i < nsel; i += kThreads) a[i] = p.cand_ws[g.soff + i];
   int P = 32;
   while (P < nsel) P <<= 1;
   merge_sort_desc<kSelMaxK / kThreads>(a, a + kSelMaxK, nsel, P);
@@ -836,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll 1
     for (int r = tid; r < win_tiles * kKeys; r += kThreads) {
       const int64_t pos = geo.L - geo.n_swa + static_cast<int64_t>(t0) * kKeys + r;
-      const uint16_t* rowp = p.swa + (static_cast<int64_t>(b) * p.W + pos % p.W) * p.Dqk;
+      const uint16_t* rowp = p.swa + (static_cast<int64_t>(geo.bs) * p.Wr + pos % p.Wr) * p.Dqk;
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rowp),
                    "r"(static_cast<uint32_t>(p.Dqk * 2))
                    : "memory");
@@ -1467,6 +1476,8 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.seq_len = a.seq_len;
   p.len_add = a.len_add;
   p.W = static_cast<int>(a.W);
+  p.T = a.T < 1 ? 1 : a.T;
+  p.Wr = static_cast<int>(a.Wr > 0 ? a.Wr : a.W);
   p.extra = static_cast<const uint16_t*>(a.extra);
   p.sp = a.sp;
   p.idx = a.idx;
@@ -1501,8 +1512,9 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   CUtensorMap qmap, swamap;
   cudaError_t e = make_tmap_2d_bf16(&qmap, a.q, a.Dqk, a.B * a.Hq, 64, pl.N, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  // full 128-row windows are loaded by TMA (a map over the ring's rows)
-  const int swa_tma = a.swa && a.W == kKeys ? 1 : 0;
+  // full 128-row windows are loaded by TMA (a map over the ring's rows; the
+  // ring then holds exactly the window)
+  const int swa_tma = a.swa && a.W == kKeys && p.Wr == a.W && p.T == 1 ? 1 : 0;
   swamap = qmap;  // (unused unless swa_tma)
   if (swa_tma) {
     e = make_tmap_2d_bf16(&swamap, a.swa, a.Dqk, a.B * a.W, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B);

@@ -132,17 +132,28 @@ struct Spans {
   int32_t add;
   int32_t ratio;
   int64_t limit;
-  HSA_DEVINL int64_t start(int b) const { return offsets[b]; }
-  HSA_DEVINL int64_t raw_count(int b) const {
+  // Rows of T query tokens per sequence (multi-token queries): row r is token
+  // r % T of sequence r / T, whose live count is (seq_len + add + r % T) /
+  // ratio; start(r) adds (r % T) * tstride (per-token score arrays, tstride
+  // apart), pool_start(r) is the sequence's first pool row.
+  int32_t T = 1;
+  int64_t tstride = 0;
+  HSA_DEVINL int seq(int r) const { return T == 1 ? r : r / T; }
+  HSA_DEVINL int tok(int r) const { return T == 1 ? 0 : r % T; }
+  HSA_DEVINL int64_t pool_start(int r) const { return offsets[seq(r)]; }
+  HSA_DEVINL int64_t start(int r) const { return offsets[seq(r)] + tok(r) * tstride; }
+  HSA_DEVINL int64_t raw_count(int r) const {
+    const int b = seq(r);
     if (!seq_len) return offsets[b + 1] - offsets[b];
-    const int64_t n = (static_cast<int64_t>(seq_len[b]) + add) / ratio;
+    const int64_t n = (static_cast<int64_t>(seq_len[b]) + add + tok(r)) / ratio;
     return n < 0 ? 0 : n;
   }
-  HSA_DEVINL bool valid(int b) const {
+  HSA_DEVINL bool valid(int r) const {
+    const int b = seq(r);
     const int64_t o0 = offsets[b], o1 = offsets[b + 1];
-    return o0 >= 0 && o1 >= o0 && o1 <= limit && raw_count(b) <= o1 - o0;
+    return o0 >= 0 && o1 >= o0 && o1 <= limit && raw_count(r) <= o1 - o0;
   }
-  HSA_DEVINL int64_t count(int b) const { return valid(b) ? raw_count(b) : 0; }
+  HSA_DEVINL int64_t count(int r) const { return valid(r) ? raw_count(r) : 0; }
 };
 
 // Arguments of one fused-attention launch (see hsa_decode_attn in hsa.h).
@@ -150,8 +161,13 @@ struct AttnArgs {
   const void* q;
   const void* swa;
   const int32_t* seq_len;
-  int32_t len_add;    // attended window length is seq_len[b] + len_add
-  int64_t W;
+  int32_t len_add;    // attended window length is seq_len[b] + len_add (per sequence b)
+  int64_t W;          // window rows attended
+  // Multi-token queries: tokens b' = b * T + t of sequence b (q, out, lse and
+  // idx rows per token); token t attends a window of length seq_len[b] +
+  // len_add + t, from a ring of Wr >= W + T - 1 rows (slot = position mod Wr)
+  int32_t T = 1;
+  int64_t Wr = 0;     // 0: W
   const void* extra;  // compressed pool (null: window only)
   Spans sp;           // its sequences
   const int32_t* idx; // [B, k] row-local indices, or null for dense

@@ -53,6 +53,7 @@ constexpr int kMaxStages = 6;
 constexpr int kFp8Di = 128;     // E4M3 keys: one 128-byte swizzle row per entry
 constexpr uint32_t kQ8Bytes = kQRows * kFp8Di;  // one sequence's E4M3 query rows
 constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kMaxT = 4;        // query tokens per sequence
 constexpr int kMaxSeqs = 4096;  // tile prefix table (built in a stage buffer before the ring starts)
 constexpr int kAcc = 4;         // accumulators in TMEM (tiles the MMA may run ahead of the epilogue)
 constexpr int kParts = 4;           // independent partial accumulators per tile
@@ -61,7 +62,12 @@ constexpr uint32_t kTmemCols = kAcc * kParts * kQRows;
 struct IndexerParams {
   const float* w;  // [B, Hi]
   Spans sp;
-  int B, Hi, Di;
+  // Hi: query rows per sequence, T tokens of Hi / T heads each (multi-token
+  // queries: row h belongs to token h / (Hi / T)); the sequence's key rows are
+  // its last token's (sp counts them); token t scores the first
+  // (seq_len + add - (T - 1 - t)) / ratio of them, into scores + t * tstride
+  int B, Hi, Di, T;
+  int64_t tstride;
   float* scores;
   uint32_t* status;
   int wait_mode;   // programmatic dependent launch: see launch_indexer in internal.h
@@ -114,12 +120,14 @@ struct SeqCursor {
     next = first + static_cast<int>((count + kTileRows - 1) / kTileRows);
   }
   // Tile of the current sequence holding a row the previous kernel may have
-  // just written, or -1: the last live row, when the new length completes a
-  // block (the lengths here are the ones after the previous kernel).
+  // just written, or -1: the last live row, when one of the step's T tokens
+  // completed a block (the lengths here are the ones after the previous
+  // kernel; at most one block completes in a step of T <= ratio tokens).
   HSA_DEVINL int appended_tile(const IndexerParams& p) const {
     if (!p.sp.seq_len || count <= 0) return -1;
     const int64_t L = static_cast<int64_t>(p.sp.seq_len[b]) + p.sp.add;
-    if (L % p.sp.ratio != 0) return -1;
+    const int64_t L0 = L - p.T;
+    if (L0 >= 0 && L / p.sp.ratio == L0 / p.sp.ratio) return -1;
     return first + static_cast<int>((count - 1) / kTileRows);
   }
   // Moves to the first sequence of the CTA's range (start) or to the next
@@ -395,6 +403,8 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_const
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     SeqCursor cur;
     float wv[kQRows];
+    int64_t nt[kMaxT];  // each token's live rows of the current sequence
+    const int hpt = p.Hi / p.T;  // heads per token
     // (kFp8) the E4M3 queries of the range's first two sequences; `ahead` is the
     // sequence of the last buffer written, `made` how many were written
     SeqCursor ahead;
@@ -447,6 +457,16 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_const
           for (int h = 0; h < kQRows; ++h)
             wv[h] = h < p.Hi ? __ldg(p.w + static_cast<int64_t>(cur.b) * p.Hi + h) : 0.f;
         }
+        // each token's live rows (the last token's are the sequence's count)
+#pragma unroll
+        for (int q = 0; q < kMaxT; ++q) {
+          int64_t n = cur.count;
+          if (q < p.T - 1 && p.sp.seq_len) {
+            n = (static_cast<int64_t>(p.sp.seq_len[cur.b]) + p.sp.add - (p.T - 1 - q)) / p.sp.ratio;
+            n = n < 0 ? 0 : (n > cur.count ? cur.count : n);
+          }
+          nt[q] = q < p.T ? n : 0;
+        }
       }
       const int64_t piece = t - cur.first;
       const int64_t left = cur.count - piece * kTileRows;
@@ -480,19 +500,39 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_const
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&sh.acc_empty[a]);
-      if (r < left) {
-        float sc = 0.f;
+      if (p.T == 1) {
+        if (r < left) {
+          float sc = 0.f;
 #pragma unroll
-        for (int h = 0; h < kQRows; ++h)
-          if (h < p.Hi) sc = fmaf(wv[h], fmaxf(dot[h], 0.f), sc);
-        if (kFp8) sc *= ks;
-        p.scores[row] = sc;
-        // the top-k's histogram: one count in the bin of the score's top key
-        // bits (a reduction: nothing waits for it)
-        if (p.row_hist)
-          atomicAdd(p.row_hist + static_cast<int64_t>(cur.b) * kRowHistBins +
-                        (order_key(__float_as_uint(sc)) >> kRowHistShift),
-                    1u);
+          for (int h = 0; h < kQRows; ++h)
+            if (h < p.Hi) sc = fmaf(wv[h], fmaxf(dot[h], 0.f), sc);
+          if (kFp8) sc *= ks;
+          p.scores[row] = sc;
+          // the top-k's histogram: one count in the bin of the score's top
+          // key bits (a reduction: nothing waits for it)
+          if (p.row_hist)
+            atomicAdd(p.row_hist + static_cast<int64_t>(cur.b) * kRowHistBins +
+                          (order_key(__float_as_uint(sc)) >> kRowHistShift),
+                      1u);
+        }
+      } else {
+        // token q: heads [q * hpt, (q + 1) * hpt), the rows visible to it
+        const int64_t jrow = piece * kTileRows + r;  // row within the sequence
+#pragma unroll
+        for (int q = 0; q < kMaxT; ++q) {
+          if (q < p.T && jrow < nt[q] && r < left) {
+            float sc = 0.f;
+#pragma unroll
+            for (int h = 0; h < kQRows; ++h)
+              if (h >= q * hpt && h < (q + 1) * hpt) sc = fmaf(wv[h], fmaxf(dot[h], 0.f), sc);
+            if (kFp8) sc *= ks;
+            p.scores[q * p.tstride + row] = sc;
+            if (p.row_hist)
+              atomicAdd(p.row_hist + (static_cast<int64_t>(cur.b) * p.T + q) * kRowHistBins +
+                            (order_key(__float_as_uint(sc)) >> kRowHistShift),
+                        1u);
+          }
+        }
       }
       }  // !dead
       if (kFp8 && (t + 1 == cur.next || t + 1 == t_end) && made == ord + 2) {
@@ -527,9 +567,10 @@ size_t indexer_smem_bytes(int Di, bool fp8) {
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
                            cudaStream_t stream, bool pdl, int wait_mode, uint32_t* row_hist,
-                           const float* key_scale) {
+                           const float* key_scale, int T) {
   if (total_rows == 0) return cudaSuccess;
-  if (B > kMaxSeqs) return cudaErrorInvalidValue;
+  if (B > kMaxSeqs || T < 1 || T > kMaxT || Hi * T > kQRows) return cudaErrorInvalidValue;
+  Hi *= T;  // query rows per sequence
   const bool fp8 = key_scale != nullptr;
   if (fp8 && (Di != kFp8Di || Hi > kQRows)) return cudaErrorInvalidValue;
   const int kb_elems = Di >= 64 ? 64 : Di;
@@ -554,8 +595,8 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
   const int64_t tiles_bound = (total_rows + kTileRows - 1) / kTileRows + B;
   const int nres = (fp8 ? 2 : 1) * device_sms();
   const int grid = static_cast<int>(tiles_bound < nres ? tiles_bound : nres);
-  IndexerParams p{w, sp, B, Hi, Di, scores, status, pdl ? wait_mode : 0, row_hist, key_scale,
-                  static_cast<const uint16_t*>(iq), wait_limit_ns(), wait_limit_polls()};
+  IndexerParams p{w, sp, B, Hi, Di, T, total_rows, scores, status, pdl ? wait_mode : 0, row_hist,
+                  key_scale, static_cast<const uint16_t*>(iq), wait_limit_ns(), wait_limit_polls()};
   return launch_k(kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, kmap, qmap, p);
 }
 

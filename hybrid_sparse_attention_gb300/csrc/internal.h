@@ -94,10 +94,14 @@ size_t indexer_smem_bytes(int Di, bool fp8 = false);
 // key_scale non-null: keys are E4M3 codes [total_rows, Di] (Di = 128) with one
 // fp32 scale per row, and the kernel quantizes each (sequence, head) query
 // row of iq the same way (E4M3 tensor-core products, fp32 accumulation).
+// T query tokens per sequence (T * Hi <= 16): iq [B, T, Hi, Di], w [B, T, Hi];
+// sp counts the sequence's rows for its last token; token t scores the rows
+// visible to it into scores + t * total_rows (row_hist: B * T histograms).
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
                            int Di, int64_t total_rows, float* scores, uint32_t* status,
                            cudaStream_t stream, bool pdl = false, int wait_mode = 0,
-                           uint32_t* row_hist = nullptr, const float* key_scale = nullptr);
+                           uint32_t* row_hist = nullptr, const float* key_scale = nullptr,
+                           int T = 1);
 
 size_t topk_workspace_bytes(int64_t B, int64_t total_rows, int64_t k);
 // Leading bytes of a top-k workspace (status word, row states, histograms)

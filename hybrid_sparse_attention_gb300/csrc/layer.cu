@@ -52,7 +52,11 @@ struct AppendParams {
   uint4* key_pool;
   float* key_scale;  // non-null: key_pool holds E4M3 codes [rows, Di] with these fp32 scales
   uint32_t* status;
+  int T;             // tokens appended per step (rows b * T + t of the new-row inputs)
+  int Wr;            // window ring rows (W + T - 1)
 };
+
+constexpr int kMaxT = 4;  // tokens per step
 
 constexpr int kMaxKeyDi = 128;  // E4M3 key rows (one warp quantizes a row, 4 channels a lane)
 
@@ -99,10 +103,14 @@ constexpr int kShortBlock = 4;
 HSA_DEVINL void append_short(const AppendParams& p, int b) {
   __shared__ float s_key[kMaxKeyDi];  // E4M3 pool: the completed block's fp32 key row
   const int cq = p.Dqk / 8, ci = p.kind == HSA_LAYER_C4 ? p.Di / 8 : 0;
-  const int r = p.r;
+  const int r = p.r, T = p.T;
   const int32_t lin = p.seq_len_in[b];
   const int64_t o0 = p.pool_offsets[b], o1 = p.pool_offsets[b + 1];
-  int64_t L = 0;
+  // the step's token whose position completes a block (at most one: T <= r)
+  int tcomp = -1;
+  for (int t = 0; t < T; ++t)
+    if ((static_cast<int64_t>(lin) + t + 1) % r == 0) tcomp = t;
+  const int64_t pc = static_cast<int64_t>(lin) + tcomp;  // its position (when tcomp >= 0)
   for (int it = threadIdx.x; it < cq + ci; it += blockDim.x) {
     const bool key = it >= cq;
     const int c = key ? it - cq : it, n8 = key ? ci : cq, C = n8 * 8;
@@ -111,8 +119,14 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
     uint4* ring_v = (key ? p.ik_ring : p.kv_ring) + static_cast<int64_t>(b) * r * n8 + c;
     uint4* ring_z = (key ? p.iz_ring : p.z_ring) + static_cast<int64_t>(b) * r * n8 + c;
     const float* bias = (key ? p.b_ik : p.b_kv) + c * 8;
-    const uint4 nv = nv_src[static_cast<int64_t>(b) * n8 + c];
-    const uint4 nz = nz_src[static_cast<int64_t>(b) * n8 + c];
+    uint4 nv[kMaxT], nz[kMaxT];  // the step's new rows (token t: row b * T + t)
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t) {
+      if (t < T) {
+        nv[t] = nv_src[(static_cast<int64_t>(b) * T + t) * n8 + c];
+        nz[t] = nz_src[(static_cast<int64_t>(b) * T + t) * n8 + c];
+      }
+    }
     uint4 rv[kShortBlock], rz[kShortBlock];
     float4 b0[kShortBlock], b1[kShortBlock];
 #pragma unroll
@@ -125,26 +139,40 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
         b1[i] = __ldg(bp + 1);
       }
     }
-    L = static_cast<int64_t>(lin) + 1;
-    const int64_t slot = (L - 1) % r;
-    if (!key) p.swa[(static_cast<int64_t>(b) * p.W + (L - 1) % p.W) * cq + c] = nv;
-    ring_v[slot * n8] = nv;
-    ring_z[slot * n8] = nz;
-    if (L % r != 0) continue;
-    const int64_t n = L / r - 1;
+    // the new rows into the window ring and the in-flight rings, in order
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t) {
+      if (t < T) {
+        const int64_t pos = static_cast<int64_t>(lin) + t;
+        if (!key) p.swa[(static_cast<int64_t>(b) * p.Wr + pos % p.Wr) * cq + c] = nv[t];
+        ring_v[(pos % r) * n8] = nv[t];
+        ring_z[(pos % r) * n8] = nz[t];
+      }
+    }
+    if (tcomp < 0) continue;
+    const int64_t n = (pc + 1) / r - 1;
     if (o0 < 0 || o1 > p.pool_total_rows || o0 + n >= o1) {
       set_status(p.status, HSA_DEV_BOUNDS);
       continue;
     }
+    // the completed block: slot i holds position pc - r + 1 + i, a new row of
+    // this step when at or past lin (the ring's copy loaded above otherwise)
     float x[kShortBlock][8], v[kShortBlock][8], mx[8];
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) mx[ch] = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kShortBlock; ++i) {
       if (i < r) {
-        const bool last = i == r - 1;  // the completing row is the new one (slot r-1)
-        bf16x8_to_f32(last ? nz : rz[i], x[i]);
-        bf16x8_to_f32(last ? nv : rv[i], v[i]);
+        const int64_t tq = pc - r + 1 + i - lin;  // token index of the row, if new
+        uint4 zi = rz[i], vi = rv[i];
+#pragma unroll
+        for (int t = 0; t < kMaxT; ++t)
+          if (t < T && tq == t) {
+            zi = nz[t];
+            vi = nv[t];
+          }
+        bf16x8_to_f32(zi, x[i]);
+        bf16x8_to_f32(vi, v[i]);
         const float bb[8] = {b0[i].x, b0[i].y, b0[i].z, b0[i].w, b1[i].x, b1[i].y, b1[i].z, b1[i].w};
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
@@ -176,11 +204,10 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
     dst[(o0 + n) * n8 + c] = f32x8_to_bf16(o);
   }
   __syncthreads();  // every thread has read seq_len_in before it may be overwritten
-  const int64_t Lw = static_cast<int64_t>(lin) + 1;
-  if (p.key_scale && threadIdx.x < 32 && Lw % r == 0) {
+  if (p.key_scale && threadIdx.x < 32 && tcomp >= 0) {
     // warp 0 quantizes the completed block's key row: amax over the row, then
     // 4 channels a lane
-    const int64_t n = Lw / r - 1;
+    const int64_t n = (pc + 1) / r - 1;
     if (!(o0 < 0 || o1 > p.pool_total_rows || o0 + n >= o1)) {
       const int lane = threadIdx.x;
       const bool live = 4 * lane < p.Di;
@@ -201,7 +228,7 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
       if (lane == 0) p.key_scale[o0 + n] = __fdiv_rn(am, 448.f);
     }
   }
-  if (threadIdx.x == 0) p.seq_len_out[b] = lin + 1;
+  if (threadIdx.x == 0) p.seq_len_out[b] = lin + T;
 }
 
 __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendParams p) {
@@ -212,49 +239,57 @@ __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendPara
     append_short(p, b);
     return;
   }
-  const int64_t L = static_cast<int64_t>(p.seq_len_in[b]) + 1;
+  const int64_t lin = p.seq_len_in[b];
   const int cq = p.Dqk / 8, ci = p.Di / 8;
-  const int64_t slot_w = (L - 1) % p.W, slot_r = (L - 1) % p.r;
-  // a1: the new token's rows into the window ring and the in-flight rings
-  for (int c = threadIdx.x; c < cq; c += blockDim.x) {
-    const uint4 kv = p.kv_new[static_cast<int64_t>(b) * cq + c];
-    const uint4 z = p.z_new[static_cast<int64_t>(b) * cq + c];
-    p.swa[(static_cast<int64_t>(b) * p.W + slot_w) * cq + c] = kv;
-    p.kv_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = kv;
-    p.z_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = z;
-  }
-  if (p.kind == HSA_LAYER_C4) {
-    for (int c = threadIdx.x; c < ci; c += blockDim.x) {
-      p.ik_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] =
-          p.ik_new[static_cast<int64_t>(b) * ci + c];
-      p.iz_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] =
-          p.iz_new[static_cast<int64_t>(b) * ci + c];
-    }
-  }
-  __syncthreads();  // ring writes visible to the block; seq_len_in read by all
-  if (threadIdx.x == 0) p.seq_len_out[b] = static_cast<int32_t>(L);
-  if (L % p.r != 0) return;
-  // a2: the block is complete -> compress it into pool row L/r - 1
-  const int64_t n = L / p.r - 1;
   const int64_t o0 = p.pool_offsets[b], o1 = p.pool_offsets[b + 1];
-  if (o0 < 0 || o1 > p.pool_total_rows || o0 + n >= o1) {
-    if (threadIdx.x == 0) set_status(p.status, HSA_DEV_BOUNDS);
-    return;
+  __syncthreads();  // seq_len_in read by every thread before it may be overwritten
+  for (int t = 0; t < p.T; ++t) {
+    const int64_t pos = lin + t;
+    const int64_t slot_w = pos % p.Wr, slot_r = pos % p.r;
+    const int64_t row = static_cast<int64_t>(b) * p.T + t;
+    // a1: token t's rows into the window ring and the in-flight rings
+    for (int c = threadIdx.x; c < cq; c += blockDim.x) {
+      const uint4 kv = p.kv_new[row * cq + c];
+      const uint4 z = p.z_new[row * cq + c];
+      p.swa[(static_cast<int64_t>(b) * p.Wr + slot_w) * cq + c] = kv;
+      p.kv_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = kv;
+      p.z_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = z;
+    }
+    if (p.kind == HSA_LAYER_C4) {
+      for (int c = threadIdx.x; c < ci; c += blockDim.x) {
+        p.ik_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] = p.ik_new[row * ci + c];
+        p.iz_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] = p.iz_new[row * ci + c];
+      }
+    }
+    __syncthreads();  // ring writes visible to the block
+    if ((pos + 1) % p.r != 0) continue;
+    // a2: the block is complete -> compress it into pool row (pos + 1)/r - 1
+    // (before a later token of the step writes the next block's first slot)
+    const int64_t n = (pos + 1) / p.r - 1;
+    if (o0 < 0 || o1 > p.pool_total_rows || o0 + n >= o1) {
+      if (threadIdx.x == 0) set_status(p.status, HSA_DEV_BOUNDS);
+      continue;
+    }
+    compress_block(p.kv_ring + static_cast<int64_t>(b) * p.r * cq,
+                   p.z_ring + static_cast<int64_t>(b) * p.r * cq, p.b_kv, p.r, p.Dqk,
+                   p.kv_pool + (o0 + n) * cq);
+    if (p.kind == HSA_LAYER_C4)
+      compress_block(p.ik_ring + static_cast<int64_t>(b) * p.r * ci,
+                     p.iz_ring + static_cast<int64_t>(b) * p.r * ci, p.b_ik, p.r, p.Di,
+                     p.key_pool + (o0 + n) * ci);
+    __syncthreads();  // the block read before the next token's rows
   }
-  compress_block(p.kv_ring + static_cast<int64_t>(b) * p.r * cq,
-                 p.z_ring + static_cast<int64_t>(b) * p.r * cq, p.b_kv, p.r, p.Dqk,
-                 p.kv_pool + (o0 + n) * cq);
-  if (p.kind == HSA_LAYER_C4)
-    compress_block(p.ik_ring + static_cast<int64_t>(b) * p.r * ci,
-                   p.iz_ring + static_cast<int64_t>(b) * p.r * ci, p.b_ik, p.r, p.Di,
-                   p.key_pool + (o0 + n) * ci);
+  if (threadIdx.x == 0) p.seq_len_out[b] = static_cast<int32_t>(lin + p.T);
 }
 
 HSA_HOST_DEVICE size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Query tokens per sequence in one step (multi-token queries).
+int layer_tokens(const hsa_layer_desc& d) { return d.T > 1 ? d.T : 1; }
+
 AttnPlan layer_attn_plan(const hsa_layer_desc& d) {
   const int64_t slots = d.kind == HSA_LAYER_C4 ? d.k : d.max_pool_rows;
-  return attn_plan(d.B, d.Hq, d.Dqk, d.Dv, d.W, slots);
+  return attn_plan(static_cast<int64_t>(d.B) * layer_tokens(d), d.Hq, d.Dqk, d.Dv, d.W, slots);
 }
 
 // A C4 layer whose rows and plan allow it selects its top-k inside the
@@ -267,25 +302,29 @@ bool layer_fused(const hsa_layer_desc& d) {
   return attn_fused_ok(layer_attn_plan(d), d.k, max_row);
 }
 
+// With T query tokens the score, top-k and selection areas are per token:
+// token t's scores at pool row positions + t * pool_total_rows.
 struct LayerWs {
   size_t scores, topk, idx, hist, attn, total;
   LayerWs(const hsa_layer_desc& d, const AttnPlan& pl) {
+    const int64_t T = layer_tokens(d), BT = static_cast<int64_t>(d.B) * T;
+    const int64_t srows = (d.pool_total_rows > 0 ? d.pool_total_rows : 1) * T;
     size_t at = kWsHeader;
     scores = topk = idx = hist = 0;
     if (d.kind == HSA_LAYER_C4) {
       scores = at;
-      if (!d.scores) at += a256(static_cast<size_t>(d.pool_total_rows > 0 ? d.pool_total_rows : 1) * 4);
+      if (!d.scores) at += a256(static_cast<size_t>(srows) * 4);
       topk = at;
-      at += a256(topk_workspace_bytes(d.B, d.pool_total_rows, d.k));
+      at += a256(topk_workspace_bytes(BT, d.pool_total_rows * T, d.k));
       idx = at;
-      if (!d.topk_idx) at += a256(static_cast<size_t>(d.B) * d.k * 4);
+      if (!d.topk_idx) at += a256(static_cast<size_t>(BT) * d.k * 4);
       if (layer_fused(d)) {
         hist = at;
-        at += a256(static_cast<size_t>(d.B) * kRowHistBins * sizeof(uint32_t));
+        at += a256(static_cast<size_t>(BT) * kRowHistBins * sizeof(uint32_t));
       }
     }
     attn = at;
-    at += a256(attn_workspace_bytes(pl, d.B, d.Hq, d.Dv));
+    at += a256(attn_workspace_bytes(pl, BT, d.Hq, d.Dv));
     total = at;
   }
 };
@@ -301,7 +340,7 @@ int layer_launch_count(const hsa_layer_desc& d) {
   int n = 1 + 1 + (pl.S > 1 && !pl.cl ? 1 : 0);  // append, attention (+ combine)
   if (d.kind == HSA_LAYER_C4)
     n += (d.pool_total_rows > 0 ? 1 : 0) +
-         (layer_fused(d) ? 0 : topk_launch_count(d.pool_total_rows, d.max_pool_rows));
+         (layer_fused(d) ? 0 : topk_launch_count(d.pool_total_rows * layer_tokens(d), d.max_pool_rows));
   return n;
 }
 
@@ -338,6 +377,9 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   ap.key_pool = static_cast<uint4*>(d.key_pool);
   ap.key_scale = d.kind == HSA_LAYER_C4 && d.key_fp8 ? d.key_scale : nullptr;
   ap.status = status;
+  const int T = layer_tokens(d);
+  ap.T = T;
+  ap.Wr = d.W + T - 1;
   auto mark = [&](int i) -> cudaError_t {
     return d.stage_events ? cudaEventRecord(static_cast<cudaEvent_t>(d.stage_events[i]), stream)
                           : cudaSuccess;
@@ -349,8 +391,18 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   if (e != cudaSuccess) return e;
   if ((e = mark(1)) != cudaSuccess) return e;
 
-  // a3-a5 read the live prefix L/r of each sequence's pool rows
+  // a3-a5 read the live prefix L/r of each sequence's pool rows (per query
+  // token: token t of a step of T sees L - (T - 1 - t) tokens).  sp / sp_in
+  // count the sequence's rows for its last token (the indexer's tiles); the
+  // token spans (tk) give token b * T + t its own count and score row.
   const Spans sp{d.pool_offsets, d.seq_len_out, 0, r, d.pool_total_rows};
+  auto tokens = [&](const Spans& s) {
+    Spans t = s;
+    t.add = s.add - (T - 1);
+    t.T = T;
+    t.tstride = d.pool_total_rows;
+    return t;
+  };
   const int32_t* idx = nullptr;
   if (d.kind == HSA_LAYER_C4) {
     float* scores = d.scores ? d.scores : reinterpret_cast<float*>(w + L.scores);
@@ -362,12 +414,12 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
     // output lengths overwrite the input ones, the geometry is read from the
     // output lengths after the append instead.
     const bool alias = d.seq_len_out == d.seq_len_in;
-    const Spans sp_in{d.pool_offsets, d.seq_len_in, 1, r, d.pool_total_rows};
+    const Spans sp_in{d.pool_offsets, d.seq_len_in, T, r, d.pool_total_rows};
     const bool fused = layer_fused(d);
     uint32_t* hist = fused ? reinterpret_cast<uint32_t*>(w + L.hist) : nullptr;
     e = launch_indexer(d.iq, d.w, d.key_pool, alias ? sp : sp_in, d.B, d.Hi, d.Di,
                        d.pool_total_rows, scores, status, stream, true, alias ? 0 : 2, hist,
-                       d.key_fp8 ? d.key_scale : nullptr);
+                       d.key_fp8 ? d.key_scale : nullptr, T);
     if (e != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
     if (fused) {
@@ -378,14 +430,16 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
       a.q = d.q;
       a.swa = d.swa;
       a.seq_len = alias ? d.seq_len_out : d.seq_len_in;
-      a.len_add = alias ? 0 : 1;
+      a.len_add = alias ? 1 - T : 1;  // token t: L_in + 1 + t
       a.W = d.W;
+      a.T = T;
+      a.Wr = d.W + T - 1;
       a.extra = d.kv_pool;
-      a.sp = alias ? sp : sp_in;
+      a.sp = tokens(alias ? sp : sp_in);
       a.idx = nullptr;
       a.k = d.k;
       a.max_rows = 0;
-      a.B = d.B;
+      a.B = static_cast<int64_t>(d.B) * T;
       a.Hq = d.Hq;
       a.Dqk = d.Dqk;
       a.Dv = d.Dv;
@@ -396,7 +450,7 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
       a.only_idx_pending = true;
       a.sel_scores = scores;
       a.row_hist = hist;
-      a.cand_ws = topk_cand_area(w + L.topk, d.B, d.pool_total_rows, d.k);
+      a.cand_ws = topk_cand_area(w + L.topk, static_cast<int64_t>(d.B) * T, d.pool_total_rows * T, d.k);
       a.topk_out = d.topk_idx;
       bool pdl = true;
       if (d.q_ready_event) {
@@ -408,8 +462,8 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
       if (e != cudaSuccess) return e;
       return mark(4);
     }
-    e = launch_topk(scores, alias ? sp : sp_in, d.B, d.pool_total_rows, d.k, tidx, nullptr,
-                    w + L.topk, status, stream, d.max_pool_rows, true);
+    e = launch_topk(scores, tokens(alias ? sp : sp_in), d.B * T, d.pool_total_rows * T, d.k, tidx,
+                    nullptr, w + L.topk, status, stream, d.max_pool_rows, true);
     if (e != cudaSuccess) return e;
     if ((e = mark(3)) != cudaSuccess) return e;
     idx = tidx;
@@ -421,14 +475,16 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   a.q = d.q;
   a.swa = d.swa;
   a.seq_len = d.seq_len_out;
-  a.len_add = 0;
+  a.len_add = 1 - T;  // token t: L_out - (T - 1 - t)
   a.W = d.W;
+  a.T = T;
+  a.Wr = d.W + T - 1;
   a.extra = d.kv_pool;
-  a.sp = sp;
+  a.sp = tokens(sp);
   a.idx = idx;
   a.k = d.kind == HSA_LAYER_C4 ? d.k : 0;
   a.max_rows = d.kind == HSA_LAYER_C4 ? 0 : d.max_pool_rows;
-  a.B = d.B;
+  a.B = static_cast<int64_t>(d.B) * T;
   a.Hq = d.Hq;
   a.Dqk = d.Dqk;
   a.Dv = d.Dv;

@@ -352,6 +352,23 @@ typedef struct hsa_layer_desc {
                                hsa_quantize_e4m3 does and step 3 is
                                hsa_indexer_scores_e4m3 */
   float* key_scale;         /* fp32 [pool_total_rows] when key_fp8, else ignored */
+  int32_t T;                /* query tokens per sequence in this step (0 or 1: one; at most
+                               4; C4: T * Hi <= 16) — speculative decoding with a one-layer
+                               multi-token-prediction head verifies the current token and a
+                               draft token together ([LH] §Tích hợp Kernel và Giải mã suy
+                               đoán), T = 2.  The step appends the T tokens in order
+                               (positions L_in .. L_in + T - 1) and token t attends exactly
+                               what it would see had the tokens been decoded one per step:
+                               the window positions [L_t - W, L_t), L_t = L_in + t + 1, and
+                               the L_t / r entries completed up to its position (C4: its own
+                               scores and top-k).  With T > 1 the per-token tensors gain a
+                               token axis after the batch axis: q [B, T, Hq, Dqk], kv_new /
+                               z_new [B, T, Dqk], ik_new / iz_new [B, T, Di], iq
+                               [B, T, Hi, Di], w [B, T, Hi], out [B, T, Hq, Dv], lse
+                               [B, T, Hq], topk_idx [B, T, k], scores [T, pool_total_rows];
+                               the window ring holds W + T - 1 rows per sequence
+                               (swa [B, W + T - 1, Dqk], slot = position mod (W + T - 1));
+                               seq_len_out = seq_len_in + T */
 } hsa_layer_desc;
 
 size_t hsa_layer_decode_workspace_size(const hsa_layer_desc* d);
