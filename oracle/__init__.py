@@ -57,6 +57,7 @@ def _load():
             I64 = ctypes.c_int64
             lib.oracle_hardware_threads.restype = ctypes.c_int
             lib.oracle_compress.argtypes = [P, P, P, I64, I64, I64, I64, P, ctypes.c_int]
+            lib.oracle_compress_overlap.argtypes = [P, P, P, I64, I64, I64, I64, P, ctypes.c_int]
             lib.oracle_indexer_scores.argtypes = [P, P, P, P, I64, I64, I64, P, ctypes.c_int]
             lib.oracle_topk.argtypes = [P, P, I64, I64, P, P, ctypes.c_int]
             lib.oracle_decode_attn.argtypes = [P, P, P, I64, P, P, P, I64, I64, I64, I64, I64,
@@ -68,7 +69,7 @@ def _load():
             lib.oracle_indexer_scores_e4m3.argtypes = [P, P, P, P, P, I64, I64, I64, P,
                                                        ctypes.c_int]
             lib.oracle_bf16_to_double.argtypes = [P, I64, P]
-            for f in ("oracle_compress", "oracle_indexer_scores", "oracle_topk",
+            for f in ("oracle_compress", "oracle_compress_overlap", "oracle_indexer_scores", "oracle_topk",
                       "oracle_decode_attn", "oracle_quantize_e4m3",
                       "oracle_indexer_scores_e4m3"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -174,6 +175,23 @@ def compress(kv, z, b, r: int, threads: int = 1) -> np.ndarray:
     out = np.empty((S, T // r, C), np.float64)
     _check(_load().oracle_compress(_ptr(kv), _ptr(z), _ptr(b), S, T, C, r, _ptr(out), threads),
            "compress")
+    return out
+
+
+def compress_overlap(kv, z, b, r: int, threads: int = 1) -> np.ndarray:
+    """C4 overlap transform: entry n over the 2r-token window of blocks n-1 and n
+    (entry 0 over block 0 alone), per-channel softmax gate with a bias b per
+    window position.
+
+    kv, z: uint16 (bf16) [S, T, C]; b: float32 [2r, C].  Returns float64 [S, T//r, C].
+    [WK] RL 训练侧 ① (C4 overlap transform).
+    """
+    kv, z, b = _c(kv, np.uint16), _c(z, np.uint16), _c(b, np.float32)
+    S, T, C = kv.shape
+    assert z.shape == kv.shape and b.shape == (2 * r, C)
+    out = np.empty((S, T // r, C), np.float64)
+    _check(_load().oracle_compress_overlap(_ptr(kv), _ptr(z), _ptr(b), S, T, C, r, _ptr(out),
+                                           threads), "compress_overlap")
     return out
 
 

@@ -22,6 +22,9 @@
 //   oracle_compress        hand-worked blocks, r=1 identity, constant-gate mean,
 //                          shift invariance, convexity, linearity, long-double
 //                          brute force
+//   oracle_compress_overlap  hand-worked windows, -inf bias on the previous
+//                          block reduces to oracle_compress, first block,
+//                          constant-gate window mean, scipy softmax
 //   oracle_indexer_scores  hand-worked example, one-hot reduction, w-linearity,
 //                          non-negativity, long-double brute force
 //   oracle_topk            hand-worked example, full sort of (value, index),
@@ -191,6 +194,44 @@ int oracle_compress(const uint16_t* kv, const uint16_t* z, const float* b, int64
       for (int64_t i = 1; i < r; ++i) m = std::max(m, logit[i]);
       double num = 0.0, den = 0.0;
       for (int64_t i = 0; i < r; ++i) {
+        const double e = std::exp(logit[i] - m);
+        num += e * val[i];
+        den += e;
+      }
+      out[(s * nblk + n) * C + ch] = num / den;
+    }
+  });
+  return 0;
+}
+
+// C4 overlap transform ([WK] §RL 训练侧 ①: C4's "overlap transform", under
+// which neighbouring compressed entries share tokens, so a context-parallel
+// split cannot compress its first block without its neighbour's tokens).  The
+// pages name it without defining it; the library's reading: entry n is the
+// gated softmax average over a window of 2r tokens with stride r — block n's
+// own r tokens and the r tokens of block n-1 before them —
+//     c[n, ch] = sum_{i in window} softmax_i(z[n*r-r+i, ch] + b[i, ch]) * kv[n*r-r+i, ch],
+// window i in [0, 2r), positions before the sequence's start absent (entry 0
+// uses i in [r, 2r) only); b is per (position in the window, channel).
+//   kv, z : bf16 [S, T, C]   b : fp32 [2r, C]   out : fp64 [S, T/r, C]
+int oracle_compress_overlap(const uint16_t* kv, const uint16_t* z, const float* b, int64_t S,
+                            int64_t T, int64_t C, int64_t r, double* out, int threads) {
+  if (r <= 0 || S < 0 || T < 0 || C <= 0) return 1;
+  const int64_t nblk = T / r;
+  parallel_for(S * nblk, threads, [&](int64_t sn) {
+    const int64_t s = sn / nblk, n = sn % nblk;
+    const int64_t i0 = n == 0 ? r : 0;  // the window's first present position
+    for (int64_t ch = 0; ch < C; ++ch) {
+      std::vector<double> logit, val;
+      for (int64_t i = i0; i < 2 * r; ++i) {
+        const int64_t t = n * r - r + i;
+        logit.push_back(bf16_to_double(z[(s * T + t) * C + ch]) + static_cast<double>(b[i * C + ch]));
+        val.push_back(bf16_to_double(kv[(s * T + t) * C + ch]));
+      }
+      double m = logit[0];
+      for (double l : logit) m = std::max(m, l);
+      double num = 0.0, den = 0.0;
+      for (size_t i = 0; i < logit.size(); ++i) {
         const double e = std::exp(logit[i] - m);
         num += e * val[i];
         den += e;

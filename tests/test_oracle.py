@@ -593,3 +593,54 @@ def test_layer_two_token_step_equals_two_single_token_steps(oracle_mod, kind, ph
     # a block completed in the step: the pool's last live row was written in it
     done = [(int(Lin[b]) + t + 1) % r == 0 for b in range(3) for t in range(2)]
     assert any(done) == (phase in ((0, 1) if kind == 4 else (0, 1)))
+
+
+# ---------------------------------------------------------------- C4 overlap transform
+
+def test_compress_overlap_worked_example(oracle_mod):
+    g = golden("compress_overlap_worked.json")
+    kv = bf16_bits(np.array(g["kv"], np.float32)).reshape(1, -1, 1)
+    z = bf16_bits(np.array(g["z"], np.float32)).reshape(1, -1, 1)
+    b = np.array(g["b"], np.float32).reshape(-1, 1)
+    got = oracle_mod.compress_overlap(kv, z, b, g["r"])[0, :, 0]
+    want = np.array([closed_form(e) for e in g["expected"]])
+    assert np.allclose(got, want, rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("r", [1, 4, 7])
+def test_compress_overlap_special_cases_reduce_to_the_compressor(oracle_mod, r):
+    """A bias of -inf over the previous block's positions weighs it 0: the
+    result is the (pinned) non-overlapping compressor with the bias of the
+    block's own positions, bit for bit; entry 0 (no previous block) equals it
+    for any bias."""
+    S, T, C = 2, 9 * r + (r - 1), 24
+    kv = _normal_bits(f"ov.kv{r}", (S, T, C))
+    z = _normal_bits(f"ov.z{r}", (S, T, C))
+    b = (np.random.default_rng(RNG_SEED + r).standard_normal((2 * r, C)) * 0.5).astype(np.float32)
+    own = oracle_mod.compress(kv, z, np.ascontiguousarray(b[r:]), r)
+    ov = oracle_mod.compress_overlap(kv, z, b, r)
+    assert np.array_equal(ov[:, 0], own[:, 0])
+    bm = b.copy()
+    bm[:r] = -np.inf
+    assert np.array_equal(oracle_mod.compress_overlap(kv, z, bm, r), own)
+
+
+def test_compress_overlap_constant_gate_and_library_softmax(oracle_mod):
+    r, S, T, C = 4, 2, 40, 16
+    kv = _normal_bits("ov.kvc", (S, T, C))
+    zeros = np.zeros((S, T, C), np.uint16)                   # bf16 +0.0
+    got = oracle_mod.compress_overlap(kv, zeros, np.zeros((2 * r, C), np.float32), r)
+    v = bf16_values(kv)
+    for n in range(T // r):
+        lo = max(0, n * r - r)
+        assert np.allclose(got[:, n], v[:, lo:n * r + r].mean(axis=1), rtol=1e-13, atol=1e-15)
+    z = _normal_bits("ov.zc", (S, T, C))
+    b = (np.random.default_rng(RNG_SEED + 9).standard_normal((2 * r, C)) * 0.5).astype(np.float32)
+    got = oracle_mod.compress_overlap(kv, z, b, r)
+    zv = bf16_values(z)
+    for n in range(T // r):
+        lo = max(0, n * r - r)
+        i0 = lo - (n * r - r)
+        logits = zv[:, lo:n * r + r] + b[i0:].astype(np.float64)[None]
+        wts = scipy.special.softmax(logits, axis=1)
+        assert np.allclose(got[:, n], (wts * v[:, lo:n * r + r]).sum(axis=1), rtol=1e-12, atol=1e-14)
