@@ -816,8 +816,9 @@ def run_profile(ctx=None):
     """Two layer steps of the bench workload (the first warms up), for ncu."""
     _lib.load(build_if_missing=True)
     L, g = build_workload(0, ctx)
-    out, lse, seq_out, idx, scores = layer_outputs(g)
-    desc = _lib.layer_desc(g, out, lse, seq_out, idx, scores)
+    out, lse, seq_out, _, scores = layer_outputs(g)
+    # as the bench's step: the attention output and log-sum-exp, no index list
+    desc = _lib.layer_desc(g, out, lse, seq_out, None, scores)
     ws = _lib.workspace(_lib.hsa_layer_decode_workspace_size(desc))
     for _ in range(2):
         _lib.hsa_layer_decode(desc, ws=ws)

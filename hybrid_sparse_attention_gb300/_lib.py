@@ -35,6 +35,7 @@ SIGNATURES = {
     "hsa_version": (I32, []),
     "hsa_workspace_status": (I32, [P, P, P]),
     "hsa_compress": (I32, [P, P, P, I64, I64, I64, I64, P, I32, P]),
+    "hsa_compress_overlap": (I32, [P, P, P, I64, I64, I64, I64, P, I32, P]),
     "hsa_indexer_scores_workspace_size": (SZ, []),
     "hsa_indexer_scores": (I32, [P, P, P, P, I64, I64, I64, I64, P, P, SZ, P]),
     "hsa_decode_attn_workspace_size": (SZ, [I64, I64, I64, I64, I64, I64]),
@@ -126,6 +127,19 @@ def hsa_compress(kv, z, b, r: int, out=None, out_dtype=torch.bfloat16, stream=No
         out = torch.empty(S, T // r, C, dtype=out_dtype, device=kv.device)
     code = {torch.float32: HSA_F32, torch.bfloat16: HSA_BF16}[out.dtype]
     _call("hsa_compress", _dev(kv, torch.bfloat16, "kv"), _dev(z, torch.bfloat16, "z"),
+          _dev(b, torch.float32, "b"), S, T, C, r, _dev(out, out.dtype, "out"), code,
+          _stream(stream))
+    return out
+
+
+def hsa_compress_overlap(kv, z, b, r: int, out=None, out_dtype=torch.bfloat16, stream=None):
+    """C4 overlap transform: kv, z bf16 [S, T, C]; b fp32 [2r, C] -> out [S, T//r, C]
+    (entry n over the window of blocks n-1 and n)."""
+    S, T, C = kv.shape
+    if out is None:
+        out = torch.empty(S, T // r, C, dtype=out_dtype, device=kv.device)
+    code = {torch.float32: HSA_F32, torch.bfloat16: HSA_BF16}[out.dtype]
+    _call("hsa_compress_overlap", _dev(kv, torch.bfloat16, "kv"), _dev(z, torch.bfloat16, "z"),
           _dev(b, torch.float32, "b"), S, T, C, r, _dev(out, out.dtype, "out"), code,
           _stream(stream))
     return out

@@ -157,21 +157,34 @@ hsa_status_t hsa_workspace_status(void* ws, void* stream, uint32_t* bits) {
   return HSA_OK;
 }
 
-hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,
-                          int64_t C, int64_t r, void* out, int out_dtype, void* stream) {
+static hsa_status_t compress_call(const void* kv, const void* z, const float* b, int64_t S,
+                                  int64_t T, int64_t C, int64_t r, void* out, int out_dtype,
+                                  void* stream, bool overlap) {
   HSA_CHECK(S >= 0 && T >= 0, HSA_ERR_INVALID_ARG, "S=%lld T=%lld must be >= 0", (long long)S,
             (long long)T);
   HSA_CHECK(C > 0 && C % 8 == 0, HSA_ERR_UNSUPPORTED, "C=%lld must be a positive multiple of 8",
             (long long)C);
-  HSA_CHECK(r >= 1 && r <= 4096, HSA_ERR_UNSUPPORTED, "r=%lld outside [1, 4096]", (long long)r);
+  HSA_CHECK(r >= 1 && r <= (overlap ? 2048 : 4096), HSA_ERR_UNSUPPORTED, "r=%lld outside [1, %d]",
+            (long long)r, overlap ? 2048 : 4096);
   HSA_CHECK(out_dtype == HSA_F32 || out_dtype == HSA_BF16, HSA_ERR_INVALID_ARG, "bad out_dtype");
   if (S == 0 || T / r == 0) return HSA_OK;
   HSA_CHECK(kv && z && b && out, HSA_ERR_INVALID_ARG, "null pointer");
   HSA_CHECK(aligned(kv, 16) && aligned(z, 16) && aligned(b, 16) && aligned(out, 16),
             HSA_ERR_INVALID_ARG, "kv, z, b and out must be 16-byte aligned");
   return cuda_status(launch_compress(kv, z, b, S, T, C, r, out, out_dtype,
-                                     static_cast<cudaStream_t>(stream)),
+                                     static_cast<cudaStream_t>(stream), overlap),
                      "compress launch");
+}
+
+hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,
+                          int64_t C, int64_t r, void* out, int out_dtype, void* stream) {
+  return compress_call(kv, z, b, S, T, C, r, out, out_dtype, stream, false);
+}
+
+hsa_status_t hsa_compress_overlap(const void* kv, const void* z, const float* b, int64_t S,
+                                  int64_t T, int64_t C, int64_t r, void* out, int out_dtype,
+                                  void* stream) {
+  return compress_call(kv, z, b, S, T, C, r, out, out_dtype, stream, true);
 }
 
 size_t hsa_indexer_scores_workspace_size(void) { return kWsHeader; }

@@ -61,7 +61,9 @@ HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, in
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const float mn = fmaxf(p.m[c], gm[c]);
-      const float alpha = __expf(p.m[c] - mn);  // 0 on the first group (m = -inf)
+      // 0 while nothing finite has been seen (m = -inf): a -inf logit (a
+      // masked position) weighs 0 and never makes -inf - -inf
+      const float alpha = p.m[c] == -INFINITY ? 0.f : __expf(p.m[c] - mn);
       p.l[c] *= alpha;
       p.acc[c] *= alpha;
       p.m[c] = mn;
@@ -71,7 +73,7 @@ HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, in
       if (j < g) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const float e = __expf(x[j][c] - p.m[c]);  // softmax numerator
+          const float e = x[j][c] == -INFINITY ? 0.f : __expf(x[j][c] - p.m[c]);  // softmax numerator
           p.l[c] += e;
           p.acc[c] = fmaf(e, v[j][c], p.acc[c]);    // dot
         }

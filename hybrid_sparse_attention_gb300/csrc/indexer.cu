@@ -206,7 +206,9 @@ HSA_DEVINL void quantize_queries(const IndexerParams& p, Shared& sh, uint8_t* q8
   tc::mbar_arrive(&sh.q8_full[buf]);
 }
 
-template <bool kFp8>
+// kMulti: more than one query token per sequence (p.T > 1); the single-token
+// instantiation carries none of the per-token bookkeeping.
+template <bool kFp8, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap qmap,
                                                              IndexerParams p) {
@@ -403,8 +405,8 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_const
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     SeqCursor cur;
     float wv[kQRows];
-    int64_t nt[kMaxT];  // each token's live rows of the current sequence
-    const int hpt = p.Hi / p.T;  // heads per token
+    int64_t nt[kMulti ? kMaxT : 1];  // (kMulti) each token's live rows of the current sequence
+    const int hpt = p.Hi / p.T;      // heads per token
     // (kFp8) the E4M3 queries of the range's first two sequences; `ahead` is the
     // sequence of the last buffer written, `made` how many were written
     SeqCursor ahead;
@@ -458,14 +460,16 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_const
             wv[h] = h < p.Hi ? __ldg(p.w + static_cast<int64_t>(cur.b) * p.Hi + h) : 0.f;
         }
         // each token's live rows (the last token's are the sequence's count)
+        if (kMulti) {
 #pragma unroll
-        for (int q = 0; q < kMaxT; ++q) {
-          int64_t n = cur.count;
-          if (q < p.T - 1 && p.sp.seq_len) {
-            n = (static_cast<int64_t>(p.sp.seq_len[cur.b]) + p.sp.add - (p.T - 1 - q)) / p.sp.ratio;
-            n = n < 0 ? 0 : (n > cur.count ? cur.count : n);
+          for (int q = 0; q < kMaxT; ++q) {
+            int64_t n = cur.count;
+            if (q < p.T - 1 && p.sp.seq_len) {
+              n = (static_cast<int64_t>(p.sp.seq_len[cur.b]) + p.sp.add - (p.T - 1 - q)) / p.sp.ratio;
+              n = n < 0 ? 0 : (n > cur.count ? cur.count : n);
+            }
+            nt[q] = q < p.T ? n : 0;
           }
-          nt[q] = q < p.T ? n : 0;
         }
       }
       const int64_t piece = t - cur.first;
@@ -500,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_const
       }
       tc::fence_before_sync();
       tc::mbar_arrive(&sh.acc_empty[a]);
-      if (p.T == 1) {
+      if (!kMulti) {
         if (r < left) {
           float sc = 0.f;
 #pragma unroll
@@ -519,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_const
         // token q: heads [q * hpt, (q + 1) * hpt), the rows visible to it
         const int64_t jrow = piece * kTileRows + r;  // row within the sequence
 #pragma unroll
-        for (int q = 0; q < kMaxT; ++q) {
+        for (int q = 0; q < (kMulti ? kMaxT : 1); ++q) {
           if (q < p.T && jrow < nt[q] && r < left) {
             float sc = 0.f;
 #pragma unroll
@@ -587,7 +591,8 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
   }
   if (e != cudaSuccess) return e;
   const size_t smem = indexer_smem_bytes(Di, fp8);
-  auto kernel = fp8 ? indexer_kernel<true> : indexer_kernel<false>;
+  auto kernel = fp8 ? (T > 1 ? indexer_kernel<true, true> : indexer_kernel<true, false>)
+                    : (T > 1 ? indexer_kernel<false, true> : indexer_kernel<false, false>);
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(fp8 ? smem : indexer_smem_bytes(128)));
   if (e != cudaSuccess) return e;

@@ -65,8 +65,10 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return launch_kc(kernel, grid, block, smem, stream, pdl, 0u, args...);
 }
 
+// overlap: the C4 overlap transform (entry n over blocks n-1 and n, b [2r, C]).
 cudaError_t launch_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,
-                            int64_t C, int64_t r, void* out, int out_dtype, cudaStream_t stream);
+                            int64_t C, int64_t r, void* out, int out_dtype, cudaStream_t stream,
+                            bool overlap = false);
 
 // 2-D bf16 tensor map (inner dimension contiguous) for TMA tiled loads.
 cudaError_t make_tmap_2d_bf16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,

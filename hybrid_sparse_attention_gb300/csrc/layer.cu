@@ -100,10 +100,12 @@ HSA_DEVINL void compress_block(const uint4* kv, const uint4* z, const float* bia
 // block's last row).
 constexpr int kShortBlock = 4;
 
+template <int kT>  // tokens appended (p.T == kT)
 HSA_DEVINL void append_short(const AppendParams& p, int b) {
   __shared__ float s_key[kMaxKeyDi];  // E4M3 pool: the completed block's fp32 key row
   const int cq = p.Dqk / 8, ci = p.kind == HSA_LAYER_C4 ? p.Di / 8 : 0;
-  const int r = p.r, T = p.T;
+  const int r = p.r;
+  constexpr int T = kT;
   const int32_t lin = p.seq_len_in[b];
   const int64_t o0 = p.pool_offsets[b], o1 = p.pool_offsets[b + 1];
   // the step's token whose position completes a block (at most one: T <= r)
@@ -119,13 +121,11 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
     uint4* ring_v = (key ? p.ik_ring : p.kv_ring) + static_cast<int64_t>(b) * r * n8 + c;
     uint4* ring_z = (key ? p.iz_ring : p.z_ring) + static_cast<int64_t>(b) * r * n8 + c;
     const float* bias = (key ? p.b_ik : p.b_kv) + c * 8;
-    uint4 nv[kMaxT], nz[kMaxT];  // the step's new rows (token t: row b * T + t)
+    uint4 nv[kT], nz[kT];  // the step's new rows (token t: row b * T + t)
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) {
-      if (t < T) {
-        nv[t] = nv_src[(static_cast<int64_t>(b) * T + t) * n8 + c];
-        nz[t] = nz_src[(static_cast<int64_t>(b) * T + t) * n8 + c];
-      }
+    for (int t = 0; t < kT; ++t) {
+      nv[t] = nv_src[(static_cast<int64_t>(b) * T + t) * n8 + c];
+      nz[t] = nz_src[(static_cast<int64_t>(b) * T + t) * n8 + c];
     }
     uint4 rv[kShortBlock], rz[kShortBlock];
     float4 b0[kShortBlock], b1[kShortBlock];
@@ -141,13 +141,11 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
     }
     // the new rows into the window ring and the in-flight rings, in order
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) {
-      if (t < T) {
-        const int64_t pos = static_cast<int64_t>(lin) + t;
-        if (!key) p.swa[(static_cast<int64_t>(b) * p.Wr + pos % p.Wr) * cq + c] = nv[t];
-        ring_v[(pos % r) * n8] = nv[t];
-        ring_z[(pos % r) * n8] = nz[t];
-      }
+    for (int t = 0; t < kT; ++t) {
+      const int64_t pos = static_cast<int64_t>(lin) + t;
+      if (!key) p.swa[(static_cast<int64_t>(b) * p.Wr + pos % p.Wr) * cq + c] = nv[t];
+      ring_v[(pos % r) * n8] = nv[t];
+      ring_z[(pos % r) * n8] = nz[t];
     }
     if (tcomp < 0) continue;
     const int64_t n = (pc + 1) / r - 1;
@@ -166,8 +164,8 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
         const int64_t tq = pc - r + 1 + i - lin;  // token index of the row, if new
         uint4 zi = rz[i], vi = rv[i];
 #pragma unroll
-        for (int t = 0; t < kMaxT; ++t)
-          if (t < T && tq == t) {
+        for (int t = 0; t < kT; ++t)
+          if (tq == t) {
             zi = nz[t];
             vi = nv[t];
           }
@@ -231,53 +229,63 @@ HSA_DEVINL void append_short(const AppendParams& p, int b) {
   if (threadIdx.x == 0) p.seq_len_out[b] = lin + T;
 }
 
+template <int kT>  // tokens per step of the short-block path (p.T == kT there)
 __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendParams p) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
   if (p.r <= kShortBlock) {
-    append_short(p, b);
+    append_short<kT>(p, b);
     return;
   }
   const int64_t lin = p.seq_len_in[b];
   const int cq = p.Dqk / 8, ci = p.Di / 8;
   const int64_t o0 = p.pool_offsets[b], o1 = p.pool_offsets[b + 1];
   __syncthreads();  // seq_len_in read by every thread before it may be overwritten
-  for (int t = 0; t < p.T; ++t) {
-    const int64_t pos = lin + t;
-    const int64_t slot_w = pos % p.Wr, slot_r = pos % p.r;
-    const int64_t row = static_cast<int64_t>(b) * p.T + t;
-    // a1: token t's rows into the window ring and the in-flight rings
-    for (int c = threadIdx.x; c < cq; c += blockDim.x) {
-      const uint4 kv = p.kv_new[row * cq + c];
-      const uint4 z = p.z_new[row * cq + c];
-      p.swa[(static_cast<int64_t>(b) * p.Wr + slot_w) * cq + c] = kv;
-      p.kv_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = kv;
-      p.z_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = z;
-    }
-    if (p.kind == HSA_LAYER_C4) {
-      for (int c = threadIdx.x; c < ci; c += blockDim.x) {
-        p.ik_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] = p.ik_new[row * ci + c];
-        p.iz_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] = p.iz_new[row * ci + c];
+  // a1: tokens [t_lo, t_hi)'s rows into the window ring and the in-flight rings
+  auto write_rows = [&](int t_lo, int t_hi) {
+    for (int t = t_lo; t < t_hi; ++t) {
+      const int64_t pos = lin + t;
+      const int64_t slot_w = pos % p.Wr, slot_r = pos % p.r;
+      const int64_t row = static_cast<int64_t>(b) * p.T + t;
+      for (int c = threadIdx.x; c < cq; c += blockDim.x) {
+        const uint4 kv = p.kv_new[row * cq + c];
+        const uint4 z = p.z_new[row * cq + c];
+        p.swa[(static_cast<int64_t>(b) * p.Wr + slot_w) * cq + c] = kv;
+        p.kv_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = kv;
+        p.z_ring[(static_cast<int64_t>(b) * p.r + slot_r) * cq + c] = z;
+      }
+      if (p.kind == HSA_LAYER_C4) {
+        for (int c = threadIdx.x; c < ci; c += blockDim.x) {
+          p.ik_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] = p.ik_new[row * ci + c];
+          p.iz_ring[(static_cast<int64_t>(b) * p.r + slot_r) * ci + c] = p.iz_new[row * ci + c];
+        }
       }
     }
-    __syncthreads();  // ring writes visible to the block
-    if ((pos + 1) % p.r != 0) continue;
-    // a2: the block is complete -> compress it into pool row (pos + 1)/r - 1
-    // (before a later token of the step writes the next block's first slot)
-    const int64_t n = (pos + 1) / p.r - 1;
+  };
+  // the step's token that completes a block (at most one: T <= r), or -1
+  int tcomp = -1;
+  for (int t = 0; t < p.T; ++t)
+    if ((lin + t + 1) % p.r == 0) tcomp = t;
+  write_rows(0, tcomp >= 0 ? tcomp + 1 : p.T);
+  __syncthreads();  // ring writes visible to the block
+  if (tcomp >= 0) {
+    // a2: the block is complete -> compress it into pool row (pos + 1)/r - 1,
+    // before the step's later tokens write the next block's first slots
+    const int64_t n = (lin + tcomp + 1) / p.r - 1;
     if (o0 < 0 || o1 > p.pool_total_rows || o0 + n >= o1) {
       if (threadIdx.x == 0) set_status(p.status, HSA_DEV_BOUNDS);
-      continue;
+    } else {
+      compress_block(p.kv_ring + static_cast<int64_t>(b) * p.r * cq,
+                     p.z_ring + static_cast<int64_t>(b) * p.r * cq, p.b_kv, p.r, p.Dqk,
+                     p.kv_pool + (o0 + n) * cq);
+      if (p.kind == HSA_LAYER_C4)
+        compress_block(p.ik_ring + static_cast<int64_t>(b) * p.r * ci,
+                       p.iz_ring + static_cast<int64_t>(b) * p.r * ci, p.b_ik, p.r, p.Di,
+                       p.key_pool + (o0 + n) * ci);
     }
-    compress_block(p.kv_ring + static_cast<int64_t>(b) * p.r * cq,
-                   p.z_ring + static_cast<int64_t>(b) * p.r * cq, p.b_kv, p.r, p.Dqk,
-                   p.kv_pool + (o0 + n) * cq);
-    if (p.kind == HSA_LAYER_C4)
-      compress_block(p.ik_ring + static_cast<int64_t>(b) * p.r * ci,
-                     p.iz_ring + static_cast<int64_t>(b) * p.r * ci, p.b_ik, p.r, p.Di,
-                     p.key_pool + (o0 + n) * ci);
-    __syncthreads();  // the block read before the next token's rows
+    __syncthreads();  // the block read before the later tokens' rows
+    write_rows(tcomp + 1, p.T);
   }
   if (threadIdx.x == 0) p.seq_len_out[b] = static_cast<int32_t>(lin + p.T);
 }
@@ -386,7 +394,11 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   };
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return e;
-  layer_append_kernel<<<d.B, kAppendThreads, 0, stream>>>(ap);
+  // (one instantiation per token count: the rows of a step live in registers)
+  if (T == 1) layer_append_kernel<1><<<d.B, kAppendThreads, 0, stream>>>(ap);
+  else if (T == 2) layer_append_kernel<2><<<d.B, kAppendThreads, 0, stream>>>(ap);
+  else if (T == 3) layer_append_kernel<3><<<d.B, kAppendThreads, 0, stream>>>(ap);
+  else layer_append_kernel<4><<<d.B, kAppendThreads, 0, stream>>>(ap);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if ((e = mark(1)) != cudaSuccess) return e;

@@ -99,6 +99,22 @@ hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t
                           int64_t C, int64_t r, void* out, int out_dtype, void* stream);
 
 /* ------------------------------------------------------------------------
+ * C4 overlap transform — [WK] §RL 训练侧 ① (neighbouring compressed entries
+ * share tokens, so a context-parallel split needs its neighbour's tokens).
+ * The pages name it without a definition; the library's reading: entry n is
+ * the gated average over the 2r-token window of blocks n-1 and n,
+ *   out[s, n, ch] = sum_{i in [i0, 2r)} softmax_i(z[s, n*r-r+i, ch] + b[i, ch])
+ *                                        * kv[s, n*r-r+i, ch],
+ * i0 = r for n = 0 (no block before it), else 0; b has one row per window
+ * position.  Arithmetic, output and requirements as hsa_compress, with
+ * 1 <= r <= 2048 and b fp32 [2r, C].  A bias of -inf masks its position (the
+ * window's other positions must hold a finite logit).
+ * ---------------------------------------------------------------------- */
+hsa_status_t hsa_compress_overlap(const void* kv, const void* z, const float* b, int64_t S,
+                                  int64_t T, int64_t C, int64_t r, void* out, int out_dtype,
+                                  void* stream);
+
+/* ------------------------------------------------------------------------
  * Indexer scores — [KD] §Flujo de Inferencia step 6 and §Arquitectura del
  * Sistema (the DSA indexer whose top-k picks the compressed candidates); [WK]
  * §RL 训练侧 (the attention indexer works like an MoE router).

@@ -65,3 +65,60 @@ def test_compress_empty_and_partial_blocks():
     kv = torch.zeros(2, 3, 16, dtype=torch.bfloat16, device="cuda")
     out = _lib.hsa_compress(kv, kv, torch.zeros(4, 16, device="cuda"), 4)
     assert out.shape == (2, 0, 16)
+
+
+# ---------------------------------------------------------------- C4 overlap transform
+
+@pytest.mark.parametrize("S,T,C,r", [(2, 1024, 512, 4), (3, 37, 24, 4), (1, 300, 16, 7),
+                                     (2, 16, 8, 1), (1, 1024, 64, 128), (4, 4096, 576, 4)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_compress_overlap_matches_oracle(oracle_mod, S, T, C, r, out_dtype):
+    """Entry n over the 2r-token window of blocks n-1 and n (entry 0 over
+    block 0 alone), a bias per window position; ragged tails dropped."""
+    kv, z, _ = _inputs(S, T, C, r, f"ov.{S}.{T}.{C}.{r}")
+    b = synth.normal(SEED, f"t.bov.{S}.{T}.{C}.{r}", (2 * r, C), std=0.5)
+    out = _lib.hsa_compress_overlap(kv.cuda(), z.cuda(), b.cuda(), r, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    ref = oracle_mod.compress_overlap(bf16_bits(kv), bf16_bits(z), b.numpy(), r, threads=8)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert got.shape == ref.shape
+    err = rel_err(got, ref)
+    assert err.max() <= 5e-3, f"max rel err {err.max():.3e}"
+    if out_dtype == torch.float32:
+        assert err.max() <= 1e-4
+
+
+def test_compress_overlap_masked_previous_block(oracle_mod):
+    """A bias of -inf over the previous block's window positions masks them:
+    the result is the non-overlapping compressor's (GPU against the oracle of
+    both forms)."""
+    S, T, C, r = 2, 512, 64, 4
+    kv, z, b = _inputs(S, T, C, r, "ovm")
+    bm = torch.cat([torch.full((r, C), float("-inf")), b], 0).contiguous()
+    out = _lib.hsa_compress_overlap(kv.cuda(), z.cuda(), bm.cuda(), r, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    ref = oracle_mod.compress(bf16_bits(kv), bf16_bits(z), b.numpy(), r)
+    assert np.array_equal(ref, oracle_mod.compress_overlap(bf16_bits(kv), bf16_bits(z), bm.numpy(), r))
+    assert np.isfinite(got).all() and rel_err(got, ref).max() <= 1e-4
+
+
+def test_compress_overlap_full_size_sampled(oracle_mod):
+    """The standalone workload (32 x 65,536 x 512) with the overlap transform at
+    r = 4; the oracle checks a seeded sample of (sequence, entry) outputs."""
+    S, T, C, r = 32, 65536, 512, 4
+    kv = synth.normal_bf16(SEED, "compress.kv", (S, T, C), device="cuda")
+    z = synth.normal_bf16(SEED, "compress.z", (S, T, C), device="cuda")
+    b = synth.normal(SEED, "compress.bov.4", (2 * r, C), std=0.5, device="cuda")
+    out = _lib.hsa_compress_overlap(kv, z, b, r)
+    torch.cuda.synchronize()
+    nblk = T // r
+    picks = synth.randint(SEED, "compress.sample.ov", 24, 0, S * nblk - 1).tolist() + [0, nblk, S * nblk - 1]
+    for p in picks:
+        s, n = divmod(int(p), nblk)
+        lo = max(0, n - 1) * r
+        ref = oracle_mod.compress_overlap(bf16_bits(kv[s:s + 1, lo:(n + 1) * r]),
+                                          bf16_bits(z[s:s + 1, lo:(n + 1) * r]),
+                                          b.cpu().numpy(), r)[0, -1]
+        got = out[s, n].float().cpu().numpy()
+        assert rel_err(got, ref).max() <= 5e-3
