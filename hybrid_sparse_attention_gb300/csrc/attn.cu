@@ -62,8 +62,8 @@ constexpr uint32_t kPairBytes = 2 * kSliceBytes;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxCl = 4;           // splits merged inside one cluster
 constexpr uint32_t kUnitBytes = kKeys * 16 * 4;  // one merge unit: 128 lanes x 16 fp32 columns
-static_assert(16 * kUnitBytes <= kRing * kPairBytes, "a split's O^T units fit its ring");
-constexpr size_t kMergeScratch = 8 * 16 * 32 * 4;  // eight warps' 16 x 32 fp32 transpose tiles
+static_assert(16 * kUnitBytes <= kRing * kPairBytes, "the units a split receives fit its ring");
+constexpr size_t kMergeScratch = 8 * 2 * 16 * 32 * 4;  // eight warps' two 16 x 32 fp32 transpose tiles
 
 // Dynamic shared memory after the ring: the Q region (Q during pass 1; then
 // the odd tiles' P^T buffer; at the end the merge's transpose tiles), then the
@@ -528,19 +528,14 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
     }
   }
   __syncthreads();
-  // (5) every split's share of the list, every listed row prefetched into L2
-  // for the splits' gathers, and the list kept for the ordered copy
+  // (5) every split's share of the list (the list kept for the ordered copy),
+  // the splits signalled, and then this split's own rows prefetched into L2
+  // for its gather (the other splits start theirs at once)
   for (int e = t; e < p.k; e += kThreads) {
     const bool live = e < static_cast<int>(nsel);
     const uint64_t x = live ? sbuf[e] : 0ull;
     const uint32_t j = live ? 0xffffffffu - static_cast<uint32_t>(x) : 0u;
-    if (live) {
-      const uint16_t* rowp = p.extra + (g.off + j) * p.Dqk;
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rowp),
-                   "r"(static_cast<uint32_t>(p.Dqk * 2))
-                   : "memory");
-      if (p.topk_out) p.cand_ws[g.soff + e] = x;
-    }
+    if (live && p.topk_out) p.cand_ws[g.soff + e] = x;
     const int q = static_cast<int>((g.n_swa + e) / p.sps);  // the split attending entry e
     uint16_t* dst = &sh.sel[e - share_first(p, g.n_swa, q)];
     const uint16_t v = live ? static_cast<uint16_t>(j) : uint16_t(0xffff);
@@ -552,6 +547,14 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
   if (t == 0) {
     asm volatile("fence.acq_rel.cluster;" ::: "memory");
     for (int q = 0; q < p.S; ++q) mbar_arrive_cluster(map_rank(&sh.sel_full, static_cast<uint32_t>(q)));
+  }
+  for (int e = t; e < static_cast<int>(nsel); e += kThreads) {
+    if ((g.n_swa + e) / p.sps != static_cast<int64_t>(rank)) continue;
+    const uint32_t j = 0xffffffffu - static_cast<uint32_t>(sbuf[e]);
+    const uint16_t* rowp = p.extra + (g.off + j) * p.Dqk;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rowp),
+                 "r"(static_cast<uint32_t>(p.Dqk * 2))
+                 : "memory");
   }
 }
 
@@ -593,13 +596,17 @@ HSA_DEVINL void write_lse(const AttnParams& p, int b, int g, int s, int h, float
 }
 
 // Merge of the S splits of one (token, head group) inside their cluster (all
-// threads of every CTA call it).  Each split copies its raw O^T from TMEM into
-// its own ring (free by now) in units of 128 value channels x 16 heads and
-// publishes its m and l; unit u is then finished by split u % S, which reads
-// the unit from every split through distributed shared memory and writes
-//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
-// The loops are kept rolled: this code runs once per launch, so its size (the
-// instruction fetches) costs more than its loop overhead.
+// threads of every CTA call it).  Unit u (128 value channels x 16 heads of
+// O^T) is finished by split u % S.  After a cluster barrier (every split's ring
+// is free), each split reads from TMEM the units the other splits finish and
+// stores them, as posted distributed-shared-memory stores, into the owner's
+// ring (slot: the sender's place among the others x units per owner + u / S);
+// m and l go to every split.  After a second barrier every owner combines its
+// own part (from TMEM) with the received parts (local shared memory):
+//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s,
+// with no remote load anywhere.  The loops are kept rolled: this code runs
+// once per launch, so its size (the instruction fetches) costs more than its
+// loop overhead.
 template <int kN>
 HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, uint8_t* scratch,
                               uint32_t tmem, int b, int g, bool own, int TC, int NMT) {
@@ -608,30 +615,17 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
   const int S = p.S;
   const int rank = static_cast<int>(cluster_rank());
   const int U = NMT * kQ;
+  const int upo = (U + S - 1) / S;  // units per owner
   // warp w reads TMEM lane quarter w & 3 (value channels); the two warps of a
   // quarter (halves hw) take alternate units
   const int quarter = warp & 3, hw = warp >> 2, row = quarter * 32 + lane;
-  if (own) {
-    tc::fence_after_sync();
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    // two units per round: both TMEM loads in flight before one wait
-#pragma unroll 1
-    for (int u = hw; u < U; u += 4) {
-      uint32_t a[16], c[16];
-      const bool two = u + 2 < U;
-      tc::tmem_ld16(lane_addr + (TC + u / kQ) * kN + (u % kQ) * 16, a);
-      const int u2 = two ? u + 2 : u;
-      tc::tmem_ld16(lane_addr + (TC + u2 / kQ) * kN + (u2 % kQ) * 16, c);
-      tc::tmem_ld_wait();
-      uint4* d = reinterpret_cast<uint4*>(ring + u * kUnitBytes + row * 16);
-      uint4* d2 = reinterpret_cast<uint4*>(ring + u2 * kUnitBytes + row * 16);
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        d[c4 * kKeys] = make_uint4(a[4 * c4], a[4 * c4 + 1], a[4 * c4 + 2], a[4 * c4 + 3]);
-        d2[c4 * kKeys] = make_uint4(c[4 * c4], c[4 * c4 + 1], c[4 * c4 + 2], c[4 * c4 + 3]);
-      }
-    }
-  }
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  auto unit_col = [&](int u) { return lane_addr + (TC + u / kQ) * kN + (u % kQ) * 16; };
+  // slot of sender s's part of unit u in the owner's ring
+  auto slot = [&](int s, int u) {
+    const int o = u % S;
+    return (s < o ? s : s - 1) * upo + u / S;
+  };
   if (tid < kN) {
     const float mv = own ? sh.m[tid] : -INFINITY, lv = own ? sh.l[tid] : 0.f;
     for (int q = 0; q < S; ++q) {
@@ -640,7 +634,35 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
     }
   }
   if (tid < S) st_cluster_u32(map_rank(&sh.xok[rank], tid), own ? 1u : 0u);
-  cluster_sync();  // every split's O^T units and statistics are published
+  cluster_sync();  // every split's roles are done: its ring may receive
+  if (own) {
+    tc::fence_after_sync();
+    // the units other splits finish, straight from TMEM into their rings; two
+    // per round (both TMEM loads in flight before one wait)
+#pragma unroll 1
+    for (int u = hw; u < U; u += 4) {
+      const int u2 = u + 2 < U ? u + 2 : u;
+      uint32_t a[16], c[16];
+      tc::tmem_ld16(unit_col(u), a);
+      tc::tmem_ld16(unit_col(u2), c);
+      tc::tmem_ld_wait();
+      if (u % S != rank) {
+        const uint32_t d = map_rank(ring + slot(rank, u) * kUnitBytes + row * 16, u % S);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          st_cluster_f32x4(d + c4 * (kKeys * 16u), __uint_as_float(a[4 * c4]), __uint_as_float(a[4 * c4 + 1]),
+                           __uint_as_float(a[4 * c4 + 2]), __uint_as_float(a[4 * c4 + 3]));
+      }
+      if (u2 != u && u2 % S != rank) {
+        const uint32_t d = map_rank(ring + slot(rank, u2) * kUnitBytes + row * 16, u2 % S);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          st_cluster_f32x4(d + c4 * (kKeys * 16u), __uint_as_float(c[4 * c4]), __uint_as_float(c[4 * c4 + 1]),
+                           __uint_as_float(c[4 * c4 + 2]), __uint_as_float(c[4 * c4 + 3]));
+      }
+    }
+  }
+  cluster_sync();  // every part and statistic has landed; no remote access follows
   if (tid < kN) {
     float M = -INFINITY;
     for (int r = 0; r < S; ++r)
@@ -659,44 +681,54 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
   __syncthreads();
   const bool bf = p.out_dtype == HSA_BF16;
   const int64_t head0 = static_cast<int64_t>(b) * p.Hq + g * p.HG;
-  uint8_t* tr = scratch + warp * (16 * 32 * 4);  // per-warp transpose buffer (kMergeScratch)
-#pragma unroll 1
-  for (int u = rank + S * hw; u < U; u += 2 * S) {
-    const int q16 = u % kQ;
-    float o[16];
+  // Warp half hw finishes units u = rank + S*hw + 2S*k, two per round (both
+  // TMEM loads in flight before one wait, two transposes).  When 2S is a
+  // multiple of kQ those units share one 16-head group, whose weights and
+  // 1/L then stay in registers (else they are read per unit).
+  const bool fixed = (2 * S) % kQ == 0;
+  float wr[kMaxCl][16], wown[16], ivr[16];
+  auto load_w = [&](int q16) {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) o[e] = 0.f;
-    // every split's part of the unit: all loads in flight at once (a split
-    // without a partial, or past S, contributes weight 0 and is not read)
-    float4 v[kMaxCl][4];
+    for (int r = 0; r < kMaxCl; ++r)
 #pragma unroll
-    for (int r = 0; r < kMaxCl; ++r) {
-      const bool use = r < S && sh.xok[r];
-      const uint32_t src = map_rank(ring + u * kUnitBytes + row * 16, use ? r : rank);
+      for (int e = 0; e < 16; ++e) wr[r][e] = r < S ? sh.red[r][q16 * 16 + e] : 0.f;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
-        v[r][c4] = use ? ld_cluster_f32x4(src + c4 * (kKeys * 16u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = 0; e < 16; ++e) {
+      wown[e] = sh.red[rank][q16 * 16 + e];
+      ivr[e] = sh.inv[q16 * 16 + e];
     }
+  };
+  if (fixed) load_w((rank + S * hw) % kQ);
+  uint8_t* tr0 = scratch + warp * (2 * 16 * 32 * 4);  // two per-warp transpose buffers
+  // combines unit u's parts (own: a, from TMEM) into o, scaled by 1/L
+  auto combine = [&](int u, const uint32_t (&a)[16], float (&o)[16]) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) o[e] = own ? __uint_as_float(a[e]) * wown[e] : 0.f;
 #pragma unroll
     for (int r = 0; r < kMaxCl; ++r) {
-      if (!(r < S && sh.xok[r])) continue;
-      const float* w = &sh.red[r][q16 * 16];
+      if (r >= S || r == rank || !sh.xok[r]) continue;
+      const float4* src = reinterpret_cast<const float4*>(ring + slot(r, u) * kUnitBytes + row * 16);
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        o[4 * c4] = fmaf(v[r][c4].x, w[4 * c4], o[4 * c4]);
-        o[4 * c4 + 1] = fmaf(v[r][c4].y, w[4 * c4 + 1], o[4 * c4 + 1]);
-        o[4 * c4 + 2] = fmaf(v[r][c4].z, w[4 * c4 + 2], o[4 * c4 + 2]);
-        o[4 * c4 + 3] = fmaf(v[r][c4].w, w[4 * c4 + 3], o[4 * c4 + 3]);
+        const float4 v = src[c4 * kKeys];
+        o[4 * c4] = fmaf(v.x, wr[r][4 * c4], o[4 * c4]);
+        o[4 * c4 + 1] = fmaf(v.y, wr[r][4 * c4 + 1], o[4 * c4 + 1]);
+        o[4 * c4 + 2] = fmaf(v.z, wr[r][4 * c4 + 2], o[4 * c4 + 2]);
+        o[4 * c4 + 3] = fmaf(v.w, wr[r][4 * c4 + 3], o[4 * c4 + 3]);
       }
     }
-    // transpose through shared memory: lane l holds channel l of 16 heads; the
-    // stores then write 16 contiguous bytes of one head per lane
+#pragma unroll
+    for (int e = 0; e < 16; ++e) o[e] *= ivr[e];
+  };
+  // transposes o (lane l: channel l of 16 heads) through tr and writes 16
+  // contiguous bytes of one head per lane
+  auto write_out = [&](int u, const float (&o)[16], uint8_t* tr) {
+    const int q16 = u % kQ;
     const int64_t base = (head0 + q16 * 16) * p.Dv + (u / kQ) * kKeys + quarter * 32;
-    __syncwarp();
     if (bf) {
       __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(tr);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) t[e * 32 + lane] = __float2bfloat16_rn(o[e] * sh.inv[q16 * 16 + e]);
+      for (int e = 0; e < 16; ++e) t[e * 32 + lane] = __float2bfloat16_rn(o[e]);
       __syncwarp();
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -708,7 +740,7 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
     } else {
       float* t = reinterpret_cast<float*>(tr);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) t[e * 32 + lane] = o[e] * sh.inv[q16 * 16 + e];
+      for (int e = 0; e < 16; ++e) t[e * 32 + lane] = o[e];
       __syncwarp();
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -718,8 +750,28 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
               *reinterpret_cast<const float4*>(t + h * 32 + part * 4);
       }
     }
+  };
+#pragma unroll 1
+  for (int u = rank + S * hw; u < U; u += 4 * S) {
+    const int u2 = u + 2 * S;
+    const bool two = u2 < U;
+    uint32_t a[16], c[16];
+    if (own) {
+      tc::tmem_ld16(unit_col(u), a);
+      tc::tmem_ld16(unit_col(two ? u2 : u), c);
+      tc::tmem_ld_wait();
+    }
+    float o[16], o2[16];
+    if (!fixed) load_w(u % kQ);
+    combine(u, a, o);
+    if (two) {
+      if (!fixed) load_w(u2 % kQ);
+      combine(u2, c, o2);
+    }
+    __syncwarp();  // the transpose buffers are free (previous round's reads done)
+    write_out(u, o, tr0);
+    if (two) write_out(u2, o2, tr0 + 16 * 32 * 4);
   }
-  cluster_sync();  // no split leaves while another may still read its ring
 }
 
 // Q of token b, head group g into the Q region by TMA: NSL boxes of 64
