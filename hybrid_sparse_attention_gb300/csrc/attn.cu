@@ -190,12 +190,6 @@ HSA_DEVINL int64_t slot_index(const AttnParams& p, int b, const SeqGeom& g, int6
                                              : 0;
 }
 
-// Byte offset of element (row, 16-byte chunk) in a 128-byte-swizzled
-// K-major block whose rows are 128 bytes (8-row atoms of 1024 bytes).
-HSA_DEVINL uint32_t sw128(int row, int chunk) {
-  return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4);
-}
-
 // 16-byte asynchronous copy issued only when `pred` (predicated, no branch).
 HSA_DEVINL void cp_async16_if(uint32_t dst, const void* src, bool pred) {
   asm volatile(

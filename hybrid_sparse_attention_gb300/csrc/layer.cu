@@ -56,7 +56,6 @@ struct AppendParams {
   int Wr;            // window ring rows (W + T - 1)
 };
 
-constexpr int kMaxT = 4;  // tokens per step
 
 constexpr int kMaxKeyDi = 128;  // E4M3 key rows (one warp quantizes a row, 4 channels a lane)
 
