@@ -962,7 +962,7 @@ def measure_topk_line(args, rank, local, dist):
         cpu = {"value": 64 / sec, "unit": "rows/s", "cores": threads, "kind": "oracle",
                "sample": sample, "threads_busy_by_stage": busy}
     launches = 1 if x.numel() <= 32768 else 2
-    line.update({"roofline": {"bound": "hbm", "kernel": "topk_hist_kernel + topk_select_kernel",
+    line.update({"roofline": {"bound": "hbm", "kernel": "topk_chunk_kernel",
                               "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                               "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "traffic": None,
                               "algorithmic_bytes": nb, "launch_us": ms * 1000},

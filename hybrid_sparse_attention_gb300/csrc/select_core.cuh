@@ -158,14 +158,16 @@ HSA_DEVINL void merge_sort_desc(uint64_t* a, uint64_t* b, int n, int P) {
   uint64_t* src = a;
   uint64_t* dst = b;
 #pragma unroll 1
-  for (int width = 32; width < P; width <<= 1) {
+  for (int lw = 5; (1 << lw) < P; ++lw) {  // runs of width 2^lw merged pairwise
+    const int width = 1 << lw;
     uint64_t x[kMaxPer];
-    int c[kMaxPer];
+    int c[kMaxPer], other[kMaxPer];  // rank within the other run; that run's start
 #pragma unroll
     for (int q = 0; q < kMaxPer; ++q) {
       const int i = t + q * T;
       x[q] = i < P ? src[i] : 0ull;
       c[q] = 0;
+      other[q] = (((i >> lw) ^ 1) << lw) - 1;
     }
 #pragma unroll 1
     for (int st = width >> 1; st >= 1; st >>= 1) {
@@ -173,19 +175,17 @@ HSA_DEVINL void merge_sort_desc(uint64_t* a, uint64_t* b, int n, int P) {
       for (int q = 0; q < kMaxPer; ++q) {  // the entries' searches step together
         const int i = t + q * T;
         if (i >= P) continue;
-        const int r = i / width;
-        const uint64_t y = src[(r ^ 1) * width + c[q] + st - 1];
-        c[q] += ((r & 1) ? y >= x[q] : y > x[q]) ? st : 0;
+        const uint64_t y = src[other[q] + c[q] + st];
+        c[q] += (((i >> lw) & 1) ? y >= x[q] : y > x[q]) ? st : 0;
       }
     }
 #pragma unroll
     for (int q = 0; q < kMaxPer; ++q) {
       const int i = t + q * T;
       if (i >= P) continue;
-      const int r = i / width;
-      const uint64_t y = src[(r ^ 1) * width + c[q]];
-      c[q] += ((r & 1) ? y >= x[q] : y > x[q]) ? 1 : 0;
-      dst[(r & ~1) * width + (i - r * width) + c[q]] = x[q];
+      const uint64_t y = src[other[q] + c[q] + 1];
+      c[q] += (((i >> lw) & 1) ? y >= x[q] : y > x[q]) ? 1 : 0;
+      dst[(((i >> lw) & ~1) << lw) + (i & (width - 1)) + c[q]] = x[q];
     }
     __syncthreads();
     uint64_t* tmp = src;

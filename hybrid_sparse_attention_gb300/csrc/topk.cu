@@ -18,25 +18,15 @@
 // Rows of at most 32,768 scores (every C4 row up to a 128K context) take one
 // launch: a thread-block cluster per row (see "short rows" below).
 //
-// Otherwise every row is cut into chunks of CH scores (about one chunk per
-// SM), one CTA per chunk, in two launches:
-//   1. histogram: each CTA histograms the top 11 key bits (digit 1) of its
-//      chunk in shared memory (16-byte loads) and adds the non-zero bins into
-//      the row's global histogram.  The row's last CTA to finish (atomic
-//      ticket, no waiting) scans it from the top for the threshold digit d1:
-//      fewer than k keys lie above bin d1, at least k at or above it.
-//   2. select: each warp re-reads its share of the chunk (from L2: it was
-//      just read) and keeps every key at or above bin d1 as a composite,
-//      written over the share's own positions of the workspace, with its
-//      count: no atomics, no reservations.  The row's last CTA gathers the
-//      lists (keys above bin d1 are winners, keys in it candidates), picks
-//      the missing winners by a radix select over the candidates' other 53
-//      composite bits, sorts the k survivors (bitonic runs of 32 in each
-//      warp, merged by binary-search ranking) and writes them.  It leaves the
-//      row's workspace zeroed.
+// Longer rows take one launch too: every row is cut into chunks of CH
+// scores (about one chunk per SM), one CTA per chunk, each reading its chunk
+// once; a CTA counts and keeps only keys that can still reach the row's top k
+// (a bar that rises as it reads), and the row's last CTA to finish (an
+// atomic ticket, no waiting) selects and sorts (see "long rows" below).
 #include "common.cuh"
 #include "internal.h"
 #include "select_core.cuh"
+#include "tc.cuh"
 
 namespace hsa {
 namespace {
@@ -49,19 +39,20 @@ constexpr int kMaxK = 2048;       // final sort buffer
 constexpr int kSmemCand = 2560;   // boundary candidates staged in shared memory when they fit
 constexpr int kMinChunk = 4096;   // scores per CTA of the chunked passes, at least
 constexpr int kFastSort = kThreads;  // survivors ranked by warp runs + merge up to this many
+constexpr int kLBinsWs = 4096;    // digit-1 bins of the chunked path (12-bit digits)
 
 struct RowState {
   uint32_t n_cand;   // clustered path, heavy ties: candidates written to the workspace
-  uint32_t done1;    // CTAs finished with pass 1
-  uint32_t done2;    // CTAs finished with pass 2
-  uint32_t digit;    // threshold digit d1 (pass 1 result)
+  uint32_t done1;    // chunked path: CTAs finished with their chunk
+  uint32_t bar;      // chunked path: the highest final bar of the row's CTAs
+  uint32_t nlow;     // chunked path: ~(the lowest final bar), 0 before any
 };
 
 struct Ws {
   uint32_t* status;
   RowState* rows;    // [B]
-  uint32_t* hist;    // [B][kBins] digit 1
-  uint32_t* wcount;  // [chunks][kWarps] pass 2: composites each warp kept
+  uint32_t* hist;    // [B][kLBins] chunked path: the row's digit-1 histogram
+  uint32_t* wcount;  // [chunks] chunked path: composites each CTA kept
   uint64_t* cand;    // [total_rows], row b uses [offsets[b], offsets[b] + N_b)
 };
 
@@ -74,8 +65,8 @@ struct WsLayout {
     const int64_t chunks = total_rows / kMinChunk + 1 + B;
     rows = kWsHeader;
     hist = rows + align256(sizeof(RowState) * B);
-    wcount = hist + align256(sizeof(uint32_t) * kBins * B);
-    cand = wcount + align256(sizeof(uint32_t) * kWarps * chunks);
+    wcount = hist + align256(sizeof(uint32_t) * kLBinsWs * B);
+    cand = wcount + align256(sizeof(uint32_t) * chunks);
     total = cand + align256(sizeof(uint64_t) * (total_rows > 0 ? total_rows : 1));
   }
 };
@@ -90,8 +81,8 @@ Ws ws_view(void* base, int64_t B, int64_t total_rows, int64_t k, uint32_t* statu
             reinterpret_cast<uint64_t*>(p + L.cand)};
 }
 
-// Live rows of sequence b (an invalid sequence is flagged in pass 1 and
-// treated as empty by both passes).
+// Live rows of sequence b (an invalid sequence is flagged and treated as
+// empty).
 HSA_DEVINL int64_t row_count(const Spans& sp, int b) { return sp.count(b); }
 
 struct ChunkPieces {
@@ -103,93 +94,6 @@ struct ChunkPieces {
     return c > 0 ? c : 1;  // every row gets a CTA, even an empty one
   }
 };
-
-// ---------------------------------------------------------------- pass 1
-
-__global__ void __launch_bounds__(kThreads, 2) topk_hist_kernel(const float* __restrict__ scores,
-                                                            Spans sp, int B, int k,
-                                                            int64_t chunk, Ws ws) {
-  __shared__ uint32_t s_hist[kBins];
-  __shared__ uint32_t s_scan[33], s_out[2];
-  __shared__ int s_last;
-  pdl_wait();
-  pdl_trigger();
-  int row;
-  int64_t piece, npieces;
-  if (!locate_piece(B, blockIdx.x, ChunkPieces{sp, chunk}, &row, &piece, &npieces)) return;
-  if (!sp.valid(row)) {
-    if (threadIdx.x == 0 && piece == 0) set_status(ws.status, HSA_DEV_BOUNDS);
-    return;
-  }
-  const int64_t n = row_count(sp, row);
-  if (n <= k) return;  // every score is selected: no threshold needed
-  for (int i = threadIdx.x; i < kBins; i += kThreads) s_hist[i] = 0;
-  __syncthreads();
-  const uint32_t* base = reinterpret_cast<const uint32_t*>(scores + sp.start(row));
-  const int64_t lo = piece * chunk, hi = min(n, lo + chunk);
-  bool nan = false;
-  auto count_key = [&](uint32_t u) {
-    nan |= is_nan_bits(u);
-    atomicAdd(&s_hist[order_key(u) >> kShift1], 1u);
-  };
-  // 16-byte loads when the chunk starts 16-byte aligned (eight in flight per thread)
-  int64_t done = lo;
-  if ((reinterpret_cast<uintptr_t>(base + lo) & 15u) == 0) {
-    const int64_t nv = (hi - lo) >> 2;
-    const uint4* b4 = reinterpret_cast<const uint4*>(base + lo);
-    constexpr int kV = 8;
-    for (int64_t v0 = threadIdx.x; v0 < nv; v0 += kThreads * kV) {
-      uint4 w[kV];
-#pragma unroll
-      for (int j = 0; j < kV; ++j) {
-        const int64_t v = v0 + j * kThreads;
-        w[j] = v < nv ? __ldcg(b4 + v) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int j = 0; j < kV; ++j) {
-        if (v0 + j * kThreads < nv) {
-          count_key(w[j].x);
-          count_key(w[j].y);
-          count_key(w[j].z);
-          count_key(w[j].w);
-        }
-      }
-    }
-    done = lo + nv * 4;
-  }
-  constexpr int kU = 16;  // scalar loads in flight per thread
-  for (int64_t i0 = done + threadIdx.x; i0 < hi; i0 += kThreads * kU) {
-    uint32_t u[kU];
-#pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int64_t i = i0 + j * kThreads;
-      u[j] = i < hi ? __ldcg(base + i) : 0u;
-    }
-#pragma unroll
-    for (int j = 0; j < kU; ++j)
-      if (i0 + j * kThreads < hi) count_key(u[j]);
-  }
-  if (nan) set_status(ws.status, HSA_DEV_NAN);
-  __syncthreads();
-  uint32_t* gh = ws.hist + static_cast<int64_t>(row) * kBins;
-  for (int i = threadIdx.x; i < kBins; i += kThreads)
-    if (s_hist[i]) atomicAdd(gh + i, s_hist[i]);
-  // the row's last CTA finds the threshold digit
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&ws.rows[row].done1, 1u) == npieces - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int i = threadIdx.x; i < kBins; i += kThreads) s_hist[i] = __ldcg(gh + i);
-  __syncthreads();
-  uint32_t above;
-  const uint32_t d = find_digit(s_hist, kBins, static_cast<uint32_t>(k), &above, s_scan, s_out);
-  if (threadIdx.x == 0) {
-    ws.rows[row].digit = d;
-    ws.rows[row].done1 = 0;
-  }
-}
 
 // ---------------------------------------------------------------- short rows: one cluster per row
 //
@@ -404,115 +308,355 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 2)
   if (heavy && t == 0) rs->n_cand = 0;  // leave the workspace zeroed
 }
 
-// ---------------------------------------------------------------- pass 2
+// ---------------------------------------------------------------- long rows: one launch, a chunk per CTA
+//
+// Every CTA streams its chunk of the row once, through a ring of cp.async
+// stages in shared memory (each thread copies and reads its own eight scores
+// per stage, so a stage needs no block barrier).  Digit 1 has 12 bits (key
+// bits 31..20).
+//
+// Rising bar.  The k-th largest key of any part of a row is at most the
+// row's k-th largest, so the bin holding the part's k-th largest key never
+// lies above the row's threshold bin d1; nor does any bin with at least k
+// keys at or above it among some of the part's keys.  A CTA counts its first
+// stage whole and takes that stage's threshold bin as its bar; from then on
+// a score is counted and kept only when it is at or above the bar (one float
+// compare: bar_float), and after each stage one warp, in turn, raises the
+// bar from the counts so far (read while other warps still add, each count
+// a count of some of the bin's keys).  Every bin at or above the bar stays
+// exactly counted, and every key at or above bin d1 is kept.  The passing
+// scores of a stage are listed by ballots and handled 32 at a time by the
+// warp, converged (count, keep).
+//
+// A CTA's kept keys go to the row's workspace over the chunk's own positions
+// (a chunk never keeps more than it holds).  At the end the CTA finds its
+// final bar from its exact counts, raises the row's bar (the highest final
+// bar so far, also never above d1), adds its counts at or above the higher
+// of the two to the row's histogram, drops the kept keys below it and takes
+// an atomic ticket.  The row's last CTA finds d1 from the row's histogram at
+// or above the row's bar, gathers the lists (keys above bin d1 are winners,
+// keys in it candidates), picks the missing winners by radix select over the
+// candidates' other 52 composite bits, sorts and writes the row.  It leaves
+// the row's workspace zeroed.
 
-// Warp w of a chunk's CTA keeps, from its contiguous share of the chunk,
-// every score at or above bin d1 (every score when the row has at most k)
-// as a composite, written to the row's workspace over the share's own
-// positions (a share never keeps more than it holds), and records how many.
-// No atomics.  The row's last CTA gathers those lists, settles the boundary
-// and sorts.
-__global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* __restrict__ scores,
-                                                              Spans sp, int B, int k,
-                                                              int64_t chunk, Ws ws,
-                                                              int32_t* __restrict__ idx_out,
-                                                              float* __restrict__ vals_out) {
-  __shared__ uint64_t s_sel[kMaxK];
-  __shared__ uint64_t s_cand[kSmemCand];
-  __shared__ uint32_t s_hist[kBins];  // list offsets, then select scratch
-  __shared__ uint32_t s_scan[33], s_out[2], s_count, s_ccount;
+constexpr int kLBits = 12;                   // digit 1 of long rows
+constexpr int kLShift = 32 - kLBits;         // key bits 31..20
+constexpr int kLBins = 1 << kLBits;          // 4,096
+static_assert(kLBins == kLBinsWs, "the workspace holds kLBins bins per row");
+constexpr int kStage = 4096;                 // scores per stage (16 KB)
+constexpr int kHalf = kStage / 2;            // each thread copies 4 scores of each half
+constexpr int kRing = 4;                     // stages in flight per CTA
+static_assert(kStage == 8 * kThreads, "eight scores per thread per stage");
+static_assert(kMinChunk % kStage == 0, "chunks are whole stages");
+static_assert(sizeof(uint64_t) * (kMaxK + kSmemCand) <= sizeof(uint32_t) * kRing * kStage,
+              "the last CTA's selection buffers fit in the ring");
+
+constexpr size_t kChunkDynSmem = sizeof(uint32_t) * (kRing * kStage + kLBins);
+
+// One warp raises the CTA's bar (atomicMax on *s_bar) to the threshold bin
+// of the counts in `hist` as read now, while other warps may still be adding
+// to it: each count read is the number of some of the bin's keys, so at
+// least `need` keys lie at or above the bin found, and the bar stays at or
+// below the true threshold bin.  Scans the bins at or above the current bar.
+HSA_DEVINL void warp_raise_bar(const uint32_t* hist, uint32_t* s_bar, uint32_t need) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t b0 = *reinterpret_cast<volatile uint32_t*>(s_bar) >> kLShift;
+  // lane L takes `per` bins from the top, after L * per of them: an odd
+  // per makes the lanes' reads conflict-free
+  const uint32_t nb = kLBins - b0;
+  const uint32_t per = ((nb + 31) / 32) | 1u;
+  const int hi = kLBins - 1 - lane * static_cast<int>(per);  // this lane's top bin
+  const int lo = max(static_cast<int>(b0), hi - static_cast<int>(per) + 1);
+  uint32_t sum = 0;
+#pragma unroll 4
+  for (int b = hi; b >= lo; --b) sum += hist[b];
+  uint32_t incl = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  const uint32_t cross = __ballot_sync(0xffffffffu, incl - sum < need && incl >= need);
+  if (lane != __ffs(cross) - 1) return;  // (no lane: fewer than need counted so far)
+  // this lane's bins again (a count read again is no smaller, so the
+  // crossing lies among them)
+  uint32_t a = incl - sum;
+  for (int b = hi; b >= lo; --b) {
+    a += hist[b];
+    if (a >= need) {
+      atomicMax(s_bar, static_cast<uint32_t>(b) << kLShift);
+      return;
+    }
+  }
+}
+
+// max(a, b), NaN when either is NaN.
+HSA_DEVINL float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// The smallest score whose order key is at least `bar` (a multiple of
+// 2^kLShift): for every non-NaN score f, order_key(f) >= bar <=> f >= bar_float(bar).
+// Non-negative keys' scores are the key without its top bit; a negative
+// score's key is its bits inverted, so the bin's first key is the bin's most
+// negative score; bars at or below the key of -inf admit every score.
+HSA_DEVINL float bar_float(uint32_t bar) {
+  if (bar >= 0x80000000u) return __uint_as_float(bar ^ 0x80000000u);
+  if (bar < 0x00800000u) return -INFINITY;
+  return __uint_as_float(~bar);
+}
+
+// The threshold bin among the bins [b0, kLBins) of a kLBins-bin shared
+// histogram, counted from the top: the d with (#above d) < need <= (#above d)
+// + hist[d].  Returns b0 when the bins hold fewer than need keys.  All threads
+// call; returns synchronised.
+HSA_DEVINL uint32_t find_top_bin(const uint32_t* hist, uint32_t b0, uint32_t need,
+                                 uint32_t* s_scan, uint32_t* s_out) {
+  const uint32_t nb = kLBins - b0;
+  const uint32_t per = (nb + kThreads - 1) / kThreads;
+  const uint32_t first = threadIdx.x * per;  // bins counted from the top
+  uint32_t sum = 0;
+  for (uint32_t i = 0; i < per; ++i)
+    if (first + i < nb) sum += hist[kLBins - 1 - (first + i)];
+  if (threadIdx.x == 0) s_out[0] = b0;  // ordered before the writes below by the scan's barriers
+  uint32_t total;
+  uint32_t a = block_inclusive_sum<uint32_t>(sum, s_scan, &total) - sum;
+  for (uint32_t i = 0; i < per && a < need; ++i) {
+    const uint32_t bb = first + i;
+    if (bb >= nb) break;
+    const uint32_t c = hist[kLBins - 1 - bb];
+    if (a + c >= need) s_out[0] = kLBins - 1 - bb;
+    a += c;
+  }
+  __syncthreads();
+  const uint32_t d = s_out[0];
+  __syncthreads();
+  return d;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) topk_chunk_kernel(const float* __restrict__ scores,
+                                                             Spans sp, int B, int k,
+                                                             int64_t chunk, Ws ws,
+                                                             int32_t* __restrict__ idx_out,
+                                                             float* __restrict__ vals_out) {
+  extern __shared__ __align__(16) uint32_t s_dyn32[];
+  uint32_t* s_ring = s_dyn32;                  // [kRing][kStage] staged scores
+  uint32_t* s_hist = s_ring + kRing * kStage;  // [kLBins] this chunk's digit-1 counts
+  __shared__ uint32_t s_scan[33], s_out[2], s_count, s_ccount, s_kept, s_bar;
+  __shared__ uint16_t s_wbuf[kStage];  // per warp: offsets of a stage's passing scores
   __shared__ int s_last;
   pdl_wait();
   pdl_trigger();
   int row;
   int64_t piece, npieces;
   if (!locate_piece(B, blockIdx.x, ChunkPieces{sp, chunk}, &row, &piece, &npieces)) return;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const uint32_t lt = (1u << lane) - 1u;
+  const int t = threadIdx.x, lane = t & 31;
+  // an invalid row is flagged and treated as empty
+  if (!sp.valid(row) && t == 0 && piece == 0) set_status(ws.status, HSA_DEV_BOUNDS);
   const int64_t n = row_count(sp, row);
-  const bool all = n <= k;
-  const uint32_t d1 = all ? 0u : __ldcg(&ws.rows[row].digit);
+  const bool all = n <= k;  // every score is selected: no threshold
   const int64_t off = sp.start(row);
   const uint32_t* base = reinterpret_cast<const uint32_t*>(scores + off);
   RowState* rs = ws.rows + row;
-  const int64_t lo = piece * chunk, hi = min(n, lo + chunk);
-  const int64_t wsub = chunk / kWarps;
-  const int64_t wlo = lo + warp * wsub, whi = min(hi, wlo + wsub);
-  {
-    uint64_t* dst = ws.cand + off + wlo;
-    uint32_t cnt = 0;
-    auto keep = [&](uint32_t u, int64_t i, bool in) {
-      const uint32_t key = order_key(u);
-      const bool take = in && (all || (key >> kShift1) >= d1);
-      const uint32_t m = __ballot_sync(0xffffffffu, take);
-      if (take) dst[cnt + __popc(m & lt)] = composite(key, static_cast<uint32_t>(i));
-      cnt += __popc(m);
-    };
-    int64_t done = wlo;
-    if (wlo < whi && (reinterpret_cast<uintptr_t>(base + wlo) & 15u) == 0) {
-      // 16-byte loads, eight in flight per lane (the trip count is the warp's)
-      const int64_t nv = (whi - wlo) >> 2;
-      const uint4* b4 = reinterpret_cast<const uint4*>(base + wlo);
-      constexpr int kV = 8;
-      for (int64_t v0 = 0; v0 < nv; v0 += 32 * kV) {
-        uint4 w[kV];
-#pragma unroll
-        for (int j = 0; j < kV; ++j) {
-          const int64_t v = v0 + j * 32 + lane;
-          w[j] = v < nv ? __ldcg(b4 + v) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < kV; ++j) {
-          const int64_t v = v0 + j * 32 + lane;
-          const bool in = v < nv;
-          const int64_t i = wlo + 4 * v;
-          keep(w[j].x, i, in);
-          keep(w[j].y, i + 1, in);
-          keep(w[j].z, i + 2, in);
-          keep(w[j].w, i + 3, in);
-        }
-      }
-      done = wlo + nv * 4;
-    }
-    for (int64_t i0 = done; i0 < whi; i0 += 32 * 8) {
-      uint32_t u[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int64_t i = i0 + j * 32 + lane;
-        u[j] = i < whi ? __ldcg(base + i) : 0u;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int64_t i = i0 + j * 32 + lane;
-        keep(u[j], i, i < whi);
-      }
-    }
-    if (lane == 0) ws.wcount[static_cast<int64_t>(blockIdx.x) * kWarps + warp] = cnt;
+  const int64_t lo = piece * chunk;
+  const int m = static_cast<int>(n > lo ? min(n - lo, chunk) : 0);  // this chunk's scores
+  const uint32_t* src = base + lo;
+  uint64_t* list = ws.cand + off + lo;  // this chunk's kept composites
+  for (int i = t; i < kLBins; i += kThreads) s_hist[i] = 0;
+  if (t == 0) {
+    s_kept = 0;
+    s_bar = 0;
   }
+  __syncthreads();
+
+  // thread t's scores of stage r: chunk positions r*kStage + h*kHalf + 4t + j
+  // (h = 0, 1; j = 0..3), at the same offsets of the stage's ring slot
+  const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+  const int nst = (m + kStage - 1) / kStage;
+  const int nfull = vec ? m / kStage : 0;  // stages copied whole, 16 bytes at a time
+  const uint32_t s_own = tc::smem_u32(s_ring) + 16u * t;
+  const uint32_t* g_own = src + 4 * t;
+  auto issue = [&](int r) {
+    if (r < nfull) {
+      const uint32_t sa = s_own + (r % kRing) * (4u * kStage);
+      const uint32_t* g = g_own + r * kStage;
+      tc::cp_async16_s(sa, g, 16u);
+      tc::cp_async16_s(sa + 4u * kHalf, g + kHalf, 16u);
+    } else if (r < nst) {
+      uint32_t* slot = s_ring + (r % kRing) * kStage;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int p = r * kStage + h * kHalf + 4 * t;
+        if (p >= m) continue;
+        const int left = m - p;
+        if (vec) {
+          tc::cp_async16(slot + h * kHalf + 4 * t, src + p, left >= 4 ? 16u : 4u * left);
+        } else {
+          for (int j = 0; j < 4 && j < left; ++j) cp_async4(slot + h * kHalf + 4 * t + j, src + p + j);
+        }
+      }
+    }
+    tc::cp_async_commit();  // one group per stage, empty past the chunk's end
+  };
+#pragma unroll 1
+  for (int r = 0; r < kRing; ++r) issue(r);
+
+  uint32_t bar = 0;         // keys at or above bar (a bin's first key) are counted and kept
+  float nanacc = 0.0f;      // NaN once any score was NaN
+  uint16_t* wb = s_wbuf + (t >> 5) * (kStage / kWarps);
+  const uint32_t lt = (1u << lane) - 1u;
+  // The passing scores of a stage: the warp lists their offsets in the stage
+  // (one ballot per score slot j places them), then handles 32 at a time,
+  // converged: count (hist), and append to the chunk's list (keep).
+  auto pass = [&](const float* f, uint32_t live, float fbar, const uint32_t* slot, uint32_t ibase,
+                  bool hist, bool keep) {
+    uint32_t nw = 0;  // the warp's passing scores
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool tk = ((live >> j) & 1u) && (all || f[j] >= fbar);
+      const uint32_t mj = __ballot_sync(0xffffffffu, tk);
+      if (mj) {
+        if (tk) wb[nw + __popc(mj & lt)] = static_cast<uint16_t>((j >> 2) * kHalf + 4 * t + (j & 3));
+        nw += __popc(mj);
+      }
+    }
+    __syncwarp();
+    for (uint32_t e0 = 0; e0 < nw; e0 += 32) {
+      const bool in = e0 + lane < nw;
+      const int o = in ? wb[e0 + lane] : 0;
+      const uint32_t key = order_key(slot[o]);
+      if (hist && in) atomicAdd(&s_hist[key >> kLShift], 1u);
+      if (keep) {
+        uint32_t pos = 0;
+        if (lane == 0) pos = atomicAdd(&s_kept, min(32u, nw - e0));
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+        if (in) list[pos + lane] = composite(key, ibase + o);
+      }
+    }
+    __syncwarp();  // the list is free for the next stage
+  };
+  auto stage = [&](int r, bool full) {
+    tc::cp_async_wait<kRing - 1>();  // this thread's copies of stage r have landed
+    // another warp may have raised the bar since this warp's last stage
+    bar = max(bar, *reinterpret_cast<volatile uint32_t*>(&s_bar));
+    const uint32_t* slot = s_ring + (r % kRing) * kStage;
+    const float4 fa = *reinterpret_cast<const float4*>(slot + 4 * t);
+    const float4 fb = *reinterpret_cast<const float4*>(slot + kHalf + 4 * t);
+    const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+    uint32_t live = 0xffu;
+    if (!full) {  // the chunk's last stage may be partial
+      const int p0 = r * kStage + 4 * t;
+      live = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) live |= (p0 + (j >> 2) * kHalf + (j & 3) < m ? 1u : 0u) << j;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) nanacc = max_nan(nanacc, (full || ((live >> j) & 1u)) ? f[j] : 0.0f);
+    const uint32_t ibase = static_cast<uint32_t>(lo + r * kStage);
+    if (r == 0 && !all) {
+      // the first stage is counted whole and sets the CTA's first bar
+      pass(f, live, -INFINITY, slot, ibase, true, false);
+      __syncthreads();
+      if (min(m, kStage) >= k) {
+        bar = find_top_bin(s_hist, 0, static_cast<uint32_t>(k), s_scan, s_out) << kLShift;
+        if (t == 0) s_bar = bar;
+      }
+      pass(f, live, bar_float(bar), slot, ibase, false, true);
+    } else {
+      pass(f, live, bar_float(bar), slot, ibase, !all, true);
+    }
+    // one warp per stage, in turn, raises the bar from the counts so far
+    if (!all && r > 0 && (t >> 5) == r % kWarps) warp_raise_bar(s_hist, &s_bar, static_cast<uint32_t>(k));
+    issue(r + kRing);
+  };
+#pragma unroll 1
+  for (int r = 0; r < nfull; ++r) stage(r, true);
+#pragma unroll 1
+  for (int r = nfull; r < nst; ++r) stage(r, false);
+  const bool nan = nanacc != nanacc;
+  tc::cp_async_wait<0>();
+  if (nan) set_status(ws.status, HSA_DEV_NAN);
+  __syncthreads();  // every count and kept composite of the chunk is in place
+
+  // the chunk's final bar; only bins at or above it can hold d1
+  uint32_t* gh = ws.hist + static_cast<int64_t>(row) * kLBins;
+  if (!all) {
+    bar = max(bar, s_bar);
+    if (bar || m >= k)
+      bar = find_top_bin(s_hist, bar >> kLShift, static_cast<uint32_t>(k), s_scan, s_out) << kLShift;
+    // The row's bar so far (the highest final bar of its CTAs done before
+    // this one) never lies above d1 either: the search for d1 starts at the
+    // row's final bar, and every CTA prunes with the higher of the two.
+    if (t == 0) {
+      s_out[0] = atomicMax(&rs->bar, bar);
+      atomicMax(&rs->nlow, ~bar);
+    }
+    __syncthreads();
+    const uint32_t pbar = max(bar, s_out[0]);
+    for (int i = (pbar >> kLShift) + t; i < kLBins; i += kThreads)
+      if (s_hist[i]) atomicAdd(gh + i, s_hist[i]);
+    // drop the kept keys below pbar: each group is read whole before any
+    // survivor of it is written, and survivors only move down
+    const uint32_t nk = pbar ? s_kept : 0u;
+    __syncthreads();
+    if (t == 0 && pbar) s_kept = 0;
+    __syncthreads();
+    constexpr int kG = 8;
+#pragma unroll 1
+    for (uint32_t e0 = 0; e0 < nk; e0 += kThreads * kG) {
+      uint64_t x[kG];
+#pragma unroll
+      for (int g = 0; g < kG; ++g) {
+        const uint32_t e = e0 + g * kThreads + t;
+        x[g] = e < nk ? list[e] : 0ull;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int g = 0; g < kG; ++g) {
+        const uint32_t e = e0 + g * kThreads + t;
+        const bool keep = e < nk && static_cast<uint32_t>(x[g] >> 32) >= pbar;
+        const uint32_t pos = warp_append(&s_kept, keep, 0xffffffffu);
+        if (keep) list[pos] = x[g];
+      }
+    }
+    __syncthreads();
+  }
+  if (t == 0) ws.wcount[blockIdx.x] = s_kept;
+  // the row's last CTA finishes the selection
   __threadfence();
   __syncthreads();
-  if (t == 0) s_last = atomicAdd(&rs->done2, 1u) == npieces - 1;
+  if (t == 0) s_last = atomicAdd(&rs->done1, 1u) == npieces - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
 
-  // ---- the row's last CTA: gather the lists, finish the selection, write the result
+  uint64_t* s_sel = reinterpret_cast<uint64_t*>(s_ring);  // [kMaxK] winners, then survivors
+  uint64_t* s_cand = s_sel + kMaxK;                       // [kSmemCand] candidates; sort scratch
   const uint32_t kk = static_cast<uint32_t>(n < k ? n : k);
+  uint32_t d1 = 0, low = 0;  // d1; the lowest bin any CTA of the row added to
+  if (!all) {
+    const uint32_t b0 = __ldcg(&rs->bar) >> kLShift;
+    low = ~__ldcg(&rs->nlow) >> kLShift;
+    for (int i = b0 + t; i < kLBins; i += kThreads) s_hist[i] = __ldcg(gh + i);
+    __syncthreads();
+    d1 = find_top_bin(s_hist, b0, kk, s_scan, s_out);
+  }
   const int64_t first_blk = static_cast<int64_t>(blockIdx.x) - piece;
-  const int64_t nl = npieces * kWarps;
   // visits every kept composite once, list by list (lists in kThreads-sized
   // groups: counts scanned into offsets), as fn(x, e) with e its rank in that order
   auto for_each_kept = [&](auto&& fn) {
     uint32_t carry = 0;
-    for (int64_t l0 = 0; l0 < nl; l0 += kThreads) {
+    for (int64_t l0 = 0; l0 < npieces; l0 += kThreads) {
       const int64_t l = l0 + t;
-      const uint32_t c = l < nl ? __ldcg(ws.wcount + first_blk * kWarps + l) : 0u;
+      const uint32_t c = l < npieces ? __ldcg(ws.wcount + first_blk + l) : 0u;
       uint32_t tot;
       const uint32_t incl = block_inclusive_sum<uint32_t>(c, s_scan, &tot);
       s_hist[t] = incl - c;
       __syncthreads();
-      const int nlc = static_cast<int>(nl - l0 < kThreads ? nl - l0 : kThreads);
-      constexpr int kG = 4;  // composites per thread per round: their loads in flight together
+      const int nlc = static_cast<int>(npieces - l0 < kThreads ? npieces - l0 : kThreads);
+      constexpr int kG = 8;  // composites per thread per round: their loads in flight together
       for (uint32_t e0 = 0; e0 < tot; e0 += kThreads * kG) {
         uint64_t x[kG];
 #pragma unroll
@@ -525,8 +669,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
               const int mid = (a + z + 1) >> 1;
               if (s_hist[mid] <= e) a = mid; else z = mid - 1;
             }
-            const int64_t lg = l0 + a;
-            x[u] = __ldcg(ws.cand + off + (lg / kWarps) * chunk + (lg % kWarps) * wsub + (e - s_hist[a]));
+            x[u] = __ldcg(ws.cand + off + (l0 + a) * chunk + (e - s_hist[a]));
           }
         }
 #pragma unroll
@@ -545,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
   }
   __syncthreads();
   for_each_kept([&](uint64_t x, bool in, uint32_t) {
-    const uint32_t dig = static_cast<uint32_t>(x >> (32 + kShift1));
+    const uint32_t dig = static_cast<uint32_t>(x >> (32 + kLShift));
     const bool w = in && (all || dig > d1), c = in && !all && dig == d1;
     const uint32_t pw = warp_append(&s_count, w, 0xffffffffu);
     if (w && pw < static_cast<uint32_t>(kMaxK)) s_sel[pw] = x;
@@ -555,7 +698,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
   __syncthreads();
   const uint32_t n_win = s_count < kk ? s_count : kk;
   const uint32_t nc = s_ccount;
-  const uint32_t kept = s_count + s_ccount;
   const uint32_t need = kk - n_win;
   __syncthreads();
   if (t == 0) s_count = n_win;
@@ -567,18 +709,21 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
         __syncthreads();
         if (t == 0) s_count = n_win + (nc < need ? nc : need);
       } else {
-        select_rest(s_cand, nc, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 53);
+        select_rest(s_cand, nc, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 64 - kLBits);
       }
     } else {
       // heavy ties: pack every kept composite to the front of the row's
       // workspace (each read lies at or after its write, and every read of a
       // group precedes its writes), then select among those in bin d1
+      uint32_t kept = 0;  // every kept composite of the row
+      for (int64_t l = 0; l < npieces; ++l) kept += __ldcg(ws.wcount + first_blk + l);
       for_each_kept([&](uint64_t x, bool in, uint32_t e) {
         __syncthreads();
         if (in) ws.cand[off + e] = x;
       });
-      select_rest(ws.cand + off, kept, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out, 53,
-                  static_cast<uint64_t>(d1) << 53, 0x7ffull << 53);
+      constexpr uint64_t kDigitMask = ((1ull << kLBits) - 1) << (64 - kLBits);
+      select_rest(ws.cand + off, kept, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out,
+                  64 - kLBits, static_cast<uint64_t>(d1) << (64 - kLBits), kDigitMask);
     }
   }
   __syncthreads();
@@ -609,13 +754,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
     if (out_v) out_v[i] = -INFINITY;
   }
   // leave the row's workspace zeroed for the next call
-  if (!all) {
-    uint32_t* gh = ws.hist + static_cast<int64_t>(row) * kBins;
-    for (int i = t; i < kBins; i += kThreads) gh[i] = 0;
-  }
+  if (!all)
+    for (int i = low + t; i < kLBins; i += kThreads) gh[i] = 0;
   if (t == 0) {
-    rs->done2 = 0;
-    rs->digit = 0;
+    rs->done1 = 0;
+    rs->bar = 0;
+    rs->nlow = 0;
   }
 }
 
@@ -634,23 +778,21 @@ uint64_t* topk_cand_area(void* ws, int64_t B, int64_t total_rows, int64_t k) {
 }
 
 int64_t topk_chunk(int64_t total_rows) {
-  // about one chunk per SM (a single wave of both passes), 4,096 to 65,536 scores
+  // about one chunk per SM (a single wave), 4,096 to 65,536 scores
   const int64_t want = total_rows / static_cast<int64_t>(device_sms());
   int64_t c = kMinChunk;
   while (c * 2 <= want && c < 65536) c *= 2;
   return c;
 }
 
-int topk_launch_count(int64_t total_rows, int64_t max_row) {
-  return (max_row > 0 && max_row <= kClMax) || total_rows <= kClMax ? 1 : 2;
-}
+int topk_launch_count(int64_t, int64_t) { return 1; }
 
 cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows, int k,
                         int32_t* idx, float* vals, void* ws, uint32_t* status,
                         cudaStream_t stream, int64_t max_row, bool pdl) {
   Ws w = ws_view(ws, B, total_rows, k, status);
-  if (topk_launch_count(total_rows, max_row) == 1) {
-    // every row fits one cluster: a single launch
+  if ((max_row > 0 && max_row <= kClMax) || total_rows <= kClMax) {
+    // every row fits one cluster
     cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kClDynSmem));
@@ -660,11 +802,11 @@ cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows
   }
   const int64_t chunk = topk_chunk(total_rows);
   const unsigned grid = static_cast<unsigned>((total_rows + chunk - 1) / chunk + B);  // >= chunks
-  cudaError_t e = launch_k(topk_hist_kernel, dim3(grid), dim3(kThreads), 0, stream, pdl, scores, sp,
-                           B, k, chunk, w);
+  cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kChunkDynSmem));
   if (e != cudaSuccess) return e;
-  return launch_k(topk_select_kernel, dim3(grid), dim3(kThreads), 0, stream, true, scores, sp, B, k,
-                  chunk, w, idx, vals);
+  return launch_k(topk_chunk_kernel, dim3(grid), dim3(kThreads), kChunkDynSmem, stream, pdl, scores,
+                  sp, B, k, chunk, w, idx, vals);
 }
 
 }  // namespace hsa

@@ -201,12 +201,13 @@ hsa_status_t hsa_indexer_scores_e4m3(const void* iq, const float* w, const uint8
  * 32768, one launch: a cluster of four CTAs per row holds the row in
  * registers, sums its histogram of the top 11 key bits through distributed
  * shared memory, compacts the keys at or above the threshold bin, and CTA 0
- * settles the boundary and sorts.  Otherwise two launches, every row cut into
- * chunks handled by separate CTAs: launch 1 histograms the top 11 key bits
- * per row and finds the threshold bin; in launch 2 each warp keeps the keys
- * at or above that bin from its share of a chunk (no atomics), and each
- * row's last CTA gathers them, settles the boundary by a radix select over
- * the threshold bin, sorts the k survivors and writes them.
+ * settles the boundary and sorts.  Otherwise also one launch, every row cut
+ * into chunks handled by separate CTAs: each CTA reads its chunk once and
+ * counts (12-bit digits) and keeps only the keys at or above a bar that
+ * rises as it reads (the threshold bin of the scores it has seen, which never
+ * lies above the row's); the row's last CTA to finish sums the counts, finds
+ * the threshold bin, gathers the kept keys, settles the boundary by a radix
+ * select over that bin, sorts the k survivors and writes them.
  * ---------------------------------------------------------------------- */
 size_t hsa_topk_workspace_size(int64_t B, int64_t total_rows, int64_t k);
 hsa_status_t hsa_topk(const float* scores, const int64_t* offsets, int64_t B, int64_t total_rows,

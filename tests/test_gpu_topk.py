@@ -102,6 +102,18 @@ def test_topk_single_launch_full_row_and_heavy_ties(oracle_mod):
             _check(oracle_mod, vals, offs, k, ws=ws)
 
 
+@pytest.mark.parametrize("k", [1, 512, 2048])
+def test_topk_rising_rows(oracle_mod, k):
+    """Long rows whose scores keep rising, so each new stage of a chunk passes
+    the bar its earlier stages set (every score is counted and kept, then
+    pruned); a sawtooth and a rising run with plateaus of equal values."""
+    up = torch.arange(90000, dtype=torch.float32) * 1e-3
+    saw = (torch.arange(70000) % 5000).to(torch.float32)
+    steps = torch.floor(torch.arange(80000, dtype=torch.float32) / 300)
+    vals, offs = _ragged([up, saw, steps, up.flip(0)])
+    _check(oracle_mod, vals, offs, k)
+
+
 def test_topk_same_workspace_reused(oracle_mod):
     rows = [synth.topk_scores(SEED, 1, n, 0.05)[0] for n in (10000, 3, 70000)]
     vals, offs = _ragged(rows)
