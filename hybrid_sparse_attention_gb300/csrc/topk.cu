@@ -348,7 +348,8 @@ constexpr int kHalf = kStage / 2;            // each thread copies 4 scores of e
 constexpr int kRing = 4;                     // stages in flight per CTA
 static_assert(kStage == 8 * kThreads, "eight scores per thread per stage");
 static_assert(kMinChunk % kStage == 0, "chunks are whole stages");
-static_assert(sizeof(uint64_t) * (kMaxK + kSmemCand) <= sizeof(uint32_t) * kRing * kStage,
+static_assert(sizeof(uint64_t) * (kMaxK + kSmemCand) + sizeof(uint32_t) * kThreads <=
+                  sizeof(uint32_t) * kRing * kStage,
               "the last CTA's selection buffers fit in the ring");
 
 constexpr size_t kChunkDynSmem = sizeof(uint32_t) * (kRing * kStage + kLBins);
@@ -582,46 +583,56 @@ __global__ void __launch_bounds__(kThreads, 2) topk_chunk_kernel(const float* __
 
   // the chunk's final bar; only bins at or above it can hold d1
   uint32_t* gh = ws.hist + static_cast<int64_t>(row) * kLBins;
+  uint32_t pbar = 0;  // the higher of this CTA's final bar and the row's bar before it
   if (!all) {
     bar = max(bar, s_bar);
     if (bar || m >= k)
       bar = find_top_bin(s_hist, bar >> kLShift, static_cast<uint32_t>(k), s_scan, s_out) << kLShift;
     // The row's bar so far (the highest final bar of its CTAs done before
-    // this one) never lies above d1 either: the search for d1 starts at the
-    // row's final bar, and every CTA prunes with the higher of the two.
+    // this one) never lies above d1 either: every CTA adds its counts and
+    // prunes its list at the higher of the two.  The list's first group is
+    // read while the row's bar comes back.
+    constexpr int kG = 8;
+    const uint32_t nk = s_kept;
+    uint64_t x[kG];
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      const uint32_t e = g * kThreads + t;
+      x[g] = e < nk ? list[e] : 0ull;
+    }
     if (t == 0) {
+      s_count = 0;
       s_out[0] = atomicMax(&rs->bar, bar);
       atomicMax(&rs->nlow, ~bar);
     }
     __syncthreads();
-    const uint32_t pbar = max(bar, s_out[0]);
+    pbar = max(bar, s_out[0]);
     for (int i = (pbar >> kLShift) + t; i < kLBins; i += kThreads)
       if (s_hist[i]) atomicAdd(gh + i, s_hist[i]);
     // drop the kept keys below pbar: each group is read whole before any
     // survivor of it is written, and survivors only move down
-    const uint32_t nk = pbar ? s_kept : 0u;
-    __syncthreads();
-    if (t == 0 && pbar) s_kept = 0;
-    __syncthreads();
-    constexpr int kG = 8;
+    if (pbar) {
 #pragma unroll 1
-    for (uint32_t e0 = 0; e0 < nk; e0 += kThreads * kG) {
-      uint64_t x[kG];
+      for (uint32_t e0 = 0; e0 < nk; e0 += kThreads * kG) {
+        if (e0) {
 #pragma unroll
-      for (int g = 0; g < kG; ++g) {
-        const uint32_t e = e0 + g * kThreads + t;
-        x[g] = e < nk ? list[e] : 0ull;
+          for (int g = 0; g < kG; ++g) {
+            const uint32_t e = e0 + g * kThreads + t;
+            x[g] = e < nk ? list[e] : 0ull;
+          }
+          __syncthreads();
+        }
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+          const uint32_t e = e0 + g * kThreads + t;
+          const bool keep = e < nk && static_cast<uint32_t>(x[g] >> 32) >= pbar;
+          const uint32_t pos = warp_append(&s_count, keep, 0xffffffffu);
+          if (keep) list[pos] = x[g];
+        }
       }
       __syncthreads();
-#pragma unroll
-      for (int g = 0; g < kG; ++g) {
-        const uint32_t e = e0 + g * kThreads + t;
-        const bool keep = e < nk && static_cast<uint32_t>(x[g] >> 32) >= pbar;
-        const uint32_t pos = warp_append(&s_kept, keep, 0xffffffffu);
-        if (keep) list[pos] = x[g];
-      }
+      if (t == 0) s_kept = s_count;
     }
-    __syncthreads();
   }
   if (t == 0) ws.wcount[blockIdx.x] = s_kept;
   // the row's last CTA finishes the selection
@@ -635,28 +646,36 @@ __global__ void __launch_bounds__(kThreads, 2) topk_chunk_kernel(const float* __
   uint64_t* s_sel = reinterpret_cast<uint64_t*>(s_ring);  // [kMaxK] winners, then survivors
   uint64_t* s_cand = s_sel + kMaxK;                       // [kSmemCand] candidates; sort scratch
   const uint32_t kk = static_cast<uint32_t>(n < k ? n : k);
+  const int64_t first_blk = static_cast<int64_t>(blockIdx.x) - piece;
+  // the first kThreads lists' counts, loaded with the histogram
+  uint32_t* s_wc = reinterpret_cast<uint32_t*>(s_cand + kSmemCand);  // [kThreads]
+  s_wc[t] = t < npieces ? __ldcg(ws.wcount + first_blk + t) : 0u;
   uint32_t d1 = 0, low = 0;  // d1; the lowest bin any CTA of the row added to
   if (!all) {
-    const uint32_t b0 = __ldcg(&rs->bar) >> kLShift;
-    low = ~__ldcg(&rs->nlow) >> kLShift;
+    // Every CTA added its counts at or above a bar no higher than d1, so the
+    // row's histogram is whole from d1 up; the search may start at pbar.
+    const uint32_t nlow = __ldcg(&rs->nlow);
+    const uint32_t b0 = pbar >> kLShift;
     for (int i = b0 + t; i < kLBins; i += kThreads) s_hist[i] = __ldcg(gh + i);
     __syncthreads();
     d1 = find_top_bin(s_hist, b0, kk, s_scan, s_out);
+    low = ~nlow >> kLShift;
   }
-  const int64_t first_blk = static_cast<int64_t>(blockIdx.x) - piece;
   // visits every kept composite once, list by list (lists in kThreads-sized
-  // groups: counts scanned into offsets), as fn(x, e) with e its rank in that order
-  auto for_each_kept = [&](auto&& fn) {
+  // groups: counts scanned into offsets), kG per thread per round, as
+  // fn(x, e0, tot, carry): thread t holds x[u] = composite e0 + u * kThreads + t
+  // of the group's tot (valid below tot), carry composites before the group
+  constexpr int kG = 8;  // composites per thread per round: their loads in flight together
+  auto for_each_round = [&](auto&& fn) {
     uint32_t carry = 0;
     for (int64_t l0 = 0; l0 < npieces; l0 += kThreads) {
       const int64_t l = l0 + t;
-      const uint32_t c = l < npieces ? __ldcg(ws.wcount + first_blk + l) : 0u;
+      const uint32_t c = l0 == 0 ? s_wc[t] : (l < npieces ? __ldcg(ws.wcount + first_blk + l) : 0u);
       uint32_t tot;
       const uint32_t incl = block_inclusive_sum<uint32_t>(c, s_scan, &tot);
       s_hist[t] = incl - c;
       __syncthreads();
       const int nlc = static_cast<int>(npieces - l0 < kThreads ? npieces - l0 : kThreads);
-      constexpr int kG = 8;  // composites per thread per round: their loads in flight together
       for (uint32_t e0 = 0; e0 < tot; e0 += kThreads * kG) {
         uint64_t x[kG];
 #pragma unroll
@@ -672,29 +691,46 @@ __global__ void __launch_bounds__(kThreads, 2) topk_chunk_kernel(const float* __
             x[u] = __ldcg(ws.cand + off + (l0 + a) * chunk + (e - s_hist[a]));
           }
         }
-#pragma unroll
-        for (int u = 0; u < kG; ++u) {
-          const uint32_t e = e0 + u * kThreads + t;
-          fn(x[u], e < tot, carry + e);
-        }
+        fn(x, e0, tot, carry);
       }
       __syncthreads();  // s_hist and s_scan are reused by the next group
       carry += tot;
     }
   };
-  if (t == 0) {
-    s_count = 0;
-    s_ccount = 0;
-  }
-  __syncthreads();
-  for_each_kept([&](uint64_t x, bool in, uint32_t) {
-    const uint32_t dig = static_cast<uint32_t>(x >> (32 + kLShift));
-    const bool w = in && (all || dig > d1), c = in && !all && dig == d1;
-    const uint32_t pw = warp_append(&s_count, w, 0xffffffffu);
-    if (w && pw < static_cast<uint32_t>(kMaxK)) s_sel[pw] = x;
-    const uint32_t pc = warp_append(&s_ccount, c, 0xffffffffu);
-    if (c && pc < static_cast<uint32_t>(kSmemCand)) s_cand[pc] = x;
+  // winners (above bin d1) to s_sel, candidates (in it) to s_cand: per-thread
+  // masks and one block scan of the packed counts place them, no atomics
+  uint32_t n_w = 0, n_c = 0;
+  for_each_round([&](const uint64_t* x, uint32_t e0, uint32_t tot, uint32_t) {
+    uint32_t wm = 0, cm = 0;
+#pragma unroll
+    for (int u = 0; u < kG; ++u) {
+      const bool in = e0 + u * kThreads + t < tot;
+      const uint32_t dig = static_cast<uint32_t>(x[u] >> (32 + kLShift));
+      wm |= (in && (all || dig > d1) ? 1u : 0u) << u;
+      cm |= (in && !all && dig == d1 ? 1u : 0u) << u;
+    }
+    const uint32_t packed = __popc(wm) | (__popc(cm) << 16);
+    uint32_t sum;
+    const uint32_t before = block_inclusive_sum<uint32_t>(packed, s_scan, &sum) - packed;
+    uint32_t pw = n_w + (before & 0xffffu), pc = n_c + (before >> 16);
+#pragma unroll
+    for (int u = 0; u < kG; ++u) {
+      if ((wm >> u) & 1u) {
+        if (pw < static_cast<uint32_t>(kMaxK)) s_sel[pw] = x[u];
+        ++pw;
+      }
+      if ((cm >> u) & 1u) {
+        if (pc < static_cast<uint32_t>(kSmemCand)) s_cand[pc] = x[u];
+        ++pc;
+      }
+    }
+    n_w += sum & 0xffffu;
+    n_c += sum >> 16;
   });
+  if (t == 0) {
+    s_count = n_w;
+    s_ccount = n_c;
+  }
   __syncthreads();
   const uint32_t n_win = s_count < kk ? s_count : kk;
   const uint32_t nc = s_ccount;
@@ -717,9 +753,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_chunk_kernel(const float* __
       // group precedes its writes), then select among those in bin d1
       uint32_t kept = 0;  // every kept composite of the row
       for (int64_t l = 0; l < npieces; ++l) kept += __ldcg(ws.wcount + first_blk + l);
-      for_each_kept([&](uint64_t x, bool in, uint32_t e) {
+      for_each_round([&](const uint64_t* x, uint32_t e0, uint32_t tot, uint32_t carry) {
         __syncthreads();
-        if (in) ws.cand[off + e] = x;
+#pragma unroll
+        for (int u = 0; u < kG; ++u) {
+          const uint32_t e = e0 + u * kThreads + t;
+          if (e < tot) ws.cand[off + carry + e] = x[u];
+        }
       });
       constexpr uint64_t kDigitMask = ((1ull << kLBits) - 1) << (64 - kLBits);
       select_rest(ws.cand + off, kept, need, s_sel, &s_count, kMaxK, s_hist, s_scan, s_out,
