@@ -425,24 +425,34 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
   constexpr int kGrp = 16;                              // slots per thread per group
   constexpr int kGroups = kSelRowMax / (kThreads * kGrp);
   auto slot_of = [&](int gi, int bit) { return ((gi * (kGrp / 4) + (bit >> 2)) * kThreads + t) * 4 + (bit & 3); };
-  const int dd = all ? -1 : static_cast<int>(d);       // winners: digit > dd
+  // Float compares against the bins' first scores (bar_float): winners lie at
+  // or above bin d + 1's, candidates at or above bin d's and below; NaN
+  // scores pass neither and are caught by a NaN-propagating max.
+  const float fw = all ? -INFINITY
+                       : (d + 1 < static_cast<uint32_t>(kRowHistBins)
+                              ? bar_float((d + 1) << kRowHistShift)
+                              : __uint_as_float(0x7fffffffu));  // (top bin: no winners)
+  const float fc = all ? -INFINITY : bar_float(d << kRowHistShift);
+  float nanacc = 0.0f;
   uint32_t wmask[kGroups], cmask[kGroups];
   uint32_t cnt = 0;
 #pragma unroll
   for (int gi = 0; gi < kGroups; ++gi) {
     wmask[gi] = cmask[gi] = 0u;
     if (gi * kThreads * kGrp >= n) continue;      // (uniform)
+    const bool whole = (gi + 1) * kThreads * kGrp <= n;  // (uniform)
 #pragma unroll
     for (int q4 = 0; q4 < kGrp / 4; ++q4) {
-      const uint4 w = reinterpret_cast<const uint4*>(s_row)[(gi * (kGrp / 4) + q4) * kThreads + t];
-      const uint32_t u4[4] = {w.x, w.y, w.z, w.w};
+      const float4 w = reinterpret_cast<const float4*>(s_row)[(gi * (kGrp / 4) + q4) * kThreads + t];
+      const float f4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int bit = 4 * q4 + e;
-        const int dig = static_cast<int>(order_key(u4[e]) >> kRowHistShift);
-        const bool in = slot_of(gi, bit) < n;
-        wmask[gi] |= (in && dig > dd ? 1u : 0u) << bit;
-        cmask[gi] |= (in && !all && dig == dd ? 1u : 0u) << bit;
+        const bool in = whole || slot_of(gi, bit) < n;
+        const bool win = f4[e] >= fw, cand = !win && f4[e] >= fc;
+        nanacc = max_nan(nanacc, in ? f4[e] : 0.0f);
+        wmask[gi] |= (in && win ? 1u : 0u) << bit;
+        cmask[gi] |= (in && !all && cand ? 1u : 0u) << bit;
       }
     }
     cnt += __popc(wmask[gi]) + (__popc(cmask[gi]) << 16);
@@ -455,7 +465,7 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
   const bool heavy = nw + ncd > static_cast<uint32_t>(kSelSort);  // (uniform)
   uint64_t* cand = heavy ? p.cand_ws + g.soff : sbuf + nw;
   uint32_t wo = off & 0xffffu, co = off >> 16;
-  bool nan = false;
+  const bool nan = nanacc != nanacc;
 #pragma unroll
   for (int gi = 0; gi < kGroups; ++gi) {  // (unrolled: the masks stay in registers)
     uint32_t m = wmask[gi] | cmask[gi];
@@ -465,7 +475,6 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
       m &= m - 1;
       const int slot = slot_of(gi, bit);
       const uint32_t u = s_row[slot];
-      nan |= is_nan_bits(u);
       const int ix = slot < body ? slot + head : (slot - body < head ? slot - body : slot);
       const uint64_t x = composite(order_key(u), static_cast<uint32_t>(ix));
       if ((wmask[gi] >> bit) & 1u) {
@@ -525,13 +534,23 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
   // (5) every split's share of the list (the list kept for the ordered copy),
   // the splits signalled, and then this split's own rows prefetched into L2
   // for its gather (the other splits start theirs at once)
+  // split q attends entries [share_first(q), share_first(q + 1)) (S <= kMaxCl)
+  int bnd[kMaxCl + 1];
+#pragma unroll
+  for (int q = 0; q <= kMaxCl; ++q) bnd[q] = q < p.S ? static_cast<int>(share_first(p, g.n_swa, q)) : p.k;
   for (int e = t; e < p.k; e += kThreads) {
     const bool live = e < static_cast<int>(nsel);
     const uint64_t x = live ? sbuf[e] : 0ull;
     const uint32_t j = live ? 0xffffffffu - static_cast<uint32_t>(x) : 0u;
     if (live && p.topk_out) p.cand_ws[g.soff + e] = x;
-    const int q = static_cast<int>((g.n_swa + e) / p.sps);  // the split attending entry e
-    uint16_t* dst = &sh.sel[e - share_first(p, g.n_swa, q)];
+    int q = 0, first = 0;  // the split attending entry e; its share's first entry
+#pragma unroll
+    for (int qq = 1; qq < kMaxCl; ++qq)
+      if (e >= bnd[qq]) {
+        q = qq;
+        first = bnd[qq];
+      }
+    uint16_t* dst = &sh.sel[e - first];
     const uint16_t v = live ? static_cast<uint16_t>(j) : uint16_t(0xffff);
     if (static_cast<uint32_t>(q) == rank) *dst = v;
     else st_cluster_u16(map_rank(dst, static_cast<uint32_t>(q)), v);
@@ -542,8 +561,14 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
     asm volatile("fence.acq_rel.cluster;" ::: "memory");
     for (int q = 0; q < p.S; ++q) mbar_arrive_cluster(map_rank(&sh.sel_full, static_cast<uint32_t>(q)));
   }
-  for (int e = t; e < static_cast<int>(nsel); e += kThreads) {
-    if ((g.n_swa + e) / p.sps != static_cast<int64_t>(rank)) continue;
+  int own_first = 0, own_end = 0;  // this split's share
+#pragma unroll
+  for (int q = 0; q < kMaxCl; ++q)
+    if (q == static_cast<int>(rank)) {
+      own_first = bnd[q];
+      own_end = min(static_cast<int>(nsel), bnd[q + 1]);
+    }
+  for (int e = own_first + t; e < own_end; e += kThreads) {
     const uint32_t j = 0xffffffffu - static_cast<uint32_t>(sbuf[e]);
     const uint16_t* rowp = p.extra + (g.off + j) * p.Dqk;
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rowp),

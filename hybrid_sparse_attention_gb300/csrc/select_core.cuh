@@ -13,6 +13,24 @@ namespace hsa {
 
 HSA_DEVINL bool is_nan_bits(uint32_t u) { return (u & 0x7fffffffu) > 0x7f800000u; }
 
+// max(a, b), NaN when either is NaN.
+HSA_DEVINL float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// A float bound for a key bound: for every non-NaN score f and every bar,
+// order_key(f) >= bar <=> f >= bar_float(bar).  A non-negative score's key is
+// its bits with the top bit set, a negative score's key its bits inverted
+// (both orders agree with the values'); every non-NaN key is at least the key
+// of -inf (0x007fffff), so lower bars admit every score.
+HSA_DEVINL float bar_float(uint32_t bar) {
+  if (bar >= 0x80000000u) return __uint_as_float(bar ^ 0x80000000u);
+  if (bar < 0x00800000u) return -INFINITY;
+  return __uint_as_float(~bar);
+}
+
 HSA_DEVINL uint64_t composite(uint32_t key, uint32_t j) {
   return (static_cast<uint64_t>(key) << 32) | static_cast<uint64_t>(0xffffffffu - j);
 }

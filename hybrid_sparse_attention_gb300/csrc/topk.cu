@@ -391,24 +391,6 @@ HSA_DEVINL void warp_raise_bar(const uint32_t* hist, uint32_t* s_bar, uint32_t n
   }
 }
 
-// max(a, b), NaN when either is NaN.
-HSA_DEVINL float max_nan(float a, float b) {
-  float d;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-  return d;
-}
-
-// The smallest score whose order key is at least `bar` (a multiple of
-// 2^kLShift): for every non-NaN score f, order_key(f) >= bar <=> f >= bar_float(bar).
-// Non-negative keys' scores are the key without its top bit; a negative
-// score's key is its bits inverted, so the bin's first key is the bin's most
-// negative score; bars at or below the key of -inf admit every score.
-HSA_DEVINL float bar_float(uint32_t bar) {
-  if (bar >= 0x80000000u) return __uint_as_float(bar ^ 0x80000000u);
-  if (bar < 0x00800000u) return -INFINITY;
-  return __uint_as_float(~bar);
-}
-
 // The threshold bin among the bins [b0, kLBins) of a kLBins-bin shared
 // histogram, counted from the top: the d with (#above d) < need <= (#above d)
 // + hist[d].  Returns b0 when the bins hold fewer than need keys.  All threads
