@@ -237,7 +237,7 @@ struct Shared {
   // fused selection: this split's share of the token's selected entries
   // (row-local indices, 0xffff past the selection), their total, and the
   // barrier the selecting split arrives on once both are written
-  uint16_t sel[kMaxTC * kKeys];
+  alignas(16) uint16_t sel[kMaxTC * kKeys];
   uint32_t sel_n;
   uint64_t sel_full;
   uint64_t sel_cp;  // the selecting split's copy of its row's scores landed
@@ -283,9 +283,12 @@ constexpr int kSelSort = 1024;     // winners + candidates held in shared memory
 constexpr int kSelRank = 512;      // candidates ranked by counting, at most
 constexpr int kSelMaxK = 512;      // k the fused selection handles
 
-// Remote arrive (release, cluster scope) on the barrier at cluster address `bar`.
-HSA_DEVINL void mbar_arrive_cluster(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+// Asynchronous 4-byte store to cluster shared memory whose completion counts
+// its bytes on the barrier at cluster address `bar` (same CTA as `addr`).
+HSA_DEVINL void st_async_u32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+               "r"(v), "r"(bar)
+               : "memory");
 }
 
 // Bounded wait (acquire, cluster scope) for the barrier's phase `parity`;
@@ -320,9 +323,13 @@ HSA_DEVINL int64_t share_first(const AttnParams& p, int n_swa, int q) {
   return e < 0 ? 0 : (e > p.k ? p.k : e);
 }
 
-HSA_DEVINL void st_cluster_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+// Bytes the selecting split stores into split q's shared memory: q's share
+// of the list as 16-bit entries in 4-byte pairs, and the list's length.
+HSA_DEVINL uint32_t sel_bytes(const AttnParams& p, int n_swa, int q) {
+  const int64_t e1 = q + 1 < p.S ? share_first(p, n_swa, q + 1) : p.k;
+  return 4u * static_cast<uint32_t>((e1 - share_first(p, n_swa, q) + 1) >> 1) + 4u;
 }
+
 
 // 4-byte asynchronous global -> shared copy (any 4-byte-aligned source).
 HSA_DEVINL void cp_async4(void* dst, const void* src) {
@@ -532,35 +539,45 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
   }
   __syncthreads();
   // (5) every split's share of the list (the list kept for the ordered copy),
-  // the splits signalled, and then this split's own rows prefetched into L2
-  // for its gather (the other splits start theirs at once)
-  // split q attends entries [share_first(q), share_first(q + 1)) (S <= kMaxCl)
+  // and then this split's own rows prefetched into L2 for its gather (the
+  // other splits start theirs at once).  Split q attends entries [bnd[q],
+  // bnd[q + 1]) (S <= kMaxCl).  Its share (16-bit entries, in pairs) and the
+  // list's length reach another split's shared memory by asynchronous stores
+  // that count their bytes on its sel_full barrier, which that split armed
+  // with exactly those bytes at launch (sel_bytes): its phase ends once they
+  // have landed (no fence, no remote arrive, no wait here).  The selecting
+  // split writes its own share with plain stores and arrives on its barrier.
   int bnd[kMaxCl + 1];
 #pragma unroll
   for (int q = 0; q <= kMaxCl; ++q) bnd[q] = q < p.S ? static_cast<int>(share_first(p, g.n_swa, q)) : p.k;
-  for (int e = t; e < p.k; e += kThreads) {
-    const bool live = e < static_cast<int>(nsel);
-    const uint64_t x = live ? sbuf[e] : 0ull;
-    const uint32_t j = live ? 0xffffffffu - static_cast<uint32_t>(x) : 0u;
-    if (live && p.topk_out) p.cand_ws[g.soff + e] = x;
-    int q = 0, first = 0;  // the split attending entry e; its share's first entry
+  if (p.topk_out)
+    for (int e = t; e < static_cast<int>(nsel); e += kThreads) p.cand_ws[g.soff + e] = sbuf[e];
+  auto entry = [&](int e) -> uint32_t {  // row-local index, 0xffff past the selection
+    return e < static_cast<int>(nsel) ? (0xffffffffu - static_cast<uint32_t>(sbuf[e])) & 0xffffu
+                                      : 0xffffu;
+  };
 #pragma unroll
-    for (int qq = 1; qq < kMaxCl; ++qq)
-      if (e >= bnd[qq]) {
-        q = qq;
-        first = bnd[qq];
-      }
-    uint16_t* dst = &sh.sel[e - first];
-    const uint16_t v = live ? static_cast<uint16_t>(j) : uint16_t(0xffff);
-    if (static_cast<uint32_t>(q) == rank) *dst = v;
-    else st_cluster_u16(map_rank(dst, static_cast<uint32_t>(q)), v);
+  for (int q = 0; q < kMaxCl; ++q) {
+    if (q >= p.S) break;
+    const int npairs = (bnd[q + 1] - bnd[q] + 1) >> 1;
+    const bool own = q == static_cast<int>(rank);
+    const uint32_t bar = own ? 0u : map_rank(&sh.sel_full, static_cast<uint32_t>(q));
+    const uint32_t dst = own ? 0u : map_rank(&sh.sel[0], static_cast<uint32_t>(q));
+    if (t == kThreads - 1) {
+      if (own) sh.sel_n = nsel;
+      else st_async_u32(map_rank(&sh.sel_n, static_cast<uint32_t>(q)), nsel, bar);
+    }
+    for (int i = t; i < npairs; i += kThreads) {
+      const int e = bnd[q] + 2 * i;
+      const uint32_t hi = e + 1 < bnd[q + 1] ? entry(e + 1) : 0xffffu;
+      const uint32_t v = entry(e) | (hi << 16);
+      if (own) reinterpret_cast<uint32_t*>(sh.sel)[i] = v;
+      else st_async_u32(dst + 4u * static_cast<uint32_t>(i), v, bar);
+    }
   }
-  if (t < p.S) st_cluster_u32(map_rank(&sh.sel_n, static_cast<uint32_t>(t)), nsel);
+  // this split's own share: plain stores, then a local arrive
   __syncthreads();
-  if (t == 0) {
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-    for (int q = 0; q < p.S; ++q) mbar_arrive_cluster(map_rank(&sh.sel_full, static_cast<uint32_t>(q)));
-  }
+  if (t == 0) tc::mbar_arrive(&sh.sel_full);
   int own_first = 0, own_end = 0;  // this split's share
 #pragma unroll
   for (int q = 0; q < kMaxCl; ++q)
@@ -891,6 +908,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     if (kSel) {
       tc::mbar_init(&sh.sel_full, 1);
       tc::mbar_init(&sh.sel_cp, 1);
+      // another split's share arrives by the selecting split's asynchronous
+      // stores, whose bytes complete the phase (the selecting split arrives
+      // on its own barrier)
+      if (!selector) tc::mbar_arrive_expect_tx(&sh.sel_full, sel_bytes(p, geo.n_swa, s));
     }
     sh.abort = 0;
     tc::fence_mbar_init();
