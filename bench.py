@@ -318,7 +318,7 @@ def main(argv=None, measure=None):
         if args.impl == "reference":
             run_reference(args, world, rank, dist)
         elif args.profile:
-            run_profile(args.profile_ctx)
+            run_profile_topk() if args.config == "topk" else run_profile(args.profile_ctx)
         else:
             run_hsa(args, world, rank, local, dist, measure)
     finally:
@@ -825,6 +825,19 @@ def run_profile(ctx=None):
     torch.cuda.synchronize()
     assert _lib.hsa_workspace_status(ws) == 0
     print(json.dumps({"profile": "ok", "sum_c4_entries": int((L // 4).sum())}))
+
+
+def run_profile_topk():
+    """Two top-k calls on the standalone workload (the first warms up), for ncu."""
+    _lib.load(build_if_missing=True)
+    x, offs = topk_inputs()
+    idx = torch.empty(64, 512, dtype=torch.int32, device="cuda")
+    ws = _lib.workspace(_lib.hsa_topk_workspace_size(64, x.numel(), 512))
+    for _ in range(2):
+        _lib.hsa_topk(x, offs, 512, idx=idx, ws=ws, with_vals=False)
+    torch.cuda.synchronize()
+    assert _lib.hsa_workspace_status(ws) == 0
+    print(json.dumps({"profile": "ok", "scores": int(x.numel())}))
 
 
 def multi_layer_graph(args, flush, runs, iters=10):

@@ -41,6 +41,8 @@
 //    a combine kernel merges.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "select_core.cuh"
@@ -507,25 +509,32 @@ HSA_DEVINL void select_token(const AttnParams& p, Shared& sh, uint8_t* ring, uin
       for (uint32_t i = t; i < ncd; i += kThreads) sbuf[nsel + i] = cand[i];
       nsel += ncd;
     } else if (!heavy && ncd <= static_cast<uint32_t>(kSelRank)) {
-      // candidate c's rank = the number of candidates greater than it (unique composites)
-      uint64_t x[kSelRank / kThreads];
-      uint32_t r[kSelRank / kThreads];
+      // candidate c's rank = the number of candidates greater than it (unique
+      // composites); one candidate per thread when they fit, else kQ
+      constexpr int kQ = kSelRank / kThreads;
+      auto rank_by_count = [&](auto nq) {
+        constexpr int Q = decltype(nq)::value;
+        uint64_t x[Q];
+        uint32_t r[Q];
 #pragma unroll
-      for (int q = 0; q < kSelRank / kThreads; ++q) {
-        const uint32_t ci = t + q * kThreads;
-        x[q] = ci < ncd ? cand[ci] : ~0ull;
-        r[q] = 0;
-      }
+        for (int q = 0; q < Q; ++q) {
+          const uint32_t ci = t + q * kThreads;
+          x[q] = ci < ncd ? cand[ci] : ~0ull;
+          r[q] = 0;
+        }
 #pragma unroll 4
-      for (uint32_t i = 0; i < ncd; ++i) {
-        const uint64_t y = cand[i];
+        for (uint32_t i = 0; i < ncd; ++i) {
+          const uint64_t y = cand[i];
 #pragma unroll
-        for (int q = 0; q < kSelRank / kThreads; ++q) r[q] += y > x[q] ? 1u : 0u;
-      }
-      __syncthreads();  // every candidate read before the list grows over them
+          for (int q = 0; q < Q; ++q) r[q] += y > x[q] ? 1u : 0u;
+        }
+        __syncthreads();  // every candidate read before the list grows over them
 #pragma unroll
-      for (int q = 0; q < kSelRank / kThreads; ++q)
-        if (t + q * kThreads < static_cast<int>(ncd) && r[q] < need) sbuf[nsel + r[q]] = x[q];
+        for (int q = 0; q < Q; ++q)
+          if (t + q * kThreads < static_cast<int>(ncd) && r[q] < need) sbuf[nsel + r[q]] = x[q];
+      };
+      if (ncd <= static_cast<uint32_t>(kThreads)) rank_by_count(std::integral_constant<int, 1>());
+      else rank_by_count(std::integral_constant<int, kQ>());
       nsel += need;
     } else {
       if (t == 0) s_cnt = nsel;
@@ -946,14 +955,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       // Q first (the previous kernel does not write it), then the selection,
       // which needs the indexer's scores and histogram
       if (tid == kProdWarp0 * 32) issue_q_tma<kN>(&qmap, sh, qs, NSL, b * p.Hq + g * p.HG);
-      pdl_wait();
-      int n = static_cast<int>(geo.nb);
       // an invalid span (bad offsets or a live count above the capacity), or a
-      // row longer than the host-checked bound: flagged, treated as empty
-      if (!p.sp.valid(b) || geo.nb > kSelRowMax) {
-        if (tid == 0) set_status(p.status, HSA_DEV_BOUNDS);
-        n = 0;
-      }
+      // row longer than the host-checked bound: flagged, treated as empty (the
+      // offsets and lengths are older than the previous kernel, like geo)
+      const bool bad = !p.sp.valid(b) || geo.nb > kSelRowMax;
+      const int n = bad ? 0 : static_cast<int>(geo.nb);
+      pdl_wait();
+      if (bad && tid == 0) set_status(p.status, HSA_DEV_BOUNDS);
       // survivors: the even tiles' P^T buffer when it holds kSelMax composites,
       // else the region the plan adds after it
       uint8_t* sel_buf = 2 * kN * 128 >= kSelMax * 8 ? pbuf0 : pbuf0 + 2 * kN * 128;
