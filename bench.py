@@ -974,10 +974,11 @@ def measure_topk_line(args, rank, local, dist):
         sec, calls = time_oracle(run, min(args.cpu_budget, 5.0))
         cpu = {"value": 64 / sec, "unit": "rows/s", "cores": threads, "kind": "oracle",
                "sample": sample, "threads_busy_by_stage": busy}
-    launches = 1 if x.numel() <= 32768 else 2
+    launches = 1  # one launch per call (clustered rows or chunked rows)
     line.update({"roofline": {"bound": "hbm", "kernel": "topk_chunk_kernel",
                               "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                              "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "traffic": None,
+                              "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
+                              "traffic": profile_traffic("topk_chunk_64x262144_traffic.json", TOPK_SOURCES),
                               "algorithmic_bytes": nb, "launch_us": ms * 1000},
                  "cpu_baseline": cpu,
                  "e2e": {"value": None, "unit": "rows/s", "h2d_bytes_per_step": x.numel() * 4,
@@ -1173,23 +1174,31 @@ def measure_longctx_line(args, rank, local, dist):
             "tokens_per_step": 4, "throughput_unit": "decode tokens/s through one layer"}
 
 
-def indexer_traffic():
-    """DRAM bytes per indexer launch from the committed ncu summary, if it was
-    taken on the current indexer source (else null)."""
+INDEXER_SOURCES = ("indexer.cu", "tc.cuh", "common.cuh")
+TOPK_SOURCES = ("topk.cu", "select_core.cuh", "tc.cuh", "common.cuh")
+
+
+def profile_traffic(name, sources):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, if it
+    was taken on the current source of the kernel (else null)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "indexer_c4layer_traffic.json")
+    path = os.path.join(ROOT, "profiles", name)
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
     h = hashlib.sha256()
-    for name in ("indexer.cu", "tc.cuh", "common.cuh"):
-        with open(os.path.join(ROOT, "hybrid_sparse_attention_gb300", "csrc", name), "rb") as f:
+    for src in sources:
+        with open(os.path.join(ROOT, "hybrid_sparse_attention_gb300", "csrc", src), "rb") as f:
             h.update(f.read())
     if rec.get("source_sha256") != h.hexdigest():
         return None
     return rec.get("dram_bytes_per_launch")
+
+
+def indexer_traffic():
+    return profile_traffic("indexer_c4layer_traffic.json", INDEXER_SOURCES)
 
 
 if __name__ == "__main__":

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__
     };
     GatePartial part;
     partial_init(part);
-    partial_rows(kv + first, z + first, chunks, 0, i1 - i0, bias, part);
+    partial_rows<kOverlap>(kv + first, z + first, chunks, 0, i1 - i0, bias, part);
     float o[8];
     partial_result(part, o);
     if (kBf16Out) {

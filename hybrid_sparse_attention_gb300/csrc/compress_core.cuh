@@ -25,8 +25,10 @@ HSA_DEVINL void partial_init(GatePartial& p) {
 }
 
 // Rows [i0, i1) of one chunk; row i at kv[i * stride] / z[i * stride]
-// (uint4 units); bias(i, lo, hi) loads the 8 fp32 biases of row i.
-template <typename BiasFn>
+// (uint4 units); bias(i, lo, hi) loads the 8 fp32 biases of row i.  kMasked:
+// a logit may be -inf (a masked position, weight 0); without it every logit
+// is finite (the guards cost about a fifth of the compressor's time).
+template <bool kMasked = false, typename BiasFn>
 HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, int i0, int i1,
                              BiasFn bias, GatePartial& p) {
   constexpr int kGroup = 4;
@@ -61,9 +63,10 @@ HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, in
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const float mn = fmaxf(p.m[c], gm[c]);
-      // 0 while nothing finite has been seen (m = -inf): a -inf logit (a
-      // masked position) weighs 0 and never makes -inf - -inf
-      const float alpha = p.m[c] == -INFINITY ? 0.f : __expf(p.m[c] - mn);
+      // (masked: 0 while nothing finite has been seen, m = -inf, so that a
+      // -inf logit weighs 0 and never makes -inf - -inf; otherwise
+      // exp(-inf) = 0 on the first group)
+      const float alpha = kMasked && p.m[c] == -INFINITY ? 0.f : __expf(p.m[c] - mn);
       p.l[c] *= alpha;
       p.acc[c] *= alpha;
       p.m[c] = mn;
@@ -73,7 +76,7 @@ HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, in
       if (j < g) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const float e = x[j][c] == -INFINITY ? 0.f : __expf(x[j][c] - p.m[c]);  // softmax numerator
+          const float e = kMasked && x[j][c] == -INFINITY ? 0.f : __expf(x[j][c] - p.m[c]);  // numerator
           p.l[c] += e;
           p.acc[c] = fmaf(e, v[j][c], p.acc[c]);    // dot
         }

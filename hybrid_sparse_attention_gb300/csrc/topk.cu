@@ -353,6 +353,7 @@ static_assert(sizeof(uint64_t) * (kMaxK + kSmemCand) + sizeof(uint32_t) * kThrea
               "the last CTA's selection buffers fit in the ring");
 
 constexpr size_t kChunkDynSmem = sizeof(uint32_t) * (kRing * kStage + kLBins);
+constexpr int kRowBarPieces = 8;  // rows cut into this many pieces or more also prune at the row's counts
 
 // One warp raises the CTA's bar (atomicMax on *s_bar) to the threshold bin
 // of the counts in `hist` as read now, while other warps may still be adding
@@ -591,6 +592,19 @@ __global__ void __launch_bounds__(kThreads, 2) topk_chunk_kernel(const float* __
     pbar = max(bar, s_out[0]);
     for (int i = (pbar >> kLShift) + t; i < kLBins; i += kThreads)
       if (s_hist[i]) atomicAdd(gh + i, s_hist[i]);
+    if (npieces >= kRowBarPieces) {
+      // Many pieces: the row's counts so far (this CTA's included) give a
+      // higher bar still.  Each count read counts some of its bin's keys, so
+      // at least k of the row's keys lie at or above the bin where their sum
+      // from the top reaches k: that bin is no higher than d1.
+      __threadfence();  // this CTA's adds are visible to its reads below
+      __syncthreads();
+      const uint32_t b0 = pbar >> kLShift;
+      for (int i = b0 + t; i < kLBins; i += kThreads) s_hist[i] = __ldcg(gh + i);
+      __syncthreads();
+      pbar = max(pbar, find_top_bin(s_hist, b0, static_cast<uint32_t>(k), s_scan, s_out) << kLShift);
+      if (t == 0) atomicMax(&rs->bar, pbar);
+    }
     // drop the kept keys below pbar: each group is read whole before any
     // survivor of it is written, and survivors only move down
     if (pbar) {
@@ -799,10 +813,14 @@ uint64_t* topk_cand_area(void* ws, int64_t B, int64_t total_rows, int64_t k) {
   return reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + WsLayout(B, total_rows, k).cand);
 }
 
-int64_t topk_chunk(int64_t total_rows) {
-  // about one chunk per SM (a single wave), 4,096 to 65,536 scores
+int64_t topk_chunk(int64_t total_rows, int k) {
+  // About one chunk per SM (a single wave), 4,096 to 65,536 scores, and at
+  // least 16 k: a chunk keeps at least its own k best until the row's counts
+  // prune it, so shorter chunks hand the row's last CTA many more kept keys
+  // than the row's top k (measured on 4 rows of 262,144: 16 k best).
   const int64_t want = total_rows / static_cast<int64_t>(device_sms());
   int64_t c = kMinChunk;
+  while (c < 16 * static_cast<int64_t>(k) && c < 65536) c *= 2;
   while (c * 2 <= want && c < 65536) c *= 2;
   return c;
 }
@@ -822,7 +840,7 @@ cudaError_t launch_topk(const float* scores, Spans sp, int B, int64_t total_rows
     return launch_k(topk_cluster_kernel, dim3(static_cast<unsigned>(B) * kCl), dim3(kThreads),
                     kClDynSmem, stream, pdl, scores, sp, k, w, idx, vals);
   }
-  const int64_t chunk = topk_chunk(total_rows);
+  const int64_t chunk = topk_chunk(total_rows, k);
   const unsigned grid = static_cast<unsigned>((total_rows + chunk - 1) / chunk + B);  // >= chunks
   cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kChunkDynSmem));

@@ -92,7 +92,8 @@ hsa_status_t hsa_workspace_status(void* ws, void* stream, uint32_t* bits);
  * fp32 result is written as fp32 or rounded to nearest-even bf16).  A trailing
  * partial block (T mod r tokens) is not compressed.
  *   kv, z : bf16 [S, T, C]     b : fp32 [r, C]     out : [S, T/r, C] of out_dtype
- * Requirements: S, T >= 0; C a positive multiple of 8; 1 <= r <= 4096.
+ * Requirements: S, T >= 0; C a positive multiple of 8; 1 <= r <= 4096; every
+ * logit z + b finite (masking by a -inf bias is hsa_compress_overlap's).
  * Reads each input byte once; one kernel launch; no workspace.
  * ---------------------------------------------------------------------- */
 hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,

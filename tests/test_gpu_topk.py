@@ -132,6 +132,18 @@ def test_topk_full_size_64_rows_of_262144(oracle_mod):
     _check(oracle_mod, x.reshape(-1), offs, 512)
 
 
+@pytest.mark.parametrize("k", [512, 2048])
+def test_topk_few_long_rows_many_pieces(oracle_mod, k):
+    """4 rows x 262,144 (the C4 length of a 1M-token context): each row is cut
+    into many pieces, whose CTAs also prune at the row's counts so far; one row
+    with ties at the threshold and one with heavy duplicates."""
+    x = synth.topk_scores(SEED, 4, 262144, 0.05)
+    x[1] = synth.pair_ties_at_top(x[1], 600)
+    x[2] = torch.round(x[2] * 16) / 16
+    offs = torch.arange(5, dtype=torch.int64) * 262144
+    _check(oracle_mod, x.reshape(-1), offs, k)
+
+
 def test_topk_nan_sets_status_without_fault():
     vals = torch.tensor([1.0, float("nan"), 2.0, 3.0, 4.0] * 100)
     offs = torch.tensor([0, 500], dtype=torch.int64)
