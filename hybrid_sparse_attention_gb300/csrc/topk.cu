@@ -584,7 +584,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_chunk_kernel(const float* __
       x[g] = e < nk ? list[e] : 0ull;
     }
     if (t == 0) {
-      s_count = 0;
       s_out[0] = atomicMax(&rs->bar, bar);
       atomicMax(&rs->nlow, ~bar);
     }
@@ -605,9 +604,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_chunk_kernel(const float* __
       pbar = max(pbar, find_top_bin(s_hist, b0, static_cast<uint32_t>(k), s_scan, s_out) << kLShift);
       if (t == 0) atomicMax(&rs->bar, pbar);
     }
-    // drop the kept keys below pbar: each group is read whole before any
-    // survivor of it is written, and survivors only move down
+    // drop the kept keys below pbar: per group, masks and one block scan place
+    // the survivors (no shared counter); each group is read whole before any
+    // survivor of it is written (the scan's barriers), and survivors only move down
     if (pbar) {
+      uint32_t kept = 0;
 #pragma unroll 1
       for (uint32_t e0 = 0; e0 < nk; e0 += kThreads * kG) {
         if (e0) {
@@ -616,18 +617,22 @@ __global__ void __launch_bounds__(kThreads, 2) topk_chunk_kernel(const float* __
             const uint32_t e = e0 + g * kThreads + t;
             x[g] = e < nk ? list[e] : 0ull;
           }
-          __syncthreads();
         }
+        uint32_t mask = 0;
 #pragma unroll
         for (int g = 0; g < kG; ++g) {
           const uint32_t e = e0 + g * kThreads + t;
-          const bool keep = e < nk && static_cast<uint32_t>(x[g] >> 32) >= pbar;
-          const uint32_t pos = warp_append(&s_count, keep, 0xffffffffu);
-          if (keep) list[pos] = x[g];
+          mask |= (e < nk && static_cast<uint32_t>(x[g] >> 32) >= pbar ? 1u : 0u) << g;
         }
+        const uint32_t c = __popc(mask);
+        uint32_t tot;
+        uint32_t pos = kept + block_inclusive_sum<uint32_t>(c, s_scan, &tot) - c;
+#pragma unroll
+        for (int g = 0; g < kG; ++g)
+          if ((mask >> g) & 1u) list[pos++] = x[g];
+        kept += tot;
       }
-      __syncthreads();
-      if (t == 0) s_kept = s_count;
+      if (t == 0) s_kept = kept;
     }
   }
   if (t == 0) ws.wcount[blockIdx.x] = s_kept;
