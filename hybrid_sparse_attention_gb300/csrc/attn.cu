@@ -1455,63 +1455,74 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 // thread of a head: cached), forms the weights in registers and combines with
 // every split's partial loads in flight; no shared memory, no barriers.
 constexpr int kMaxSplits = 1024;
-constexpr int kCombineRegs = 16;  // splits whose weights stay in registers
+constexpr int kCombineBlock = 128;  // threads per combine CTA
+constexpr int kCombineChunk = 8;    // splits whose loads are in flight together
 
-__global__ void __launch_bounds__(512) attn_combine_kernel(const float* __restrict__ po,
-                                                          const float* __restrict__ plse, int S,
-                                                          int64_t BH, int Hq, int Dv, void* out,
-                                                          int out_dtype, float* lse) {
+// One thread per 4 output channels of one head: the splits' partial outputs
+// and log-sum-exps, combined in chunks of kCombineChunk splits (every load of
+// a chunk in flight before its arithmetic) with a running maximum.
+__global__ void __launch_bounds__(kCombineBlock) attn_combine_kernel(const float* __restrict__ po,
+                                                                   const float* __restrict__ plse,
+                                                                   int S, int64_t BH, int Hq, int Dv,
+                                                                   void* out, int out_dtype,
+                                                                   float* lse) {
   pdl_wait();
   pdl_trigger();
   const int d4n = Dv / 4;
-  const int64_t gi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 2;
+  const int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gi >= BH * d4n) return;
-  const int64_t head = gi / d4n;  // b * Hq + h; both groups of this thread share it (d4n even)
+  const int64_t head = gi / d4n;  // b * Hq + h
   const int d4 = static_cast<int>(gi % d4n);
   const int64_t b = head / Hq, h = head % Hq;
   const float* ls = plse + b * S * Hq + h;
-  float lv[kCombineRegs];
-  float mx = -INFINITY;
-#pragma unroll
-  for (int s = 0; s < kCombineRegs; ++s) {
-    lv[s] = s < S ? __ldg(ls + static_cast<int64_t>(s) * Hq) : -INFINITY;
-    mx = fmaxf(mx, lv[s]);
-  }
-  for (int s = kCombineRegs; s < S; ++s) mx = fmaxf(mx, __ldg(ls + static_cast<int64_t>(s) * Hq));
   const float4* p4 = reinterpret_cast<const float4*>(po + (b * S * Hq + h) * Dv) + d4;
   const int64_t split4 = static_cast<int64_t>(Hq) * Dv / 4;  // float4s between splits
-  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-  float tot = 0.f;
-  auto add = [&](float l, int s) {
-    if (l == -INFINITY) return;
-    const float w = __expf(l - mx);
-    tot += w;
-    const float4 v0 = __ldcs(p4 + s * split4), v1 = __ldcs(p4 + s * split4 + 1);
-    a0.x = fmaf(w, v0.x, a0.x); a0.y = fmaf(w, v0.y, a0.y);
-    a0.z = fmaf(w, v0.z, a0.z); a0.w = fmaf(w, v0.w, a0.w);
-    a1.x = fmaf(w, v1.x, a1.x); a1.y = fmaf(w, v1.y, a1.y);
-    a1.z = fmaf(w, v1.z, a1.z); a1.w = fmaf(w, v1.w, a1.w);
-  };
+  float mx = -INFINITY, tot = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+  for (int s0 = 0; s0 < S; s0 += kCombineChunk) {
+    float l[kCombineChunk];
+    float4 v[kCombineChunk];
 #pragma unroll
-  for (int s = 0; s < kCombineRegs; ++s) add(lv[s], s);
-  for (int s = kCombineRegs; s < S; ++s) add(__ldg(ls + static_cast<int64_t>(s) * Hq), s);
+    for (int j = 0; j < kCombineChunk; ++j) {
+      const int s = s0 + j;
+      l[j] = s < S ? __ldg(ls + static_cast<int64_t>(s) * Hq) : -INFINITY;
+      v[j] = s < S ? __ldcs(p4 + s * split4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float cm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kCombineChunk; ++j) cm = fmaxf(cm, l[j]);
+    if (cm == -INFINITY) continue;  // nothing attended in this chunk
+    const float nm = fmaxf(mx, cm);
+    const float r = mx == -INFINITY ? 0.f : __expf(mx - nm);  // rescales what came before
+    tot *= r;
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+#pragma unroll
+    for (int j = 0; j < kCombineChunk; ++j) {
+      const float w = l[j] == -INFINITY ? 0.f : __expf(l[j] - nm);
+      tot += w;
+      acc.x = fmaf(w, v[j].x, acc.x);
+      acc.y = fmaf(w, v[j].y, acc.y);
+      acc.z = fmaf(w, v[j].z, acc.z);
+      acc.w = fmaf(w, v[j].w, acc.w);
+    }
+    mx = nm;
+  }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
   const int64_t at = head * Dv + 4 * d4;
   if (out_dtype == HSA_BF16) {
-    const __nv_bfloat162 p0 = __floats2bfloat162_rn(a0.x * inv, a0.y * inv);
-    const __nv_bfloat162 p1 = __floats2bfloat162_rn(a0.z * inv, a0.w * inv);
-    const __nv_bfloat162 p2 = __floats2bfloat162_rn(a1.x * inv, a1.y * inv);
-    const __nv_bfloat162 p3 = __floats2bfloat162_rn(a1.z * inv, a1.w * inv);
-    uint4 pk;
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    const __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 pk;
     pk.x = *reinterpret_cast<const uint32_t*>(&p0);
     pk.y = *reinterpret_cast<const uint32_t*>(&p1);
-    pk.z = *reinterpret_cast<const uint32_t*>(&p2);
-    pk.w = *reinterpret_cast<const uint32_t*>(&p3);
-    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + at) = pk;
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + at) = pk;
   } else {
-    float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + at);
-    o4[0] = make_float4(a0.x * inv, a0.y * inv, a0.z * inv, a0.w * inv);
-    o4[1] = make_float4(a1.x * inv, a1.y * inv, a1.z * inv, a1.w * inv);
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + at) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
   if (d4 == 0 && lse) lse[head] = tot > 0.f ? mx + logf(tot) : -INFINITY;
 }
@@ -1631,8 +1642,10 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
                 static_cast<unsigned>(pl.cl ? pl.S : 0), qmap, swamap, swa_tma, p);
   if (e != cudaSuccess || pl.S == 1 || pl.cl) return e;
   const int64_t bh = a.B * a.Hq;
-  const int64_t threads = bh * (a.Dv / 8);  // two 16-byte groups each
-  return launch_k(attn_combine_kernel, dim3(static_cast<unsigned>((threads + 511) / 512)), dim3(512),
+  const int64_t threads = bh * (a.Dv / 4);  // one per 4 channels of a head
+  return launch_k(attn_combine_kernel,
+                  dim3(static_cast<unsigned>((threads + kCombineBlock - 1) / kCombineBlock)),
+                  dim3(kCombineBlock),
                   0, stream, true, static_cast<const float*>(p.po),
                   static_cast<const float*>(p.plse), pl.S, bh, p.Hq, p.Dv, a.out, a.out_dtype,
                   a.lse);

@@ -24,13 +24,12 @@ HSA_DEVINL void partial_init(GatePartial& p) {
   }
 }
 
-// Rows [i0, i1) of one chunk; row i at kv[i * stride] / z[i * stride]
-// (uint4 units); bias(i, lo, hi) loads the 8 fp32 biases of row i.  kMasked:
+// Rows [i0, i1) of one chunk; rows(i, &kv, &z) gives row i's two 16-byte
+// chunks; bias(i, b0, b1) loads the 8 fp32 biases of row i.  kMasked:
 // a logit may be -inf (a masked position, weight 0); without it every logit
 // is finite (the guards cost about a fifth of the compressor's time).
-template <bool kMasked = false, typename BiasFn>
-HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, int i0, int i1,
-                             BiasFn bias, GatePartial& p) {
+template <bool kMasked = false, typename RowFn, typename BiasFn>
+HSA_DEVINL void partial_rows_at(RowFn rows, int i0, int i1, BiasFn bias, GatePartial& p) {
   constexpr int kGroup = 4;
   for (int r0 = i0; r0 < i1; r0 += kGroup) {
     const int g = min(kGroup, i1 - r0);
@@ -39,8 +38,10 @@ HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, in
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
       if (j < g) {
-        kraw[j] = ld_stream_u4(kv + (r0 + j) * stride);
-        zraw[j] = ld_stream_u4(z + (r0 + j) * stride);
+        const uint4 *kp, *zp;
+        rows(r0 + j, &kp, &zp);
+        kraw[j] = ld_stream_u4(kp);
+        zraw[j] = ld_stream_u4(zp);
         bias(r0 + j, &b0[j], &b1[j]);
       }
     }
@@ -83,6 +84,18 @@ HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, in
       }
     }
   }
+}
+
+// The same over rows at kv[i * stride] / z[i * stride].
+template <bool kMasked = false, typename BiasFn>
+HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, int i0, int i1,
+                             BiasFn bias, GatePartial& p) {
+  partial_rows_at<kMasked>(
+      [&](int i, const uint4** kp, const uint4** zp) {
+        *kp = kv + i * stride;
+        *zp = z + i * stride;
+      },
+      i0, i1, bias, p);
 }
 
 // Merges the partials of `width` adjacent lanes (width a power of two <= 32;

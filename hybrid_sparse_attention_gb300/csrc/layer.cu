@@ -30,6 +30,7 @@ namespace hsa {
 namespace {
 
 constexpr int kAppendThreads = 256;
+constexpr int kAppendLongCtas = 8;  // CTAs per sequence for blocks of more than 4 rows
 
 struct AppendParams {
   int kind, r, B, Dqk, Di, W;
@@ -52,43 +53,13 @@ struct AppendParams {
   uint4* key_pool;
   float* key_scale;  // non-null: key_pool holds E4M3 codes [rows, Di] with these fp32 scales
   uint32_t* status;
+  uint32_t* tickets;  // [B] (blocks of more than kShortBlock rows) CTAs done per sequence, zero between steps
   int T;             // tokens appended per step (rows b * T + t of the new-row inputs)
   int Wr;            // window ring rows (W + T - 1)
 };
 
 
 constexpr int kMaxKeyDi = 128;  // E4M3 key rows (one warp quantizes a row, 4 channels a lane)
-
-// Compresses the r-row ring block of width C (C/8 chunks) of sequence b into
-// `dst` (one bf16 row).  Rows are split over `split` adjacent lanes.
-HSA_DEVINL void compress_block(const uint4* kv, const uint4* z, const float* bias, int r, int C,
-                               uint4* dst) {
-  const int chunks = C / 8;
-  const int split = r >= 32 ? 8 : 1;
-  const int items = chunks * split;  // a multiple of 32 whenever split > 1
-  for (int i0 = 0; i0 < items; i0 += blockDim.x) {
-    const int i = i0 + threadIdx.x;
-    if (split > 1 && i0 + static_cast<int>(threadIdx.x & ~31u) >= items) break;  // whole idle warp
-    const bool live = i < items;
-    const int c = live ? i / split : 0, part = live ? i % split : 0;
-    const int per = (r + split - 1) / split;
-    const int lo = live ? min(r, part * per) : 0, hi = live ? min(r, lo + per) : 0;
-    auto brow = [&](int row, float4* b0, float4* b1) {
-      const float4* bp = reinterpret_cast<const float4*>(bias + static_cast<int64_t>(row) * C + c * 8);
-      *b0 = __ldg(bp);
-      *b1 = __ldg(bp + 1);
-    };
-    GatePartial pt;
-    partial_init(pt);
-    partial_rows(kv + c, z + c, chunks, lo, hi, brow, pt);
-    if (split > 1) partial_merge_lanes(pt, split);
-    if (live && part == 0) {
-      float o[8];
-      partial_result(pt, o);
-      dst[c] = f32x8_to_bf16(o);
-    }
-  }
-}
 
 // Short blocks (r <= 4, the C4 layer): one thread owns one 8-channel chunk of
 // the kv row or of the indexer-key row end to end.  Every load it may need is
@@ -232,15 +203,26 @@ template <int kT>  // tokens per step of the short-block path (p.T == kT there)
 __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendParams p) {
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x;
-  if (p.r <= kShortBlock) {
-    append_short<kT>(p, b);
-    return;
-  }
+  append_short<kT>(p, blockIdx.x);
+}
+
+// Blocks of more than kShortBlock rows (the C128 layer): kAppendLongCtas
+// CTAs per sequence, each compressing a slice of the block's 8-channel chunks
+// (each chunk's rows split over up to 32 lanes, one load round per lane).
+// Block row i is ring slot i; the rows this step appends come straight from
+// the new-row inputs, so no CTA waits for another's ring writes.  The
+// sequence's CTAs take an atomic ticket when done; the last one writes the
+// rows of the step's tokens after the completing one (the next block's first
+// slots, read by the others until then) and the new length (which may alias
+// the one every CTA read), and resets the ticket.
+__global__ void __launch_bounds__(kAppendThreads) layer_append_long_kernel(AppendParams p) {
+  __shared__ int s_last;
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x / kAppendLongCtas, g = blockIdx.x % kAppendLongCtas;
   const int64_t lin = p.seq_len_in[b];
   const int cq = p.Dqk / 8, ci = p.Di / 8;
   const int64_t o0 = p.pool_offsets[b], o1 = p.pool_offsets[b + 1];
-  __syncthreads();  // seq_len_in read by every thread before it may be overwritten
   // a1: tokens [t_lo, t_hi)'s rows into the window ring and the in-flight rings
   auto write_rows = [&](int t_lo, int t_hi) {
     for (int t = t_lo; t < t_hi; ++t) {
@@ -266,27 +248,68 @@ __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendPara
   int tcomp = -1;
   for (int t = 0; t < p.T; ++t)
     if ((lin + t + 1) % p.r == 0) tcomp = t;
-  write_rows(0, tcomp >= 0 ? tcomp + 1 : p.T);
-  __syncthreads();  // ring writes visible to the block
+  if (g == 0) write_rows(0, tcomp >= 0 ? tcomp + 1 : p.T);
   if (tcomp >= 0) {
-    // a2: the block is complete -> compress it into pool row (pos + 1)/r - 1,
-    // before the step's later tokens write the next block's first slots
+    // a2: the block is complete -> compress it into pool row (pos + 1)/r - 1
     const int64_t n = (lin + tcomp + 1) / p.r - 1;
     if (o0 < 0 || o1 > p.pool_total_rows || o0 + n >= o1) {
-      if (threadIdx.x == 0) set_status(p.status, HSA_DEV_BOUNDS);
+      if (threadIdx.x == 0 && g == 0) set_status(p.status, HSA_DEV_BOUNDS);
     } else {
-      compress_block(p.kv_ring + static_cast<int64_t>(b) * p.r * cq,
-                     p.z_ring + static_cast<int64_t>(b) * p.r * cq, p.b_kv, p.r, p.Dqk,
-                     p.kv_pool + (o0 + n) * cq);
-      if (p.kind == HSA_LAYER_C4)
-        compress_block(p.ik_ring + static_cast<int64_t>(b) * p.r * ci,
-                       p.iz_ring + static_cast<int64_t>(b) * p.r * ci, p.b_ik, p.r, p.Di,
-                       p.key_pool + (o0 + n) * ci);
+      // rows [inew, r) are this step's tokens 0..tcomp
+      const int inew = p.r - 1 - tcomp;
+      const uint4* ring_kv = p.kv_ring + static_cast<int64_t>(b) * p.r * cq;
+      const uint4* ring_z = p.z_ring + static_cast<int64_t>(b) * p.r * cq;
+      const int64_t new0 = static_cast<int64_t>(b) * p.T;  // row of the step's token 0
+      const int c0 = g * cq / kAppendLongCtas, c1 = (g + 1) * cq / kAppendLongCtas;
+      int split = 1;
+      while (split < 32 && 8 * split <= p.r) split <<= 1;
+      const int items = (c1 - c0) * split;
+      uint4* dst = p.kv_pool + (o0 + n) * cq;
+      for (int i0 = 0; i0 < items; i0 += blockDim.x) {
+        const int i = i0 + threadIdx.x;
+        if (split > 1 && i0 + static_cast<int>(threadIdx.x & ~31u) >= items) break;  // whole idle warp
+        const bool live = i < items;
+        const int c = c0 + (live ? i / split : 0), part = live ? i % split : 0;
+        const int per = (p.r + split - 1) / split;
+        const int lo = live ? min(p.r, part * per) : 0, hi = live ? min(p.r, lo + per) : 0;
+        auto rows = [&](int row, const uint4** kp, const uint4** zp) {
+          if (row < inew) {
+            *kp = ring_kv + static_cast<int64_t>(row) * cq + c;
+            *zp = ring_z + static_cast<int64_t>(row) * cq + c;
+          } else {
+            *kp = p.kv_new + (new0 + row - inew) * cq + c;
+            *zp = p.z_new + (new0 + row - inew) * cq + c;
+          }
+        };
+        auto brow = [&](int row, float4* b0, float4* b1) {
+          const float4* bp = reinterpret_cast<const float4*>(p.b_kv + static_cast<int64_t>(row) * p.Dqk + c * 8);
+          *b0 = __ldg(bp);
+          *b1 = __ldg(bp + 1);
+        };
+        GatePartial pt;
+        partial_init(pt);
+        partial_rows_at(rows, lo, hi, brow, pt);
+        if (split > 1) partial_merge_lanes(pt, split);
+        if (live && part == 0) {
+          float o[8];
+          partial_result(pt, o);
+          dst[c] = f32x8_to_bf16(o);
+        }
+      }
     }
-    __syncthreads();  // the block read before the later tokens' rows
-    write_rows(tcomp + 1, p.T);
   }
-  if (threadIdx.x == 0) p.seq_len_out[b] = static_cast<int32_t>(lin + p.T);
+  // the sequence's last CTA: the later tokens' rows and the new length
+  __syncthreads();
+  __threadfence();
+  if (threadIdx.x == 0) s_last = atomicAdd(p.tickets + b, 1u) == kAppendLongCtas - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tcomp >= 0) write_rows(tcomp + 1, p.T);
+  if (threadIdx.x == 0) {
+    p.seq_len_out[b] = static_cast<int32_t>(lin + p.T);
+    p.tickets[b] = 0;
+  }
 }
 
 HSA_HOST_DEVICE size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -312,12 +335,14 @@ bool layer_fused(const hsa_layer_desc& d) {
 // With T query tokens the score, top-k and selection areas are per token:
 // token t's scores at pool row positions + t * pool_total_rows.
 struct LayerWs {
-  size_t scores, topk, idx, hist, attn, total;
+  size_t scores, topk, idx, hist, attn, tickets, total;
   LayerWs(const hsa_layer_desc& d, const AttnPlan& pl) {
     const int64_t T = layer_tokens(d), BT = static_cast<int64_t>(d.B) * T;
     const int64_t srows = (d.pool_total_rows > 0 ? d.pool_total_rows : 1) * T;
     size_t at = kWsHeader;
     scores = topk = idx = hist = 0;
+    tickets = at;
+    at += a256(static_cast<size_t>(d.B) * sizeof(uint32_t));
     if (d.kind == HSA_LAYER_C4) {
       scores = at;
       if (!d.scores) at += a256(static_cast<size_t>(srows) * 4);
@@ -384,6 +409,7 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   ap.key_pool = static_cast<uint4*>(d.key_pool);
   ap.key_scale = d.kind == HSA_LAYER_C4 && d.key_fp8 ? d.key_scale : nullptr;
   ap.status = status;
+  ap.tickets = reinterpret_cast<uint32_t*>(w + L.tickets);
   const int T = layer_tokens(d);
   ap.T = T;
   ap.Wr = d.W + T - 1;
@@ -394,7 +420,9 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return e;
   // (one instantiation per token count: the rows of a step live in registers)
-  if (T == 1) layer_append_kernel<1><<<d.B, kAppendThreads, 0, stream>>>(ap);
+  if (ap.r > kShortBlock)
+    layer_append_long_kernel<<<d.B * kAppendLongCtas, kAppendThreads, 0, stream>>>(ap);
+  else if (T == 1) layer_append_kernel<1><<<d.B, kAppendThreads, 0, stream>>>(ap);
   else if (T == 2) layer_append_kernel<2><<<d.B, kAppendThreads, 0, stream>>>(ap);
   else if (T == 3) layer_append_kernel<3><<<d.B, kAppendThreads, 0, stream>>>(ap);
   else layer_append_kernel<4><<<d.B, kAppendThreads, 0, stream>>>(ap);
