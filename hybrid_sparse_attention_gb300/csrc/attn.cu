@@ -834,7 +834,9 @@ HSA_DEVINL void issue_q_tma(const CUtensorMap* qmap, Shared& sh, uint8_t* qs, in
 template <int kN, bool kSel>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ CUtensorMap qmap,
                                                           const __grid_constant__ CUtensorMap swamap,
-                                                          int swa_tma, AttnParams p) {
+                                                          int swa_tma,
+                                                          const __grid_constant__ CUtensorMap poolmap,
+                                                          int pool_tma, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   // Programmatic dependent launch.  When the previous kernel is the top-k
@@ -1091,6 +1093,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           // row) arrives by TMA: the ring's rows in slot order, 64-channel
           // boxes, 128-byte swizzled as the MMA reads them.
           const bool win_tma = swa_tma && tb + tc_ == 0 && geo.n_swa == kKeys && a0 == 0;
+          // A dense tile of 128 live compressed rows (contiguous in the pool)
+          // arrives by TMA too, from a map over the pool's rows.
+          const int64_t tile_slot = static_cast<int64_t>(tb + tc_) * kKeys;
+          const int64_t e_first = tile_slot - geo.n_swa;
+          const bool pool_tile = pool_tma && e_first >= 0 && e_first + kKeys <= geo.n_extra &&
+                                 tile_slot >= a0 && tile_slot + kKeys <= a1;
           for (int it = 0; it < nit; ++it, ++item) {
             if (!ok || item % kProdWarps != pw) continue;
             const int slot = static_cast<int>(item % kRing);
@@ -1102,17 +1110,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 if (!ok) continue;
               }
             }
-            if (win_tma) {
+            if (win_tma || pool_tile) {
               // lane 0 arms the slot with the bytes and issues both slices; the
               // other lanes arrive (the slot's barrier counts 32 arrivals)
               const int j0 = 2 * it;
               const bool two = j0 + 1 < NSL;
               if (lane == 0) {
+                const CUtensorMap* map = win_tma ? &swamap : &poolmap;
+                const int32_t y = win_tma ? b * p.W : static_cast<int32_t>(geo.off + e_first);
                 tc::mbar_arrive_expect_tx(&sh.full[slot], (two ? 2u : 1u) * kSliceBytes);
-                tc::tma_load_2d(ring + slot * kPairBytes, &swamap, j0 * 64, b * p.W, &sh.full[slot]);
+                tc::tma_load_2d(ring + slot * kPairBytes, map, j0 * 64, y, &sh.full[slot]);
                 if (two)
-                  tc::tma_load_2d(ring + slot * kPairBytes + kSliceBytes, &swamap, (j0 + 1) * 64,
-                                  b * p.W, &sh.full[slot]);
+                  tc::tma_load_2d(ring + slot * kPairBytes + kSliceBytes, map, (j0 + 1) * 64, y,
+                                  &sh.full[slot]);
               } else {
                 tc::mbar_arrive(&sh.full[slot]);
               }
@@ -1631,6 +1641,14 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
     e = make_tmap_2d_bf16(&swamap, a.swa, a.Dqk, a.B * a.W, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
   }
+  // dense tiles of 128 live compressed rows are loaded by TMA (a map over
+  // the pool's rows)
+  CUtensorMap poolmap = qmap;  // (unused unless pool_tma)
+  const int pool_tma = !fused && a.extra && !a.idx && a.sp.limit > 0 ? 1 : 0;
+  if (pool_tma) {
+    e = make_tmap_2d_bf16(&poolmap, a.extra, a.Dqk, a.sp.limit, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+  }
   auto* kernel = fused ? (pl.N == 16 ? attn_kernel<16, true>
                                      : (pl.N == 32 ? attn_kernel<32, true> : attn_kernel<64, true>))
                        : (pl.N == 16 ? attn_kernel<16, false>
@@ -1639,7 +1657,8 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
                            static_cast<int>(pl.smem));
   if (e != cudaSuccess) return e;
   e = launch_kc(kernel, dim3(grid), dim3(kThreads), pl.smem, stream, pdl,
-                static_cast<unsigned>(pl.cl ? pl.S : 0), qmap, swamap, swa_tma, p);
+                static_cast<unsigned>(pl.cl ? pl.S : 0), qmap, swamap, swa_tma, poolmap, pool_tma,
+                p);
   if (e != cudaSuccess || pl.S == 1 || pl.cl) return e;
   const int64_t bh = a.B * a.Hq;
   const int64_t threads = bh * (a.Dv / 4);  // one per 4 channels of a head

@@ -30,7 +30,13 @@ namespace hsa {
 namespace {
 
 constexpr int kAppendThreads = 256;
-constexpr int kAppendLongCtas = 8;  // CTAs per sequence for blocks of more than 4 rows
+// rows of a block's 8-channel chunk split over this many lanes (one load
+// round of at most 4 rows each, up to 32 lanes)
+HSA_HOST_DEVICE int block_split(int r) {
+  int split = 1;
+  while (split < 32 && 8 * split <= r) split <<= 1;
+  return split;
+}
 
 struct AppendParams {
   int kind, r, B, Dqk, Di, W;
@@ -54,6 +60,7 @@ struct AppendParams {
   float* key_scale;  // non-null: key_pool holds E4M3 codes [rows, Di] with these fp32 scales
   uint32_t* status;
   uint32_t* tickets;  // [B] (blocks of more than kShortBlock rows) CTAs done per sequence, zero between steps
+  int G;             // (blocks of more than kShortBlock rows) CTAs per sequence
   int T;             // tokens appended per step (rows b * T + t of the new-row inputs)
   int Wr;            // window ring rows (W + T - 1)
 };
@@ -206,9 +213,10 @@ __global__ void __launch_bounds__(kAppendThreads) layer_append_kernel(AppendPara
   append_short<kT>(p, blockIdx.x);
 }
 
-// Blocks of more than kShortBlock rows (the C128 layer): kAppendLongCtas
-// CTAs per sequence, each compressing a slice of the block's 8-channel chunks
-// (each chunk's rows split over up to 32 lanes, one load round per lane).
+// Blocks of more than kShortBlock rows (the C128 layer): p.G CTAs per
+// sequence, each compressing a slice of the block's 8-channel chunks (each
+// chunk's rows split over block_split(r) lanes: one load round per lane, one
+// round of the CTA's threads).
 // Block row i is ring slot i; the rows this step appends come straight from
 // the new-row inputs, so no CTA waits for another's ring writes.  The
 // sequence's CTAs take an atomic ticket when done; the last one writes the
@@ -219,7 +227,8 @@ __global__ void __launch_bounds__(kAppendThreads) layer_append_long_kernel(Appen
   __shared__ int s_last;
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x / kAppendLongCtas, g = blockIdx.x % kAppendLongCtas;
+  const int G = p.G;
+  const int b = blockIdx.x / G, g = blockIdx.x % G;
   const int64_t lin = p.seq_len_in[b];
   const int cq = p.Dqk / 8, ci = p.Di / 8;
   const int64_t o0 = p.pool_offsets[b], o1 = p.pool_offsets[b + 1];
@@ -260,9 +269,8 @@ __global__ void __launch_bounds__(kAppendThreads) layer_append_long_kernel(Appen
       const uint4* ring_kv = p.kv_ring + static_cast<int64_t>(b) * p.r * cq;
       const uint4* ring_z = p.z_ring + static_cast<int64_t>(b) * p.r * cq;
       const int64_t new0 = static_cast<int64_t>(b) * p.T;  // row of the step's token 0
-      const int c0 = g * cq / kAppendLongCtas, c1 = (g + 1) * cq / kAppendLongCtas;
-      int split = 1;
-      while (split < 32 && 8 * split <= p.r) split <<= 1;
+      const int c0 = g * cq / G, c1 = (g + 1) * cq / G;
+      const int split = block_split(p.r);
       const int items = (c1 - c0) * split;
       uint4* dst = p.kv_pool + (o0 + n) * cq;
       for (int i0 = 0; i0 < items; i0 += blockDim.x) {
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(kAppendThreads) layer_append_long_kernel(Appen
   // the sequence's last CTA: the later tokens' rows and the new length
   __syncthreads();
   __threadfence();
-  if (threadIdx.x == 0) s_last = atomicAdd(p.tickets + b, 1u) == kAppendLongCtas - 1;
+  if (threadIdx.x == 0) s_last = atomicAdd(p.tickets + b, 1u) == static_cast<uint32_t>(G) - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -410,6 +418,9 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   ap.key_scale = d.kind == HSA_LAYER_C4 && d.key_fp8 ? d.key_scale : nullptr;
   ap.status = status;
   ap.tickets = reinterpret_cast<uint32_t*>(w + L.tickets);
+  // (blocks of more than kShortBlock rows) CTAs per sequence: the block's
+  // chunk-lane items in one round of each CTA's threads
+  ap.G = (d.Dqk / 8 * block_split(r) + kAppendThreads - 1) / kAppendThreads;
   const int T = layer_tokens(d);
   ap.T = T;
   ap.Wr = d.W + T - 1;
@@ -421,7 +432,7 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   if (e != cudaSuccess) return e;
   // (one instantiation per token count: the rows of a step live in registers)
   if (ap.r > kShortBlock)
-    layer_append_long_kernel<<<d.B * kAppendLongCtas, kAppendThreads, 0, stream>>>(ap);
+    layer_append_long_kernel<<<d.B * ap.G, kAppendThreads, 0, stream>>>(ap);
   else if (T == 1) layer_append_kernel<1><<<d.B, kAppendThreads, 0, stream>>>(ap);
   else if (T == 2) layer_append_kernel<2><<<d.B, kAppendThreads, 0, stream>>>(ap);
   else if (T == 3) layer_append_kernel<3><<<d.B, kAppendThreads, 0, stream>>>(ap);
