@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 T = 2
 
 
-def _run(g):
+def _run(g, T=T):
     B, sh = g.seq_len_in.numel(), g.shape
     res = {"out": torch.empty(B, T, sh.Hq, sh.Dv, dtype=torch.bfloat16, device="cuda"),
            "lse": torch.empty(B, T, sh.Hq, dtype=torch.float32, device="cuda"),
@@ -43,7 +43,7 @@ def _score_tol(iq, w, keys, offs):
     return 2.0 ** -7 * out + 1e-30
 
 
-def _check(oracle_mod, g, s, res, ref, min_agree):
+def _check(oracle_mod, g, s, res, ref, min_agree, T=T):
     kind = g.kind
     Lin = s["seq_len_in"].astype(np.int64)
     assert np.array_equal(res["seq_len_out"].cpu().numpy(), Lin + T)
@@ -103,6 +103,23 @@ def test_layer_two_tokens_tiny(oracle_mod, kind, phase):
     res = _run(g)
     ref = oracle_mod.layer_decode(s, threads=16)
     _check(oracle_mod, g, s, res, ref, min_agree=62 / 64)
+
+
+@pytest.mark.parametrize("kind,tokens,phase", [(4, 3, 1), (4, 3, 3), (4, 4, 0), (4, 4, 3),
+                                               (128, 3, 2), (128, 3, 0), (128, 4, 3),
+                                               (128, 4, 1), (128, 4, 9)])
+def test_layer_three_and_four_tokens_tiny(oracle_mod, kind, tokens, phase):
+    """T = 3 and 4 (the most a step takes): a block completion on the first
+    token (the later tokens then write the next block's first slots after the
+    completed block is read), on the last, or on none."""
+    base = [4096, 384, 260] if kind == 4 else [8192, 1024, 256]
+    L = torch.tensor([b + phase for b in base], dtype=torch.int32)
+    g = synth.filled_state(synth.SEED["tiny"], kind, synth.TINY, L, device="cuda",
+                           name=f"mtp{kind}t{tokens}", T=tokens)
+    s = np_state(g)
+    res = _run(g, T=tokens)
+    ref = oracle_mod.layer_decode(s, threads=16)
+    _check(oracle_mod, g, s, res, ref, min_agree=62 / 64, T=tokens)
 
 
 def test_layer_two_tokens_c4_full_128k_batch64(oracle_mod):
