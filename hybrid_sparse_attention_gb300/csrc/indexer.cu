@@ -16,11 +16,15 @@
 // the K-major layout the MMA descriptors describe.
 //
 // The kernel is bound by the key bytes (2*Di bytes per entry against 4*Hi*Di
-// flops), so it is built to keep HBM busy: one persistent CTA per SM walks a
-// contiguous range of 128-key tiles (tiles never straddle two sequences)
-// through a TMA ring; warp 0 issues the loads, one lane of warp 1 issues the
-// MMAs into alternating TMEM accumulators, and warps 2-5 (one TMEM lane
-// quarter each) drain the accumulators while the next tiles load.
+// flops), so it is built to keep HBM busy: two persistent CTAs per SM each
+// walk a contiguous range of 128-key tiles (tiles never straddle two
+// sequences) through a two-stage TMA ring; warp 0 issues the loads, one lane
+// of warp 1 issues the MMAs into alternating TMEM accumulators, and warps 2-5
+// (one TMEM lane quarter each) drain the accumulators while the next tiles
+// load.  Two CTAs with two stages each stream the pool faster than one CTA
+// with four or six stages (the same or more bytes in flight per SM: 58 against
+// 60-62 us over 1.18 M bf16 keys; 40 against 42-44 us for E4M3), and more
+// than two CTAs per SM are slower again.
 //
 // E4M3 key pool (kFp8): the keys are 8-bit codes with one fp32 scale per entry
 // (half the bytes), the MMAs are kind::f8f6f4 E4M3 x E4M3, and the queries
@@ -44,12 +48,14 @@ namespace {
 
 constexpr int kTileRows = 128;  // M
 constexpr int kQRows = 16;      // N (heads, padded)
-constexpr int kStagesBf16 = 6;  // 36 KB stages (keys + queries), one CTA per SM
-// 16 KB stages (keys), two CTAs per SM: the E4M3 stream is bound by a per-CTA
-// tile rate (more stages, larger boxes or fewer MMAs per tile measured no
-// faster; a second CTA per SM did: 54 -> 42 us over 1.18 M keys)
-constexpr int kStagesFp8 = 6;
-constexpr int kMaxStages = 6;
+constexpr int kStagesBf16 = 2;  // 36 KB stages (keys + queries)
+constexpr int kStagesFp8 = 2;   // 16 KB stages (keys)
+constexpr int kMaxStages = 2;
+constexpr int kCtasPerSm = 2;
+// Dynamic shared memory a CTA asks for at least, so that no third CTA shares
+// an SM: two CTAs hold all 512 TMEM columns (kTmemCols each), and a third
+// would wait in tcgen05.alloc until one of them has finished.
+constexpr size_t kMinSmem = 80 * 1024;
 constexpr int kFp8Di = 128;     // E4M3 keys: one 128-byte swizzle row per entry
 constexpr uint32_t kQ8Bytes = kQRows * kFp8Di;  // one sequence's E4M3 query rows
 constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
@@ -58,6 +64,8 @@ constexpr int kMaxSeqs = 4096;  // tile prefix table (built in a stage buffer be
 constexpr int kAcc = 4;         // accumulators in TMEM (tiles the MMA may run ahead of the epilogue)
 constexpr int kParts = 4;           // independent partial accumulators per tile
 constexpr uint32_t kTmemCols = kAcc * kParts * kQRows;
+static_assert(kCtasPerSm * kTmemCols <= 512, "the resident CTAs' accumulators exceed TMEM");
+static_assert((kCtasPerSm + 1) * kMinSmem > 228 * 1024, "a further CTA would fit in shared memory");
 
 struct IndexerParams {
   const float* w;  // [B, Hi]
@@ -564,8 +572,9 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_kernel(const __grid_const
 }  // namespace
 
 size_t indexer_smem_bytes(int Di, bool fp8) {
-  if (fp8) return static_cast<size_t>(kStagesFp8) * kTileRows * kFp8Di + 2 * kQ8Bytes + 1024;
-  return static_cast<size_t>(kStagesBf16) * Di * 2 * (kTileRows + kQRows) + 1024;
+  const size_t need = fp8 ? static_cast<size_t>(kStagesFp8) * kTileRows * kFp8Di + 2 * kQ8Bytes + 1024
+                          : static_cast<size_t>(kStagesBf16) * Di * 2 * (kTileRows + kQRows) + 1024;
+  return need > kMinSmem ? need : kMinSmem;
 }
 
 cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spans sp, int B, int Hi,
@@ -596,9 +605,9 @@ cudaError_t launch_indexer(const void* iq, const float* w, const void* keys, Spa
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(fp8 ? smem : indexer_smem_bytes(128)));
   if (e != cudaSuccess) return e;
-  // persistent: one CTA per SM (E4M3: two), fewer when there are fewer tiles
+  // persistent: two CTAs per SM, fewer when there are fewer tiles
   const int64_t tiles_bound = (total_rows + kTileRows - 1) / kTileRows + B;
-  const int nres = (fp8 ? 2 : 1) * device_sms();
+  const int nres = kCtasPerSm * device_sms();
   const int grid = static_cast<int>(tiles_bound < nres ? tiles_bound : nres);
   IndexerParams p{w, sp, B, Hi, Di, T, total_rows, scores, status, pdl ? wait_mode : 0, row_hist,
                   key_scale, static_cast<const uint16_t*>(iq), wait_limit_ns(), wait_limit_polls()};

@@ -94,7 +94,11 @@ hsa_status_t hsa_workspace_status(void* ws, void* stream, uint32_t* bits);
  *   kv, z : bf16 [S, T, C]     b : fp32 [r, C]     out : [S, T/r, C] of out_dtype
  * Requirements: S, T >= 0; C a positive multiple of 8; 1 <= r <= 4096; every
  * logit z + b finite (masking by a -inf bias is hsa_compress_overlap's).
- * Reads each input byte once; one kernel launch; no workspace.
+ * Reads each input byte once; one kernel launch; no workspace.  Blocks of
+ * r <= 16 tokens with C <= 768 pass through a shared-memory ring (bulk
+ * copies); its waits are bounded (200 ms, which a working GPU does not reach),
+ * and one that runs out ends the kernel with the output incomplete: with no
+ * status word, that is not reported.
  * ---------------------------------------------------------------------- */
 hsa_status_t hsa_compress(const void* kv, const void* z, const float* b, int64_t S, int64_t T,
                           int64_t C, int64_t r, void* out, int out_dtype, void* stream);
@@ -128,7 +132,7 @@ hsa_status_t hsa_compress_overlap(const void* kv, const void* z, const float* b,
  *   offsets : int64 [B+1]   scores : fp32 [total_rows]
  * Requirements: 1 <= B <= 4096; 1 <= Hi <= 16; Di in {32, 64, 128}; iq and
  * keys 16-byte aligned.  Rows outside every sequence are not written.  One
- * launch (persistent, one CTA per SM).
+ * launch (persistent, two CTAs per SM).
  * Workspace: hsa_indexer_scores_workspace_size() bytes (status word only).
  * ---------------------------------------------------------------------- */
 size_t hsa_indexer_scores_workspace_size(void);

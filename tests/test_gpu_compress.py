@@ -22,9 +22,16 @@ def _inputs(S, T, C, r, tag):
     return kv, z, b
 
 
+# besides the ratios and widths of the workloads: shared-memory stages that
+# span two sequences (5 blocks a sequence, 4 a stage, 2 tail tokens each), one
+# block a stage (r = 16, the longest staged block), the first lengths past it
+# (r = 20, 33: one thread per chunk and block), the widest staged row (C = 768)
+# and the first width past it (C = 776)
 @pytest.mark.parametrize("S,T,C,r", [(2, 1024, 512, 4), (2, 1024, 512, 128), (3, 37, 24, 4),
                                      (1, 130, 64, 128), (2, 16, 8, 1), (1, 300, 16, 7),
-                                     (4, 4096, 576, 4), (4, 4096, 128, 4)])
+                                     (4, 4096, 576, 4), (4, 4096, 128, 4), (3, 22, 512, 4),
+                                     (2, 160, 256, 16), (2, 100, 64, 20), (2, 300, 576, 33),
+                                     (2, 90, 768, 3), (1, 64, 776, 4)])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_compress_matches_oracle(oracle_mod, S, T, C, r, out_dtype):
     kv, z, b = _inputs(S, T, C, r, f"{S}.{T}.{C}.{r}")
