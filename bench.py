@@ -295,7 +295,9 @@ def parse_args(argv):
     ap.add_argument("--no-extra", action="store_true",
                     help="c4layer: skip the other configurations' timings")
     ap.add_argument("--profile", action="store_true",
-                    help="profiling run: build the workload, run two layer steps, exit")
+                    help="profiling run, for ncu: build the workload of --config, run it twice "
+                         "(c4layer: two layer steps; topk: two calls; compress: two calls at each "
+                         "ratio on 4 sequences), exit")
     ap.add_argument("--profile-ctx", type=int, nargs=2, default=None, metavar=("LO", "HI"),
                     help="with --profile: context lengths ~ U[LO, HI] instead of the bench's "
                          "(a smaller case of the same layer for multi-pass ncu captures)")
@@ -318,7 +320,12 @@ def main(argv=None, measure=None):
         if args.impl == "reference":
             run_reference(args, world, rank, dist)
         elif args.profile:
-            run_profile_topk() if args.config == "topk" else run_profile(args.profile_ctx)
+            if args.config == "topk":
+                run_profile_topk()
+            elif args.config == "compress":
+                run_profile_compress()
+            else:
+                run_profile(args.profile_ctx)
         else:
             run_hsa(args, world, rank, local, dist, measure)
     finally:
@@ -838,6 +845,23 @@ def run_profile_topk():
     torch.cuda.synchronize()
     assert _lib.hsa_workspace_status(ws) == 0
     print(json.dumps({"profile": "ok", "scores": int(x.numel())}))
+
+
+def run_profile_compress(S=4):
+    """Two compressor calls at each ratio (r = 4, then r = 128; the first of
+    each warms up) on S sequences of the standalone shape (65,536 x 512: 537 MB
+    of kv and z at S = 4, larger than L2), for ncu."""
+    _lib.load(build_if_missing=True)
+    seed = synth.SEED["compress"]
+    kv = synth.normal_bf16(seed, "compress.kv", (S, 65536, 512), device="cuda")
+    z = synth.normal_bf16(seed, "compress.z", (S, 65536, 512), device="cuda")
+    for r in (4, 128):
+        b = synth.normal(seed, f"compress.b{r}", (r, 512), std=0.5, device="cuda")
+        out = torch.empty(S, 65536 // r, 512, dtype=torch.bfloat16, device="cuda")
+        for _ in range(2):
+            _lib.hsa_compress(kv, z, b, r, out=out)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": "ok", "sequences": S}))
 
 
 def multi_layer_graph(args, flush, runs, iters=10):
