@@ -894,9 +894,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const uint32_t qslice = kN * 128;       // bytes of one Q slice (kN heads x 64 channels)
   uint8_t* ring = smem;
   uint8_t* qs = ring + kRing * kPairBytes;  // Q during pass 1 ...
-  // P^T buffers (2 K-blocks of 64 keys x kN heads each): tile gt uses buffer
-  // gt & 1; buffer 1 is the start of the Q region, written only once the
-  // chunk's pass 1 is complete
+  // P^T buffers (2 K-blocks of 64 keys x kN heads each; with 64 heads instead
+  // one 128-byte row of 64 heads per key, MN-major for the O^T MMA, so that a
+  // softmax thread writes its key's row with 16-byte stores): tile gt uses
+  // buffer gt & 1; buffer 1 is the start of the Q region, written only once
+  // the chunk's pass 1 is complete
   uint8_t* const pbuf0 = qs + attn_q_region(NSL, kN);
   uint8_t* const pbuf1 = qs;
   // TMEM columns: S^T of chunk tile tc at tc*kN; O^T M-tile m at (TC + m)*kN
@@ -1157,7 +1159,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idS = tc::idesc_bf16_f32(kKeys, kN);
-      const uint32_t idO = tc::idesc_bf16_f32(kKeys, kN, /*a_mn=*/true, /*b_mn=*/false);
+      const uint32_t idO = tc::idesc_bf16_f32(kKeys, kN, /*a_mn=*/true, /*b_mn=*/kN == 64);
       bool ok = true;
       int64_t item = 0;
       int gt = 0;  // tiles through pass 2 so far (P^T buffer gt & 1)
@@ -1217,8 +1219,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             tc::fence_after_sync();
             const uint32_t va = tc::smem_u32(ring + slot * kPairBytes);
             for (int kk = 0; kk < kKeys / 16; ++kk) {
-              const uint64_t bp = tc::smem_desc(pa + (kk >> 2) * kN * 128 + (kk & 3) * 32, 16, 1024,
-                                                tc::kSwizzle128B);
+              // P: 16 keys (K) per step; 64 heads are one 128-byte row per key
+              // (MN-major), fewer heads a K-major row per head
+              const uint64_t bp =
+                  kN == 64 ? tc::smem_desc(pa + kk * 2048, 16, 1024, tc::kSwizzle128B)
+                           : tc::smem_desc(pa + (kk >> 2) * kN * 128 + (kk & 3) * 32, 16, 1024,
+                                           tc::kSwizzle128B);
               const uint64_t a = tc::smem_desc(va + kk * 2048, kSliceBytes, 1024, tc::kSwizzle128B);
               tc::mma_bf16(tmem + (TC + m) * kN, a, bp, idO, (gt > 0 || kk > 0) ? 1u : 0u);
             }
@@ -1354,27 +1360,49 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             break;
           }
         }
-        uint8_t* ptb = (buf ? pbuf1 : pbuf0) + (tid >> 6) * kN * 128;
-        const int kc = (tid & 63) >> 3, ke = (tid & 7) << 1;
+        // P = 2^(S^T - m), rounded to bf16 (l sums the rounded values)
+        auto p_pair = [&](const float (&x)[32], int i, int h) {
+          const float m0 = sh.m[h], m1 = sh.m[h + 1];
+          const float p0 = m0 == -INFINITY ? 0.f : tc::ex2_approx(x[i] - m0);
+          const float p1 = m1 == -INFINITY ? 0.f : tc::ex2_approx(x[i + 1] - m1);
+          const __nv_bfloat162 q2 = __floats2bfloat162_rn(p0, p1);
+          l_part[h] += __low2float(q2);
+          l_part[h + 1] += __high2float(q2);
+          return *reinterpret_cast<const uint32_t*>(&q2);
+        };
+        if constexpr (kN == 64) {
+          // key tid's row: 8 chunks of 8 heads, 128-byte swizzled (chunk c at c ^ (tid & 7))
+          uint8_t* prow = (buf ? pbuf1 : pbuf0) + (tid >> 3) * 1024 + (tid & 7) * 128;
 #pragma unroll
-        for (int gi = 0; gi < kGroups; ++gi) {
-          float x[32];
-          load_s(tc_ * kN + gi * 32, valid, x);
+          for (int gi = 0; gi < kGroups; ++gi) {
+            float x[32];
+            load_s(tc_ * kN + gi * 32, valid, x);
 #pragma unroll
-          for (int i = 0; i < kGW; i += 2) {
-            const int h = gi * 32 + i;
-            const float m0 = sh.m[h], m1 = sh.m[h + 1];
-            const float p0 = m0 == -INFINITY ? 0.f : tc::ex2_approx(x[i] - m0);
-            const float p1 = m1 == -INFINITY ? 0.f : tc::ex2_approx(x[i + 1] - m1);
-            const __nv_bfloat162 q2 = __floats2bfloat162_rn(p0, p1);
-            l_part[h] += __low2float(q2);
-            l_part[h + 1] += __high2float(q2);
-            const uint32_t pk = *reinterpret_cast<const uint32_t*>(&q2);
-            *reinterpret_cast<uint16_t*>(ptb + (h >> 3) * 1024 + (h & 7) * 128 +
-                                         ((kc ^ (h & 7)) << 4) + ke) = static_cast<uint16_t>(pk);
-            const int h1 = h + 1;
-            *reinterpret_cast<uint16_t*>(ptb + (h1 >> 3) * 1024 + (h1 & 7) * 128 +
-                                         ((kc ^ (h1 & 7)) << 4) + ke) = static_cast<uint16_t>(pk >> 16);
+            for (int c4 = 0; c4 < 4; ++c4) {
+              uint32_t w[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) w[j] = p_pair(x, c4 * 8 + 2 * j, gi * 32 + c4 * 8 + 2 * j);
+              const int c = gi * 4 + c4;
+              *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        } else {
+          uint8_t* ptb = (buf ? pbuf1 : pbuf0) + (tid >> 6) * kN * 128;
+          const int kc = (tid & 63) >> 3, ke = (tid & 7) << 1;
+#pragma unroll
+          for (int gi = 0; gi < kGroups; ++gi) {
+            float x[32];
+            load_s(tc_ * kN + gi * 32, valid, x);
+#pragma unroll
+            for (int i = 0; i < kGW; i += 2) {
+              const int h = gi * 32 + i;
+              const uint32_t pk = p_pair(x, i, h);
+              *reinterpret_cast<uint16_t*>(ptb + (h >> 3) * 1024 + (h & 7) * 128 +
+                                           ((kc ^ (h & 7)) << 4) + ke) = static_cast<uint16_t>(pk);
+              const int h1 = h + 1;
+              *reinterpret_cast<uint16_t*>(ptb + (h1 >> 3) * 1024 + (h1 & 7) * 128 +
+                                           ((kc ^ (h1 & 7)) << 4) + ke) = static_cast<uint16_t>(pk >> 16);
+            }
           }
         }
         tc::fence_proxy_async_smem();
