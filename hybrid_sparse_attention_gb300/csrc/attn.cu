@@ -726,8 +726,10 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
   __syncthreads();
   const bool bf = p.out_dtype == HSA_BF16;
   const int64_t head0 = static_cast<int64_t>(b) * p.Hq + g * p.HG;
-  // Warp half hw finishes units u = rank + S*hw + 2S*k, two per round (both
-  // TMEM loads in flight before one wait, two transposes).  When 2S is a
+  // Warp half hw finishes units u = rank + S*hw + 2S*k, one per round (two
+  // per round, their TMEM loads in flight together, measured 0.7 us slower
+  // per layer: this code runs once per launch, and the larger loop body costs
+  // more in instruction fetches than the overlap saves).  When 2S is a
   // multiple of kQ those units share one 16-head group, whose weights and
   // 1/L then stay in registers (else they are read per unit).
   const bool fixed = (2 * S) % kQ == 0;
@@ -744,7 +746,7 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
     }
   };
   if (fixed) load_w((rank + S * hw) % kQ);
-  uint8_t* tr0 = scratch + warp * (2 * 16 * 32 * 4);  // two per-warp transpose buffers
+  uint8_t* tr0 = scratch + warp * (2 * 16 * 32 * 4);  // the warp's transpose buffer
   // combines unit u's parts (own: a, from TMEM) into o, scaled by 1/L
   auto combine = [&](int u, const uint32_t (&a)[16], float (&o)[16]) {
 #pragma unroll
@@ -797,25 +799,17 @@ HSA_DEVINL void cluster_merge(const AttnParams& p, Shared& sh, uint8_t* ring, ui
     }
   };
 #pragma unroll 1
-  for (int u = rank + S * hw; u < U; u += 4 * S) {
-    const int u2 = u + 2 * S;
-    const bool two = u2 < U;
-    uint32_t a[16], c[16];
+  for (int u = rank + S * hw; u < U; u += 2 * S) {
+    uint32_t a[16];
     if (own) {
       tc::tmem_ld16(unit_col(u), a);
-      tc::tmem_ld16(unit_col(two ? u2 : u), c);
       tc::tmem_ld_wait();
     }
-    float o[16], o2[16];
+    float o[16];
     if (!fixed) load_w(u % kQ);
     combine(u, a, o);
-    if (two) {
-      if (!fixed) load_w(u2 % kQ);
-      combine(u2, c, o2);
-    }
-    __syncwarp();  // the transpose buffers are free (previous round's reads done)
+    __syncwarp();  // the transpose buffer is free (previous round's reads done)
     write_out(u, o, tr0);
-    if (two) write_out(u2, o2, tr0 + 16 * 32 * 4);
   }
 }
 
@@ -885,6 +879,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     return kSel && static_cast<int64_t>(chunk_tb(c) + chunk_nct(c)) * kKeys > geo.n_swa;
   };
   const int nchunks = win_tiles > 0 ? 1 + (nt - win_tiles + TC - 1) / TC : (nt + TC - 1) / TC;
+  // Q shares its region with P^T buffer 1, which the tiles with an odd index
+  // (counted over the split's chunks) use: chunk c reloads Q only when chunk
+  // c - 1 had such a tile (a one-tile window chunk leaves Q in place)
+  auto q_reload = [&](int c) {
+    return c > 0 && (chunk_nct(c - 1) >= 2 || ((chunk_tb(c - 1) - t0) & 1) != 0);
+  };
   const uint32_t crank = p.cl ? cluster_rank() : 0u;
   const bool selector = kSel && s == p.S - 1;
   const int64_t sel_e0 = kSel ? share_first(p, geo.n_swa, s) : 0;  // first entry of this split's share
@@ -1069,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         }
       }
       tc::named_barrier(2, kProdThreads);
-      if (c > 0) {
+      if (q_reload(c)) {
         // Q shares its region with the P^T buffers of the previous chunk, free
         // once that chunk's last O^T MMAs are done
         const int lt = tb - t0 - 1;
@@ -1163,13 +1163,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       bool ok = true;
       int64_t item = 0;
       int gt = 0;  // tiles through pass 2 so far (P^T buffer gt & 1)
+      int nq = 0;  // Q loads waited for
       for (int c = 0; c < nchunks && ok; ++c) {
         const int nct = chunk_nct(c);
         if (c > 0 && !wait_or_abort(sh, &sh.s_empty, (c - 1) & 1, p.status)) {
           ok = false;
           break;
         }
-        if (!wait_or_abort(sh, &sh.q_full, c & 1, p.status)) {
+        if ((c == 0 || q_reload(c)) && !wait_or_abort(sh, &sh.q_full, (nq++) & 1, p.status)) {
           ok = false;
           break;
         }
