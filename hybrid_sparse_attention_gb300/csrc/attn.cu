@@ -100,7 +100,7 @@ struct AttnParams {
   float* po;              // partial outputs [B, S, Hq, Dv] (S > 1)
   float* plse;            // partial lse [B, S, Hq] (S > 1)
   uint32_t* status;
-  int early;              // the previous kernel writes only idx (see AttnArgs)
+  int early;              // 1: the previous kernel writes only idx; 2: it is the append (see AttnArgs)
   int cl;                 // the S splits form a cluster and merge in shared memory
   // Fused selection (the layer's C4 path; sel_scores != null): idx is null and
   // the last split of every token selects the token's top-k itself from the
@@ -834,10 +834,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   // Programmatic dependent launch.  When the previous kernel is the top-k
-  // (p.early), it triggered this launch only after its own wait, so everything
-  // older (the append's window rows and lengths, q) is complete and only the
-  // index lists need the wait, which the gather and softmax threads take right
-  // before reading them.  Otherwise every thread waits first.
+  // (p.early 1), it triggered this launch only after its own wait, so
+  // everything older (the append's window rows and lengths, q) is complete and
+  // only the index lists need the wait, which the gather and softmax threads
+  // take right before reading them.  When it is the append of a dense layer
+  // (p.early 2), the lengths come from the step's input and the gatherers wait
+  // right before the first tile holding a row the append writes.  Otherwise
+  // every thread waits first.
   if (!p.early) {
     pdl_wait();
     pdl_trigger();
@@ -864,6 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           for (int dv = tid; dv < p.Dv; dv += kKeys) write_result(p, b, g, s, h, dv, 0.f);
       if (tid < p.HG) write_lse(p, b, g, s, tid, -INFINITY);
     }
+    if (p.early == 2 && tid == 0) pdl_wait();  // the grid completes only after the previous kernel
     return;
   }
   if (!kSel && p.extra && !p.idx && geo.nb > p.max_rows && tid == 0 && s == 0 && g == 0)
@@ -1016,6 +1020,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       ++np;
     };
     bool q_pre = selector;  // the selecting split issued chunk 0's Q before selecting
+    // (p.early 2) whether tile tt holds a row the append writes: a window row
+    // (the step's tokens are among them) or a pool row of a block completed in
+    // this step (rows L_in / r and later; here slot n_swa + e holds pool row e)
+    bool dep_waited = p.early != 2;
+    auto append_tile = [&](int tt) {
+      const int64_t s0 = static_cast<int64_t>(tt) * kKeys;
+      if (s0 < geo.n_swa) return true;
+      const int64_t L_in = geo.L - 1 - (p.T == 1 ? 0 : b % p.T);
+      return s0 + kKeys > geo.n_swa + L_in / p.sp.ratio;
+    };
     auto issue_q = [&]() {  // Q by TMA, one thread
       if (q_pre) {
         q_pre = false;
@@ -1034,7 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       }
       if (c == 0) {
         issue_q();  // q is not written by the previous kernel: load it before waiting
-        pdl_wait();
+        if (p.early != 2) pdl_wait();
         pdl_trigger();
       }
       if (chunk_sel(c)) {  // this chunk's compressed rows come from the selection
@@ -1084,6 +1098,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       for (int pass = 0; pass < 2; ++pass) {
         const int nit = pass == 0 ? NP1 : NMT;
         for (int tc_ = 0; tc_ < nct; ++tc_) {
+          if (!dep_waited && append_tile(tb + tc_)) {
+            pdl_wait();
+            dep_waited = true;
+          }
           const uint16_t* const* table = sh.rows[tc_];
           // this lane's rows r0 + 4k of the tile, held in registers for the
           // tile's items: the copy loop below then issues back to back (its
@@ -1155,6 +1173,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       retire_all();  // the chunk's Q and items are all signalled
     }
     retire_all();
+    if (!dep_waited) pdl_wait();  // the grid completes only after the previous kernel
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -1268,7 +1287,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     for (int c = 0; c < nchunks && ok; ++c) {
       const int tb = chunk_tb(c), nct = chunk_nct(c);
       // which of this lane's slots are attended, per chunk tile (loads issued before any wait)
-      if (c == 0) pdl_wait();  // the index lists come from the previous kernel
+      if (c == 0 && p.early != 2) pdl_wait();  // the index lists come from the previous kernel
       if (chunk_sel(c) && !agree(!wait_cluster_or_abort(&sh.abort, &sh.sel_full, 0, p.status))) {
         ok = false;
         break;
@@ -1647,7 +1666,7 @@ cudaError_t launch_attn(const AttnArgs& a, const AttnPlan& pl, void* ws, uint32_
   p.out_dtype = a.out_dtype;
   p.lse = a.lse;
   p.status = status;
-  p.early = a.only_idx_pending ? 1 : 0;
+  p.early = a.only_idx_pending ? 1 : (a.append_pending && !a.idx && !a.sel_scores ? 2 : 0);
   p.cl = pl.cl;
   p.sel_scores = a.sel_scores;
   p.row_hist = a.row_hist;

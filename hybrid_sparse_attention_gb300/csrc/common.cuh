@@ -182,6 +182,11 @@ struct AttnArgs {
   // writes only the index lists: the window rows, lengths and q may be read
   // before waiting for it.  False when it may write anything else.
   bool only_idx_pending = false;
+  // Dense attention (idx null) right after the append: the lengths come from
+  // the step's input (seq_len + len_add, not written by the append), and only
+  // the tiles holding rows the append writes (the window's, and the pool rows
+  // of a block completed in this step) wait for it.
+  bool append_pending = false;
   // Fused selection (idx null): the kernel selects every token's top-k itself
   // from these scores (at the pool's row positions) and the per-row key
   // histograms the indexer built (zeroed again), writing the selection in

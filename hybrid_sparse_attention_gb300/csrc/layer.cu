@@ -521,16 +521,20 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
     if ((e = mark(2)) != cudaSuccess) return e;
     if ((e = mark(3)) != cudaSuccess) return e;
   }
+  // C128: with separate output lengths the attention takes its geometry from
+  // the input lengths (plus one per token) and starts while the append runs
+  const bool early = d.kind == HSA_LAYER_C128 && d.seq_len_out != d.seq_len_in;
+  const Spans sp_in{d.pool_offsets, d.seq_len_in, T, r, d.pool_total_rows};
   AttnArgs a;
   a.q = d.q;
   a.swa = d.swa;
-  a.seq_len = d.seq_len_out;
-  a.len_add = 1 - T;  // token t: L_out - (T - 1 - t)
+  a.seq_len = early ? d.seq_len_in : d.seq_len_out;
+  a.len_add = early ? 1 : 1 - T;  // token t: L_in + 1 + t = L_out - (T - 1 - t)
   a.W = d.W;
   a.T = T;
   a.Wr = d.W + T - 1;
   a.extra = d.kv_pool;
-  a.sp = tokens(sp);
+  a.sp = tokens(early ? sp_in : sp);
   a.idx = idx;
   a.k = d.kind == HSA_LAYER_C4 ? d.k : 0;
   a.max_rows = d.kind == HSA_LAYER_C4 ? 0 : d.max_pool_rows;
@@ -543,6 +547,7 @@ cudaError_t launch_layer(const hsa_layer_desc& d, void* ws, cudaStream_t stream)
   a.out_dtype = d.out_dtype;
   a.lse = d.lse;
   a.only_idx_pending = d.kind == HSA_LAYER_C4;  // C128: the append comes right before
+  a.append_pending = early;
   bool pdl = true;
   if (d.q_ready_event) {
     // q may still be arriving on another stream: the attention waits for it

@@ -144,10 +144,13 @@ def test_layer_tiny_dense_equivalence_k_covers_all():
     assert (res["lse"] - l).abs().max().item() <= 1e-3
 
 
-def test_layer_multi_step_in_place(oracle_mod):
+@pytest.mark.parametrize("kind", [4, 128])
+def test_layer_multi_step_in_place(oracle_mod, kind):
     """Six consecutive in-place steps (seq_len_out aliases seq_len_in) crossing
-    two block completions; the state carried by the rings stays in parity."""
-    kind = 4
+    block completions (C4: two; C128: one, at L = 4096); the state carried by
+    the rings stays in parity.  With aliased lengths the C128 attention waits
+    for the append before reading any length (with separate ones it starts
+    while the append runs)."""
     st, raw = build_tiny(kind, L=4091, slack=4)   # room for the blocks of 6 more tokens
     s = np_state(st)
     oracle_prefix_pools(oracle_mod, s, raw, kind)
@@ -155,7 +158,7 @@ def test_layer_multi_step_in_place(oracle_mod):
     gpu_prefix_pools(g, raw, kind)
     for step in range(6):
         name = f"step{step}"
-        for key in ("kv_new", "z_new", "ik_new", "iz_new"):
+        for key in ("kv_new", "z_new") + (("ik_new", "iz_new") if kind == 4 else ()):
             v = synth.normal_bf16(synth.SEED["tiny"], f"{name}.{key}", tuple(getattr(st, key).shape))
             getattr(g, key).copy_(v.cuda())
             s[key] = bf16_bits(v)
