@@ -867,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           for (int dv = tid; dv < p.Dv; dv += kKeys) write_result(p, b, g, s, h, dv, 0.f);
       if (tid < p.HG) write_lse(p, b, g, s, tid, -INFINITY);
     }
-    if (p.early == 2 && tid == 0) pdl_wait();  // the grid completes only after the previous kernel
+    if (!kSel && p.early == 2 && tid == 0) pdl_wait();  // the grid completes only after the previous kernel
     return;
   }
   if (!kSel && p.extra && !p.idx && geo.nb > p.max_rows && tid == 0 && s == 0 && g == 0)
@@ -1023,7 +1023,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     // (p.early 2) whether tile tt holds a row the append writes: a window row
     // (the step's tokens are among them) or a pool row of a block completed in
     // this step (rows L_in / r and later; here slot n_swa + e holds pool row e)
-    bool dep_waited = p.early != 2;
+    bool dep_waited = kSel || p.early != 2;  // (compiled out of the fused-selection kernel)
     auto append_tile = [&](int tt) {
       const int64_t s0 = static_cast<int64_t>(tt) * kKeys;
       if (s0 < geo.n_swa) return true;
@@ -1048,7 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       }
       if (c == 0) {
         issue_q();  // q is not written by the previous kernel: load it before waiting
-        if (p.early != 2) pdl_wait();
+        if (kSel || p.early != 2) pdl_wait();
         pdl_trigger();
       }
       if (chunk_sel(c)) {  // this chunk's compressed rows come from the selection
@@ -1287,7 +1287,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     for (int c = 0; c < nchunks && ok; ++c) {
       const int tb = chunk_tb(c), nct = chunk_nct(c);
       // which of this lane's slots are attended, per chunk tile (loads issued before any wait)
-      if (c == 0 && p.early != 2) pdl_wait();  // the index lists come from the previous kernel
+      if (c == 0 && (kSel || p.early != 2)) pdl_wait();  // the index lists come from the previous kernel
       if (chunk_sel(c) && !agree(!wait_cluster_or_abort(&sh.abort, &sh.sel_full, 0, p.status))) {
         ok = false;
         break;
