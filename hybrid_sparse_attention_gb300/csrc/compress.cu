@@ -15,13 +15,14 @@
 // shared memory, a thread per 16-byte chunk (8 channels) of one block.  The
 // ring keeps the bytes in flight independent of the registers a thread
 // needs: the per-thread layout below, every thread loading its block's rows
-// into registers, holds one 256-thread CTA per SM (213 registers a thread),
-// which keeps too few short blocks in flight (r = 4: 1.59 ms against 0.90 ms
-// over 32 x 65,536 x 512).
+// into registers in groups of 4, held one 256-thread CTA per SM (213
+// registers a thread), which kept too few short blocks in flight (r = 4:
+// 1.59 ms against 0.90 ms over 32 x 65,536 x 512).
 //
 // Longer blocks (and the overlap variant, and C > 768): one thread owns one
 // chunk of one block and streams the block's r rows of kv and z through
-// registers; its long row loop keeps enough loads in flight.  Consecutive
+// registers, one row at a time (few registers: two CTAs per SM keep enough
+// loads in flight).  Consecutive
 // threads own consecutive chunks of the same row (a warp reads 512 contiguous
 // bytes per load).  The staged layout with 16-row slices of long blocks cut
 // across lanes was slower there (r = 128: 1.60 ms against 1.07 ms).
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm) compress_str
 }
 
 template <bool kBf16Out, bool kOverlap>
-__global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__ kv,
+__global__ void __launch_bounds__(256, 2) compress_kernel(const uint4* __restrict__ kv,
                                                        const uint4* __restrict__ z,
                                                        const float* __restrict__ b, int64_t S,
                                                        int64_t T, int64_t C, int r,
@@ -233,7 +234,9 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__
     };
     GatePartial part;
     partial_init(part);
-    partial_rows<kOverlap>(kv + first, z + first, chunks, 0, i1 - i0, bias, part);
+    // one row at a time: ~70 registers, two CTAs per SM (groups of 4 rows took
+    // 213 registers and one CTA per SM: r = 128 1.07 -> 0.91 ms)
+    partial_rows<kOverlap, 1>(kv + first, z + first, chunks, 0, i1 - i0, bias, part);
     float o[8];
     partial_result(part, o);
     if (kBf16Out) {

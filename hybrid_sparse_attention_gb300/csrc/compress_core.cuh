@@ -28,9 +28,10 @@ HSA_DEVINL void partial_init(GatePartial& p) {
 // chunks; bias(i, b0, b1) loads the 8 fp32 biases of row i.  kMasked:
 // a logit may be -inf (a masked position, weight 0); without it every logit
 // is finite (the guards cost about a fifth of the compressor's time).
-template <bool kMasked = false, typename RowFn, typename BiasFn>
+// kGroup rows share one maximum and one rescale: larger groups take fewer
+// exponentials, smaller ones fewer registers (1 = one rescale per row).
+template <bool kMasked = false, int kGroup = 4, typename RowFn, typename BiasFn>
 HSA_DEVINL void partial_rows_at(RowFn rows, int i0, int i1, BiasFn bias, GatePartial& p) {
-  constexpr int kGroup = 4;
   for (int r0 = i0; r0 < i1; r0 += kGroup) {
     const int g = min(kGroup, i1 - r0);
     uint4 kraw[kGroup], zraw[kGroup];
@@ -87,10 +88,10 @@ HSA_DEVINL void partial_rows_at(RowFn rows, int i0, int i1, BiasFn bias, GatePar
 }
 
 // The same over rows at kv[i * stride] / z[i * stride].
-template <bool kMasked = false, typename BiasFn>
+template <bool kMasked = false, int kGroup = 4, typename BiasFn>
 HSA_DEVINL void partial_rows(const uint4* kv, const uint4* z, int64_t stride, int i0, int i1,
                              BiasFn bias, GatePartial& p) {
-  partial_rows_at<kMasked>(
+  partial_rows_at<kMasked, kGroup>(
       [&](int i, const uint4** kp, const uint4** zp) {
         *kp = kv + i * stride;
         *zp = z + i * stride;
