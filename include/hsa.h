@@ -316,7 +316,12 @@ hsa_status_t hsa_decode_attn(const void* q, const void* swa, const int32_t* seq_
  * [pool_offsets[b], pool_offsets[b+1]) of kv_pool (and key_pool), of which
  * the first L_b / r are live; a step that would write past the capacity sets
  * HSA_DEV_BOUNDS and skips that write.  Rings hold r rows per sequence, in
- * block order.  Five kernel launches for C4, two for C128.
+ * block order.  Kernel launches (hsa_layer_decode_launches gives the count):
+ * C4 three (the top-k inside the attention kernel) or four (the top-k on
+ * its own, when the rows exceed the fused selection's limit); C128 two, or
+ * three when the attention's key splits are merged by their own kernel.
+ * Consecutive launches overlap under programmatic dependent launch, with the
+ * results of the stream order above.
  * Shapes as for the individual stages; C4 needs Hi, Di, k, iq, w, key_pool,
  * the ik / iz rings and b_ik; C128 needs max_pool_rows >= every N_b.
  * ---------------------------------------------------------------------- */
