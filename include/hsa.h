@@ -317,9 +317,9 @@ hsa_status_t hsa_decode_attn(const void* q, const void* swa, const int32_t* seq_
  * the first L_b / r are live; a step that would write past the capacity sets
  * HSA_DEV_BOUNDS and skips that write.  Rings hold r rows per sequence, in
  * block order.  Kernel launches (hsa_layer_decode_launches gives the count):
- * C4 three (the top-k inside the attention kernel) or four (the top-k on
- * its own, when the rows exceed the fused selection's limit); C128 two, or
- * three when the attention's key splits are merged by their own kernel.
+ * C4 three (the top-k inside the attention kernel), or four with the top-k
+ * on its own (rows above the fused selection's limit); C128 two; one more
+ * when the attention's key splits are merged by their own kernel.
  * Consecutive launches overlap under programmatic dependent launch, with the
  * results of the stream order above.
  * Shapes as for the individual stages; C4 needs Hi, Di, k, iq, w, key_pool,
